@@ -1,0 +1,543 @@
+/*
+ * vsa_oracle.c -- plain, slow CPU oracle for VSA (Video Sparse Attention).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: only the tests, the smoke check and the CPU-baseline leg
+ * of the benchmark do.  It shares no code, header, table or constant with the
+ * CUDA library; the two are compared against each other, and this file is
+ * pinned on its own by the tests (brute force, closed forms, dense-attention
+ * special cases, autograd and finite differences).
+ *
+ * Every quantity is float64 and every step is written as plain loops in the
+ * order the method states it.  Tensors are contiguous [BH, N, d] (BH = batch
+ * x heads, N tokens, d head dim); pooled tensors are [BH, Nc, d] with
+ * Nc = N / 64.  OpenMP only splits independent rows across threads; it never
+ * changes the order of any sum.
+ *
+ * Sources (cited by page and section):
+ *  [AMD] "VSA: Accelerating Video Diffusion Inference with Sparse Attention on
+ *        AMD GPUs" (ROCm blog).
+ *  [ABS] "VSA: Faster Video Diffusion with Trainable Sparse Attention",
+ *        Abstract.
+ *
+ * Readings where the pages are silent:
+ *  - The 3D space-filling curve is cube-raster order: cubes of (4,4,4) tokens
+ *    in (t/4, h/4, w/4) raster order, tokens inside a cube in
+ *    (t%4, h%4, w%4) raster order.
+ *  - Coarse scores carry the SDPA scale (the pseudocode einsum in [AMD]
+ *    "Generating Sparsity Patterns" shows none; Top-K is unaffected).
+ *  - The coarse output is softmax(Sc) Vc over all cubes, broadcast to the
+ *    64 tokens of each query cube.
+ *  - The gated combination is out = g_c * O_c + g_f * O_f elementwise; a
+ *    missing gate means all ones.
+ *  - Top-K ties go to the lower cube id; the index list is stored in
+ *    selection order (descending score), as torch.topk returns it.
+ *  - A query cube with zero valid blocks has O_f = 0 and LSE = -inf.
+ *  - The Top-K set is a constant in the backward pass.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define CUBE 64 /* (Ct, Ch, Cw) = (4, 4, 4) tokens per cube */
+
+/* ------------------------------------------------------------------------ */
+/* Pre-stage: 3D space-filling-curve token reordering.
+ * [AMD] "Two-Stage Architecture", "Pre-stage: 3D Space-Filling Curve (SFC)
+ * Token Reordering": tokens are remapped so that each fixed-size block of the
+ * 1D sequence is a contiguous spatio-temporal region. */
+
+/* Position in the reordered sequence of native token (t, h, w). */
+int64_t orc_sfc_position(int t, int h, int w, int T, int H, int W)
+{
+    (void)T;
+    int64_t cube_t = t / 4, cube_h = h / 4, cube_w = w / 4;
+    int64_t cubes_h = H / 4, cubes_w = W / 4;
+    int64_t cube = (cube_t * cubes_h + cube_h) * cubes_w + cube_w;
+    int64_t off = ((int64_t)(t % 4) * 4 + (h % 4)) * 4 + (w % 4);
+    return cube * CUBE + off;
+}
+
+/* pos[n] = reordered position of the native token n = (t*H + h)*W + w. */
+void orc_sfc_table(int T, int H, int W, int64_t *pos)
+{
+    for (int t = 0; t < T; t++)
+        for (int h = 0; h < H; h++)
+            for (int w = 0; w < W; w++) {
+                int64_t n = ((int64_t)t * H + h) * W + w;
+                pos[n] = orc_sfc_position(t, h, w, T, H, W);
+            }
+}
+
+/* inverse == 0: y[pos[n]] = x[n] (native -> cube order);
+ * inverse != 0: y[n] = x[pos[n]] (cube order -> native). */
+void orc_permute(const double *x, double *y, int64_t BH, int d,
+                 int T, int H, int W, int inverse)
+{
+    int64_t N = (int64_t)T * H * W;
+    int64_t *pos = (int64_t *)malloc(sizeof(int64_t) * N);
+    orc_sfc_table(T, H, W, pos);
+#pragma omp parallel for
+    for (int64_t bh = 0; bh < BH; bh++)
+        for (int64_t n = 0; n < N; n++) {
+            const double *src = x + (bh * N + (inverse ? pos[n] : n)) * d;
+            double *dst = y + (bh * N + (inverse ? n : pos[n])) * d;
+            for (int c = 0; c < d; c++)
+                dst[c] = src[c];
+        }
+    free(pos);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Stage 1: cube mean-pool.  [AMD] "Stage 1: Coarse Selection": each cube of
+ * 64 tokens is mean-pooled into one cube-level vector (Qc, Kc, Vc).
+ * Input is in reordered (cube-contiguous) order. */
+void orc_pool(const double *xp, double *xc, int64_t BH, int64_t N, int d)
+{
+    int64_t Nc = N / CUBE;
+#pragma omp parallel for
+    for (int64_t bh = 0; bh < BH; bh++)
+        for (int64_t c = 0; c < Nc; c++)
+            for (int k = 0; k < d; k++) {
+                double s = 0.0;
+                for (int o = 0; o < CUBE; o++)
+                    s += xp[(bh * N + c * CUBE + o) * d + k];
+                xc[(bh * Nc + c) * d + k] = s / CUBE;
+            }
+}
+
+/* Stage 1: coarse cube-to-cube attention.
+ * [AMD] "Stage 1: Coarse Selection" (cube-to-cube scores) and
+ * "Stage 2: Fine Computation" (the coarse-stage output keeps global context);
+ * the scale is the SDPA one of [AMD] "The Attention Bottleneck in Video
+ * Diffusion".  scores [BH, Nc, Nc] (may be NULL), oc [BH, Nc, d] (may be
+ * NULL), lse_c [BH, Nc] (may be NULL). */
+void orc_coarse(const double *qc, const double *kc, const double *vc,
+                int64_t BH, int Nc, int d, double scale,
+                double *scores, double *oc, double *lse_c)
+{
+#pragma omp parallel for
+    for (int64_t r = 0; r < BH * Nc; r++) {
+        int64_t bh = r / Nc;
+        double *s = (double *)malloc(sizeof(double) * Nc);
+        const double *q = qc + r * d;
+        for (int b = 0; b < Nc; b++) {
+            const double *k = kc + (bh * Nc + b) * d;
+            double dot = 0.0;
+            for (int c = 0; c < d; c++)
+                dot += q[c] * k[c];
+            s[b] = scale * dot;
+        }
+        if (scores)
+            for (int b = 0; b < Nc; b++)
+                scores[r * Nc + b] = s[b];
+        double m = -INFINITY;
+        for (int b = 0; b < Nc; b++)
+            if (s[b] > m)
+                m = s[b];
+        double l = 0.0;
+        for (int b = 0; b < Nc; b++)
+            l += exp(s[b] - m);
+        if (lse_c)
+            lse_c[r] = m + log(l);
+        if (oc)
+            for (int c = 0; c < d; c++) {
+                double acc = 0.0;
+                for (int b = 0; b < Nc; b++)
+                    acc += exp(s[b] - m) / l * vc[(bh * Nc + b) * d + c];
+                oc[r * d + c] = acc;
+            }
+        free(s);
+    }
+}
+
+/* Stage 1: per-query-cube Top-K.  [AMD] "Stage 1: Coarse Selection" and the
+ * torch.topk call in "Generating Sparsity Patterns": the K key cubes with the
+ * highest scores, highest first; ties go to the lower cube id.
+ * scores [rows, Nc] (rows = BH * number of query cubes); idx [rows, K]. */
+typedef struct {
+    double score;
+    int32_t id;
+} orc_scored_t;
+
+static int orc_cmp_desc(const void *pa, const void *pb)
+{
+    const orc_scored_t *a = (const orc_scored_t *)pa;
+    const orc_scored_t *b = (const orc_scored_t *)pb;
+    if (a->score > b->score) return -1;
+    if (a->score < b->score) return 1;
+    return (a->id > b->id) - (a->id < b->id);
+}
+
+void orc_topk(const double *scores, int64_t rows, int Nc, int K, int32_t *idx)
+{
+#pragma omp parallel for
+    for (int64_t r = 0; r < rows; r++) {
+        orc_scored_t *row = (orc_scored_t *)malloc(sizeof(orc_scored_t) * Nc);
+        for (int b = 0; b < Nc; b++) {
+            row[b].score = scores[r * Nc + b];
+            row[b].id = b;
+        }
+        qsort(row, Nc, sizeof(orc_scored_t), orc_cmp_desc);
+        for (int k = 0; k < K; k++)
+            idx[r * K + k] = row[k].id;
+        free(row);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Stage 2: fine token-level attention over the selected cubes only.
+ * [AMD] "Stage 2: Fine Computation" and "Sparse Traversal": for query block
+ * q, visit kv_block_idx[q][i] for i < valid_block_num[q]; unselected cubes are
+ * skipped.  The softmax is the SDPA one over the union of the selected cubes'
+ * tokens.  One row: query token i (reordered order) of head bh. */
+static void orc_fine_row(const double *qp, const double *kp, const double *vp,
+                         const int32_t *idx, const int32_t *cnt, int Kmax,
+                         int64_t N, int d, double scale, int64_t bh, int64_t i,
+                         double *of_row, double *lse_row)
+{
+    int64_t Nc = N / CUBE;
+    int64_t qcube = i / CUBE;
+    int n = cnt[bh * Nc + qcube];
+    const int32_t *list = idx + (bh * Nc + qcube) * Kmax;
+    const double *q = qp + (bh * N + i) * d;
+    int64_t nk = (int64_t)n * CUBE;
+    if (nk == 0) {
+        for (int c = 0; c < d; c++)
+            of_row[c] = 0.0;
+        *lse_row = -INFINITY;
+        return;
+    }
+    double *s = (double *)malloc(sizeof(double) * nk);
+    for (int e = 0; e < n; e++)
+        for (int o = 0; o < CUBE; o++) {
+            int64_t j = (int64_t)list[e] * CUBE + o;
+            const double *k = kp + (bh * N + j) * d;
+            double dot = 0.0;
+            for (int c = 0; c < d; c++)
+                dot += q[c] * k[c];
+            s[e * CUBE + o] = scale * dot;
+        }
+    double m = -INFINITY;
+    for (int64_t a = 0; a < nk; a++)
+        if (s[a] > m)
+            m = s[a];
+    double l = 0.0;
+    for (int64_t a = 0; a < nk; a++)
+        l += exp(s[a] - m);
+    *lse_row = m + log(l);
+    for (int c = 0; c < d; c++) {
+        double acc = 0.0;
+        for (int e = 0; e < n; e++)
+            for (int o = 0; o < CUBE; o++) {
+                int64_t j = (int64_t)list[e] * CUBE + o;
+                acc += exp(s[e * CUBE + o] - m) / l * vp[(bh * N + j) * d + c];
+            }
+        of_row[c] = acc;
+    }
+    free(s);
+}
+
+void orc_fine_fwd(const double *qp, const double *kp, const double *vp,
+                  const int32_t *idx, const int32_t *cnt, int Kmax,
+                  int64_t BH, int64_t N, int d, double scale,
+                  double *of, double *lse)
+{
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t r = 0; r < BH * N; r++)
+        orc_fine_row(qp, kp, vp, idx, cnt, Kmax, N, d, scale, r / N, r % N,
+                     of + r * d, lse + r);
+}
+
+/* Same as orc_fine_fwd on a list of rows (r = bh*N + i), for sampled checks
+ * at full size.  of_rows [nrows, d], lse_rows [nrows]. */
+void orc_fine_fwd_rows(const double *qp, const double *kp, const double *vp,
+                       const int32_t *idx, const int32_t *cnt, int Kmax,
+                       int64_t BH, int64_t N, int d, double scale,
+                       const int64_t *rows, int64_t nrows,
+                       double *of_rows, double *lse_rows)
+{
+    (void)BH;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t a = 0; a < nrows; a++)
+        orc_fine_row(qp, kp, vp, idx, cnt, Kmax, N, d, scale, rows[a] / N,
+                     rows[a] % N, of_rows + a * d, lse_rows + a);
+}
+
+/* Gated combination, in reordered order.  [AMD] "Stage 2: Fine Computation"
+ * (the output combines the coarse and fine outputs through learnable gates)
+ * and "Algorithmic Design".  gc / gf may be NULL (all ones). */
+void orc_combine(const double *gc, const double *gf, const double *oc,
+                 const double *of, int64_t BH, int64_t N, int d, double *outp)
+{
+    int64_t Nc = N / CUBE;
+#pragma omp parallel for
+    for (int64_t bh = 0; bh < BH; bh++)
+        for (int64_t i = 0; i < N; i++)
+            for (int c = 0; c < d; c++) {
+                int64_t e = (bh * N + i) * d + c;
+                double a = gc ? gc[e] : 1.0;
+                double b = gf ? gf[e] : 1.0;
+                outp[e] = a * oc[(bh * Nc + i / CUBE) * d + c] + b * of[e];
+            }
+}
+
+/* The whole forward pass, native order in and out.
+ * q, k, v, gc, gf: [BH, N, d] native (t, h, w) order; gc, gf may be NULL.
+ * lut_in: if not NULL, [BH, Nc, K] index list used instead of the Top-K
+ * (the valid count is then K for every query cube).
+ * Outputs (all caller-allocated):
+ *   out [BH, N, d] native; idx [BH, Nc, K]; of [BH, N, d] and lse [BH, N]
+ *   (reordered order); oc [BH, Nc, d]; scores [BH, Nc, Nc] (may be NULL). */
+void orc_forward(const double *q, const double *k, const double *v,
+                 const double *gc, const double *gf, int64_t BH, int d,
+                 int T, int H, int W, int K, double scale,
+                 const int32_t *lut_in, double *out, int32_t *idx,
+                 double *of, double *lse, double *oc, double *scores)
+{
+    int64_t N = (int64_t)T * H * W, Nc = N / CUBE;
+    size_t big = sizeof(double) * BH * N * d, small = sizeof(double) * BH * Nc * d;
+    double *qp = (double *)malloc(big), *kp = (double *)malloc(big), *vp = (double *)malloc(big);
+    double *qc = (double *)malloc(small), *kc = (double *)malloc(small), *vc = (double *)malloc(small);
+    double *sc = scores ? scores : (double *)malloc(sizeof(double) * BH * Nc * Nc);
+    int32_t *cnt = (int32_t *)malloc(sizeof(int32_t) * BH * Nc);
+    orc_permute(q, qp, BH, d, T, H, W, 0);
+    orc_permute(k, kp, BH, d, T, H, W, 0);
+    orc_permute(v, vp, BH, d, T, H, W, 0);
+    orc_pool(qp, qc, BH, N, d);
+    orc_pool(kp, kc, BH, N, d);
+    orc_pool(vp, vc, BH, N, d);
+    orc_coarse(qc, kc, vc, BH, (int)Nc, d, scale, sc, oc, NULL);
+    if (lut_in)
+        memcpy(idx, lut_in, sizeof(int32_t) * BH * Nc * K);
+    else
+        orc_topk(sc, BH * Nc, (int)Nc, K, idx);
+    for (int64_t r = 0; r < BH * Nc; r++)
+        cnt[r] = K;
+    orc_fine_fwd(qp, kp, vp, idx, cnt, K, BH, N, d, scale, of, lse);
+    double *gcp = NULL, *gfp = NULL, *outp = (double *)malloc(big);
+    if (gc) {
+        gcp = (double *)malloc(big);
+        orc_permute(gc, gcp, BH, d, T, H, W, 0);
+    }
+    if (gf) {
+        gfp = (double *)malloc(big);
+        orc_permute(gf, gfp, BH, d, T, H, W, 0);
+    }
+    orc_combine(gcp, gfp, oc, of, BH, N, d, outp);
+    orc_permute(outp, out, BH, d, T, H, W, 1);
+    free(qp); free(kp); free(vp); free(qc); free(kc); free(vc);
+    if (!scores) free(sc);
+    free(cnt); free(gcp); free(gfp); free(outp);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward.  [ABS]: VSA trains end to end as one differentiable operator.
+ * The derivative of each step is the textbook one (softmax Jacobian
+ * dS = P * (dP - sum_k P dP)); the Top-K selection is held constant. */
+
+/* Fine stage backward, reordered order.  dof = dL/dO_f.  dq, dk, dv are
+ * overwritten. */
+void orc_fine_bwd(const double *qp, const double *kp, const double *vp,
+                  const double *dof, const int32_t *idx, const int32_t *cnt,
+                  int Kmax, int64_t BH, int64_t N, int d, double scale,
+                  double *dq, double *dk, double *dv)
+{
+    int64_t Nc = N / CUBE;
+    memset(dq, 0, sizeof(double) * BH * N * d);
+    memset(dk, 0, sizeof(double) * BH * N * d);
+    memset(dv, 0, sizeof(double) * BH * N * d);
+    /* Heads are independent; inside a head the rows are visited in order. */
+#pragma omp parallel for
+    for (int64_t bh = 0; bh < BH; bh++) {
+        int64_t maxk = (int64_t)Kmax * CUBE;
+        double *s = (double *)malloc(sizeof(double) * (maxk + 1));
+        double *p = (double *)malloc(sizeof(double) * (maxk + 1));
+        double *dp = (double *)malloc(sizeof(double) * (maxk + 1));
+        int64_t *key = (int64_t *)malloc(sizeof(int64_t) * (maxk + 1));
+        for (int64_t i = 0; i < N; i++) {
+            int64_t qcube = i / CUBE;
+            int n = cnt[bh * Nc + qcube];
+            const int32_t *list = idx + (bh * Nc + qcube) * Kmax;
+            int64_t nk = (int64_t)n * CUBE;
+            if (nk == 0)
+                continue;
+            const double *q = qp + (bh * N + i) * d;
+            const double *g = dof + (bh * N + i) * d;
+            for (int e = 0; e < n; e++)
+                for (int o = 0; o < CUBE; o++)
+                    key[e * CUBE + o] = (int64_t)list[e] * CUBE + o;
+            double m = -INFINITY;
+            for (int64_t a = 0; a < nk; a++) {
+                const double *kk = kp + (bh * N + key[a]) * d;
+                double dot = 0.0;
+                for (int c = 0; c < d; c++)
+                    dot += q[c] * kk[c];
+                s[a] = scale * dot;
+                if (s[a] > m)
+                    m = s[a];
+            }
+            double l = 0.0;
+            for (int64_t a = 0; a < nk; a++)
+                l += exp(s[a] - m);
+            for (int64_t a = 0; a < nk; a++)
+                p[a] = exp(s[a] - m) / l;
+            /* dP_ij = dO_i . V_j ; D_i = sum_j P_ij dP_ij */
+            double D = 0.0;
+            for (int64_t a = 0; a < nk; a++) {
+                const double *vv = vp + (bh * N + key[a]) * d;
+                double dot = 0.0;
+                for (int c = 0; c < d; c++)
+                    dot += g[c] * vv[c];
+                dp[a] = dot;
+                D += p[a] * dot;
+            }
+            double *dqi = dq + (bh * N + i) * d;
+            for (int64_t a = 0; a < nk; a++) {
+                double ds = p[a] * (dp[a] - D);
+                const double *kk = kp + (bh * N + key[a]) * d;
+                double *dkj = dk + (bh * N + key[a]) * d;
+                double *dvj = dv + (bh * N + key[a]) * d;
+                for (int c = 0; c < d; c++) {
+                    dvj[c] += p[a] * g[c];
+                    dqi[c] += scale * ds * kk[c];
+                    dkj[c] += scale * ds * q[c];
+                }
+            }
+        }
+        free(s); free(p); free(dp); free(key);
+    }
+}
+
+/* Coarse stage backward: doc = dL/dO_c [BH, Nc, d]; outputs overwritten. */
+void orc_coarse_bwd(const double *qc, const double *kc, const double *vc,
+                    const double *doc, int64_t BH, int Nc, int d, double scale,
+                    double *dqc, double *dkc, double *dvc)
+{
+    memset(dqc, 0, sizeof(double) * BH * Nc * d);
+    memset(dkc, 0, sizeof(double) * BH * Nc * d);
+    memset(dvc, 0, sizeof(double) * BH * Nc * d);
+#pragma omp parallel for
+    for (int64_t bh = 0; bh < BH; bh++) {
+        double *s = (double *)malloc(sizeof(double) * Nc);
+        double *p = (double *)malloc(sizeof(double) * Nc);
+        double *dp = (double *)malloc(sizeof(double) * Nc);
+        for (int a = 0; a < Nc; a++) {
+            const double *q = qc + (bh * Nc + a) * d;
+            const double *g = doc + (bh * Nc + a) * d;
+            double m = -INFINITY;
+            for (int b = 0; b < Nc; b++) {
+                const double *k = kc + (bh * Nc + b) * d;
+                double dot = 0.0;
+                for (int c = 0; c < d; c++)
+                    dot += q[c] * k[c];
+                s[b] = scale * dot;
+                if (s[b] > m)
+                    m = s[b];
+            }
+            double l = 0.0;
+            for (int b = 0; b < Nc; b++)
+                l += exp(s[b] - m);
+            double D = 0.0;
+            for (int b = 0; b < Nc; b++) {
+                p[b] = exp(s[b] - m) / l;
+                const double *v = vc + (bh * Nc + b) * d;
+                double dot = 0.0;
+                for (int c = 0; c < d; c++)
+                    dot += g[c] * v[c];
+                dp[b] = dot;
+                D += p[b] * dot;
+            }
+            for (int b = 0; b < Nc; b++) {
+                double ds = p[b] * (dp[b] - D);
+                const double *k = kc + (bh * Nc + b) * d;
+                for (int c = 0; c < d; c++) {
+                    dvc[(bh * Nc + b) * d + c] += p[b] * g[c];
+                    dqc[(bh * Nc + a) * d + c] += scale * ds * k[c];
+                    dkc[(bh * Nc + b) * d + c] += scale * ds * q[c];
+                }
+            }
+        }
+        free(s); free(p); free(dp);
+    }
+}
+
+/* The whole backward pass, native order in and out.
+ * Inputs as orc_forward, plus idx (the index list the forward used, [BH,Nc,K])
+ * and dout [BH, N, d] native.  Outputs (caller-allocated, native order):
+ * dq, dk, dv [BH, N, d]; dgc, dgf [BH, N, d] (ignored when the gate is NULL). */
+void orc_backward(const double *q, const double *k, const double *v,
+                  const double *gc, const double *gf, int64_t BH, int d,
+                  int T, int H, int W, int K, double scale, const int32_t *idx,
+                  const double *dout, double *dq, double *dk, double *dv,
+                  double *dgc, double *dgf)
+{
+    int64_t N = (int64_t)T * H * W, Nc = N / CUBE;
+    size_t big = sizeof(double) * BH * N * d, small = sizeof(double) * BH * Nc * d;
+    double *qp = (double *)malloc(big), *kp = (double *)malloc(big), *vp = (double *)malloc(big);
+    double *qc = (double *)malloc(small), *kc = (double *)malloc(small), *vc = (double *)malloc(small);
+    double *oc = (double *)malloc(small), *of = (double *)malloc(big);
+    double *lse = (double *)malloc(sizeof(double) * BH * N);
+    double *dop = (double *)malloc(big), *gcp = (double *)malloc(big), *gfp = (double *)malloc(big);
+    double *dgcp = (double *)malloc(big), *dgfp = (double *)malloc(big);
+    double *dof = (double *)malloc(big), *doc = (double *)malloc(small);
+    double *dqp = (double *)malloc(big), *dkp = (double *)malloc(big), *dvp = (double *)malloc(big);
+    double *dqc = (double *)malloc(small), *dkc = (double *)malloc(small), *dvc = (double *)malloc(small);
+    int32_t *cnt = (int32_t *)malloc(sizeof(int32_t) * BH * Nc);
+    for (int64_t r = 0; r < BH * Nc; r++)
+        cnt[r] = K;
+
+    /* Recompute the forward intermediates. */
+    orc_permute(q, qp, BH, d, T, H, W, 0);
+    orc_permute(k, kp, BH, d, T, H, W, 0);
+    orc_permute(v, vp, BH, d, T, H, W, 0);
+    orc_pool(qp, qc, BH, N, d);
+    orc_pool(kp, kc, BH, N, d);
+    orc_pool(vp, vc, BH, N, d);
+    orc_coarse(qc, kc, vc, BH, (int)Nc, d, scale, NULL, oc, NULL);
+    orc_fine_fwd(qp, kp, vp, idx, cnt, K, BH, N, d, scale, of, lse);
+
+    /* Gated combination out_p = gc*Oc[cube] + gf*Of, differentiated. */
+    orc_permute(dout, dop, BH, d, T, H, W, 0);
+    if (gc)
+        orc_permute(gc, gcp, BH, d, T, H, W, 0);
+    if (gf)
+        orc_permute(gf, gfp, BH, d, T, H, W, 0);
+    memset(doc, 0, small);
+    for (int64_t bh = 0; bh < BH; bh++)
+        for (int64_t i = 0; i < N; i++)
+            for (int c = 0; c < d; c++) {
+                int64_t e = (bh * N + i) * d + c;
+                int64_t ec = (bh * Nc + i / CUBE) * d + c;
+                double a = gc ? gcp[e] : 1.0, b = gf ? gfp[e] : 1.0;
+                dof[e] = b * dop[e];
+                doc[ec] += a * dop[e];
+                dgcp[e] = dop[e] * oc[ec];
+                dgfp[e] = dop[e] * of[e];
+            }
+    if (gc && dgc)
+        orc_permute(dgcp, dgc, BH, d, T, H, W, 1);
+    if (gf && dgf)
+        orc_permute(dgfp, dgf, BH, d, T, H, W, 1);
+
+    orc_fine_bwd(qp, kp, vp, dof, idx, cnt, K, BH, N, d, scale, dqp, dkp, dvp);
+    orc_coarse_bwd(qc, kc, vc, doc, BH, (int)Nc, d, scale, dqc, dkc, dvc);
+
+    /* Mean-pool backward: every token of a cube gets dXc / 64. */
+    for (int64_t bh = 0; bh < BH; bh++)
+        for (int64_t i = 0; i < N; i++)
+            for (int c = 0; c < d; c++) {
+                int64_t e = (bh * N + i) * d + c, ec = (bh * Nc + i / CUBE) * d + c;
+                dqp[e] += dqc[ec] / CUBE;
+                dkp[e] += dkc[ec] / CUBE;
+                dvp[e] += dvc[ec] / CUBE;
+            }
+    orc_permute(dqp, dq, BH, d, T, H, W, 1);
+    orc_permute(dkp, dk, BH, d, T, H, W, 1);
+    orc_permute(dvp, dv, BH, d, T, H, W, 1);
+
+    free(qp); free(kp); free(vp); free(qc); free(kc); free(vc); free(oc); free(of);
+    free(lse); free(dop); free(gcp); free(gfp); free(dgcp); free(dgfp); free(dof); free(doc);
+    free(dqp); free(dkp); free(dvp); free(dqc); free(dkc); free(dvc); free(cnt);
+}

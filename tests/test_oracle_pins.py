@@ -1,0 +1,327 @@
+"""Pins for the CPU oracle, each against something other than the oracle itself:
+brute force, closed forms, textbook special cases (dense SDPA), an independent
+dense masked formulation with torch autograd, and finite differences.
+
+Runs on the CPU only.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from dense_ref import cube_ids, dense_vsa
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+GRIDS = [(4, 8, 8), (8, 16, 32), (8, 12, 20), (4, 4, 4), (12, 4, 8)]
+
+
+# ---------------------------------------------------------------------------
+# 3D SFC reordering ("Pre-stage: 3D Space-Filling Curve (SFC) Token Reordering")
+
+@pytest.mark.parametrize("grid", GRIDS)
+def test_sfc_is_bijection_onto_contiguous_cubes(oracle_mod, grid):
+    T, H, W = grid
+    pos = oracle_mod.sfc_table(T, H, W)
+    N = T * H * W
+    assert sorted(pos.tolist()) == list(range(N))        # bijection
+    # Every block of 64 consecutive reordered tokens is one 4x4x4 box.
+    inv = np.empty(N, dtype=np.int64)
+    inv[pos] = np.arange(N)
+    t, h, w = inv // (H * W), (inv // W) % H, inv % W
+    for c in range(N // 64):
+        sl = slice(64 * c, 64 * c + 64)
+        for axis in (t, h, w):
+            vals = axis[sl]
+            assert vals.max() - vals.min() == 3 and vals.min() % 4 == 0
+        assert len(set(zip(t[sl], h[sl], w[sl]))) == 64
+
+
+@pytest.mark.parametrize("grid", GRIDS)
+def test_sfc_matches_reshape_transpose(oracle_mod, grid):
+    """Cube-raster order equals the library reshape/transpose of the grid."""
+    T, H, W = grid
+    x = np.arange(T * H * W, dtype=np.float64).reshape(1, T * H * W, 1)
+    y = oracle_mod.permute(x, T, H, W)
+    ref = np.arange(T * H * W).reshape(T // 4, 4, H // 4, 4, W // 4, 4)
+    ref = ref.transpose(0, 2, 4, 1, 3, 5).reshape(-1)
+    np.testing.assert_array_equal(y.reshape(-1), ref)
+    back = oracle_mod.permute(y, T, H, W, inverse=True)
+    np.testing.assert_array_equal(back, x)
+
+
+def test_sfc_golden_positions(oracle_mod):
+    with open(os.path.join(GOLDEN, "sfc_positions.json")) as f:
+        g = json.load(f)
+    for case in g["cases"]:
+        T, H, W = case["grid"]
+        for (t, h, w), p in case["positions"]:
+            assert oracle_mod._load().orc_sfc_position(t, h, w, T, H, W) == p
+
+
+# ---------------------------------------------------------------------------
+# Cube mean-pool ("Stage 1: Coarse Selection")
+
+def test_pool_bruteforce_on_native_boxes(oracle_mod):
+    T, H, W, d = 8, 12, 20, 5
+    x = synth.make_random((2, T * H * W, d), seed=11)
+    xc = oracle_mod.pool(oracle_mod.permute(x, T, H, W))
+    xn = x.astype(np.float64).reshape(2, T, H, W, d)
+    c = 0
+    for ct in range(T // 4):
+        for ch in range(H // 4):
+            for cw in range(W // 4):
+                box = xn[:, 4 * ct:4 * ct + 4, 4 * ch:4 * ch + 4, 4 * cw:4 * cw + 4]
+                np.testing.assert_allclose(xc[:, c], box.reshape(2, 64, d).mean(1), rtol=0, atol=1e-13)
+                c += 1
+
+
+def test_pool_constant_cube(oracle_mod):
+    T, H, W, d = 4, 8, 8, 3
+    vals = np.array([1.5, -2.25, 7.0])
+    xp = np.tile(vals, (T * H * W, 1))[None]
+    assert np.array_equal(oracle_mod.pool(xp)[0], np.tile(vals, (4, 1)))
+    assert np.array_equal(oracle_mod.pool(np.zeros((1, T * H * W, d))), np.zeros((1, 4, d)))
+
+
+# ---------------------------------------------------------------------------
+# Coarse stage and Top-K ("Stage 1", "Generating Sparsity Patterns")
+
+def test_coarse_equals_sdpa_on_pooled(oracle_mod):
+    rng = np.random.default_rng(3)
+    qc, kc, vc = (rng.normal(size=(3, 20, 16)) for _ in range(3))
+    scale = 0.3
+    scores, oc, lse = oracle_mod.coarse(qc, kc, vc, scale)
+    t = [torch.tensor(a) for a in (qc, kc, vc)]
+    ref = torch.nn.functional.scaled_dot_product_attention(*t, scale=scale).numpy()
+    np.testing.assert_allclose(oc, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(scores, scale * qc @ kc.transpose(0, 2, 1), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(lse, torch.logsumexp(torch.tensor(scores), -1).numpy(), rtol=1e-13)
+
+
+def _bruteforce_topk(scores, K):
+    Nc = scores.shape[-1]
+    out = np.empty(scores.shape[:-1] + (K,), dtype=np.int64)
+    for r in np.ndindex(scores.shape[:-1]):
+        order = np.lexsort((np.arange(Nc), -scores[r]))   # score desc, id asc
+        out[r] = order[:K]
+    return out
+
+
+@pytest.mark.parametrize("K", [1, 3, 16, 64])
+def test_topk_bruteforce_random(oracle_mod, K):
+    rng = np.random.default_rng(K)
+    scores = rng.normal(size=(2, 64, 64))
+    np.testing.assert_array_equal(oracle_mod.topk(scores, K), _bruteforce_topk(scores, K))
+
+
+def test_topk_ties_go_to_lower_id(oracle_mod):
+    rng = np.random.default_rng(7)
+    scores = rng.integers(0, 4, size=(3, 40, 40)).astype(np.float64)   # many ties
+    for K in (1, 5, 13, 40):
+        np.testing.assert_array_equal(oracle_mod.topk(scores, K), _bruteforce_topk(scores, K))
+    flat = np.zeros((1, 1, 10))
+    np.testing.assert_array_equal(oracle_mod.topk(flat, 4)[0, 0], [0, 1, 2, 3])
+
+
+def test_topk_golden(oracle_mod):
+    with open(os.path.join(GOLDEN, "topk_cases.json")) as f:
+        g = json.load(f)
+    for case in g["cases"]:
+        s = np.array(case["scores"], dtype=np.float64)[None, None]
+        got = oracle_mod.topk(s, case["K"])[0, 0].tolist()
+        assert got == case["expected"], case["note"]
+
+
+# ---------------------------------------------------------------------------
+# Fine stage ("Stage 2: Fine Computation", "Sparse Traversal")
+
+def test_fine_all_cubes_is_dense_sdpa(oracle_mod):
+    """K = all cubes: nothing is skipped, so the fine stage is plain SDPA."""
+    BH, N, d = 2, 256, 64
+    q, k, v = (synth.make_random((BH, N, d), seed=s) for s in (1, 2, 3))
+    Nc = N // 64
+    idx = np.tile(np.arange(Nc, dtype=np.int32), (BH, Nc, 1))[:, :, ::-1].copy()
+    cnt = np.full((BH, Nc), Nc, dtype=np.int32)
+    of, lse = oracle_mod.fine_fwd(q, k, v, idx, cnt, d ** -0.5)
+    tq, tk, tv = (torch.tensor(a, dtype=torch.float64) for a in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv).numpy()
+    np.testing.assert_allclose(of, ref, rtol=1e-11, atol=1e-11)
+    ref_lse = torch.logsumexp(tq @ tk.transpose(-1, -2) * d ** -0.5, -1).numpy()
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-12)
+
+
+def test_fine_single_cube_is_local_sdpa(oracle_mod):
+    BH, N, d = 1, 512, 32
+    q, k, v = (synth.make_random((BH, N, d), seed=s) for s in (4, 5, 6))
+    Nc = N // 64
+    own = np.arange(Nc, dtype=np.int32).reshape(1, Nc, 1)
+    of, _ = oracle_mod.fine_fwd(q, k, v, own, np.ones((1, Nc), np.int32), 0.2)
+    t = [torch.tensor(a, dtype=torch.float64).reshape(Nc, 64, d) for a in (q, k, v)]
+    ref = torch.nn.functional.scaled_dot_product_attention(*t, scale=0.2).reshape(1, N, d).numpy()
+    np.testing.assert_allclose(of, ref, rtol=1e-11, atol=1e-11)
+
+
+def test_fine_zero_query_closed_form(oracle_mod):
+    """Q = 0: every selected key has weight 1/(64 K); LSE = log(64 K)."""
+    BH, N, d, K = 1, 512, 16, 3
+    rng = np.random.default_rng(9)
+    k, v = rng.normal(size=(2, BH, N, d))
+    q = np.zeros((BH, N, d))
+    idx = np.stack([rng.permutation(8)[:K] for _ in range(8)])[None].astype(np.int32)
+    of, lse = oracle_mod.fine_fwd(q, k, v, idx, np.full((1, 8), K, np.int32), 0.5)
+    for a in range(8):
+        keys = np.concatenate([np.arange(64 * c, 64 * c + 64) for c in idx[0, a]])
+        np.testing.assert_allclose(of[0, 64 * a:64 * a + 64], np.tile(v[0, keys].mean(0), (64, 1)), atol=1e-13)
+    np.testing.assert_allclose(lse, np.log(64 * K), rtol=1e-14)
+
+
+def test_fine_empty_and_ragged_counts(oracle_mod):
+    BH, N, d = 1, 256, 8
+    q, k, v = (synth.make_random((BH, N, d), seed=s) for s in (7, 8, 9))
+    idx = np.array([[[2, 0, 1], [1, 3, 0], [0, 0, 0], [3, 2, 1]]], dtype=np.int32)
+    cnt = np.array([[3, 1, 0, 2]], dtype=np.int32)
+    of, lse = oracle_mod.fine_fwd(q, k, v, idx, cnt, 0.35)
+    assert np.all(of[0, 128:192] == 0) and np.all(np.isneginf(lse[0, 128:192]))
+    for a, n in enumerate(cnt[0]):
+        if n == 0:
+            continue
+        keys = np.concatenate([np.arange(64 * c, 64 * c + 64) for c in idx[0, a, :n]])
+        s = q[0, 64 * a:64 * a + 64].astype(np.float64) @ k[0, keys].T.astype(np.float64) * 0.35
+        p = np.exp(s - s.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        np.testing.assert_allclose(of[0, 64 * a:64 * a + 64], p @ v[0, keys], atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Whole forward and backward against the independent dense formulation
+
+def _tiny_inputs(wl, gates):
+    q, k, v = synth.make_qkv(wl)
+    sh = (wl.BH, wl.N, wl.d)
+    q, k, v = (a.reshape(sh) for a in (q, k, v))
+    gc = gf = None
+    if gates:
+        gc, gf = (a.reshape(sh) for a in synth.make_gates(wl))
+    dout = synth.make_dout(wl).reshape(sh)
+    return q, k, v, gc, gf, dout
+
+
+def _t(a):
+    return None if a is None else torch.tensor(a, dtype=torch.float64)
+
+
+@pytest.mark.parametrize("name,gates", [("tiny", True), ("tiny", False), ("tiny_dense", True)])
+def test_forward_matches_dense_masked(oracle_mod, name, gates):
+    wl = synth.WORKLOADS[name]
+    q, k, v, gc, gf, _ = _tiny_inputs(wl, gates)
+    scale = wl.d ** -0.5
+    r = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, scale, gc=gc, gf=gf)
+    out, of, ocb, sc, lse = dense_vsa(_t(q), _t(k), _t(v), wl.T, wl.H, wl.W, r["idx"], scale,
+                                      gc=_t(gc), gf=_t(gf))
+    np.testing.assert_allclose(r["scores"], sc.numpy(), rtol=1e-12, atol=1e-10)
+    # Selection: the dense formulation's own torch.topk gives the same sets.
+    tk_idx = torch.topk(sc, wl.topk, dim=-1).indices.numpy()
+    assert np.array_equal(np.sort(tk_idx, -1), np.sort(r["idx"], -1))
+    np.testing.assert_allclose(r["out"], out.numpy(), rtol=1e-10, atol=1e-10)
+    pos = oracle_mod.sfc_table(wl.T, wl.H, wl.W)
+    np.testing.assert_allclose(r["of"][:, pos], of.numpy(), rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(r["lse"][:, pos], lse.numpy(), rtol=1e-12)
+
+
+@pytest.mark.parametrize("gates", [True, False])
+def test_backward_matches_autograd(oracle_mod, gates):
+    wl = synth.WORKLOADS["tiny"]
+    q, k, v, gc, gf, dout = _tiny_inputs(wl, gates)
+    scale = wl.d ** -0.5
+    r = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, scale, gc=gc, gf=gf)
+    g = oracle_mod.backward(q, k, v, dout, r["idx"], wl.T, wl.H, wl.W, scale, gc=gc, gf=gf)
+    leaves = {n: torch.tensor(a, dtype=torch.float64, requires_grad=True)
+              for n, a in (("q", q), ("k", k), ("v", v), ("gc", gc), ("gf", gf)) if a is not None}
+    out, *_ = dense_vsa(leaves["q"], leaves["k"], leaves["v"], wl.T, wl.H, wl.W, r["idx"], scale,
+                        gc=leaves.get("gc"), gf=leaves.get("gf"))
+    (out * torch.tensor(dout, dtype=torch.float64)).sum().backward()
+    for n, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("gc", "dgc"), ("gf", "dgf")):
+        if n in leaves:
+            np.testing.assert_allclose(g[key], leaves[n].grad.numpy(), rtol=1e-9, atol=1e-9,
+                                       err_msg=key)
+
+
+def test_backward_finite_differences(oracle_mod):
+    """fp64 central differences of L = sum(out * dO) with the index list frozen."""
+    wl = synth.WORKLOADS["tiny"]
+    q, k, v, gc, gf, dout = (None if a is None else a.astype(np.float64)
+                             for a in _tiny_inputs(wl, True))
+    # Shrink Q and K so the softmax is not saturated and every term matters.
+    q, k = q * 0.1, k * 0.1
+    scale = wl.d ** -0.5
+    r = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, scale, gc=gc, gf=gf)
+    lut = r["idx"]
+    g = oracle_mod.backward(q, k, v, dout, lut, wl.T, wl.H, wl.W, scale, gc=gc, gf=gf)
+    inputs = dict(q=q, k=k, v=v, gc=gc, gf=gf)
+    grads = dict(q=g["dq"], k=g["dk"], v=g["dv"], gc=g["dgc"], gf=g["dgf"])
+    rng = np.random.default_rng(0)
+    h = 1e-5
+
+    def loss(ins):
+        o = oracle_mod.forward(ins["q"], ins["k"], ins["v"], wl.T, wl.H, wl.W, wl.topk, scale,
+                               gc=ins["gc"], gf=ins["gf"], lut=lut, want_scores=False)
+        return float((o["out"] * dout).sum())
+
+    for name in inputs:
+        for _ in range(12):
+            e = tuple(int(rng.integers(0, s)) for s in inputs[name].shape)
+            ins = {n: a.copy() for n, a in inputs.items()}
+            ins[name][e] += h
+            lp = loss(ins)
+            ins[name][e] -= 2 * h
+            lm = loss(ins)
+            fd = (lp - lm) / (2 * h)
+            an = grads[name][e]
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, e, fd, an)
+
+
+def test_gate_special_cases(oracle_mod):
+    """g_c = 0, g_f = 1 gives the fine output alone; g_c = 1, g_f = 0 the coarse one."""
+    wl = synth.WORKLOADS["tiny"]
+    q, k, v, *_ = _tiny_inputs(wl, False)
+    zeros, ones = np.zeros_like(q), np.ones_like(q)
+    pos = oracle_mod.sfc_table(wl.T, wl.H, wl.W)
+    r = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=zeros, gf=ones)
+    np.testing.assert_array_equal(r["out"], r["of"][:, pos])
+    r2 = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=ones, gf=zeros)
+    cid = cube_ids(wl.T, wl.H, wl.W)
+    np.testing.assert_array_equal(r2["out"], r2["oc"][:, cid])
+
+
+def test_dense_k_equals_sdpa_end_to_end(oracle_mod):
+    """K = Nc with g_c = 0: VSA is exactly dense attention in native order."""
+    wl = synth.WORKLOADS["tiny_dense"]
+    q, k, v, *_ = _tiny_inputs(wl, False)
+    r = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=np.zeros_like(q))
+    t = [torch.tensor(a, dtype=torch.float64) for a in (q, k, v)]
+    ref = torch.nn.functional.scaled_dot_product_attention(*t).numpy()
+    np.testing.assert_allclose(r["out"], ref, rtol=1e-10, atol=1e-10)
+
+
+def test_small_forward_one_head_matches_dense(oracle_mod):
+    """A mid-size case (4096 tokens, 64 cubes, K=16) spanning many cubes."""
+    wl = synth.WORKLOADS["small"]
+    q, k, v = (a.reshape(1, wl.N, wl.d) for a in synth.make_qkv(wl, heads_subset=[3]))
+    scale = wl.d ** -0.5
+    r = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, scale)
+    out, *_ = dense_vsa(_t(q), _t(k), _t(v), wl.T, wl.H, wl.W, r["idx"], scale)
+    np.testing.assert_allclose(r["out"], out.numpy(), rtol=1e-10, atol=1e-10)
+
+
+def test_head_subset_generator_matches_full(oracle_mod):
+    """Heads are independent: the oracle on a generated head subset equals the
+    same heads of a full run (the basis of sampled checks at full size)."""
+    wl = synth.WORKLOADS["small"]
+    full = synth.make_qkv(wl)
+    sub = synth.make_qkv(wl, heads_subset=[0, 7])
+    for f, s in zip(full, sub):
+        np.testing.assert_array_equal(f[:, [0, 7]], s)
