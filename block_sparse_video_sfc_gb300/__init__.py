@@ -1,0 +1,193 @@
+"""GB300 (sm_103a) implementation of VSA, the trainable coarse-to-fine
+block-sparse attention for video diffusion transformers.
+
+All compute runs in libvsa.so (hand-written CUDA: SFC reorder + cube pool,
+coarse attention + Top-K, tcgen05 fine attention forward and backward).  This
+module only allocates torch device tensors and passes pointers and the current
+stream through the C ABI of include/vsa.h.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import Grid, VSAError, VSA_DTYPE_BF16, VSA_DTYPE_F32
+
+__all__ = ["permute", "coarse_topk", "fine_fwd", "fine_bwd", "forward", "backward",
+           "workspace_bytes", "device_status", "VSAError", "ForwardState", "Grid"]
+
+_DT = {torch.bfloat16: VSA_DTYPE_BF16, torch.float32: VSA_DTYPE_F32}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libvsa takes CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libvsa takes contiguous tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _bhnd(x: torch.Tensor):
+    if x.dim() == 4:
+        return x.shape[0] * x.shape[1], x.shape[2], x.shape[3]
+    if x.dim() == 3:
+        return tuple(x.shape)
+    raise ValueError("expected [B, heads, N, d] or [BH, N, d]")
+
+
+def permute(x: torch.Tensor, T: int, H: int, W: int, inverse: bool = False, pool: bool = False):
+    """vsa_permute: native <-> cube order; with pool=True also the cube means."""
+    BH, N, d = _bhnd(x)
+    y = torch.empty_like(x)
+    pooled = None
+    if pool:
+        pooled = torch.empty(x.shape[:-2] + (N // 64, d), dtype=torch.float32, device=x.device)
+    _lib.check("vsa_permute", _lib.load().vsa_permute(_ptr(x), _ptr(y), _ptr(pooled), BH, d,
+                                                       Grid.of(T, H, W), int(inverse), _stream()))
+    return (y, pooled) if pool else y
+
+
+def coarse_topk(qc, kc, vc, topk: int, scale: Optional[float] = None, want_oc: bool = True,
+                want_scores: bool = False):
+    """vsa_coarse_topk -> dict(idx, cnt, oc, lse_c, scores)."""
+    BH, Nc, d = _bhnd(qc)
+    scale = d ** -0.5 if scale is None else scale
+    lead = qc.shape[:-2]
+    dev = qc.device
+    idx = torch.empty(lead + (Nc, topk), dtype=torch.int32, device=dev)
+    cnt = torch.empty(lead + (Nc,), dtype=torch.int32, device=dev)
+    oc = torch.empty_like(qc) if want_oc else None
+    lse_c = torch.empty(lead + (Nc,), dtype=torch.float32, device=dev) if want_oc else None
+    scores = torch.empty(lead + (Nc, Nc), dtype=torch.float32, device=dev) if want_scores else None
+    _lib.check("vsa_coarse_topk", _lib.load().vsa_coarse_topk(
+        _ptr(qc), _ptr(kc), _ptr(vc if want_oc else None), BH, Nc, d, topk, float(scale), _ptr(oc),
+        _ptr(lse_c), _ptr(idx), _ptr(cnt), _ptr(scores), _stream()))
+    return dict(idx=idx, cnt=cnt, oc=oc, lse_c=lse_c, scores=scores)
+
+
+def fine_fwd(qp, kp, vp, idx, cnt, scale: Optional[float] = None, out_dtype=torch.float32):
+    """vsa_fine_fwd on cube-ordered bf16 tensors -> (O_f, lse)."""
+    BH, N, d = _bhnd(qp)
+    scale = d ** -0.5 if scale is None else scale
+    of = torch.empty(qp.shape, dtype=out_dtype, device=qp.device)
+    lse = torch.empty(qp.shape[:-1], dtype=torch.float32, device=qp.device)
+    _lib.check("vsa_fine_fwd", _lib.load().vsa_fine_fwd(
+        _ptr(qp), _ptr(kp), _ptr(vp), _ptr(idx), _ptr(cnt), idx.shape[-1], BH, N, d, float(scale),
+        _ptr(of), _DT[out_dtype], _ptr(lse), _stream()))
+    return of, lse
+
+
+def workspace_bytes(op: int, B: int, heads: int, d: int, T: int, H: int, W: int, topk: int) -> int:
+    return int(_lib.load().vsa_workspace_bytes(op, B, heads, d, Grid.of(T, H, W), topk))
+
+
+def fine_bwd(qp, kp, vp, of, lse, dof, idx, cnt, scale: Optional[float] = None):
+    """vsa_fine_bwd -> (dq, dk, dv) fp32, cube order."""
+    BH, N, d = _bhnd(qp)
+    scale = d ** -0.5 if scale is None else scale
+    kmax = idx.shape[-1]
+    nbytes = workspace_bytes(_lib.VSA_OP_FINE_BWD, 1, BH, d, 4, 4, N // 16, kmax) if N % 64 == 0 else 0
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=qp.device)
+    dq = torch.empty(qp.shape, dtype=torch.float32, device=qp.device)
+    dk = torch.empty_like(dq)
+    dv = torch.empty_like(dq)
+    _lib.check("vsa_fine_bwd", _lib.load().vsa_fine_bwd(
+        _ptr(qp), _ptr(kp), _ptr(vp), _ptr(of), _DT[of.dtype], _ptr(lse), _ptr(dof), _ptr(idx), _ptr(cnt),
+        kmax, BH, N, d, float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), nbytes, _stream()))
+    return dq, dk, dv
+
+
+@dataclass
+class ForwardState:
+    """The saved state of one forward call (lives in `ws`)."""
+
+    ws: torch.Tensor
+    B: int
+    heads: int
+    d: int
+    T: int
+    H: int
+    W: int
+    topk: int
+    scale: float
+
+    def saved(self) -> dict:
+        """Views of the saved intermediates as torch tensors."""
+        s = _lib.Saved()
+        _lib.check("vsa_forward_saved", _lib.load().vsa_forward_saved(
+            _ptr(self.ws), self.B, self.heads, self.d, Grid.of(self.T, self.H, self.W), self.topk,
+            ctypes.byref(s)))
+        BH, N, d, K = self.B * self.heads, self.T * self.H * self.W, self.d, self.topk
+        Nc = N // 64
+        base = self.ws.data_ptr()
+
+        def view(ptr, shape, dtype):
+            esize = torch.empty((), dtype=dtype).element_size()
+            off = ptr - base
+            n = 1
+            for x in shape:
+                n *= x
+            return self.ws[off:off + n * esize].view(dtype).view(shape)
+
+        return dict(
+            qp=view(s.qp, (BH, N, d), torch.bfloat16), kp=view(s.kp, (BH, N, d), torch.bfloat16),
+            vp=view(s.vp, (BH, N, d), torch.bfloat16), qc=view(s.qc, (BH, Nc, d), torch.float32),
+            kc=view(s.kc, (BH, Nc, d), torch.float32), vc=view(s.vc, (BH, Nc, d), torch.float32),
+            oc=view(s.o_coarse, (BH, Nc, d), torch.float32),
+            lse_c=view(s.lse_coarse, (BH, Nc), torch.float32),
+            idx=view(s.kv_block_idx, (BH, Nc, K), torch.int32),
+            cnt=view(s.valid_block_num, (BH, Nc), torch.int32),
+            of=view(s.o_fine, (BH, N, d), torch.float32), lse=view(s.lse, (BH, N), torch.float32))
+
+
+def forward(q, k, v, T: int, H: int, W: int, topk: int, g_coarse=None, g_fine=None,
+            scale: Optional[float] = None, out_dtype=torch.bfloat16, out=None, ws=None):
+    """vsa_forward on native-order [B, heads, N, d] bf16 -> (out, ForwardState)."""
+    B, heads, N, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    nbytes = workspace_bytes(_lib.VSA_OP_FORWARD, B, heads, d, T, H, W, topk)
+    if nbytes == 0:
+        raise VSAError("vsa_workspace_bytes", _lib.VSA_ERR_ARG)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    _lib.check("vsa_forward", _lib.load().vsa_forward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g_coarse), _ptr(g_fine), B, heads, d, Grid.of(T, H, W), topk,
+        float(scale), _ptr(out), _DT[out.dtype], _ptr(ws), nbytes, _stream()))
+    return out, ForwardState(ws, B, heads, d, T, H, W, topk, scale)
+
+
+def backward(state: ForwardState, dout, g_coarse=None, g_fine=None, grad_dtype=torch.float32,
+             grads=None, ws=None):
+    """vsa_backward -> dict(dq, dk, dv, dgc, dgf) in native order."""
+    B, heads, d = state.B, state.heads, state.d
+    nbytes = workspace_bytes(_lib.VSA_OP_BACKWARD, B, heads, d, state.T, state.H, state.W, state.topk)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dout.device)
+    if grads is None:
+        mk = lambda: torch.empty(dout.shape, dtype=grad_dtype, device=dout.device)
+        grads = dict(dq=mk(), dk=mk(), dv=mk(), dgc=mk() if g_coarse is not None else None,
+                     dgf=mk() if g_fine is not None else None)
+    dt = grads["dq"].dtype
+    _lib.check("vsa_backward", _lib.load().vsa_backward(
+        _ptr(state.ws), _ptr(g_coarse), _ptr(g_fine), _ptr(dout), B, heads, d,
+        Grid.of(state.T, state.H, state.W), state.topk, float(state.scale), _ptr(grads["dq"]),
+        _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads.get("dgc")), _ptr(grads.get("dgf")), _DT[dt],
+        _ptr(ws), nbytes, _stream()))
+    return grads
+
+
+def device_status() -> int:
+    """Waits for the current stream; returns and clears the device error word."""
+    return int(_lib.load().vsa_device_status(_stream()))

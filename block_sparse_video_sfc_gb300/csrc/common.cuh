@@ -1,0 +1,103 @@
+// common.cuh -- shared definitions of the VSA CUDA library (host and device).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/vsa.h"
+
+namespace vsa {
+
+constexpr int kCube = 64;  // (4, 4, 4) tokens per cube
+
+// Bits of the device-side error word (see vsa_device_status).
+enum : int { kErrLut = 1, kErrTimeout = 2 };
+
+__device__ __forceinline__ void flag_error(int* err, int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// Native token index of offset o (0..63) of cube (ct, ch, cw):
+// t = 4ct + o/16, h = 4ch + (o/4)%4, w = 4cw + o%4.
+__host__ __device__ __forceinline__ int64_t native_token(int cube, int o, int H, int W) {
+  int cw_n = W >> 2, ch_n = H >> 2;
+  int cw = cube % cw_n;
+  int ch = (cube / cw_n) % ch_n;
+  int ct = cube / (cw_n * ch_n);
+  int t = 4 * ct + (o >> 4), h = 4 * ch + ((o >> 2) & 3), w = 4 * cw + (o & 3);
+  return (static_cast<int64_t>(t) * H + h) * W + w;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// Store 8 consecutive floats as bf16 (16 bytes) or f32 (32 bytes).
+__device__ __forceinline__ void store8(void* base, int64_t elem, const float* v, int dtype) {
+  if (dtype == VSA_DTYPE_BF16) {
+    uint4 u;
+    u.x = pack_bf16(v[0], v[1]);
+    u.y = pack_bf16(v[2], v[3]);
+    u.z = pack_bf16(v[4], v[5]);
+    u.w = pack_bf16(v[6], v[7]);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + elem) = u;
+  } else {
+    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + elem);
+    p[0] = make_float4(v[0], v[1], v[2], v[3]);
+    p[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+}
+__device__ __forceinline__ void load8_bf16(const void* base, int64_t elem, float* v) {
+  uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + elem);
+  v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x);
+  v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+  v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z);
+  v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+}
+__device__ __forceinline__ void load8_f32(const float* base, int64_t elem, float* v) {
+  float4 a = *reinterpret_cast<const float4*>(base + elem);
+  float4 b = *reinterpret_cast<const float4*>(base + elem + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const void* base, int64_t elem, int dtype, float* v) {
+  if (dtype == VSA_DTYPE_BF16) load8_bf16(base, elem, v);
+  else load8_f32(static_cast<const float*>(base), elem, v);
+}
+
+// ---------------------------------------------------------------- host side
+int* device_error_word();          // per-device error word (vsa_api.cu)
+int num_sms();                     // SM count of the current device
+
+int launch_permute(const void* const* src, void* const* dst, float* const* pooled, int ntensors, int BH,
+                   int d, int T, int H, int W, int inverse, cudaStream_t s);
+int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk,
+                       float scale, float* oc, float* lse_c, int32_t* idx, int32_t* cnt, float* scores,
+                       cudaStream_t s);
+int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt,
+                    int kmax, int BH, int N, int d, float scale, void* of, int of_dtype, float* lse,
+                    cudaStream_t s);
+size_t fine_bwd_ws_bytes(int BH, int N, int kmax);
+int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* of, int of_dtype,
+                    const float* lse, const void* dof, const int32_t* idx, const int32_t* cnt, int kmax, int BH,
+                    int N, int d, float scale, float* dq, float* dk, float* dv, void* ws, size_t ws_bytes,
+                    cudaStream_t s);
+int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const void* dof, const float* lse,
+                         const float* delta, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
+                         float scale, float* dq, float* dk, float* dv, uint32_t* inv_ws, cudaStream_t s);
+int launch_combine(const float* oc, const float* of, const void* gc, const void* gf, void* out, int out_dtype,
+                   int BH, int d, int T, int H, int W, cudaStream_t s);
+int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const float* oc, const float* of,
+                    __nv_bfloat16* dof, float* delta, float* doc, void* dgc, void* dgf, int grad_dtype, int BH, int d,
+                    int T, int H, int W, cudaStream_t s);
+int launch_coarse_bwd(const float* qc, const float* kc, const float* vc, const float* doc, const float* lse_c,
+                      int BH, int Nc, int d, float scale, float* P, float* dS, float* dqc, float* dkc, float* dvc,
+                      cudaStream_t s);
+int launch_finalize(const float* dqp, const float* dkp, const float* dvp, const float* dqc, const float* dkc,
+                    const float* dvc, void* dq, void* dk, void* dv, int grad_dtype, int BH, int d, int T, int H,
+                    int W, cudaStream_t s);
+
+}  // namespace vsa

@@ -1,0 +1,84 @@
+// permute_pool.cu -- 3D space-filling-curve token reordering with the cube
+// mean-pool fused ("VSA: Accelerating Video Diffusion Inference with Sparse
+// Attention on AMD GPUs", "Two-Stage Architecture": pre-stage SFC reordering
+// and the Stage 1 cube mean-pool).
+//
+// One CTA moves one cube (64 tokens x d) of one tensor: 16-byte vector loads
+// and stores; a cube's native tokens are 16 runs of 4 contiguous tokens, its
+// cube-order destination is one contiguous 64*d*2-byte block.  The pooled
+// mean is summed in fp32 while the data passes through registers.
+// HBM-bound: per tensor, N*d*2 bytes read + N*d*2 written (+ Nc*d*4 pooled).
+#include "common.cuh"
+
+namespace vsa {
+
+struct PermuteArgs {
+  const __nv_bfloat16* src[3];
+  __nv_bfloat16* dst[3];
+  float* pooled[3];
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc, int H, int W, int N,
+                                                           int inverse) {
+  constexpr int kChunks = D / 8;           // 16-byte chunks per token
+  constexpr int kTokPerPass = 256 / kChunks;
+  constexpr int kPasses = kCube / kTokPerPass;
+  __shared__ float red[kTokPerPass][D];
+  const int tensor = blockIdx.y;
+  const int64_t cube_glob = blockIdx.x;    // bh * Nc + cube
+  const int64_t bh = cube_glob / Nc;
+  const int cube = static_cast<int>(cube_glob % Nc);
+  const __nv_bfloat16* src = a.src[tensor] + bh * static_cast<int64_t>(N) * D;
+  __nv_bfloat16* dst = a.dst[tensor] + bh * static_cast<int64_t>(N) * D;
+  float* pooled = a.pooled[tensor];
+  const int j = threadIdx.x % kChunks;     // channel chunk, fixed per thread
+  const int o0 = threadIdx.x / kChunks;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+  for (int p = 0; p < kPasses; ++p) {
+    const int o = o0 + p * kTokPerPass;
+    const int64_t nat = native_token(cube, o, H, W);
+    const int64_t cub = static_cast<int64_t>(cube) * kCube + o;
+    const int64_t s_tok = inverse ? cub : nat;
+    const int64_t d_tok = inverse ? nat : cub;
+    uint4 v = *reinterpret_cast<const uint4*>(src + s_tok * D + j * 8);
+    *reinterpret_cast<uint4*>(dst + d_tok * D + j * 8) = v;
+    if (pooled) {
+      acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x);
+      acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
+      acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z);
+      acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
+    }
+  }
+  if (pooled) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red[o0][j * 8 + e] = acc[e];
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += 256) {
+      float s = 0.f;
+#pragma unroll 8
+      for (int r = 0; r < kTokPerPass; ++r) s += red[r][c];
+      pooled[cube_glob * D + c] = s * (1.0f / kCube);
+    }
+  }
+}
+
+int launch_permute(const void* const* src, void* const* dst, float* const* pooled, int ntensors, int BH, int d,
+                   int T, int H, int W, int inverse, cudaStream_t s) {
+  PermuteArgs a{};
+  for (int i = 0; i < ntensors; ++i) {
+    a.src[i] = static_cast<const __nv_bfloat16*>(src[i]);
+    a.dst[i] = static_cast<__nv_bfloat16*>(dst[i]);
+    a.pooled[i] = pooled ? pooled[i] : nullptr;
+  }
+  const int N = T * H * W, Nc = N / kCube;
+  dim3 grid(static_cast<unsigned>(static_cast<int64_t>(BH) * Nc), ntensors);
+  if (d == 128)
+    permute_pool_kernel<128><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse);
+  else
+    permute_pool_kernel<64><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse);
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
+}  // namespace vsa

@@ -1,0 +1,315 @@
+// vsa_api.cu -- the C ABI declared in include/vsa.h: argument checks, the
+// workspace layouts, and the order in which the kernels run.  Nothing here
+// allocates memory; every buffer belongs to the caller.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace vsa {
+namespace {
+
+__device__ int g_error_word;  // latched kernel-side errors (kErrLut | kErrTimeout)
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+std::mutex g_mu;
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+struct Dims {
+  int64_t BH, N, Nc;
+  int d, T, H, W;
+};
+
+int check_grid(const vsa_grid_t& g, int d, Dims* out, int64_t BH) {
+  if (g.ct != 4 || g.ch != 4 || g.cw != 4) return VSA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return VSA_ERR_UNSUPPORTED;
+  if (g.T <= 0 || g.H <= 0 || g.W <= 0 || BH <= 0) return VSA_ERR_ARG;
+  if (g.T % 4 || g.H % 4 || g.W % 4) return VSA_ERR_SHAPE;
+  const int64_t N = static_cast<int64_t>(g.T) * g.H * g.W;
+  if (N * BH >= (int64_t(1) << 31)) return VSA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+  *out = Dims{BH, N, N / kCube, d, g.T, g.H, g.W};
+  return VSA_OK;
+}
+
+// Forward workspace: the saved state of one vsa_forward call.
+struct FwdWs {
+  size_t qp, kp, vp, qc, kc, vc, oc, lsec, idx, cnt, of, lse, total;
+};
+FwdWs fwd_layout(const Dims& D, int K) {
+  FwdWs w{};
+  size_t o = 0;
+  const size_t big_bf16 = sizeof(__nv_bfloat16) * D.BH * D.N * D.d;
+  const size_t pooled = sizeof(float) * D.BH * D.Nc * D.d;
+  w.qp = o; o += align256(big_bf16);
+  w.kp = o; o += align256(big_bf16);
+  w.vp = o; o += align256(big_bf16);
+  w.qc = o; o += align256(pooled);
+  w.kc = o; o += align256(pooled);
+  w.vc = o; o += align256(pooled);
+  w.oc = o; o += align256(pooled);
+  w.lsec = o; o += align256(sizeof(float) * D.BH * D.Nc);
+  w.idx = o; o += align256(sizeof(int32_t) * D.BH * D.Nc * K);
+  w.cnt = o; o += align256(sizeof(int32_t) * D.BH * D.Nc);
+  w.of = o; o += align256(sizeof(float) * D.BH * D.N * D.d);
+  w.lse = o; o += align256(sizeof(float) * D.BH * D.N);
+  w.total = o;
+  return w;
+}
+
+// Backward workspace (scratch of one vsa_backward call).
+struct BwdWs {
+  size_t dof, delta, doc, P, dS, dqc, dkc, dvc, dqp, dkp, dvp, inv, total;
+};
+BwdWs bwd_layout(const Dims& D) {
+  BwdWs w{};
+  size_t o = 0;
+  const size_t pooled = sizeof(float) * D.BH * D.Nc * D.d;
+  const size_t big_f32 = sizeof(float) * D.BH * D.N * D.d;
+  const int64_t nwords = (D.Nc + 31) / 32;
+  w.dof = o; o += align256(sizeof(__nv_bfloat16) * D.BH * D.N * D.d);
+  w.delta = o; o += align256(sizeof(float) * D.BH * D.N);
+  w.doc = o; o += align256(pooled);
+  w.P = o; o += align256(sizeof(float) * D.BH * D.Nc * D.Nc);
+  w.dS = o; o += align256(sizeof(float) * D.BH * D.Nc * D.Nc);
+  w.dqc = o; o += align256(pooled);
+  w.dkc = o; o += align256(pooled);
+  w.dvc = o; o += align256(pooled);
+  w.dqp = o; o += align256(big_f32);
+  w.dkp = o; o += align256(big_f32);
+  w.dvp = o; o += align256(big_f32);
+  w.inv = o; o += align256(sizeof(uint32_t) * D.BH * D.Nc * nwords);
+  w.total = o;
+  return w;
+}
+
+template <typename T>
+T* at(const void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(const_cast<void*>(base)) + off);
+}
+
+}  // namespace
+
+int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess) g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_num_sms[dev]) cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  return g_num_sms[dev] > 0 ? g_num_sms[dev] : 148;
+}
+
+}  // namespace vsa
+
+using namespace vsa;
+
+extern "C" {
+
+const char* vsa_status_string(int status) {
+  switch (status) {
+    case VSA_OK: return "ok";
+    case VSA_ERR_ARG: return "invalid argument (null pointer, misaligned pointer, bad enum or size)";
+    case VSA_ERR_SHAPE: return "shape error (grid not divisible by the (4,4,4) cube or sizes inconsistent)";
+    case VSA_ERR_UNSUPPORTED: return "unsupported configuration (d must be 64 or 128, cube (4,4,4))";
+    case VSA_ERR_CUDA: return "a CUDA runtime call failed";
+    case VSA_ERR_TIMEOUT: return "a kernel's bounded wait expired";
+    case VSA_ERR_LUT: return "block index list entry or count out of range, or a repeated cube";
+    case VSA_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int vsa_device_status(void* stream) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return VSA_ERR_CUDA;
+  int* p = device_error_word();
+  if (!p) return VSA_ERR_CUDA;
+  int v = 0, zero = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return VSA_ERR_CUDA;
+  if (v && cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return VSA_ERR_CUDA;
+  if (v & kErrTimeout) return VSA_ERR_TIMEOUT;
+  if (v & kErrLut) return VSA_ERR_LUT;
+  return VSA_OK;
+}
+
+int vsa_permute(const void* x, void* y, float* pooled, int BH, int d, vsa_grid_t g, int inverse, void* stream) {
+  Dims D;
+  int st = check_grid(g, d, &D, BH);
+  if (st != VSA_OK) return st;
+  if (!x || !y || x == y || !aligned16(x) || !aligned16(y) || (pooled && !aligned16(pooled))) return VSA_ERR_ARG;
+  if (inverse != 0 && inverse != 1) return VSA_ERR_ARG;
+  if (inverse && pooled) return VSA_ERR_ARG;
+  const void* src[1] = {x};
+  void* dst[1] = {y};
+  float* pl[1] = {pooled};
+  return launch_permute(src, dst, pl, 1, BH, d, g.T, g.H, g.W, inverse, as_stream(stream));
+}
+
+int vsa_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk, float scale,
+                    float* o_coarse, float* lse_coarse, int32_t* kv_block_idx, int32_t* valid_block_num,
+                    float* scores, void* stream) {
+  if (d != 64 && d != 128) return VSA_ERR_UNSUPPORTED;
+  if (BH <= 0 || Nc <= 0) return VSA_ERR_ARG;
+  if (topk < 1 || topk > Nc) return VSA_ERR_ARG;
+  if (!qc || !kc || !kv_block_idx || (o_coarse && !vc)) return VSA_ERR_ARG;
+  if (!aligned16(qc) || !aligned16(kc) || (vc && !aligned16(vc)) || (o_coarse && !aligned16(o_coarse)))
+    return VSA_ERR_ARG;
+  return launch_coarse_topk(qc, kc, vc, BH, Nc, d, topk, scale, o_coarse, lse_coarse, kv_block_idx,
+                            valid_block_num, scores, as_stream(stream));
+}
+
+static int check_fine(const void* qp, const void* kp, const void* vp, const int32_t* idx, int kmax, int BH, int N,
+                      int d) {
+  if (d != 64 && d != 128) return VSA_ERR_UNSUPPORTED;
+  if (BH <= 0 || N <= 0 || kmax < 0) return VSA_ERR_ARG;
+  if (N % kCube) return VSA_ERR_SHAPE;
+  if (static_cast<int64_t>(BH) * N >= (int64_t(1) << 31)) return VSA_ERR_UNSUPPORTED;
+  if (!qp || !kp || !vp || (kmax > 0 && !idx)) return VSA_ERR_ARG;
+  if (!aligned16(qp) || !aligned16(kp) || !aligned16(vp)) return VSA_ERR_ARG;
+  return VSA_OK;
+}
+
+int vsa_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* kv_block_idx,
+                 const int32_t* valid_block_num, int max_kv_blocks, int BH, int N, int d, float scale, void* o_fine,
+                 int o_dtype, float* lse, void* stream) {
+  int st = check_fine(qp, kp, vp, kv_block_idx, max_kv_blocks, BH, N, d);
+  if (st != VSA_OK) return st;
+  if (!o_fine || !aligned16(o_fine)) return VSA_ERR_ARG;
+  if (o_dtype != VSA_DTYPE_BF16 && o_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
+  return launch_fine_fwd(qp, kp, vp, kv_block_idx, valid_block_num, max_kv_blocks, BH, N, d, scale, o_fine, o_dtype,
+                         lse, as_stream(stream));
+}
+
+int vsa_fine_bwd(const void* qp, const void* kp, const void* vp, const void* o_fine, int o_dtype, const float* lse,
+                 const void* do_fine, const int32_t* kv_block_idx, const int32_t* valid_block_num, int max_kv_blocks,
+                 int BH, int N, int d, float scale, float* dq, float* dk, float* dv, void* ws, size_t ws_bytes,
+                 void* stream) {
+  int st = check_fine(qp, kp, vp, kv_block_idx, max_kv_blocks, BH, N, d);
+  if (st != VSA_OK) return st;
+  if (!o_fine || !lse || !do_fine || !dq || !dk || !dv) return VSA_ERR_ARG;
+  if (!aligned16(o_fine) || !aligned16(do_fine) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return VSA_ERR_ARG;
+  if (o_dtype != VSA_DTYPE_BF16 && o_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
+  return launch_fine_bwd(qp, kp, vp, o_fine, o_dtype, lse, do_fine, kv_block_idx, valid_block_num, max_kv_blocks,
+                         BH, N, d, scale, dq, dk, dv, ws, ws_bytes, as_stream(stream));
+}
+
+size_t vsa_workspace_bytes(int op, int B, int heads, int d, vsa_grid_t g, int topk) {
+  Dims D;
+  if (B <= 0 || heads <= 0) return 0;
+  if (check_grid(g, d, &D, static_cast<int64_t>(B) * heads) != VSA_OK) return 0;
+  if (topk < 1 || topk > D.Nc) return 0;
+  switch (op) {
+    case VSA_OP_FORWARD: return fwd_layout(D, topk).total;
+    case VSA_OP_BACKWARD: return bwd_layout(D).total;
+    case VSA_OP_FINE_BWD: return fine_bwd_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.N), topk);
+    default: return 0;
+  }
+}
+
+int vsa_forward_saved(const void* fwd_ws, int B, int heads, int d, vsa_grid_t g, int topk, vsa_saved_t* out) {
+  Dims D;
+  if (!fwd_ws || !out || B <= 0 || heads <= 0) return VSA_ERR_ARG;
+  int st = check_grid(g, d, &D, static_cast<int64_t>(B) * heads);
+  if (st != VSA_OK) return st;
+  if (topk < 1 || topk > D.Nc) return VSA_ERR_ARG;
+  FwdWs w = fwd_layout(D, topk);
+  out->qp = at<void>(fwd_ws, w.qp);
+  out->kp = at<void>(fwd_ws, w.kp);
+  out->vp = at<void>(fwd_ws, w.vp);
+  out->qc = at<float>(fwd_ws, w.qc);
+  out->kc = at<float>(fwd_ws, w.kc);
+  out->vc = at<float>(fwd_ws, w.vc);
+  out->o_coarse = at<float>(fwd_ws, w.oc);
+  out->lse_coarse = at<float>(fwd_ws, w.lsec);
+  out->kv_block_idx = at<int32_t>(fwd_ws, w.idx);
+  out->valid_block_num = at<int32_t>(fwd_ws, w.cnt);
+  out->o_fine = at<float>(fwd_ws, w.of);
+  out->lse = at<float>(fwd_ws, w.lse);
+  return VSA_OK;
+}
+
+int vsa_forward(const void* q, const void* k, const void* v, const void* g_coarse, const void* g_fine, int B,
+                int heads, int d, vsa_grid_t g, int topk, float scale, void* out, int out_dtype, void* ws,
+                size_t ws_bytes, void* stream) {
+  Dims D;
+  if (B <= 0 || heads <= 0) return VSA_ERR_ARG;
+  int st = check_grid(g, d, &D, static_cast<int64_t>(B) * heads);
+  if (st != VSA_OK) return st;
+  if (topk < 1 || topk > D.Nc) return VSA_ERR_ARG;
+  if (!q || !k || !v || !out) return VSA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (g_coarse && !aligned16(g_coarse)) ||
+      (g_fine && !aligned16(g_fine)))
+    return VSA_ERR_ARG;
+  if (out_dtype != VSA_DTYPE_BF16 && out_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
+  FwdWs w = fwd_layout(D, topk);
+  if (!ws || ws_bytes < w.total || !aligned16(ws)) return VSA_ERR_WORKSPACE;
+  cudaStream_t s = as_stream(stream);
+  const int BH = static_cast<int>(D.BH), Nc = static_cast<int>(D.Nc), N = static_cast<int>(D.N);
+  const void* src[3] = {q, k, v};
+  void* dst[3] = {at<void>(ws, w.qp), at<void>(ws, w.kp), at<void>(ws, w.vp)};
+  float* pooled[3] = {at<float>(ws, w.qc), at<float>(ws, w.kc), at<float>(ws, w.vc)};
+  if ((st = launch_permute(src, dst, pooled, 3, BH, d, g.T, g.H, g.W, 0, s)) != VSA_OK) return st;
+  if ((st = launch_coarse_topk(pooled[0], pooled[1], pooled[2], BH, Nc, d, topk, scale, at<float>(ws, w.oc),
+                               at<float>(ws, w.lsec), at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), nullptr, s)) !=
+      VSA_OK)
+    return st;
+  if ((st = launch_fine_fwd(dst[0], dst[1], dst[2], at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), topk, BH, N, d,
+                            scale, at<float>(ws, w.of), VSA_DTYPE_F32, at<float>(ws, w.lse), s)) != VSA_OK)
+    return st;
+  return launch_combine(at<float>(ws, w.oc), at<float>(ws, w.of), g_coarse, g_fine, out, out_dtype, BH, d, g.T, g.H,
+                        g.W, s);
+}
+
+int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, const void* dout, int B, int heads,
+                 int d, vsa_grid_t g, int topk, float scale, void* dq, void* dk, void* dv, void* dg_coarse,
+                 void* dg_fine, int grad_dtype, void* ws, size_t ws_bytes, void* stream) {
+  Dims D;
+  if (B <= 0 || heads <= 0) return VSA_ERR_ARG;
+  int st = check_grid(g, d, &D, static_cast<int64_t>(B) * heads);
+  if (st != VSA_OK) return st;
+  if (topk < 1 || topk > D.Nc) return VSA_ERR_ARG;
+  if (!fwd_ws || !dout || !dq || !dk || !dv) return VSA_ERR_ARG;
+  if (!aligned16(fwd_ws) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (g_coarse && !aligned16(g_coarse)) || (g_fine && !aligned16(g_fine)) || (dg_coarse && !aligned16(dg_coarse)) ||
+      (dg_fine && !aligned16(dg_fine)))
+    return VSA_ERR_ARG;
+  if (grad_dtype != VSA_DTYPE_BF16 && grad_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
+  BwdWs w = bwd_layout(D);
+  if (!ws || ws_bytes < w.total || !aligned16(ws)) return VSA_ERR_WORKSPACE;
+  FwdWs f = fwd_layout(D, topk);
+  cudaStream_t s = as_stream(stream);
+  const int BH = static_cast<int>(D.BH), Nc = static_cast<int>(D.Nc), N = static_cast<int>(D.N);
+  if ((st = launch_bwd_prep(dout, g_coarse, g_fine, at<float>(fwd_ws, f.oc), at<float>(fwd_ws, f.of),
+                            at<__nv_bfloat16>(ws, w.dof), at<float>(ws, w.delta), at<float>(ws, w.doc),
+                            g_coarse ? dg_coarse : nullptr, g_fine ? dg_fine : nullptr, grad_dtype, BH, d, g.T, g.H,
+                            g.W, s)) != VSA_OK)
+    return st;
+  if ((st = launch_coarse_bwd(at<float>(fwd_ws, f.qc), at<float>(fwd_ws, f.kc), at<float>(fwd_ws, f.vc),
+                              at<float>(ws, w.doc), at<float>(fwd_ws, f.lsec), BH, Nc, d, scale, at<float>(ws, w.P),
+                              at<float>(ws, w.dS), at<float>(ws, w.dqc), at<float>(ws, w.dkc), at<float>(ws, w.dvc),
+                              s)) != VSA_OK)
+    return st;
+  if ((st = launch_fine_bwd_core(at<void>(fwd_ws, f.qp), at<void>(fwd_ws, f.kp), at<void>(fwd_ws, f.vp),
+                                 at<void>(ws, w.dof), at<float>(fwd_ws, f.lse), at<float>(ws, w.delta),
+                                 at<int32_t>(fwd_ws, f.idx), at<int32_t>(fwd_ws, f.cnt), topk, BH, N, d, scale,
+                                 at<float>(ws, w.dqp), at<float>(ws, w.dkp), at<float>(ws, w.dvp),
+                                 at<uint32_t>(ws, w.inv), s)) != VSA_OK)
+    return st;
+  return launch_finalize(at<float>(ws, w.dqp), at<float>(ws, w.dkp), at<float>(ws, w.dvp), at<float>(ws, w.dqc),
+                         at<float>(ws, w.dkc), at<float>(ws, w.dvc), dq, dk, dv, grad_dtype, BH, d, g.T, g.H, g.W, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,201 @@
+/*
+ * vsa.h -- C ABI of the GB300 (sm_103a) VSA library: the coarse-to-fine
+ * block-sparse video attention of "VSA: Accelerating Video Diffusion Inference
+ * with Sparse Attention on AMD GPUs" (ROCm blog; cited below as [AMD] with the
+ * section name) and of "VSA: Faster Video Diffusion with Trainable Sparse
+ * Attention" (Abstract; cited as [ABS]).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers are DEVICE pointers unless stated otherwise, owned by the
+ *    caller.  The library never allocates or frees memory; scratch space is a
+ *    caller-provided workspace whose size the *_workspace_bytes queries give.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Every call only enqueues work on that stream and returns; results are
+ *    ready when the stream reaches that point.
+ *  - Q, K, V (and gates, dO) are bf16, contiguous [B, heads, N, d] with
+ *    N = T*H*W tokens in native (t, h, w) raster order, token n = (t*H+h)*W+w,
+ *    unless a function says it takes the "cube order" (after vsa_permute).
+ *  - Cubes are (Ct, Ch, Cw) = (4, 4, 4) = 64 tokens ([AMD] "Stage 1: Coarse
+ *    Selection"); T, H, W must be multiples of 4.  Nc = N / 64 cubes.
+ *  - d (head dim) must be 64 or 128.
+ *  - Cube order: the 3D space-filling-curve reordering of [AMD] "Two-Stage
+ *    Architecture" is taken as cube-raster order: cube c = ((t/4)*(H/4) +
+ *    h/4)*(W/4) + w/4, offset o = ((t%4)*4 + h%4)*4 + w%4, position 64c + o.
+ *  - Block index list ("LUT", [AMD] "Block-Sparse Encoding" and "Using VSA
+ *    with CK Tile"): kv_block_idx int32 [BH, Nc, max_kv_blocks] holds the key
+ *    cubes each query cube attends to; valid_block_num int32 [BH, Nc] holds how
+ *    many entries of each row are used (0 <= count <= max_kv_blocks).
+ *    vsa_coarse_topk writes rows in descending coarse score, ties to the lower
+ *    cube id.  Entries are used as given (a repeated cube counts twice).
+ *  - Output dtype selectors take VSA_DTYPE_BF16 or VSA_DTYPE_F32.
+ *  - Return value: VSA_OK, or a negative vsa_status_t.  Argument and shape
+ *    errors are found on the host before anything is enqueued.  Errors found
+ *    by a kernel while it runs (an index outside [0, Nc), a count above
+ *    max_kv_blocks, a bounded wait that expired) are latched in a device-side
+ *    flag: the offending entry is skipped, and vsa_device_status() reports
+ *    and clears the flag.
+ */
+#ifndef VSA_H_
+#define VSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    VSA_OK = 0,
+    VSA_ERR_ARG = -1,         /* null pointer, bad enum, non-positive size */
+    VSA_ERR_SHAPE = -2,       /* grid not divisible by the cube, N mismatch */
+    VSA_ERR_UNSUPPORTED = -3, /* d not in {64,128}, cube shape not (4,4,4) */
+    VSA_ERR_CUDA = -4,        /* a CUDA runtime call failed */
+    VSA_ERR_TIMEOUT = -5,     /* a kernel's bounded wait expired */
+    VSA_ERR_LUT = -6,         /* index list entry or count out of range */
+    VSA_ERR_WORKSPACE = -7    /* workspace missing or too small */
+} vsa_status_t;
+
+typedef enum { VSA_DTYPE_BF16 = 0, VSA_DTYPE_F32 = 1 } vsa_dtype_t;
+
+/* Latent video grid and cube shape.  ct = ch = cw = 4 only. */
+typedef struct {
+    int T, H, W;
+    int ct, ch, cw;
+} vsa_grid_t;
+
+/*
+ * vsa_permute -- 3D space-filling-curve token reordering, with the cube
+ * mean-pool fused.  [AMD] "Two-Stage Architecture" (pre-stage SFC reordering;
+ * Stage 1 mean-pools each cube into one vector).
+ *   x        bf16 [BH, N, d]: native order (inverse = 0) or cube order (1).
+ *   y        bf16 [BH, N, d]: the same tokens in cube order (inverse = 0) or
+ *            native order (inverse = 1).  Must not alias x.
+ *   pooled   fp32 [BH, Nc, d] or NULL: with inverse = 0, the mean of the 64
+ *            tokens of every cube.  Must be NULL when inverse = 1.
+ */
+int vsa_permute(const void* x, void* y, float* pooled, int BH, int d, vsa_grid_t g, int inverse, void* stream);
+
+/*
+ * vsa_coarse_topk -- coarse cube-to-cube attention and the per-query-cube
+ * Top-K selection.  [AMD] "Stage 1: Coarse Selection" and "Generating Sparsity
+ * Patterns" (scores of pooled Q against pooled K, torch.topk over the last
+ * dimension); the coarse output of "Stage 2: Fine Computation" (global
+ * context).  All arithmetic is fp32.
+ *   qc, kc, vc  fp32 [BH, Nc, d] pooled Q, K, V (vc may be NULL when
+ *               o_coarse is NULL).
+ *   topk        1 <= topk <= Nc.
+ *   scale       score scale (1/sqrt(d) for the SDPA one).
+ *   o_coarse    fp32 [BH, Nc, d] or NULL: softmax(scale*Qc Kc^T) Vc.
+ *   lse_coarse  fp32 [BH, Nc] or NULL: log-sum-exp of each score row.
+ *   kv_block_idx    int32 [BH, Nc, topk]: selected key cubes, highest first.
+ *   valid_block_num int32 [BH, Nc] or NULL: set to topk.
+ *   scores      fp32 [BH, Nc, Nc] or NULL: the scaled coarse scores (for
+ *               inspection; costs Nc^2 writes per head).
+ */
+int vsa_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk,
+                    float scale, float* o_coarse, float* lse_coarse, int32_t* kv_block_idx,
+                    int32_t* valid_block_num, float* scores, void* stream);
+
+/*
+ * vsa_fine_fwd -- fine token-level attention inside the listed cubes only,
+ * online softmax.  [AMD] "Stage 2: Fine Computation", "Kernel Architecture"
+ * (running max and sum), "Sparse Traversal" (the index-list loop).
+ *   qp, kp, vp  bf16 [BH, N, d] in cube order.
+ *   o_fine      [BH, N, d] in cube order, dtype o_dtype:
+ *               O_f[i] = softmax_j(scale * q_i . k_j) v_j over the tokens j of
+ *               the listed cubes of i's cube; rows of a query cube with count 0
+ *               are 0.
+ *   lse         fp32 [BH, N] or NULL: natural-log sum-exp of each row
+ *               (-inf for count 0).
+ */
+int vsa_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* kv_block_idx,
+                 const int32_t* valid_block_num, int max_kv_blocks, int BH, int N, int d, float scale,
+                 void* o_fine, int o_dtype, float* lse, void* stream);
+
+/*
+ * vsa_fine_bwd -- gradient of the fine stage.  [ABS] (VSA is trained end to
+ * end as one differentiable operator); the index list is held constant.
+ *   qp, kp, vp, kv_block_idx, valid_block_num, max_kv_blocks, scale: as in
+ *               the forward call.
+ *   o_fine      [BH, N, d] the forward output (dtype o_dtype), lse fp32 [BH, N].
+ *   do_fine     bf16 [BH, N, d]: dL/dO_f in cube order.
+ *   dq, dk, dv  fp32 [BH, N, d] in cube order (overwritten).
+ *   ws          workspace of vsa_workspace_bytes(VSA_OP_FINE_BWD, ...) bytes.
+ */
+int vsa_fine_bwd(const void* qp, const void* kp, const void* vp, const void* o_fine, int o_dtype,
+                 const float* lse, const void* do_fine, const int32_t* kv_block_idx,
+                 const int32_t* valid_block_num, int max_kv_blocks, int BH, int N, int d, float scale,
+                 float* dq, float* dk, float* dv, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * vsa_forward -- the whole VSA forward pass: reorder + pool, coarse attention
+ * + Top-K, fine block-sparse attention, gated combination, inverse reorder.
+ * [AMD] "Two-Stage Architecture" end to end; the gated combination of the
+ * coarse and fine outputs ("Stage 2: Fine Computation", "Algorithmic Design")
+ * is read as out = g_coarse * O_c + g_fine * O_f elementwise, O_c broadcast to
+ * the 64 tokens of its cube.
+ *   q, k, v     bf16 [B, heads, N, d] native order.
+ *   g_coarse, g_fine  bf16 [B, heads, N, d] native order, or NULL (= ones).
+ *   scale       score scale for both stages (1/sqrt(d) for SDPA).
+ *   out         [B, heads, N, d] native order, dtype out_dtype.
+ *   ws          workspace of vsa_workspace_bytes(VSA_OP_FORWARD, ...) bytes.
+ *               It holds everything vsa_backward needs (the saved state):
+ *               keep it unchanged until the matching vsa_backward is done.
+ */
+int vsa_forward(const void* q, const void* k, const void* v, const void* g_coarse, const void* g_fine, int B,
+                int heads, int d, vsa_grid_t g, int topk, float scale, void* out, int out_dtype, void* ws,
+                size_t ws_bytes, void* stream);
+
+/*
+ * vsa_backward -- gradients of vsa_forward.  [ABS].
+ *   fwd_ws      the workspace the forward call filled (read only).
+ *   g_coarse, g_fine, B, heads, d, g, topk, scale: the same as in the forward.
+ *   dout        bf16 [B, heads, N, d] native order: dL/dout.
+ *   dq, dk, dv  [B, heads, N, d] native order, dtype grad_dtype.
+ *   dg_coarse, dg_fine  [B, heads, N, d] native, dtype grad_dtype; may be NULL,
+ *               and are ignored when the matching gate is NULL.
+ *   ws          workspace of vsa_workspace_bytes(VSA_OP_BACKWARD, ...) bytes.
+ */
+int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, const void* dout, int B,
+                 int heads, int d, vsa_grid_t g, int topk, float scale, void* dq, void* dk, void* dv,
+                 void* dg_coarse, void* dg_fine, int grad_dtype, void* ws, size_t ws_bytes, void* stream);
+
+enum { VSA_OP_FORWARD = 0, VSA_OP_BACKWARD = 1, VSA_OP_FINE_BWD = 2 };
+
+/* Workspace bytes for an operation (0 on a bad argument).  For
+ * VSA_OP_FINE_BWD, B*heads is BH and g/topk give N and max_kv_blocks. */
+size_t vsa_workspace_bytes(int op, int B, int heads, int d, vsa_grid_t g, int topk);
+
+/* Device pointers into a forward workspace (the saved state), for callers
+ * that want the intermediate results. */
+typedef struct {
+    void* qp;          /* bf16 [BH, N, d] cube order */
+    void* kp;
+    void* vp;
+    float* qc;         /* fp32 [BH, Nc, d] pooled */
+    float* kc;
+    float* vc;
+    float* o_coarse;   /* fp32 [BH, Nc, d] */
+    float* lse_coarse; /* fp32 [BH, Nc] */
+    int32_t* kv_block_idx;    /* [BH, Nc, topk] */
+    int32_t* valid_block_num; /* [BH, Nc] */
+    float* o_fine;     /* fp32 [BH, N, d] cube order */
+    float* lse;        /* fp32 [BH, N] */
+} vsa_saved_t;
+
+int vsa_forward_saved(const void* fwd_ws, int B, int heads, int d, vsa_grid_t g, int topk, vsa_saved_t* out);
+
+/* Waits for `stream`, then returns and clears the device-side error flag:
+ * VSA_OK, VSA_ERR_LUT or VSA_ERR_TIMEOUT (or VSA_ERR_CUDA). */
+int vsa_device_status(void* stream);
+
+/* Static description of a status code. */
+const char* vsa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VSA_H_ */

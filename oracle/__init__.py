@@ -62,6 +62,9 @@ def _load():
                 "orc_fine_bwd": ([P, P, P, P, P, P, I, I64, I64, I, D, P, P, P], None),
                 "orc_coarse_bwd": ([P, P, P, P, I64, I, I, D, P, P, P], None),
                 "orc_backward": ([P, P, P, P, P, I64, I, I, I, I, I, D, P, P, P, P, P, P, P], None),
+                "orc_fine_bwd_query_rows": ([P, P, P, P, P, P, I, I64, I, D, P, I64, P], None),
+                "orc_fine_bwd_key_cube": ([P, P, P, P, P, P, I, I64, I, D, I64, I, P, P], None),
+                "orc_combine_bwd": ([P, P, P, P, P, I64, I64, I, P, P, P, P], None),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -211,6 +214,42 @@ def fine_bwd(qp, kp, vp, dof, idx, cnt, scale: float):
     _load().orc_fine_bwd(_p(qp), _p(kp), _p(vp), _p(dof), _p(idx), _p(cnt), idx.shape[-1],
                          BH, N, d, float(scale), _p(dq), _p(dk), _p(dv))
     return dq, dk, dv
+
+
+def fine_bwd_query_rows(qp, kp, vp, dof, idx, cnt, scale: float, rows):
+    """dQ of the fine stage for the listed flat rows r = bh*N + i."""
+    qp, kp, vp, dof = _f64(qp), _f64(kp), _f64(vp), _f64(dof)
+    idx, cnt = _i32(idx), _i32(cnt)
+    BH, N, d = _bh(qp)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, d), dtype=np.float64)
+    _load().orc_fine_bwd_query_rows(_p(qp), _p(kp), _p(vp), _p(dof), _p(idx), _p(cnt), idx.shape[-1],
+                                    N, d, float(scale), _p(rows), rows.size, _p(out))
+    return out
+
+
+def fine_bwd_key_cube(qp, kp, vp, dof, idx, cnt, scale: float, bh: int, kcube: int):
+    """(dK, dV) of the 64 tokens of key cube `kcube` in head `bh`, fine stage."""
+    qp, kp, vp, dof = _f64(qp), _f64(kp), _f64(vp), _f64(dof)
+    idx, cnt = _i32(idx), _i32(cnt)
+    BH, N, d = _bh(qp)
+    dk = np.empty((64, d), dtype=np.float64)
+    dv = np.empty((64, d), dtype=np.float64)
+    _load().orc_fine_bwd_key_cube(_p(qp), _p(kp), _p(vp), _p(dof), _p(idx), _p(cnt), idx.shape[-1],
+                                  N, d, float(scale), bh, kcube, _p(dk), _p(dv))
+    return dk, dv
+
+
+def combine_bwd(dout_p, gc_p, gf_p, oc, of):
+    """Backward of the gated combination (reordered order) -> dof, doc, dgc, dgf."""
+    dout_p, oc, of = _f64(dout_p), _f64(oc), _f64(of)
+    gc_p, gf_p = _f64(gc_p), _f64(gf_p)
+    BH, N, d = _bh(of)
+    dof, dgc, dgf = np.empty_like(of), np.empty_like(of), np.empty_like(of)
+    doc = np.empty_like(oc)
+    _load().orc_combine_bwd(_p(dout_p), _p(gc_p), _p(gf_p), _p(oc), _p(of), BH, N, d,
+                            _p(dof), _p(doc), _p(dgc), _p(dgf))
+    return dof, doc, dgc, dgf
 
 
 def coarse_bwd(qc, kc, vc, doc, scale: float):

@@ -410,6 +410,149 @@ void orc_fine_bwd(const double *qp, const double *kp, const double *vp,
     }
 }
 
+/* Sampled fine backward, for checks at full size.
+ * dQ of the listed query rows r = bh*N + i (dq_rows [nrows, d]); the row's
+ * softmax, dP and D are recomputed from scratch exactly as orc_fine_bwd does. */
+void orc_fine_bwd_query_rows(const double *qp, const double *kp, const double *vp,
+                             const double *dof, const int32_t *idx, const int32_t *cnt,
+                             int Kmax, int64_t N, int d, double scale,
+                             const int64_t *rows, int64_t nrows, double *dq_rows)
+{
+    int64_t Nc = N / CUBE;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t a = 0; a < nrows; a++) {
+        int64_t bh = rows[a] / N, i = rows[a] % N;
+        int64_t qcube = i / CUBE;
+        int n = cnt[bh * Nc + qcube];
+        const int32_t *list = idx + (bh * Nc + qcube) * Kmax;
+        int64_t nk = (int64_t)n * CUBE;
+        double *out = dq_rows + a * d;
+        for (int c = 0; c < d; c++)
+            out[c] = 0.0;
+        if (nk == 0)
+            continue;
+        double *s = (double *)malloc(sizeof(double) * nk);
+        double *dp = (double *)malloc(sizeof(double) * nk);
+        const double *q = qp + (bh * N + i) * d;
+        const double *g = dof + (bh * N + i) * d;
+        double m = -INFINITY;
+        for (int64_t e = 0; e < nk; e++) {
+            int64_t j = (int64_t)list[e / CUBE] * CUBE + e % CUBE;
+            const double *kk = kp + (bh * N + j) * d;
+            const double *vv = vp + (bh * N + j) * d;
+            double dot = 0.0, dot2 = 0.0;
+            for (int c = 0; c < d; c++) {
+                dot += q[c] * kk[c];
+                dot2 += g[c] * vv[c];
+            }
+            s[e] = scale * dot;
+            dp[e] = dot2;
+            if (s[e] > m)
+                m = s[e];
+        }
+        double l = 0.0;
+        for (int64_t e = 0; e < nk; e++)
+            l += exp(s[e] - m);
+        double D = 0.0;
+        for (int64_t e = 0; e < nk; e++)
+            D += exp(s[e] - m) / l * dp[e];
+        for (int64_t e = 0; e < nk; e++) {
+            double ds = exp(s[e] - m) / l * (dp[e] - D);
+            int64_t j = (int64_t)list[e / CUBE] * CUBE + e % CUBE;
+            const double *kk = kp + (bh * N + j) * d;
+            for (int c = 0; c < d; c++)
+                out[c] += scale * ds * kk[c];
+        }
+        free(s);
+        free(dp);
+    }
+}
+
+/* dK and dV of the 64 tokens of key cube `kcube` of head bh: the sum over
+ * every query row whose cube lists kcube.  dk_rows, dv_rows [64, d]. */
+void orc_fine_bwd_key_cube(const double *qp, const double *kp, const double *vp,
+                           const double *dof, const int32_t *idx, const int32_t *cnt,
+                           int Kmax, int64_t N, int d, double scale, int64_t bh,
+                           int kcube, double *dk_rows, double *dv_rows)
+{
+    int64_t Nc = N / CUBE;
+    for (int64_t e = 0; e < (int64_t)CUBE * d; e++) {
+        dk_rows[e] = 0.0;
+        dv_rows[e] = 0.0;
+    }
+    int64_t maxk = (int64_t)Kmax * CUBE;
+    double *s = (double *)malloc(sizeof(double) * (maxk + 1));
+    double *dp = (double *)malloc(sizeof(double) * (maxk + 1));
+    for (int64_t i = 0; i < N; i++) {
+        int64_t qcube = i / CUBE;
+        int n = cnt[bh * Nc + qcube];
+        const int32_t *list = idx + (bh * Nc + qcube) * Kmax;
+        int hit = -1;
+        for (int e = 0; e < n; e++)
+            if (list[e] == kcube)
+                hit = e;
+        if (hit < 0)
+            continue;
+        int64_t nk = (int64_t)n * CUBE;
+        const double *q = qp + (bh * N + i) * d;
+        const double *g = dof + (bh * N + i) * d;
+        double m = -INFINITY;
+        for (int64_t e = 0; e < nk; e++) {
+            int64_t j = (int64_t)list[e / CUBE] * CUBE + e % CUBE;
+            const double *kk = kp + (bh * N + j) * d;
+            const double *vv = vp + (bh * N + j) * d;
+            double dot = 0.0, dot2 = 0.0;
+            for (int c = 0; c < d; c++) {
+                dot += q[c] * kk[c];
+                dot2 += g[c] * vv[c];
+            }
+            s[e] = scale * dot;
+            dp[e] = dot2;
+            if (s[e] > m)
+                m = s[e];
+        }
+        double l = 0.0;
+        for (int64_t e = 0; e < nk; e++)
+            l += exp(s[e] - m);
+        double D = 0.0;
+        for (int64_t e = 0; e < nk; e++)
+            D += exp(s[e] - m) / l * dp[e];
+        for (int o = 0; o < CUBE; o++) {
+            int64_t e = (int64_t)hit * CUBE + o;
+            double p = exp(s[e] - m) / l;
+            double ds = p * (dp[e] - D);
+            for (int c = 0; c < d; c++) {
+                dv_rows[o * d + c] += p * g[c];
+                dk_rows[o * d + c] += scale * ds * q[c];
+            }
+        }
+    }
+    free(s);
+    free(dp);
+}
+
+/* Backward of the gated combination, reordered order: dout_p = dL/dout.
+ * dof = g_f * dO; doc[cube] = sum over the cube of g_c * dO; dgc = dO * O_c;
+ * dgf = dO * O_f.  gc / gf may be NULL (ones). */
+void orc_combine_bwd(const double *dout_p, const double *gc, const double *gf,
+                     const double *oc, const double *of, int64_t BH, int64_t N, int d,
+                     double *dof, double *doc, double *dgc, double *dgf)
+{
+    int64_t Nc = N / CUBE;
+    memset(doc, 0, sizeof(double) * BH * Nc * d);
+    for (int64_t bh = 0; bh < BH; bh++)
+        for (int64_t i = 0; i < N; i++)
+            for (int c = 0; c < d; c++) {
+                int64_t e = (bh * N + i) * d + c;
+                int64_t ec = (bh * Nc + i / CUBE) * d + c;
+                double a = gc ? gc[e] : 1.0, b = gf ? gf[e] : 1.0;
+                dof[e] = b * dout_p[e];
+                doc[ec] += a * dout_p[e];
+                dgc[e] = dout_p[e] * oc[ec];
+                dgf[e] = dout_p[e] * of[e];
+            }
+}
+
 /* Coarse stage backward: doc = dL/dO_c [BH, Nc, d]; outputs overwritten. */
 void orc_coarse_bwd(const double *qc, const double *kc, const double *vc,
                     const double *doc, int64_t BH, int Nc, int d, double scale,
@@ -504,18 +647,7 @@ void orc_backward(const double *q, const double *k, const double *v,
         orc_permute(gc, gcp, BH, d, T, H, W, 0);
     if (gf)
         orc_permute(gf, gfp, BH, d, T, H, W, 0);
-    memset(doc, 0, small);
-    for (int64_t bh = 0; bh < BH; bh++)
-        for (int64_t i = 0; i < N; i++)
-            for (int c = 0; c < d; c++) {
-                int64_t e = (bh * N + i) * d + c;
-                int64_t ec = (bh * Nc + i / CUBE) * d + c;
-                double a = gc ? gcp[e] : 1.0, b = gf ? gfp[e] : 1.0;
-                dof[e] = b * dop[e];
-                doc[ec] += a * dop[e];
-                dgcp[e] = dop[e] * oc[ec];
-                dgfp[e] = dop[e] * of[e];
-            }
+    orc_combine_bwd(dop, gc ? gcp : NULL, gf ? gfp : NULL, oc, of, BH, N, d, dof, doc, dgcp, dgfp);
     if (gc && dgc)
         orc_permute(dgcp, dgc, BH, d, T, H, W, 1);
     if (gf && dgf)

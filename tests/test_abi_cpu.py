@@ -1,0 +1,86 @@
+"""The C-ABI library loads, exports every entry point include/vsa.h declares,
+and rejects bad arguments on the host before any CUDA call.  No GPU needed:
+every call here returns from the argument checks."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_video_sfc_gb300 import build
+    build.build()
+    from block_sparse_video_sfc_gb300 import _lib
+    return _lib
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "vsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(vsa_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 10
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for n in names:
+        assert hasattr(so, n), n
+    assert set(names) == set(lib.SIGNATURES)
+
+
+def test_status_strings(lib):
+    L = lib.load()
+    for s in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert L.vsa_status_string(s)
+    assert L.vsa_status_string(12345) == b"unknown status"
+
+
+def test_workspace_bytes(lib):
+    L = lib.load()
+    g = lib.Grid.of(16, 32, 64)
+    fwd = L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 154)
+    N, Nc = 32768, 512
+    assert fwd >= 12 * N * 128 * (3 * 2 + 4)   # permuted Q/K/V + fp32 O_f at least
+    assert L.vsa_workspace_bytes(lib.VSA_OP_BACKWARD, 1, 12, 128, g, 154) > 12 * N * 128 * 12
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 0) == 0        # K < 1
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, Nc + 1) == 0   # K > Nc
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 96, g, 4) == 0         # d
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, lib.Grid.of(6, 8, 8), 1) == 0
+    assert L.vsa_workspace_bytes(7, 1, 12, 128, g, 4) == 0
+
+
+def test_host_side_argument_errors(lib):
+    L = lib.load()
+    fake = ctypes.c_void_p(0x1000)       # never dereferenced: every call fails its checks first
+    fake2 = ctypes.c_void_p(0x2000)
+    g = lib.Grid.of(4, 8, 8)
+    # bad grid / cube / d
+    assert L.vsa_permute(fake, fake2, None, 1, 64, lib.Grid.of(4, 8, 6), 0, None) == lib.VSA_ERR_SHAPE
+    assert L.vsa_permute(fake, fake2, None, 1, 64, lib.Grid(4, 8, 8, 2, 4, 4), 0, None) == lib.VSA_ERR_UNSUPPORTED
+    assert L.vsa_permute(fake, fake2, None, 1, 80, g, 0, None) == lib.VSA_ERR_UNSUPPORTED
+    # null, aliasing, misaligned, pooled with inverse
+    assert L.vsa_permute(None, fake2, None, 1, 64, g, 0, None) == lib.VSA_ERR_ARG
+    assert L.vsa_permute(fake, fake, None, 1, 64, g, 0, None) == lib.VSA_ERR_ARG
+    assert L.vsa_permute(ctypes.c_void_p(0x1002), fake2, None, 1, 64, g, 0, None) == lib.VSA_ERR_ARG
+    assert L.vsa_permute(fake, fake2, fake, 1, 64, g, 1, None) == lib.VSA_ERR_ARG
+    # Top-K range
+    for K in (0, 5):
+        assert L.vsa_coarse_topk(fake, fake, fake, 1, 4, 64, K, 0.125, None, None, fake2, None, None,
+                                 None) == lib.VSA_ERR_ARG
+    # fine: N not a multiple of 64
+    assert L.vsa_fine_fwd(fake, fake, fake, fake2, None, 2, 1, 100, 64, 0.125, fake2, 1, None,
+                          None) == lib.VSA_ERR_SHAPE
+    assert L.vsa_fine_fwd(fake, fake, fake, fake2, None, 2, 1, 128, 64, 0.125, fake2, 7, None,
+                          None) == lib.VSA_ERR_ARG
+    # forward: workspace too small
+    assert L.vsa_forward(fake, fake, fake, None, None, 1, 2, 64, g, 2, 0.125, fake2, 0, fake2, 16,
+                         None) == lib.VSA_ERR_WORKSPACE
+    assert L.vsa_forward(fake, fake, fake, None, None, 1, 2, 64, g, 9, 0.125, fake2, 0, fake2, 1 << 30,
+                         None) == lib.VSA_ERR_ARG
+    assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, 0.125, fake2, fake2, fake2, None, None, 3,
+                          fake2, 1 << 30, None) == lib.VSA_ERR_ARG

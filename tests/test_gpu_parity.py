@@ -1,0 +1,246 @@
+"""GPU parity: every step of the CUDA path (through the C ABI) against the CPU
+oracle on the same seeded inputs.  Integer work (reordering, Top-K on given
+scores) must match bit for bit; floating-point outputs and gradients within
+max-abs 2e-2 / mean-abs 2e-3 (tests/parity.py).  The Top-K selection is
+checked against the oracle's float64 scores up to near-ties, and the fine
+stage is then checked on the GPU-chosen lists."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from parity import assert_close, check_topk_validity, exact_topk
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vsa():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from block_sparse_video_sfc_gb300 import build
+    build.build()
+    import block_sparse_video_sfc_gb300 as m
+    return m
+
+
+def dev(a, dtype=torch.bfloat16):
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda").to(dtype).contiguous()
+
+
+def host(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def status_ok(vsa):
+    torch.cuda.synchronize()
+    assert vsa.device_status() == 0
+
+
+# ---------------------------------------------------------------- reorder + pool
+@pytest.mark.parametrize("grid,d", [((4, 8, 8), 64), ((8, 12, 20), 128), ((12, 4, 8), 64), ((16, 32, 64), 128)])
+def test_permute_pool(vsa, oracle_mod, grid, d):
+    T, H, W = grid
+    BH = 3
+    x = synth.make_random((BH, T * H * W, d), seed=sum(grid) + d)
+    y, pooled = vsa.permute(dev(x), T, H, W, pool=True)
+    ref = oracle_mod.permute(x, T, H, W)
+    assert np.array_equal(host(y), ref)                               # bit exact (data move)
+    back = vsa.permute(y, T, H, W, inverse=True)
+    assert np.array_equal(host(back), x.astype(np.float64))           # round trip
+    np.testing.assert_allclose(host(pooled), oracle_mod.pool(ref), rtol=1e-5, atol=1e-6)
+    status_ok(vsa)
+
+
+# ---------------------------------------------------------------- coarse + Top-K
+@pytest.mark.parametrize("name", ["tiny", "small", "wan1.3b", "long"])
+def test_coarse_topk(vsa, oracle_mod, name):
+    wl = synth.WORKLOADS[name]
+    heads = list(range(wl.heads)) if wl.heads <= 12 else [0, wl.heads // 2, wl.heads - 1]
+    q, k, v = synth.make_qkv(wl, heads_subset=heads)
+    sh = (len(heads), wl.N, wl.d)
+    q, k, v = (a.reshape(sh) for a in (q, k, v))
+    pooled = [vsa.permute(dev(a), wl.T, wl.H, wl.W, pool=True)[1] for a in (q, k, v)]
+    r = vsa.coarse_topk(*pooled, wl.topk, want_scores=True)
+    status_ok(vsa)
+    gidx = r["idx"].cpu().numpy()
+    # 1) exact: the GPU Top-K of its own fp32 scores is the brute-force one
+    gscores = r["scores"].cpu().numpy()
+    np.testing.assert_array_equal(gidx, exact_topk(gscores, wl.topk))
+    assert np.all(r["cnt"].cpu().numpy() == wl.topk)
+    # 2) against the oracle's float64 scores: identical sets up to near-ties
+    pq, pk, pv = (oracle_mod.pool(oracle_mod.permute(a, wl.T, wl.H, wl.W)) for a in (q, k, v))
+    scores, oc, lse_c = oracle_mod.coarse(pq, pk, pv, wl.d ** -0.5)
+    np.testing.assert_allclose(gscores, scores, rtol=1e-4, atol=1e-4)
+    differing = check_topk_validity(gidx, scores, wl.topk)
+    assert differing <= max(2, gidx.shape[0] * gidx.shape[1] // 100), differing
+    np.testing.assert_allclose(host(r["oc"]), oc, rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(host(r["lse_c"]), lse_c, rtol=1e-5, atol=1e-4)
+
+
+# ---------------------------------------------------------------- fine forward
+def _fine_case(oracle_mod, wl, heads=None):
+    q, k, v = synth.make_qkv(wl, heads_subset=heads)
+    nh = wl.heads if heads is None else len(heads)
+    sh = (nh, wl.N, wl.d)
+    qp, kp, vp = (oracle_mod.permute(a.reshape(sh), wl.T, wl.H, wl.W) for a in (q, k, v))
+    return qp, kp, vp
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_dense", "small"])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_fine_fwd(vsa, oracle_mod, name, out_dtype):
+    wl = synth.WORKLOADS[name]
+    qp, kp, vp = _fine_case(oracle_mod, wl)
+    rng = np.random.default_rng(1)
+    idx = np.stack([np.stack([rng.permutation(wl.Nc)[:wl.topk] for _ in range(wl.Nc)])
+                    for _ in range(wl.BH)]).astype(np.int32)
+    cnt = np.full(idx.shape[:-1], wl.topk, np.int32)
+    of, lse = vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), dev(cnt, torch.int32),
+                           out_dtype=out_dtype)
+    status_ok(vsa)
+    rof, rlse = oracle_mod.fine_fwd(qp, kp, vp, idx, cnt, wl.d ** -0.5)
+    assert_close(host(of), rof, bf16_out=out_dtype == torch.bfloat16, what="O_f")
+    np.testing.assert_allclose(host(lse), rlse, rtol=1e-5, atol=1e-3)
+
+
+def test_fine_fwd_ragged_and_edge_lists(vsa, oracle_mod):
+    """Counts 0 / 1 / odd / K, K = 1 and an odd number of cubes (lone last pair)."""
+    wl = synth.Workload("odd", 1, 3, 128, 4, 4, 20, 3)   # Nc = 5 cubes (odd)
+    qp, kp, vp = _fine_case(oracle_mod, wl)
+    idx = np.array([[[4, 0, 2], [1, 3, 0], [0, 1, 2], [2, 4, 3], [3, 2, 1]]] * 3, dtype=np.int32)
+    cnt = np.array([[3, 0, 1, 2, 3], [0, 0, 0, 0, 1], [1, 1, 1, 1, 1]], dtype=np.int32)
+    of, lse = vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), dev(cnt, torch.int32))
+    status_ok(vsa)
+    rof, rlse = oracle_mod.fine_fwd(qp, kp, vp, idx, cnt, wl.d ** -0.5)
+    assert_close(host(of), rof, what="O_f ragged")
+    empty = np.isneginf(rlse)
+    assert np.all(np.isneginf(host(lse)[empty])) and np.all(host(of)[empty] == 0)
+    np.testing.assert_allclose(host(lse)[~empty], rlse[~empty], rtol=1e-5, atol=1e-3)
+
+
+def test_fine_fwd_dense_is_sdpa(vsa, oracle_mod):
+    """K = all cubes: the fine kernel equals dense attention (torch SDPA, fp32)."""
+    wl = synth.WORKLOADS["small"]
+    qp, kp, vp = _fine_case(oracle_mod, wl, heads=[0, 1])
+    idx = np.tile(np.arange(wl.Nc, dtype=np.int32), (2, wl.Nc, 1))
+    cnt = np.full((2, wl.Nc), wl.Nc, np.int32)
+    of, _ = vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), dev(cnt, torch.int32))
+    ref = torch.nn.functional.scaled_dot_product_attention(*(torch.tensor(a) for a in (qp, kp, vp))).numpy()
+    assert_close(host(of), ref, what="dense")
+
+
+def test_lut_errors_are_reported(vsa, oracle_mod):
+    wl = synth.WORKLOADS["tiny"]
+    qp, kp, vp = _fine_case(oracle_mod, wl)
+    idx = np.zeros((wl.BH, wl.Nc, 2), np.int32)
+    idx[..., 1] = 1
+    idx[0, 1, 1] = 7            # out of range
+    of, _ = vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), None)
+    assert vsa.device_status() == -6
+    idx[0, 1, 1] = 0            # repeated cube in a row
+    vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), None)
+    assert vsa.device_status() == -6
+    idx[0, 1, 1] = 1
+    vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), None)
+    assert vsa.device_status() == 0
+
+
+# ---------------------------------------------------------------- whole forward / backward
+def _e2e(vsa, oracle_mod, wl, gates, out_dtype, grad_dtype, heads=None):
+    q, k, v = synth.make_qkv(wl, heads_subset=heads)
+    gc = gf = None
+    if gates:
+        gc, gf = synth.make_gates(wl, heads_subset=heads)
+    dout = synth.make_dout(wl, heads_subset=heads)
+    D = lambda a: None if a is None else dev(a)
+    out, st = vsa.forward(D(q), D(k), D(v), wl.T, wl.H, wl.W, wl.topk, g_coarse=D(gc), g_fine=D(gf),
+                          out_dtype=out_dtype)
+    g = vsa.backward(st, D(dout), g_coarse=D(gc), g_fine=D(gf), grad_dtype=grad_dtype)
+    status_ok(vsa)
+    saved = st.saved()
+    return q, k, v, gc, gf, dout, out, g, saved
+
+
+@pytest.mark.parametrize("name,gates", [("tiny", True), ("tiny", False), ("tiny_dense", True), ("small", True)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_forward_backward(vsa, oracle_mod, name, gates, dtype):
+    wl = synth.WORKLOADS[name]
+    q, k, v, gc, gf, dout, out, g, saved = _e2e(vsa, oracle_mod, wl, gates, dtype, dtype)
+    gidx = saved["idx"].cpu().numpy().reshape(wl.B, wl.heads, wl.Nc, wl.topk)
+    ref0 = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=gc, gf=gf)
+    check_topk_validity(gidx, ref0["scores"], wl.topk)
+    # fine stage and everything after it on the GPU-chosen (validated) lists
+    ref = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=gc, gf=gf, lut=gidx)
+    bf = dtype == torch.bfloat16
+    assert_close(host(out), ref["out"], bf16_out=bf, what="out")
+    rg = oracle_mod.backward(q, k, v, dout, gidx, wl.T, wl.H, wl.W, gc=gc, gf=gf)
+    for n in ("dq", "dk", "dv", "dgc", "dgf"):
+        if rg[n] is not None:
+            assert_close(host(g[n]), rg[n], bf16_out=bf, what=n)
+
+
+def test_fine_bwd_entry_point(vsa, oracle_mod):
+    wl = synth.WORKLOADS["small"]
+    heads = [1, 6]
+    qp, kp, vp = _fine_case(oracle_mod, wl, heads=heads)
+    rng = np.random.default_rng(4)
+    idx = np.stack([np.stack([rng.permutation(wl.Nc)[:wl.topk] for _ in range(wl.Nc)])
+                    for _ in heads]).astype(np.int32)
+    cnt = np.full(idx.shape[:-1], wl.topk, np.int32)
+    cnt[0, 3] = 0
+    cnt[1, 7] = 5
+    dof = synth.make_random(qp.shape, seed=8)
+    of, lse = vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), dev(cnt, torch.int32))
+    dq, dk, dv = vsa.fine_bwd(dev(qp), dev(kp), dev(vp), of, lse, dev(dof), dev(idx, torch.int32),
+                              dev(cnt, torch.int32))
+    status_ok(vsa)
+    rq, rk, rv = oracle_mod.fine_bwd(qp, kp, vp, dof, idx, cnt, wl.d ** -0.5)
+    assert_close(host(dq), rq, what="dq")
+    assert_close(host(dk), rk, what="dk")
+    assert_close(host(dv), rv, what="dv")
+
+
+def test_full_size_head_sample(vsa, oracle_mod):
+    """Wan-1.3B-shaped layer (32768 tokens, 512 cubes, K=154, 12 heads) in the
+    launch configuration the benchmark times; the oracle recomputes head 0 in
+    full for the forward, and sampled query rows / key cubes for the backward."""
+    wl = synth.WORKLOADS["wan1.3b"]
+    q, k, v, gc, gf, dout, out, g, saved = _e2e(vsa, oracle_mod, wl, True, torch.float32, torch.float32)
+    h0 = lambda a: a[:, :1]
+    gidx = saved["idx"].cpu().numpy().reshape(wl.B, wl.heads, wl.Nc, wl.topk)
+    scale = wl.d ** -0.5
+    ref = oracle_mod.forward(h0(q), h0(k), h0(v), wl.T, wl.H, wl.W, wl.topk, gc=h0(gc), gf=h0(gf))
+    check_topk_validity(gidx[:, :1], ref["scores"], wl.topk)
+    lut = gidx[:, :1]
+    ref = oracle_mod.forward(h0(q), h0(k), h0(v), wl.T, wl.H, wl.W, wl.topk, gc=h0(gc), gf=h0(gf), lut=lut,
+                             want_scores=False)
+    assert_close(host(out)[:, :1], ref["out"], what="out head 0")
+    # backward, head 0: sampled rows of the fine stage + exact coarse stage
+    T_, H_, W_ = wl.T, wl.H, wl.W
+    P = lambda a: oracle_mod.permute(a.reshape(1, wl.N, wl.d), T_, H_, W_)
+    qp, kp, vp, gcp, gfp, dop = (P(h0(a)) for a in (q, k, v, gc, gf, dout))
+    pos = oracle_mod.sfc_table(T_, H_, W_)
+    dof, doc, _, _ = oracle_mod.combine_bwd(dop, gcp, gfp, ref["oc"].reshape(1, wl.Nc, wl.d),
+                                            ref["of"].reshape(1, wl.N, wl.d))
+    pq, pk, pv = (oracle_mod.pool(a) for a in (qp, kp, vp))
+    dqc, dkc, dvc = oracle_mod.coarse_bwd(pq, pk, pv, doc, scale)
+    idx1 = lut.reshape(1, wl.Nc, wl.topk)
+    cnt1 = np.full((1, wl.Nc), wl.topk, np.int32)
+    rows = np.random.default_rng(0).choice(wl.N, 48, replace=False)        # reordered positions
+    dq_rows = oracle_mod.fine_bwd_query_rows(qp, kp, vp, dof, idx1, cnt1, scale, rows)
+    dq_rows += dqc[0, rows // 64] / 64.0
+    native = np.argsort(pos)[rows]                                          # native token of each row
+    assert_close(host(g["dq"])[0, 0, native], dq_rows, what="dq rows")
+    inv_count = np.bincount(idx1.reshape(-1), minlength=wl.Nc)
+    for c in (int(np.argmin(np.where(inv_count > 0, inv_count, 1 << 30))), int(np.argmax(inv_count == 0)) if
+              (inv_count == 0).any() else 0):
+        dk_c, dv_c = oracle_mod.fine_bwd_key_cube(qp, kp, vp, dof, idx1, cnt1, scale, 0, c)
+        dk_c += dkc[0, c] / 64.0
+        dv_c += dvc[0, c] / 64.0
+        nat = np.argsort(pos)[64 * c:64 * c + 64]
+        assert_close(host(g["dk"])[0, 0, nat], dk_c, what=f"dk cube {c}")
+        assert_close(host(g["dv"])[0, 0, nat], dv_c, what=f"dv cube {c}")
+    # properties at full size, all heads: sum_j dK_j = 0 per head and channel
+    dk_sum = host(g["dk"]).sum(axis=2)
+    assert np.abs(dk_sum).max() < 5e-2 * max(1.0, np.abs(host(g["dk"])).max())

@@ -325,3 +325,26 @@ def test_head_subset_generator_matches_full(oracle_mod):
     sub = synth.make_qkv(wl, heads_subset=[0, 7])
     for f, s in zip(full, sub):
         np.testing.assert_array_equal(f[:, [0, 7]], s)
+
+
+def test_sampled_backward_functions_match_full(oracle_mod):
+    """The sampled dQ-row and dK/dV-key-cube functions (used at full size)
+    reproduce the full fine backward, which autograd pins above."""
+    wl = synth.WORKLOADS["small"]
+    q, k, v = (a.reshape(1, wl.N, wl.d) for a in synth.make_qkv(wl, heads_subset=[2]))
+    pos = oracle_mod.sfc_table(wl.T, wl.H, wl.W)
+    qp, kp, vp = (oracle_mod.permute(a, wl.T, wl.H, wl.W) for a in (q, k, v))
+    dof = synth.make_random((1, wl.N, wl.d), seed=5)
+    r = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk)
+    idx = r["idx"]
+    cnt = np.full(idx.shape[:-1], wl.topk, np.int32)
+    scale = wl.d ** -0.5
+    dq, dk, dv = oracle_mod.fine_bwd(qp, kp, vp, dof, idx, cnt, scale)
+    rows = np.array([0, 5, 64, 1000, wl.N - 1])
+    np.testing.assert_allclose(oracle_mod.fine_bwd_query_rows(qp, kp, vp, dof, idx, cnt, scale, rows),
+                               dq[0, rows], rtol=1e-10, atol=1e-12)
+    for c in (0, 17, wl.Nc - 1):
+        sk, sv = oracle_mod.fine_bwd_key_cube(qp, kp, vp, dof, idx, cnt, scale, 0, c)
+        np.testing.assert_allclose(sk, dk[0, 64 * c:64 * c + 64], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(sv, dv[0, 64 * c:64 * c + 64], rtol=1e-10, atol=1e-12)
+    assert pos.size == wl.N
