@@ -140,8 +140,8 @@ class ForwardState:
             return self.ws[off:off + n * esize].view(dtype).view(shape)
 
         return dict(
-            qp=view(s.qp, (BH, N, d), torch.bfloat16), kp=view(s.kp, (BH, N, d), torch.bfloat16),
-            vp=view(s.vp, (BH, N, d), torch.bfloat16), qc=view(s.qc, (BH, Nc, d), torch.float32),
+            qp=view(s.qp, (BH, N, d), torch.float16), kp=view(s.kp, (BH, N, d), torch.float16),
+            vp=view(s.vp, (BH, N, d), torch.float16), qc=view(s.qc, (BH, Nc, d), torch.float32),
             kc=view(s.kc, (BH, Nc, d), torch.float32), vc=view(s.vc, (BH, Nc, d), torch.float32),
             oc=view(s.o_coarse, (BH, Nc, d), torch.float32),
             lse_c=view(s.lse_coarse, (BH, Nc), torch.float32),

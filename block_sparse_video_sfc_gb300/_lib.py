@@ -19,6 +19,7 @@ VSA_ERR_CUDA = -4
 VSA_ERR_TIMEOUT = -5
 VSA_ERR_LUT = -6
 VSA_ERR_WORKSPACE = -7
+VSA_ERR_RANGE = -8
 
 VSA_DTYPE_BF16 = 0
 VSA_DTYPE_F32 = 1

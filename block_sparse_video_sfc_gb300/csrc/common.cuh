@@ -1,6 +1,7 @@
 // common.cuh -- shared definitions of the VSA CUDA library (host and device).
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -11,7 +12,7 @@ namespace vsa {
 constexpr int kCube = 64;  // (4, 4, 4) tokens per cube
 
 // Bits of the device-side error word (see vsa_device_status).
-enum : int { kErrLut = 1, kErrTimeout = 2 };
+enum : int { kErrLut = 1, kErrTimeout = 2, kErrRange = 4 };
 
 __device__ __forceinline__ void flag_error(int* err, int bit) {
   if (err) atomicOr(err, bit);
@@ -33,6 +34,27 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
+}
+// fp16 pair, round to nearest; values beyond the fp16 range saturate to
+// +-65504 instead of becoming infinite.
+constexpr float kF16Max = 65504.0f;
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 p = __floats2half2_rn(fminf(fmaxf(lo, -kF16Max), kF16Max), fminf(fmaxf(hi, -kF16Max), kF16Max));
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+__device__ __forceinline__ float f16_lo(uint32_t v) { return __low2float(*reinterpret_cast<const __half2*>(&v)); }
+__device__ __forceinline__ float f16_hi(uint32_t v) { return __high2float(*reinterpret_cast<const __half2*>(&v)); }
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
+template <bool F16>
+__device__ __forceinline__ float lo2(uint32_t v) {
+  return F16 ? f16_lo(v) : bf16_lo(v);
+}
+template <bool F16>
+__device__ __forceinline__ float hi2(uint32_t v) {
+  return F16 ? f16_hi(v) : bf16_hi(v);
 }
 
 // Store 8 consecutive floats as bf16 (16 bytes) or f32 (32 bytes).
@@ -73,12 +95,13 @@ int* device_error_word();          // per-device error word (vsa_api.cu)
 int num_sms();                     // SM count of the current device
 
 int launch_permute(const void* const* src, void* const* dst, float* const* pooled, int ntensors, int BH,
-                   int d, int T, int H, int W, int inverse, cudaStream_t s);
+                   int d, int T, int H, int W, int inverse, int f16_out, cudaStream_t s);
+int make_tile_map(void* map, const void* base, int64_t rows, int d, int f16);
 int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk,
                        float scale, float* oc, float* lse_c, int32_t* idx, int32_t* cnt, float* scores,
                        cudaStream_t s);
 int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt,
-                    int kmax, int BH, int N, int d, float scale, void* of, int of_dtype, float* lse,
+                    int kmax, int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, int f16_in,
                     cudaStream_t s);
 size_t fine_bwd_ws_bytes(int BH, int N, int kmax);
 int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* of, int of_dtype,
@@ -91,7 +114,7 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
 int launch_combine(const float* oc, const float* of, const void* gc, const void* gf, void* out, int out_dtype,
                    int BH, int d, int T, int H, int W, cudaStream_t s);
 int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const float* oc, const float* of,
-                    __nv_bfloat16* dof, float* delta, float* doc, void* dgc, void* dgf, int grad_dtype, int BH, int d,
+                    __half* dof, float* delta, float* doc, void* dgc, void* dgf, int grad_dtype, int BH, int d,
                     int T, int H, int W, cudaStream_t s);
 int launch_coarse_bwd(const float* qc, const float* kc, const float* vc, const float* doc, const float* lse_c,
                       int BH, int Nc, int d, float scale, float* P, float* dS, float* dqc, float* dkc, float* dvc,

@@ -28,8 +28,6 @@
 
 namespace vsa {
 
-int make_tile_map(CUtensorMap* map, const void* base, int64_t rows, int d);
-
 namespace {
 
 constexpr int kThreads = 192;
@@ -181,9 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0 && steps > 0) {
-      constexpr uint32_t id_ss = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t id_ts = idesc_bf16_f32(128, D, 0, 1);
-      constexpr uint32_t id_dq = idesc_bf16_f32(128, 128, 1, 1);
+      constexpr uint32_t id_ss = idesc_f32acc(128, 128, 0, 0, 1);
+      constexpr uint32_t id_ts = idesc_f32acc(128, D, 0, 1, 1);
+      constexpr uint32_t id_dq = idesc_f32acc(128, 128, 1, 1, 1);
       constexpr uint32_t lbo_kt = D == 128 ? 16384u : static_cast<uint32_t>(L::kZero - L::kK);
       bool ok = mbar_wait(&bar_kv, 0);
       for (int j = 0; j < steps && ok; ++j) {
@@ -194,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int b = kk >> 2, w = kk & 3;
-          mma_bf16_ss(tmem + kColS, sdesc_sw128(smem_u32(sm + L::kK + b * 16384 + w * 32), 16, 1024),
+          mma_ss(tmem + kColS, sdesc_sw128(smem_u32(sm + L::kK + b * 16384 + w * 32), 16, 1024),
                       sdesc_sw128(smem_u32(sm + L::kQ + b * 16384 + w * 32), 16, 1024), id_ss, kk > 0);
         }
         if (j > 0) ok = ok && mbar_wait(&bar_dqr, (j - 1) & 1);  // dQ^T of step j-1 read out
@@ -203,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int b = kk >> 2, w = kk & 3;
-          mma_bf16_ss(tmem + kColDP, sdesc_sw128(smem_u32(sm + L::kV + b * 16384 + w * 32), 16, 1024),
+          mma_ss(tmem + kColDP, sdesc_sw128(smem_u32(sm + L::kV + b * 16384 + w * 32), 16, 1024),
                       sdesc_sw128(smem_u32(sm + L::kDO + b * 16384 + w * 32), 16, 1024), id_ss, kk > 0);
         }
         mma_commit(&bar_mma1);
@@ -220,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ss(tmem + kColDQ, sdesc_sw128(smem_u32(sm + L::kK + kk * 2048), lbo_kt, 1024),
+          mma_ss(tmem + kColDQ, sdesc_sw128(smem_u32(sm + L::kK + kk * 2048), lbo_kt, 1024),
                       sdesc_sw128(smem_u32(sm + L::kDS + kk * 2048), 16384, 1024), id_dq, kk > 0);
         mma_commit(&bar_mma2);
       }
@@ -273,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
           float pb = valid ? fast_exp2(sv[c + 1] * p.scale_log2 - lse2[q + 1]) : 0.f;
           float da = pa * (dv[c] - del[q]);
           float db = pb * (dv[c + 1] - del[q + 1]);
-          pp[c >> 1] = __uint_as_float(pack_bf16(pa, pb));
-          dsp[32 * h + (c >> 1)] = pack_bf16(da, db);
+          pp[c >> 1] = __uint_as_float(pack_f16(pa, pb));
+          dsp[32 * h + (c >> 1)] = pack_f16(da, db);
         }
 #pragma unroll
         for (int c = 0; c < 32; c += 16) tmem_st16(lane_addr + kColP + 32 * h + c, pp + c);
@@ -375,8 +373,8 @@ __global__ void build_inverse_bits(const int32_t* __restrict__ idx, const int32_
   atomicOr(inv + (bh * Nc + c) * nwords + (q >> 5), 1u << (q & 31));
 }
 
-// D_i = dO_i . O_i (fp32), one warp per row.
-__global__ void delta_kernel(const void* __restrict__ of, int of_dtype, const __nv_bfloat16* __restrict__ dof,
+// D_i = dO_i . O_i (fp32, dO as the fp16 operand the MMAs use), one warp per row.
+__global__ void delta_kernel(const void* __restrict__ of, int of_dtype, const __half* __restrict__ dof,
                              int64_t rows, int d, float* __restrict__ delta) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -385,13 +383,31 @@ __global__ void delta_kernel(const void* __restrict__ of, int of_dtype, const __
   for (int c = lane * 8; c < d; c += 256) {
     float a[8], b[8];
     load8(of, row * d + c, of_dtype, a);
-    load8_bf16(dof, row * d + c, b);
+    uint4 u = *reinterpret_cast<const uint4*>(dof + row * d + c);
+    b[0] = f16_lo(u.x); b[1] = f16_hi(u.x); b[2] = f16_lo(u.y); b[3] = f16_hi(u.y);
+    b[4] = f16_lo(u.z); b[5] = f16_hi(u.z); b[6] = f16_lo(u.w); b[7] = f16_hi(u.w);
 #pragma unroll
     for (int i = 0; i < 8; ++i) s = fmaf(a[i], b[i], s);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (lane == 0) delta[row] = s;
+}
+
+// bf16 -> fp16 copy (exact within the fp16 range; larger values saturate and
+// latch kErrRange).  n8 = number of 8-element groups.
+__global__ void to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n8, int* err) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    uint4 v = src[i];
+    const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                        bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+    bool big = false;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) big |= !(fabsf(f[e]) <= kF16Max);
+    if (big) flag_error(err, kErrRange);
+    dst[i] = make_uint4(pack_f16(f[0], f[1]), pack_f16(f[2], f[3]), pack_f16(f[4], f[5]), pack_f16(f[6], f[7]));
+  }
 }
 
 }  // namespace
@@ -401,28 +417,29 @@ size_t fine_bwd_ws_bytes(int BH, int N, int kmax) {
   const int64_t Nc = N / kCube, nwords = (Nc + 31) / 32;
   size_t inv = sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords;
   size_t delta = sizeof(float) * static_cast<size_t>(BH) * N;
-  return ((inv + 255) & ~size_t(255)) + ((delta + 255) & ~size_t(255));
+  size_t copy = sizeof(__half) * static_cast<size_t>(BH) * N * 128;  // room for d <= 128
+  return ((inv + 255) & ~size_t(255)) + ((delta + 255) & ~size_t(255)) + 4 * ((copy + 255) & ~size_t(255));
 }
 
 int launch_delta(const void* of, int of_dtype, const void* dof, int64_t rows, int d, float* delta, cudaStream_t s) {
   const int warps = 8;
   delta_kernel<<<static_cast<unsigned>((rows + warps - 1) / warps), warps * 32, 0, s>>>(
-      of, of_dtype, static_cast<const __nv_bfloat16*>(dof), rows, d, delta);
+      of, of_dtype, static_cast<const __half*>(dof), rows, d, delta);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
-// Fine backward with the row statistics D given.  inv_ws: bit-matrix scratch
-// of fine_bwd_ws_bytes' first part.
+// Fine backward with the row statistics D given.  qp, kp, vp, dof are fp16
+// (cube order); inv_ws: scratch for the inverse-list bit matrix.
 int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const void* dof, const float* lse,
                          const float* delta, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
                          float scale, float* dq, float* dk, float* dv, uint32_t* inv_ws, cudaStream_t s) {
   BwdParams p{};
   const int64_t rows = static_cast<int64_t>(BH) * N;
   int st;
-  if ((st = make_tile_map(&p.tq, qp, rows, d)) != VSA_OK) return st;
-  if ((st = make_tile_map(&p.tk, kp, rows, d)) != VSA_OK) return st;
-  if ((st = make_tile_map(&p.tv, vp, rows, d)) != VSA_OK) return st;
-  if ((st = make_tile_map(&p.tdo, dof, rows, d)) != VSA_OK) return st;
+  if ((st = make_tile_map(&p.tq, qp, rows, d, 1)) != VSA_OK) return st;
+  if ((st = make_tile_map(&p.tk, kp, rows, d, 1)) != VSA_OK) return st;
+  if ((st = make_tile_map(&p.tv, vp, rows, d, 1)) != VSA_OK) return st;
+  if ((st = make_tile_map(&p.tdo, dof, rows, d, 1)) != VSA_OK) return st;
   const int Nc = N / kCube, nwords = (Nc + 31) / 32;
   p.lse = lse;
   p.delta = delta;
@@ -463,17 +480,33 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
+// Public fine backward: bf16 inputs are copied to fp16 in the workspace first.
 int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* of, int of_dtype, const float* lse,
                     const void* dof, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
                     float scale, float* dq, float* dk, float* dv, void* ws, size_t ws_bytes, cudaStream_t s) {
   if (!ws || ws_bytes < fine_bwd_ws_bytes(BH, N, kmax)) return VSA_ERR_WORKSPACE;
-  const int64_t Nc = N / kCube, nwords = (Nc + 31) / 32;
-  const size_t inv = sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords;
-  uint32_t* inv_ws = static_cast<uint32_t*>(ws);
-  float* delta = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ((inv + 255) & ~size_t(255)));
-  int st = launch_delta(of, of_dtype, dof, static_cast<int64_t>(BH) * N, d, delta, s);
+  const int64_t Nc = N / kCube, nwords = (Nc + 31) / 32, rows = static_cast<int64_t>(BH) * N;
+  auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint32_t* inv_ws = reinterpret_cast<uint32_t*>(w);
+  w += a256(sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords);
+  float* delta = reinterpret_cast<float*>(w);
+  w += a256(sizeof(float) * rows);
+  const size_t copy = a256(sizeof(__half) * static_cast<size_t>(rows) * 128);
+  const void* srcs[4] = {qp, kp, vp, dof};
+  void* h[4];
+  int* err = device_error_word();
+  for (int i = 0; i < 4; ++i, w += copy) {
+    h[i] = w;
+    const int64_t n8 = rows * d / 8;
+    const int64_t nblk = (n8 + 255) / 256;
+    to_f16_kernel<<<static_cast<unsigned>(nblk < 65535 ? nblk : 65535), 256, 0, s>>>(
+        static_cast<const uint4*>(srcs[i]), static_cast<uint4*>(h[i]), n8, err);
+  }
+  int st = launch_delta(of, of_dtype, h[3], rows, d, delta, s);
   if (st != VSA_OK) return st;
-  return launch_fine_bwd_core(qp, kp, vp, dof, lse, delta, idx, cnt, kmax, BH, N, d, scale, dq, dk, dv, inv_ws, s);
+  return launch_fine_bwd_core(h[0], h[1], h[2], h[3], lse, delta, idx, cnt, kmax, BH, N, d, scale, dq, dk, dv, inv_ws,
+                              s);
 }
 
 }  // namespace vsa

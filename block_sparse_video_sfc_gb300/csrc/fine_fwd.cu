@@ -59,7 +59,8 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-template <int D>
+// F16: Q, K, V (and P) are fp16 instead of bf16; accumulation is fp32 either way.
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -222,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0 && steps > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
+      constexpr uint32_t idesc_s = idesc_f32acc(128, 128, 0, 0, F16);
+      constexpr uint32_t idesc_pv = idesc_f32acc(128, D, 0, 1, F16);
       bool ok = mbar_wait(&bar_q, 0);
       auto issue_s = [&](int j) {
         const int s = j % kStages;
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
           const int b = kk >> 2, w = kk & 3;
           uint64_t ad = sdesc_sw128(smem_u32(sm + L::kQ + b * 16384 + w * 32), 16, 1024);
           uint64_t bd = sdesc_sw128(smem_u32(sm + L::kK + s * L::kTile + b * 16384 + w * 32), 16, 1024);
-          mma_bf16_ss(tmem + dcol, ad, bd, idesc_s, kk > 0);
+          mma_ss(tmem + dcol, ad, bd, idesc_s, kk > 0);
         }
         mma_commit(&bar_s[j & 1]);
       };
@@ -325,8 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       for (int c = 0; c < 128; c += 2) {
         const float a = (m == -INFINITY) ? 0.f : fast_exp2(sv[c] - m);
         const float b = (m == -INFINITY) ? 0.f : fast_exp2(sv[c + 1] - m);
-        rs += a + b;
-        pk[c >> 1] = __uint_as_float(pack_bf16(a, b));
+        const uint32_t pp = pack2<F16>(a, b);
+        // The row sum uses the same rounded weights the PV MMA sees, so
+        // O / l stays an exact convex combination of V rows.
+        rs += lo2<F16>(pp) + hi2<F16>(pp);
+        pk[c >> 1] = __uint_as_float(pp);
       }
       l += rs;
       // P(j) may overwrite buffer j&1 once PV(j-2), which read it, is done.
@@ -390,28 +394,30 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
 
 }  // namespace
 
-// 2D bf16 tensor map over [rows, d] with a {64, 64} box and 128-byte swizzle.
-int make_tile_map(CUtensorMap* map, const void* base, int64_t rows, int d) {
+// 2D bf16 / fp16 tensor map over [rows, d] with a {64, 64} box and 128-byte swizzle.
+int make_tile_map(void* map_out, const void* base, int64_t rows, int d, int f16) {
+  CUtensorMap* map = static_cast<CUtensorMap*>(map_out);
   auto enc = get_encoder();
   if (!enc) return VSA_ERR_CUDA;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
   cuuint32_t box[2] = {64, 64};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? VSA_OK : VSA_ERR_CUDA;
 }
 
 int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt, int kmax,
-                    int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, cudaStream_t s) {
+                    int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, int f16_in,
+                    cudaStream_t s) {
   FwdParams p{};
   const int64_t rows = static_cast<int64_t>(BH) * N;
   int st;
-  if ((st = make_tile_map(&p.tq, qp, rows, d)) != VSA_OK) return st;
-  if ((st = make_tile_map(&p.tk, kp, rows, d)) != VSA_OK) return st;
-  if ((st = make_tile_map(&p.tv, vp, rows, d)) != VSA_OK) return st;
+  if ((st = make_tile_map(&p.tq, qp, rows, d, f16_in)) != VSA_OK) return st;
+  if ((st = make_tile_map(&p.tk, kp, rows, d, f16_in)) != VSA_OK) return st;
+  if ((st = make_tile_map(&p.tv, vp, rows, d, f16_in)) != VSA_OK) return st;
   p.idx = idx;
   p.cnt = cnt;
   p.kmax = kmax;
@@ -426,21 +432,20 @@ int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_
   const int nwords = (p.Nc + 31) / 32;
   const size_t extra = sizeof(uint32_t) * (2 * kmax + 2 + 2 * nwords);
   dim3 grid(p.npairs, BH);
-  if (d == 128) {
-    size_t smem = FwdLayout<128>::kEnd + 1024 + extra;
+  auto go = [&](auto kernel, size_t tiles) -> int {
+    const size_t smem = tiles + 1024 + extra;
     if (smem > 227 * 1024) return VSA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(fine_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
       return VSA_ERR_CUDA;
-    fine_fwd_kernel<128><<<grid, kThreads, smem, s>>>(p);
-  } else {
-    size_t smem = FwdLayout<64>::kEnd + 1024 + extra;
-    if (smem > 227 * 1024) return VSA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(fine_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return VSA_ERR_CUDA;
-    fine_fwd_kernel<64><<<grid, kThreads, smem, s>>>(p);
-  }
+    kernel<<<grid, kThreads, smem, s>>>(p);
+    return VSA_OK;
+  };
+  if (d == 128)
+    st = f16_in ? go(fine_fwd_kernel<128, true>, FwdLayout<128>::kEnd) : go(fine_fwd_kernel<128, false>, FwdLayout<128>::kEnd);
+  else
+    st = f16_in ? go(fine_fwd_kernel<64, true>, FwdLayout<64>::kEnd) : go(fine_fwd_kernel<64, false>, FwdLayout<64>::kEnd);
+  if (st != VSA_OK) return st;
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 

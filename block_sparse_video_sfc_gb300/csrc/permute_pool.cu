@@ -14,13 +14,15 @@ namespace vsa {
 
 struct PermuteArgs {
   const __nv_bfloat16* src[3];
-  __nv_bfloat16* dst[3];
+  void* dst[3];
   float* pooled[3];
 };
 
-template <int D>
+// F16OUT: the destination holds the same values as fp16 (exact for inputs of
+// magnitude <= 65504; larger ones saturate and latch kErrRange).
+template <int D, bool F16OUT>
 __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc, int H, int W, int N,
-                                                           int inverse) {
+                                                           int inverse, int* err) {
   constexpr int kChunks = D / 8;           // 16-byte chunks per token
   constexpr int kTokPerPass = 256 / kChunks;
   constexpr int kPasses = kCube / kTokPerPass;
@@ -30,7 +32,7 @@ __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc
   const int64_t bh = cube_glob / Nc;
   const int cube = static_cast<int>(cube_glob % Nc);
   const __nv_bfloat16* src = a.src[tensor] + bh * static_cast<int64_t>(N) * D;
-  __nv_bfloat16* dst = a.dst[tensor] + bh * static_cast<int64_t>(N) * D;
+  uint16_t* dst = static_cast<uint16_t*>(a.dst[tensor]) + bh * static_cast<int64_t>(N) * D;
   float* pooled = a.pooled[tensor];
   const int j = threadIdx.x % kChunks;     // channel chunk, fixed per thread
   const int o0 = threadIdx.x / kChunks;
@@ -43,7 +45,18 @@ __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc
     const int64_t s_tok = inverse ? cub : nat;
     const int64_t d_tok = inverse ? nat : cub;
     uint4 v = *reinterpret_cast<const uint4*>(src + s_tok * D + j * 8);
-    *reinterpret_cast<uint4*>(dst + d_tok * D + j * 8) = v;
+    if (F16OUT) {
+      const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                          bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+      bool big = false;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) big |= !(fabsf(f[e]) <= kF16Max);
+      if (big) flag_error(err, kErrRange);
+      uint4 h = make_uint4(pack_f16(f[0], f[1]), pack_f16(f[2], f[3]), pack_f16(f[4], f[5]), pack_f16(f[6], f[7]));
+      *reinterpret_cast<uint4*>(dst + d_tok * D + j * 8) = h;
+    } else {
+      *reinterpret_cast<uint4*>(dst + d_tok * D + j * 8) = v;
+    }
     if (pooled) {
       acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x);
       acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
@@ -65,19 +78,27 @@ __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc
 }
 
 int launch_permute(const void* const* src, void* const* dst, float* const* pooled, int ntensors, int BH, int d,
-                   int T, int H, int W, int inverse, cudaStream_t s) {
+                   int T, int H, int W, int inverse, int f16_out, cudaStream_t s) {
   PermuteArgs a{};
   for (int i = 0; i < ntensors; ++i) {
     a.src[i] = static_cast<const __nv_bfloat16*>(src[i]);
-    a.dst[i] = static_cast<__nv_bfloat16*>(dst[i]);
+    a.dst[i] = dst[i];
     a.pooled[i] = pooled ? pooled[i] : nullptr;
   }
   const int N = T * H * W, Nc = N / kCube;
   dim3 grid(static_cast<unsigned>(static_cast<int64_t>(BH) * Nc), ntensors);
-  if (d == 128)
-    permute_pool_kernel<128><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse);
-  else
-    permute_pool_kernel<64><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse);
+  int* err = device_error_word();
+  if (d == 128) {
+    if (f16_out)
+      permute_pool_kernel<128, true><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse, err);
+    else
+      permute_pool_kernel<128, false><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse, err);
+  } else {
+    if (f16_out)
+      permute_pool_kernel<64, true><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse, err);
+    else
+      permute_pool_kernel<64, false><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse, err);
+  }
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 

@@ -87,20 +87,24 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator.
-// a_mn / b_mn select MN-major (1) or K-major (0) operands.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
+// Instruction descriptor, kind::f16, fp32 accumulator.  f16 = 1 selects
+// fp16 A and B (format 0), f16 = 0 bf16 (format 1); A and B always share one
+// type.  a_mn / b_mn select MN-major (1) or K-major (0) operands.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int a_mn, int b_mn, int f16) {
   return (1u << 4)                                   // D format: f32
-         | (1u << 7)                                 // A format: bf16
-         | (1u << 10)                                // B format: bf16
+         | ((f16 ? 0u : 1u) << 7)                    // A format
+         | ((f16 ? 0u : 1u) << 10)                   // B format
          | (static_cast<uint32_t>(a_mn) << 15)       // A major
          | (static_cast<uint32_t>(b_mn) << 16)       // B major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
+  return idesc_f32acc(M, N, a_mn, b_mn, 0);
+}
 
 // D[tmem] (+)= A[smem] * B[smem]; issued by a single thread.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"

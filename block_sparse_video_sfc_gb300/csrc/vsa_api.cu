@@ -42,7 +42,7 @@ struct FwdWs {
 FwdWs fwd_layout(const Dims& D, int K) {
   FwdWs w{};
   size_t o = 0;
-  const size_t big_bf16 = sizeof(__nv_bfloat16) * D.BH * D.N * D.d;
+  const size_t big_bf16 = sizeof(__half) * D.BH * D.N * D.d;  // fp16 copies of Q, K, V
   const size_t pooled = sizeof(float) * D.BH * D.Nc * D.d;
   w.qp = o; o += align256(big_bf16);
   w.kp = o; o += align256(big_bf16);
@@ -70,7 +70,7 @@ BwdWs bwd_layout(const Dims& D) {
   const size_t pooled = sizeof(float) * D.BH * D.Nc * D.d;
   const size_t big_f32 = sizeof(float) * D.BH * D.N * D.d;
   const int64_t nwords = (D.Nc + 31) / 32;
-  w.dof = o; o += align256(sizeof(__nv_bfloat16) * D.BH * D.N * D.d);
+  w.dof = o; o += align256(sizeof(__half) * D.BH * D.N * D.d);
   w.delta = o; o += align256(sizeof(float) * D.BH * D.N);
   w.doc = o; o += align256(pooled);
   w.P = o; o += align256(sizeof(float) * D.BH * D.Nc * D.Nc);
@@ -128,6 +128,7 @@ const char* vsa_status_string(int status) {
     case VSA_ERR_TIMEOUT: return "a kernel's bounded wait expired";
     case VSA_ERR_LUT: return "block index list entry or count out of range, or a repeated cube";
     case VSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case VSA_ERR_RANGE: return "a value exceeded the fp16 operand range (|x| > 65504) and was saturated";
     default: return "unknown status";
   }
 }
@@ -141,6 +142,7 @@ int vsa_device_status(void* stream) {
   if (v && cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return VSA_ERR_CUDA;
   if (v & kErrTimeout) return VSA_ERR_TIMEOUT;
   if (v & kErrLut) return VSA_ERR_LUT;
+  if (v & kErrRange) return VSA_ERR_RANGE;
   return VSA_OK;
 }
 
@@ -154,7 +156,7 @@ int vsa_permute(const void* x, void* y, float* pooled, int BH, int d, vsa_grid_t
   const void* src[1] = {x};
   void* dst[1] = {y};
   float* pl[1] = {pooled};
-  return launch_permute(src, dst, pl, 1, BH, d, g.T, g.H, g.W, inverse, as_stream(stream));
+  return launch_permute(src, dst, pl, 1, BH, d, g.T, g.H, g.W, inverse, 0, as_stream(stream));
 }
 
 int vsa_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk, float scale,
@@ -189,7 +191,7 @@ int vsa_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* 
   if (!o_fine || !aligned16(o_fine)) return VSA_ERR_ARG;
   if (o_dtype != VSA_DTYPE_BF16 && o_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
   return launch_fine_fwd(qp, kp, vp, kv_block_idx, valid_block_num, max_kv_blocks, BH, N, d, scale, o_fine, o_dtype,
-                         lse, as_stream(stream));
+                         lse, 0, as_stream(stream));
 }
 
 int vsa_fine_bwd(const void* qp, const void* kp, const void* vp, const void* o_fine, int o_dtype, const float* lse,
@@ -261,13 +263,13 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
   const void* src[3] = {q, k, v};
   void* dst[3] = {at<void>(ws, w.qp), at<void>(ws, w.kp), at<void>(ws, w.vp)};
   float* pooled[3] = {at<float>(ws, w.qc), at<float>(ws, w.kc), at<float>(ws, w.vc)};
-  if ((st = launch_permute(src, dst, pooled, 3, BH, d, g.T, g.H, g.W, 0, s)) != VSA_OK) return st;
+  if ((st = launch_permute(src, dst, pooled, 3, BH, d, g.T, g.H, g.W, 0, 1, s)) != VSA_OK) return st;
   if ((st = launch_coarse_topk(pooled[0], pooled[1], pooled[2], BH, Nc, d, topk, scale, at<float>(ws, w.oc),
                                at<float>(ws, w.lsec), at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), nullptr, s)) !=
       VSA_OK)
     return st;
   if ((st = launch_fine_fwd(dst[0], dst[1], dst[2], at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), topk, BH, N, d,
-                            scale, at<float>(ws, w.of), VSA_DTYPE_F32, at<float>(ws, w.lse), s)) != VSA_OK)
+                            scale, at<float>(ws, w.of), VSA_DTYPE_F32, at<float>(ws, w.lse), 1, s)) != VSA_OK)
     return st;
   return launch_combine(at<float>(ws, w.oc), at<float>(ws, w.of), g_coarse, g_fine, out, out_dtype, BH, d, g.T, g.H,
                         g.W, s);
@@ -293,7 +295,7 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
   cudaStream_t s = as_stream(stream);
   const int BH = static_cast<int>(D.BH), Nc = static_cast<int>(D.Nc), N = static_cast<int>(D.N);
   if ((st = launch_bwd_prep(dout, g_coarse, g_fine, at<float>(fwd_ws, f.oc), at<float>(fwd_ws, f.of),
-                            at<__nv_bfloat16>(ws, w.dof), at<float>(ws, w.delta), at<float>(ws, w.doc),
+                            at<__half>(ws, w.dof), at<float>(ws, w.delta), at<float>(ws, w.doc),
                             g_coarse ? dg_coarse : nullptr, g_fine ? dg_fine : nullptr, grad_dtype, BH, d, g.T, g.H,
                             g.W, s)) != VSA_OK)
     return st;

@@ -4,7 +4,7 @@
 //             Attention on AMD GPUs", "Stage 2: Fine Computation": the output
 //             combines the coarse and fine outputs through learnable gates).
 //   bwd_prep  backward of the combine: dO to cube order, dO_f = g_f * dO
-//             (bf16 for the fine backward), D = dO_f . O_f, dO_c = sum over the
+//             (fp16 for the fine backward), D = dO_f . O_f, dO_c = sum over the
 //             cube of g_c * dO, and the gate gradients.
 //   coarse backward  softmax Jacobian of the coarse stage (fp32 SIMT).
 //   finalize  mean-pool backward (+ dXc / 64 to every token of a cube) and
@@ -51,10 +51,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        const __nv_bfloat16* __restrict__ gc,
                                                        const __nv_bfloat16* __restrict__ gf,
                                                        const float* __restrict__ oc, const float* __restrict__ of,
-                                                       __nv_bfloat16* __restrict__ dof, float* __restrict__ delta,
+                                                       __half* __restrict__ dof, float* __restrict__ delta,
                                                        float* __restrict__ doc, void* __restrict__ dgc,
                                                        void* __restrict__ dgf, int grad_dtype, int Nc, int H, int W,
-                                                       int N) {
+                                                       int N, int* err) {
   constexpr int kChunks = D / 8, kTok = 256 / kChunks, kPasses = kCube / kTok;
   __shared__ float red[kTok][D];
   const int64_t cg = blockIdx.x;
@@ -76,14 +76,17 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
     uint4 packed;
     uint32_t* pk = reinterpret_cast<uint32_t*>(&packed);
     float dsum = 0.f;
+    bool big = false;
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
       const float x0 = (gf ? b[e] : 1.f) * g[e], x1 = (gf ? b[e + 1] : 1.f) * g[e + 1];
-      pk[e >> 1] = pack_bf16(x0, x1);
-      // D uses the bf16 values the fine backward multiplies with.
-      dsum = fmaf(bf16_lo(pk[e >> 1]), f[e], dsum);
-      dsum = fmaf(bf16_hi(pk[e >> 1]), f[e + 1], dsum);
+      big |= !(fabsf(x0) <= kF16Max) || !(fabsf(x1) <= kF16Max);
+      pk[e >> 1] = pack_f16(x0, x1);
+      // D uses the fp16 values the fine backward multiplies with.
+      dsum = fmaf(f16_lo(pk[e >> 1]), f[e], dsum);
+      dsum = fmaf(f16_hi(pk[e >> 1]), f[e + 1], dsum);
     }
+    if (big) flag_error(err, kErrRange);
     *reinterpret_cast<uint4*>(dof + cub * D + j * 8) = packed;
 #pragma unroll
     for (int off = kChunks / 2; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
@@ -338,7 +341,7 @@ int launch_combine(const float* oc, const float* of, const void* gc, const void*
 }
 
 int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const float* oc, const float* of,
-                    __nv_bfloat16* dof, float* delta, float* doc, void* dgc, void* dgf, int grad_dtype, int BH, int d,
+                    __half* dof, float* delta, float* doc, void* dgc, void* dgf, int grad_dtype, int BH, int d,
                     int T, int H, int W, cudaStream_t s) {
   const int N = T * H * W, Nc = N / kCube;
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(BH) * Nc);
@@ -346,9 +349,11 @@ int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const floa
   auto g = static_cast<const __nv_bfloat16*>(gc);
   auto f = static_cast<const __nv_bfloat16*>(gf);
   if (d == 128)
-    bwd_prep_kernel<128><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, H, W, N);
+    bwd_prep_kernel<128><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, H, W, N,
+                                              device_error_word());
   else
-    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, H, W, N);
+    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, H, W, N,
+                                             device_error_word());
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 

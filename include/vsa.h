@@ -35,6 +35,13 @@
  *    max_kv_blocks, a bounded wait that expired) are latched in a device-side
  *    flag: the offending entry is skipped, and vsa_device_status() reports
  *    and clears the flag.
+ *  - Precision: the pooled vectors, coarse scores and Top-K are fp32; the
+ *    fine-stage tensor-core products take 16-bit operands with fp32
+ *    accumulation.  vsa_fine_fwd uses the bf16 inputs as given.
+ *    vsa_forward / vsa_backward / vsa_fine_bwd convert Q, K, V and
+ *    dO_f = g_fine * dO to fp16 (exact for bf16 values of magnitude up to
+ *    65504; 8x finer rounding of the probabilities and of dS than bf16).  An
+ *    operand beyond 65504 is saturated and latches VSA_ERR_RANGE.
  */
 #ifndef VSA_H_
 #define VSA_H_
@@ -54,7 +61,8 @@ typedef enum {
     VSA_ERR_CUDA = -4,        /* a CUDA runtime call failed */
     VSA_ERR_TIMEOUT = -5,     /* a kernel's bounded wait expired */
     VSA_ERR_LUT = -6,         /* index list entry or count out of range */
-    VSA_ERR_WORKSPACE = -7    /* workspace missing or too small */
+    VSA_ERR_WORKSPACE = -7,   /* workspace missing or too small */
+    VSA_ERR_RANGE = -8        /* an operand exceeded the fp16 range (see below) */
 } vsa_status_t;
 
 typedef enum { VSA_DTYPE_BF16 = 0, VSA_DTYPE_F32 = 1 } vsa_dtype_t;
@@ -171,7 +179,7 @@ size_t vsa_workspace_bytes(int op, int B, int heads, int d, vsa_grid_t g, int to
 /* Device pointers into a forward workspace (the saved state), for callers
  * that want the intermediate results. */
 typedef struct {
-    void* qp;          /* bf16 [BH, N, d] cube order */
+    void* qp;          /* fp16 [BH, N, d] cube order */
     void* kp;
     void* vp;
     float* qc;         /* fp32 [BH, Nc, d] pooled */

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings(lib):
     L = lib.load()
-    for s in (0, -1, -2, -3, -4, -5, -6, -7):
+    for s in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert L.vsa_status_string(s)
     assert L.vsa_status_string(12345) == b"unknown status"
 
