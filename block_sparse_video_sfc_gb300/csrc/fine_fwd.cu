@@ -11,8 +11,8 @@
 // the UNION of their two lists, two key cubes (128 keys) per step; each half
 // of the tile masks the cubes its own list does not hold.  Per step:
 //   S  = Q K^T         tcgen05.mma, A = Q (smem), B = K (smem), D = TMEM
-//   P  = exp2(S - m)   softmax warps, one thread per row, P -> TMEM (bf16)
-//   O += P V           tcgen05.mma, A = P (TMEM), B = V (smem), D = TMEM
+//   P  = exp2(S - m)   softmax warps, one thread per row, P -> TMEM (fp16)
+//   O += P V           tcgen05.mma, A = P (TMEM), B = V (smem, fp16), D = TMEM
 // K/V tiles arrive by TMA (128-byte swizzle) through a 2-stage ring; S and P
 // are double-buffered in TMEM so S(j+1) overlaps softmax(j).  The running max
 // is only raised (and O rescaled) when a row's max grows by more than 2^8,
@@ -59,8 +59,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// F16: Q, K, V (and P) are fp16 instead of bf16; accumulation is fp32 either way.
-template <int D, bool F16>
+// F16IN: Q, K, V arrive as fp16; otherwise as bf16, and the softmax warps
+// convert each V tile to fp16 in shared memory (exact within +-65504) so that
+// P V always runs on fp16 operands (P rounded to 2^-12, not bf16's 2^-9).
+// Accumulation is fp32 either way.
+template <int D, bool F16IN>
 __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -223,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0 && steps > 0) {
-      constexpr uint32_t idesc_s = idesc_f32acc(128, 128, 0, 0, F16);
-      constexpr uint32_t idesc_pv = idesc_f32acc(128, D, 0, 1, F16);
+      constexpr uint32_t idesc_s = idesc_f32acc(128, 128, 0, 0, F16IN);
+      constexpr uint32_t idesc_pv = idesc_f32acc(128, D, 0, 1, 1);
       bool ok = mbar_wait(&bar_q, 0);
       auto issue_s = [&](int j) {
         const int s = j % kStages;
@@ -326,10 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       for (int c = 0; c < 128; c += 2) {
         const float a = (m == -INFINITY) ? 0.f : fast_exp2(sv[c] - m);
         const float b = (m == -INFINITY) ? 0.f : fast_exp2(sv[c + 1] - m);
-        const uint32_t pp = pack2<F16>(a, b);
+        const uint32_t pp = pack_f16(a, b);
         // The row sum uses the same rounded weights the PV MMA sees, so
         // O / l stays an exact convex combination of V rows.
-        rs += lo2<F16>(pp) + hi2<F16>(pp);
+        rs += f16_lo(pp) + f16_hi(pp);
         pk[c >> 1] = __uint_as_float(pp);
       }
       l += rs;
@@ -341,6 +344,22 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       const uint32_t pcol = (j & 1) ? kColP1 : kColP0;
 #pragma unroll
       for (int c = 0; c < 64; c += 16) tmem_st16(lane_addr + pcol + c, pk + c);
+      if (!F16IN) {
+        // bf16 V tile -> fp16 in place, before the PV MMA may read it.
+        const int s = j % kStages;
+        if (!mbar_wait(&bar_v[s], (j / kStages) & 1)) {
+          ok = false;
+          break;
+        }
+        uint4* vt = reinterpret_cast<uint4*>(sm + L::kV + s * L::kTile);
+        const int t128 = threadIdx.x - 64;
+        for (int e = t128; e < L::kTile / 16; e += 128) {
+          uint4 u = vt[e];
+          vt[e] = make_uint4(pack_f16(bf16_lo(u.x), bf16_hi(u.x)), pack_f16(bf16_lo(u.y), bf16_hi(u.y)),
+                             pack_f16(bf16_lo(u.z), bf16_hi(u.z)), pack_f16(bf16_lo(u.w), bf16_hi(u.w)));
+        }
+        fence_proxy_async_smem();
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar_p[j & 1]);

@@ -37,8 +37,9 @@
  *    and clears the flag.
  *  - Precision: the pooled vectors, coarse scores and Top-K are fp32; the
  *    fine-stage tensor-core products take 16-bit operands with fp32
- *    accumulation.  vsa_fine_fwd uses the bf16 inputs as given.
- *    vsa_forward / vsa_backward / vsa_fine_bwd convert Q, K, V and
+ *    accumulation.  vsa_fine_fwd multiplies Q K^T in bf16 and P V in fp16
+ *    (V converted on chip).  vsa_forward / vsa_backward / vsa_fine_bwd
+ *    convert Q, K, V and
  *    dO_f = g_fine * dO to fp16 (exact for bf16 values of magnitude up to
  *    65504; 8x finer rounding of the probabilities and of dS than bf16).  An
  *    operand beyond 65504 is saturated and latches VSA_ERR_RANGE.
