@@ -1,0 +1,362 @@
+#!/usr/bin/env python
+"""Benchmark: VSA (video sparse attention) forward + backward on GB300.
+
+One step = the whole hot path on one batch: SFC reorder + cube pool, coarse
+attention + Top-K, tcgen05 fine attention, gated combine (forward), then the
+full backward (combine backward, coarse backward, fine backward, pool backward
++ inverse reorder), through the library's C ABI (vsa_forward / vsa_backward).
+
+Metric: effective TFLOP/s = FLOPs the method needs at the given sparsity
+(fine: 4*N*64K*d forward + 10*N*64K*d backward; coarse: 4*Nc^2*d + 10*Nc^2*d,
+per batch*head) divided by the step time; reported whole-job (all ranks).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
+independent replica of the workload (heads are independent; no collective on
+the data path) and the max time over ranks is used.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "VSA fwd+bwd effective TFLOPS at 32K tokens, 70% sparsity; % of bf16 tensor peak"
+UNIT = "TFLOP/s"
+WORKLOAD = "wan1.3b"
+
+
+def step_flops(wl: synth.Workload) -> dict:
+    keys = 64 * wl.topk
+    fine_fwd = 4.0 * wl.N * keys * wl.d * wl.BH
+    fine_bwd = 10.0 * wl.N * keys * wl.d * wl.BH
+    coarse = 14.0 * wl.Nc * wl.Nc * wl.d * wl.BH
+    return dict(fine_fwd=fine_fwd, fine_bwd=fine_bwd, coarse=coarse, total=fine_fwd + fine_bwd + coarse)
+
+
+def config_of(wl: synth.Workload, parallelism: str) -> dict:
+    return {
+        "workload": (f"{wl.name}: B={wl.B}, heads={wl.heads}, d={wl.d}, grid (T,H,W)=({wl.T},{wl.H},{wl.W}) = "
+                     f"{wl.N} tokens, {wl.Nc} cubes of (4,4,4), Top-K={wl.topk} "
+                     f"({100 * wl.sparsity:.1f}% sparsity), learnable gates on"),
+        "global_batch": wl.B,
+        "seq_len": wl.N,
+        "heads": wl.heads,
+        "head_dim": wl.d,
+        "topk": wl.topk,
+        "parallelism": parallelism,
+        "l2": "inputs larger than L2: 6 bf16 tensors of 100.7 MB per step (Q,K,V,gates,dO)",
+        "inputs": "synthetic smooth field + noise (synth.py), seed base 20250519",
+        "out_dtype": "bf16", "grad_dtype": "bf16",
+    }
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(tflops=p.get("bf16_tflops_sustained") or p["bf16_tflops"], tflops_burst=p["bf16_tflops"],
+                    hbm=p["hbm_gbs"], source="measured (MEASURED_PEAKS.json)")
+    return dict(tflops=1700.0, tflops_burst=1900.0, hbm=6800.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+def oracle_sample(wl: synth.Workload, budget_s: float, rows_hint: int = 0):
+    """Time the CPU oracle on head 0: the coarse stage in full plus the fine
+    forward and the fine backward (dQ) of a subset of query rows.  Returns
+    (effective FLOPs done, seconds, rows, threads)."""
+    import oracle
+    oracle.build()
+    q, k, v = (a.reshape(1, wl.N, wl.d) for a in synth.make_qkv(wl, heads_subset=[0]))
+    dout = synth.make_dout(wl, heads_subset=[0]).reshape(1, wl.N, wl.d)
+    scale = wl.d ** -0.5
+    rng = np.random.default_rng(7)
+
+    def run(rows: int):
+        t0 = time.perf_counter()
+        qp, kp, vp, dp = (oracle.permute(a, wl.T, wl.H, wl.W) for a in (q, k, v, dout))
+        pq, pk, pv = (oracle.pool(a) for a in (qp, kp, vp))
+        scores, _, _ = oracle.coarse(pq, pk, pv, scale)
+        idx = oracle.topk(scores, wl.topk)
+        cnt = np.full(idx.shape[:-1], wl.topk, np.int32)
+        sel = np.sort(rng.choice(wl.N, rows, replace=False))
+        oracle.fine_fwd_rows(qp, kp, vp, idx, cnt, scale, sel)
+        oracle.fine_bwd_query_rows(qp, kp, vp, dp, idx, cnt, scale, sel)
+        dt = time.perf_counter() - t0
+        # per row: forward 4*64K*d; backward recompute of S, dP and dQ 6*64K*d
+        flops = rows * 10.0 * 64 * wl.topk * wl.d + 4.0 * wl.Nc * wl.Nc * wl.d
+        return flops, dt
+
+    if rows_hint <= 0:
+        f0, t0 = run(128)
+        per_row = max(t0, 1e-3) / 128
+        rows_hint = int(min(wl.N, max(64, budget_s / per_row)))
+    flops, dt = run(rows_hint)
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return flops, dt, rows_hint, threads
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_ours(args, rank: int, world: int):
+    import torch
+    import block_sparse_video_sfc_gb300 as vsa
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = synth.WORKLOADS[args.config]
+    fl = step_flops(wl)
+
+    q, k, v = synth.make_qkv(wl)
+    gc, gf = synth.make_gates(wl)
+    dout = synth.make_dout(wl)
+    host = [torch.from_numpy(a).to(torch.bfloat16).pin_memory() for a in (q, k, v, gc, gf, dout)]
+    dq_, dk_, dv_, dgc_, dgf_, ddo = (h.to(dev) for h in host)
+    out = torch.empty_like(dq_)
+    grads = dict(dq=torch.empty_like(dq_), dk=torch.empty_like(dq_), dv=torch.empty_like(dq_),
+                 dgc=torch.empty_like(dq_), dgf=torch.empty_like(dq_))
+    fws = torch.empty(vsa.workspace_bytes(0, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk),
+                      dtype=torch.uint8, device=dev)
+    bws = torch.empty(vsa.workspace_bytes(1, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk),
+                      dtype=torch.uint8, device=dev)
+
+    def step(qd, kd, vd, gcd, gfd, dod):
+        _, st = vsa.forward(qd, kd, vd, wl.T, wl.H, wl.W, wl.topk, g_coarse=gcd, g_fine=gfd, out=out, ws=fws)
+        vsa.backward(st, dod, g_coarse=gcd, g_fine=gfd, grads=grads, ws=bws)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step(dq_, dk_, dv_, dgc_, dgf_, ddo)
+    torch.cuda.synchronize()
+    assert vsa.device_status() == 0, "device error flag set during warm-up"
+    vsa.timing_read()
+
+    # ---- timed region: inputs resident in HBM
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    vsa.timing_enable(True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(dq_, dk_, dv_, dgc_, dgf_, ddo)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    vsa.timing_enable(False)
+    ms = e0.elapsed_time(e1)
+    kern = vsa.timing_read()
+    status = vsa.device_status()
+    assert status == 0, f"device error flag {status}"
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_out = [torch.empty(out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(6)]
+        dev_in = [dq_, dk_, dv_, dgc_, dgf_, ddo]
+        results = [out, grads["dq"], grads["dk"], grads["dv"], grads["dgc"], grads["dgf"]]
+        h2d = sum(h.numel() * h.element_size() for h in host)
+        d2h = sum(r.numel() * r.element_size() for r in results)
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            for d, h in zip(dev_in, host):
+                d.copy_(h, non_blocking=True)
+            step(*dev_in)
+            for h, r in zip(host_out, results):
+                h.copy_(r, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": round(world * fl["total"] * args.steps / (ems * 1e-3) / 1e12, 2), "unit": UNIT,
+               "ms_per_step": round(ems / args.steps, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    value = world * fl["total"] * args.steps / (ms * 1e-3) / 1e12
+    per_kernel = {n: round(t / max(c, 1), 4) for n, (t, c) in kern.items()}
+    launches = {n: c for n, (t, c) in kern.items()}
+    bwd_ms = per_kernel["fine_bwd"]
+    fwd_ms = per_kernel["fine_fwd"]
+    dominant = max(("fine_bwd", "fine_fwd"), key=lambda n: per_kernel[n])
+    dom_flops = fl[dominant] / 1.0
+    achieved = dom_flops / (per_kernel[dominant] * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get(dominant)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded smooth field + noise; Wan2.1 activations are not available)",
+        "config": config_of(wl, "replicas" if world > 1 else "single GPU"),
+        "pct_of_peak": round(100 * value / world / peaks["tflops"], 2),
+        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
+                     "peak": peaks["tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["tflops"], 4),
+                     "traffic": traffic,
+                     "peak_source": peaks["source"] + ", bf16 sustained (fp16 nominal rate = bf16)",
+                     "flops_per_launch": dom_flops},
+        "fine_fwd": {"ms": fwd_ms, "tflops": round(fl["fine_fwd"] / (fwd_ms * 1e-3) / 1e12, 2),
+                     "frac": round(fl["fine_fwd"] / (fwd_ms * 1e-3) / 1e12 / peaks["tflops"], 4)},
+        "fine_bwd": {"ms": bwd_ms, "tflops": round(fl["fine_bwd"] / (bwd_ms * 1e-3) / 1e12, 2),
+                     "frac": round(fl["fine_bwd"] / (bwd_ms * 1e-3) / 1e12 / peaks["tflops"], 4)},
+        "kernel_ms_per_step": per_kernel,
+        "gpu_launches": 11 * args.steps,
+        "kernel_launches_timed": launches,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        flops, dt, rows, threads = oracle_sample(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": (f"head 0 of {wl.heads}: coarse stage in full, fine forward and fine backward (dQ) of "
+                       f"{rows} random query rows; {dt:.1f} s; FLOPs counted per row 10*64K*d")}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.config]
+    budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    _, _, rows, threads = oracle_sample(wl, budget)
+    for _ in range(args.warmup):
+        oracle_sample(wl, budget, rows_hint=rows)
+    tot_f, tot_t = 0.0, 0.0
+    for _ in range(args.steps):
+        f, t, _, _ = oracle_sample(wl, budget, rows_hint=rows)
+        tot_f += f
+        tot_t += t
+    value = tot_f / tot_t / 1e12
+    sample = (f"per step: head 0 of {wl.heads}, coarse stage in full + fine forward and backward (dQ) of {rows} "
+              f"query rows on the CPU oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded smooth field + noise)", "config": config_of(wl, "single process, host cores"),
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

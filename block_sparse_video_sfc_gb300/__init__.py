@@ -18,7 +18,8 @@ from . import _lib
 from ._lib import Grid, VSAError, VSA_DTYPE_BF16, VSA_DTYPE_F32
 
 __all__ = ["permute", "coarse_topk", "fine_fwd", "fine_bwd", "forward", "backward",
-           "workspace_bytes", "device_status", "VSAError", "ForwardState", "Grid"]
+           "workspace_bytes", "device_status", "timing_enable", "timing_read", "VSAError",
+           "ForwardState", "Grid"]
 
 _DT = {torch.bfloat16: VSA_DTYPE_BF16, torch.float32: VSA_DTYPE_F32}
 
@@ -186,6 +187,21 @@ def backward(state: ForwardState, dout, g_coarse=None, g_fine=None, grad_dtype=t
         _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads.get("dgc")), _ptr(grads.get("dgf")), _DT[dt],
         _ptr(ws), nbytes, _stream()))
     return grads
+
+
+def timing_enable(on: bool = True) -> None:
+    """Bracket each main-kernel launch with CUDA events (vsa_timing_enable)."""
+    _lib.check("vsa_timing_enable", _lib.load().vsa_timing_enable(int(on)))
+
+
+def timing_read() -> dict:
+    """{kernel: (total_ms, launches)} since the last read (vsa_timing_read)."""
+    out = {}
+    for i, name in enumerate(_lib.KERNELS):
+        ms, n = ctypes.c_double(), ctypes.c_int()
+        _lib.check("vsa_timing_read", _lib.load().vsa_timing_read(i, ctypes.byref(ms), ctypes.byref(n)))
+        out[name] = (ms.value, n.value)
+    return out
 
 
 def device_status() -> int:

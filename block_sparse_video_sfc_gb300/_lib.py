@@ -63,7 +63,11 @@ SIGNATURES = {
     "vsa_forward_saved": ([P, I, I, I, Grid, I, ctypes.POINTER(Saved)], I),
     "vsa_device_status": ([P], I),
     "vsa_status_string": ([I], ctypes.c_char_p),
+    "vsa_timing_enable": ([I], I),
+    "vsa_timing_read": ([I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I)], I),
 }
+
+KERNELS = ["permute", "coarse_topk", "fine_fwd", "combine", "bwd_prep", "coarse_bwd", "fine_bwd", "finalize"]
 
 _lib = None
 

@@ -262,6 +262,7 @@ int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH
   size_t smem = CoarseSmem{R, Kpad, d, Nc}.total();
   if (smem > kMaxSmem) return VSA_ERR_UNSUPPORTED;
   dim3 grid((Nc + R - 1) / R, BH);
+  timing_mark(VSA_K_COARSE, true, s);
   if (d == 128) {
     auto k = coarse_topk_kernel<128>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
@@ -273,6 +274,7 @@ int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH
       return VSA_ERR_CUDA;
     k<<<grid, kThreads, smem, s>>>(qc, kc, vc, Nc, topk, R, Kpad, scale, oc, lse_c, idx, cnt, scores);
   }
+  timing_mark(VSA_K_COARSE, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 

@@ -92,6 +92,8 @@ __device__ __forceinline__ void load8(const void* base, int64_t elem, int dtype,
 
 // ---------------------------------------------------------------- host side
 int* device_error_word();          // per-device error word (vsa_api.cu)
+// Kernel timing hooks (vsa_timing_enable): no-ops unless enabled.
+void timing_mark(int kernel, bool begin, cudaStream_t s);
 int num_sms();                     // SM count of the current device
 
 int launch_permute(const void* const* src, void* const* dst, float* const* pooled, int ntensors, int BH,

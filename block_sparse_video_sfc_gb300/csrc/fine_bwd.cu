@@ -468,14 +468,18 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
     if (cudaFuncSetAttribute(fine_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return VSA_ERR_CUDA;
+    timing_mark(VSA_K_FINE_BWD, true, s);
     fine_bwd_kernel<128><<<grid, kThreads, smem, s>>>(p);
+    timing_mark(VSA_K_FINE_BWD, false, s);
   } else {
     size_t smem = BwdLayout<64>::kEnd + 1024 + extra;
     if (smem > 227 * 1024) return VSA_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(fine_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return VSA_ERR_CUDA;
+    timing_mark(VSA_K_FINE_BWD, true, s);
     fine_bwd_kernel<64><<<grid, kThreads, smem, s>>>(p);
+    timing_mark(VSA_K_FINE_BWD, false, s);
   }
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }

@@ -457,7 +457,9 @@ int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       return VSA_ERR_CUDA;
+    timing_mark(VSA_K_FINE_FWD, true, s);
     kernel<<<grid, kThreads, smem, s>>>(p);
+    timing_mark(VSA_K_FINE_FWD, false, s);
     return VSA_OK;
   };
   if (d == 128)

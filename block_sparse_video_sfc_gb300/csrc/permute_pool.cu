@@ -88,6 +88,7 @@ int launch_permute(const void* const* src, void* const* dst, float* const* poole
   const int N = T * H * W, Nc = N / kCube;
   dim3 grid(static_cast<unsigned>(static_cast<int64_t>(BH) * Nc), ntensors);
   int* err = device_error_word();
+  timing_mark(VSA_K_PERMUTE, true, s);
   if (d == 128) {
     if (f16_out)
       permute_pool_kernel<128, true><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse, err);
@@ -99,6 +100,7 @@ int launch_permute(const void* const* src, void* const* dst, float* const* poole
     else
       permute_pool_kernel<64, false><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse, err);
   }
+  timing_mark(VSA_K_PERMUTE, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 

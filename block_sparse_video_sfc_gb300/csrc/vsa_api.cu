@@ -2,6 +2,7 @@
 // workspace layouts, and the order in which the kernels run.  Nothing here
 // allocates memory; every buffer belongs to the caller.
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -91,7 +92,40 @@ T* at(const void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(const_cast<void*>(base)) + off);
 }
 
+struct TimedLaunch {
+  cudaEvent_t start, stop;
+};
+bool g_timing = false;
+std::vector<TimedLaunch> g_timed[VSA_K_COUNT];
+std::vector<cudaEvent_t> g_event_pool;
+cudaEvent_t pooled_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
 }  // namespace
+
+void timing_mark(int kernel, bool begin, cudaStream_t s) {
+  if (!g_timing || kernel < 0 || kernel >= VSA_K_COUNT) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (begin) {
+    cudaEvent_t e = pooled_event();
+    if (!e) return;
+    cudaEventRecord(e, s);
+    g_timed[kernel].push_back(TimedLaunch{e, nullptr});
+  } else if (!g_timed[kernel].empty() && !g_timed[kernel].back().stop) {
+    cudaEvent_t e = pooled_event();
+    if (!e) return;
+    cudaEventRecord(e, s);
+    g_timed[kernel].back().stop = e;
+  }
+}
 
 int* device_error_word() {
   int dev = 0;
@@ -131,6 +165,34 @@ const char* vsa_status_string(int status) {
     case VSA_ERR_RANGE: return "a value exceeded the fp16 operand range (|x| > 65504) and was saturated";
     default: return "unknown status";
   }
+}
+
+int vsa_timing_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_timing = on != 0;
+  return VSA_OK;
+}
+
+int vsa_timing_read(int kernel, double* total_ms, int* launches) {
+  if (kernel < 0 || kernel >= VSA_K_COUNT || !total_ms || !launches) return VSA_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  double sum = 0.0;
+  int n = 0, st = VSA_OK;
+  for (auto& t : g_timed[kernel]) {
+    if (t.stop) {
+      float ms = 0.f;
+      if (cudaEventSynchronize(t.stop) != cudaSuccess || cudaEventElapsedTime(&ms, t.start, t.stop) != cudaSuccess)
+        st = VSA_ERR_CUDA;
+      sum += ms;
+      ++n;
+      g_event_pool.push_back(t.stop);
+    }
+    g_event_pool.push_back(t.start);
+  }
+  g_timed[kernel].clear();
+  *total_ms = sum;
+  *launches = n;
+  return st;
 }
 
 int vsa_device_status(void* stream) {

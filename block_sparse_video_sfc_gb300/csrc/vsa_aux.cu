@@ -333,10 +333,12 @@ int launch_combine(const float* oc, const float* of, const void* gc, const void*
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(BH) * Nc);
   auto g = static_cast<const __nv_bfloat16*>(gc);
   auto f = static_cast<const __nv_bfloat16*>(gf);
+  timing_mark(VSA_K_COMBINE, true, s);
   if (d == 128)
     combine_kernel<128><<<grid, 256, 0, s>>>(oc, of, g, f, out, out_dtype, Nc, H, W, N);
   else
     combine_kernel<64><<<grid, 256, 0, s>>>(oc, of, g, f, out, out_dtype, Nc, H, W, N);
+  timing_mark(VSA_K_COMBINE, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
@@ -348,12 +350,14 @@ int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const floa
   auto dO = static_cast<const __nv_bfloat16*>(dout);
   auto g = static_cast<const __nv_bfloat16*>(gc);
   auto f = static_cast<const __nv_bfloat16*>(gf);
+  timing_mark(VSA_K_BWD_PREP, true, s);
   if (d == 128)
     bwd_prep_kernel<128><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, H, W, N,
                                               device_error_word());
   else
     bwd_prep_kernel<64><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, H, W, N,
                                              device_error_word());
+  timing_mark(VSA_K_BWD_PREP, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
@@ -370,6 +374,7 @@ int launch_coarse_bwd(const float* qc, const float* kc, const float* vc, const f
   if (smem > 200 * 1024) return VSA_ERR_UNSUPPORTED;
   dim3 grid((Nc + R - 1) / R, BH);
   dim3 g2((Nc + 31) / 32, BH);
+  timing_mark(VSA_K_COARSE_BWD, true, s);
   if (d == 128) {
     if (cudaFuncSetAttribute(coarse_bwd_rows<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
@@ -385,6 +390,7 @@ int launch_coarse_bwd(const float* qc, const float* kc, const float* vc, const f
     coarse_atb<64><<<g2, 256, 0, s>>>(dS, qc, Nc, scale, dkc);
     coarse_atb<64><<<g2, 256, 0, s>>>(P, doc, Nc, 1.0f, dvc);
   }
+  timing_mark(VSA_K_COARSE_BWD, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
@@ -394,10 +400,12 @@ int launch_finalize(const float* dqp, const float* dkp, const float* dvp, const 
   const int N = T * H * W, Nc = N / kCube;
   FinalizeArgs a{{dqp, dkp, dvp}, {dqc, dkc, dvc}, {dq, dk, dv}};
   dim3 grid(static_cast<unsigned>(static_cast<int64_t>(BH) * Nc), 3);
+  timing_mark(VSA_K_FINALIZE, true, s);
   if (d == 128)
     finalize_kernel<128><<<grid, 256, 0, s>>>(a, grad_dtype, Nc, H, W, N);
   else
     finalize_kernel<64><<<grid, 256, 0, s>>>(a, grad_dtype, Nc, H, W, N);
+  timing_mark(VSA_K_FINALIZE, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 

@@ -196,6 +196,27 @@ typedef struct {
 
 int vsa_forward_saved(const void* fwd_ws, int B, int heads, int d, vsa_grid_t g, int topk, vsa_saved_t* out);
 
+/*
+ * Kernel timing (instrumentation, off by default).  While enabled, every
+ * launch of the kernels below is bracketed by a pair of CUDA events recorded
+ * on the stream the kernel is launched on.  vsa_timing_read waits for the
+ * recorded events of one kernel, returns the summed elapsed milliseconds and
+ * the number of launches since the last read, and forgets them.
+ */
+enum {
+    VSA_K_PERMUTE = 0,     /* reorder + pool (vsa_permute, vsa_forward) */
+    VSA_K_COARSE = 1,      /* coarse attention + Top-K */
+    VSA_K_FINE_FWD = 2,    /* tcgen05 fine forward */
+    VSA_K_COMBINE = 3,     /* gated combine + inverse reorder */
+    VSA_K_BWD_PREP = 4,    /* backward of the combine */
+    VSA_K_COARSE_BWD = 5,  /* coarse backward (three kernels) */
+    VSA_K_FINE_BWD = 6,    /* tcgen05 fine backward */
+    VSA_K_FINALIZE = 7,    /* pool backward + inverse reorder */
+    VSA_K_COUNT = 8
+};
+int vsa_timing_enable(int on);
+int vsa_timing_read(int kernel, double* total_ms, int* launches);
+
 /* Waits for `stream`, then returns and clears the device-side error flag:
  * VSA_OK, VSA_ERR_LUT or VSA_ERR_TIMEOUT (or VSA_ERR_CUDA). */
 int vsa_device_status(void* stream);
