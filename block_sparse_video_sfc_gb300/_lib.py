@@ -57,6 +57,7 @@ SIGNATURES = {
     "vsa_coarse_topk": ([P, P, P, I, I, I, I, F, P, P, P, P, P, P], I),
     "vsa_fine_fwd": ([P, P, P, P, P, I, I, I, I, F, P, I, P, P], I),
     "vsa_fine_bwd": ([P, P, P, P, I, P, P, P, P, I, I, I, I, F, P, P, P, P, SZ, P], I),
+    "vsa_fine_bwd_noalloc": ([P, P, P, P, I, P, P, P, P, I, I, I, I, F, P, P, P, P], I),
     "vsa_forward": ([P, P, P, P, P, I, I, I, Grid, I, F, P, I, P, SZ, P], I),
     "vsa_backward": ([P, P, P, P, I, I, I, Grid, I, F, P, P, P, P, P, I, P, SZ, P], I),
     "vsa_workspace_bytes": ([I, I, I, I, Grid, I], SZ),

@@ -139,6 +139,34 @@ int vsa_fine_bwd(const void* qp, const void* kp, const void* vp, const void* o_f
                  float* dq, float* dk, float* dv, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * vsa_fine_bwd_noalloc -- vsa_fine_bwd without a caller workspace.  The
+ * pages have no counterpart of this call; it exists for callers that cannot
+ * give the library scratch memory: code inside a runtime or framework that
+ * hands out device memory only through its own pool (or allows no new
+ * allocations once running), and plain C callers that hold the inputs and
+ * outputs but no allocator for a workspace.
+ *   Arguments and results are those of vsa_fine_bwd, minus ws / ws_bytes.
+ *   Scratch: a fixed device array of VSA_NOALLOC_SCRATCH_BYTES inside the
+ *   library (held by every GPU that loads the library, until exit).  Problems
+ *   whose vsa_fine_bwd workspace exceeds it are rejected with
+ *   VSA_ERR_WORKSPACE before anything is enqueued: the limit is about
+ *   BH * N <= 65000 query rows (for example 12 heads of 4096 tokens); use
+ *   vsa_fine_bwd beyond it.
+ *   The call allocates nothing.  Its first call on a device looks up the
+ *   array's device address (cudaGetSymbolAddress) with that device current;
+ *   make that first call before any stream capture.  All calls share the one
+ *   array and leave their contents in it (the parts that must start at zero
+ *   are cleared on the stream by each call): calls whose GPU work overlaps
+ *   -- on different streams, or from different threads -- race with each
+ *   other, so serialise them.
+ */
+#define VSA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int vsa_fine_bwd_noalloc(const void* qp, const void* kp, const void* vp, const void* o_fine, int o_dtype,
+                         const float* lse, const void* do_fine, const int32_t* kv_block_idx,
+                         const int32_t* valid_block_num, int max_kv_blocks, int BH, int N, int d, float scale,
+                         float* dq, float* dk, float* dv, void* stream);
+
+/*
  * vsa_forward -- the whole VSA forward pass: reorder + pool, coarse attention
  * + Top-K, fine block-sparse attention, gated combination, inverse reorder.
  * [AMD] "Two-Stage Architecture" end to end; the gated combination of the
