@@ -84,7 +84,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
   uint32_t* bitA = ulist + 2 * p.Nc + 2;
   uint32_t* bitB = bitA + p.nwords;
 
-  __shared__ uint64_t bar_kv, bar_load, bar_mma1, bar_ds, bar_mma2, bar_dqr;
+  // Per-step barriers (each completes once per step): Q(j) / dO(j) loaded;
+  // S^T, dP^T done (mma1); P^T, dS^T written (ds, 128 threads); dV done (dO
+  // free); dK done (Q free); dQ^T done (mma2); dQ^T read out (dqr, 128).
+  __shared__ uint64_t bar_kv, bar_qld, bar_dold, bar_mma1, bar_ds, bar_dofree, bar_qfree, bar_mma2, bar_dqr;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int n_union;
 
@@ -97,7 +100,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
 
   if (tid == 0) {
     mbar_init(&bar_kv, 1);
-    mbar_init(&bar_load, 1);
+    mbar_init(&bar_qld, 1);
+    mbar_init(&bar_dold, 1);
+    mbar_init(&bar_dofree, 1);
+    mbar_init(&bar_qfree, 1);
     mbar_init(&bar_mma1, 1);
     mbar_init(&bar_ds, 128);
     mbar_init(&bar_mma2, 1);
@@ -161,18 +167,26 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
         tma_load_2d(sm + L::kV + b * 16384 + 8192, &p.tv, &bar_kv, 64 * b, static_cast<int>(row_base + 64 * c1));
       }
       for (int j = 0; j < steps; ++j) {
-        if (j > 0 && !mbar_wait(&bar_mma2, (j - 1) & 1)) {
+        const int q0 = ulist[2 * j] & 0x3FFFFFFF;
+        const int q1 = (2 * j + 1 < U) ? (ulist[2 * j + 1] & 0x3FFFFFFF) : q0;
+        // dO(j) replaces dO(j-1) once dV(j-1) is done; Q(j) once dK(j-1) is.
+        if (j > 0 && !mbar_wait(&bar_dofree, (j - 1) & 1)) {
           flag_error(p.err, kErrTimeout);
           break;
         }
-        const int q0 = ulist[2 * j] & 0x3FFFFFFF;
-        const int q1 = (2 * j + 1 < U) ? (ulist[2 * j + 1] & 0x3FFFFFFF) : q0;
-        mbar_expect_tx(&bar_load, 2 * L::kTile);
+        mbar_expect_tx(&bar_dold, L::kTile);
         for (int b = 0; b < D / 64; ++b) {
-          tma_load_2d(sm + L::kQ + b * 16384, &p.tq, &bar_load, 64 * b, static_cast<int>(row_base + 64 * q0));
-          tma_load_2d(sm + L::kQ + b * 16384 + 8192, &p.tq, &bar_load, 64 * b, static_cast<int>(row_base + 64 * q1));
-          tma_load_2d(sm + L::kDO + b * 16384, &p.tdo, &bar_load, 64 * b, static_cast<int>(row_base + 64 * q0));
-          tma_load_2d(sm + L::kDO + b * 16384 + 8192, &p.tdo, &bar_load, 64 * b, static_cast<int>(row_base + 64 * q1));
+          tma_load_2d(sm + L::kDO + b * 16384, &p.tdo, &bar_dold, 64 * b, static_cast<int>(row_base + 64 * q0));
+          tma_load_2d(sm + L::kDO + b * 16384 + 8192, &p.tdo, &bar_dold, 64 * b, static_cast<int>(row_base + 64 * q1));
+        }
+        if (j > 0 && !mbar_wait(&bar_qfree, (j - 1) & 1)) {
+          flag_error(p.err, kErrTimeout);
+          break;
+        }
+        mbar_expect_tx(&bar_qld, L::kTile);
+        for (int b = 0; b < D / 64; ++b) {
+          tma_load_2d(sm + L::kQ + b * 16384, &p.tq, &bar_qld, 64 * b, static_cast<int>(row_base + 64 * q0));
+          tma_load_2d(sm + L::kQ + b * 16384 + 8192, &p.tq, &bar_qld, 64 * b, static_cast<int>(row_base + 64 * q1));
         }
       }
     }
@@ -185,8 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
       constexpr uint32_t lbo_kt = D == 128 ? 16384u : static_cast<uint32_t>(L::kZero - L::kK);
       bool ok = mbar_wait(&bar_kv, 0);
       for (int j = 0; j < steps && ok; ++j) {
-        if (j > 0) ok = ok && mbar_wait(&bar_mma2, (j - 1) & 1);  // P/dS of step j-1 consumed
-        ok = ok && mbar_wait(&bar_load, j & 1);
+        if (j > 0) ok = ok && mbar_wait(&bar_qfree, (j - 1) & 1);  // P/dS of step j-1 consumed
+        ok = ok && mbar_wait(&bar_qld, j & 1);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -196,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
                       sdesc_sw128(smem_u32(sm + L::kQ + b * 16384 + w * 32), 16, 1024), id_ss, kk > 0);
         }
         if (j > 0) ok = ok && mbar_wait(&bar_dqr, (j - 1) & 1);  // dQ^T of step j-1 read out
+        ok = ok && mbar_wait(&bar_dold, j & 1);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -209,13 +224,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+        for (int kk = 0; kk < 8; ++kk)
           mma_ts(tmem + kColDV, tmem + kColP + kk * 8, sdesc_sw128(smem_u32(sm + L::kDO + kk * 2048), 16384, 1024),
-                 id_ts, acc);
+                 id_ts, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar_dofree);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
           mma_ts(tmem + kColDK, tmem + kColDS + kk * 8, sdesc_sw128(smem_u32(sm + L::kQ + kk * 2048), 16384, 1024),
-                 id_ts, acc);
-        }
+                 id_ts, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar_qfree);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tmem + kColDQ, sdesc_sw128(smem_u32(sm + L::kK + kk * 2048), lbo_kt, 1024),
@@ -300,21 +317,19 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
       tc_fence_after();
       const int64_t qbase0 = row_base + 64 * static_cast<int64_t>(e0 & 0x3FFFFFFF);
       const int64_t qbase1 = row_base + 64 * static_cast<int64_t>(e1 & 0x3FFFFFFF);
+      // Read the whole dQ^T row out of TMEM first so the next step's dP^T
+      // may overwrite it while the reductions drain.
+      float qv[128];
 #pragma unroll
-      for (int c = 0; c < 128; c += 16) {
-        float qv[16];
-        tmem_ld16(lane_addr + kColDQ + c, qv);
-        tmem_wait_ld();
-        const int g = c >> 6;
-        if (r < D && (g == 0 || has1)) {
-          const int64_t qb = g ? qbase1 : qbase0;
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            atomicAdd(p.dq + (qb + ((c + i) & 63)) * D + r, qv[i] * p.scale);
-        }
-      }
+      for (int c = 0; c < 128; c += 16) tmem_ld16(lane_addr + kColDQ + c, qv + c);
+      tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bar_dqr);
+      if (r < D) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c < 64 || has1) atomicAdd(p.dq + ((c < 64 ? qbase0 : qbase1) + (c & 63)) * D + r, qv[c] * p.scale);
+      }
     }
     if (!ok) flag_error(p.err, kErrTimeout);
     // ---------------- dK, dV rows of this key pair

@@ -13,10 +13,12 @@
 //   S  = Q K^T         tcgen05.mma, A = Q (smem), B = K (smem), D = TMEM
 //   P  = exp2(S - m)   softmax warps, one thread per row, P -> TMEM (fp16)
 //   O += P V           tcgen05.mma, A = P (TMEM), B = V (smem, fp16), D = TMEM
-// K/V tiles arrive by TMA (128-byte swizzle) through a 2-stage ring; S and P
-// are double-buffered in TMEM so S(j+1) overlaps softmax(j).  The running max
-// is only raised (and O rescaled) when a row's max grows by more than 2^8,
-// so P <= 256 and the fp32 accumulators stay exact enough.
+// K/V tiles arrive by TMA (128-byte swizzle), one K and one V stage; K(j+1)
+// streams in while softmax(j) and PV(j) run.  Each CTA uses 256 TMEM columns
+// (S, with P written over it, and O) and ~100 KB of shared memory, so two
+// CTAs share an SM and hide each other's latencies.  The running max is only
+// raised (and O rescaled) when a row's max grows by more than 2^8, so P <= 256
+// and the fp32 accumulators stay exact enough.
 // Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 softmax/epilogue.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -28,9 +30,9 @@ namespace vsa {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kStages = 2;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColP0 = 256, kColP1 = 320, kColO = 384;
+constexpr uint32_t kTmemCols = 256;        // two CTAs share an SM's 512 columns
+constexpr uint32_t kColS = 0, kColP = 0, kColO = 128;  // P (fp16) overwrites S
 
 struct FwdParams {
   CUtensorMap tq, tk, tv;  // [BH*N, d] bf16, box {64, 64}, 128B swizzle
@@ -49,8 +51,8 @@ struct FwdLayout {
   static constexpr int kTile = 128 * D * 2;  // 128 rows x D bf16
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTile;
-  static constexpr int kV = kK + kStages * kTile;
-  static constexpr int kEnd = kV + kStages * kTile;
+  static constexpr int kV = kK + kTile;
+  static constexpr int kEnd = kV + kTile;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -64,7 +66,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // P V always runs on fp16 operands (P rounded to 2^-12, not bf16's 2^-9).
 // Accumulation is fp32 either way.
 template <int D, bool F16IN>
-__global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kThreads, 2) fine_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using L = FwdLayout<D>;
@@ -73,11 +75,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
   uint32_t* bitA = ulist + 2 * p.kmax + 2;
   uint32_t* bitB = bitA + nwords;
 
-  __shared__ uint64_t bar_q, bar_k[kStages], bar_v[kStages], bar_empty[kStages];
-  __shared__ uint64_t bar_s[2], bar_p[2], bar_pv[2];  // bar_pv[b]: PV of steps b, b+2, ... done
+  // Each barrier completes once per step (bar_q once): K(j) / V(j) loaded,
+  // S(j) done, P(j) written (128 softmax threads), PV(j) done.
+  __shared__ uint64_t bar_q, bar_k, bar_v, bar_s, bar_p, bar_pv;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int n_union, n_cnt[2];
-  __shared__ int failed;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pair = blockIdx.x;
@@ -88,21 +90,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
   // ---------------- prologue: barriers, TMEM, union of the two index lists
   if (tid == 0) {
     mbar_init(&bar_q, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar_k[s], 1);
-      mbar_init(&bar_v[s], 1);
-      mbar_init(&bar_empty[s], 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_s[s], 1);
-      mbar_init(&bar_p[s], 128);
-      mbar_init(&bar_pv[s], 1);
-    }
+    mbar_init(&bar_k, 1);
+    mbar_init(&bar_v, 1);
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_p, 128);
+    mbar_init(&bar_pv, 1);
     fence_mbar_init();
-    failed = 0;
   }
   if (warp == 0) {
-    tmem_alloc(&tmem_base_sh, 512);
+    tmem_alloc(&tmem_base_sh, kTmemCols);
     tmem_relinquish();
   }
   for (int w = tid; w < 2 * nwords; w += kThreads) bitA[w] = 0;  // bitA and bitB are contiguous
@@ -188,7 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
   const int64_t row_base = bh * p.N;  // first row of this head in the 2D tensor maps
 
   if (warp == 0) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer: one K stage and one V stage.  K(j) may be
+    // loaded once S(j-1) is done with K(j-1); V(j) once PV(j-1) is done.
     if (lane == 0 && steps > 0) {
       tma_prefetch_desc(&p.tq);
       tma_prefetch_desc(&p.tk);
@@ -199,78 +196,67 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
           tma_load_2d(sm + L::kQ + b * 16384 + h * 8192, &p.tq, &bar_q, 64 * b,
                       static_cast<int>(row_base + 128 * pair + 64 * h));
       for (int j = 0; j < steps; ++j) {
-        const int s = j % kStages;
-        if (j >= kStages && !mbar_wait(&bar_empty[s], ((j / kStages) - 1) & 1)) {
-          flag_error(p.err, kErrTimeout);
-          atomicExch(&failed, 1);
-          break;
-        }
         const int c0 = ulist[2 * j] & 0x3FFFFFFF;
         const int c1 = (2 * j + 1 < U) ? (ulist[2 * j + 1] & 0x3FFFFFFF) : c0;
-        mbar_expect_tx(&bar_k[s], L::kTile);
-        for (int b = 0; b < D / 64; ++b) {
-          tma_load_2d(sm + L::kK + s * L::kTile + b * 16384, &p.tk, &bar_k[s], 64 * b,
-                      static_cast<int>(row_base + 64 * c0));
-          tma_load_2d(sm + L::kK + s * L::kTile + b * 16384 + 8192, &p.tk, &bar_k[s], 64 * b,
-                      static_cast<int>(row_base + 64 * c1));
+        if (j > 0 && !mbar_wait(&bar_s, (j - 1) & 1)) {
+          flag_error(p.err, kErrTimeout);
+          break;
         }
-        mbar_expect_tx(&bar_v[s], L::kTile);
+        mbar_expect_tx(&bar_k, L::kTile);
         for (int b = 0; b < D / 64; ++b) {
-          tma_load_2d(sm + L::kV + s * L::kTile + b * 16384, &p.tv, &bar_v[s], 64 * b,
-                      static_cast<int>(row_base + 64 * c0));
-          tma_load_2d(sm + L::kV + s * L::kTile + b * 16384 + 8192, &p.tv, &bar_v[s], 64 * b,
-                      static_cast<int>(row_base + 64 * c1));
+          tma_load_2d(sm + L::kK + b * 16384, &p.tk, &bar_k, 64 * b, static_cast<int>(row_base + 64 * c0));
+          tma_load_2d(sm + L::kK + b * 16384 + 8192, &p.tk, &bar_k, 64 * b, static_cast<int>(row_base + 64 * c1));
+        }
+        if (j > 0 && !mbar_wait(&bar_pv, (j - 1) & 1)) {
+          flag_error(p.err, kErrTimeout);
+          break;
+        }
+        mbar_expect_tx(&bar_v, L::kTile);
+        for (int b = 0; b < D / 64; ++b) {
+          tma_load_2d(sm + L::kV + b * 16384, &p.tv, &bar_v, 64 * b, static_cast<int>(row_base + 64 * c0));
+          tma_load_2d(sm + L::kV + b * 16384 + 8192, &p.tv, &bar_v, 64 * b, static_cast<int>(row_base + 64 * c1));
         }
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer.  S and P share TMEM columns [0, 128): S(j)
+    // is issued only after PV(j-1) has read P(j-1).
     if (lane == 0 && steps > 0) {
       constexpr uint32_t idesc_s = idesc_f32acc(128, 128, 0, 0, F16IN);
       constexpr uint32_t idesc_pv = idesc_f32acc(128, D, 0, 1, 1);
       bool ok = mbar_wait(&bar_q, 0);
-      auto issue_s = [&](int j) {
-        const int s = j % kStages;
-        ok = ok && mbar_wait(&bar_k[s], (j / kStages) & 1);
-        if (!ok) return;
+      for (int j = 0; j < steps && ok; ++j) {
+        ok = ok && mbar_wait(&bar_k, j & 1);
+        if (j > 0) ok = ok && mbar_wait(&bar_pv, (j - 1) & 1);
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t dcol = (j & 1) ? kColS1 : kColS0;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int b = kk >> 2, w = kk & 3;
           uint64_t ad = sdesc_sw128(smem_u32(sm + L::kQ + b * 16384 + w * 32), 16, 1024);
-          uint64_t bd = sdesc_sw128(smem_u32(sm + L::kK + s * L::kTile + b * 16384 + w * 32), 16, 1024);
-          mma_ss(tmem + dcol, ad, bd, idesc_s, kk > 0);
+          uint64_t bd = sdesc_sw128(smem_u32(sm + L::kK + b * 16384 + w * 32), 16, 1024);
+          mma_ss(tmem + kColS, ad, bd, idesc_s, kk > 0);
         }
-        mma_commit(&bar_s[j & 1]);
-      };
-      issue_s(0);
-      for (int j = 0; j < steps && ok; ++j) {
-        if (j + 1 < steps) issue_s(j + 1);
-        const int s = j % kStages;
-        ok = ok && mbar_wait(&bar_p[j & 1], (j >> 1) & 1);
-        ok = ok && mbar_wait(&bar_v[s], (j / kStages) & 1);
+        mma_commit(&bar_s);
+        ok = ok && mbar_wait(&bar_p, j & 1);
+        ok = ok && mbar_wait(&bar_v, j & 1);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t pcol = (j & 1) ? kColP1 : kColP0;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          uint64_t bd = sdesc_sw128(smem_u32(sm + L::kV + s * L::kTile + kk * 2048), 16384, 1024);
+          uint64_t bd = sdesc_sw128(smem_u32(sm + L::kV + kk * 2048), 16384, 1024);
           asm volatile(
               "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem + kColO),
-              "r"(tmem + pcol + kk * 8), "l"(bd), "r"(idesc_pv), "r"(static_cast<uint32_t>(j > 0 || kk > 0)));
+              "r"(tmem + kColP + kk * 8), "l"(bd), "r"(idesc_pv), "r"(static_cast<uint32_t>(j > 0 || kk > 0)));
         }
-        mma_commit(&bar_empty[s]);
-        mma_commit(&bar_pv[j & 1]);
+        mma_commit(&bar_pv);
       }
-      if (!ok) {
-        flag_error(p.err, kErrTimeout);
-        atomicExch(&failed, 1);
-      }
+      if (!ok) flag_error(p.err, kErrTimeout);
     }
   } else {
-    // ---------------- softmax + epilogue: one thread per query row
+    // ---------------- softmax + epilogue: one thread per query row.  The two
+    // 64-column halves of S are the step's two key cubes.
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // TMEM lane == tile row
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -278,37 +264,35 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < steps; ++j) {
-      if (!mbar_wait(&bar_s[j & 1], (j >> 1) & 1)) {
+      // S(j) done implies PV(j-1) done: O may be rescaled without another wait.
+      if (!mbar_wait(&bar_s, j & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t scol = (j & 1) ? kColS1 : kColS0;
       const uint32_t e0 = ulist[2 * j];
       const uint32_t e1 = (2 * j + 1 < U) ? ulist[2 * j + 1] : 0u;
-      const bool v0 = (e0 >> my_bit) & 1u, v1 = (e1 >> my_bit) & 1u;
-      float sv[128];
-#pragma unroll
-      for (int c = 0; c < 128; c += 16) tmem_ld16(lane_addr + scol + c, sv + c);
-      tmem_wait_ld();
+      const bool vh[2] = {((e0 >> my_bit) & 1u) != 0, ((e1 >> my_bit) & 1u) != 0};
+      // pass 1: row max over the valid halves (warp-uniform loads)
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const bool valid = c < 64 ? v0 : v1;
-        sv[c] = valid ? sv[c] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, sv[c]);
+      for (int h = 0; h < 2; ++h) {
+        if (!__any_sync(0xffffffffu, vh[h])) continue;
+        float sv[64];
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) tmem_ld16(lane_addr + kColS + 64 * h + c, sv + c);
+        tmem_wait_ld();
+        if (vh[h]) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) mx = fmaxf(mx, sv[c]);
+        }
       }
+      mx *= p.scale_log2;
       // Raise the running max only when it grows by more than the threshold.
       const bool raise = mx > m + kRescaleThreshold;
       const float m_new = raise ? mx : m;
       const bool need_rescale = raise && (l > 0.f);
       if (__any_sync(0xffffffffu, need_rescale)) {
-        // O holds earlier contributions: wait for the previous PV, then scale.
-        if (!mbar_wait(&bar_pv[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
         const float alpha = need_rescale ? fast_exp2(m - m_new) : 1.0f;
 #pragma unroll
         for (int c = 0; c < D; c += 16) {
@@ -323,35 +307,44 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
         l *= alpha;
       }
       m = m_new;
+      // pass 2: P = exp2(S*scale - m) per half, packed fp16 into TMEM columns
+      // [32h, 32h + 32) (over S columns this thread has already read).
       float rs = 0.f;
-      float pk[64];
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const float a = (m == -INFINITY) ? 0.f : fast_exp2(sv[c] - m);
-        const float b = (m == -INFINITY) ? 0.f : fast_exp2(sv[c + 1] - m);
-        const uint32_t pp = pack_f16(a, b);
-        // The row sum uses the same rounded weights the PV MMA sees, so
-        // O / l stays an exact convex combination of V rows.
-        rs += f16_lo(pp) + f16_hi(pp);
-        pk[c >> 1] = __uint_as_float(pp);
+      for (int h = 0; h < 2; ++h) {
+        float pk[32];
+        const bool any = __any_sync(0xffffffffu, vh[h]);
+        if (any) {
+          float sv[64];
+#pragma unroll
+          for (int c = 0; c < 64; c += 16) tmem_ld16(lane_addr + kColS + 64 * h + c, sv + c);
+          tmem_wait_ld();
+          const bool use = vh[h] && m != -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const float a = use ? fast_exp2(fmaf(sv[c], p.scale_log2, -m)) : 0.f;
+            const float b = use ? fast_exp2(fmaf(sv[c + 1], p.scale_log2, -m)) : 0.f;
+            const uint32_t pp = pack_f16(a, b);
+            // The row sum uses the same rounded weights the PV MMA sees, so
+            // O / l stays an exact convex combination of V rows.
+            rs += f16_lo(pp) + f16_hi(pp);
+            pk[c >> 1] = __uint_as_float(pp);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) tmem_st16(lane_addr + kColP + 32 * h + c, pk + c);
       }
       l += rs;
-      // P(j) may overwrite buffer j&1 once PV(j-2), which read it, is done.
-      if (j >= 2 && !mbar_wait(&bar_pv[j & 1], ((j - 2) >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      const uint32_t pcol = (j & 1) ? kColP1 : kColP0;
-#pragma unroll
-      for (int c = 0; c < 64; c += 16) tmem_st16(lane_addr + pcol + c, pk + c);
       if (!F16IN) {
         // bf16 V tile -> fp16 in place, before the PV MMA may read it.
-        const int s = j % kStages;
-        if (!mbar_wait(&bar_v[s], (j / kStages) & 1)) {
+        if (!mbar_wait(&bar_v, j & 1)) {
           ok = false;
           break;
         }
-        uint4* vt = reinterpret_cast<uint4*>(sm + L::kV + s * L::kTile);
+        uint4* vt = reinterpret_cast<uint4*>(sm + L::kV);
         const int t128 = threadIdx.x - 64;
         for (int e = t128; e < L::kTile / 16; e += 128) {
           uint4 u = vt[e];
@@ -362,13 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bar_p[j & 1]);
+      mbar_arrive(&bar_p);
     }
-    if (ok && steps > 0 && !mbar_wait(&bar_pv[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
-    if (!ok) {
-      flag_error(p.err, kErrTimeout);
-      atomicExch(&failed, 1);
-    }
+    if (ok && steps > 0 && !mbar_wait(&bar_pv, (steps - 1) & 1)) ok = false;
+    if (!ok) flag_error(p.err, kErrTimeout);
     tc_fence_after();
     // ---------------- epilogue: O / l, LSE
     const bool row_valid = row < 64 || has_b;
@@ -394,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
   __syncthreads();
   if (warp == 0) {
     __syncwarp();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
