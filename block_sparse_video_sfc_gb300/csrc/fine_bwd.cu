@@ -4,23 +4,36 @@
 // stage of "VSA: Accelerating Video Diffusion Inference with Sparse Attention
 // on AMD GPUs" ("Stage 2: Fine Computation").  The index list is constant.
 //
-// Per query row i and listed key j (S = scale * Q K^T, P = softmax(S)):
+// Per query row i and listed key j (S = scale * Q K^T, P = softmax(S) with the
+// forward's LSE, D_i = dO_i . O_i):
 //   dV_j += P_ij dO_i,  dP_ij = dO_i . V_j,  dS_ij = P_ij (dP_ij - D_i),
-//   D_i = dO_i . O_i,  dQ_i += scale dS_ij K_j,  dK_j += scale dS_ij Q_i.
+//   dQ_i += scale dS_ij K_j,  dK_j += scale dS_ij Q_i.
 //
-// GB300 mapping (key-stationary).  One CTA owns a PAIR of consecutive key
-// cubes (128 keys; their K and V stay in shared memory, dK and dV accumulate
-// in TMEM) and walks the union of the two cubes' inverse lists -- the query
-// cubes whose index list holds either key cube -- two query cubes (128 rows)
-// per step.  Quadrants (key cube, query cube) that are not in the list are
-// masked.  With keys on the MMA M dimension every product is an M = 128 MMA:
-//   S^T  = K Q^T      (SS)          dP^T = V dO^T     (SS)
-//   dV  += P^T dO     (A = P^T in TMEM)
-//   dK  += dS^T Q     (A = dS^T in TMEM)
-//   dQ^T = K^T dS^T   (SS; dS^T also staged in shared memory)
-// and dQ^T is added to a global fp32 dQ with warp-coalesced reductions.
-// The inverse lists come from a bit matrix inv[bh][key cube][query cube]
-// built from the index list (workspace).
+// GB300 mapping: two kernels, neither of which reduces partial sums through
+// global memory (an fp32 reduce-add into L2 runs at only ~3-4 TB/s on GB300,
+// which would bound a fused key-stationary kernel's dQ traffic).
+//
+// fine_bwd_kv_kernel (key-stationary): one CTA owns a PAIR of consecutive key
+// cubes (128 keys; K, V in shared memory; dK, dV accumulated in TMEM) and
+// walks the union of the two cubes' inverse lists (the query cubes whose index
+// list holds either key cube), two query cubes (128 rows) per step, masking
+// quadrants that are not listed.  Keys sit on the MMA M dimension:
+//   S^T = K Q^T, dP^T = V dO^T        (A, B in shared memory)
+//   dV += P^T dO, dK += dS^T Q        (A = P^T / dS^T in TMEM)
+// dV(j) is issued as soon as P^T(j) is written, before dS^T(j) exists; Q and
+// dO are double-buffered.
+//
+// fine_bwd_dq_kernel (query-stationary): one CTA owns a pair of query cubes
+// (128 rows; Q, dO in shared memory; dQ accumulated in TMEM) and walks the
+// union of their index lists two key cubes per step, like the forward:
+//   S = Q K^T, dP = dO V^T            (A, B in shared memory)
+//   dQ += dS K                        (A = dS in TMEM)
+// S is double-buffered in TMEM so P(j+1) = exp(S - LSE) is computed while
+// dQ(j) and dP(j+1) run; K, V go through a 2-stage ring.
+//
+// Operands are fp16 (exact for the bf16 inputs within +-65504), accumulation
+// fp32.  The inverse lists come from a bit matrix inv[bh][key cube][query
+// cube] built from the index list (workspace).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -28,34 +41,26 @@
 
 namespace vsa {
 
+int make_tile_map(void* map, const void* base, int64_t rows, int d, int f16);
+
 namespace {
 
-constexpr int kThreads = 192;
-constexpr uint32_t kColS = 0, kColP = 0, kColDS = 64, kColDP = 128, kColDQ = 128, kColDV = 256, kColDK = 384;
+constexpr int kThreads = 320;  // producer, MMA issuer, 2 compute warpgroups
+constexpr int kCompute = 256;
 
 struct BwdParams {
-  CUtensorMap tq, tk, tv, tdo;
-  const float* lse;    // natural-log LSE per row [BH*N]
-  const float* delta;  // D per row [BH*N]
-  const uint32_t* inv; // [BH][Nc][nwords]
-  float* dq;           // fp32 accumulator [BH*N, d] (zeroed by the launcher)
+  CUtensorMap tq, tk, tv, tdo;  // fp16 [BH*N, d], box {64, 64}, 128B swizzle
+  const float* lse;             // natural-log LSE per row [BH*N]
+  const float* delta;           // D per row [BH*N]
+  const uint32_t* inv;          // [BH][Nc][nwords]
+  const int32_t* idx;           // forward index list [BH][Nc][kmax]
+  const int32_t* cnt;           // [BH][Nc] or null (= kmax)
+  float* dq;
   float* dk;
   float* dv;
-  int N, Nc, nwords;
+  int N, Nc, nwords, kmax;
   float scale, scale_log2;
   int* err;
-};
-
-template <int D>
-struct BwdLayout {
-  static constexpr int kTile = 128 * D * 2;
-  static constexpr int kK = 0;
-  static constexpr int kV = kK + kTile;
-  static constexpr int kQ = kV + kTile;
-  static constexpr int kDO = kQ + kTile;
-  static constexpr int kDS = kDO + kTile;               // [2 query atoms][128 key rows][128 B]
-  static constexpr int kZero = kDS + 32768;             // zero atom (D = 64 only)
-  static constexpr int kEnd = kZero + (D == 64 ? 16384 : 0);
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -73,21 +78,94 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
       "r"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
+// Union of two cube bitmaps as an ascending list: entry = id | inA<<30 | inB<<31.
+// Executed by one full warp; returns the length (to every lane).
+__device__ int warp_union_list(const uint32_t* bitA, const uint32_t* bitB, int nwords, uint32_t* ulist) {
+  const int lane = threadIdx.x & 31;
+  int pos = 0;
+  for (int w0 = 0; w0 < nwords; w0 += 32) {
+    const int w = w0 + lane;
+    const uint32_t a = w < nwords ? bitA[w] : 0u, b = w < nwords ? bitB[w] : 0u;
+    uint32_t u = a | b;
+    const int n = __popc(u);
+    int incl = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int o = pos + incl - n;
+    while (u) {
+      const int bit = __ffs(u) - 1;
+      u &= u - 1;
+      ulist[o++] = static_cast<uint32_t>(w * 32 + bit) | (((a >> bit) & 1u) << 30) | (((b >> bit) & 1u) << 31);
+    }
+    pos += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return pos;
+}
+
+// Loads the two 64-row cubes c0, c1 of a [BH*N, D] tensor into a 128-row
+// 128B-swizzled tile ([D/64][128 rows][128 B]).
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_constant__ BwdParams p) {
+__device__ __forceinline__ void load_cube_pair(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int64_t row_base,
+                                               int c0, int c1) {
+#pragma unroll
+  for (int b = 0; b < D / 64; ++b) {
+    tma_load_2d(dst + b * 16384, map, bar, 64 * b, static_cast<int>(row_base + 64 * c0));
+    tma_load_2d(dst + b * 16384 + 8192, map, bar, 64 * b, static_cast<int>(row_base + 64 * c1));
+  }
+}
+
+// A x B^T over d for two 128-row K-major tiles (S = Q K^T style), D/16 MMAs.
+template <int D>
+__device__ __forceinline__ void mma_rows_x_rows(uint32_t dtm, const uint8_t* a, const uint8_t* b) {
+  constexpr uint32_t id = idesc_f32acc(128, 128, 0, 0, 1);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const int blk = kk >> 2, w = kk & 3;
+    mma_ss(dtm, sdesc_sw128(smem_u32(a + blk * 16384 + w * 32), 16, 1024),
+           sdesc_sw128(smem_u32(b + blk * 16384 + w * 32), 16, 1024), id, kk > 0);
+  }
+}
+// D(+)= A(TMEM) x B (128 rows x D, MN-major view of a row tile), 8 MMAs of
+// K = 16.  A is 128 x 128 packed fp16 held as two 64-wide K halves of 32
+// columns each, at columns atm and atm + 64 (one half per compute warpgroup).
+template <int D>
+__device__ __forceinline__ void mma_tmem_x_rows(uint32_t dtm, uint32_t atm, const uint8_t* b, bool accumulate) {
+  constexpr uint32_t id = idesc_f32acc(128, D, 0, 1, 1);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts(dtm, atm + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(smem_u32(b + kk * 2048), 16384, 1024), id,
+           (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// =============================================================== dK, dV
+template <int D>
+struct KvLayout {
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kK = 0, kV = kTile, kQ = 2 * kTile, kDO = 4 * kTile;  // Q, dO: 2 stages each
+  static constexpr int kEnd = 6 * kTile;
+};
+constexpr uint32_t kKvS = 0, kKvP = 0, kKvDP = 128, kKvDS = 128, kKvDV = 256, kKvDK = 384;
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  using L = BwdLayout<D>;
+  using L = KvLayout<D>;
   float* s_lse = reinterpret_cast<float*>(sm + L::kEnd);  // [2][128]
   float* s_del = s_lse + 256;                              // [2][128]
   uint32_t* ulist = reinterpret_cast<uint32_t*>(s_del + 256);
   uint32_t* bitA = ulist + 2 * p.Nc + 2;
   uint32_t* bitB = bitA + p.nwords;
 
-  // Per-step barriers (each completes once per step): Q(j) / dO(j) loaded;
-  // S^T, dP^T done (mma1); P^T, dS^T written (ds, 128 threads); dV done (dO
-  // free); dK done (Q free); dQ^T done (mma2); dQ^T read out (dqr, 128).
-  __shared__ uint64_t bar_kv, bar_qld, bar_dold, bar_mma1, bar_ds, bar_dofree, bar_qfree, bar_mma2, bar_dqr;
+  // bar_qld / bar_dold [s]: Q / dO stage s filled; bar_qfree / bar_dofree [s]:
+  // dK / dV of the step using stage s done.  Per step: bar_s (S^T done), bar_dp
+  // (dP^T done), bar_pds (P^T and dS^T written, all compute threads), bar_dv /
+  // bar_dk (dV / dK done).
+  __shared__ uint64_t bar_kv, bar_qld[2], bar_dold[2], bar_qfree[2], bar_dofree[2];
+  __shared__ uint64_t bar_s, bar_dp, bar_pds, bar_dv, bar_dk;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int n_union;
 
@@ -100,14 +178,17 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
 
   if (tid == 0) {
     mbar_init(&bar_kv, 1);
-    mbar_init(&bar_qld, 1);
-    mbar_init(&bar_dold, 1);
-    mbar_init(&bar_dofree, 1);
-    mbar_init(&bar_qfree, 1);
-    mbar_init(&bar_mma1, 1);
-    mbar_init(&bar_ds, 128);
-    mbar_init(&bar_mma2, 1);
-    mbar_init(&bar_dqr, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_qld[i], 1);
+      mbar_init(&bar_dold[i], 1);
+      mbar_init(&bar_qfree[i], 1);
+      mbar_init(&bar_dofree[i], 1);
+    }
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_dp, 1);
+    mbar_init(&bar_pds, kCompute);
+    mbar_init(&bar_dv, 1);
+    mbar_init(&bar_dk, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -120,33 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
       bitA[w] = ra[w];
       bitB[w] = has_k2 ? ra[p.nwords + w] : 0u;
     }
-    if (D == 64)
-      for (int e = tid; e < 16384 / 16; e += kThreads)
-        reinterpret_cast<uint4*>(sm + L::kZero)[e] = make_uint4(0, 0, 0, 0);
   }
-  fence_proxy_async_smem();
   __syncthreads();
   if (warp == 0) {
-    int pos = 0;
-    for (int w0 = 0; w0 < p.nwords; w0 += 32) {
-      int w = w0 + lane;
-      uint32_t a = w < p.nwords ? bitA[w] : 0u, b = w < p.nwords ? bitB[w] : 0u;
-      uint32_t u = a | b;
-      int n = __popc(u), incl = n;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        int v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
-      }
-      int o = pos + incl - n;
-      while (u) {
-        int bit = __ffs(u) - 1;
-        u &= u - 1;
-        ulist[o++] = static_cast<uint32_t>(w * 32 + bit) | (((a >> bit) & 1u) << 30) | (((b >> bit) & 1u) << 31);
-      }
-      pos += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) n_union = pos;
+    const int n = warp_union_list(bitA, bitB, p.nwords, ulist);
+    if (lane == 0) n_union = n;
   }
   tc_fence_before();
   __syncthreads();
@@ -154,206 +213,409 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kernel(const __grid_cons
   const uint32_t tmem = tmem_base_sh;
   const int U = n_union;
   const int steps = (U + 1) >> 1;
+  auto qcube = [&](int j, int g) -> int {
+    const int e = (g == 1 && 2 * j + 1 < U) ? 2 * j + 1 : 2 * j;
+    return static_cast<int>(ulist[e] & 0x3FFFFFFF);
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer
     if (lane == 0 && steps > 0) {
-      const int c1 = has_k2 ? k2 : k1;
       mbar_expect_tx(&bar_kv, 2 * L::kTile);
-      for (int b = 0; b < D / 64; ++b) {
-        tma_load_2d(sm + L::kK + b * 16384, &p.tk, &bar_kv, 64 * b, static_cast<int>(row_base + 64 * k1));
-        tma_load_2d(sm + L::kK + b * 16384 + 8192, &p.tk, &bar_kv, 64 * b, static_cast<int>(row_base + 64 * c1));
-        tma_load_2d(sm + L::kV + b * 16384, &p.tv, &bar_kv, 64 * b, static_cast<int>(row_base + 64 * k1));
-        tma_load_2d(sm + L::kV + b * 16384 + 8192, &p.tv, &bar_kv, 64 * b, static_cast<int>(row_base + 64 * c1));
-      }
+      const int c1 = has_k2 ? k2 : k1;
+      load_cube_pair<D>(sm + L::kK, &p.tk, &bar_kv, row_base, k1, c1);
+      load_cube_pair<D>(sm + L::kV, &p.tv, &bar_kv, row_base, k1, c1);
       for (int j = 0; j < steps; ++j) {
-        const int q0 = ulist[2 * j] & 0x3FFFFFFF;
-        const int q1 = (2 * j + 1 < U) ? (ulist[2 * j + 1] & 0x3FFFFFFF) : q0;
-        // dO(j) replaces dO(j-1) once dV(j-1) is done; Q(j) once dK(j-1) is.
-        if (j > 0 && !mbar_wait(&bar_dofree, (j - 1) & 1)) {
+        const int s = j & 1;
+        const int q0 = qcube(j, 0), q1 = qcube(j, 1);
+        if (j >= 2 && !mbar_wait(&bar_qfree[s], ((j >> 1) - 1) & 1)) {
           flag_error(p.err, kErrTimeout);
           break;
         }
-        mbar_expect_tx(&bar_dold, L::kTile);
-        for (int b = 0; b < D / 64; ++b) {
-          tma_load_2d(sm + L::kDO + b * 16384, &p.tdo, &bar_dold, 64 * b, static_cast<int>(row_base + 64 * q0));
-          tma_load_2d(sm + L::kDO + b * 16384 + 8192, &p.tdo, &bar_dold, 64 * b, static_cast<int>(row_base + 64 * q1));
-        }
-        if (j > 0 && !mbar_wait(&bar_qfree, (j - 1) & 1)) {
+        mbar_expect_tx(&bar_qld[s], L::kTile);
+        load_cube_pair<D>(sm + L::kQ + s * L::kTile, &p.tq, &bar_qld[s], row_base, q0, q1);
+        if (j >= 2 && !mbar_wait(&bar_dofree[s], ((j >> 1) - 1) & 1)) {
           flag_error(p.err, kErrTimeout);
           break;
         }
-        mbar_expect_tx(&bar_qld, L::kTile);
-        for (int b = 0; b < D / 64; ++b) {
-          tma_load_2d(sm + L::kQ + b * 16384, &p.tq, &bar_qld, 64 * b, static_cast<int>(row_base + 64 * q0));
-          tma_load_2d(sm + L::kQ + b * 16384 + 8192, &p.tq, &bar_qld, 64 * b, static_cast<int>(row_base + 64 * q1));
-        }
+        mbar_expect_tx(&bar_dold[s], L::kTile);
+        load_cube_pair<D>(sm + L::kDO + s * L::kTile, &p.tdo, &bar_dold[s], row_base, q0, q1);
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer: S^T(0), dP^T(0), then per step j
+    //   [P^T, dS^T (j)] dV(j), dK(j), [dV(j) done] S^T(j+1), [dK(j) done] dP^T(j+1)
     if (lane == 0 && steps > 0) {
-      constexpr uint32_t id_ss = idesc_f32acc(128, 128, 0, 0, 1);
-      constexpr uint32_t id_ts = idesc_f32acc(128, D, 0, 1, 1);
-      constexpr uint32_t id_dq = idesc_f32acc(128, 128, 1, 1, 1);
-      constexpr uint32_t lbo_kt = D == 128 ? 16384u : static_cast<uint32_t>(L::kZero - L::kK);
-      bool ok = mbar_wait(&bar_kv, 0);
+      bool ok = mbar_wait(&bar_kv, 0) && mbar_wait(&bar_qld[0], 0);
+      if (ok) {
+        tc_fence_after();
+        mma_rows_x_rows<D>(tmem + kKvS, sm + L::kK, sm + L::kQ);
+        mma_commit(&bar_s);
+      }
+      ok = ok && mbar_wait(&bar_dold[0], 0);
+      if (ok) {
+        tc_fence_after();
+        mma_rows_x_rows<D>(tmem + kKvDP, sm + L::kV, sm + L::kDO);
+        mma_commit(&bar_dp);
+      }
       for (int j = 0; j < steps && ok; ++j) {
-        if (j > 0) ok = ok && mbar_wait(&bar_qfree, (j - 1) & 1);  // P/dS of step j-1 consumed
-        ok = ok && mbar_wait(&bar_qld, j & 1);
+        const int s = j & 1, sn = (j + 1) & 1;
+        ok = ok && mbar_wait(&bar_pds, j & 1);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int b = kk >> 2, w = kk & 3;
-          mma_ss(tmem + kColS, sdesc_sw128(smem_u32(sm + L::kK + b * 16384 + w * 32), 16, 1024),
-                      sdesc_sw128(smem_u32(sm + L::kQ + b * 16384 + w * 32), 16, 1024), id_ss, kk > 0);
+        mma_tmem_x_rows<D>(tmem + kKvDV, tmem + kKvP, sm + L::kDO + s * L::kTile, j > 0);
+        mma_commit(&bar_dofree[s]);
+        mma_commit(&bar_dv);
+        mma_tmem_x_rows<D>(tmem + kKvDK, tmem + kKvDS, sm + L::kQ + s * L::kTile, j > 0);
+        mma_commit(&bar_qfree[s]);
+        mma_commit(&bar_dk);
+        if (j + 1 < steps) {
+          ok = ok && mbar_wait(&bar_qld[sn], ((j + 1) >> 1) & 1) && mbar_wait(&bar_dv, j & 1);
+          if (!ok) break;
+          tc_fence_after();
+          mma_rows_x_rows<D>(tmem + kKvS, sm + L::kK, sm + L::kQ + sn * L::kTile);
+          mma_commit(&bar_s);
+          ok = ok && mbar_wait(&bar_dold[sn], ((j + 1) >> 1) & 1) && mbar_wait(&bar_dk, j & 1);
+          if (!ok) break;
+          tc_fence_after();
+          mma_rows_x_rows<D>(tmem + kKvDP, sm + L::kV, sm + L::kDO + sn * L::kTile);
+          mma_commit(&bar_dp);
         }
-        if (j > 0) ok = ok && mbar_wait(&bar_dqr, (j - 1) & 1);  // dQ^T of step j-1 read out
-        ok = ok && mbar_wait(&bar_dold, j & 1);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int b = kk >> 2, w = kk & 3;
-          mma_ss(tmem + kColDP, sdesc_sw128(smem_u32(sm + L::kV + b * 16384 + w * 32), 16, 1024),
-                      sdesc_sw128(smem_u32(sm + L::kDO + b * 16384 + w * 32), 16, 1024), id_ss, kk > 0);
-        }
-        mma_commit(&bar_mma1);
-        ok = ok && mbar_wait(&bar_ds, j & 1);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + kColDV, tmem + kColP + kk * 8, sdesc_sw128(smem_u32(sm + L::kDO + kk * 2048), 16384, 1024),
-                 id_ts, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar_dofree);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + kColDK, tmem + kColDS + kk * 8, sdesc_sw128(smem_u32(sm + L::kQ + kk * 2048), 16384, 1024),
-                 id_ts, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar_qfree);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + kColDQ, sdesc_sw128(smem_u32(sm + L::kK + kk * 2048), lbo_kt, 1024),
-                      sdesc_sw128(smem_u32(sm + L::kDS + kk * 2048), 16384, 1024), id_dq, kk > 0);
-        mma_commit(&bar_mma2);
       }
       if (!ok) flag_error(p.err, kErrTimeout);
     }
   } else {
-    // ---------------- compute warps: thread = TMEM lane (key row, then d row)
+    // ---------------- compute warps: warpgroup g takes query cube g of each
+    // step (TMEM columns 64g..64g+63); thread = key row r (TMEM lane).
     const int quarter = warp & 3;
+    const int g = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
-    const int ct = tid - 64;  // 0..127, index for cooperative loads
+    const int ct = tid - 64;  // 0..255
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t key_bit = r < 64 ? 30u : 31u;
     bool ok = true;
+    float pf_lse = 0.f, pf_del = 0.f;
+    auto prefetch = [&](int j) {
+      if (ct < 128) {
+        const int64_t qrow = row_base + 64 * static_cast<int64_t>(qcube(j, ct >> 6)) + (ct & 63);
+        pf_lse = p.lse[qrow] * 1.4426950408889634f;
+        pf_del = p.delta[qrow];
+      }
+    };
+    if (steps > 0) prefetch(0);
     for (int j = 0; j < steps; ++j) {
-      const uint32_t e0 = ulist[2 * j];
       const bool has1 = 2 * j + 1 < U;
-      const uint32_t e1 = has1 ? ulist[2 * j + 1] : 0u;
-      {
-        const int g = ct >> 6;
-        const int qc = static_cast<int>((g ? (has1 ? e1 : e0) : e0) & 0x3FFFFFFF);
-        const int64_t qrow = row_base + 64 * qc + (ct & 63);
-        s_lse[(j & 1) * 128 + ct] = p.lse[qrow] * 1.4426950408889634f;
-        s_del[(j & 1) * 128 + ct] = p.delta[qrow];
+      const uint32_t e = (g == 0) ? ulist[2 * j] : (has1 ? ulist[2 * j + 1] : 0u);
+      const bool valid = (g == 0 || has1) && ((e >> key_bit) & 1u) != 0;
+      const bool any = __any_sync(0xffffffffu, valid);
+      float* lse2 = s_lse + (j & 1) * 128 + 64 * g;
+      float* del = s_del + (j & 1) * 128 + 64 * g;
+      if (ct < 128) {
+        s_lse[(j & 1) * 128 + ct] = pf_lse;
+        s_del[(j & 1) * 128 + ct] = pf_del;
       }
-      named_bar_sync(1, 128);
-      if (!mbar_wait(&bar_mma1, j & 1)) {
+      named_bar_sync(1, kCompute);
+      if (j + 1 < steps) prefetch(j + 1);
+      // ---- P^T = exp2(S^T * scale - LSE) and dS^T = P^T (dP^T - D), 16 query
+      // columns at a time; both packed fp16 into this warpgroup's own half of
+      // the S^T / dP^T columns (chunk c lands on columns already read).
+      if (!mbar_wait(&bar_s, j & 1) || !mbar_wait(&bar_dp, j & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool v0 = (e0 >> key_bit) & 1u, v1 = has1 && ((e1 >> key_bit) & 1u);
-      const float* lse2 = s_lse + (j & 1) * 128;
-      const float* del = s_del + (j & 1) * 128;
-      uint32_t dsp[64];
+#pragma unroll 1
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        uint32_t pk[8], dk[8];
+        if (any) {
+          float sv[16], dv[16];
+          tmem_ld16(lane_addr + kKvS + 64 * g + c0, sv);
+          tmem_ld16(lane_addr + kKvDP + 64 * g + c0, dv);
+          tmem_wait_ld();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const bool valid = h ? v1 : v0;
-        float sv[64], dv[64];
+          for (int i = 0; i < 16; i += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c0 + i);
+            const float4 d4 = *reinterpret_cast<const float4*>(del + c0 + i);
+            const float p0 = valid ? fast_exp2(fmaf(sv[i], p.scale_log2, -l4.x)) : 0.f;
+            const float p1 = valid ? fast_exp2(fmaf(sv[i + 1], p.scale_log2, -l4.y)) : 0.f;
+            const float p2 = valid ? fast_exp2(fmaf(sv[i + 2], p.scale_log2, -l4.z)) : 0.f;
+            const float p3 = valid ? fast_exp2(fmaf(sv[i + 3], p.scale_log2, -l4.w)) : 0.f;
+            pk[i >> 1] = pack_f16(p0, p1);
+            pk[(i >> 1) + 1] = pack_f16(p2, p3);
+            dk[i >> 1] = pack_f16(p0 * (dv[i] - d4.x), p1 * (dv[i + 1] - d4.y));
+            dk[(i >> 1) + 1] = pack_f16(p2 * (dv[i + 2] - d4.z), p3 * (dv[i + 3] - d4.w));
+          }
+        } else {
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) {
-          tmem_ld16(lane_addr + kColS + 64 * h + c, sv + c);
-          tmem_ld16(lane_addr + kColDP + 64 * h + c, dv + c);
+          for (int i = 0; i < 8; ++i) pk[i] = dk[i] = 0u;
         }
-        tmem_wait_ld();
-        float pp[32];
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const int q = 64 * h + c;
-          float pa = valid ? fast_exp2(sv[c] * p.scale_log2 - lse2[q]) : 0.f;
-          float pb = valid ? fast_exp2(sv[c + 1] * p.scale_log2 - lse2[q + 1]) : 0.f;
-          float da = pa * (dv[c] - del[q]);
-          float db = pb * (dv[c + 1] - del[q + 1]);
-          pp[c >> 1] = __uint_as_float(pack_f16(pa, pb));
-          dsp[32 * h + (c >> 1)] = pack_f16(da, db);
-        }
-#pragma unroll
-        for (int c = 0; c < 32; c += 16) tmem_st16(lane_addr + kColP + 32 * h + c, pp + c);
-        // dS^T row r, queries 64h..64h+63 -> shared tile (query atom h, key row r)
-        uint8_t* dst = sm + L::kDS + h * 16384;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint4 v = make_uint4(dsp[32 * h + 4 * ch], dsp[32 * h + 4 * ch + 1], dsp[32 * h + 4 * ch + 2],
-                               dsp[32 * h + 4 * ch + 3]);
-          *reinterpret_cast<uint4*>(dst + sw128_offset(r, ch * 8)) = v;
-        }
+        tmem_st8(lane_addr + kKvP + 64 * g + (c0 >> 1), pk);
+        tmem_st8(lane_addr + kKvDS + 64 * g + (c0 >> 1), dk);
       }
-      float* dsf = reinterpret_cast<float*>(dsp);
-#pragma unroll
-      for (int c = 0; c < 64; c += 16) tmem_st16(lane_addr + kColDS + c, dsf + c);
       tmem_wait_st();
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar_ds);
-      // dQ^T: lane = d row, columns = the step's 128 query rows.
-      if (!mbar_wait(&bar_mma2, j & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int64_t qbase0 = row_base + 64 * static_cast<int64_t>(e0 & 0x3FFFFFFF);
-      const int64_t qbase1 = row_base + 64 * static_cast<int64_t>(e1 & 0x3FFFFFFF);
-      // Read the whole dQ^T row out of TMEM first so the next step's dP^T
-      // may overwrite it while the reductions drain.
-      float qv[128];
-#pragma unroll
-      for (int c = 0; c < 128; c += 16) tmem_ld16(lane_addr + kColDQ + c, qv + c);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bar_dqr);
-      if (r < D) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c < 64 || has1) atomicAdd(p.dq + ((c < 64 ? qbase0 : qbase1) + (c & 63)) * D + r, qv[c] * p.scale);
-      }
+      mbar_arrive(&bar_pds);
     }
+    if (ok && steps > 0 && !mbar_wait(&bar_dk, (steps - 1) & 1)) ok = false;
     if (!ok) flag_error(p.err, kErrTimeout);
-    // ---------------- dK, dV rows of this key pair
+    tc_fence_after();
+    // ---------------- dK, dV rows of this key pair (warpgroup 0: dV, 1: dK)
     const int kc = r < 64 ? k1 : k2;
     const bool key_valid = r < 64 || has_k2;
     const int64_t krow = row_base + 64 * static_cast<int64_t>(kc) + (r & 63);
+    float* outp = g == 0 ? p.dv : p.dk;
+    const float mul = g == 0 ? 1.0f : p.scale;
 #pragma unroll
     for (int c = 0; c < D; c += 16) {
-      float a[16], b[16];
+      float a[16];
       if (steps > 0 && ok) {
-        tmem_ld16(lane_addr + kColDV + c, a);
-        tmem_ld16(lane_addr + kColDK + c, b);
+        tmem_ld16(lane_addr + (g == 0 ? kKvDV : kKvDK) + c, a);
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) a[i] = b[i] = 0.f;
+        for (int i = 0; i < 16; ++i) a[i] = 0.f;
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) b[i] *= p.scale;
+      for (int i = 0; i < 16; ++i) a[i] *= mul;
       if (key_valid) {
-        store8(p.dv, krow * D + c, a, VSA_DTYPE_F32);
-        store8(p.dv, krow * D + c + 8, a + 8, VSA_DTYPE_F32);
-        store8(p.dk, krow * D + c, b, VSA_DTYPE_F32);
-        store8(p.dk, krow * D + c + 8, b + 8, VSA_DTYPE_F32);
+        store8(outp, krow * D + c, a, VSA_DTYPE_F32);
+        store8(outp, krow * D + c + 8, a + 8, VSA_DTYPE_F32);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// =============================================================== dQ
+template <int D>
+struct DqLayout {
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kQ = 0, kDO = kTile, kK = 2 * kTile, kV = 4 * kTile;  // K, V: 2 stages each
+  static constexpr int kEnd = 6 * kTile;
+};
+constexpr uint32_t kDqS0 = 0, kDqS1 = 128, kDqDP = 256, kDqDQ = 384;  // dS (fp16) overwrites its S buffer
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using L = DqLayout<D>;
+  uint32_t* ulist = reinterpret_cast<uint32_t*>(sm + L::kEnd);
+  const int nwords = p.nwords;
+  uint32_t* bitA = ulist + 2 * p.kmax + 2;
+  uint32_t* bitB = bitA + nwords;
+
+  // bar_k / bar_v [s]: K / V stage s filled; bar_kvfree[s]: dQ of the step using
+  // stage s done.  bar_s[b]: S in TMEM buffer b done; bar_ds[b]: dS written into
+  // buffer b (128 threads); bar_dq[b]: dQ from buffer b done; bar_dp: dP done.
+  __shared__ uint64_t bar_qdo, bar_k[2], bar_v[2], bar_kvfree[2], bar_s[2], bar_ds[2], bar_dq[2], bar_dp;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int n_union, n_cnt[2];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int pair = blockIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int qa = 2 * pair, qb = 2 * pair + 1;
+  const bool has_b = qb < p.Nc;
+  const int64_t row_base = bh * p.N;
+
+  if (tid == 0) {
+    mbar_init(&bar_qdo, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_k[i], 1);
+      mbar_init(&bar_v[i], 1);
+      mbar_init(&bar_kvfree[i], 1);
+      mbar_init(&bar_s[i], 1);
+      mbar_init(&bar_ds[i], kCompute);
+      mbar_init(&bar_dq[i], 1);
+    }
+    mbar_init(&bar_dp, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  for (int w = tid; w < 2 * nwords; w += kThreads) bitA[w] = 0;  // bitA and bitB are contiguous
+  __syncthreads();
+  {
+    const int64_t rowa = bh * p.Nc + qa;
+    int ca = p.cnt ? p.cnt[rowa] : p.kmax;
+    int cb = has_b ? (p.cnt ? p.cnt[rowa + 1] : p.kmax) : 0;
+    ca = min(max(ca, 0), p.kmax);
+    cb = min(max(cb, 0), p.kmax);
+    if (tid == 0) {
+      n_cnt[0] = ca;
+      n_cnt[1] = cb;
+    }
+    const int32_t* la = p.idx + rowa * p.kmax;
+    const int32_t* lb = la + p.kmax;
+    for (int e = tid; e < ca + cb; e += kThreads) {
+      const bool isA = e < ca;
+      const int c = isA ? la[e] : lb[e - ca];
+      if (c < 0 || c >= p.Nc) continue;  // reported by the inverse-list build
+      atomicOr(&(isA ? bitA : bitB)[c >> 5], 1u << (c & 31));
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int n = warp_union_list(bitA, bitB, nwords, ulist);
+    if (lane == 0) n_union = n;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int U = n_union;
+  const int steps = (U + 1) >> 1;
+  auto kcube = [&](int j, int g) -> int {
+    const int e = (g == 1 && 2 * j + 1 < U) ? 2 * j + 1 : 2 * j;
+    return static_cast<int>(ulist[e] & 0x3FFFFFFF);
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0 && steps > 0) {
+      mbar_expect_tx(&bar_qdo, 2 * L::kTile);
+      const int cq1 = has_b ? qb : qa;
+      load_cube_pair<D>(sm + L::kQ, &p.tq, &bar_qdo, row_base, qa, cq1);
+      load_cube_pair<D>(sm + L::kDO, &p.tdo, &bar_qdo, row_base, qa, cq1);
+      for (int j = 0; j < steps; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(&bar_kvfree[s], ((j >> 1) - 1) & 1)) {
+          flag_error(p.err, kErrTimeout);
+          break;
+        }
+        const int c0 = kcube(j, 0), c1 = kcube(j, 1);
+        mbar_expect_tx(&bar_k[s], L::kTile);
+        load_cube_pair<D>(sm + L::kK + s * L::kTile, &p.tk, &bar_k[s], row_base, c0, c1);
+        mbar_expect_tx(&bar_v[s], L::kTile);
+        load_cube_pair<D>(sm + L::kV + s * L::kTile, &p.tv, &bar_v[s], row_base, c0, c1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: S(0), dP(0), then per step j
+    //   S(j+1) -> buffer (j+1)&1, [dS(j)] dQ(j), dP(j+1)
+    if (lane == 0 && steps > 0) {
+      bool ok = mbar_wait(&bar_qdo, 0) && mbar_wait(&bar_k[0], 0);
+      if (ok) {
+        tc_fence_after();
+        mma_rows_x_rows<D>(tmem + kDqS0, sm + L::kQ, sm + L::kK);
+        mma_commit(&bar_s[0]);
+      }
+      ok = ok && mbar_wait(&bar_v[0], 0);
+      if (ok) {
+        tc_fence_after();
+        mma_rows_x_rows<D>(tmem + kDqDP, sm + L::kDO, sm + L::kV);
+        mma_commit(&bar_dp);
+      }
+      for (int j = 0; j < steps && ok; ++j) {
+        const int s = j & 1, sn = (j + 1) & 1;
+        const bool more = j + 1 < steps;
+        if (more) {
+          ok = ok && mbar_wait(&bar_k[sn], ((j + 1) >> 1) & 1);
+          if (j >= 1) ok = ok && mbar_wait(&bar_dq[sn], ((j - 1) >> 1) & 1);  // dQ(j-1) read buffer sn
+          if (!ok) break;
+          tc_fence_after();
+          mma_rows_x_rows<D>(tmem + (sn ? kDqS1 : kDqS0), sm + L::kQ, sm + L::kK + sn * L::kTile);
+          mma_commit(&bar_s[sn]);
+        }
+        ok = ok && mbar_wait(&bar_ds[s], (j >> 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        mma_tmem_x_rows<D>(tmem + kDqDQ, tmem + (s ? kDqS1 : kDqS0), sm + L::kK + s * L::kTile, j > 0);
+        mma_commit(&bar_dq[s]);
+        mma_commit(&bar_kvfree[s]);
+        if (more) {
+          ok = ok && mbar_wait(&bar_v[sn], ((j + 1) >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          mma_rows_x_rows<D>(tmem + kDqDP, sm + L::kDO, sm + L::kV + sn * L::kTile);
+          mma_commit(&bar_dp);
+        }
+      }
+      if (!ok) flag_error(p.err, kErrTimeout);
+    }
+  } else {
+    // ---------------- compute warps: warpgroup g takes key cube g of each
+    // step (TMEM columns 64g..64g+63); thread = query row (TMEM lane).
+    const int quarter = warp & 3;
+    const int g = (warp - 2) >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t my_bit = row < 64 ? 30u : 31u;
+    const bool row_valid = row < 64 || has_b;
+    const int64_t grow = row_base + 128 * pair + row;
+    const float lse2 = row_valid ? p.lse[grow] * 1.4426950408889634f : 0.f;
+    const float dlt = row_valid ? p.delta[grow] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < steps; ++j) {
+      const int b = j & 1;
+      const uint32_t sbuf = b ? kDqS1 : kDqS0;
+      const bool has1 = 2 * j + 1 < U;
+      const uint32_t e = (g == 0) ? ulist[2 * j] : (has1 ? ulist[2 * j + 1] : 0u);
+      const bool valid = (g == 0 || has1) && ((e >> my_bit) & 1u) != 0;
+      const bool any = __any_sync(0xffffffffu, valid);
+      if (!mbar_wait(&bar_s[b], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      if (!mbar_wait(&bar_dp, j & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // ---- P = exp2(S * scale - LSE), dS = P (dP - D), 16 key columns at a
+      // time; dS packed fp16 into this warpgroup's half of the S buffer.
+#pragma unroll 1
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        uint32_t ds[8];
+        if (any) {
+          float sv[16], dv[16];
+          tmem_ld16(lane_addr + sbuf + 64 * g + c0, sv);
+          tmem_ld16(lane_addr + kDqDP + 64 * g + c0, dv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            const float p0 = valid ? fast_exp2(fmaf(sv[i], p.scale_log2, -lse2)) : 0.f;
+            const float p1 = valid ? fast_exp2(fmaf(sv[i + 1], p.scale_log2, -lse2)) : 0.f;
+            ds[i >> 1] = pack_f16(p0 * (dv[i] - dlt), p1 * (dv[i + 1] - dlt));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ds[i] = 0u;
+        }
+        tmem_st8(lane_addr + sbuf + 64 * g + (c0 >> 1), ds);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar_ds[b]);
+    }
+    if (ok && steps > 0 && !mbar_wait(&bar_dq[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
+    if (!ok) flag_error(p.err, kErrTimeout);
+    tc_fence_after();
+    // ---------------- dQ rows (warpgroup g writes columns [g*D/2, (g+1)*D/2))
+#pragma unroll
+    for (int c0 = 0; c0 < D / 2; c0 += 16) {
+      const int c = g * (D / 2) + c0;
+      float v[16];
+      if (steps > 0 && ok) {
+        tmem_ld16(lane_addr + kDqDQ + c, v);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] *= p.scale;
+      if (row_valid) {
+        store8(p.dq, grow * D + c, v, VSA_DTYPE_F32);
+        store8(p.dq, grow * D + c + 8, v + 8, VSA_DTYPE_F32);
       }
     }
   }
@@ -385,7 +647,8 @@ __global__ void build_inverse_bits(const int32_t* __restrict__ idx, const int32_
   }
   const int64_t bh = row / Nc;
   const int q = static_cast<int>(row % Nc);
-  atomicOr(inv + (bh * Nc + c) * nwords + (q >> 5), 1u << (q & 31));
+  const uint32_t old = atomicOr(inv + (bh * Nc + c) * nwords + (q >> 5), 1u << (q & 31));
+  if (old & (1u << (q & 31))) flag_error(err, kErrLut);  // repeated cube in a row
 }
 
 // D_i = dO_i . O_i (fp32, dO as the fp16 operand the MMAs use), one warp per row.
@@ -459,43 +722,45 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   p.lse = lse;
   p.delta = delta;
   p.inv = inv_ws;
+  p.idx = idx;
+  p.cnt = cnt;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
   p.N = N;
   p.Nc = Nc;
   p.nwords = nwords;
+  p.kmax = kmax;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = device_error_word();
   const size_t inv_bytes = sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords;
   if (cudaMemsetAsync(inv_ws, 0, inv_bytes, s) != cudaSuccess) return VSA_ERR_CUDA;
-  if (cudaMemsetAsync(dq, 0, sizeof(float) * rows * d, s) != cudaSuccess) return VSA_ERR_CUDA;
   const int64_t entries = static_cast<int64_t>(BH) * Nc * kmax;
   if (entries > 0)
     build_inverse_bits<<<static_cast<unsigned>((entries + 255) / 256), 256, 0, s>>>(
         idx, cnt, kmax, Nc, nwords, static_cast<int64_t>(BH) * Nc, inv_ws, p.err);
-  const size_t extra = sizeof(float) * 512 + sizeof(uint32_t) * (2 * Nc + 2 + 2 * nwords);
+  const size_t kv_extra = sizeof(float) * 512 + sizeof(uint32_t) * (2 * Nc + 2 + 2 * nwords);
+  const size_t dq_extra = sizeof(uint32_t) * (2 * kmax + 2 + 2 * nwords);
   dim3 grid((Nc + 1) / 2, BH);
+  auto go = [&](auto kernel, size_t bytes) -> int {
+    const size_t smem = bytes + 1024;
+    if (smem > 227 * 1024) return VSA_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+      return VSA_ERR_CUDA;
+    kernel<<<grid, kThreads, smem, s>>>(p);
+    return VSA_OK;
+  };
+  timing_mark(VSA_K_FINE_BWD, true, s);
   if (d == 128) {
-    size_t smem = BwdLayout<128>::kEnd + 1024 + extra;
-    if (smem > 227 * 1024) return VSA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(fine_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return VSA_ERR_CUDA;
-    timing_mark(VSA_K_FINE_BWD, true, s);
-    fine_bwd_kernel<128><<<grid, kThreads, smem, s>>>(p);
-    timing_mark(VSA_K_FINE_BWD, false, s);
+    if ((st = go(fine_bwd_kv_kernel<128>, KvLayout<128>::kEnd + kv_extra)) != VSA_OK) return st;
+    if ((st = go(fine_bwd_dq_kernel<128>, DqLayout<128>::kEnd + dq_extra)) != VSA_OK) return st;
   } else {
-    size_t smem = BwdLayout<64>::kEnd + 1024 + extra;
-    if (smem > 227 * 1024) return VSA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(fine_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return VSA_ERR_CUDA;
-    timing_mark(VSA_K_FINE_BWD, true, s);
-    fine_bwd_kernel<64><<<grid, kThreads, smem, s>>>(p);
-    timing_mark(VSA_K_FINE_BWD, false, s);
+    if ((st = go(fine_bwd_kv_kernel<64>, KvLayout<64>::kEnd + kv_extra)) != VSA_OK) return st;
+    if ((st = go(fine_bwd_dq_kernel<64>, DqLayout<64>::kEnd + dq_extra)) != VSA_OK) return st;
   }
+  timing_mark(VSA_K_FINE_BWD, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
