@@ -154,7 +154,10 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }
 
 // 32 lanes x 32 bits, 16 consecutive columns: thread t of the warp gets lane
-// (warp's lane quarter)*32 + t, columns col..col+15.
+// (warp's lane quarter)*32 + t, columns col..col+15.  The destination
+// registers are written asynchronously: call tmem_wait_ld() right after the
+// loads and before anything else touches those registers (the compiler does
+// not know the asm's outputs arrive late and may move them in between).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
   asm volatile(
