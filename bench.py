@@ -262,16 +262,27 @@ def run_ours(args, rank: int, world: int):
     value = world * fl["total"] * args.steps / (ms * 1e-3) / 1e12
     per_kernel = {n: round(t / max(c, 1), 4) for n, (t, c) in kern.items()}
     launches = {n: c for n, (t, c) in kern.items()}
-    bwd_ms = per_kernel["fine_bwd"]
-    fwd_ms = per_kernel["fine_fwd"]
-    dominant = max(("fine_bwd", "fine_fwd"), key=lambda n: per_kernel[n])
-    dom_flops = fl[dominant] / 1.0
-    achieved = dom_flops / (per_kernel[dominant] * 1e-3) / 1e12
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    # Work each fine kernel does per launch (products of 2*N*64K*d FLOP each):
+    # forward S and PV (2); backward dK/dV kernel S^T, dP^T, dV, dK (4); dQ
+    # kernel S, dP, dQ (3).  The effective metric counts 2 + 5.
+    unit = 2.0 * wl.N * 64 * wl.topk * wl.d * wl.BH
+    kflops = {"fine_fwd": 2 * unit, "fine_bwd_kv": 4 * unit, "fine_bwd_dq": 3 * unit}
+    dominant = max(kflops, key=lambda n: per_kernel[n])
+    traffic = None  # DRAM bytes per launch from the committed ncu capture (profiles/traffic.txt)
+    tpath = os.path.join(ROOT, "profiles", "traffic.txt")
     if os.path.exists(tpath):
         with open(tpath) as f:
-            traffic = json.load(f).get(dominant)
+            for ln in f:
+                parts = ln.split()
+                if len(parts) == 2 and not ln.startswith("#") and parts[0] == dominant:
+                    traffic = int(parts[1])
+
+    def roof(n):
+        a = kflops[n] / (per_kernel[n] * 1e-3) / 1e12
+        return {"ms": per_kernel[n], "tflops": round(a, 2), "frac": round(a / peaks["tflops"], 4),
+                "flops_per_launch": kflops[n]}
+
+    bwd_ms = per_kernel["fine_bwd_kv"] + per_kernel["fine_bwd_dq"]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3), "higher_is_better": True,
@@ -279,17 +290,18 @@ def run_ours(args, rank: int, world: int):
         "data": "synthetic (seeded smooth field + noise; Wan2.1 activations are not available)",
         "config": config_of(wl, "replicas" if world > 1 else "single GPU"),
         "pct_of_peak": round(100 * value / world / peaks["tflops"], 2),
-        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
-                     "peak": peaks["tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["tflops"], 4),
+        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": roof(dominant)["tflops"],
+                     "peak": peaks["tflops"], "unit": "TFLOP/s", "frac": roof(dominant)["frac"],
                      "traffic": traffic,
                      "peak_source": peaks["source"] + ", bf16 sustained (fp16 nominal rate = bf16)",
-                     "flops_per_launch": dom_flops},
-        "fine_fwd": {"ms": fwd_ms, "tflops": round(fl["fine_fwd"] / (fwd_ms * 1e-3) / 1e12, 2),
-                     "frac": round(fl["fine_fwd"] / (fwd_ms * 1e-3) / 1e12 / peaks["tflops"], 4)},
-        "fine_bwd": {"ms": bwd_ms, "tflops": round(fl["fine_bwd"] / (bwd_ms * 1e-3) / 1e12, 2),
-                     "frac": round(fl["fine_bwd"] / (bwd_ms * 1e-3) / 1e12 / peaks["tflops"], 4)},
+                     "flops_per_launch": kflops[dominant]},
+        "fine_fwd": roof("fine_fwd"),
+        "fine_bwd_kv": roof("fine_bwd_kv"),
+        "fine_bwd_dq": roof("fine_bwd_dq"),
+        "fine_bwd_effective": {"ms": round(bwd_ms, 4),
+                               "tflops": round(fl["fine_bwd"] / (bwd_ms * 1e-3) / 1e12, 2)},
         "kernel_ms_per_step": per_kernel,
-        "gpu_launches": 11 * args.steps,
+        "gpu_launches": 12 * args.steps,
         "kernel_launches_timed": launches,
         "clocks": clocks.summary(),
         "e2e": e2e,

@@ -753,14 +753,15 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
     return VSA_OK;
   };
   timing_mark(VSA_K_FINE_BWD, true, s);
-  if (d == 128) {
-    if ((st = go(fine_bwd_kv_kernel<128>, KvLayout<128>::kEnd + kv_extra)) != VSA_OK) return st;
-    if ((st = go(fine_bwd_dq_kernel<128>, DqLayout<128>::kEnd + dq_extra)) != VSA_OK) return st;
-  } else {
-    if ((st = go(fine_bwd_kv_kernel<64>, KvLayout<64>::kEnd + kv_extra)) != VSA_OK) return st;
-    if ((st = go(fine_bwd_dq_kernel<64>, DqLayout<64>::kEnd + dq_extra)) != VSA_OK) return st;
-  }
+  st = d == 128 ? go(fine_bwd_kv_kernel<128>, KvLayout<128>::kEnd + kv_extra)
+                : go(fine_bwd_kv_kernel<64>, KvLayout<64>::kEnd + kv_extra);
   timing_mark(VSA_K_FINE_BWD, false, s);
+  if (st != VSA_OK) return st;
+  timing_mark(VSA_K_FINE_BWD_DQ, true, s);
+  st = d == 128 ? go(fine_bwd_dq_kernel<128>, DqLayout<128>::kEnd + dq_extra)
+                : go(fine_bwd_dq_kernel<64>, DqLayout<64>::kEnd + dq_extra);
+  timing_mark(VSA_K_FINE_BWD_DQ, false, s);
+  if (st != VSA_OK) return st;
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 

@@ -238,9 +238,10 @@ enum {
     VSA_K_COMBINE = 3,     /* gated combine + inverse reorder */
     VSA_K_BWD_PREP = 4,    /* backward of the combine */
     VSA_K_COARSE_BWD = 5,  /* coarse backward (three kernels) */
-    VSA_K_FINE_BWD = 6,    /* tcgen05 fine backward */
+    VSA_K_FINE_BWD = 6,    /* tcgen05 fine backward, dK/dV kernel */
     VSA_K_FINALIZE = 7,    /* pool backward + inverse reorder */
-    VSA_K_COUNT = 8
+    VSA_K_FINE_BWD_DQ = 8, /* tcgen05 fine backward, dQ kernel */
+    VSA_K_COUNT = 9
 };
 int vsa_timing_enable(int on);
 int vsa_timing_read(int kernel, double* total_ms, int* launches);
