@@ -481,54 +481,70 @@ void orc_fine_bwd_key_cube(const double *qp, const double *kp, const double *vp,
         dv_rows[e] = 0.0;
     }
     int64_t maxk = (int64_t)Kmax * CUBE;
-    double *s = (double *)malloc(sizeof(double) * (maxk + 1));
-    double *dp = (double *)malloc(sizeof(double) * (maxk + 1));
-    for (int64_t i = 0; i < N; i++) {
-        int64_t qcube = i / CUBE;
-        int n = cnt[bh * Nc + qcube];
-        const int32_t *list = idx + (bh * Nc + qcube) * Kmax;
-        int hit = -1;
-        for (int e = 0; e < n; e++)
-            if (list[e] == kcube)
-                hit = e;
-        if (hit < 0)
-            continue;
-        int64_t nk = (int64_t)n * CUBE;
-        const double *q = qp + (bh * N + i) * d;
-        const double *g = dof + (bh * N + i) * d;
-        double m = -INFINITY;
-        for (int64_t e = 0; e < nk; e++) {
-            int64_t j = (int64_t)list[e / CUBE] * CUBE + e % CUBE;
-            const double *kk = kp + (bh * N + j) * d;
-            const double *vv = vp + (bh * N + j) * d;
-            double dot = 0.0, dot2 = 0.0;
-            for (int c = 0; c < d; c++) {
-                dot += q[c] * kk[c];
-                dot2 += g[c] * vv[c];
+    /* Query rows are independent; each thread sums its rows' contributions
+     * and the partial sums are added at the end (only the order of the
+     * additions depends on the thread count). */
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (maxk + 1));
+        double *dp = (double *)malloc(sizeof(double) * (maxk + 1));
+        double *dk_part = (double *)calloc((size_t)CUBE * d, sizeof(double));
+        double *dv_part = (double *)calloc((size_t)CUBE * d, sizeof(double));
+#pragma omp for schedule(dynamic, 64)
+        for (int64_t i = 0; i < N; i++) {
+            int64_t qcube = i / CUBE;
+            int n = cnt[bh * Nc + qcube];
+            const int32_t *list = idx + (bh * Nc + qcube) * Kmax;
+            int hit = -1;
+            for (int e = 0; e < n; e++)
+                if (list[e] == kcube)
+                    hit = e;
+            if (hit < 0)
+                continue;
+            int64_t nk = (int64_t)n * CUBE;
+            const double *q = qp + (bh * N + i) * d;
+            const double *g = dof + (bh * N + i) * d;
+            double m = -INFINITY;
+            for (int64_t e = 0; e < nk; e++) {
+                int64_t j = (int64_t)list[e / CUBE] * CUBE + e % CUBE;
+                const double *kk = kp + (bh * N + j) * d;
+                const double *vv = vp + (bh * N + j) * d;
+                double dot = 0.0, dot2 = 0.0;
+                for (int c = 0; c < d; c++) {
+                    dot += q[c] * kk[c];
+                    dot2 += g[c] * vv[c];
+                }
+                s[e] = scale * dot;
+                dp[e] = dot2;
+                if (s[e] > m)
+                    m = s[e];
             }
-            s[e] = scale * dot;
-            dp[e] = dot2;
-            if (s[e] > m)
-                m = s[e];
-        }
-        double l = 0.0;
-        for (int64_t e = 0; e < nk; e++)
-            l += exp(s[e] - m);
-        double D = 0.0;
-        for (int64_t e = 0; e < nk; e++)
-            D += exp(s[e] - m) / l * dp[e];
-        for (int o = 0; o < CUBE; o++) {
-            int64_t e = (int64_t)hit * CUBE + o;
-            double p = exp(s[e] - m) / l;
-            double ds = p * (dp[e] - D);
-            for (int c = 0; c < d; c++) {
-                dv_rows[o * d + c] += p * g[c];
-                dk_rows[o * d + c] += scale * ds * q[c];
+            double l = 0.0;
+            for (int64_t e = 0; e < nk; e++)
+                l += exp(s[e] - m);
+            double D = 0.0;
+            for (int64_t e = 0; e < nk; e++)
+                D += exp(s[e] - m) / l * dp[e];
+            for (int o = 0; o < CUBE; o++) {
+                int64_t e = (int64_t)hit * CUBE + o;
+                double p = exp(s[e] - m) / l;
+                double ds = p * (dp[e] - D);
+                for (int c = 0; c < d; c++) {
+                    dv_part[o * d + c] += p * g[c];
+                    dk_part[o * d + c] += scale * ds * q[c];
+                }
             }
         }
+#pragma omp critical
+        for (int64_t e = 0; e < (int64_t)CUBE * d; e++) {
+            dk_rows[e] += dk_part[e];
+            dv_rows[e] += dv_part[e];
+        }
+        free(s);
+        free(dp);
+        free(dk_part);
+        free(dv_part);
     }
-    free(s);
-    free(dp);
 }
 
 /* Backward of the gated combination, reordered order: dout_p = dL/dout.

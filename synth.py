@@ -16,11 +16,15 @@ native raster order.  Values are produced in float32 and rounded to bfloat16
 with round-to-nearest-even; every consumer gets the same bits.  The upstream
 gradient dO is N(0, 1).  Gates (when used) are U[0, 1).
 
-Seeds: numpy PCG64 seeded with base_seed XOR crc32("<config>/<tensor>").
+Seeds: every (batch row, head) of every tensor has its own numpy PCG64
+stream, seeded with SeedSequence([base_seed XOR crc32("<config>/<tensor>"),
+b, head]); the smooth field draws its frequencies first and its noise second.
 """
 from __future__ import annotations
 
+import os
 import zlib
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
 
 import numpy as np
@@ -83,10 +87,10 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
     Non-finite inputs are not expected here (the generator never makes them).
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    lsb = (u >> 16) & 1
-    u = (u + 0x7FFF + lsb) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32)
+    u = x.view(np.uint32)
+    # For finite x the sum stays below 2**32 (largest finite pattern 0xFF7FFFFF).
+    u = (u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))) & np.uint32(0xFFFF0000)
+    return u.view(np.float32)
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -99,74 +103,76 @@ def bf16_from_bits(b: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def smooth_field(rng: np.random.Generator, B: int, heads: int, d: int,
-                 T: int, H: int, W: int, nfreq: int = 8,
-                 fmax: float = 0.8, noise_std: float = 0.5,
+def _head_rng(seed: int, b: int, hd: int) -> np.random.Generator:
+    """Independent PCG64 stream for one (batch row, head) of one tensor."""
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, b, hd])))
+
+
+def _per_head(B: int, heads: int, heads_subset, N: int, d: int, fill) -> np.ndarray:
+    """[B, len(hs), N, d] float32 with fill(b, head) -> [N, d] run on a thread
+    pool (numpy releases the GIL in the bulk fills)."""
+    hs = list(range(heads)) if heads_subset is None else list(heads_subset)
+    out = np.empty((B, len(hs), N, d), dtype=np.float32)
+    jobs = [(b, oi, hd) for b in range(B) for oi, hd in enumerate(hs)]
+
+    def run(job):
+        b, oi, hd = job
+        out[b, oi] = fill(b, hd)
+
+    with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 1)) as ex:
+        list(ex.map(run, jobs))
+    return out
+
+
+def smooth_field(seed: int, B: int, heads: int, d: int, T: int, H: int, W: int,
+                 nfreq: int = 8, fmax: float = 0.8, noise_std: float = 0.5,
                  heads_subset=None) -> np.ndarray:
     """[B, len(heads), T*H*W, d] float32 (bf16-exact) smooth field plus noise.
 
-    The frequencies are drawn for all heads first and the noise second, so
-    that a head subset (``heads_subset``) yields exactly the rows of the full
-    tensor for those heads.
+    Each (batch row, head) draws its frequencies and then its noise from its
+    own stream, so a head subset yields exactly those heads of the full tensor.
     """
-    freqs = rng.uniform(0.0, fmax, size=(B, heads, d, nfreq, 3))
-    noise_state = rng.bit_generator.state
-    hs = list(range(heads)) if heads_subset is None else list(heads_subset)
     N = T * H * W
-    out = np.empty((B, len(hs), N, d), dtype=np.float32)
     t = np.arange(T, dtype=np.float64)
     h = np.arange(H, dtype=np.float64)
     w = np.arange(W, dtype=np.float64)
-    for b in range(B):
-        for oi, hd in enumerate(hs):
-            f = freqs[b, hd]                                     # [d, j, 3]
-            et = np.exp(1j * f[:, :, 0, None] * t)               # [d, j, T]
-            eh = np.exp(1j * f[:, :, 1, None] * h)               # [d, j, H]
-            ew = np.exp(1j * f[:, :, 2, None] * w)               # [d, j, W]
-            eth = (et[:, :, :, None] * eh[:, :, None, :]).reshape(d, nfreq, T * H)
-            # sum_j e^{i(a t + b h)} e^{i c w}, imaginary part -> [d, T*H, W]
-            field = np.matmul(eth.transpose(0, 2, 1), ew).imag
-            out[b, oi] = field.reshape(d, N).T
-    # Noise: one stream per tensor, drawn head by head in a fixed order.
-    nrng = np.random.Generator(np.random.PCG64())
-    nrng.bit_generator.state = noise_state
-    for b in range(B):
-        for hd in range(heads):
-            if hd in hs:
-                out[b, hs.index(hd)] += nrng.normal(0.0, noise_std, size=(N, d)).astype(np.float32)
-            else:
-                nrng.normal(0.0, noise_std, size=(N, d))
-    return round_to_bf16(out)
+
+    def fill(b, hd):
+        rng = _head_rng(seed, b, hd)
+        f = rng.uniform(0.0, fmax, size=(d, nfreq, 3))
+        # sin(A + C) = sin A cos C + cos A sin C with A = a t + b h and C = c w,
+        # summed over j as one real product [T*H, 2j] x [2j, W] per channel.
+        A = (f[:, :, 0, None, None] * t[:, None] + f[:, :, 1, None, None] * h[None, :]).reshape(d, nfreq, T * H)
+        C = f[:, :, 2, None] * w                                  # [d, j, W]
+        L = np.concatenate([np.sin(A), np.cos(A)], axis=1)        # [d, 2j, T*H]
+        R = np.concatenate([np.cos(C), np.sin(C)], axis=1)        # [d, 2j, W]
+        field = np.matmul(L.transpose(0, 2, 1), R).reshape(d, N).T
+        noise = rng.standard_normal(size=(N, d), dtype=np.float32)
+        return round_to_bf16(field.astype(np.float32) + np.float32(noise_std) * noise)
+
+    return _per_head(B, heads, heads_subset, N, d, fill)
 
 
 def make_qkv(wl: Workload, heads_subset=None, base: int = BASE_SEED):
     """Q, K, V as float32 bf16-exact arrays [B, heads, N, d] (native order)."""
-    out = []
-    for name in ("q", "k", "v"):
-        rng = np.random.default_rng(seed_for(wl.name, name, base))
-        out.append(smooth_field(rng, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W,
-                                heads_subset=heads_subset))
-    return tuple(out)
+    return tuple(smooth_field(seed_for(wl.name, name, base), wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W,
+                              heads_subset=heads_subset) for name in ("q", "k", "v"))
 
 
 def make_dout(wl: Workload, heads_subset=None, base: int = BASE_SEED) -> np.ndarray:
     """Upstream gradient dO ~ N(0, 1), bf16-exact, [B, heads, N, d]."""
-    rng = np.random.default_rng(seed_for(wl.name, "dout", base))
-    full = rng.standard_normal(size=(wl.B, wl.heads, wl.N, wl.d), dtype=np.float32)
-    if heads_subset is not None:
-        full = full[:, list(heads_subset)]
-    return round_to_bf16(full)
+    seed = seed_for(wl.name, "dout", base)
+    return _per_head(wl.B, wl.heads, heads_subset, wl.N, wl.d, lambda b, hd: round_to_bf16(
+        _head_rng(seed, b, hd).standard_normal(size=(wl.N, wl.d), dtype=np.float32)))
 
 
 def make_gates(wl: Workload, heads_subset=None, base: int = BASE_SEED):
     """Coarse and fine gates U[0, 1), bf16-exact, [B, heads, N, d] each."""
     out = []
     for name in ("g_coarse", "g_fine"):
-        rng = np.random.default_rng(seed_for(wl.name, name, base))
-        g = rng.random(size=(wl.B, wl.heads, wl.N, wl.d), dtype=np.float32)
-        if heads_subset is not None:
-            g = g[:, list(heads_subset)]
-        out.append(round_to_bf16(g))
+        seed = seed_for(wl.name, name, base)
+        out.append(_per_head(wl.B, wl.heads, heads_subset, wl.N, wl.d, lambda b, hd, seed=seed: round_to_bf16(
+            _head_rng(seed, b, hd).random(size=(wl.N, wl.d), dtype=np.float32))))
     return tuple(out)
 
 

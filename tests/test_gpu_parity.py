@@ -4,6 +4,8 @@ scores) must match bit for bit; floating-point outputs and gradients within
 max-abs 2e-2 / mean-abs 2e-3 (tests/parity.py).  The Top-K selection is
 checked against the oracle's float64 scores up to near-ties, and the fine
 stage is then checked on the GPU-chosen lists."""
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -244,3 +246,67 @@ def test_full_size_head_sample(vsa, oracle_mod):
     # properties at full size, all heads: sum_j dK_j = 0 per head and channel
     dk_sum = host(g["dk"]).sum(axis=2)
     assert np.abs(dk_sum).max() < 5e-2 * max(1.0, np.abs(host(g["dk"])).max())
+
+
+# ---------------------------------------------------------------- full sizes, sampled
+def _sampled_checks(vsa, oracle_mod, wl, dtype, n_cubes=4, n_rows=48):
+    """Full-size run of `wl` (all heads, bench launch configuration); the
+    oracle recomputes, for the first and last head: the coarse scores (Top-K
+    validity of the GPU lists), whole query cubes of the output, dQ on sampled
+    rows and dg_c / dg_f on the sampled cubes; and, for head 0, dK / dV of the
+    least-listed key cube (and of an unlisted one, if any).  All heads:
+    sum_j dK_j = 0 per channel."""
+    q, k, v, gc, gf, dout, out, g, saved = _e2e(vsa, oracle_mod, wl, True, dtype, dtype)
+    bf = dtype == torch.bfloat16
+    gidx = saved["idx"].view(wl.B, wl.heads, wl.Nc, wl.topk).cpu().numpy()
+    scale = wl.d ** -0.5
+    pos = oracle_mod.sfc_table(wl.T, wl.H, wl.W)
+    native_of = np.argsort(pos)                          # reordered position -> native token
+    rng = np.random.default_rng(zlib.crc32(wl.name.encode()))
+    cnt1 = np.full((1, wl.Nc), wl.topk, np.int32)
+    at = lambda t, h, nat: host(t[0, h, torch.from_numpy(nat).to(t.device)])
+    for h in sorted({0, wl.heads - 1}):
+        P = lambda a: oracle_mod.permute(a[0, h].reshape(1, wl.N, wl.d), wl.T, wl.H, wl.W)
+        qp, kp, vp, gcp, gfp, dop = (P(a) for a in (q, k, v, gc, gf, dout))
+        pq, pk, pv = (oracle_mod.pool(a) for a in (qp, kp, vp))
+        scores, oc, _ = oracle_mod.coarse(pq, pk, pv, scale)
+        idx1 = gidx[0, h].reshape(1, wl.Nc, wl.topk)
+        check_topk_validity(idx1, scores, wl.topk)
+        # whole query cubes of the output (the first, the last, two random)
+        cubes = np.unique(np.r_[0, wl.Nc - 1, rng.choice(wl.Nc, n_cubes - 2, replace=False)])
+        rows = (64 * cubes[:, None] + np.arange(64)).reshape(-1)
+        of_rows, _ = oracle_mod.fine_fwd_rows(qp, kp, vp, idx1, cnt1, scale, rows)
+        sub = lambda a: a[:, rows]
+        out_ref = oracle_mod.combine(sub(gcp), sub(gfp), oc[:, cubes], of_rows[None])
+        assert_close(at(out, h, native_of[rows]), out_ref[0], bf16_out=bf, what=f"out head {h}")
+        _, _, dgc_ref, dgf_ref = oracle_mod.combine_bwd(sub(dop), sub(gcp), sub(gfp), oc[:, cubes], of_rows[None])
+        assert_close(at(g["dgc"], h, native_of[rows]), dgc_ref[0], bf16_out=bf, what=f"dgc head {h}")
+        assert_close(at(g["dgf"], h, native_of[rows]), dgf_ref[0], bf16_out=bf, what=f"dgf head {h}")
+        # dO_f and dO_c of every row (O_f enters only dg_f, not used from this call)
+        dof, doc, _, _ = oracle_mod.combine_bwd(dop, gcp, gfp, oc, np.zeros_like(dop))
+        dqc, dkc, dvc = oracle_mod.coarse_bwd(pq, pk, pv, doc, scale)
+        qrows = np.unique(np.r_[0, wl.N - 1, rng.choice(wl.N, n_rows - 2, replace=False)])
+        dq_ref = oracle_mod.fine_bwd_query_rows(qp, kp, vp, dof, idx1, cnt1, scale, qrows) + dqc[0, qrows // 64] / 64.0
+        assert_close(at(g["dq"], h, native_of[qrows]), dq_ref, bf16_out=bf, what=f"dq rows head {h}")
+        if h == 0:
+            inv_count = np.bincount(idx1.reshape(-1), minlength=wl.Nc)
+            kcubes = [int(np.argmin(np.where(inv_count > 0, inv_count, 1 << 30)))]
+            if (inv_count == 0).any():
+                kcubes.append(int(np.argmax(inv_count == 0)))
+            for c in kcubes:
+                dk_c, dv_c = oracle_mod.fine_bwd_key_cube(qp, kp, vp, dof, idx1, cnt1, scale, 0, c)
+                nat = native_of[64 * c:64 * c + 64]
+                assert_close(at(g["dk"], h, nat), dk_c + dkc[0, c] / 64.0, bf16_out=bf, what=f"dk cube {c}")
+                assert_close(at(g["dv"], h, nat), dv_c + dvc[0, c] / 64.0, bf16_out=bf, what=f"dv cube {c}")
+    dk_sum = g["dk"].float().sum(dim=2)
+    dk_max = g["dk"].float().abs().amax()
+    assert float(dk_sum.abs().amax()) < 5e-2 * max(1.0, float(dk_max))
+
+
+@pytest.mark.parametrize("name,dtype", [("wan1.3b_k512", torch.float32), ("wan1.3b_k256", torch.float32),
+                                        ("wan1.3b_k64", torch.float32), ("wan14b", torch.bfloat16),
+                                        ("long", torch.float32)])
+def test_full_size_sampled(vsa, oracle_mod, name, dtype):
+    """The 32K-token sparsity sweep (K = 512, 256, 64 of 512 cubes), the
+    40-head Wan-14B-shaped layer and the 122880-token long video, at full size."""
+    _sampled_checks(vsa, oracle_mod, synth.WORKLOADS[name], dtype)
