@@ -745,7 +745,7 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   dim3 grid((Nc + 1) / 2, BH);
   auto go = [&](auto kernel, size_t bytes) -> int {
     const size_t smem = bytes + 1024;
-    if (smem > 227 * 1024) return VSA_ERR_UNSUPPORTED;
+    if (smem > 226 * 1024) return VSA_ERR_UNSUPPORTED;  // 1 KB of the 227 KB is left for static shared memory
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       return VSA_ERR_CUDA;

@@ -9,17 +9,27 @@
 // columns per MMA, while the index list is per 64-token query cube.  One CTA
 // therefore owns a PAIR of consecutive query cubes (128 query rows) and walks
 // the UNION of their two lists, two key cubes (128 keys) per step; each half
-// of the tile masks the cubes its own list does not hold.  Per step:
-//   S  = Q K^T         tcgen05.mma, A = Q (smem), B = K (smem), D = TMEM
-//   P  = exp2(S - m)   softmax warps, one thread per row, P -> TMEM (fp16)
-//   O += P V           tcgen05.mma, A = P (TMEM), B = V (smem, fp16), D = TMEM
-// K/V tiles arrive by TMA (128-byte swizzle), one K and one V stage; K(j+1)
-// streams in while softmax(j) and PV(j) run.  Each CTA uses 256 TMEM columns
-// (S, with P written over it, and O) and ~100 KB of shared memory, so two
-// CTAs share an SM and hide each other's latencies.  The running max is only
-// raised (and O rescaled) when a row's max grows by more than 2^8, so P <= 256
-// and the fp32 accumulators stay exact enough.
-// Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 softmax/epilogue.
+// of the tile masks the cubes its own list does not hold.  Per step j:
+//   S(j) = Q K(j)^T     tcgen05.mma, A = Q (smem), B = K (smem), D = TMEM
+//   P(j) = exp2(S - m)  softmax warps, one thread per row, P -> TMEM (fp16)
+//   O   += P(j) V(j)    tcgen05.mma, A = P (TMEM), B = V (smem, fp16)
+// One CTA per SM.  K and V stream through rings of up to three 32 KB shared-
+// memory stages each.  Q sits in TMEM and is the A operand of S = Q K^T, so
+// the tensor core reads only K and V from shared memory: every byte of it
+// also has to be written there by the TMA, and the two share the shared-
+// memory bandwidth (an SM ingests only ~45 B/clk from L2).  TMEM columns:
+// S (128), two P buffers (2 x 64), O (D) and Q (D / 2).  The S buffer is
+// released as soon as the softmax warps have read it into registers, so
+// S(j+1) runs while they compute P(j); P is double-buffered so that storing
+// P(j) never waits for the PV product just before it.
+// The running max is only raised (and O rescaled) when a row's max grows by
+// more than 2^8, so P <= 256.
+// A warp's 32 rows all belong to one query cube, so a key cube outside that
+// cube's list is skipped by the whole warp (no loads, no exponentials).
+// Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2-9 softmax/epilogue
+// (two warps per TMEM lane quarter, one per key cube of the step).
+#include <algorithm>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -29,16 +39,23 @@
 namespace vsa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 256;  // 8 softmax warps
+constexpr int kThreads = 64 + kSoftmaxThreads;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr uint32_t kTmemCols = 256;        // two CTAs share an SM's 512 columns
-constexpr uint32_t kColS = 0, kColP = 0, kColO = 128;  // P (fp16) overwrites S
+constexpr uint32_t kTmemCols = 512;        // the whole SM: one CTA per SM
+constexpr uint32_t kColS = 0;              // S: 128 fp32 columns
+constexpr uint32_t kColP = 128;            // P(j) in 128 + 64 (j % 2): 64 columns of fp16 pairs
+constexpr uint32_t kColO = 256;            // O: D columns
+constexpr uint32_t kColQ = 384;            // Q as the A operand: D / 2 columns of fp16 pairs
+constexpr int kMaxStages = 3;              // K and V ring depth
 
 struct FwdParams {
-  CUtensorMap tq, tk, tv;  // [BH*N, d] bf16, box {64, 64}, 128B swizzle
+  CUtensorMap tk, tv;  // [BH*N, d] fp16 / bf16, box {64, 64}, 128B swizzle
+  const uint16_t* q;   // [BH*N, d] fp16 / bf16, row-major
   const int32_t* idx;
   const int32_t* cnt;
   int kmax, N, Nc, npairs;
+  int nk, nv;        // K and V ring depths (1..kMaxStages)
   float scale_log2;  // scale * log2(e)
   void* of;
   int of_dtype;
@@ -48,11 +65,8 @@ struct FwdParams {
 
 template <int D>
 struct FwdLayout {
-  static constexpr int kTile = 128 * D * 2;  // 128 rows x D bf16
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;
-  static constexpr int kV = kK + kTile;
-  static constexpr int kEnd = kV + kTile;
+  static constexpr int kTile = 128 * D * 2;  // 128 rows x D 16-bit
+  static constexpr int kRing = 0;  // nk K stages, then nv V stages
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -61,25 +75,85 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of 64 values as a shallow tree of three-input maxima.
+__device__ __forceinline__ float max64(const uint32_t* v) {
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float* x = reinterpret_cast<const float*>(v + 8 * k);
+    float t = fmax3(x[0], x[1], x[2]);
+    t = fmax3(t, x[3], x[4]);
+    t = fmax3(t, x[5], x[6]);
+    a[k] = fmaxf(t, x[7]);
+  }
+  return fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+}
+
+// 64 weights P = exp2(S * sl2 - m) of one key cube: packed fp16 pairs into
+// pk[32], and their rounded values (what the PV product multiplies with)
+// added to the two row-sum partials.  S * sl2 - m runs as a packed fp32 pair.
+__device__ __forceinline__ void softmax64(const uint32_t* sv, uint64_t sl2x2, uint64_t negmx2, uint32_t* pk, float& acc0,
+                                          float& acc1) {
+#pragma unroll
+  for (int c = 0; c < 64; c += 2) {
+    uint64_t x, t;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(sv[c]), "r"(sv[c + 1]));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(t) : "l"(x), "l"(sl2x2), "l"(negmx2));
+    float t0, t1;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(t0), "=f"(t1) : "l"(t));
+    const float a = fast_exp2(t0), b = fast_exp2(t1);
+    uint32_t h;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(b), "f"(a));  // a -> low half
+    pk[c >> 1] = h;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(h));
+  }
+}
+
+__device__ __forceinline__ uint64_t splat2(float v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(v));
+  return r;
+}
+
 // F16IN: Q, K, V arrive as fp16; otherwise as bf16, and the softmax warps
 // convert each V tile to fp16 in shared memory (exact within +-65504) so that
 // P V always runs on fp16 operands (P rounded to 2^-12, not bf16's 2^-9).
 // Accumulation is fp32 either way.
 template <int D, bool F16IN>
-__global__ void __launch_bounds__(kThreads, 2) fine_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using L = FwdLayout<D>;
-  uint32_t* ulist = reinterpret_cast<uint32_t*>(sm + L::kEnd);  // union entries: id | inA<<30 | inB<<31
+  const int nk = p.nk, nv = p.nv;
+  uint8_t* kring = sm + L::kRing;
+  uint8_t* vring = kring + nk * L::kTile;
+  uint32_t* ulist = reinterpret_cast<uint32_t*>(vring + nv * L::kTile);  // id | inA<<30 | inB<<31
   const int nwords = (p.Nc + 31) >> 5;
   uint32_t* bitA = ulist + 2 * p.kmax + 2;
   uint32_t* bitB = bitA + nwords;
 
-  // Each barrier completes once per step (bar_q once): K(j) / V(j) loaded,
-  // S(j) done, P(j) written (128 softmax threads), PV(j) done.
-  __shared__ uint64_t bar_q, bar_k, bar_v, bar_s, bar_p, bar_pv;
+  // kfull/vfull: a stage's TMA landed.  kfree/vfree: the MMA that read the
+  // stage completed.  bar_s: S(j) done.  s_free: the softmax warps have read
+  // S(j) (the buffer may take S(j+1)).  bar_p[b]: P(j) written into P buffer
+  // b = j % 2 (all softmax threads).  pv_done[b]: PV(j) completed (O
+  // includes it and P buffer b is free).  A parity wait is only correct while
+  // the barrier is in the awaited phase or the one after it; each wait below
+  // keeps to that (P(j) is stored only after PV(j - 2) has completed).
+  __shared__ uint64_t bar_qt, kfull[kMaxStages], kfree[kMaxStages], vfull[kMaxStages], vfree[kMaxStages];
+  __shared__ uint64_t bar_s, s_free, bar_p[2], pv_done[2];
+  __shared__ uint64_t pair_bar[4];  // per lane quarter: its two softmax warps (64 threads)
   __shared__ uint32_t tmem_base_sh;
-  __shared__ int n_union, n_cnt[2];
+  __shared__ int n_union, n_first, n_cnt[2];
+  __shared__ float xmax[2][2][128];  // row max / sum exchange between the two warps of a pair
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pair = blockIdx.x;
@@ -89,12 +163,20 @@ __global__ void __launch_bounds__(kThreads, 2) fine_fwd_kernel(const __grid_cons
 
   // ---------------- prologue: barriers, TMEM, union of the two index lists
   if (tid == 0) {
-    mbar_init(&bar_q, 1);
-    mbar_init(&bar_k, 1);
-    mbar_init(&bar_v, 1);
+    mbar_init(&bar_qt, kSoftmaxThreads);
+    for (int i = 0; i < 4; ++i) mbar_init(&pair_bar[i], 64);
+    for (int i = 0; i < kMaxStages; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kfree[i], 1);
+      mbar_init(&vfull[i], 1);
+      mbar_init(&vfree[i], 1);
+    }
     mbar_init(&bar_s, 1);
-    mbar_init(&bar_p, 128);
-    mbar_init(&bar_pv, 1);
+    mbar_init(&s_free, kSoftmaxThreads);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_p[i], kSoftmaxThreads);
+      mbar_init(&pv_done[i], 1);
+    }
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -133,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 2) fine_fwd_kernel(const __grid_cons
   __syncthreads();
   if (warp == 0) {
     // Visit order: the first (highest-scored) entry of each list, then the
-    // rest of the union by increasing cube id.
+    // rest of the union by increasing cube id (walked from a rotated start).
     const int ca = n_cnt[0], cb = n_cnt[1];
     const int32_t* la = p.idx + (bh * p.Nc + qa) * p.kmax;
     int first[2] = {-1, -1};
@@ -173,212 +255,291 @@ __global__ void __launch_bounds__(kThreads, 2) fine_fwd_kernel(const __grid_cons
       }
       pos += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) n_union = pos;
+    if (lane == 0) {
+      n_union = pos;
+      n_first = nf;
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const int U = n_union;
+  // The part of the union after the first entries is walked from a rotated
+  // start, so that the CTAs running at the same time read different key
+  // cubes instead of all sweeping the head's cubes in the same order.
+  const int nf = n_first, ntail = U - nf;
+  const int rot = ntail > 0 ? static_cast<int>((static_cast<uint32_t>(pair) * 2654435761u >> 7) % ntail) : 0;
+  auto uent = [&](int e) -> uint32_t {
+    if (e < nf) return ulist[e];
+    int t = e - nf + rot;
+    if (t >= ntail) t -= ntail;
+    return ulist[nf + t];
+  };
   const int steps = (U + 1) >> 1;
   const int64_t row_base = bh * p.N;  // first row of this head in the 2D tensor maps
 
   if (warp == 0) {
-    // ---------------- TMA producer: one K stage and one V stage.  K(j) may be
-    // loaded once S(j-1) is done with K(j-1); V(j) once PV(j-1) is done.
+    // ---------------- TMA producer.  K(j) goes to stage j % nk once S(j - nk)
+    // has completed; V(j) to stage j % nv once PV(j - nv) has.  K(j + 1) is
+    // requested before V(j): the MMA issuer needs them in that order.
     if (lane == 0 && steps > 0) {
-      tma_prefetch_desc(&p.tq);
       tma_prefetch_desc(&p.tk);
       tma_prefetch_desc(&p.tv);
-      mbar_expect_tx(&bar_q, L::kTile);
-      for (int b = 0; b < D / 64; ++b)
-        for (int h = 0; h < 2; ++h)
-          tma_load_2d(sm + L::kQ + b * 16384 + h * 8192, &p.tq, &bar_q, 64 * b,
-                      static_cast<int>(row_base + 128 * pair + 64 * h));
-      for (int j = 0; j < steps; ++j) {
-        const int c0 = ulist[2 * j] & 0x3FFFFFFF;
-        const int c1 = (2 * j + 1 < U) ? (ulist[2 * j + 1] & 0x3FFFFFFF) : c0;
-        if (j > 0 && !mbar_wait(&bar_s, (j - 1) & 1)) {
-          flag_error(p.err, kErrTimeout);
-          break;
-        }
-        mbar_expect_tx(&bar_k, L::kTile);
+      auto load = [&](int j, const CUtensorMap* map, uint8_t* ring, int depth, uint64_t* full,
+                      uint64_t* free_) -> bool {
+        const int st = j % depth, use = j / depth;
+        if (use > 0 && !mbar_wait(&free_[st], (use - 1) & 1)) return false;
+        const int c0 = uent(2 * j) & 0x3FFFFFFF;
+        const int c1 = (2 * j + 1 < U) ? (uent(2 * j + 1) & 0x3FFFFFFF) : c0;
+        uint8_t* dst = ring + st * L::kTile;
+        mbar_expect_tx(&full[st], L::kTile);
         for (int b = 0; b < D / 64; ++b) {
-          tma_load_2d(sm + L::kK + b * 16384, &p.tk, &bar_k, 64 * b, static_cast<int>(row_base + 64 * c0));
-          tma_load_2d(sm + L::kK + b * 16384 + 8192, &p.tk, &bar_k, 64 * b, static_cast<int>(row_base + 64 * c1));
+          tma_load_2d(dst + b * 16384, map, &full[st], 64 * b, static_cast<int>(row_base + 64 * c0));
+          tma_load_2d(dst + b * 16384 + 8192, map, &full[st], 64 * b, static_cast<int>(row_base + 64 * c1));
         }
-        if (j > 0 && !mbar_wait(&bar_pv, (j - 1) & 1)) {
-          flag_error(p.err, kErrTimeout);
-          break;
-        }
-        mbar_expect_tx(&bar_v, L::kTile);
-        for (int b = 0; b < D / 64; ++b) {
-          tma_load_2d(sm + L::kV + b * 16384, &p.tv, &bar_v, 64 * b, static_cast<int>(row_base + 64 * c0));
-          tma_load_2d(sm + L::kV + b * 16384 + 8192, &p.tv, &bar_v, 64 * b, static_cast<int>(row_base + 64 * c1));
-        }
+        return true;
+      };
+      bool ok = load(0, &p.tk, kring, nk, kfull, kfree);
+      for (int j = 0; ok && j < steps; ++j) {
+        if (j + 1 < steps) ok = load(j + 1, &p.tk, kring, nk, kfull, kfree);
+        ok = ok && load(j, &p.tv, vring, nv, vfull, vfree);
       }
+      if (!ok) flag_error(p.err, kErrTimeout);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer.  S and P share TMEM columns [0, 128): S(j)
-    // is issued only after PV(j-1) has read P(j-1).
+    // ---------------- MMA issuer: S(j+1) runs while the softmax warps work on
+    // S(j); PV(j) follows once P(j) is written.
+    // S = Q K^T takes Q from TMEM, so that the tensor core reads only K (not
+    // Q as well) from shared memory while the TMA writes the next tiles.
     if (lane == 0 && steps > 0) {
       constexpr uint32_t idesc_s = idesc_f32acc(128, 128, 0, 0, F16IN);
       constexpr uint32_t idesc_pv = idesc_f32acc(128, D, 0, 1, 1);
-      bool ok = mbar_wait(&bar_q, 0);
-      for (int j = 0; j < steps && ok; ++j) {
-        ok = ok && mbar_wait(&bar_k, j & 1);
-        if (j > 0) ok = ok && mbar_wait(&bar_pv, (j - 1) & 1);
-        if (!ok) break;
-        tc_fence_after();
+      bool ok = mbar_wait(&bar_qt, 0);
+      // The issuer shares its SM sub-partition with two busy softmax warps, so
+      // it is kept lean: ring slots and parities are stepped, not divided,
+      // and the operand descriptors are advanced from per-ring bases (the
+      // start-address field is linear in the byte address).
+      const uint64_t kdesc0 = sdesc_sw128(smem_u32(kring), 16, 1024);
+      const uint64_t vdesc0 = sdesc_sw128(smem_u32(vring), 16384, 1024);
+      constexpr uint32_t kTileUnits = L::kTile >> 4;
+      int ns = 0, npv = 0;                 // next S and next PV to issue
+      uint32_t ks = 0, kph = 0;            // K stage of S(ns) and its fill parity
+      uint32_t vs = 0, vph = 0;            // V stage of PV(npv) and its fill parity
+      uint32_t idle = 0;
+      // A suspended wait (try_wait) wakes up hundreds of cycles after the
+      // phase completes, so the issuer polls with test_wait and issues
+      // whichever of S(ns) and PV(npv) is ready first.
+      while (ok && npv < steps) {
+        bool progressed = false;
+        // S(ns) once the softmax warps have read S(ns - 1) out of the buffer.
+        if (ns < steps && (ns == 0 || mbar_test(&s_free, (ns - 1) & 1)) && mbar_test(&kfull[ks], kph)) {
+          tc_fence_after();
+          const uint64_t kd = kdesc0 + ks * kTileUnits;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int b = kk >> 2, w = kk & 3;
-          uint64_t ad = sdesc_sw128(smem_u32(sm + L::kQ + b * 16384 + w * 32), 16, 1024);
-          uint64_t bd = sdesc_sw128(smem_u32(sm + L::kK + b * 16384 + w * 32), 16, 1024);
-          mma_ss(tmem + kColS, ad, bd, idesc_s, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t bd = kd + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem + kColS),
+                "r"(tmem + kColQ + kk * 8), "l"(bd), "r"(idesc_s), "r"(static_cast<uint32_t>(kk > 0)));
+          }
+          mma_commit(&bar_s);
+          mma_commit(&kfree[ks]);
+          ++ns;
+          if (++ks == static_cast<uint32_t>(nk)) {
+            ks = 0;
+            kph ^= 1u;
+          }
+          progressed = true;
         }
-        mma_commit(&bar_s);
-        ok = ok && mbar_wait(&bar_p, j & 1);
-        ok = ok && mbar_wait(&bar_v, j & 1);
-        if (!ok) break;
-        tc_fence_after();
+        if (npv < ns && mbar_test(&bar_p[npv & 1], (npv >> 1) & 1) && mbar_test(&vfull[vs], vph)) {
+          tc_fence_after();
+          const uint32_t pcol = tmem + kColP + 64 * (npv & 1);
+          const uint64_t vd = vdesc0 + vs * kTileUnits;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          uint64_t bd = sdesc_sw128(smem_u32(sm + L::kV + kk * 2048), 16384, 1024);
-          asm volatile(
-              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-              "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem + kColO),
-              "r"(tmem + kColP + kk * 8), "l"(bd), "r"(idesc_pv), "r"(static_cast<uint32_t>(j > 0 || kk > 0)));
+          for (int kk = 0; kk < 8; ++kk) {
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem + kColO),
+                "r"(pcol + kk * 8), "l"(vd + ((kk * 2048) >> 4)), "r"(idesc_pv),
+                "r"(static_cast<uint32_t>(npv > 0 || kk > 0)));
+          }
+          mma_commit(&vfree[vs]);
+          mma_commit(&pv_done[npv & 1]);
+          ++npv;
+          if (++vs == static_cast<uint32_t>(nv)) {
+            vs = 0;
+            vph ^= 1u;
+          }
+          progressed = true;
         }
-        mma_commit(&bar_pv);
+        idle = progressed ? 0u : idle + 1u;
+        if (idle > (1u << 26)) ok = false;
       }
       if (!ok) flag_error(p.err, kErrTimeout);
     }
   } else {
-    // ---------------- softmax + epilogue: one thread per query row.  The two
-    // 64-column halves of S are the step's two key cubes.
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // TMEM lane == tile row
+    // ---------------- softmax + epilogue.  Two warps share each 32-row lane
+    // quarter: warp (q, h) handles key cube h (columns [64h, 64h + 64)) of
+    // the step for rows 32q..32q+31, so each SM sub-partition runs two
+    // softmax warps.  The pair agrees on the row max through shared memory;
+    // each keeps a partial row sum over its own key cubes.
+    const int sw = warp - 2;               // 0..7
+    const int quarter = warp & 3;          // TMEM lane quarter this warp may access
+    const int half = sw >> 2;              // key cube of the step (S columns)
+    const int row = quarter * 32 + lane;   // TMEM lane == tile row
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t my_bit = row < 64 ? 30u : 31u;
-    float m = -INFINITY, l = 0.f;
+    const uint32_t my_bit = row < 64 ? 30u : 31u;  // warp-uniform
+    uint64_t* pair_mb = &pair_bar[quarter];       // 64-thread barrier of the two warps
+    uint32_t pair_uses = 0;
+    float m = -INFINITY, l = 0.f;                  // m is identical in both warps
     bool ok = true;
+    {
+      // Q rows into TMEM (lane = row, column c = elements 2c and 2c + 1):
+      // warp (q, h) writes elements [h D/2, (h + 1) D/2) of its 32 rows.
+      const bool qrow = row < 64 || has_b;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + (row_base + 128 * pair + row) * D + half * (D / 2));
+#pragma unroll
+      for (int c = 0; c < D / 4; c += 8) {
+        uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+        if (qrow && steps > 0) {
+          a = src[c / 4];
+          b = src[c / 4 + 1];
+        }
+        const uint32_t r[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        tmem_st8(lane_addr + kColQ + half * (D / 4) + c, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar_qt);
+    }
     for (int j = 0; j < steps; ++j) {
-      // S(j) done implies PV(j-1) done: O may be rescaled without another wait.
-      if (!mbar_wait(&bar_s, j & 1)) {
+      if (!mbar_spin(&bar_s, j & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t e0 = ulist[2 * j];
-      const uint32_t e1 = (2 * j + 1 < U) ? ulist[2 * j + 1] : 0u;
-      const bool vh[2] = {((e0 >> my_bit) & 1u) != 0, ((e1 >> my_bit) & 1u) != 0};
-      // pass 1: row max over the valid halves (warp-uniform loads)
+      const uint32_t sb = lane_addr + kColS;
+      const uint32_t e = (2 * j + half < U) ? uent(2 * j + half) : 0u;
+      const bool valid = ((e >> my_bit) & 1u) != 0;  // warp-uniform
+      uint32_t sr[64];
       float mx = -INFINITY;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (!__any_sync(0xffffffffu, vh[h])) continue;
-        float sv[64];
-#pragma unroll
-        for (int c = 0; c < 64; c += 16) tmem_ld16(lane_addr + kColS + 64 * h + c, sv + c);
-        tmem_wait_ld();
-        if (vh[h]) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) mx = fmaxf(mx, sv[c]);
-        }
+      if (valid) {
+        tmem_ld64_wait(sb + 64 * half, sr);
+        mx = max64(sr) * p.scale_log2;
       }
-      mx *= p.scale_log2;
+      // S is in registers: the buffer may take S(j + 1).
+      tc_fence_before();
+      mbar_arrive(&s_free);
+      // Exchange the half maxima (double-buffered by step parity).
+      xmax[j & 1][half][row] = mx;
+      mbar_arrive(pair_mb);
+      if (!mbar_spin(pair_mb, pair_uses++ & 1)) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, xmax[j & 1][half ^ 1][row]);
+
       // Raise the running max only when it grows by more than the threshold.
       const bool raise = mx > m + kRescaleThreshold;
       const float m_new = raise ? mx : m;
-      const bool need_rescale = raise && (l > 0.f);
+      const bool need_rescale = raise && (m != -INFINITY);
       if (__any_sync(0xffffffffu, need_rescale)) {
+        // O holds PV(0..j-1); the last of them may still be running.  Each
+        // warp of the pair rescales its half of O's columns.
+        if (!mbar_spin(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         const float alpha = need_rescale ? fast_exp2(m - m_new) : 1.0f;
 #pragma unroll
-        for (int c = 0; c < D; c += 16) {
-          float ov[16];
-          tmem_ld16(lane_addr + kColO + c, ov);
-          tmem_wait_ld();
+        for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
+          uint32_t ov[32];
+          tmem_ld32_wait(lane_addr + kColO + c, ov);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) ov[i] *= alpha;
-          tmem_st16(lane_addr + kColO + c, ov);
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) tmem_st8(lane_addr + kColO + c + i, ov + i);
         }
         tmem_wait_st();
         l *= alpha;
       }
       m = m_new;
-      // pass 2: P = exp2(S*scale - m) per half, packed fp16 into TMEM columns
-      // [32h, 32h + 32) (over S columns this thread has already read).
-      float rs = 0.f;
+      // P = exp2(S * scale - m), fp16 pairs into columns [32h, 32h + 32) of
+      // P buffer j % 2 once PV(j - 2) has read P(j - 2) out of it.
+      // The row sum adds the same rounded weights the PV MMA sees, so O / l
+      // stays an exact convex combination of V rows (summing the unrounded
+      // weights instead made the output ~4x and dK ~6x less accurate).
+      uint32_t pk[32];
+      if (valid) {
+        float acc0 = 0.f, acc1 = 0.f;
+        softmax64(sr, splat2(p.scale_log2), splat2(-m), pk, acc0, acc1);
+        l += acc0 + acc1;
+      } else {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float pk[32];
-        const bool any = __any_sync(0xffffffffu, vh[h]);
-        if (any) {
-          float sv[64];
-#pragma unroll
-          for (int c = 0; c < 64; c += 16) tmem_ld16(lane_addr + kColS + 64 * h + c, sv + c);
-          tmem_wait_ld();
-          const bool use = vh[h] && m != -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float a = use ? fast_exp2(fmaf(sv[c], p.scale_log2, -m)) : 0.f;
-            const float b = use ? fast_exp2(fmaf(sv[c + 1], p.scale_log2, -m)) : 0.f;
-            const uint32_t pp = pack_f16(a, b);
-            // The row sum uses the same rounded weights the PV MMA sees, so
-            // O / l stays an exact convex combination of V rows.
-            rs += f16_lo(pp) + f16_hi(pp);
-            pk[c >> 1] = __uint_as_float(pp);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = 0.f;
-        }
-#pragma unroll
-        for (int c = 0; c < 32; c += 16) tmem_st16(lane_addr + kColP + 32 * h + c, pk + c);
+        for (int c = 0; c < 32; ++c) pk[c] = 0u;
       }
-      l += rs;
-      if (!F16IN) {
-        // bf16 V tile -> fp16 in place, before the PV MMA may read it.
-        if (!mbar_wait(&bar_v, j & 1)) {
+      if (j >= 2) {
+        if (!mbar_spin(&pv_done[j & 1], ((j >> 1) - 1) & 1)) {
           ok = false;
           break;
         }
-        uint4* vt = reinterpret_cast<uint4*>(sm + L::kV);
-        const int t128 = threadIdx.x - 64;
-        for (int e = t128; e < L::kTile / 16; e += 128) {
-          uint4 u = vt[e];
-          vt[e] = make_uint4(pack_f16(bf16_lo(u.x), bf16_hi(u.x)), pack_f16(bf16_lo(u.y), bf16_hi(u.y)),
-                             pack_f16(bf16_lo(u.z), bf16_hi(u.z)), pack_f16(bf16_lo(u.w), bf16_hi(u.w)));
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int c = 0; c < 32; c += 8) tmem_st8(lane_addr + kColP + 64 * (j & 1) + 32 * half + c, pk + c);
+      if (!F16IN) {
+        // bf16 V tile -> fp16 in place, before the PV MMA may read it.
+        const int st = j % nv;
+        if (!mbar_wait(&vfull[st], (j / nv) & 1)) {
+          ok = false;
+          break;
+        }
+        uint4* vt = reinterpret_cast<uint4*>(vring + st * L::kTile);
+        for (int e2 = threadIdx.x - 64; e2 < L::kTile / 16; e2 += kSoftmaxThreads) {
+          uint4 u = vt[e2];
+          vt[e2] = make_uint4(pack_f16(bf16_lo(u.x), bf16_hi(u.x)), pack_f16(bf16_lo(u.y), bf16_hi(u.y)),
+                              pack_f16(bf16_lo(u.z), bf16_hi(u.z)), pack_f16(bf16_lo(u.w), bf16_hi(u.w)));
         }
         fence_proxy_async_smem();
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bar_p);
+      mbar_arrive(&bar_p[j & 1]);
     }
-    if (ok && steps > 0 && !mbar_wait(&bar_pv, (steps - 1) & 1)) ok = false;
+    if (ok && steps > 0 && !mbar_wait(&pv_done[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
     if (!ok) flag_error(p.err, kErrTimeout);
     tc_fence_after();
-    // ---------------- epilogue: O / l, LSE
+    // ---------------- epilogue: O / l (each warp of the pair writes half of
+    // the columns), LSE.
+    // The row sums go through the exchange buffer of the parity no warp of
+    // the pair reads any more.
+    xmax[steps & 1][half][row] = l;
+    mbar_arrive(pair_mb);
+    if (!mbar_wait(pair_mb, pair_uses & 1)) {
+      ok = false;
+      flag_error(p.err, kErrTimeout);
+    }
+    const float lt = l + xmax[steps & 1][half ^ 1][row];
     const bool row_valid = row < 64 || has_b;
     const int64_t grow = row_base + 128 * pair + row;
-    const float inv = l > 0.f ? 1.0f / l : 0.f;
+    const float inv = lt > 0.f ? 1.0f / lt : 0.f;
 #pragma unroll
-    for (int c = 0; c < D; c += 16) {
-      float ov[16];
-      if (steps > 0) {
-        tmem_ld16(lane_addr + kColO + c, ov);
-        tmem_wait_ld();
-      }
+    for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
+      uint32_t ov[32];
+      if (steps > 0) tmem_ld32_wait(lane_addr + kColO + c, ov);
+      float o[32];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) ov[i] = (steps > 0 && ok) ? ov[i] * inv : 0.f;
+      for (int i = 0; i < 32; ++i) o[i] = (steps > 0 && ok) ? __uint_as_float(ov[i]) * inv : 0.f;
       if (row_valid) {
-        store8(p.of, grow * D + c, ov, p.of_dtype);
-        store8(p.of, grow * D + c + 8, ov + 8, p.of_dtype);
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) store8(p.of, grow * D + c + i, o + i, p.of_dtype);
       }
     }
-    if (row_valid && p.lse) p.lse[grow] = (l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    if (half == 0 && row_valid && p.lse)
+      p.lse[grow] = (lt > 0.f) ? (m + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
   }
   tc_fence_before();
   __syncthreads();
@@ -424,9 +585,9 @@ int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_
   FwdParams p{};
   const int64_t rows = static_cast<int64_t>(BH) * N;
   int st;
-  if ((st = make_tile_map(&p.tq, qp, rows, d, f16_in)) != VSA_OK) return st;
   if ((st = make_tile_map(&p.tk, kp, rows, d, f16_in)) != VSA_OK) return st;
   if ((st = make_tile_map(&p.tv, vp, rows, d, f16_in)) != VSA_OK) return st;
+  p.q = static_cast<const uint16_t*>(qp);
   p.idx = idx;
   p.cnt = cnt;
   p.kmax = kmax;
@@ -441,9 +602,20 @@ int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_
   const int nwords = (p.Nc + 31) / 32;
   const size_t extra = sizeof(uint32_t) * (2 * kmax + 2 + 2 * nwords);
   dim3 grid(p.npairs, BH);
-  auto go = [&](auto kernel, size_t tiles) -> int {
-    const size_t smem = tiles + 1024 + extra;
-    if (smem > 227 * 1024) return VSA_ERR_UNSUPPORTED;
+  auto go = [&](auto kernel, size_t tile) -> int {
+    // Q plus as many K/V stages as fit (at most three each, at least one).
+    // The 227 KB per-block limit covers the kernel's static shared memory
+    // (barriers, row-max exchange) as well.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return VSA_ERR_CUDA;
+    const size_t kSmemMax = 227 * 1024 - fa.sharedSizeBytes;
+    const size_t fixed = 1024 + extra;
+    const long slots = fixed + 2 * tile <= kSmemMax ? static_cast<long>((kSmemMax - fixed) / tile) : 0;
+    if (slots < 2) return VSA_ERR_UNSUPPORTED;
+    p.nk = static_cast<int>(std::min<long>((slots + 1) / 2, kMaxStages));
+    p.nv = static_cast<int>(std::min<long>(slots / 2, kMaxStages));
+    // At least 120 KB, so that two CTAs (2 x 512 TMEM columns) never share an SM.
+    const size_t smem = std::max<size_t>(fixed + static_cast<size_t>(p.nk + p.nv) * tile, 120 * 1024);
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       return VSA_ERR_CUDA;
@@ -453,9 +625,11 @@ int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_
     return VSA_OK;
   };
   if (d == 128)
-    st = f16_in ? go(fine_fwd_kernel<128, true>, FwdLayout<128>::kEnd) : go(fine_fwd_kernel<128, false>, FwdLayout<128>::kEnd);
+    st = f16_in ? go(fine_fwd_kernel<128, true>, FwdLayout<128>::kTile)
+                : go(fine_fwd_kernel<128, false>, FwdLayout<128>::kTile);
   else
-    st = f16_in ? go(fine_fwd_kernel<64, true>, FwdLayout<64>::kEnd) : go(fine_fwd_kernel<64, false>, FwdLayout<64>::kEnd);
+    st = f16_in ? go(fine_fwd_kernel<64, true>, FwdLayout<64>::kTile)
+                : go(fine_fwd_kernel<64, false>, FwdLayout<64>::kTile);
   if (st != VSA_OK) return st;
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
