@@ -36,6 +36,11 @@ import synth  # noqa: E402
 
 METRIC = "VSA fwd+bwd effective TFLOPS at 32K tokens, 70% sparsity; % of bf16 tensor peak"
 UNIT = "TFLOP/s"
+# libvsa kernels launched by one forward + backward step: permute_pool,
+# coarse_topk, build_list_bits, plan_pairs, fine_fwd, combine | bwd_prep,
+# coarse_bwd_rows, coarse_atb (x2), build_inverse_bits, plan_pairs,
+# fine_bwd_kv, fine_bwd_dq, finalize.
+KERNELS_PER_STEP = 15
 WORKLOAD = "wan1.3b"
 
 
@@ -301,7 +306,7 @@ def run_ours(args, rank: int, world: int):
         "fine_bwd_effective": {"ms": round(bwd_ms, 4),
                                "tflops": round(fl["fine_bwd"] / (bwd_ms * 1e-3) / 1e12, 2)},
         "kernel_ms_per_step": per_kernel,
-        "gpu_launches": 12 * args.steps,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
         "kernel_launches_timed": launches,
         "clocks": clocks.summary(),
         "e2e": e2e,

@@ -148,7 +148,8 @@ class ForwardState:
             lse_c=view(s.lse_coarse, (BH, Nc), torch.float32),
             idx=view(s.kv_block_idx, (BH, Nc, K), torch.int32),
             cnt=view(s.valid_block_num, (BH, Nc), torch.int32),
-            of=view(s.o_fine, (BH, N, d), torch.float32), lse=view(s.lse, (BH, N), torch.float32))
+            of=view(s.o_fine, (BH, N, d), torch.float32), lse=view(s.lse, (BH, N), torch.float32),
+            tile_pairs=view(s.tile_pairs, (BH, (Nc + 1) // 2, 2), torch.int32))
 
 
 def forward(q, k, v, T: int, H: int, W: int, topk: int, g_coarse=None, g_fine=None,

@@ -49,7 +49,7 @@ class Saved(ctypes.Structure):
     """vsa_saved_t: device pointers into a forward workspace."""
 
     _fields_ = [(n, P) for n in ("qp", "kp", "vp", "qc", "kc", "vc", "o_coarse", "lse_coarse",
-                                 "kv_block_idx", "valid_block_num", "o_fine", "lse")]
+                                 "kv_block_idx", "valid_block_num", "o_fine", "lse", "tile_pairs")]
 
 
 SIGNATURES = {

@@ -104,7 +104,11 @@ int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH
                        cudaStream_t s);
 int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt,
                     int kmax, int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, int f16_in,
-                    cudaStream_t s);
+                    const int32_t* pairs, cudaStream_t s);
+size_t pair_plan_smem(int Nc);
+int launch_list_bits(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, uint32_t* bits,
+                     cudaStream_t s);
+int launch_pair_plan(const uint32_t* bits, int BH, int Nc, int32_t* pairs, cudaStream_t s);
 size_t fine_bwd_ws_bytes(int BH, int N, int kmax);
 int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* of, int of_dtype,
                     const float* lse, const void* dof, const int32_t* idx, const int32_t* cnt, int kmax, int BH,
@@ -112,7 +116,8 @@ int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* 
                     cudaStream_t s);
 int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const void* dof, const float* lse,
                          const float* delta, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
-                         float scale, float* dq, float* dk, float* dv, uint32_t* inv_ws, cudaStream_t s);
+                         float scale, float* dq, float* dk, float* dv, uint32_t* inv_ws, const int32_t* qpairs,
+                         int32_t* kpairs_ws, cudaStream_t s);
 int launch_combine(const float* oc, const float* of, const void* gc, const void* gf, void* out, int out_dtype,
                    int BH, int d, int T, int H, int W, cudaStream_t s);
 int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const float* oc, const float* of,

@@ -58,10 +58,29 @@ struct BwdParams {
   float* dq;
   float* dk;
   float* dv;
-  int N, Nc, nwords, kmax;
+  const int32_t* qpairs;        // [BH][npairs][2] query-cube tiles of the dQ kernel, or null (2t, 2t + 1)
+  const int32_t* kpairs;        // [BH][npairs][2] key-cube tiles of the dK/dV kernel, or null
+  int N, Nc, nwords, kmax, npairs;
   float scale, scale_log2;
   int* err;
 };
+
+// The two cubes of tile `t`: from a pair plan (second -1: none), else 2t and
+// 2t + 1.  A plan entry out of range latches kErrLut and leaves one cube.
+__device__ __forceinline__ void tile_cubes(const int32_t* plan, int64_t bh, int t, int npairs, int Nc, int* err,
+                                           int& a, int& b) {
+  a = 2 * t;
+  b = 2 * t + 1 < Nc ? 2 * t + 1 : -1;
+  if (plan) {
+    a = plan[(bh * npairs + t) * 2];
+    b = plan[(bh * npairs + t) * 2 + 1];
+    if (a < 0 || a >= Nc || b < -1 || b >= Nc) {
+      if (threadIdx.x == 0) flag_error(err, kErrLut);
+      a = min(max(a, 0), Nc - 1);
+      b = -1;
+    }
+  }
+}
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -172,8 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pair = blockIdx.x;
   const int64_t bh = blockIdx.y;
-  const int k1 = 2 * pair, k2 = 2 * pair + 1;
-  const bool has_k2 = k2 < p.Nc;
+  int k1, k2;
+  tile_cubes(p.kpairs, bh, pair, p.npairs, p.Nc, p.err, k1, k2);
+  const bool has_k2 = k2 >= 0;
   const int64_t row_base = bh * p.N;
 
   if (tid == 0) {
@@ -197,9 +217,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
   }
   {
     const uint32_t* ra = p.inv + (bh * p.Nc + k1) * p.nwords;
+    const uint32_t* rb = p.inv + (bh * p.Nc + (has_k2 ? k2 : k1)) * p.nwords;
     for (int w = tid; w < p.nwords; w += kThreads) {
       bitA[w] = ra[w];
-      bitB[w] = has_k2 ? ra[p.nwords + w] : 0u;
+      bitB[w] = has_k2 ? rb[w] : 0u;
     }
   }
   __syncthreads();
@@ -420,8 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pair = blockIdx.x;
   const int64_t bh = blockIdx.y;
-  const int qa = 2 * pair, qb = 2 * pair + 1;
-  const bool has_b = qb < p.Nc;
+  int qa, qb;
+  tile_cubes(p.qpairs, bh, pair, p.npairs, p.Nc, p.err, qa, qb);
+  const bool has_b = qb >= 0;
   const int64_t row_base = bh * p.N;
 
   if (tid == 0) {
@@ -444,9 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
   for (int w = tid; w < 2 * nwords; w += kThreads) bitA[w] = 0;  // bitA and bitB are contiguous
   __syncthreads();
   {
-    const int64_t rowa = bh * p.Nc + qa;
+    const int64_t rowa = bh * p.Nc + qa, rowb = bh * p.Nc + (has_b ? qb : qa);
     int ca = p.cnt ? p.cnt[rowa] : p.kmax;
-    int cb = has_b ? (p.cnt ? p.cnt[rowa + 1] : p.kmax) : 0;
+    int cb = has_b ? (p.cnt ? p.cnt[rowb] : p.kmax) : 0;
     ca = min(max(ca, 0), p.kmax);
     cb = min(max(cb, 0), p.kmax);
     if (tid == 0) {
@@ -454,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
       n_cnt[1] = cb;
     }
     const int32_t* la = p.idx + rowa * p.kmax;
-    const int32_t* lb = la + p.kmax;
+    const int32_t* lb = p.idx + rowb * p.kmax;
     for (int e = tid; e < ca + cb; e += kThreads) {
       const bool isA = e < ca;
       const int c = isA ? la[e] : lb[e - ca];
@@ -550,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t my_bit = row < 64 ? 30u : 31u;
     const bool row_valid = row < 64 || has_b;
-    const int64_t grow = row_base + 128 * pair + row;
+    const int64_t grow = row_base + 64 * static_cast<int64_t>(row < 64 ? qa : (has_b ? qb : qa)) + (row & 63);
     const float lse2 = row_valid ? p.lse[grow] * 1.4426950408889634f : 0.f;
     const float dlt = row_valid ? p.delta[grow] : 0.f;
     bool ok = true;
@@ -696,7 +718,9 @@ size_t fine_bwd_ws_bytes(int BH, int N, int kmax) {
   size_t inv = sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords;
   size_t delta = sizeof(float) * static_cast<size_t>(BH) * N;
   size_t copy = sizeof(__half) * static_cast<size_t>(BH) * N * 128;  // room for d <= 128
-  return ((inv + 255) & ~size_t(255)) + ((delta + 255) & ~size_t(255)) + 4 * ((copy + 255) & ~size_t(255));
+  size_t kpairs = sizeof(int32_t) * static_cast<size_t>(BH) * ((Nc + 1) / 2) * 2;
+  return ((inv + 255) & ~size_t(255)) + ((delta + 255) & ~size_t(255)) + 4 * ((copy + 255) & ~size_t(255)) +
+         ((kpairs + 255) & ~size_t(255));
 }
 
 int launch_delta(const void* of, int of_dtype, const void* dof, int64_t rows, int d, float* delta, cudaStream_t s) {
@@ -707,10 +731,13 @@ int launch_delta(const void* of, int of_dtype, const void* dof, int64_t rows, in
 }
 
 // Fine backward with the row statistics D given.  qp, kp, vp, dof are fp16
-// (cube order); inv_ws: scratch for the inverse-list bit matrix.
+// (cube order); inv_ws: scratch for the inverse-list bit matrix; qpairs: the
+// query-cube tiles of the dQ kernel (null: cubes 2t, 2t + 1); kpairs_ws:
+// scratch for the key-cube pair plan (null: cubes 2t, 2t + 1).
 int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const void* dof, const float* lse,
                          const float* delta, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
-                         float scale, float* dq, float* dk, float* dv, uint32_t* inv_ws, cudaStream_t s) {
+                         float scale, float* dq, float* dk, float* dv, uint32_t* inv_ws, const int32_t* qpairs,
+                         int32_t* kpairs_ws, cudaStream_t s) {
   BwdParams p{};
   const int64_t rows = static_cast<int64_t>(BH) * N;
   int st;
@@ -734,12 +761,16 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = device_error_word();
+  p.npairs = (Nc + 1) / 2;
+  p.qpairs = qpairs;
+  p.kpairs = kpairs_ws;
   const size_t inv_bytes = sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords;
   if (cudaMemsetAsync(inv_ws, 0, inv_bytes, s) != cudaSuccess) return VSA_ERR_CUDA;
   const int64_t entries = static_cast<int64_t>(BH) * Nc * kmax;
   if (entries > 0)
     build_inverse_bits<<<static_cast<unsigned>((entries + 255) / 256), 256, 0, s>>>(
         idx, cnt, kmax, Nc, nwords, static_cast<int64_t>(BH) * Nc, inv_ws, p.err);
+  if (kpairs_ws && (st = launch_pair_plan(inv_ws, BH, Nc, kpairs_ws, s)) != VSA_OK) return st;
   const size_t kv_extra = sizeof(float) * 512 + sizeof(uint32_t) * (2 * Nc + 2 + 2 * nwords);
   const size_t dq_extra = sizeof(uint32_t) * (2 * kmax + 2 + 2 * nwords);
   dim3 grid((Nc + 1) / 2, BH);
@@ -788,10 +819,11 @@ int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* 
     to_f16_kernel<<<static_cast<unsigned>(nblk < 65535 ? nblk : 65535), 256, 0, s>>>(
         static_cast<const uint4*>(srcs[i]), static_cast<uint4*>(h[i]), n8, err);
   }
+  int32_t* kpairs = reinterpret_cast<int32_t*>(w);
   int st = launch_delta(of, of_dtype, h[3], rows, d, delta, s);
   if (st != VSA_OK) return st;
   return launch_fine_bwd_core(h[0], h[1], h[2], h[3], lse, delta, idx, cnt, kmax, BH, N, d, scale, dq, dk, dv, inv_ws,
-                              s);
+                              nullptr, kpairs, s);
 }
 
 }  // namespace vsa

@@ -54,6 +54,7 @@ struct FwdParams {
   const uint16_t* q;   // [BH*N, d] fp16 / bf16, row-major
   const int32_t* idx;
   const int32_t* cnt;
+  const int32_t* pairs;  // [BH][npairs][2] tile -> query cubes (second -1: none), or null
   int kmax, N, Nc, npairs;
   int nk, nv;        // K and V ring depths (1..kMaxStages)
   float scale_log2;  // scale * log2(e)
@@ -158,8 +159,18 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pair = blockIdx.x;
   const int64_t bh = blockIdx.y;
-  const int qa = 2 * pair, qb = 2 * pair + 1;
-  const bool has_b = qb < p.Nc;
+  // The tile's two query cubes: the pair plan's, else cubes 2t and 2t + 1.
+  int qa = 2 * pair, qb = 2 * pair + 1 < p.Nc ? 2 * pair + 1 : -1;
+  if (p.pairs) {
+    qa = p.pairs[(bh * p.npairs + pair) * 2];
+    qb = p.pairs[(bh * p.npairs + pair) * 2 + 1];
+    if (qa < 0 || qa >= p.Nc || qb < -1 || qb >= p.Nc) {  // not a plan this library wrote
+      if (threadIdx.x == 0) flag_error(p.err, kErrLut);
+      qa = min(max(qa, 0), p.Nc - 1);
+      qb = -1;
+    }
+  }
+  const bool has_b = qb >= 0;
 
   // ---------------- prologue: barriers, TMEM, union of the two index lists
   if (tid == 0) {
@@ -186,9 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
   for (int w = tid; w < 2 * nwords; w += kThreads) bitA[w] = 0;  // bitA and bitB are contiguous
   __syncthreads();
   {
-    const int64_t rowa = bh * p.Nc + qa;
+    const int64_t rowa = bh * p.Nc + qa, rowb = bh * p.Nc + (has_b ? qb : qa);
     int ca = p.cnt ? p.cnt[rowa] : p.kmax;
-    int cb = has_b ? (p.cnt ? p.cnt[rowa + 1] : p.kmax) : 0;
+    int cb = has_b ? (p.cnt ? p.cnt[rowb] : p.kmax) : 0;
     if (ca < 0 || ca > p.kmax || cb < 0 || cb > p.kmax) {
       if (tid == 0) flag_error(p.err, kErrLut);
       ca = min(max(ca, 0), p.kmax);
@@ -199,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       n_cnt[1] = cb;
     }
     const int32_t* la = p.idx + rowa * p.kmax;
-    const int32_t* lb = la + p.kmax;
+    const int32_t* lb = p.idx + rowb * p.kmax;
     for (int e = tid; e < ca + cb; e += kThreads) {
       const bool isA = e < ca;
       const int c = isA ? la[e] : lb[e - ca];
@@ -218,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
     // rest of the union by increasing cube id (walked from a rotated start).
     const int ca = n_cnt[0], cb = n_cnt[1];
     const int32_t* la = p.idx + (bh * p.Nc + qa) * p.kmax;
+    const int32_t* lb = p.idx + (bh * p.Nc + (has_b ? qb : qa)) * p.kmax;
     int first[2] = {-1, -1};
     int nf = 0;
     if (ca > 0) {
@@ -225,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       if (c >= 0 && c < p.Nc) first[nf++] = c;
     }
     if (cb > 0) {
-      int c = la[p.kmax];
+      int c = lb[0];
       if (c >= 0 && c < p.Nc && (nf == 0 || c != first[0])) first[nf++] = c;
     }
     if (lane < nf) {
@@ -399,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       // Q rows into TMEM (lane = row, column c = elements 2c and 2c + 1):
       // warp (q, h) writes elements [h D/2, (h + 1) D/2) of its 32 rows.
       const bool qrow = row < 64 || has_b;
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + (row_base + 128 * pair + row) * D + half * (D / 2));
+      const int64_t qsrc = row_base + 64 * static_cast<int64_t>(row < 64 ? qa : (has_b ? qb : qa)) + (row & 63);
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + qsrc * D + half * (D / 2));
 #pragma unroll
       for (int c = 0; c < D / 4; c += 8) {
         uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
@@ -524,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
     }
     const float lt = l + xmax[steps & 1][half ^ 1][row];
     const bool row_valid = row < 64 || has_b;
-    const int64_t grow = row_base + 128 * pair + row;
+    const int64_t grow = row_base + 64 * static_cast<int64_t>(row < 64 ? qa : (has_b ? qb : qa)) + (row & 63);
     const float inv = lt > 0.f ? 1.0f / lt : 0.f;
 #pragma unroll
     for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
@@ -581,13 +594,14 @@ int make_tile_map(void* map_out, const void* base, int64_t rows, int d, int f16)
 
 int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt, int kmax,
                     int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, int f16_in,
-                    cudaStream_t s) {
+                    const int32_t* pairs, cudaStream_t s) {
   FwdParams p{};
   const int64_t rows = static_cast<int64_t>(BH) * N;
   int st;
   if ((st = make_tile_map(&p.tk, kp, rows, d, f16_in)) != VSA_OK) return st;
   if ((st = make_tile_map(&p.tv, vp, rows, d, f16_in)) != VSA_OK) return st;
   p.q = static_cast<const uint16_t*>(qp);
+  p.pairs = pairs;
   p.idx = idx;
   p.cnt = cnt;
   p.kmax = kmax;

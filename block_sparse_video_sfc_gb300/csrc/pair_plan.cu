@@ -1,0 +1,189 @@
+// pair_plan.cu -- which two 64-token cubes share a 128-row tile of the fine
+// kernels.
+//
+// The fine kernels run 128-row tensor-core tiles over pairs of cubes and walk
+// the UNION of the pair's two cube lists ("Sparse Traversal" of "VSA:
+// Accelerating Video Diffusion Inference with Sparse Attention on AMD GPUs"
+// walks one list per tile; the pairing is this implementation's, see
+// fine_fwd.cu).  The work of a tile is proportional to the size of that
+// union, so pairing cubes whose lists overlap most saves work; it changes
+// the schedule only, never a result.  Query cubes are paired by their Top-K
+// lists (forward and dQ), key cubes by their inverse lists (dK, dV).
+//
+// Heuristic (deterministic): within a window of +-kWindow cubes in curve
+// order, every unpaired cube picks the unpaired cube it shares the most list
+// entries with (ties: nearer, then lower id); mutual picks become pairs.
+// After kRounds rounds the cubes left over are paired in curve order.  On
+// the synthetic 32K-token layer this cuts the mean union from 1.63 K to
+// about 1.51 K cubes per pair (a global greedy matching reaches 1.48 K).
+#include "common.cuh"
+
+namespace vsa {
+namespace {
+
+constexpr int kWindow = 32;
+constexpr int kRounds = 8;
+constexpr int kPlanThreads = 512;
+
+// bits[bh][c][nwords] |= bit of every cube listed in row c (the lists as a
+// bit matrix; entries outside [0, Nc) are skipped, the fine kernels report them).
+__global__ void build_list_bits(const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int kmax, int Nc,
+                                int nwords, int64_t rows, uint32_t* __restrict__ bits) {
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (e >= rows * kmax) return;
+  const int64_t row = e / kmax;
+  const int slot = static_cast<int>(e % kmax);
+  int n = cnt ? cnt[row] : kmax;
+  n = min(max(n, 0), kmax);
+  if (slot >= n) return;
+  const int c = idx[e];
+  if (c < 0 || c >= Nc) return;
+  atomicOr(bits + row * nwords + (c >> 5), 1u << (c & 31));
+}
+
+// Exclusive prefix sum of one int per thread over the block; returns the
+// thread's offset, and the total in *total.
+__device__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? scratch[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += t;
+    }
+    if (lane < nwarps) scratch[lane] = wi - w;
+    if (lane == 31) scratch[32] = wi;
+  }
+  __syncthreads();
+  const int res = scratch[warp] + incl - v;
+  *total = scratch[32];
+  __syncthreads();
+  return res;
+}
+
+// One CTA per (batch, head).  Shared memory: overlap[Nc][kWindow] (uint16),
+// partner[Nc], pick[Nc], rank list[Nc] (int16).
+__global__ void __launch_bounds__(kPlanThreads) plan_pairs_kernel(const uint32_t* __restrict__ bits, int Nc, int nwords,
+                                                                  int32_t* __restrict__ pairs) {
+  extern __shared__ uint8_t smem[];
+  uint16_t* ov = reinterpret_cast<uint16_t*>(smem);  // ov[c * kWindow + d - 1] = |list c & list c+d|
+  int16_t* partner = reinterpret_cast<int16_t*>(ov + static_cast<size_t>(Nc) * kWindow);
+  int16_t* pick = partner + Nc;
+  int16_t* order = pick + Nc;
+  __shared__ int scan_scratch[33];
+  const int64_t bh = blockIdx.x;
+  const uint32_t* B = bits + bh * Nc * nwords;
+  const int tid = threadIdx.x;
+
+  for (int it = tid; it < Nc * kWindow; it += blockDim.x) {
+    const int c = it / kWindow, d = it % kWindow + 1;
+    int n = 0;
+    if (c + d < Nc) {
+      const uint32_t* a = B + static_cast<int64_t>(c) * nwords;
+      const uint32_t* b = B + static_cast<int64_t>(c + d) * nwords;
+      for (int w = 0; w < nwords; ++w) n += __popc(a[w] & b[w]);
+    }
+    ov[it] = static_cast<uint16_t>(n);
+  }
+  for (int c = tid; c < Nc; c += blockDim.x) partner[c] = -1;
+  __syncthreads();
+
+  auto overlap = [&](int c, int b) -> int {
+    return c < b ? ov[c * kWindow + (b - c - 1)] : ov[b * kWindow + (c - b - 1)];
+  };
+  for (int round = 0; round < kRounds; ++round) {
+    for (int c = tid; c < Nc; c += blockDim.x) {
+      int best = -1, best_ov = -1, best_dist = 0;
+      if (partner[c] < 0) {
+        const int lo = max(0, c - kWindow), hi = min(Nc - 1, c + kWindow);
+        for (int b = lo; b <= hi; ++b) {
+          if (b == c || partner[b] >= 0) continue;
+          const int o = overlap(c, b), dist = abs(b - c);
+          if (o > best_ov || (o == best_ov && dist < best_dist)) {  // scanning b upward keeps the lower id on a full tie
+            best = b;
+            best_ov = o;
+            best_dist = dist;
+          }
+        }
+      }
+      pick[c] = static_cast<int16_t>(best);
+    }
+    __syncthreads();
+    for (int c = tid; c < Nc; c += blockDim.x) {
+      const int b = pick[c];
+      if (partner[c] < 0 && b >= 0 && pick[b] == c) partner[c] = static_cast<int16_t>(b);
+    }
+    __syncthreads();
+  }
+
+  // Cubes still unpaired: pair them in curve order (a lone cube when the count is odd).
+  const int per = (Nc + blockDim.x - 1) / blockDim.x;
+  const int c0 = tid * per, c1 = min(Nc, c0 + per);
+  int mine = 0;
+  for (int c = c0; c < c1; ++c) mine += partner[c] < 0;
+  int nleft = 0;
+  int r = block_exclusive_scan(mine, scan_scratch, &nleft);
+  for (int c = c0; c < c1; ++c)
+    if (partner[c] < 0) order[r++] = static_cast<int16_t>(c);
+  __syncthreads();
+  for (int i = tid; 2 * i + 1 < nleft; i += blockDim.x) {
+    partner[order[2 * i]] = order[2 * i + 1];
+    partner[order[2 * i + 1]] = order[2 * i];
+  }
+  __syncthreads();
+
+  // One tile per pair, listed by the pair's lower cube (curve order).
+  const int lone = (nleft & 1) ? order[nleft - 1] : -1;
+  mine = 0;
+  for (int c = c0; c < c1; ++c) mine += (partner[c] > c) || (c == lone);
+  int total = 0;
+  r = block_exclusive_scan(mine, scan_scratch, &total);
+  const int npairs = (Nc + 1) / 2;
+  int32_t* out = pairs + bh * npairs * 2;
+  for (int c = c0; c < c1; ++c) {
+    if (partner[c] > c || c == lone) {
+      out[2 * r] = c;
+      out[2 * r + 1] = c == lone ? -1 : partner[c];
+      ++r;
+    }
+  }
+}
+
+}  // namespace
+
+size_t pair_plan_smem(int Nc) { return static_cast<size_t>(Nc) * (kWindow * 2 + 3 * 2); }
+
+int launch_list_bits(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, uint32_t* bits,
+                     cudaStream_t s) {
+  const int nwords = (Nc + 31) / 32;
+  if (cudaMemsetAsync(bits, 0, sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  const int64_t rows = static_cast<int64_t>(BH) * Nc, entries = rows * kmax;
+  if (entries > 0)
+    build_list_bits<<<static_cast<unsigned>((entries + 255) / 256), 256, 0, s>>>(idx, cnt, kmax, Nc, nwords, rows,
+                                                                                    bits);
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
+int launch_pair_plan(const uint32_t* bits, int BH, int Nc, int32_t* pairs, cudaStream_t s) {
+  if (Nc > 32767) return VSA_ERR_UNSUPPORTED;
+  const size_t smem = pair_plan_smem(Nc);
+  if (smem > 200 * 1024) return VSA_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(plan_pairs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return VSA_ERR_CUDA;
+  plan_pairs_kernel<<<BH, kPlanThreads, smem, s>>>(bits, Nc, (Nc + 31) / 32, pairs);
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
+}  // namespace vsa

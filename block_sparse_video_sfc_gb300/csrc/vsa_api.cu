@@ -38,7 +38,7 @@ int check_grid(const vsa_grid_t& g, int d, Dims* out, int64_t BH) {
 
 // Forward workspace: the saved state of one vsa_forward call.
 struct FwdWs {
-  size_t qp, kp, vp, qc, kc, vc, oc, lsec, idx, cnt, of, lse, total;
+  size_t qp, kp, vp, qc, kc, vc, oc, lsec, idx, cnt, of, lse, lbits, pairs, total;
 };
 FwdWs fwd_layout(const Dims& D, int K) {
   FwdWs w{};
@@ -57,13 +57,15 @@ FwdWs fwd_layout(const Dims& D, int K) {
   w.cnt = o; o += align256(sizeof(int32_t) * D.BH * D.Nc);
   w.of = o; o += align256(sizeof(float) * D.BH * D.N * D.d);
   w.lse = o; o += align256(sizeof(float) * D.BH * D.N);
+  w.lbits = o; o += align256(sizeof(uint32_t) * D.BH * D.Nc * ((D.Nc + 31) / 32));
+  w.pairs = o; o += align256(sizeof(int32_t) * D.BH * ((D.Nc + 1) / 2) * 2);
   w.total = o;
   return w;
 }
 
 // Backward workspace (scratch of one vsa_backward call).
 struct BwdWs {
-  size_t dof, delta, doc, P, dS, dqc, dkc, dvc, dqp, dkp, dvp, inv, total;
+  size_t dof, delta, doc, P, dS, dqc, dkc, dvc, dqp, dkp, dvp, inv, kpairs, total;
 };
 BwdWs bwd_layout(const Dims& D) {
   BwdWs w{};
@@ -83,6 +85,7 @@ BwdWs bwd_layout(const Dims& D) {
   w.dkp = o; o += align256(big_f32);
   w.dvp = o; o += align256(big_f32);
   w.inv = o; o += align256(sizeof(uint32_t) * D.BH * D.Nc * nwords);
+  w.kpairs = o; o += align256(sizeof(int32_t) * D.BH * ((D.Nc + 1) / 2) * 2);
   w.total = o;
   return w;
 }
@@ -253,7 +256,7 @@ int vsa_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* 
   if (!o_fine || !aligned16(o_fine)) return VSA_ERR_ARG;
   if (o_dtype != VSA_DTYPE_BF16 && o_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
   return launch_fine_fwd(qp, kp, vp, kv_block_idx, valid_block_num, max_kv_blocks, BH, N, d, scale, o_fine, o_dtype,
-                         lse, 0, as_stream(stream));
+                         lse, 0, nullptr, as_stream(stream));
 }
 
 int vsa_fine_bwd(const void* qp, const void* kp, const void* vp, const void* o_fine, int o_dtype, const float* lse,
@@ -302,6 +305,7 @@ int vsa_forward_saved(const void* fwd_ws, int B, int heads, int d, vsa_grid_t g,
   out->valid_block_num = at<int32_t>(fwd_ws, w.cnt);
   out->o_fine = at<float>(fwd_ws, w.of);
   out->lse = at<float>(fwd_ws, w.lse);
+  out->tile_pairs = at<int32_t>(fwd_ws, w.pairs);
   return VSA_OK;
 }
 
@@ -330,8 +334,14 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
                                at<float>(ws, w.lsec), at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), nullptr, s)) !=
       VSA_OK)
     return st;
+  // Pair query cubes whose lists overlap most into the fine kernels' tiles.
+  if ((st = launch_list_bits(at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), topk, BH, Nc, at<uint32_t>(ws, w.lbits),
+                             s)) != VSA_OK)
+    return st;
+  if ((st = launch_pair_plan(at<uint32_t>(ws, w.lbits), BH, Nc, at<int32_t>(ws, w.pairs), s)) != VSA_OK) return st;
   if ((st = launch_fine_fwd(dst[0], dst[1], dst[2], at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), topk, BH, N, d,
-                            scale, at<float>(ws, w.of), VSA_DTYPE_F32, at<float>(ws, w.lse), 1, s)) != VSA_OK)
+                            scale, at<float>(ws, w.of), VSA_DTYPE_F32, at<float>(ws, w.lse), 1,
+                            at<int32_t>(ws, w.pairs), s)) != VSA_OK)
     return st;
   return launch_combine(at<float>(ws, w.oc), at<float>(ws, w.of), g_coarse, g_fine, out, out_dtype, BH, d, g.T, g.H,
                         g.W, s);
@@ -370,7 +380,8 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
                                  at<void>(ws, w.dof), at<float>(fwd_ws, f.lse), at<float>(ws, w.delta),
                                  at<int32_t>(fwd_ws, f.idx), at<int32_t>(fwd_ws, f.cnt), topk, BH, N, d, scale,
                                  at<float>(ws, w.dqp), at<float>(ws, w.dkp), at<float>(ws, w.dvp),
-                                 at<uint32_t>(ws, w.inv), s)) != VSA_OK)
+                                 at<uint32_t>(ws, w.inv), at<int32_t>(fwd_ws, f.pairs), at<int32_t>(ws, w.kpairs),
+                                 s)) != VSA_OK)
     return st;
   return launch_finalize(at<float>(ws, w.dqp), at<float>(ws, w.dkp), at<float>(ws, w.dvp), at<float>(ws, w.dqc),
                          at<float>(ws, w.dkc), at<float>(ws, w.dvc), dq, dk, dv, grad_dtype, BH, d, g.T, g.H, g.W, s);

@@ -220,6 +220,8 @@ typedef struct {
     int32_t* valid_block_num; /* [BH, Nc] */
     float* o_fine;     /* fp32 [BH, N, d] cube order */
     float* lse;        /* fp32 [BH, N] */
+    int32_t* tile_pairs; /* [BH, (Nc + 1) / 2, 2] query cubes of each fine-kernel tile
+                            (second -1: a lone cube); a scheduling choice, not a result */
 } vsa_saved_t;
 
 int vsa_forward_saved(const void* fwd_ws, int B, int heads, int d, vsa_grid_t g, int topk, vsa_saved_t* out);

@@ -310,3 +310,27 @@ def test_full_size_sampled(vsa, oracle_mod, name, dtype):
     """The 32K-token sparsity sweep (K = 512, 256, 64 of 512 cubes), the
     40-head Wan-14B-shaped layer and the 122880-token long video, at full size."""
     _sampled_checks(vsa, oracle_mod, synth.WORKLOADS[name], dtype)
+
+
+@pytest.mark.parametrize("name", ["small", "wan1.3b"])
+def test_tile_pairs_partition(vsa, oracle_mod, name):
+    """The query-cube pairing of the fine kernels' tiles (a scheduling choice):
+    every cube in exactly one tile, and the pairing never walks more list
+    entries in total than pairing cubes 2t and 2t + 1 would."""
+    wl = synth.WORKLOADS[name]
+    heads = [0, wl.heads - 1]
+    q, k, v = (dev(a) for a in synth.make_qkv(wl, heads_subset=heads))
+    out, st = vsa.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, out_dtype=torch.float32)
+    status_ok(vsa)
+    sv = st.saved()
+    pairs = sv["tile_pairs"].cpu().numpy()
+    idx = sv["idx"].cpu().numpy()
+    for h in range(len(heads)):
+        cubes = pairs[h].reshape(-1)
+        assert (cubes == -1).sum() == wl.Nc % 2
+        assert np.array_equal(np.sort(cubes[cubes >= 0]), np.arange(wl.Nc))
+        sets = [set(r) for r in idx[h]]
+        plan = sum(len(sets[a] | (sets[b] if b >= 0 else set())) for a, b in pairs[h])
+        adjacent = sum(len(sets[2 * t] | (sets[2 * t + 1] if 2 * t + 1 < wl.Nc else set()))
+                       for t in range((wl.Nc + 1) // 2))
+        assert plan <= adjacent, (plan, adjacent)
