@@ -160,31 +160,47 @@ __device__ __forceinline__ void mma_tmem_x_rows(uint32_t dtm, uint32_t atm, cons
 }
 
 // =============================================================== dK, dV
+// One CTA per pair of key cubes (128 key rows, K and V resident in shared
+// memory); it walks the union of the two cubes' inverse lists ONE query cube
+// (64 queries) per step:
+//   S^T = K Q^T, dP^T = V dO^T       (M = 128 keys, N = 64 queries, SS)
+//   P^T = exp2(S^T scale - LSE), dS^T = P^T (dP^T - D)   compute warps
+//   dV += P^T dO, dK += dS^T Q       (A from TMEM, N = d)
+// With 64-query steps the Q / dO stages are 16 KB each, so the rings are
+// four deep (the loads of a step start four steps ahead), and S^T / dP^T are
+// double-buffered in TMEM, so S^T(j+1), dP^T(j+1) and dV(j-1), dK(j-1) run
+// while the compute warps work on step j.  N = 64 SS products run at about
+// two thirds of the full rate (shared-memory operand bandwidth); overlap buys
+// more than that costs.
+constexpr int kKvStages = 4;
 template <int D>
 struct KvLayout {
-  static constexpr int kTile = 128 * D * 2;
-  static constexpr int kK = 0, kV = kTile, kQ = 2 * kTile, kDO = 4 * kTile;  // Q, dO: 2 stages each
-  static constexpr int kEnd = 6 * kTile;
+  static constexpr int kTileK = 128 * D * 2;  // K or V: 128 key rows
+  static constexpr int kTileQ = 64 * D * 2;   // Q or dO of one query cube
+  static constexpr int kK = 0, kV = kTileK, kRing = 2 * kTileK;
+  static constexpr int kStage = 2 * kTileQ;   // Q, then dO
+  static constexpr int kStats = kRing + kKvStages * kStage;  // [stage][LSE 64 | D 64] fp32
+  static constexpr int kEnd = kStats + kKvStages * 512;
 };
-constexpr uint32_t kKvS = 0, kKvP = 0, kKvDP = 128, kKvDS = 128, kKvDV = 256, kKvDK = 384;
+// TMEM: S^T buffers 0 / 64, dP^T buffers 128 / 192 (64 columns each; P^T and
+// dS^T overwrite them as fp16 pairs), dV 256, dK 384.
+constexpr uint32_t kKvS = 0, kKvDP = 128, kKvDV = 256, kKvDK = 384;
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using L = KvLayout<D>;
-  float* s_lse = reinterpret_cast<float*>(sm + L::kEnd);  // [2][128]
-  float* s_del = s_lse + 256;                              // [2][128]
-  uint32_t* ulist = reinterpret_cast<uint32_t*>(s_del + 256);
+  uint32_t* ulist = reinterpret_cast<uint32_t*>(sm + L::kEnd);
   uint32_t* bitA = ulist + 2 * p.Nc + 2;
   uint32_t* bitB = bitA + p.nwords;
 
-  // bar_qld / bar_dold [s]: Q / dO stage s filled; bar_qfree / bar_dofree [s]:
-  // dK / dV of the step using stage s done.  Per step: bar_s (S^T done), bar_dp
-  // (dP^T done), bar_pds (P^T and dS^T written, all compute threads), bar_dv /
-  // bar_dk (dV / dK done).
-  __shared__ uint64_t bar_kv, bar_qld[2], bar_dold[2], bar_qfree[2], bar_dofree[2];
-  __shared__ uint64_t bar_s, bar_dp, bar_pds, bar_dv, bar_dk;
+  // full[s]: Q, dO, LSE and D of the step in stage s landed; stage_free[s]:
+  // dV and dK of that step completed.  s_done[b]: S^T and dP^T into buffer b
+  // done; pds[b]: P^T and dS^T written into buffer b (all compute threads);
+  // buf_free[b]: dV and dK that read buffer b completed.  Every parity wait
+  // targets a barrier in the awaited phase or the one after it.
+  __shared__ uint64_t bar_kv, full[kKvStages], stage_free[kKvStages], s_done[2], pds[2], buf_free[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int n_union;
 
@@ -198,17 +214,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
 
   if (tid == 0) {
     mbar_init(&bar_kv, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_qld[i], 1);
-      mbar_init(&bar_dold[i], 1);
-      mbar_init(&bar_qfree[i], 1);
-      mbar_init(&bar_dofree[i], 1);
+    for (int i = 0; i < kKvStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&stage_free[i], 1);
     }
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_dp, 1);
-    mbar_init(&bar_pds, kCompute);
-    mbar_init(&bar_dv, 1);
-    mbar_init(&bar_dk, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_done[i], 1);
+      mbar_init(&pds[i], kCompute);
+      mbar_init(&buf_free[i], 1);
+    }
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -232,152 +246,149 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const int U = n_union;
-  const int steps = (U + 1) >> 1;
-  auto qcube = [&](int j, int g) -> int {
-    const int e = (g == 1 && 2 * j + 1 < U) ? 2 * j + 1 : 2 * j;
-    return static_cast<int>(ulist[e] & 0x3FFFFFFF);
-  };
+  const int steps = n_union;  // one query cube per step
 
   if (warp == 0) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer: K, V once; then per step the query cube's
+    // Q and dO tiles and its 64 LSE and D values into stage j % 4.
     if (lane == 0 && steps > 0) {
-      mbar_expect_tx(&bar_kv, 2 * L::kTile);
+      mbar_expect_tx(&bar_kv, 2 * L::kTileK);
       const int c1 = has_k2 ? k2 : k1;
       load_cube_pair<D>(sm + L::kK, &p.tk, &bar_kv, row_base, k1, c1);
       load_cube_pair<D>(sm + L::kV, &p.tv, &bar_kv, row_base, k1, c1);
       for (int j = 0; j < steps; ++j) {
-        const int s = j & 1;
-        const int q0 = qcube(j, 0), q1 = qcube(j, 1);
-        if (j >= 2 && !mbar_wait(&bar_qfree[s], ((j >> 1) - 1) & 1)) {
+        const int st = j & (kKvStages - 1);
+        if (j >= kKvStages && !mbar_wait(&stage_free[st], ((j / kKvStages) - 1) & 1)) {
           flag_error(p.err, kErrTimeout);
           break;
         }
-        mbar_expect_tx(&bar_qld[s], L::kTile);
-        load_cube_pair<D>(sm + L::kQ + s * L::kTile, &p.tq, &bar_qld[s], row_base, q0, q1);
-        if (j >= 2 && !mbar_wait(&bar_dofree[s], ((j >> 1) - 1) & 1)) {
-          flag_error(p.err, kErrTimeout);
-          break;
+        const int q = static_cast<int>(ulist[j] & 0x3FFFFFFF);
+        const int64_t qrow = row_base + 64 * static_cast<int64_t>(q);
+        uint8_t* stage = sm + L::kRing + st * L::kStage;
+        float* stats = reinterpret_cast<float*>(sm + L::kStats + st * 512);
+        mbar_expect_tx(&full[st], L::kStage + 512);
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b) {
+          tma_load_2d(stage + b * 8192, &p.tq, &full[st], 64 * b, static_cast<int>(qrow));
+          tma_load_2d(stage + L::kTileQ + b * 8192, &p.tdo, &full[st], 64 * b, static_cast<int>(qrow));
         }
-        mbar_expect_tx(&bar_dold[s], L::kTile);
-        load_cube_pair<D>(sm + L::kDO + s * L::kTile, &p.tdo, &bar_dold[s], row_base, q0, q1);
+        bulk_load(stats, p.lse + qrow, 256, &full[st]);
+        bulk_load(stats + 64, p.delta + qrow, 256, &full[st]);
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer: S^T(0), dP^T(0), then per step j
-    //   [P^T, dS^T (j)] dV(j), dK(j), [dV(j) done] S^T(j+1), [dK(j) done] dP^T(j+1)
+    // ---------------- MMA issuer.  S^T(0), S^T(1) (each with its dP^T), then
+    // per step j: dV(j), dK(j) once P^T / dS^T(j) are written; S^T(j+2) into
+    // the same buffer once dV(j) and dK(j) have read it.
     if (lane == 0 && steps > 0) {
-      bool ok = mbar_wait(&bar_kv, 0) && mbar_wait(&bar_qld[0], 0);
-      if (ok) {
+      constexpr uint32_t idesc_s = idesc_f32acc(128, 64, 0, 0, 1);
+      constexpr uint32_t idesc_g = idesc_f32acc(128, D, 0, 1, 1);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & (kKvStages - 1), b = j & 1;
+        if (!mbar_spin(&full[st], (j / kKvStages) & 1)) return false;
         tc_fence_after();
-        mma_rows_x_rows<D>(tmem + kKvS, sm + L::kK, sm + L::kQ);
-        mma_commit(&bar_s);
-      }
-      ok = ok && mbar_wait(&bar_dold[0], 0);
-      if (ok) {
+        const uint8_t* qt = sm + L::kRing + st * L::kStage;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int blk = kk >> 2, w = kk & 3;
+          mma_ss(tmem + kKvS + 64 * b, sdesc_sw128(smem_u32(sm + L::kK + blk * 16384 + w * 32), 16, 1024),
+                 sdesc_sw128(smem_u32(qt + blk * 8192 + w * 32), 16, 1024), idesc_s, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int blk = kk >> 2, w = kk & 3;
+          mma_ss(tmem + kKvDP + 64 * b, sdesc_sw128(smem_u32(sm + L::kV + blk * 16384 + w * 32), 16, 1024),
+                 sdesc_sw128(smem_u32(qt + L::kTileQ + blk * 8192 + w * 32), 16, 1024), idesc_s, kk > 0);
+        }
+        mma_commit(&s_done[b]);
+        return true;
+      };
+      bool ok = mbar_spin(&bar_kv, 0) && issue_s(0) && (steps < 2 || issue_s(1));
+      for (int j = 0; ok && j < steps; ++j) {
+        const int st = j & (kKvStages - 1), b = j & 1;
+        if (!mbar_spin(&pds[b], (j >> 1) & 1)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        mma_rows_x_rows<D>(tmem + kKvDP, sm + L::kV, sm + L::kDO);
-        mma_commit(&bar_dp);
-      }
-      for (int j = 0; j < steps && ok; ++j) {
-        const int s = j & 1, sn = (j + 1) & 1;
-        ok = ok && mbar_wait(&bar_pds, j & 1);
-        if (!ok) break;
-        tc_fence_after();
-        mma_tmem_x_rows<D>(tmem + kKvDV, tmem + kKvP, sm + L::kDO + s * L::kTile, j > 0);
-        mma_commit(&bar_dofree[s]);
-        mma_commit(&bar_dv);
-        mma_tmem_x_rows<D>(tmem + kKvDK, tmem + kKvDS, sm + L::kQ + s * L::kTile, j > 0);
-        mma_commit(&bar_qfree[s]);
-        mma_commit(&bar_dk);
-        if (j + 1 < steps) {
-          ok = ok && mbar_wait(&bar_qld[sn], ((j + 1) >> 1) & 1) && mbar_wait(&bar_dv, j & 1);
-          if (!ok) break;
-          tc_fence_after();
-          mma_rows_x_rows<D>(tmem + kKvS, sm + L::kK, sm + L::kQ + sn * L::kTile);
-          mma_commit(&bar_s);
-          ok = ok && mbar_wait(&bar_dold[sn], ((j + 1) >> 1) & 1) && mbar_wait(&bar_dk, j & 1);
-          if (!ok) break;
-          tc_fence_after();
-          mma_rows_x_rows<D>(tmem + kKvDP, sm + L::kV, sm + L::kDO + sn * L::kTile);
-          mma_commit(&bar_dp);
+        const uint8_t* qt = sm + L::kRing + st * L::kStage;
+        // A = P^T / dS^T (K = 64 queries in 4 steps of 16: warpgroup g's 16
+        // packed columns sit at 32 g of the buffer), B = dO / Q (MN-major).
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + kKvDV, tmem + kKvS + 64 * b + (kk >> 1) * 32 + (kk & 1) * 8,
+                 sdesc_sw128(smem_u32(qt + L::kTileQ + kk * 2048), 8192, 1024), idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + kKvDK, tmem + kKvDP + 64 * b + (kk >> 1) * 32 + (kk & 1) * 8,
+                 sdesc_sw128(smem_u32(qt + kk * 2048), 8192, 1024), idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&stage_free[st]);
+        mma_commit(&buf_free[b]);
+        if (j + 2 < steps) {
+          if (!mbar_spin(&buf_free[b], (j >> 1) & 1) || !issue_s(j + 2)) {
+            ok = false;
+            break;
+          }
         }
       }
       if (!ok) flag_error(p.err, kErrTimeout);
     }
   } else {
-    // ---------------- compute warps: warpgroup g takes query cube g of each
-    // step (TMEM columns 64g..64g+63); thread = key row r (TMEM lane).
+    // ---------------- compute warps: thread = key row r (TMEM lane);
+    // warpgroup g takes query columns [32 g, 32 g + 32) of each step.
     const int quarter = warp & 3;
     const int g = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
-    const int ct = tid - 64;  // 0..255
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t key_bit = r < 64 ? 30u : 31u;
+    const uint32_t key_bit = r < 64 ? 30u : 31u;  // warp-uniform
     bool ok = true;
-    float pf_lse = 0.f, pf_del = 0.f;
-    auto prefetch = [&](int j) {
-      if (ct < 128) {
-        const int64_t qrow = row_base + 64 * static_cast<int64_t>(qcube(j, ct >> 6)) + (ct & 63);
-        pf_lse = p.lse[qrow] * 1.4426950408889634f;
-        pf_del = p.delta[qrow];
-      }
-    };
-    if (steps > 0) prefetch(0);
     for (int j = 0; j < steps; ++j) {
-      const bool has1 = 2 * j + 1 < U;
-      const uint32_t e = (g == 0) ? ulist[2 * j] : (has1 ? ulist[2 * j + 1] : 0u);
-      const bool valid = (g == 0 || has1) && ((e >> key_bit) & 1u) != 0;
-      const bool any = __any_sync(0xffffffffu, valid);
-      float* lse2 = s_lse + (j & 1) * 128 + 64 * g;
-      float* del = s_del + (j & 1) * 128 + 64 * g;
-      if (ct < 128) {
-        s_lse[(j & 1) * 128 + ct] = pf_lse;
-        s_del[(j & 1) * 128 + ct] = pf_del;
-      }
-      named_bar_sync(1, kCompute);
-      if (j + 1 < steps) prefetch(j + 1);
-      // ---- P^T = exp2(S^T * scale - LSE) and dS^T = P^T (dP^T - D), 16 query
-      // columns at a time; both packed fp16 into this warpgroup's own half of
-      // the S^T / dP^T columns (chunk c lands on columns already read).
-      if (!mbar_wait(&bar_s, j & 1) || !mbar_wait(&bar_dp, j & 1)) {
+      const int st = j & (kKvStages - 1), b = j & 1;
+      // The stage's LSE / D are read from shared memory: wait for its fill
+      // too (it has landed once S^T(j) is done, but this makes it visible).
+      if (!mbar_spin(&s_done[b], (j >> 1) & 1) || !mbar_spin(&full[st], (j / kKvStages) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-#pragma unroll 1
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        uint32_t pk[8], dk[8];
-        if (any) {
-          float sv[16], dv[16];
-          tmem_ld16(lane_addr + kKvS + 64 * g + c0, sv);
-          tmem_ld16(lane_addr + kKvDP + 64 * g + c0, dv);
-          tmem_wait_ld();
+      const bool valid = ((ulist[j] >> key_bit) & 1u) != 0;
+      const float* lse = reinterpret_cast<const float*>(sm + L::kStats + st * 512) + 32 * g;
+      const float* dlt = lse + 64;
+      uint32_t pk[16], dk[16];
+      if (valid) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32_wait(lane_addr + kKvS + 64 * b + 32 * g, sv);
+        tmem_ld32_wait(lane_addr + kKvDP + 64 * b + 32 * g, dv);
 #pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c0 + i);
-            const float4 d4 = *reinterpret_cast<const float4*>(del + c0 + i);
-            const float p0 = valid ? fast_exp2(fmaf(sv[i], p.scale_log2, -l4.x)) : 0.f;
-            const float p1 = valid ? fast_exp2(fmaf(sv[i + 1], p.scale_log2, -l4.y)) : 0.f;
-            const float p2 = valid ? fast_exp2(fmaf(sv[i + 2], p.scale_log2, -l4.z)) : 0.f;
-            const float p3 = valid ? fast_exp2(fmaf(sv[i + 3], p.scale_log2, -l4.w)) : 0.f;
-            pk[i >> 1] = pack_f16(p0, p1);
-            pk[(i >> 1) + 1] = pack_f16(p2, p3);
-            dk[i >> 1] = pack_f16(p0 * (dv[i] - d4.x), p1 * (dv[i + 1] - d4.y));
-            dk[(i >> 1) + 1] = pack_f16(p2 * (dv[i + 2] - d4.z), p3 * (dv[i + 3] - d4.w));
+        for (int c = 0; c < 32; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse + c);
+          const float4 d4 = *reinterpret_cast<const float4*>(dlt + c);
+          const float l[4] = {l4.x, l4.y, l4.z, l4.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pr[4], ds[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            pr[i] = fast_exp2(fmaf(__uint_as_float(sv[c + i]), p.scale_log2, -l[i] * 1.4426950408889634f));
+            ds[i] = pr[i] * (__uint_as_float(dv[c + i]) - dd[i]);
           }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) pk[i] = dk[i] = 0u;
+          pk[c >> 1] = pack_f16(pr[0], pr[1]);
+          pk[(c >> 1) + 1] = pack_f16(pr[2], pr[3]);
+          dk[c >> 1] = pack_f16(ds[0], ds[1]);
+          dk[(c >> 1) + 1] = pack_f16(ds[2], ds[3]);
         }
-        tmem_st8(lane_addr + kKvP + 64 * g + (c0 >> 1), pk);
-        tmem_st8(lane_addr + kKvDS + 64 * g + (c0 >> 1), dk);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = dk[i] = 0u;
       }
+      // Packed over the first half of this warpgroup's own columns (already read).
+      tmem_st8(lane_addr + kKvS + 64 * b + 32 * g, pk);
+      tmem_st8(lane_addr + kKvS + 64 * b + 32 * g + 8, pk + 8);
+      tmem_st8(lane_addr + kKvDP + 64 * b + 32 * g, dk);
+      tmem_st8(lane_addr + kKvDP + 64 * b + 32 * g + 8, dk + 8);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bar_pds);
+      mbar_arrive(&pds[b]);
     }
-    if (ok && steps > 0 && !mbar_wait(&bar_dk, (steps - 1) & 1)) ok = false;
+    if (ok && steps > 0 && !mbar_spin(&buf_free[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
     if (!ok) flag_error(p.err, kErrTimeout);
     tc_fence_after();
     // ---------------- dK, dV rows of this key pair (warpgroup 0: dV, 1: dK)
@@ -387,20 +398,20 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
     float* outp = g == 0 ? p.dv : p.dk;
     const float mul = g == 0 ? 1.0f : p.scale;
 #pragma unroll
-    for (int c = 0; c < D; c += 16) {
-      float a[16];
+    for (int c = 0; c < D; c += 32) {
+      uint32_t a[32];
       if (steps > 0 && ok) {
-        tmem_ld16(lane_addr + (g == 0 ? kKvDV : kKvDK) + c, a);
-        tmem_wait_ld();
+        tmem_ld32_wait(lane_addr + (g == 0 ? kKvDV : kKvDK) + c, a);
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) a[i] = 0.f;
+        for (int i = 0; i < 32; ++i) a[i] = 0u;
       }
+      float o[32];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) a[i] *= mul;
+      for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(a[i]) * mul;
       if (key_valid) {
-        store8(outp, krow * D + c, a, VSA_DTYPE_F32);
-        store8(outp, krow * D + c + 8, a + 8, VSA_DTYPE_F32);
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) store8(outp, krow * D + c + i, o + i, VSA_DTYPE_F32);
       }
     }
   }
@@ -771,7 +782,7 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
     build_inverse_bits<<<static_cast<unsigned>((entries + 255) / 256), 256, 0, s>>>(
         idx, cnt, kmax, Nc, nwords, static_cast<int64_t>(BH) * Nc, inv_ws, p.err);
   if (kpairs_ws && (st = launch_pair_plan(inv_ws, BH, Nc, kpairs_ws, s)) != VSA_OK) return st;
-  const size_t kv_extra = sizeof(float) * 512 + sizeof(uint32_t) * (2 * Nc + 2 + 2 * nwords);
+  const size_t kv_extra = sizeof(uint32_t) * (2 * Nc + 2 + 2 * nwords);
   const size_t dq_extra = sizeof(uint32_t) * (2 * kmax + 2 + 2 * nwords);
   dim3 grid((Nc + 1) / 2, BH);
   auto go = [&](auto kernel, size_t bytes) -> int {

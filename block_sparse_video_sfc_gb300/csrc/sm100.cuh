@@ -101,6 +101,14 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const 
       "r"(smem_u32(smem_src)), "r"(x), "r"(y)
       : "memory");
 }
+// Plain (untiled) bulk copy global -> shared, completing on an mbarrier.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N bulk groups still read their shared-memory source.
 template <int N>

@@ -266,7 +266,8 @@ int vsa_fine_bwd(const void* qp, const void* kp, const void* vp, const void* o_f
   int st = check_fine(qp, kp, vp, kv_block_idx, max_kv_blocks, BH, N, d);
   if (st != VSA_OK) return st;
   if (!o_fine || !lse || !do_fine || !dq || !dk || !dv) return VSA_ERR_ARG;
-  if (!aligned16(o_fine) || !aligned16(do_fine) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+  if (!aligned16(o_fine) || !aligned16(lse) || !aligned16(do_fine) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dv))
     return VSA_ERR_ARG;
   if (o_dtype != VSA_DTYPE_BF16 && o_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
   return launch_fine_bwd(qp, kp, vp, o_fine, o_dtype, lse, do_fine, kv_block_idx, valid_block_num, max_kv_blocks,

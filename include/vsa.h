@@ -130,6 +130,7 @@ int vsa_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* 
  *               the forward call.
  *   o_fine      [BH, N, d] the forward output (dtype o_dtype), lse fp32 [BH, N].
  *   do_fine     bf16 [BH, N, d]: dL/dO_f in cube order.
+ *   Every pointer 16-byte aligned (VSA_ERR_ARG otherwise).
  *   dq, dk, dv  fp32 [BH, N, d] in cube order (overwritten).
  *   ws          workspace of vsa_workspace_bytes(VSA_OP_FINE_BWD, ...) bytes.
  */
