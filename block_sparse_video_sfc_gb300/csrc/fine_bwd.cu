@@ -167,11 +167,12 @@ __device__ __forceinline__ void mma_tmem_x_rows(uint32_t dtm, uint32_t atm, cons
 //   P^T = exp2(S^T scale - LSE), dS^T = P^T (dP^T - D)   compute warps
 //   dV += P^T dO, dK += dS^T Q       (A from TMEM, N = d)
 // With 64-query steps the Q / dO stages are 16 KB each, so the rings are
-// four deep (the loads of a step start four steps ahead), and S^T / dP^T are
-// double-buffered in TMEM, so S^T(j+1), dP^T(j+1) and dV(j-1), dK(j-1) run
-// while the compute warps work on step j.  N = 64 SS products run at about
-// two thirds of the full rate (shared-memory operand bandwidth); overlap buys
-// more than that costs.
+// four deep (the loads of a step start four steps ahead).  S^T / dP^T are
+// released as soon as the compute warps have read them into registers, and
+// P^T / dS^T go to one of two separate buffers, so S^T(j+1) and dV(j-1),
+// dK(j-1) run while the compute warps work on step j and the tensor pipe
+// never drains between steps.  N = 64 SS products run at about two thirds
+// of the full rate (shared-memory operand bandwidth); the overlap buys more.
 constexpr int kKvStages = 4;
 template <int D>
 struct KvLayout {
@@ -182,9 +183,9 @@ struct KvLayout {
   static constexpr int kStats = kRing + kKvStages * kStage;  // [stage][LSE 64 | D 64] fp32
   static constexpr int kEnd = kStats + kKvStages * 512;
 };
-// TMEM: S^T buffers 0 / 64, dP^T buffers 128 / 192 (64 columns each; P^T and
-// dS^T overwrite them as fp16 pairs), dV 256, dK 384.
-constexpr uint32_t kKvS = 0, kKvDP = 128, kKvDV = 256, kKvDK = 384;
+// TMEM: S^T 0 and dP^T 64 (64 fp32 columns each); P^T / dS^T buffer b at
+// 128 + 64 b (32 columns of fp16 pairs each: P^T, then dS^T); dV 256, dK 384.
+constexpr uint32_t kKvS = 0, kKvDP = 64, kKvPB = 128, kKvDV = 256, kKvDK = 384;
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_constant__ BwdParams p) {
@@ -196,11 +197,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
   uint32_t* bitB = bitA + p.nwords;
 
   // full[s]: Q, dO, LSE and D of the step in stage s landed; stage_free[s]:
-  // dV and dK of that step completed.  s_done[b]: S^T and dP^T into buffer b
-  // done; pds[b]: P^T and dS^T written into buffer b (all compute threads);
-  // buf_free[b]: dV and dK that read buffer b completed.  Every parity wait
-  // targets a barrier in the awaited phase or the one after it.
-  __shared__ uint64_t bar_kv, full[kKvStages], stage_free[kKvStages], s_done[2], pds[2], buf_free[2];
+  // dV and dK of that step completed.  s_done: S^T(j) and dP^T(j) done;
+  // s_free: the compute warps have read them (all compute threads); pds[b]:
+  // P^T / dS^T(j) written into buffer b = j % 2; pb_free[b]: dV and dK that
+  // read buffer b completed.  Every parity wait targets a barrier in the
+  // awaited phase or the one after it.
+  __shared__ uint64_t bar_kv, full[kKvStages], stage_free[kKvStages], s_done, s_free, pds[2], pb_free[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int n_union;
 
@@ -218,10 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       mbar_init(&full[i], 1);
       mbar_init(&stage_free[i], 1);
     }
+    mbar_init(&s_done, 1);
+    mbar_init(&s_free, kCompute);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_done[i], 1);
       mbar_init(&pds[i], kCompute);
-      mbar_init(&buf_free[i], 1);
+      mbar_init(&pb_free[i], 1);
     }
     fence_mbar_init();
   }
@@ -277,59 +280,58 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer.  S^T(0), S^T(1) (each with its dP^T), then
-    // per step j: dV(j), dK(j) once P^T / dS^T(j) are written; S^T(j+2) into
-    // the same buffer once dV(j) and dK(j) have read it.
+    // ---------------- MMA issuer: S^T / dP^T (j+1) once the compute warps have
+    // read step j's; dV / dK (j) once P^T / dS^T (j) are written.  Polls with
+    // test_wait and issues whichever is ready.
     if (lane == 0 && steps > 0) {
       constexpr uint32_t idesc_s = idesc_f32acc(128, 64, 0, 0, 1);
       constexpr uint32_t idesc_g = idesc_f32acc(128, D, 0, 1, 1);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & (kKvStages - 1), b = j & 1;
-        if (!mbar_spin(&full[st], (j / kKvStages) & 1)) return false;
-        tc_fence_after();
-        const uint8_t* qt = sm + L::kRing + st * L::kStage;
+      bool ok = mbar_spin(&bar_kv, 0);
+      int ns = 0, ng = 0;  // next S^T / dP^T and next dV / dK to issue
+      uint32_t idle = 0;
+      while (ok && ng < steps) {
+        bool progressed = false;
+        if (ns < steps && (ns == 0 || mbar_test(&s_free, (ns - 1) & 1)) &&
+            mbar_test(&full[ns & (kKvStages - 1)], (ns / kKvStages) & 1)) {
+          tc_fence_after();
+          const uint8_t* qt = sm + L::kRing + (ns & (kKvStages - 1)) * L::kStage;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int blk = kk >> 2, w = kk & 3;
-          mma_ss(tmem + kKvS + 64 * b, sdesc_sw128(smem_u32(sm + L::kK + blk * 16384 + w * 32), 16, 1024),
-                 sdesc_sw128(smem_u32(qt + blk * 8192 + w * 32), 16, 1024), idesc_s, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int blk = kk >> 2, w = kk & 3;
-          mma_ss(tmem + kKvDP + 64 * b, sdesc_sw128(smem_u32(sm + L::kV + blk * 16384 + w * 32), 16, 1024),
-                 sdesc_sw128(smem_u32(qt + L::kTileQ + blk * 8192 + w * 32), 16, 1024), idesc_s, kk > 0);
-        }
-        mma_commit(&s_done[b]);
-        return true;
-      };
-      bool ok = mbar_spin(&bar_kv, 0) && issue_s(0) && (steps < 2 || issue_s(1));
-      for (int j = 0; ok && j < steps; ++j) {
-        const int st = j & (kKvStages - 1), b = j & 1;
-        if (!mbar_spin(&pds[b], (j >> 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint8_t* qt = sm + L::kRing + st * L::kStage;
-        // A = P^T / dS^T (K = 64 queries in 4 steps of 16: warpgroup g's 16
-        // packed columns sit at 32 g of the buffer), B = dO / Q (MN-major).
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + kKvDV, tmem + kKvS + 64 * b + (kk >> 1) * 32 + (kk & 1) * 8,
-                 sdesc_sw128(smem_u32(qt + L::kTileQ + kk * 2048), 8192, 1024), idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + kKvDK, tmem + kKvDP + 64 * b + (kk >> 1) * 32 + (kk & 1) * 8,
-                 sdesc_sw128(smem_u32(qt + kk * 2048), 8192, 1024), idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&stage_free[st]);
-        mma_commit(&buf_free[b]);
-        if (j + 2 < steps) {
-          if (!mbar_spin(&buf_free[b], (j >> 1) & 1) || !issue_s(j + 2)) {
-            ok = false;
-            break;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int blk = kk >> 2, w = kk & 3;
+            mma_ss(tmem + kKvS, sdesc_sw128(smem_u32(sm + L::kK + blk * 16384 + w * 32), 16, 1024),
+                   sdesc_sw128(smem_u32(qt + blk * 8192 + w * 32), 16, 1024), idesc_s, kk > 0);
           }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int blk = kk >> 2, w = kk & 3;
+            mma_ss(tmem + kKvDP, sdesc_sw128(smem_u32(sm + L::kV + blk * 16384 + w * 32), 16, 1024),
+                   sdesc_sw128(smem_u32(qt + L::kTileQ + blk * 8192 + w * 32), 16, 1024), idesc_s, kk > 0);
+          }
+          mma_commit(&s_done);
+          ++ns;
+          progressed = true;
         }
+        if (ng < ns && mbar_test(&pds[ng & 1], (ng >> 1) & 1)) {
+          tc_fence_after();
+          const int st = ng & (kKvStages - 1);
+          const uint8_t* qt = sm + L::kRing + st * L::kStage;
+          const uint32_t pb = tmem + kKvPB + 64 * (ng & 1);
+          // A = P^T / dS^T (K = 64 queries in 4 steps of 16), B = dO / Q (MN-major).
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + kKvDV, pb + kk * 8, sdesc_sw128(smem_u32(qt + L::kTileQ + kk * 2048), 8192, 1024), idesc_g,
+                   (ng > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + kKvDK, pb + 32 + kk * 8, sdesc_sw128(smem_u32(qt + kk * 2048), 8192, 1024), idesc_g,
+                   (ng > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&stage_free[st]);
+          mma_commit(&pb_free[ng & 1]);
+          ++ng;
+          progressed = true;
+        }
+        idle = progressed ? 0u : idle + 1u;
+        if (idle > (1u << 26)) ok = false;
       }
       if (!ok) flag_error(p.err, kErrTimeout);
     }
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       const int st = j & (kKvStages - 1), b = j & 1;
       // The stage's LSE / D are read from shared memory: wait for its fill
       // too (it has landed once S^T(j) is done, but this makes it visible).
-      if (!mbar_spin(&s_done[b], (j >> 1) & 1) || !mbar_spin(&full[st], (j / kKvStages) & 1)) {
+      if (!mbar_spin(&s_done, j & 1) || !mbar_spin(&full[st], (j / kKvStages) & 1)) {
         ok = false;
         break;
       }
@@ -355,10 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       const float* lse = reinterpret_cast<const float*>(sm + L::kStats + st * 512) + 32 * g;
       const float* dlt = lse + 64;
       uint32_t pk[16], dk[16];
+      uint32_t sv[32], dv[32];
       if (valid) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32_wait(lane_addr + kKvS + 64 * b + 32 * g, sv);
-        tmem_ld32_wait(lane_addr + kKvDP + 64 * b + 32 * g, dv);
+        tmem_ld32_wait(lane_addr + kKvS + 32 * g, sv);
+        tmem_ld32_wait(lane_addr + kKvDP + 32 * g, dv);
+      }
+      // S^T / dP^T are in registers: the MMA issuer may overwrite them.
+      tc_fence_before();
+      mbar_arrive(&s_free);
+      if (valid) {
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(lse + c);
@@ -379,16 +386,24 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = dk[i] = 0u;
       }
-      // Packed over the first half of this warpgroup's own columns (already read).
-      tmem_st8(lane_addr + kKvS + 64 * b + 32 * g, pk);
-      tmem_st8(lane_addr + kKvS + 64 * b + 32 * g + 8, pk + 8);
-      tmem_st8(lane_addr + kKvDP + 64 * b + 32 * g, dk);
-      tmem_st8(lane_addr + kKvDP + 64 * b + 32 * g + 8, dk + 8);
+      // Into P^T / dS^T buffer b once dV / dK (j - 2) have read it.
+      if (j >= 2) {
+        if (!mbar_spin(&pb_free[b], ((j >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      const uint32_t pb = lane_addr + kKvPB + 64 * b;
+      tmem_st8(pb + 16 * g, pk);
+      tmem_st8(pb + 16 * g + 8, pk + 8);
+      tmem_st8(pb + 32 + 16 * g, dk);
+      tmem_st8(pb + 32 + 16 * g + 8, dk + 8);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&pds[b]);
     }
-    if (ok && steps > 0 && !mbar_spin(&buf_free[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
+    if (ok && steps > 0 && !mbar_spin(&pb_free[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
     if (!ok) flag_error(p.err, kErrTimeout);
     tc_fence_after();
     // ---------------- dK, dV rows of this key pair (warpgroup 0: dV, 1: dK)
