@@ -287,6 +287,20 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       constexpr uint32_t idesc_s = idesc_f32acc(128, 64, 0, 0, 1);
       constexpr uint32_t idesc_g = idesc_f32acc(128, D, 0, 1, 1);
       bool ok = mbar_spin(&bar_kv, 0);
+      // The issuer shares its sub-partition with two busy compute warps, so
+      // every descriptor is precomputed: K / V per K-step, Q / dO stage bases
+      // (the start-address field is linear in the byte address, so a K-step
+      // or a stage is a constant added to a base).
+      uint64_t kdesc[D / 16], vdesc[D / 16];
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        kdesc[kk] = sdesc_sw128(smem_u32(sm + L::kK + off), 16, 1024);
+        vdesc[kk] = sdesc_sw128(smem_u32(sm + L::kV + off), 16, 1024);
+      }
+      const uint64_t qkm0 = sdesc_sw128(smem_u32(sm + L::kRing), 16, 1024);          // Q / dO, K-major
+      const uint64_t qmn0 = sdesc_sw128(smem_u32(sm + L::kRing), 8192, 1024);        // Q / dO, MN-major
+      constexpr uint32_t kStageU = L::kStage >> 4, kTileQU = L::kTileQ >> 4;
       int ns = 0, ng = 0;  // next S^T / dP^T and next dV / dK to issue
       uint32_t idle = 0;
       while (ok && ng < steps) {
@@ -294,19 +308,14 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
         if (ns < steps && (ns == 0 || mbar_test(&s_free, (ns - 1) & 1)) &&
             mbar_test(&full[ns & (kKvStages - 1)], (ns / kKvStages) & 1)) {
           tc_fence_after();
-          const uint8_t* qt = sm + L::kRing + (ns & (kKvStages - 1)) * L::kStage;
+          const uint64_t qd = qkm0 + (ns & (kKvStages - 1)) * kStageU;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int blk = kk >> 2, w = kk & 3;
-            mma_ss(tmem + kKvS, sdesc_sw128(smem_u32(sm + L::kK + blk * 16384 + w * 32), 16, 1024),
-                   sdesc_sw128(smem_u32(qt + blk * 8192 + w * 32), 16, 1024), idesc_s, kk > 0);
-          }
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + kKvS, kdesc[kk], qd + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int blk = kk >> 2, w = kk & 3;
-            mma_ss(tmem + kKvDP, sdesc_sw128(smem_u32(sm + L::kV + blk * 16384 + w * 32), 16, 1024),
-                   sdesc_sw128(smem_u32(qt + L::kTileQ + blk * 8192 + w * 32), 16, 1024), idesc_s, kk > 0);
-          }
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + kKvDP, vdesc[kk], qd + kTileQU + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s,
+                   kk > 0);
           mma_commit(&s_done);
           ++ns;
           progressed = true;
@@ -314,17 +323,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
         if (ng < ns && mbar_test(&pds[ng & 1], (ng >> 1) & 1)) {
           tc_fence_after();
           const int st = ng & (kKvStages - 1);
-          const uint8_t* qt = sm + L::kRing + st * L::kStage;
+          const uint64_t qd = qmn0 + st * kStageU;
           const uint32_t pb = tmem + kKvPB + 64 * (ng & 1);
           // A = P^T / dS^T (K = 64 queries in 4 steps of 16), B = dO / Q (MN-major).
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kKvDV, pb + kk * 8, sdesc_sw128(smem_u32(qt + L::kTileQ + kk * 2048), 8192, 1024), idesc_g,
-                   (ng > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + kKvDV, pb + kk * 8, qd + kTileQU + ((kk * 2048) >> 4), idesc_g, (ng > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kKvDK, pb + 32 + kk * 8, sdesc_sw128(smem_u32(qt + kk * 2048), 8192, 1024), idesc_g,
-                   (ng > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + kKvDK, pb + 32 + kk * 8, qd + ((kk * 2048) >> 4), idesc_g, (ng > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&stage_free[st]);
           mma_commit(&pb_free[ng & 1]);
           ++ng;
