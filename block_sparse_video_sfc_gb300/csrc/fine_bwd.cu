@@ -452,7 +452,10 @@ struct DqLayout {
   static constexpr int kQ = 0, kDO = kTile, kK = 2 * kTile, kV = 4 * kTile;  // K, V: 2 stages each
   static constexpr int kEnd = 6 * kTile;
 };
-constexpr uint32_t kDqS0 = 0, kDqS1 = 128, kDqDP = 256, kDqDQ = 384;  // dS (fp16) overwrites its S buffer
+// TMEM: S 0 and dP 128 (128 fp32 columns each, released once the compute
+// warps have read them); dS buffer b at 256 + 64 b (64 columns of fp16
+// pairs); dQ 384.
+constexpr uint32_t kDqS = 0, kDqDP = 128, kDqDS = 256, kDqDQ = 384;
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
@@ -464,10 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
   uint32_t* bitA = ulist + 2 * p.kmax + 2;
   uint32_t* bitB = bitA + nwords;
 
-  // bar_k / bar_v [s]: K / V stage s filled; bar_kvfree[s]: dQ of the step using
-  // stage s done.  bar_s[b]: S in TMEM buffer b done; bar_ds[b]: dS written into
-  // buffer b (128 threads); bar_dq[b]: dQ from buffer b done; bar_dp: dP done.
-  __shared__ uint64_t bar_qdo, bar_k[2], bar_v[2], bar_kvfree[2], bar_s[2], bar_ds[2], bar_dq[2], bar_dp;
+  // bar_k / bar_v [s]: K / V stage s filled; bar_kvfree[s]: dQ of the step
+  // using stage s done.  s_done: S(j) and dP(j) done; s_free: the compute
+  // warps have read them (all compute threads); bar_ds[b]: dS(j) written into
+  // buffer b = j % 2; ds_free[b]: the dQ that read buffer b completed.  Every
+  // parity wait targets a barrier in the awaited phase or the one after it.
+  __shared__ uint64_t bar_qdo, bar_k[2], bar_v[2], bar_kvfree[2], s_done, s_free, bar_ds[2], ds_free[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int n_union, n_cnt[2];
 
@@ -485,11 +490,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
       mbar_init(&bar_k[i], 1);
       mbar_init(&bar_v[i], 1);
       mbar_init(&bar_kvfree[i], 1);
-      mbar_init(&bar_s[i], 1);
       mbar_init(&bar_ds[i], kCompute);
-      mbar_init(&bar_dq[i], 1);
+      mbar_init(&ds_free[i], 1);
     }
-    mbar_init(&bar_dp, 1);
+    mbar_init(&s_done, 1);
+    mbar_init(&s_free, kCompute);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -554,45 +559,57 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer: S(0), dP(0), then per step j
-    //   S(j+1) -> buffer (j+1)&1, [dS(j)] dQ(j), dP(j+1)
+    // ---------------- MMA issuer: S(j+1) and dP(j+1) once the compute warps
+    // have read S(j) and dP(j); dQ(j) once dS(j) is written.  Polls with
+    // test_wait and issues whichever is ready; descriptors are precomputed.
     if (lane == 0 && steps > 0) {
-      bool ok = mbar_wait(&bar_qdo, 0) && mbar_wait(&bar_k[0], 0);
-      if (ok) {
-        tc_fence_after();
-        mma_rows_x_rows<D>(tmem + kDqS0, sm + L::kQ, sm + L::kK);
-        mma_commit(&bar_s[0]);
+      constexpr uint32_t idesc_s = idesc_f32acc(128, 128, 0, 0, 1);
+      constexpr uint32_t idesc_q = idesc_f32acc(128, D, 0, 1, 1);
+      uint64_t qdesc[D / 16], odesc[D / 16];
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        qdesc[kk] = sdesc_sw128(smem_u32(sm + L::kQ + off), 16, 1024);
+        odesc[kk] = sdesc_sw128(smem_u32(sm + L::kDO + off), 16, 1024);
       }
-      ok = ok && mbar_wait(&bar_v[0], 0);
-      if (ok) {
-        tc_fence_after();
-        mma_rows_x_rows<D>(tmem + kDqDP, sm + L::kDO, sm + L::kV);
-        mma_commit(&bar_dp);
-      }
-      for (int j = 0; j < steps && ok; ++j) {
-        const int s = j & 1, sn = (j + 1) & 1;
-        const bool more = j + 1 < steps;
-        if (more) {
-          ok = ok && mbar_wait(&bar_k[sn], ((j + 1) >> 1) & 1);
-          if (j >= 1) ok = ok && mbar_wait(&bar_dq[sn], ((j - 1) >> 1) & 1);  // dQ(j-1) read buffer sn
-          if (!ok) break;
+      const uint64_t kkm0 = sdesc_sw128(smem_u32(sm + L::kK), 16, 1024);      // K stages, K-major
+      const uint64_t vkm0 = sdesc_sw128(smem_u32(sm + L::kV), 16, 1024);      // V stages, K-major
+      const uint64_t kmn0 = sdesc_sw128(smem_u32(sm + L::kK), 16384, 1024);   // K stages, MN-major
+      constexpr uint32_t kTileU = L::kTile >> 4;
+      bool ok = mbar_spin(&bar_qdo, 0);
+      int ns = 0, ng = 0;  // next S / dP and next dQ to issue
+      uint32_t idle = 0;
+      while (ok && ng < steps) {
+        bool progressed = false;
+        if (ns < steps && (ns == 0 || mbar_test(&s_free, (ns - 1) & 1)) &&
+            mbar_test(&bar_k[ns & 1], (ns >> 1) & 1) && mbar_test(&bar_v[ns & 1], (ns >> 1) & 1)) {
           tc_fence_after();
-          mma_rows_x_rows<D>(tmem + (sn ? kDqS1 : kDqS0), sm + L::kQ, sm + L::kK + sn * L::kTile);
-          mma_commit(&bar_s[sn]);
+          const uint64_t kd = kkm0 + (ns & 1) * kTileU, vd = vkm0 + (ns & 1) * kTileU;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + kDqS, qdesc[kk], kd + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + kDqDP, odesc[kk], vd + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
+          mma_commit(&s_done);
+          ++ns;
+          progressed = true;
         }
-        ok = ok && mbar_wait(&bar_ds[s], (j >> 1) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        mma_tmem_x_rows<D>(tmem + kDqDQ, tmem + (s ? kDqS1 : kDqS0), sm + L::kK + s * L::kTile, j > 0);
-        mma_commit(&bar_dq[s]);
-        mma_commit(&bar_kvfree[s]);
-        if (more) {
-          ok = ok && mbar_wait(&bar_v[sn], ((j + 1) >> 1) & 1);
-          if (!ok) break;
+        if (ng < ns && mbar_test(&bar_ds[ng & 1], (ng >> 1) & 1)) {
           tc_fence_after();
-          mma_rows_x_rows<D>(tmem + kDqDP, sm + L::kDO, sm + L::kV + sn * L::kTile);
-          mma_commit(&bar_dp);
+          const uint32_t dsb = tmem + kDqDS + 64 * (ng & 1);
+          const uint64_t kd = kmn0 + (ng & 1) * kTileU;
+          // A = dS (K = 128 keys in 8 steps of 16), B = the K stage (MN-major).
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + kDqDQ, dsb + kk * 8, kd + ((kk * 2048) >> 4), idesc_q, (ng > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bar_kvfree[ng & 1]);
+          mma_commit(&ds_free[ng & 1]);
+          ++ng;
+          progressed = true;
         }
+        idle = progressed ? 0u : idle + 1u;
+        if (idle > (1u << 26)) ok = false;
       }
       if (!ok) flag_error(p.err, kErrTimeout);
     }
@@ -611,47 +628,47 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
     bool ok = true;
     for (int j = 0; j < steps; ++j) {
       const int b = j & 1;
-      const uint32_t sbuf = b ? kDqS1 : kDqS0;
       const bool has1 = 2 * j + 1 < U;
       const uint32_t e = (g == 0) ? ulist[2 * j] : (has1 ? ulist[2 * j + 1] : 0u);
-      const bool valid = (g == 0 || has1) && ((e >> my_bit) & 1u) != 0;
-      const bool any = __any_sync(0xffffffffu, valid);
-      if (!mbar_wait(&bar_s[b], (j >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      if (!mbar_wait(&bar_dp, j & 1)) {
+      const bool valid = (g == 0 || has1) && ((e >> my_bit) & 1u) != 0;  // warp-uniform
+      if (!mbar_spin(&s_done, j & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // ---- P = exp2(S * scale - LSE), dS = P (dP - D), 16 key columns at a
-      // time; dS packed fp16 into this warpgroup's half of the S buffer.
-#pragma unroll 1
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        uint32_t ds[8];
-        if (any) {
-          float sv[16], dv[16];
-          tmem_ld16(lane_addr + sbuf + 64 * g + c0, sv);
-          tmem_ld16(lane_addr + kDqDP + 64 * g + c0, dv);
-          tmem_wait_ld();
+      // S and dP of this warpgroup's key cube into registers, then release them.
+      uint32_t sv[64], dv[64];
+      if (valid) tmem_ld64x2_wait(lane_addr + kDqS + 64 * g, sv, lane_addr + kDqDP + 64 * g, dv);
+      tc_fence_before();
+      mbar_arrive(&s_free);
+      // P = exp2(S * scale - LSE), dS = P (dP - D), packed fp16.
+      uint32_t ds[32];
+      if (valid) {
 #pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            const float p0 = valid ? fast_exp2(fmaf(sv[i], p.scale_log2, -lse2)) : 0.f;
-            const float p1 = valid ? fast_exp2(fmaf(sv[i + 1], p.scale_log2, -lse2)) : 0.f;
-            ds[i >> 1] = pack_f16(p0 * (dv[i] - dlt), p1 * (dv[i + 1] - dlt));
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) ds[i] = 0u;
+        for (int i = 0; i < 64; i += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[i]), p.scale_log2, -lse2));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[i + 1]), p.scale_log2, -lse2));
+          ds[i >> 1] = pack_f16(p0 * (__uint_as_float(dv[i]) - dlt), p1 * (__uint_as_float(dv[i + 1]) - dlt));
         }
-        tmem_st8(lane_addr + sbuf + 64 * g + (c0 >> 1), ds);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ds[i] = 0u;
       }
+      // Into dS buffer b once dQ(j - 2) has read it.
+      if (j >= 2) {
+        if (!mbar_spin(&ds_free[b], ((j >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int c = 0; c < 32; c += 8) tmem_st8(lane_addr + kDqDS + 64 * b + 32 * g + c, ds + c);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar_ds[b]);
     }
-    if (ok && steps > 0 && !mbar_wait(&bar_dq[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
+    if (ok && steps > 0 && !mbar_spin(&ds_free[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
     if (!ok) flag_error(p.err, kErrTimeout);
     tc_fence_after();
     // ---------------- dQ rows (warpgroup g writes columns [g*D/2, (g+1)*D/2))
