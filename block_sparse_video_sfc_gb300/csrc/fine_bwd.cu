@@ -468,11 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
   uint32_t* bitB = bitA + nwords;
 
   // bar_k / bar_v [s]: K / V stage s filled; bar_kvfree[s]: dQ of the step
-  // using stage s done.  s_done: S(j) and dP(j) done; s_free: the compute
+  // using stage s done (K read); bar_vfree[s]: dP of that step done (V read).  s_done: S(j) and dP(j) done; s_free: the compute
   // warps have read them (all compute threads); bar_ds[b]: dS(j) written into
   // buffer b = j % 2; ds_free[b]: the dQ that read buffer b completed.  Every
   // parity wait targets a barrier in the awaited phase or the one after it.
-  __shared__ uint64_t bar_qdo, bar_k[2], bar_v[2], bar_kvfree[2], s_done, s_free, bar_ds[2], ds_free[2];
+  __shared__ uint64_t bar_qdo, bar_k[2], bar_v[2], bar_kvfree[2], bar_vfree[2], s_done, s_free, bar_ds[2], ds_free[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int n_union, n_cnt[2];
 
@@ -490,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
       mbar_init(&bar_k[i], 1);
       mbar_init(&bar_v[i], 1);
       mbar_init(&bar_kvfree[i], 1);
+      mbar_init(&bar_vfree[i], 1);
       mbar_init(&bar_ds[i], kCompute);
       mbar_init(&ds_free[i], 1);
     }
@@ -545,17 +546,23 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
       const int cq1 = has_b ? qb : qa;
       load_cube_pair<D>(sm + L::kQ, &p.tq, &bar_qdo, row_base, qa, cq1);
       load_cube_pair<D>(sm + L::kDO, &p.tdo, &bar_qdo, row_base, qa, cq1);
+      // V(j) goes in once dP(j - 2) is done, K(j) once dQ(j - 2) is: V is
+      // released a step earlier, so it is requested first.
       for (int j = 0; j < steps; ++j) {
         const int s = j & 1;
+        const int c0 = kcube(j, 0), c1 = kcube(j, 1);
+        if (j >= 2 && !mbar_wait(&bar_vfree[s], ((j >> 1) - 1) & 1)) {
+          flag_error(p.err, kErrTimeout);
+          break;
+        }
+        mbar_expect_tx(&bar_v[s], L::kTile);
+        load_cube_pair<D>(sm + L::kV + s * L::kTile, &p.tv, &bar_v[s], row_base, c0, c1);
         if (j >= 2 && !mbar_wait(&bar_kvfree[s], ((j >> 1) - 1) & 1)) {
           flag_error(p.err, kErrTimeout);
           break;
         }
-        const int c0 = kcube(j, 0), c1 = kcube(j, 1);
         mbar_expect_tx(&bar_k[s], L::kTile);
         load_cube_pair<D>(sm + L::kK + s * L::kTile, &p.tk, &bar_k[s], row_base, c0, c1);
-        mbar_expect_tx(&bar_v[s], L::kTile);
-        load_cube_pair<D>(sm + L::kV + s * L::kTile, &p.tv, &bar_v[s], row_base, c0, c1);
       }
     }
   } else if (warp == 1) {
@@ -592,6 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + kDqDP, odesc[kk], vd + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
           mma_commit(&s_done);
+          mma_commit(&bar_vfree[ns & 1]);
           ++ns;
           progressed = true;
         }
