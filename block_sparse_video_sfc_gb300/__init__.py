@@ -205,6 +205,12 @@ def timing_read() -> dict:
     return out
 
 
+def selftest_wait_timeout(polls: int = 1 << 16) -> None:
+    """Runs the bounded-wait failure path once (vsa_selftest_wait_timeout);
+    device_status() then reports VSA_ERR_TIMEOUT."""
+    _lib.check("vsa_selftest_wait_timeout", _lib.load().vsa_selftest_wait_timeout(polls, _stream()))
+
+
 def device_status() -> int:
     """Waits for the current stream; returns and clears the device error word."""
     return int(_lib.load().vsa_device_status(_stream()))

@@ -5,6 +5,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace vsa {
 namespace {
@@ -112,6 +113,15 @@ cudaEvent_t pooled_event() {
   return e;
 }
 
+// One thread waits on a barrier that nothing completes, with the bounded
+// wait of the fine kernels, then records the timeout like they do.
+__global__ void wait_timeout_kernel(uint32_t polls, int* err) {
+  __shared__ uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  if (!mbar_wait(&bar, 0, polls)) flag_error(err, kErrTimeout);
+}
+
 }  // namespace
 
 void timing_mark(int kernel, bool begin, cudaStream_t s) {
@@ -196,6 +206,14 @@ int vsa_timing_read(int kernel, double* total_ms, int* launches) {
   *total_ms = sum;
   *launches = n;
   return st;
+}
+
+int vsa_selftest_wait_timeout(uint32_t polls, void* stream) {
+  if (polls < 1 || polls > (1u << 24)) return VSA_ERR_ARG;
+  int* err = device_error_word();
+  if (!err) return VSA_ERR_CUDA;
+  wait_timeout_kernel<<<1, 1, 0, as_stream(stream)>>>(polls, err);
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
 int vsa_device_status(void* stream) {

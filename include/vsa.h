@@ -256,6 +256,18 @@ int vsa_device_status(void* stream);
 /* Static description of a status code. */
 const char* vsa_status_string(int status);
 
+/*
+ * vsa_selftest_wait_timeout -- exercises the failure path every kernel of
+ * this library takes when a wait never completes (the pages have no
+ * counterpart; this is the library's own failure detection).  Launches one
+ * thread that waits, with the same bounded mbarrier wait the fine kernels
+ * use, on a barrier nothing will complete; after `polls` polls it gives up,
+ * latches the timeout bit and exits.  The GPU context stays usable:
+ * vsa_device_status() then returns VSA_ERR_TIMEOUT (and clears it).
+ *   polls  number of polls before giving up (1 .. 2^24; VSA_ERR_ARG otherwise).
+ */
+int vsa_selftest_wait_timeout(uint32_t polls, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -334,3 +334,19 @@ def test_tile_pairs_partition(vsa, oracle_mod, name):
         adjacent = sum(len(sets[2 * t] | (sets[2 * t + 1] if 2 * t + 1 < wl.Nc else set()))
                        for t in range((wl.Nc + 1) // 2))
         assert plan <= adjacent, (plan, adjacent)
+
+
+def test_bounded_wait_timeout_is_reported(vsa, oracle_mod):
+    """A wait that never completes gives up after its poll limit, latches
+    VSA_ERR_TIMEOUT and leaves the context usable (no GPU fault involved)."""
+    assert vsa.device_status() == 0
+    vsa.selftest_wait_timeout(1 << 12)
+    assert vsa.device_status() == -5  # VSA_ERR_TIMEOUT
+    assert vsa.device_status() == 0   # reading cleared it
+    wl = synth.WORKLOADS["tiny"]
+    q, k, v = synth.make_qkv(wl)
+    out, st = vsa.forward(dev(q), dev(k), dev(v), wl.T, wl.H, wl.W, wl.topk, out_dtype=torch.float32)
+    status_ok(vsa)
+    gidx = st.saved()["idx"].cpu().numpy().reshape(wl.B, wl.heads, wl.Nc, wl.topk)
+    ref = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, lut=gidx)
+    assert_close(host(out), ref["out"], what="out after a timeout")
