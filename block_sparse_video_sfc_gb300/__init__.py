@@ -76,6 +76,32 @@ def coarse_topk(qc, kc, vc, topk: int, scale: Optional[float] = None, want_oc: b
     return dict(idx=idx, cnt=cnt, oc=oc, lse_c=lse_c, scores=scores)
 
 
+def mask_to_lut(mask, max_kv_blocks: int):
+    """vsa_mask_to_lut: uint8/bool block matrix [.., Nc, Nc] -> (idx [.., Nc, max_kv_blocks], cnt [.., Nc])."""
+    mask = mask.to(torch.uint8).contiguous()
+    Nc = mask.shape[-1]
+    BH = mask.numel() // (Nc * Nc)
+    lead = mask.shape[:-2]
+    idx = torch.empty(lead + (Nc, max_kv_blocks), dtype=torch.int32, device=mask.device)
+    cnt = torch.empty(lead + (Nc,), dtype=torch.int32, device=mask.device)
+    _lib.check("vsa_mask_to_lut", _lib.load().vsa_mask_to_lut(
+        _ptr(mask), BH, Nc, max_kv_blocks, _ptr(idx), _ptr(cnt), _stream()))
+    return idx, cnt
+
+
+def lut_add_neighbors(idx, cnt, T: int, H: int, W: int, radius: int, max_kv_blocks: int):
+    """vsa_lut_add_neighbors: list united with the radius-r cube neighbourhood -> (idx, cnt)."""
+    Nc, kin = idx.shape[-2], idx.shape[-1]
+    BH = idx.numel() // (Nc * kin)
+    lead = idx.shape[:-2]
+    out = torch.empty(lead + (Nc, max_kv_blocks), dtype=torch.int32, device=idx.device)
+    ocnt = torch.empty(lead + (Nc,), dtype=torch.int32, device=idx.device)
+    _lib.check("vsa_lut_add_neighbors", _lib.load().vsa_lut_add_neighbors(
+        _ptr(idx), _ptr(cnt), kin, BH, Grid.of(T, H, W), radius, max_kv_blocks, _ptr(out), _ptr(ocnt),
+        _stream()))
+    return out, ocnt
+
+
 def fine_fwd(qp, kp, vp, idx, cnt, scale: Optional[float] = None, out_dtype=torch.float32):
     """vsa_fine_fwd on cube-ordered bf16 tensors -> (O_f, lse)."""
     BH, N, d = _bhnd(qp)

@@ -64,6 +64,8 @@ SIGNATURES = {
     "vsa_forward_saved": ([P, I, I, I, Grid, I, ctypes.POINTER(Saved)], I),
     "vsa_device_status": ([P], I),
     "vsa_selftest_wait_timeout": ([ctypes.c_uint32, P], I),
+    "vsa_mask_to_lut": ([P, I, I, I, P, P, P], I),
+    "vsa_lut_add_neighbors": ([P, P, I, I, Grid, I, I, P, P, P], I),
     "vsa_status_string": ([I], ctypes.c_char_p),
     "vsa_timing_enable": ([I], I),
     "vsa_timing_read": ([I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I)], I),

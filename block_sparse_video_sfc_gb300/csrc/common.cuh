@@ -109,6 +109,9 @@ size_t pair_plan_smem(int Nc);
 int launch_list_bits(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, uint32_t* bits,
                      cudaStream_t s);
 int launch_pair_plan(const uint32_t* bits, int BH, int Nc, int32_t* pairs, cudaStream_t s);
+int launch_mask_to_lut(const uint8_t* mask, int BH, int Nc, int kmax, int32_t* idx, int32_t* cnt, cudaStream_t s);
+int launch_add_neighbors(const int32_t* idx_in, const int32_t* cnt_in, int kmax_in, int BH, int Tc, int Hc, int Wc,
+                         int radius, int kmax_out, int32_t* idx_out, int32_t* cnt_out, cudaStream_t s);
 size_t fine_bwd_ws_bytes(int BH, int N, int kmax);
 int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* of, int of_dtype,
                     const float* lse, const void* dof, const int32_t* idx, const int32_t* cnt, int kmax, int BH,

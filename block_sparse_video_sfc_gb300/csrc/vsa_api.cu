@@ -208,6 +208,28 @@ int vsa_timing_read(int kernel, double* total_ms, int* launches) {
   return st;
 }
 
+int vsa_mask_to_lut(const uint8_t* mask, int BH, int Nc, int max_kv_blocks, int32_t* kv_block_idx,
+                    int32_t* valid_block_num, void* stream) {
+  if (!mask || !kv_block_idx || !valid_block_num) return VSA_ERR_ARG;
+  if (BH <= 0 || Nc <= 0 || max_kv_blocks < 1) return VSA_ERR_ARG;
+  if (static_cast<int64_t>(BH) * Nc >= (int64_t(1) << 31) || Nc > (1 << 16)) return VSA_ERR_UNSUPPORTED;
+  return launch_mask_to_lut(mask, BH, Nc, max_kv_blocks, kv_block_idx, valid_block_num, as_stream(stream));
+}
+
+int vsa_lut_add_neighbors(const int32_t* kv_block_idx_in, const int32_t* valid_block_num_in, int max_kv_blocks_in,
+                          int BH, vsa_grid_t g, int radius, int max_kv_blocks_out, int32_t* kv_block_idx_out,
+                          int32_t* valid_block_num_out, void* stream) {
+  Dims D;
+  if (BH <= 0) return VSA_ERR_ARG;
+  int st = check_grid(g, 128, &D, BH);
+  if (st != VSA_OK) return st;
+  if (!kv_block_idx_in || !kv_block_idx_out || !valid_block_num_out) return VSA_ERR_ARG;
+  if (max_kv_blocks_in < 1 || max_kv_blocks_out < 1 || radius < 0 || radius > 7) return VSA_ERR_ARG;
+  if (D.Nc > (1 << 16)) return VSA_ERR_UNSUPPORTED;
+  return launch_add_neighbors(kv_block_idx_in, valid_block_num_in, max_kv_blocks_in, BH, g.T / 4, g.H / 4, g.W / 4,
+                              radius, max_kv_blocks_out, kv_block_idx_out, valid_block_num_out, as_stream(stream));
+}
+
 int vsa_selftest_wait_timeout(uint32_t polls, void* stream) {
   if (polls < 1 || polls > (1u << 24)) return VSA_ERR_ARG;
   int* err = device_error_word();

@@ -257,6 +257,47 @@ int vsa_device_status(void* stream);
 const char* vsa_status_string(int status);
 
 /*
+ * vsa_mask_to_lut -- converts a block relation matrix into index lists.
+ * [AMD] "Sparse Encoding in CK Tile": Jenga stores the full M x M one-hot
+ * block matrix B, VSA the selected blocks of each query block plus a valid
+ * count; this call turns the first form into the second, on the device.
+ *   mask             uint8 [BH, Nc, Nc], row-major: nonzero = query cube i
+ *                    attends to key cube j (i = row, j = column).
+ *   max_kv_blocks    list length per row (>= 1).
+ *   kv_block_idx     out int32 [BH, Nc, max_kv_blocks]: the kept key cubes of
+ *                    each row in ascending id, then -1.
+ *   valid_block_num  out int32 [BH, Nc]: the number kept (<= max_kv_blocks).
+ * A row with more nonzero cells than max_kv_blocks keeps its lowest ids and
+ * latches VSA_ERR_LUT (read with vsa_device_status).  Asynchronous on stream;
+ * argument errors are returned before any launch.
+ */
+int vsa_mask_to_lut(const uint8_t* mask, int BH, int Nc, int max_kv_blocks, int32_t* kv_block_idx,
+                    int32_t* valid_block_num, void* stream);
+
+/*
+ * vsa_lut_add_neighbors -- unites every row's list with its cube's spatial
+ * neighbourhood.  [AMD] "Comparison with Jenga", "Algorithmic Design":
+ * Jenga's block selection is the union of three masks, one of them spatial
+ * adjacency; this adds that adjacency to a Top-K list.  Cube ids follow the
+ * cube-raster order of vsa_permute: c = (t * Hc + h) * Wc + w on the cube grid
+ * (Tc, Hc, Wc) = (T / 4, H / 4, W / 4).
+ *   kv_block_idx_in, valid_block_num_in (may be NULL = max_kv_blocks_in),
+ *   max_kv_blocks_in   the input lists [BH, Nc, max_kv_blocks_in].
+ *   g                  the video grid (as in vsa_forward; 4 x 4 x 4 cubes).
+ *   radius             0..7: cubes whose t, h and w cube coordinates each
+ *                      differ from the query cube's by at most radius (the
+ *                      query cube itself included) are added.
+ *   max_kv_blocks_out  output list length; kv_block_idx_out int32
+ *                      [BH, Nc, max_kv_blocks_out] ascending, then -1;
+ *                      valid_block_num_out int32 [BH, Nc].
+ * Overflow: as vsa_mask_to_lut.  Entries of the input outside [0, Nc) are
+ * skipped and latch VSA_ERR_LUT.  Input and output must not overlap.
+ */
+int vsa_lut_add_neighbors(const int32_t* kv_block_idx_in, const int32_t* valid_block_num_in, int max_kv_blocks_in,
+                          int BH, vsa_grid_t g, int radius, int max_kv_blocks_out, int32_t* kv_block_idx_out,
+                          int32_t* valid_block_num_out, void* stream);
+
+/*
  * vsa_selftest_wait_timeout -- exercises the failure path every kernel of
  * this library takes when a wait never completes (the pages have no
  * counterpart; this is the library's own failure detection).  Launches one

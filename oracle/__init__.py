@@ -65,6 +65,8 @@ def _load():
                 "orc_fine_bwd_query_rows": ([P, P, P, P, P, P, I, I64, I, D, P, I64, P], None),
                 "orc_fine_bwd_key_cube": ([P, P, P, P, P, P, I, I64, I, D, I64, I, P, P], None),
                 "orc_combine_bwd": ([P, P, P, P, P, I64, I64, I, P, P, P, P], None),
+                "orc_mask_to_lut": ([P, I64, I, I, P, P, P], None),
+                "orc_lut_add_neighbors": ([P, P, I, I64, I, I, I, I, I, P, P, P], None),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -278,3 +280,31 @@ def backward(q, k, v, dout, idx, T: int, H: int, W: int, scale=None,
                          float(scale), _p(idx), _p(dout), _p(dq), _p(dk), _p(dv),
                          _p(dgc), _p(dgf))
     return dict(dq=dq, dk=dk, dv=dv, dgc=dgc, dgf=dgf)
+
+
+def mask_to_lut(mask, max_kv_blocks: int):
+    """Block relation matrix [.., Nc, Nc] (nonzero = keep) -> (idx, cnt, overflow)."""
+    m = np.ascontiguousarray(np.asarray(mask) != 0, dtype=np.uint8)
+    Nc = m.shape[-1]
+    rows = m.size // Nc
+    idx = np.empty(m.shape[:-1] + (max_kv_blocks,), dtype=np.int32)
+    cnt = np.empty(m.shape[:-1], dtype=np.int32)
+    ovf = ctypes.c_int(0)
+    _load().orc_mask_to_lut(m.ctypes.data_as(ctypes.c_void_p), rows, Nc, max_kv_blocks, _p(idx), _p(cnt),
+                            ctypes.byref(ovf))
+    return idx, cnt, bool(ovf.value)
+
+
+def lut_add_neighbors(idx, cnt, T: int, H: int, W: int, radius: int, max_kv_blocks: int):
+    """Lists united with the radius-r cube neighbourhood -> (idx, cnt, overflow)."""
+    idx = _i32(idx)
+    cnt = None if cnt is None else _i32(cnt)
+    Tc, Hc, Wc = T // 4, H // 4, W // 4
+    Nc, kin = idx.shape[-2], idx.shape[-1]
+    BH = idx.size // (Nc * kin)
+    out = np.empty(idx.shape[:-1] + (max_kv_blocks,), dtype=np.int32)
+    ocnt = np.empty(idx.shape[:-1], dtype=np.int32)
+    ovf = ctypes.c_int(0)
+    _load().orc_lut_add_neighbors(_p(idx), _p(cnt), kin, BH, Tc, Hc, Wc, radius, max_kv_blocks, _p(out), _p(ocnt),
+                                  ctypes.byref(ovf))
+    return out, ocnt, bool(ovf.value)

@@ -689,3 +689,72 @@ void orc_backward(const double *q, const double *k, const double *v,
     free(lse); free(dop); free(gcp); free(gfp); free(dgcp); free(dgfp); free(dof); free(doc);
     free(dqp); free(dkp); free(dvp); free(dqc); free(dkc); free(dvc); free(cnt);
 }
+
+/* ---- index-list conversions ("Sparse Encoding in CK Tile": Jenga's M x M
+ * block matrix B vs VSA's selected-block list plus valid count; "Comparison
+ * with Jenga", "Algorithmic Design": adjacency as one of Jenga's masks). */
+
+/* Row r of a keep-set (sel[0..Nc)) as an ascending list of at most kmax ids,
+ * -1 after the count; a longer row keeps its lowest ids and sets *overflow. */
+static void orc_write_list(const unsigned char *sel, int Nc, int kmax, int32_t *idx, int32_t *cnt, int *overflow)
+{
+    int n = 0;
+    for (int j = 0; j < Nc; j++) {
+        if (!sel[j])
+            continue;
+        if (n < kmax)
+            idx[n] = j;
+        n++;
+    }
+    if (n > kmax) {
+        *overflow = 1;
+        n = kmax;
+    }
+    for (int e = n; e < kmax; e++)
+        idx[e] = -1;
+    *cnt = n;
+}
+
+/* mask[row][j] != 0: query cube `row % Nc` keeps key cube j. */
+void orc_mask_to_lut(const unsigned char *mask, int64_t rows, int Nc, int kmax, int32_t *idx, int32_t *cnt,
+                     int *overflow)
+{
+    *overflow = 0;
+    for (int64_t r = 0; r < rows; r++)
+        orc_write_list(mask + r * Nc, Nc, kmax, idx + r * kmax, cnt + r, overflow);
+}
+
+/* The list of every query cube united with all cubes whose cube-grid
+ * coordinates (t, h, w) each differ from the query cube's by at most
+ * `radius`.  Cube id c = (t * Hc + h) * Wc + w. */
+void orc_lut_add_neighbors(const int32_t *idx_in, const int32_t *cnt_in, int kin, int64_t BH, int Tc, int Hc,
+                           int Wc, int radius, int kout, int32_t *idx_out, int32_t *cnt_out, int *overflow)
+{
+    const int Nc = Tc * Hc * Wc;
+    *overflow = 0;
+    unsigned char *sel = (unsigned char *)malloc((size_t)Nc);
+    for (int64_t bh = 0; bh < BH; bh++) {
+        for (int q = 0; q < Nc; q++) {
+            const int64_t row = bh * Nc + q;
+            memset(sel, 0, (size_t)Nc);
+            int n = cnt_in ? cnt_in[row] : kin;
+            if (n < 0)
+                n = 0;
+            if (n > kin)
+                n = kin;
+            for (int e = 0; e < n; e++) {
+                int c = idx_in[row * kin + e];
+                if (c >= 0 && c < Nc)
+                    sel[c] = 1;
+            }
+            const int qt = q / (Hc * Wc), qh = (q / Wc) % Hc, qw = q % Wc;
+            for (int c = 0; c < Nc; c++) {
+                const int t = c / (Hc * Wc), h = (c / Wc) % Hc, w = c % Wc;
+                if (abs(t - qt) <= radius && abs(h - qh) <= radius && abs(w - qw) <= radius)
+                    sel[c] = 1;
+            }
+            orc_write_list(sel, Nc, kout, idx_out + row * kout, cnt_out + row, overflow);
+        }
+    }
+    free(sel);
+}

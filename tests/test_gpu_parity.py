@@ -350,3 +350,50 @@ def test_bounded_wait_timeout_is_reported(vsa, oracle_mod):
     gidx = st.saved()["idx"].cpu().numpy().reshape(wl.B, wl.heads, wl.Nc, wl.topk)
     ref = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, lut=gidx)
     assert_close(host(out), ref["out"], what="out after a timeout")
+
+
+# ---------------------------------------------------------------- index-list conversions
+@pytest.mark.parametrize("BH,Nc,density,kmax", [(2, 64, 0.3, 64), (12, 512, 0.3, 512), (3, 1920, 0.1, 256)])
+def test_mask_to_lut(vsa, oracle_mod, BH, Nc, density, kmax):
+    """Jenga-style block matrix -> index list + count, bit for bit."""
+    rng = np.random.default_rng(Nc)
+    m = rng.random((BH, Nc, Nc)) < density
+    idx, cnt = vsa.mask_to_lut(torch.from_numpy(m).cuda(), kmax)
+    torch.cuda.synchronize()
+    ridx, rcnt, ovf = oracle_mod.mask_to_lut(m, kmax)
+    assert vsa.device_status() == (-6 if ovf else 0)
+    assert np.array_equal(cnt.cpu().numpy(), rcnt)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+
+
+def test_mask_to_lut_overflow_is_reported(vsa, oracle_mod):
+    m = np.ones((1, 40, 40), bool)
+    idx, cnt = vsa.mask_to_lut(torch.from_numpy(m).cuda(), 16)
+    assert vsa.device_status() == -6  # VSA_ERR_LUT
+    ridx, rcnt, ovf = oracle_mod.mask_to_lut(m, 16)
+    assert ovf and np.array_equal(idx.cpu().numpy(), ridx) and np.array_equal(cnt.cpu().numpy(), rcnt)
+
+
+@pytest.mark.parametrize("name,radius", [("small", 1), ("wan1.3b", 1), ("long", 1), ("small", 2)])
+def test_lut_add_neighbors_and_fine_fwd(vsa, oracle_mod, name, radius):
+    """Top-K lists united with the spatial neighbourhood (bit for bit against
+    the oracle), then the fine forward on the widened, ragged lists."""
+    wl = synth.WORKLOADS[name]
+    heads = [0]
+    rng = np.random.default_rng(radius)
+    idx = np.stack([np.stack([rng.permutation(wl.Nc)[:wl.topk] for _ in range(wl.Nc)])
+                    for _ in heads]).astype(np.int32)
+    cnt = rng.integers(wl.topk // 2, wl.topk + 1, size=idx.shape[:-1]).astype(np.int32)
+    kout = wl.topk + (2 * radius + 1) ** 3
+    gi, gc = vsa.lut_add_neighbors(dev(idx, torch.int32), dev(cnt, torch.int32), wl.T, wl.H, wl.W, radius, kout)
+    status_ok(vsa)
+    ri, rc, ovf = oracle_mod.lut_add_neighbors(idx, cnt, wl.T, wl.H, wl.W, radius, kout)
+    assert not ovf
+    assert np.array_equal(gc.cpu().numpy(), rc) and np.array_equal(gi.cpu().numpy(), ri)
+    if name == "small":
+        qp, kp, vp = _fine_case(oracle_mod, wl, heads=heads)
+        of, lse = vsa.fine_fwd(dev(qp), dev(kp), dev(vp), gi, gc)
+        status_ok(vsa)
+        rof, rlse = oracle_mod.fine_fwd(qp, kp, vp, ri, rc, wl.d ** -0.5)
+        assert_close(host(of), rof, what="O_f on widened lists")
+        assert_close(host(lse), rlse, what="lse on widened lists")

@@ -348,3 +348,55 @@ def test_sampled_backward_functions_match_full(oracle_mod):
         np.testing.assert_allclose(sk, dk[0, 64 * c:64 * c + 64], rtol=1e-10, atol=1e-12)
         np.testing.assert_allclose(sv, dv[0, 64 * c:64 * c + 64], rtol=1e-10, atol=1e-12)
     assert pos.size == wl.N
+
+
+# ---------------------------------------------------------------- index-list conversions
+def test_mask_to_lut_matches_nonzero(oracle_mod):
+    """Block matrix -> list: the ascending nonzero columns of each row (brute
+    force with numpy), -1 after the count; overflow keeps the lowest ids."""
+    rng = np.random.default_rng(21)
+    for Nc, density, kmax in ((8, 0.3, 8), (40, 0.5, 40), (40, 0.5, 12), (70, 0.05, 9)):
+        m = rng.random((3, Nc, Nc)) < density
+        idx, cnt, ovf = oracle_mod.mask_to_lut(m, kmax)
+        any_over = False
+        for r in range(3 * Nc):
+            cols = np.flatnonzero(m.reshape(-1, Nc)[r])
+            any_over |= cols.size > kmax
+            keep = cols[:kmax]
+            assert cnt.reshape(-1)[r] == keep.size
+            row = idx.reshape(-1, kmax)[r]
+            assert np.array_equal(row[:keep.size], keep)
+            assert np.all(row[keep.size:] == -1)
+        assert ovf == any_over
+    full, cnt, _ = oracle_mod.mask_to_lut(np.ones((1, 5, 5)), 5)
+    assert np.array_equal(full[0], np.tile(np.arange(5), (5, 1))) and np.all(cnt == 5)
+    empty, cnt, _ = oracle_mod.mask_to_lut(np.zeros((1, 5, 5)), 3)
+    assert np.all(empty == -1) and np.all(cnt == 0)
+
+
+def test_lut_add_neighbors_brute_force(oracle_mod):
+    """List united with the radius-r neighbourhood, against explicit cube
+    coordinates; an interior cube gains (2r+1)^3 cubes, a corner (r+1)^3."""
+    rng = np.random.default_rng(22)
+    T, H, W = 12, 16, 20
+    Tc, Hc, Wc = T // 4, H // 4, W // 4
+    Nc = Tc * Hc * Wc
+    coords = np.array([(t, h, w) for t in range(Tc) for h in range(Hc) for w in range(Wc)])
+    K = 6
+    idx = np.stack([np.stack([rng.permutation(Nc)[:K] for _ in range(Nc)]) for _ in range(2)]).astype(np.int32)
+    cnt = rng.integers(0, K + 1, size=(2, Nc)).astype(np.int32)
+    for radius in (0, 1, 2):
+        kout = K + (2 * radius + 1) ** 3
+        out, ocnt, ovf = oracle_mod.lut_add_neighbors(idx, cnt, T, H, W, radius, kout)
+        assert not ovf
+        for h in range(2):
+            for q in range(Nc):
+                near = np.flatnonzero(np.abs(coords - coords[q]).max(axis=1) <= radius)
+                want = np.union1d(near, idx[h, q, :cnt[h, q]])
+                assert ocnt[h, q] == want.size
+                assert np.array_equal(out[h, q, :want.size], want)
+                assert np.all(out[h, q, want.size:] == -1)
+    empty = np.full((1, Nc, 1), -1, np.int32)
+    out, ocnt, _ = oracle_mod.lut_add_neighbors(empty, np.zeros((1, Nc), np.int32), T, H, W, 1, 27)
+    interior = (1 * Hc + 1) * Wc + 1
+    assert ocnt[0, interior] == 27 and ocnt[0, 0] == 8
