@@ -74,7 +74,7 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
 // One CTA per (batch, head).  Shared memory: overlap[Nc][kWindow] (uint16),
 // partner[Nc], pick[Nc], rank list[Nc] (int16).
 __global__ void __launch_bounds__(kPlanThreads) plan_pairs_kernel(const uint32_t* __restrict__ bits, int Nc, int nwords,
-                                                                  int32_t* __restrict__ pairs) {
+                                                                  int stage_bits, int32_t* __restrict__ pairs) {
   extern __shared__ uint8_t smem[];
   uint16_t* ov = reinterpret_cast<uint16_t*>(smem);  // ov[c * kWindow + d - 1] = |list c & list c+d|
   int16_t* partner = reinterpret_cast<int16_t*>(ov + static_cast<size_t>(Nc) * kWindow);
@@ -84,6 +84,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_pairs_kernel(const uint32_t
   const int64_t bh = blockIdx.x;
   const uint32_t* B = bits + bh * Nc * nwords;
   const int tid = threadIdx.x;
+  if (stage_bits) {
+    // The head's bit matrix fits: read it from shared memory (16-byte aligned
+    // after the int16 arrays).
+    uint32_t* sb = reinterpret_cast<uint32_t*>(smem + ((static_cast<size_t>(Nc) * (kWindow * 2 + 6) + 15) & ~size_t(15)));
+    for (int i = tid; i < Nc * nwords; i += blockDim.x) sb[i] = B[i];
+    B = sb;
+    __syncthreads();
+  }
 
   for (int it = tid; it < Nc * kWindow; it += blockDim.x) {
     const int c = it / kWindow, d = it % kWindow + 1;
@@ -162,6 +170,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_pairs_kernel(const uint32_t
 }  // namespace
 
 size_t pair_plan_smem(int Nc) { return static_cast<size_t>(Nc) * (kWindow * 2 + 3 * 2); }
+size_t pair_plan_smem_staged(int Nc) {
+  return ((pair_plan_smem(Nc) + 15) & ~size_t(15)) + sizeof(uint32_t) * static_cast<size_t>(Nc) * ((Nc + 31) / 32);
+}
 
 int launch_list_bits(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, uint32_t* bits,
                      cudaStream_t s) {
@@ -177,12 +188,13 @@ int launch_list_bits(const int32_t* idx, const int32_t* cnt, int kmax, int BH, i
 
 int launch_pair_plan(const uint32_t* bits, int BH, int Nc, int32_t* pairs, cudaStream_t s) {
   if (Nc > 32767) return VSA_ERR_UNSUPPORTED;
-  const size_t smem = pair_plan_smem(Nc);
+  const bool staged = pair_plan_smem_staged(Nc) <= 200 * 1024;
+  const size_t smem = staged ? pair_plan_smem_staged(Nc) : pair_plan_smem(Nc);
   if (smem > 200 * 1024) return VSA_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(plan_pairs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return VSA_ERR_CUDA;
-  plan_pairs_kernel<<<BH, kPlanThreads, smem, s>>>(bits, Nc, (Nc + 31) / 32, pairs);
+  plan_pairs_kernel<<<BH, kPlanThreads, smem, s>>>(bits, Nc, (Nc + 31) / 32, staged ? 1 : 0, pairs);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
