@@ -44,18 +44,6 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 }
 __device__ __forceinline__ float f16_lo(uint32_t v) { return __low2float(*reinterpret_cast<const __half2*>(&v)); }
 __device__ __forceinline__ float f16_hi(uint32_t v) { return __high2float(*reinterpret_cast<const __half2*>(&v)); }
-template <bool F16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
-}
-template <bool F16>
-__device__ __forceinline__ float lo2(uint32_t v) {
-  return F16 ? f16_lo(v) : bf16_lo(v);
-}
-template <bool F16>
-__device__ __forceinline__ float hi2(uint32_t v) {
-  return F16 ? f16_hi(v) : bf16_hi(v);
-}
 
 // Store 8 consecutive floats as bf16 (16 bytes) or f32 (32 bytes).
 __device__ __forceinline__ void store8(void* base, int64_t elem, const float* v, int dtype) {

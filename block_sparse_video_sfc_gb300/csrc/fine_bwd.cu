@@ -87,9 +87,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -136,28 +133,6 @@ __device__ __forceinline__ void load_cube_pair(uint8_t* dst, const CUtensorMap* 
   }
 }
 
-// A x B^T over d for two 128-row K-major tiles (S = Q K^T style), D/16 MMAs.
-template <int D>
-__device__ __forceinline__ void mma_rows_x_rows(uint32_t dtm, const uint8_t* a, const uint8_t* b) {
-  constexpr uint32_t id = idesc_f32acc(128, 128, 0, 0, 1);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const int blk = kk >> 2, w = kk & 3;
-    mma_ss(dtm, sdesc_sw128(smem_u32(a + blk * 16384 + w * 32), 16, 1024),
-           sdesc_sw128(smem_u32(b + blk * 16384 + w * 32), 16, 1024), id, kk > 0);
-  }
-}
-// D(+)= A(TMEM) x B (128 rows x D, MN-major view of a row tile), 8 MMAs of
-// K = 16.  A is 128 x 128 packed fp16 held as two 64-wide K halves of 32
-// columns each, at columns atm and atm + 64 (one half per compute warpgroup).
-template <int D>
-__device__ __forceinline__ void mma_tmem_x_rows(uint32_t dtm, uint32_t atm, const uint8_t* b, bool accumulate) {
-  constexpr uint32_t id = idesc_f32acc(128, D, 0, 1, 1);
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk)
-    mma_ts(dtm, atm + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(smem_u32(b + kk * 2048), 16384, 1024), id,
-           (accumulate || kk > 0) ? 1u : 0u);
-}
 
 // =============================================================== dK, dV
 // One CTA per pair of key cubes (128 key rows, K and V resident in shared
@@ -681,21 +656,21 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
     tc_fence_after();
     // ---------------- dQ rows (warpgroup g writes columns [g*D/2, (g+1)*D/2))
 #pragma unroll
-    for (int c0 = 0; c0 < D / 2; c0 += 16) {
+    for (int c0 = 0; c0 < D / 2; c0 += 32) {
       const int c = g * (D / 2) + c0;
-      float v[16];
+      uint32_t a[32];
       if (steps > 0 && ok) {
-        tmem_ld16(lane_addr + kDqDQ + c, v);
-        tmem_wait_ld();
+        tmem_ld32_wait(lane_addr + kDqDQ + c, a);
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        for (int i = 0; i < 32; ++i) a[i] = 0u;
       }
+      float v[32];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] *= p.scale;
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(a[i]) * p.scale;
       if (row_valid) {
-        store8(p.dq, grow * D + c, v, VSA_DTYPE_F32);
-        store8(p.dq, grow * D + c + 8, v + 8, VSA_DTYPE_F32);
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) store8(p.dq, grow * D + c + i, v + i, VSA_DTYPE_F32);
       }
     }
   }

@@ -92,15 +92,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// 2D tile reduce-add (fp32 +=) from shared memory into global memory through
-// a tensor map; completion is tracked with bulk groups of the issuing thread.
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* smem_src, int x, int y) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(smem_src)), "r"(x), "r"(y)
-      : "memory");
-}
 // Plain (untiled) bulk copy global -> shared, completing on an mbarrier.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -108,17 +99,6 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
                    smem_u32(smem_dst)),
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until at most N bulk groups still read their shared-memory source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Wait until at most N bulk groups are still in flight.
-template <int N>
-__device__ __forceinline__ void bulk_wait() {
-  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -146,9 +126,6 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int a_mn, int 
          | (static_cast<uint32_t>(b_mn) << 16)       // B major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
-}
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
-  return idesc_f32acc(M, N, a_mn, b_mn, 0);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]; issued by a single thread.
@@ -180,43 +157,16 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-// 32 lanes x 32 bits, 16 consecutive columns: thread t of the warp gets lane
-// (warp's lane quarter)*32 + t, columns col..col+15.  The destination
-// registers are written asynchronously: call tmem_wait_ld() right after the
-// loads and before anything else touches those registers (the compiler does
-// not know the asm's outputs arrive late and may move them in between).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])));
-}
-// 8-column variants (thread t: lane quarter*32 + t, columns col..col+7).
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-}
+// TMEM loads: thread t of a warp reads lane (warp's lane quarter) * 32 + t.
+// The destination registers of tcgen05.ld are written asynchronously and the
+// compiler does not know that, so every load helper below issues the loads
+// and tcgen05.wait::ld inside ONE asm statement: the outputs are complete
+// when the statement ends.  (Issuing a load in one statement and waiting in
+// another let the compiler read the registers in between and gave wrong dK.)
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
                "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
 }
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 64 consecutive columns loaded AND waited for inside one asm statement, so
@@ -277,11 +227,5 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t* r) {
       : "memory");
 }
 
-// Byte offset of element (row, col) inside a 128B-swizzled tile whose rows
-// hold 64 bf16 (col in [0, 64)).
-__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
-  uint32_t chunk = (col >> 3) ^ (row & 7);
-  return row * 128u + chunk * 16u + (col & 7u) * 2u;
-}
 
 }  // namespace vsa
