@@ -37,10 +37,11 @@ import synth  # noqa: E402
 METRIC = "VSA fwd+bwd effective TFLOPS at 32K tokens, 70% sparsity; % of bf16 tensor peak"
 UNIT = "TFLOP/s"
 # libvsa kernels launched by one forward + backward step: permute_pool,
-# coarse_topk, build_list_bits, plan_pairs, fine_fwd, combine | bwd_prep,
-# coarse_bwd_rows, coarse_atb (x2), build_inverse_bits, plan_pairs,
-# fine_bwd_kv, fine_bwd_dq, finalize.
-KERNELS_PER_STEP = 15
+# coarse_gemm, topk_rows, coarse_gemm, build_list_bits, pair_overlap,
+# plan_pairs, fine_fwd, combine | bwd_prep, coarse_gemm, bwd_rows, coarse_gemm,
+# build_inverse_bits, pair_overlap, plan_pairs, fine_bwd_kv, fine_bwd_dq,
+# finalize.
+KERNELS_PER_STEP = 19
 WORKLOAD = "wan1.3b"
 
 

@@ -94,6 +94,7 @@ int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_
                     int kmax, int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, int f16_in,
                     const int32_t* pairs, cudaStream_t s);
 size_t pair_plan_smem(int Nc);
+size_t pair_plan_ws_bytes(int BH, int Nc);  // pairs + overlap scratch of launch_pair_plan
 int launch_list_bits(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, uint32_t* bits,
                      cudaStream_t s);
 int launch_pair_plan(const uint32_t* bits, int BH, int Nc, int32_t* pairs, cudaStream_t s);

@@ -751,7 +751,7 @@ size_t fine_bwd_ws_bytes(int BH, int N, int kmax) {
   size_t inv = sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords;
   size_t delta = sizeof(float) * static_cast<size_t>(BH) * N;
   size_t copy = sizeof(__half) * static_cast<size_t>(BH) * N * 128;  // room for d <= 128
-  size_t kpairs = sizeof(int32_t) * static_cast<size_t>(BH) * ((Nc + 1) / 2) * 2;
+  size_t kpairs = pair_plan_ws_bytes(BH, static_cast<int>(Nc));
   return ((inv + 255) & ~size_t(255)) + ((delta + 255) & ~size_t(255)) + 4 * ((copy + 255) & ~size_t(255)) +
          ((kpairs + 255) & ~size_t(255));
 }

@@ -72,37 +72,39 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
   return res;
 }
 
-// One CTA per (batch, head).  Shared memory: overlap[Nc][kWindow] (uint16),
-// partner[Nc], pick[Nc], rank list[Nc] (int16).
-__global__ void __launch_bounds__(kPlanThreads) plan_pairs_kernel(const uint32_t* __restrict__ bits, int Nc, int nwords,
-                                                                  int stage_bits, int32_t* __restrict__ pairs) {
-  extern __shared__ uint8_t smem[];
+// ov[bh][c][d - 1] = |list c & list c + d| for d = 1..kWindow (0 past the
+// last cube): one thread per (cube, offset), spread over the whole GPU.
+__global__ void __launch_bounds__(256) pair_overlap_kernel(const uint32_t* __restrict__ bits, int Nc, int nwords,
+                                                           uint16_t* __restrict__ ov) {
+  const int64_t bh = blockIdx.y;
+  const int it = blockIdx.x * blockDim.x + threadIdx.x;
+  if (it >= Nc * kWindow) return;
+  const int c = it / kWindow, d = it % kWindow + 1;
+  int n = 0;
+  if (c + d < Nc) {
+    const uint32_t* a = bits + (bh * Nc + c) * nwords;
+    const uint32_t* b = a + static_cast<int64_t>(d) * nwords;
+    for (int w = 0; w < nwords; ++w) n += __popc(__ldg(a + w) & __ldg(b + w));
+  }
+  ov[bh * Nc * kWindow + it] = static_cast<uint16_t>(n);
+}
+
+// One CTA per (batch, head).  Shared memory: the head's overlaps
+// [Nc][kWindow] (uint16), partner[Nc], pick[Nc], rank list[Nc] (int16).
+__global__ void __launch_bounds__(kPlanThreads) plan_pairs_kernel(const uint16_t* __restrict__ ov_g, int Nc,
+                                                                  int32_t* __restrict__ pairs) {
+  extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* ov = reinterpret_cast<uint16_t*>(smem);  // ov[c * kWindow + d - 1] = |list c & list c+d|
   int16_t* partner = reinterpret_cast<int16_t*>(ov + static_cast<size_t>(Nc) * kWindow);
   int16_t* pick = partner + Nc;
   int16_t* order = pick + Nc;
   __shared__ int scan_scratch[33];
   const int64_t bh = blockIdx.x;
-  const uint32_t* B = bits + bh * Nc * nwords;
   const int tid = threadIdx.x;
-  if (stage_bits) {
-    // The head's bit matrix fits: read it from shared memory (16-byte aligned
-    // after the int16 arrays).
-    uint32_t* sb = reinterpret_cast<uint32_t*>(smem + ((static_cast<size_t>(Nc) * (kWindow * 2 + 6) + 15) & ~size_t(15)));
-    for (int i = tid; i < Nc * nwords; i += blockDim.x) sb[i] = B[i];
-    B = sb;
-    __syncthreads();
-  }
-
-  for (int it = tid; it < Nc * kWindow; it += blockDim.x) {
-    const int c = it / kWindow, d = it % kWindow + 1;
-    int n = 0;
-    if (c + d < Nc) {
-      const uint32_t* a = B + static_cast<int64_t>(c) * nwords;
-      const uint32_t* b = B + static_cast<int64_t>(c + d) * nwords;
-      for (int w = 0; w < nwords; ++w) n += __popc(a[w] & b[w]);
-    }
-    ov[it] = static_cast<uint16_t>(n);
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(ov_g + bh * Nc * kWindow);  // kWindow * 2 B = 4 x 16 B per cube
+    uint4* dst = reinterpret_cast<uint4*>(ov);
+    for (int i = tid; i < Nc * kWindow / 8; i += blockDim.x) dst[i] = src[i];
   }
   for (int c = tid; c < Nc; c += blockDim.x) partner[c] = -1;
   __syncthreads();
@@ -171,8 +173,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_pairs_kernel(const uint32_t
 }  // namespace
 
 size_t pair_plan_smem(int Nc) { return static_cast<size_t>(Nc) * (kWindow * 2 + 3 * 2); }
-size_t pair_plan_smem_staged(int Nc) {
-  return ((pair_plan_smem(Nc) + 15) & ~size_t(15)) + sizeof(uint32_t) * static_cast<size_t>(Nc) * ((Nc + 31) / 32);
+static size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+size_t pair_plan_ws_bytes(int BH, int Nc) {
+  return a256(sizeof(int32_t) * static_cast<size_t>(BH) * ((Nc + 1) / 2) * 2) +
+         a256(sizeof(uint16_t) * static_cast<size_t>(BH) * Nc * kWindow);
 }
 
 int launch_list_bits(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, uint32_t* bits,
@@ -187,15 +191,20 @@ int launch_list_bits(const int32_t* idx, const int32_t* cnt, int kmax, int BH, i
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
-int launch_pair_plan(const uint32_t* bits, int BH, int Nc, int32_t* pairs, cudaStream_t s) {
+// pairs_ws: pair_plan_ws_bytes(BH, Nc) bytes; the pairs come first, the
+// overlap scratch after them.
+int launch_pair_plan(const uint32_t* bits, int BH, int Nc, int32_t* pairs_ws, cudaStream_t s) {
   if (Nc > 32767) return VSA_ERR_UNSUPPORTED;
-  const bool staged = pair_plan_smem_staged(Nc) <= 200 * 1024;
-  const size_t smem = staged ? pair_plan_smem_staged(Nc) : pair_plan_smem(Nc);
+  const size_t smem = pair_plan_smem(Nc);
   if (smem > 200 * 1024) return VSA_ERR_UNSUPPORTED;
+  uint16_t* ov = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(pairs_ws) +
+                                             a256(sizeof(int32_t) * static_cast<size_t>(BH) * ((Nc + 1) / 2) * 2));
+  dim3 g1((Nc * kWindow + 255) / 256, BH);
+  pair_overlap_kernel<<<g1, 256, 0, s>>>(bits, Nc, (Nc + 31) / 32, ov);
   if (cudaFuncSetAttribute(plan_pairs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return VSA_ERR_CUDA;
-  plan_pairs_kernel<<<BH, kPlanThreads, smem, s>>>(bits, Nc, (Nc + 31) / 32, staged ? 1 : 0, pairs);
+  plan_pairs_kernel<<<BH, kPlanThreads, smem, s>>>(ov, Nc, pairs_ws);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 

@@ -39,7 +39,7 @@ int check_grid(const vsa_grid_t& g, int d, Dims* out, int64_t BH) {
 
 // Forward workspace: the saved state of one vsa_forward call.
 struct FwdWs {
-  size_t qp, kp, vp, qc, kc, vc, oc, lsec, idx, cnt, of, lse, lbits, pairs, total;
+  size_t qp, kp, vp, qc, kc, vc, oc, lsec, sc, idx, cnt, of, lse, lbits, pairs, total;
 };
 FwdWs fwd_layout(const Dims& D, int K) {
   FwdWs w{};
@@ -54,12 +54,13 @@ FwdWs fwd_layout(const Dims& D, int K) {
   w.vc = o; o += align256(pooled);
   w.oc = o; o += align256(pooled);
   w.lsec = o; o += align256(sizeof(float) * D.BH * D.Nc);
+  w.sc = o; o += align256(sizeof(float) * D.BH * D.Nc * D.Nc);
   w.idx = o; o += align256(sizeof(int32_t) * D.BH * D.Nc * K);
   w.cnt = o; o += align256(sizeof(int32_t) * D.BH * D.Nc);
   w.of = o; o += align256(sizeof(float) * D.BH * D.N * D.d);
   w.lse = o; o += align256(sizeof(float) * D.BH * D.N);
   w.lbits = o; o += align256(sizeof(uint32_t) * D.BH * D.Nc * ((D.Nc + 31) / 32));
-  w.pairs = o; o += align256(sizeof(int32_t) * D.BH * ((D.Nc + 1) / 2) * 2);
+  w.pairs = o; o += align256(pair_plan_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.Nc)));
   w.total = o;
   return w;
 }
@@ -86,7 +87,7 @@ BwdWs bwd_layout(const Dims& D) {
   w.dkp = o; o += align256(big_f32);
   w.dvp = o; o += align256(big_f32);
   w.inv = o; o += align256(sizeof(uint32_t) * D.BH * D.Nc * nwords);
-  w.kpairs = o; o += align256(sizeof(int32_t) * D.BH * ((D.Nc + 1) / 2) * 2);
+  w.kpairs = o; o += align256(pair_plan_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.Nc)));
   w.total = o;
   return w;
 }
@@ -270,8 +271,9 @@ int vsa_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, i
   if (d != 64 && d != 128) return VSA_ERR_UNSUPPORTED;
   if (BH <= 0 || Nc <= 0) return VSA_ERR_ARG;
   if (topk < 1 || topk > Nc) return VSA_ERR_ARG;
-  if (!qc || !kc || !kv_block_idx || (o_coarse && !vc)) return VSA_ERR_ARG;
-  if (!aligned16(qc) || !aligned16(kc) || (vc && !aligned16(vc)) || (o_coarse && !aligned16(o_coarse)))
+  if (!qc || !kc || !kv_block_idx || !scores || (o_coarse && (!vc || !lse_coarse))) return VSA_ERR_ARG;
+  if (!aligned16(qc) || !aligned16(kc) || (vc && !aligned16(vc)) || (o_coarse && !aligned16(o_coarse)) ||
+      !aligned16(scores))
     return VSA_ERR_ARG;
   return launch_coarse_topk(qc, kc, vc, BH, Nc, d, topk, scale, o_coarse, lse_coarse, kv_block_idx,
                             valid_block_num, scores, as_stream(stream));
@@ -372,7 +374,7 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
   float* pooled[3] = {at<float>(ws, w.qc), at<float>(ws, w.kc), at<float>(ws, w.vc)};
   if ((st = launch_permute(src, dst, pooled, 3, BH, d, g.T, g.H, g.W, 0, 1, s)) != VSA_OK) return st;
   if ((st = launch_coarse_topk(pooled[0], pooled[1], pooled[2], BH, Nc, d, topk, scale, at<float>(ws, w.oc),
-                               at<float>(ws, w.lsec), at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), nullptr, s)) !=
+                               at<float>(ws, w.lsec), at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), at<float>(ws, w.sc), s)) !=
       VSA_OK)
     return st;
   // Pair query cubes whose lists overlap most into the fine kernels' tiles.

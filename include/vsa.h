@@ -97,11 +97,16 @@ int vsa_permute(const void* x, void* y, float* pooled, int BH, int d, vsa_grid_t
  *   topk        1 <= topk <= Nc.
  *   scale       score scale (1/sqrt(d) for the SDPA one).
  *   o_coarse    fp32 [BH, Nc, d] or NULL: softmax(scale*Qc Kc^T) Vc.
- *   lse_coarse  fp32 [BH, Nc] or NULL: log-sum-exp of each score row.
+ *   lse_coarse  fp32 [BH, Nc]: log-sum-exp of each score row; may be NULL
+ *               only when o_coarse is NULL.
  *   kv_block_idx    int32 [BH, Nc, topk]: selected key cubes, highest first.
  *   valid_block_num int32 [BH, Nc] or NULL: set to topk.
- *   scores      fp32 [BH, Nc, Nc] or NULL: the scaled coarse scores (for
- *               inspection; costs Nc^2 writes per head).
+ *   scores      fp32 [BH, Nc, Nc], 16-byte aligned, required: receives the
+ *               scaled coarse scores, which the selection and O_c read back
+ *               (the caller's scratch; the library allocates nothing).
+ * The score matrix comes from one tiled fp32 product, the selection and the
+ * log-sum-exp from one warp per row, and O_c from a second product that
+ * applies the row softmax as it loads the scores.
  */
 int vsa_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk,
                     float scale, float* o_coarse, float* lse_coarse, int32_t* kv_block_idx,
