@@ -49,24 +49,26 @@ def _load():
             I = ctypes.c_int
             D = ctypes.c_double
             sig = {
-                "orc_sfc_position": ([I, I, I, I, I, I], I64),
-                "orc_sfc_table": ([I, I, I, P], None),
-                "orc_permute": ([P, P, I64, I, I, I, I, I], None),
+                "orc_hilbert_point": ([ctypes.c_uint64, I, P], None),
+                "orc_cube_rank": ([I, I, I, I, P], None),
+                "orc_sfc_position": ([I, I, I, I, I, I, P], I64),
+                "orc_sfc_table": ([I, I, I, P, P], None),
+                "orc_permute": ([P, P, I64, I, I, I, I, P, I], None),
                 "orc_pool": ([P, P, I64, I64, I], None),
                 "orc_coarse": ([P, P, P, I64, I, I, D, P, P, P], None),
                 "orc_topk": ([P, I64, I, I, P], None),
                 "orc_fine_fwd": ([P, P, P, P, P, I, I64, I64, I, D, P, P], None),
                 "orc_fine_fwd_rows": ([P, P, P, P, P, I, I64, I64, I, D, P, I64, P, P], None),
                 "orc_combine": ([P, P, P, P, I64, I64, I, P], None),
-                "orc_forward": ([P, P, P, P, P, I64, I, I, I, I, I, D, P, P, P, P, P, P, P], None),
+                "orc_forward": ([P, P, P, P, P, I64, I, I, I, I, P, I, D, P, P, P, P, P, P, P], None),
                 "orc_fine_bwd": ([P, P, P, P, P, P, I, I64, I64, I, D, P, P, P], None),
                 "orc_coarse_bwd": ([P, P, P, P, I64, I, I, D, P, P, P], None),
-                "orc_backward": ([P, P, P, P, P, I64, I, I, I, I, I, D, P, P, P, P, P, P, P], None),
+                "orc_backward": ([P, P, P, P, P, I64, I, I, I, I, P, I, D, P, P, P, P, P, P, P], None),
                 "orc_fine_bwd_query_rows": ([P, P, P, P, P, P, I, I64, I, D, P, I64, P], None),
                 "orc_fine_bwd_key_cube": ([P, P, P, P, P, P, I, I64, I, D, I64, I, P, P], None),
                 "orc_combine_bwd": ([P, P, P, P, P, I64, I64, I, P, P, P, P], None),
                 "orc_mask_to_lut": ([P, I64, I, I, P, P, P], None),
-                "orc_lut_add_neighbors": ([P, P, I, I64, I, I, I, I, I, P, P, P], None),
+                "orc_lut_add_neighbors": ([P, P, I, I64, I, I, I, P, I, I, P, P, P], None),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -99,18 +101,40 @@ def default_scale(d: int) -> float:
     return 1.0 / np.sqrt(d)
 
 
-def sfc_table(T: int, H: int, W: int) -> np.ndarray:
+CURVES = {"raster": 0, "hilbert": 1}
+
+
+def hilbert_point(hidx: int, b: int):
+    """(t, h, w) of index hidx on the order-b 3-D Hilbert curve."""
+    x = np.zeros(3, dtype=np.uint32)
+    _load().orc_hilbert_point(hidx, b, _p(x))
+    return tuple(int(v) for v in x)
+
+
+def cube_rank(Tc: int, Hc: int, Wc: int, curve: str = "raster") -> np.ndarray:
+    """rank[raster cube id] = the cube's position in the cube sequence."""
+    rank = np.empty(Tc * Hc * Wc, dtype=np.int32)
+    _load().orc_cube_rank(Tc, Hc, Wc, CURVES[curve], _p(rank))
+    return rank
+
+
+def _rank_of(T: int, H: int, W: int, curve: str):
+    return None if curve == "raster" else cube_rank(T // 4, H // 4, W // 4, curve)
+
+
+def sfc_table(T: int, H: int, W: int, curve: str = "raster") -> np.ndarray:
     """pos[n]: reordered position of native token n = (t*H + h)*W + w."""
     pos = np.empty(T * H * W, dtype=np.int64)
-    _load().orc_sfc_table(T, H, W, _p(pos))
+    _load().orc_sfc_table(T, H, W, _p(_rank_of(T, H, W, curve)), _p(pos))
     return pos
 
 
-def permute(x, T: int, H: int, W: int, inverse: bool = False) -> np.ndarray:
+def permute(x, T: int, H: int, W: int, inverse: bool = False, curve: str = "raster") -> np.ndarray:
     x = _f64(x)
     BH, N, d = _bh(x)
     y = np.empty_like(x)
-    _load().orc_permute(_p(x), _p(y), BH, d, T, H, W, int(bool(inverse)))
+    rank = _rank_of(T, H, W, curve)
+    _load().orc_permute(_p(x), _p(y), BH, d, T, H, W, _p(rank), int(bool(inverse)))
     return y
 
 
@@ -182,7 +206,7 @@ def combine(gc, gf, oc, of) -> np.ndarray:
 
 
 def forward(q, k, v, T: int, H: int, W: int, K: int, scale=None,
-            gc=None, gf=None, lut=None, want_scores: bool = True):
+            gc=None, gf=None, lut=None, want_scores: bool = True, curve: str = "raster"):
     """Whole forward pass (native order in/out).
 
     Returns a dict with out, idx, of, lse, oc and scores.
@@ -202,7 +226,8 @@ def forward(q, k, v, T: int, H: int, W: int, K: int, scale=None,
     oc = np.empty(lead + (Nc, d), dtype=np.float64)
     scores = np.empty(lead + (Nc, Nc), dtype=np.float64) if want_scores else None
     lut = _i32(lut)
-    _load().orc_forward(_p(q), _p(k), _p(v), _p(gc), _p(gf), BH, d, T, H, W, K,
+    rank = _rank_of(T, H, W, curve)
+    _load().orc_forward(_p(q), _p(k), _p(v), _p(gc), _p(gf), BH, d, T, H, W, _p(rank), K,
                         float(scale), _p(lut), _p(out), _p(idx), _p(of), _p(lse),
                         _p(oc), _p(scores))
     return dict(out=out, idx=idx, of=of, lse=lse, oc=oc, scores=scores)
@@ -264,7 +289,7 @@ def coarse_bwd(qc, kc, vc, doc, scale: float):
 
 
 def backward(q, k, v, dout, idx, T: int, H: int, W: int, scale=None,
-             gc=None, gf=None):
+             gc=None, gf=None, curve: str = "raster"):
     """Whole backward pass; returns dict dq, dk, dv, dgc, dgf (native order)."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     gc, gf = _f64(gc), _f64(gf)
@@ -276,7 +301,8 @@ def backward(q, k, v, dout, idx, T: int, H: int, W: int, scale=None,
     dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
     dgc = np.empty_like(q) if gc is not None else None
     dgf = np.empty_like(q) if gf is not None else None
-    _load().orc_backward(_p(q), _p(k), _p(v), _p(gc), _p(gf), BH, d, T, H, W, K,
+    rank = _rank_of(T, H, W, curve)
+    _load().orc_backward(_p(q), _p(k), _p(v), _p(gc), _p(gf), BH, d, T, H, W, _p(rank), K,
                          float(scale), _p(idx), _p(dout), _p(dq), _p(dk), _p(dv),
                          _p(dgc), _p(dgf))
     return dict(dq=dq, dk=dk, dv=dv, dgc=dgc, dgf=dgf)
@@ -295,7 +321,8 @@ def mask_to_lut(mask, max_kv_blocks: int):
     return idx, cnt, bool(ovf.value)
 
 
-def lut_add_neighbors(idx, cnt, T: int, H: int, W: int, radius: int, max_kv_blocks: int):
+def lut_add_neighbors(idx, cnt, T: int, H: int, W: int, radius: int, max_kv_blocks: int,
+                      curve: str = "raster"):
     """Lists united with the radius-r cube neighbourhood -> (idx, cnt, overflow)."""
     idx = _i32(idx)
     cnt = None if cnt is None else _i32(cnt)
@@ -305,6 +332,8 @@ def lut_add_neighbors(idx, cnt, T: int, H: int, W: int, radius: int, max_kv_bloc
     out = np.empty(idx.shape[:-1] + (max_kv_blocks,), dtype=np.int32)
     ocnt = np.empty(idx.shape[:-1], dtype=np.int32)
     ovf = ctypes.c_int(0)
-    _load().orc_lut_add_neighbors(_p(idx), _p(cnt), kin, BH, Tc, Hc, Wc, radius, max_kv_blocks, _p(out), _p(ocnt),
+    rank = _rank_of(T, H, W, curve)
+    _load().orc_lut_add_neighbors(_p(idx), _p(cnt), kin, BH, Tc, Hc, Wc, _p(rank), radius, max_kv_blocks, _p(out),
+                                  _p(ocnt),
                                   ctypes.byref(ovf))
     return out, ocnt, bool(ovf.value)

@@ -21,9 +21,14 @@
  *        Abstract.
  *
  * Readings where the pages are silent:
- *  - The 3D space-filling curve is cube-raster order: cubes of (4,4,4) tokens
- *    in (t/4, h/4, w/4) raster order, tokens inside a cube in
- *    (t%4, h%4, w%4) raster order.
+ *  - The 3D space-filling curve orders cubes of (4,4,4) tokens; tokens inside
+ *    a cube stay in (t%4, h%4, w%4) raster order.  Two cube orders are
+ *    provided: cube-raster order (t/4, h/4, w/4) -- the default -- and the
+ *    3-D Hilbert curve of the enclosing power-of-two cube grid with the cells
+ *    outside the grid skipped ("clipped" Hilbert order; the curve itself is
+ *    J. Skilling's, "Programming the Hilbert curve", AIP Conf. Proc. 707,
+ *    2004).  Every function taking `rank` uses rank[raster cube id] as the
+ *    cube's position in the sequence; rank == NULL means raster order.
  *  - Coarse scores carry the SDPA scale (the pseudocode einsum in [AMD]
  *    "Generating Sparsity Patterns" shows none; Top-K is unaffected).
  *  - The coarse output is softmax(Sc) Vc over all cubes, broadcast to the
@@ -48,36 +53,99 @@
  * Token Reordering": tokens are remapped so that each fixed-size block of the
  * 1D sequence is a contiguous spatio-temporal region. */
 
+/* Point x[0..2] (t, h, w) of the 3-D Hilbert curve of order b (a side of
+ * 2^b cells) at curve index hidx, following Skilling's construction read
+ * from index to point: the index's bits, taken three at a time from the
+ * top, form the "transposed" coordinates (the first of each three bits goes
+ * to t, the second to h, the third to w); these are Gray-decoded, and the
+ * rotations and reflections the curve applies at each level are then undone
+ * from the lowest level up. */
+void orc_hilbert_point(uint64_t hidx, int b, uint32_t x[3])
+{
+    x[0] = x[1] = x[2] = 0;
+    for (int level = b - 1; level >= 0; level--)
+        for (int a = 0; a < 3; a++)
+            x[a] |= (uint32_t)((hidx >> (3 * level + 2 - a)) & 1u) << level;
+    if (b == 0)
+        return;
+    /* Gray decode: each axis takes the parity of the axes before it; the
+     * first axis takes the last axis shifted down one level. */
+    uint32_t carry = x[2] >> 1;
+    x[2] ^= x[1];
+    x[1] ^= x[0];
+    x[0] ^= carry;
+    /* Undo the per-level transforms, low level first. */
+    for (uint32_t bit = 2; bit < (1u << b); bit <<= 1) {
+        uint32_t low = bit - 1;
+        for (int a = 2; a >= 0; a--) {
+            if (x[a] & bit) {
+                x[0] ^= low;               /* reflection of the low bits */
+            } else {
+                uint32_t swap = (x[0] ^ x[a]) & low;  /* exchange with axis 0 */
+                x[0] ^= swap;
+                x[a] ^= swap;
+            }
+        }
+    }
+}
+
+/* rank[c] = position of raster cube c = (ct * Hc + ch) * Wc + cw in the cube
+ * sequence.  curve 0: raster order (rank[c] = c).  curve 1: clipped Hilbert
+ * order -- walk the Hilbert curve of the smallest 2^b >= max(Tc, Hc, Wc)
+ * cube grid and number the cells that lie inside the grid in the order the
+ * curve meets them. */
+void orc_cube_rank(int Tc, int Hc, int Wc, int curve, int32_t *rank)
+{
+    const int64_t Nc = (int64_t)Tc * Hc * Wc;
+    if (curve == 0) {
+        for (int64_t c = 0; c < Nc; c++)
+            rank[c] = (int32_t)c;
+        return;
+    }
+    int b = 0;
+    while ((1 << b) < Tc || (1 << b) < Hc || (1 << b) < Wc)
+        b++;
+    int32_t next = 0;
+    for (uint64_t hidx = 0; hidx < ((uint64_t)1 << (3 * b)); hidx++) {
+        uint32_t x[3];
+        orc_hilbert_point(hidx, b, x);
+        if (x[0] < (uint32_t)Tc && x[1] < (uint32_t)Hc && x[2] < (uint32_t)Wc)
+            rank[((int64_t)x[0] * Hc + x[1]) * Wc + x[2]] = next++;
+    }
+}
+
 /* Position in the reordered sequence of native token (t, h, w). */
-int64_t orc_sfc_position(int t, int h, int w, int T, int H, int W)
+int64_t orc_sfc_position(int t, int h, int w, int T, int H, int W, const int32_t *rank)
 {
     (void)T;
     int64_t cube_t = t / 4, cube_h = h / 4, cube_w = w / 4;
     int64_t cubes_h = H / 4, cubes_w = W / 4;
     int64_t cube = (cube_t * cubes_h + cube_h) * cubes_w + cube_w;
+    if (rank)
+        cube = rank[cube];
     int64_t off = ((int64_t)(t % 4) * 4 + (h % 4)) * 4 + (w % 4);
     return cube * CUBE + off;
 }
 
 /* pos[n] = reordered position of the native token n = (t*H + h)*W + w. */
-void orc_sfc_table(int T, int H, int W, int64_t *pos)
+void orc_sfc_table(int T, int H, int W, const int32_t *rank, int64_t *pos)
 {
     for (int t = 0; t < T; t++)
         for (int h = 0; h < H; h++)
             for (int w = 0; w < W; w++) {
                 int64_t n = ((int64_t)t * H + h) * W + w;
-                pos[n] = orc_sfc_position(t, h, w, T, H, W);
+                pos[n] = orc_sfc_position(t, h, w, T, H, W, rank);
             }
 }
 
 /* inverse == 0: y[pos[n]] = x[n] (native -> cube order);
  * inverse != 0: y[n] = x[pos[n]] (cube order -> native). */
 void orc_permute(const double *x, double *y, int64_t BH, int d,
-                 int T, int H, int W, int inverse)
+                 int T, int H, int W, const int32_t *rank, int inverse)
 {
     int64_t N = (int64_t)T * H * W;
     int64_t *pos = (int64_t *)malloc(sizeof(int64_t) * N);
-    orc_sfc_table(T, H, W, pos);
+    orc_sfc_table(T, H, W, rank, pos);
 #pragma omp parallel for
     for (int64_t bh = 0; bh < BH; bh++)
         for (int64_t n = 0; n < N; n++) {
@@ -292,7 +360,7 @@ void orc_combine(const double *gc, const double *gf, const double *oc,
  *   (reordered order); oc [BH, Nc, d]; scores [BH, Nc, Nc] (may be NULL). */
 void orc_forward(const double *q, const double *k, const double *v,
                  const double *gc, const double *gf, int64_t BH, int d,
-                 int T, int H, int W, int K, double scale,
+                 int T, int H, int W, const int32_t *rank, int K, double scale,
                  const int32_t *lut_in, double *out, int32_t *idx,
                  double *of, double *lse, double *oc, double *scores)
 {
@@ -302,9 +370,9 @@ void orc_forward(const double *q, const double *k, const double *v,
     double *qc = (double *)malloc(small), *kc = (double *)malloc(small), *vc = (double *)malloc(small);
     double *sc = scores ? scores : (double *)malloc(sizeof(double) * BH * Nc * Nc);
     int32_t *cnt = (int32_t *)malloc(sizeof(int32_t) * BH * Nc);
-    orc_permute(q, qp, BH, d, T, H, W, 0);
-    orc_permute(k, kp, BH, d, T, H, W, 0);
-    orc_permute(v, vp, BH, d, T, H, W, 0);
+    orc_permute(q, qp, BH, d, T, H, W, rank, 0);
+    orc_permute(k, kp, BH, d, T, H, W, rank, 0);
+    orc_permute(v, vp, BH, d, T, H, W, rank, 0);
     orc_pool(qp, qc, BH, N, d);
     orc_pool(kp, kc, BH, N, d);
     orc_pool(vp, vc, BH, N, d);
@@ -319,14 +387,14 @@ void orc_forward(const double *q, const double *k, const double *v,
     double *gcp = NULL, *gfp = NULL, *outp = (double *)malloc(big);
     if (gc) {
         gcp = (double *)malloc(big);
-        orc_permute(gc, gcp, BH, d, T, H, W, 0);
+        orc_permute(gc, gcp, BH, d, T, H, W, rank, 0);
     }
     if (gf) {
         gfp = (double *)malloc(big);
-        orc_permute(gf, gfp, BH, d, T, H, W, 0);
+        orc_permute(gf, gfp, BH, d, T, H, W, rank, 0);
     }
     orc_combine(gcp, gfp, oc, of, BH, N, d, outp);
-    orc_permute(outp, out, BH, d, T, H, W, 1);
+    orc_permute(outp, out, BH, d, T, H, W, rank, 1);
     free(qp); free(kp); free(vp); free(qc); free(kc); free(vc);
     if (!scores) free(sc);
     free(cnt); free(gcp); free(gfp); free(outp);
@@ -628,7 +696,7 @@ void orc_coarse_bwd(const double *qc, const double *kc, const double *vc,
  * dq, dk, dv [BH, N, d]; dgc, dgf [BH, N, d] (ignored when the gate is NULL). */
 void orc_backward(const double *q, const double *k, const double *v,
                   const double *gc, const double *gf, int64_t BH, int d,
-                  int T, int H, int W, int K, double scale, const int32_t *idx,
+                  int T, int H, int W, const int32_t *rank, int K, double scale, const int32_t *idx,
                   const double *dout, double *dq, double *dk, double *dv,
                   double *dgc, double *dgf)
 {
@@ -648,9 +716,9 @@ void orc_backward(const double *q, const double *k, const double *v,
         cnt[r] = K;
 
     /* Recompute the forward intermediates. */
-    orc_permute(q, qp, BH, d, T, H, W, 0);
-    orc_permute(k, kp, BH, d, T, H, W, 0);
-    orc_permute(v, vp, BH, d, T, H, W, 0);
+    orc_permute(q, qp, BH, d, T, H, W, rank, 0);
+    orc_permute(k, kp, BH, d, T, H, W, rank, 0);
+    orc_permute(v, vp, BH, d, T, H, W, rank, 0);
     orc_pool(qp, qc, BH, N, d);
     orc_pool(kp, kc, BH, N, d);
     orc_pool(vp, vc, BH, N, d);
@@ -658,16 +726,16 @@ void orc_backward(const double *q, const double *k, const double *v,
     orc_fine_fwd(qp, kp, vp, idx, cnt, K, BH, N, d, scale, of, lse);
 
     /* Gated combination out_p = gc*Oc[cube] + gf*Of, differentiated. */
-    orc_permute(dout, dop, BH, d, T, H, W, 0);
+    orc_permute(dout, dop, BH, d, T, H, W, rank, 0);
     if (gc)
-        orc_permute(gc, gcp, BH, d, T, H, W, 0);
+        orc_permute(gc, gcp, BH, d, T, H, W, rank, 0);
     if (gf)
-        orc_permute(gf, gfp, BH, d, T, H, W, 0);
+        orc_permute(gf, gfp, BH, d, T, H, W, rank, 0);
     orc_combine_bwd(dop, gc ? gcp : NULL, gf ? gfp : NULL, oc, of, BH, N, d, dof, doc, dgcp, dgfp);
     if (gc && dgc)
-        orc_permute(dgcp, dgc, BH, d, T, H, W, 1);
+        orc_permute(dgcp, dgc, BH, d, T, H, W, rank, 1);
     if (gf && dgf)
-        orc_permute(dgfp, dgf, BH, d, T, H, W, 1);
+        orc_permute(dgfp, dgf, BH, d, T, H, W, rank, 1);
 
     orc_fine_bwd(qp, kp, vp, dof, idx, cnt, K, BH, N, d, scale, dqp, dkp, dvp);
     orc_coarse_bwd(qc, kc, vc, doc, BH, (int)Nc, d, scale, dqc, dkc, dvc);
@@ -681,9 +749,9 @@ void orc_backward(const double *q, const double *k, const double *v,
                 dkp[e] += dkc[ec] / CUBE;
                 dvp[e] += dvc[ec] / CUBE;
             }
-    orc_permute(dqp, dq, BH, d, T, H, W, 1);
-    orc_permute(dkp, dk, BH, d, T, H, W, 1);
-    orc_permute(dvp, dv, BH, d, T, H, W, 1);
+    orc_permute(dqp, dq, BH, d, T, H, W, rank, 1);
+    orc_permute(dkp, dk, BH, d, T, H, W, rank, 1);
+    orc_permute(dvp, dv, BH, d, T, H, W, rank, 1);
 
     free(qp); free(kp); free(vp); free(qc); free(kc); free(vc); free(oc); free(of);
     free(lse); free(dop); free(gcp); free(gfp); free(dgcp); free(dgfp); free(dof); free(doc);
@@ -726,13 +794,19 @@ void orc_mask_to_lut(const unsigned char *mask, int64_t rows, int Nc, int kmax, 
 
 /* The list of every query cube united with all cubes whose cube-grid
  * coordinates (t, h, w) each differ from the query cube's by at most
- * `radius`.  Cube id c = (t * Hc + h) * Wc + w. */
+ * `radius`.  Cube ids are positions in the cube sequence: raster cube
+ * (t * Hc + h) * Wc + w sits at position rank[raster id] (rank NULL: the
+ * raster id itself). */
 void orc_lut_add_neighbors(const int32_t *idx_in, const int32_t *cnt_in, int kin, int64_t BH, int Tc, int Hc,
-                           int Wc, int radius, int kout, int32_t *idx_out, int32_t *cnt_out, int *overflow)
+                           int Wc, const int32_t *rank, int radius, int kout, int32_t *idx_out, int32_t *cnt_out,
+                           int *overflow)
 {
     const int Nc = Tc * Hc * Wc;
     *overflow = 0;
     unsigned char *sel = (unsigned char *)malloc((size_t)Nc);
+    int *raster_of = (int *)malloc(sizeof(int) * (size_t)Nc);  /* position -> raster id */
+    for (int r = 0; r < Nc; r++)
+        raster_of[rank ? rank[r] : r] = r;
     for (int64_t bh = 0; bh < BH; bh++) {
         for (int q = 0; q < Nc; q++) {
             const int64_t row = bh * Nc + q;
@@ -747,9 +821,11 @@ void orc_lut_add_neighbors(const int32_t *idx_in, const int32_t *cnt_in, int kin
                 if (c >= 0 && c < Nc)
                     sel[c] = 1;
             }
-            const int qt = q / (Hc * Wc), qh = (q / Wc) % Hc, qw = q % Wc;
+            const int qr = raster_of[q];
+            const int qt = qr / (Hc * Wc), qh = (qr / Wc) % Hc, qw = qr % Wc;
             for (int c = 0; c < Nc; c++) {
-                const int t = c / (Hc * Wc), h = (c / Wc) % Hc, w = c % Wc;
+                const int cr = raster_of[c];
+                const int t = cr / (Hc * Wc), h = (cr / Wc) % Hc, w = cr % Wc;
                 if (abs(t - qt) <= radius && abs(h - qh) <= radius && abs(w - qw) <= radius)
                     sel[c] = 1;
             }
@@ -757,4 +833,5 @@ void orc_lut_add_neighbors(const int32_t *idx_in, const int32_t *cnt_in, int kin
         }
     }
     free(sel);
+    free(raster_of);
 }

@@ -59,7 +59,7 @@ def test_sfc_golden_positions(oracle_mod):
     for case in g["cases"]:
         T, H, W = case["grid"]
         for (t, h, w), p in case["positions"]:
-            assert oracle_mod._load().orc_sfc_position(t, h, w, T, H, W) == p
+            assert oracle_mod._load().orc_sfc_position(t, h, w, T, H, W, None) == p
 
 
 # ---------------------------------------------------------------------------
@@ -400,3 +400,80 @@ def test_lut_add_neighbors_brute_force(oracle_mod):
     out, ocnt, _ = oracle_mod.lut_add_neighbors(empty, np.zeros((1, Nc), np.int32), T, H, W, 1, 27)
     interior = (1 * Hc + 1) * Wc + 1
     assert ocnt[0, interior] == 27 and ocnt[0, 0] == 8
+
+
+# ---------------------------------------------------------------- Hilbert cube order
+# The curve of Skilling's construction ("Programming the Hilbert curve", 2004)
+# is pinned by the properties that define a Hilbert curve, not by retyping it:
+# every cell visited once, unit steps between consecutive cells, and the
+# recursive structure (each aligned run of 8^k indices fills one aligned
+# 2^k cube), starting at the origin.
+@pytest.mark.parametrize("b", [1, 2, 3, 4])
+def test_hilbert_curve_is_continuous_and_nested(oracle_mod, b):
+    pts = np.array([oracle_mod.hilbert_point(h, b) for h in range(8 ** b)], dtype=np.int64)
+    assert len({tuple(p) for p in pts}) == 8 ** b and pts.max() == 2 ** b - 1
+    assert np.all(np.abs(np.diff(pts, axis=0)).sum(1) == 1)
+    assert tuple(pts[0]) == (0, 0, 0)
+    for k in range(1, b):
+        blk = pts.reshape(-1, 8 ** k, 3)
+        lo, hi = blk.min(1), blk.max(1)
+        assert np.all(hi - lo == 2 ** k - 1) and np.all(lo % 2 ** k == 0)
+
+
+@pytest.mark.parametrize("grid", [(1, 1, 1), (1, 2, 2), (2, 4, 8), (3, 5, 7), (4, 4, 4)])
+def test_cube_rank_follows_the_curve(oracle_mod, grid):
+    Tc, Hc, Wc = grid
+    rank = oracle_mod.cube_rank(Tc, Hc, Wc, "hilbert")
+    Nc = Tc * Hc * Wc
+    assert sorted(rank.tolist()) == list(range(Nc))
+    assert np.array_equal(oracle_mod.cube_rank(Tc, Hc, Wc, "raster"), np.arange(Nc))
+    # positions in curve order -> grid cells; brute force over the enclosing curve
+    b = max(int(np.ceil(np.log2(max(grid)))), 0)
+    inside = [p for p in (oracle_mod.hilbert_point(h, b) for h in range(8 ** b))
+              if p[0] < Tc and p[1] < Hc and p[2] < Wc]
+    order = np.argsort(rank)
+    cells = [((r // (Hc * Wc)), (r // Wc) % Hc, r % Wc) for r in order]
+    assert cells == inside
+    if grid == (4, 4, 4):   # a full power-of-two grid: consecutive cubes are face neighbours
+        c = np.array(cells)
+        assert np.all(np.abs(np.diff(c, axis=0)).sum(1) == 1)
+
+
+def test_forward_backward_invariant_to_cube_order(oracle_mod):
+    """The cube order only relabels cubes: native-order outputs and gradients
+    are the same for raster and Hilbert order (no score ties in this data),
+    and the selected cubes are the same grid cells."""
+    wl = synth.Workload("ord", 1, 2, 64, 8, 8, 16, 5)   # cube grid (2, 2, 4)
+    q, k, v = synth.make_qkv(wl)
+    gc, gf = synth.make_gates(wl)
+    dout = synth.make_dout(wl)
+    ra = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=gc, gf=gf)
+    hi = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=gc, gf=gf, curve="hilbert")
+    np.testing.assert_allclose(hi["out"], ra["out"], rtol=0, atol=1e-12)
+    rank = oracle_mod.cube_rank(2, 2, 4, "hilbert")
+    order = np.argsort(rank)                       # position -> raster cube
+    sets_h = np.sort(order[hi["idx"]], axis=-1)[..., rank, :]   # per raster query cube
+    np.testing.assert_array_equal(sets_h, np.sort(ra["idx"], axis=-1))
+    ga = oracle_mod.backward(q, k, v, dout, ra["idx"], wl.T, wl.H, wl.W, gc=gc, gf=gf)
+    gh = oracle_mod.backward(q, k, v, dout, hi["idx"], wl.T, wl.H, wl.W, gc=gc, gf=gf, curve="hilbert")
+    for n in ("dq", "dk", "dv", "dgc", "dgf"):
+        np.testing.assert_allclose(gh[n], ga[n], rtol=0, atol=1e-12)
+
+
+def test_add_neighbors_is_order_independent(oracle_mod):
+    """Neighbourhoods are grid cells: with Hilbert ids the lists map back to
+    the raster-order result."""
+    T, H, W = 12, 8, 20        # cube grid (3, 2, 5)
+    Tc, Hc, Wc = 3, 2, 5
+    Nc = Tc * Hc * Wc
+    rank = oracle_mod.cube_rank(Tc, Hc, Wc, "hilbert")
+    order = np.argsort(rank)
+    rng = np.random.default_rng(3)
+    idx_r = np.stack([rng.permutation(Nc)[:4] for _ in range(Nc)]).astype(np.int32)[None]
+    out_r, cnt_r, _ = oracle_mod.lut_add_neighbors(idx_r, None, T, H, W, 1, Nc)
+    idx_h = rank[idx_r][:, order]            # relabel entries and reorder rows by position
+    out_h, cnt_h, _ = oracle_mod.lut_add_neighbors(idx_h, None, T, H, W, 1, Nc, curve="hilbert")
+    np.testing.assert_array_equal(cnt_h[:, rank], cnt_r)
+    for r in range(Nc):
+        got = np.sort(order[out_h[0, rank[r], :cnt_h[0, rank[r]]]])
+        np.testing.assert_array_equal(got, out_r[0, r, :cnt_r[0, r]])
