@@ -53,7 +53,7 @@ def step_flops(wl: synth.Workload) -> dict:
     return dict(fine_fwd=fine_fwd, fine_bwd=fine_bwd, coarse=coarse, total=fine_fwd + fine_bwd + coarse)
 
 
-def config_of(wl: synth.Workload, parallelism: str) -> dict:
+def config_of(wl: synth.Workload, parallelism: str, curve: str = "raster") -> dict:
     return {
         "workload": (f"{wl.name}: B={wl.B}, heads={wl.heads}, d={wl.d}, grid (T,H,W)=({wl.T},{wl.H},{wl.W}) = "
                      f"{wl.N} tokens, {wl.Nc} cubes of (4,4,4), Top-K={wl.topk} "
@@ -67,6 +67,7 @@ def config_of(wl: synth.Workload, parallelism: str) -> dict:
         "l2": "inputs larger than L2: 6 bf16 tensors of 100.7 MB per step (Q,K,V,gates,dO)",
         "inputs": "synthetic smooth field + noise (synth.py), seed base 20250519",
         "out_dtype": "bf16", "grad_dtype": "bf16",
+        "cube_order": curve,
     }
 
 
@@ -196,9 +197,11 @@ def run_ours(args, rank: int, world: int):
                       dtype=torch.uint8, device=dev)
     bws = torch.empty(vsa.workspace_bytes(1, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk),
                       dtype=torch.uint8, device=dev)
+    order = None if args.curve == "raster" else vsa.cube_order(wl.T, wl.H, wl.W, args.curve, device=dev)
 
     def step(qd, kd, vd, gcd, gfd, dod):
-        _, st = vsa.forward(qd, kd, vd, wl.T, wl.H, wl.W, wl.topk, g_coarse=gcd, g_fine=gfd, out=out, ws=fws)
+        _, st = vsa.forward(qd, kd, vd, wl.T, wl.H, wl.W, wl.topk, g_coarse=gcd, g_fine=gfd, out=out, ws=fws,
+                            cube_order=order)
         vsa.backward(st, dod, g_coarse=gcd, g_fine=gfd, grads=grads, ws=bws)
 
     def barrier():
@@ -294,7 +297,7 @@ def run_ours(args, rank: int, world: int):
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded smooth field + noise; Wan2.1 activations are not available)",
-        "config": config_of(wl, "replicas" if world > 1 else "single GPU"),
+        "config": config_of(wl, "replicas" if world > 1 else "single GPU", args.curve),
         "pct_of_peak": round(100 * value / world / peaks["tflops"], 2),
         "roofline": {"bound": "tensor", "kernel": dominant, "achieved": roof(dominant)["tflops"],
                      "peak": peaks["tflops"], "unit": "TFLOP/s", "frac": roof(dominant)["frac"],
@@ -359,6 +362,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--curve", choices=["raster", "hilbert"], default="raster",
+                    help="cube order of the space-filling-curve reordering")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -17,7 +17,7 @@ import torch
 from . import _lib
 from ._lib import Grid, VSAError, VSA_DTYPE_BF16, VSA_DTYPE_F32
 
-__all__ = ["permute", "coarse_topk", "fine_fwd", "fine_bwd", "forward", "backward",
+__all__ = ["cube_order", "permute", "coarse_topk", "fine_fwd", "fine_bwd", "forward", "backward",
            "workspace_bytes", "device_status", "timing_enable", "timing_read", "VSAError",
            "ForwardState", "Grid"]
 
@@ -46,7 +46,18 @@ def _bhnd(x: torch.Tensor):
     raise ValueError("expected [B, heads, N, d] or [BH, N, d]")
 
 
-def permute(x: torch.Tensor, T: int, H: int, W: int, inverse: bool = False, pool: bool = False):
+def cube_order(T: int, H: int, W: int, curve: str = "hilbert", device="cuda") -> torch.Tensor:
+    """vsa_cube_order: int32 [2 * Nc] table (position -> raster cube id, then
+    raster cube id -> position) for curve "raster" or "hilbert"."""
+    Nc = (T // 4) * (H // 4) * (W // 4)
+    order = torch.empty(2 * Nc, dtype=torch.int32, device=device)
+    code = {"raster": _lib.VSA_CURVE_RASTER, "hilbert": _lib.VSA_CURVE_HILBERT}[curve]
+    _lib.check("vsa_cube_order", _lib.load().vsa_cube_order(Grid.of(T, H, W), code, _ptr(order), _stream()))
+    return order
+
+
+def permute(x: torch.Tensor, T: int, H: int, W: int, inverse: bool = False, pool: bool = False,
+            cube_order=None):
     """vsa_permute: native <-> cube order; with pool=True also the cube means."""
     BH, N, d = _bhnd(x)
     y = torch.empty_like(x)
@@ -54,7 +65,8 @@ def permute(x: torch.Tensor, T: int, H: int, W: int, inverse: bool = False, pool
     if pool:
         pooled = torch.empty(x.shape[:-2] + (N // 64, d), dtype=torch.float32, device=x.device)
     _lib.check("vsa_permute", _lib.load().vsa_permute(_ptr(x), _ptr(y), _ptr(pooled), BH, d,
-                                                       Grid.of(T, H, W), int(inverse), _stream()))
+                                                       Grid.of(T, H, W, _ptr(cube_order)), int(inverse),
+                                                       _stream()))
     return (y, pooled) if pool else y
 
 
@@ -89,7 +101,7 @@ def mask_to_lut(mask, max_kv_blocks: int):
     return idx, cnt
 
 
-def lut_add_neighbors(idx, cnt, T: int, H: int, W: int, radius: int, max_kv_blocks: int):
+def lut_add_neighbors(idx, cnt, T: int, H: int, W: int, radius: int, max_kv_blocks: int, cube_order=None):
     """vsa_lut_add_neighbors: list united with the radius-r cube neighbourhood -> (idx, cnt)."""
     Nc, kin = idx.shape[-2], idx.shape[-1]
     BH = idx.numel() // (Nc * kin)
@@ -97,7 +109,8 @@ def lut_add_neighbors(idx, cnt, T: int, H: int, W: int, radius: int, max_kv_bloc
     out = torch.empty(lead + (Nc, max_kv_blocks), dtype=torch.int32, device=idx.device)
     ocnt = torch.empty(lead + (Nc,), dtype=torch.int32, device=idx.device)
     _lib.check("vsa_lut_add_neighbors", _lib.load().vsa_lut_add_neighbors(
-        _ptr(idx), _ptr(cnt), kin, BH, Grid.of(T, H, W), radius, max_kv_blocks, _ptr(out), _ptr(ocnt),
+        _ptr(idx), _ptr(cnt), kin, BH, Grid.of(T, H, W, _ptr(cube_order)), radius, max_kv_blocks, _ptr(out),
+        _ptr(ocnt),
         _stream()))
     return out, ocnt
 
@@ -147,6 +160,7 @@ class ForwardState:
     W: int
     topk: int
     scale: float
+    cube_order: Optional[torch.Tensor] = None
 
     def saved(self) -> dict:
         """Views of the saved intermediates as torch tensors."""
@@ -179,7 +193,7 @@ class ForwardState:
 
 
 def forward(q, k, v, T: int, H: int, W: int, topk: int, g_coarse=None, g_fine=None,
-            scale: Optional[float] = None, out_dtype=torch.bfloat16, out=None, ws=None):
+            scale: Optional[float] = None, out_dtype=torch.bfloat16, out=None, ws=None, cube_order=None):
     """vsa_forward on native-order [B, heads, N, d] bf16 -> (out, ForwardState)."""
     B, heads, N, d = q.shape
     scale = d ** -0.5 if scale is None else scale
@@ -191,9 +205,9 @@ def forward(q, k, v, T: int, H: int, W: int, topk: int, g_coarse=None, g_fine=No
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     _lib.check("vsa_forward", _lib.load().vsa_forward(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g_coarse), _ptr(g_fine), B, heads, d, Grid.of(T, H, W), topk,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g_coarse), _ptr(g_fine), B, heads, d, Grid.of(T, H, W, _ptr(cube_order)), topk,
         float(scale), _ptr(out), _DT[out.dtype], _ptr(ws), nbytes, _stream()))
-    return out, ForwardState(ws, B, heads, d, T, H, W, topk, scale)
+    return out, ForwardState(ws, B, heads, d, T, H, W, topk, scale, cube_order)
 
 
 def backward(state: ForwardState, dout, g_coarse=None, g_fine=None, grad_dtype=torch.float32,
@@ -210,7 +224,7 @@ def backward(state: ForwardState, dout, g_coarse=None, g_fine=None, grad_dtype=t
     dt = grads["dq"].dtype
     _lib.check("vsa_backward", _lib.load().vsa_backward(
         _ptr(state.ws), _ptr(g_coarse), _ptr(g_fine), _ptr(dout), B, heads, d,
-        Grid.of(state.T, state.H, state.W), state.topk, float(state.scale), _ptr(grads["dq"]),
+        Grid.of(state.T, state.H, state.W, _ptr(state.cube_order)), state.topk, float(state.scale), _ptr(grads["dq"]),
         _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads.get("dgc")), _ptr(grads.get("dgf")), _DT[dt],
         _ptr(ws), nbytes, _stream()))
     return grads

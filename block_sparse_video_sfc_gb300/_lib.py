@@ -27,6 +27,8 @@ VSA_DTYPE_F32 = 1
 VSA_OP_FORWARD = 0
 VSA_OP_BACKWARD = 1
 VSA_OP_FINE_BWD = 2
+VSA_CURVE_RASTER = 0
+VSA_CURVE_HILBERT = 1
 
 # Every function the header declares, with its ctypes signature.
 P = ctypes.c_void_p
@@ -36,13 +38,14 @@ SZ = ctypes.c_size_t
 
 
 class Grid(ctypes.Structure):
-    """vsa_grid_t: latent grid (T, H, W) and cube shape (must be 4, 4, 4)."""
+    """vsa_grid_t: latent grid (T, H, W), cube shape (must be 4, 4, 4) and the
+    device address of a cube order table (0: cube-raster order)."""
 
-    _fields_ = [("T", I), ("H", I), ("W", I), ("ct", I), ("ch", I), ("cw", I)]
+    _fields_ = [("T", I), ("H", I), ("W", I), ("ct", I), ("ch", I), ("cw", I), ("cube_order", P)]
 
     @classmethod
-    def of(cls, T, H, W):
-        return cls(T, H, W, 4, 4, 4)
+    def of(cls, T, H, W, cube_order=None):
+        return cls(T, H, W, 4, 4, 4, cube_order)
 
 
 class Saved(ctypes.Structure):
@@ -54,6 +57,7 @@ class Saved(ctypes.Structure):
 
 SIGNATURES = {
     "vsa_permute": ([P, P, P, I, I, Grid, I, P], I),
+    "vsa_cube_order": ([Grid, I, P, P], I),
     "vsa_coarse_topk": ([P, P, P, I, I, I, I, F, P, P, P, P, P, P], I),
     "vsa_fine_fwd": ([P, P, P, P, P, I, I, I, I, F, P, I, P, P], I),
     "vsa_fine_bwd": ([P, P, P, P, I, P, P, P, P, I, I, I, I, F, P, P, P, P, SZ, P], I),

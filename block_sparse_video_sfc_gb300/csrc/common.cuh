@@ -29,6 +29,10 @@ __host__ __device__ __forceinline__ int64_t native_token(int cube, int o, int H,
   return (static_cast<int64_t>(t) * H + h) * W + w;
 }
 
+// Raster id of the cube at position `pos` of the cube sequence: the first
+// half of a vsa_cube_order table, or pos itself when there is none.
+__device__ __forceinline__ int raster_cube(const int32_t* order, int pos) { return order ? __ldg(order + pos) : pos; }
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -85,7 +89,8 @@ void timing_mark(int kernel, bool begin, cudaStream_t s);
 int num_sms();                     // SM count of the current device
 
 int launch_permute(const void* const* src, void* const* dst, float* const* pooled, int ntensors, int BH,
-                   int d, int T, int H, int W, int inverse, int f16_out, cudaStream_t s);
+                   int d, int T, int H, int W, const int32_t* order, int inverse, int f16_out, cudaStream_t s);
+int launch_cube_order(int Tc, int Hc, int Wc, int curve, int32_t* order, cudaStream_t s);
 int make_tile_map(void* map, const void* base, int64_t rows, int d, int f16);
 int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk,
                        float scale, float* oc, float* lse_c, int32_t* idx, int32_t* cnt, float* scores,
@@ -100,7 +105,8 @@ int launch_list_bits(const int32_t* idx, const int32_t* cnt, int kmax, int BH, i
 int launch_pair_plan(const uint32_t* bits, int BH, int Nc, int32_t* pairs, cudaStream_t s);
 int launch_mask_to_lut(const uint8_t* mask, int BH, int Nc, int kmax, int32_t* idx, int32_t* cnt, cudaStream_t s);
 int launch_add_neighbors(const int32_t* idx_in, const int32_t* cnt_in, int kmax_in, int BH, int Tc, int Hc, int Wc,
-                         int radius, int kmax_out, int32_t* idx_out, int32_t* cnt_out, cudaStream_t s);
+                         const int32_t* order, int radius, int kmax_out, int32_t* idx_out, int32_t* cnt_out,
+                         cudaStream_t s);
 size_t fine_bwd_ws_bytes(int BH, int N, int kmax);
 int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* of, int of_dtype,
                     const float* lse, const void* dof, const int32_t* idx, const int32_t* cnt, int kmax, int BH,
@@ -111,15 +117,15 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
                          float scale, float* dq, float* dk, float* dv, uint32_t* inv_ws, const int32_t* qpairs,
                          int32_t* kpairs_ws, cudaStream_t s);
 int launch_combine(const float* oc, const float* of, const void* gc, const void* gf, void* out, int out_dtype,
-                   int BH, int d, int T, int H, int W, cudaStream_t s);
+                   int BH, int d, int T, int H, int W, const int32_t* order, cudaStream_t s);
 int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const float* oc, const float* of,
                     __half* dof, float* delta, float* doc, void* dgc, void* dgf, int grad_dtype, int BH, int d,
-                    int T, int H, int W, cudaStream_t s);
+                    int T, int H, int W, const int32_t* order, cudaStream_t s);
 int launch_coarse_bwd(const float* qc, const float* kc, const float* vc, const float* doc, const float* lse_c,
                       int BH, int Nc, int d, float scale, float* P, float* dS, float* dqc, float* dkc, float* dvc,
                       cudaStream_t s);
 int launch_finalize(const float* dqp, const float* dkp, const float* dvp, const float* dqc, const float* dkc,
                     const float* dvc, void* dq, void* dk, void* dv, int grad_dtype, int BH, int d, int T, int H,
-                    int W, cudaStream_t s);
+                    int W, const int32_t* order, cudaStream_t s);
 
 }  // namespace vsa

@@ -10,6 +10,8 @@
 //   vsa_mask_to_lut        B (one byte per cell) -> ascending list + count
 //   vsa_lut_add_neighbors  list -> list united with every cube within a
 //                          Chebyshev radius on the (T/4, H/4, W/4) cube grid
+//                          (ids are positions in the cube sequence; a cube
+//                          order table maps them to and from grid cells)
 //
 // Both write each row's cubes in ascending id, the count, and -1 in the
 // unused slots.  A row with more cubes than the output holds keeps its first
@@ -72,7 +74,9 @@ __global__ void __launch_bounds__(kRowThreads) mask_to_lut_kernel(const uint8_t*
 
 __global__ void __launch_bounds__(kRowThreads) add_neighbors_kernel(const int32_t* __restrict__ idx_in,
                                                                     const int32_t* __restrict__ cnt_in, int kmax_in,
-                                                                    int Tc, int Hc, int Wc, int radius, int kmax_out,
+                                                                    int Tc, int Hc, int Wc,
+                                                                    const int32_t* __restrict__ order, int radius,
+                                                                    int kmax_out,
                                                                     int32_t* __restrict__ idx_out,
                                                                     int32_t* __restrict__ cnt_out, int* err) {
   extern __shared__ uint32_t bits[];
@@ -96,12 +100,14 @@ __global__ void __launch_bounds__(kRowThreads) add_neighbors_kernel(const int32_
   }
   // The neighbourhood: every cube whose grid coordinates differ from the
   // query cube's by at most `radius` in each of t, h, w (the cube itself too).
-  const int qt = q / (Hc * Wc), qh = (q / Wc) % Hc, qw = q % Wc;
+  const int qr = raster_cube(order, q);
+  const int qt = qr / (Hc * Wc), qh = (qr / Wc) % Hc, qw = qr % Wc;
   const int side = 2 * radius + 1, count = side * side * side;
   for (int e = threadIdx.x; e < count; e += blockDim.x) {
     const int t = qt + e / (side * side) - radius, h = qh + (e / side) % side - radius, w = qw + e % side - radius;
     if (t < 0 || t >= Tc || h < 0 || h >= Hc || w < 0 || w >= Wc) continue;
-    const int c = (t * Hc + h) * Wc + w;
+    const int r = (t * Hc + h) * Wc + w;
+    const int c = order ? __ldg(order + Nc + r) : r;  // raster id -> position
     atomicOr(&bits[c >> 5], 1u << (c & 31));
   }
   __syncthreads();
@@ -120,13 +126,14 @@ int launch_mask_to_lut(const uint8_t* mask, int BH, int Nc, int kmax, int32_t* i
 }
 
 int launch_add_neighbors(const int32_t* idx_in, const int32_t* cnt_in, int kmax_in, int BH, int Tc, int Hc, int Wc,
-                         int radius, int kmax_out, int32_t* idx_out, int32_t* cnt_out, cudaStream_t s) {
+                         const int32_t* order, int radius, int kmax_out, int32_t* idx_out, int32_t* cnt_out,
+                         cudaStream_t s) {
   const int Nc = Tc * Hc * Wc;
   const int64_t rows = static_cast<int64_t>(BH) * Nc;
   if (rows == 0) return VSA_OK;
   const size_t smem = sizeof(uint32_t) * ((Nc + 31) / 32);
   add_neighbors_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, s>>>(
-      idx_in, cnt_in, kmax_in, Tc, Hc, Wc, radius, kmax_out, idx_out, cnt_out, device_error_word());
+      idx_in, cnt_in, kmax_in, Tc, Hc, Wc, order, radius, kmax_out, idx_out, cnt_out, device_error_word());
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 

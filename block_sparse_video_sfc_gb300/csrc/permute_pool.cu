@@ -22,7 +22,7 @@ struct PermuteArgs {
 // magnitude <= 65504; larger ones saturate and latch kErrRange).
 template <int D, bool F16OUT>
 __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc, int H, int W, int N,
-                                                           int inverse, int* err) {
+                                                           const int32_t* __restrict__ order, int inverse, int* err) {
   constexpr int kChunks = D / 8;           // 16-byte chunks per token
   constexpr int kTokPerPass = 256 / kChunks;
   constexpr int kPasses = kCube / kTokPerPass;
@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc
   const int64_t cube_glob = blockIdx.x;    // bh * Nc + cube
   const int64_t bh = cube_glob / Nc;
   const int cube = static_cast<int>(cube_glob % Nc);
+  const int rcube = raster_cube(order, cube);
   const __nv_bfloat16* src = a.src[tensor] + bh * static_cast<int64_t>(N) * D;
   uint16_t* dst = static_cast<uint16_t*>(a.dst[tensor]) + bh * static_cast<int64_t>(N) * D;
   float* pooled = a.pooled[tensor];
@@ -40,7 +41,7 @@ __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc
 #pragma unroll
   for (int p = 0; p < kPasses; ++p) {
     const int o = o0 + p * kTokPerPass;
-    const int64_t nat = native_token(cube, o, H, W);
+    const int64_t nat = native_token(rcube, o, H, W);
     const int64_t cub = static_cast<int64_t>(cube) * kCube + o;
     const int64_t s_tok = inverse ? cub : nat;
     const int64_t d_tok = inverse ? nat : cub;
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc
 }
 
 int launch_permute(const void* const* src, void* const* dst, float* const* pooled, int ntensors, int BH, int d,
-                   int T, int H, int W, int inverse, int f16_out, cudaStream_t s) {
+                   int T, int H, int W, const int32_t* order, int inverse, int f16_out, cudaStream_t s) {
   PermuteArgs a{};
   for (int i = 0; i < ntensors; ++i) {
     a.src[i] = static_cast<const __nv_bfloat16*>(src[i]);
@@ -91,14 +92,14 @@ int launch_permute(const void* const* src, void* const* dst, float* const* poole
   timing_mark(VSA_K_PERMUTE, true, s);
   if (d == 128) {
     if (f16_out)
-      permute_pool_kernel<128, true><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse, err);
+      permute_pool_kernel<128, true><<<grid, 256, 0, s>>>(a, Nc, H, W, N, order, inverse, err);
     else
-      permute_pool_kernel<128, false><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse, err);
+      permute_pool_kernel<128, false><<<grid, 256, 0, s>>>(a, Nc, H, W, N, order, inverse, err);
   } else {
     if (f16_out)
-      permute_pool_kernel<64, true><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse, err);
+      permute_pool_kernel<64, true><<<grid, 256, 0, s>>>(a, Nc, H, W, N, order, inverse, err);
     else
-      permute_pool_kernel<64, false><<<grid, 256, 0, s>>>(a, Nc, H, W, N, inverse, err);
+      permute_pool_kernel<64, false><<<grid, 256, 0, s>>>(a, Nc, H, W, N, order, inverse, err);
   }
   timing_mark(VSA_K_PERMUTE, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;

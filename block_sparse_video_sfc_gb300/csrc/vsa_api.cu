@@ -31,6 +31,7 @@ int check_grid(const vsa_grid_t& g, int d, Dims* out, int64_t BH) {
   if (d != 64 && d != 128) return VSA_ERR_UNSUPPORTED;
   if (g.T <= 0 || g.H <= 0 || g.W <= 0 || BH <= 0) return VSA_ERR_ARG;
   if (g.T % 4 || g.H % 4 || g.W % 4) return VSA_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(g.cube_order) & 3u) return VSA_ERR_ARG;
   const int64_t N = static_cast<int64_t>(g.T) * g.H * g.W;
   if (N * BH >= (int64_t(1) << 31)) return VSA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
   *out = Dims{BH, N, N / kCube, d, g.T, g.H, g.W};
@@ -228,7 +229,17 @@ int vsa_lut_add_neighbors(const int32_t* kv_block_idx_in, const int32_t* valid_b
   if (max_kv_blocks_in < 1 || max_kv_blocks_out < 1 || radius < 0 || radius > 7) return VSA_ERR_ARG;
   if (D.Nc > (1 << 16)) return VSA_ERR_UNSUPPORTED;
   return launch_add_neighbors(kv_block_idx_in, valid_block_num_in, max_kv_blocks_in, BH, g.T / 4, g.H / 4, g.W / 4,
-                              radius, max_kv_blocks_out, kv_block_idx_out, valid_block_num_out, as_stream(stream));
+                              g.cube_order, radius, max_kv_blocks_out, kv_block_idx_out, valid_block_num_out, as_stream(stream));
+}
+
+int vsa_cube_order(vsa_grid_t g, int curve, int32_t* order, void* stream) {
+  g.cube_order = nullptr;
+  Dims D;
+  int st = check_grid(g, 128, &D, 1);
+  if (st != VSA_OK) return st;
+  if (!order || (reinterpret_cast<uintptr_t>(order) & 3u)) return VSA_ERR_ARG;
+  if (curve != VSA_CURVE_RASTER && curve != VSA_CURVE_HILBERT) return VSA_ERR_ARG;
+  return launch_cube_order(g.T / 4, g.H / 4, g.W / 4, curve, order, as_stream(stream));
 }
 
 int vsa_selftest_wait_timeout(uint32_t polls, void* stream) {
@@ -262,7 +273,7 @@ int vsa_permute(const void* x, void* y, float* pooled, int BH, int d, vsa_grid_t
   const void* src[1] = {x};
   void* dst[1] = {y};
   float* pl[1] = {pooled};
-  return launch_permute(src, dst, pl, 1, BH, d, g.T, g.H, g.W, inverse, 0, as_stream(stream));
+  return launch_permute(src, dst, pl, 1, BH, d, g.T, g.H, g.W, g.cube_order, inverse, 0, as_stream(stream));
 }
 
 int vsa_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk, float scale,
@@ -372,7 +383,7 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
   const void* src[3] = {q, k, v};
   void* dst[3] = {at<void>(ws, w.qp), at<void>(ws, w.kp), at<void>(ws, w.vp)};
   float* pooled[3] = {at<float>(ws, w.qc), at<float>(ws, w.kc), at<float>(ws, w.vc)};
-  if ((st = launch_permute(src, dst, pooled, 3, BH, d, g.T, g.H, g.W, 0, 1, s)) != VSA_OK) return st;
+  if ((st = launch_permute(src, dst, pooled, 3, BH, d, g.T, g.H, g.W, g.cube_order, 0, 1, s)) != VSA_OK) return st;
   if ((st = launch_coarse_topk(pooled[0], pooled[1], pooled[2], BH, Nc, d, topk, scale, at<float>(ws, w.oc),
                                at<float>(ws, w.lsec), at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), at<float>(ws, w.sc), s)) !=
       VSA_OK)
@@ -387,7 +398,7 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
                             at<int32_t>(ws, w.pairs), s)) != VSA_OK)
     return st;
   return launch_combine(at<float>(ws, w.oc), at<float>(ws, w.of), g_coarse, g_fine, out, out_dtype, BH, d, g.T, g.H,
-                        g.W, s);
+                        g.W, g.cube_order, s);
 }
 
 int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, const void* dout, int B, int heads,
@@ -412,7 +423,7 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
   if ((st = launch_bwd_prep(dout, g_coarse, g_fine, at<float>(fwd_ws, f.oc), at<float>(fwd_ws, f.of),
                             at<__half>(ws, w.dof), at<float>(ws, w.delta), at<float>(ws, w.doc),
                             g_coarse ? dg_coarse : nullptr, g_fine ? dg_fine : nullptr, grad_dtype, BH, d, g.T, g.H,
-                            g.W, s)) != VSA_OK)
+                            g.W, g.cube_order, s)) != VSA_OK)
     return st;
   if ((st = launch_coarse_bwd(at<float>(fwd_ws, f.qc), at<float>(fwd_ws, f.kc), at<float>(fwd_ws, f.vc),
                               at<float>(ws, w.doc), at<float>(fwd_ws, f.lsec), BH, Nc, d, scale, at<float>(ws, w.P),
@@ -427,7 +438,8 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
                                  s)) != VSA_OK)
     return st;
   return launch_finalize(at<float>(ws, w.dqp), at<float>(ws, w.dkp), at<float>(ws, w.dvp), at<float>(ws, w.dqc),
-                         at<float>(ws, w.dkc), at<float>(ws, w.dvc), dq, dk, dv, grad_dtype, BH, d, g.T, g.H, g.W, s);
+                         at<float>(ws, w.dkc), at<float>(ws, w.dvc), dq, dk, dv, grad_dtype, BH, d, g.T, g.H, g.W,
+                         g.cube_order, s);
 }
 
 }  // extern "C"

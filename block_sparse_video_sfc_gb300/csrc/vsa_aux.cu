@@ -21,18 +21,20 @@ template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ oc, const float* __restrict__ of,
                                                       const __nv_bfloat16* __restrict__ gc,
                                                       const __nv_bfloat16* __restrict__ gf, void* __restrict__ out,
-                                                      int out_dtype, int Nc, int H, int W, int N) {
+                                                      int out_dtype, int Nc, int H, int W, int N,
+                                                      const int32_t* __restrict__ order) {
   constexpr int kChunks = D / 8, kTok = 256 / kChunks, kPasses = kCube / kTok;
   const int64_t cg = blockIdx.x;
   const int64_t bh = cg / Nc;
   const int cube = static_cast<int>(cg % Nc);
+  const int rcube = raster_cube(order, cube);
   const int j = threadIdx.x % kChunks, o0 = threadIdx.x / kChunks;
   float c[8];
   load8_f32(oc, cg * D + j * 8, c);
 #pragma unroll
   for (int p = 0; p < kPasses; ++p) {
     const int o = o0 + p * kTok;
-    const int64_t nat = bh * N + native_token(cube, o, H, W);
+    const int64_t nat = bh * N + native_token(rcube, o, H, W);
     const int64_t cub = bh * N + static_cast<int64_t>(cube) * kCube + o;
     float f[8], a[8], b[8], r[8];
     load8_f32(of, cub * D + j * 8, f);
@@ -53,19 +55,20 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        __half* __restrict__ dof, float* __restrict__ delta,
                                                        float* __restrict__ doc, void* __restrict__ dgc,
                                                        void* __restrict__ dgf, int grad_dtype, int Nc, int H, int W,
-                                                       int N, int* err) {
+                                                       int N, const int32_t* __restrict__ order, int* err) {
   constexpr int kChunks = D / 8, kTok = 256 / kChunks, kPasses = kCube / kTok;
   __shared__ float red[kTok][D];
   const int64_t cg = blockIdx.x;
   const int64_t bh = cg / Nc;
   const int cube = static_cast<int>(cg % Nc);
+  const int rcube = raster_cube(order, cube);
   const int j = threadIdx.x % kChunks, o0 = threadIdx.x / kChunks;
   float c[8], acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   load8_f32(oc, cg * D + j * 8, c);
 #pragma unroll
   for (int p = 0; p < kPasses; ++p) {
     const int o = o0 + p * kTok;
-    const int64_t nat = bh * N + native_token(cube, o, H, W);
+    const int64_t nat = bh * N + native_token(rcube, o, H, W);
     const int64_t cub = bh * N + static_cast<int64_t>(cube) * kCube + o;
     float g[8], a[8], b[8], f[8], t[8];
     load8_bf16(dout, nat * D + j * 8, g);
@@ -121,12 +124,14 @@ struct FinalizeArgs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256) finalize_kernel(FinalizeArgs a, int grad_dtype, int Nc, int H, int W, int N) {
+__global__ void __launch_bounds__(256) finalize_kernel(FinalizeArgs a, int grad_dtype, int Nc, int H, int W, int N,
+                                                       const int32_t* __restrict__ order) {
   constexpr int kChunks = D / 8, kTok = 256 / kChunks, kPasses = kCube / kTok;
   const int t = blockIdx.y;
   const int64_t cg = blockIdx.x;
   const int64_t bh = cg / Nc;
   const int cube = static_cast<int>(cg % Nc);
+  const int rcube = raster_cube(order, cube);
   const int j = threadIdx.x % kChunks, o0 = threadIdx.x / kChunks;
   float c[8];
   load8_f32(a.pooled[t], cg * D + j * 8, c);
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(FinalizeArgs a, int grad_
 #pragma unroll
   for (int p = 0; p < kPasses; ++p) {
     const int o = o0 + p * kTok;
-    const int64_t nat = bh * N + native_token(cube, o, H, W);
+    const int64_t nat = bh * N + native_token(rcube, o, H, W);
     const int64_t cub = bh * N + static_cast<int64_t>(cube) * kCube + o;
     float f[8];
     load8_f32(a.fine[t], cub * D + j * 8, f);
@@ -148,23 +153,23 @@ __global__ void __launch_bounds__(256) finalize_kernel(FinalizeArgs a, int grad_
 }  // namespace
 
 int launch_combine(const float* oc, const float* of, const void* gc, const void* gf, void* out, int out_dtype, int BH,
-                   int d, int T, int H, int W, cudaStream_t s) {
+                   int d, int T, int H, int W, const int32_t* order, cudaStream_t s) {
   const int N = T * H * W, Nc = N / kCube;
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(BH) * Nc);
   auto g = static_cast<const __nv_bfloat16*>(gc);
   auto f = static_cast<const __nv_bfloat16*>(gf);
   timing_mark(VSA_K_COMBINE, true, s);
   if (d == 128)
-    combine_kernel<128><<<grid, 256, 0, s>>>(oc, of, g, f, out, out_dtype, Nc, H, W, N);
+    combine_kernel<128><<<grid, 256, 0, s>>>(oc, of, g, f, out, out_dtype, Nc, H, W, N, order);
   else
-    combine_kernel<64><<<grid, 256, 0, s>>>(oc, of, g, f, out, out_dtype, Nc, H, W, N);
+    combine_kernel<64><<<grid, 256, 0, s>>>(oc, of, g, f, out, out_dtype, Nc, H, W, N, order);
   timing_mark(VSA_K_COMBINE, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
 int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const float* oc, const float* of,
                     __half* dof, float* delta, float* doc, void* dgc, void* dgf, int grad_dtype, int BH, int d,
-                    int T, int H, int W, cudaStream_t s) {
+                    int T, int H, int W, const int32_t* order, cudaStream_t s) {
   const int N = T * H * W, Nc = N / kCube;
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(BH) * Nc);
   auto dO = static_cast<const __nv_bfloat16*>(dout);
@@ -172,10 +177,10 @@ int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const floa
   auto f = static_cast<const __nv_bfloat16*>(gf);
   timing_mark(VSA_K_BWD_PREP, true, s);
   if (d == 128)
-    bwd_prep_kernel<128><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, H, W, N,
+    bwd_prep_kernel<128><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, H, W, N, order,
                                               device_error_word());
   else
-    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, H, W, N,
+    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, H, W, N, order,
                                              device_error_word());
   timing_mark(VSA_K_BWD_PREP, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
@@ -183,15 +188,15 @@ int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const floa
 
 int launch_finalize(const float* dqp, const float* dkp, const float* dvp, const float* dqc, const float* dkc,
                     const float* dvc, void* dq, void* dk, void* dv, int grad_dtype, int BH, int d, int T, int H,
-                    int W, cudaStream_t s) {
+                    int W, const int32_t* order, cudaStream_t s) {
   const int N = T * H * W, Nc = N / kCube;
   FinalizeArgs a{{dqp, dkp, dvp}, {dqc, dkc, dvc}, {dq, dk, dv}};
   dim3 grid(static_cast<unsigned>(static_cast<int64_t>(BH) * Nc), 3);
   timing_mark(VSA_K_FINALIZE, true, s);
   if (d == 128)
-    finalize_kernel<128><<<grid, 256, 0, s>>>(a, grad_dtype, Nc, H, W, N);
+    finalize_kernel<128><<<grid, 256, 0, s>>>(a, grad_dtype, Nc, H, W, N, order);
   else
-    finalize_kernel<64><<<grid, 256, 0, s>>>(a, grad_dtype, Nc, H, W, N);
+    finalize_kernel<64><<<grid, 256, 0, s>>>(a, grad_dtype, Nc, H, W, N, order);
   timing_mark(VSA_K_FINALIZE, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }

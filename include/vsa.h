@@ -68,11 +68,42 @@ typedef enum {
 
 typedef enum { VSA_DTYPE_BF16 = 0, VSA_DTYPE_F32 = 1 } vsa_dtype_t;
 
-/* Latent video grid and cube shape.  ct = ch = cw = 4 only. */
+/* Latent video grid and cube shape.  ct = ch = cw = 4 only.
+ * cube_order: NULL for cube-raster order, or a device table written by
+ * vsa_cube_order for this grid (it must stay valid while calls that take the
+ * grid run); it fixes which cube sits at which position of the sequence. */
 typedef struct {
     int T, H, W;
     int ct, ch, cw;
+    const int32_t* cube_order;
 } vsa_grid_t;
+
+/* Cube orders of vsa_cube_order. */
+enum { VSA_CURVE_RASTER = 0, VSA_CURVE_HILBERT = 1 };
+
+/*
+ * vsa_cube_order -- the order of the cubes along the 3D space-filling curve.
+ * [AMD] "Two-Stage Architecture", pre-stage: tokens are reordered along a 3D
+ * space-filling curve so that each block of the sequence is a compact
+ * spatio-temporal region; the page names the curve (Jenga's) but does not
+ * print it.
+ *   g       the grid (T, H, W multiples of 4; g.cube_order is ignored).
+ *   curve   VSA_CURVE_RASTER: cube (ct, ch, cw) at position
+ *           (ct * H/4 + ch) * W/4 + cw.
+ *           VSA_CURVE_HILBERT: cubes in the order in which the 3-D Hilbert
+ *           curve (J. Skilling, "Programming the Hilbert curve", 2004) of the
+ *           smallest enclosing 2^b x 2^b x 2^b cube grid visits them, cells
+ *           outside the grid skipped; the index bits interleave t, h, w with
+ *           t the most significant.  Each side of the cube grid <= 1024.
+ *   order   out int32 [2 * Nc], device: order[p] = raster id
+ *           (ct * H/4 + ch) * W/4 + cw of the cube at position p, and
+ *           order[Nc + r] = position of raster cube r.
+ * Tokens inside a cube keep (t%4, h%4, w%4) raster order.  Pass the table as
+ * g.cube_order to vsa_permute, vsa_forward, vsa_backward and
+ * vsa_lut_add_neighbors; cube ids in index lists are then positions along the
+ * curve (so Top-K ties go to the cube met first).  Asynchronous on stream.
+ */
+int vsa_cube_order(vsa_grid_t g, int curve, int32_t* order, void* stream);
 
 /*
  * vsa_permute -- 3D space-filling-curve token reordering, with the cube
@@ -283,9 +314,10 @@ int vsa_mask_to_lut(const uint8_t* mask, int BH, int Nc, int max_kv_blocks, int3
  * vsa_lut_add_neighbors -- unites every row's list with its cube's spatial
  * neighbourhood.  [AMD] "Comparison with Jenga", "Algorithmic Design":
  * Jenga's block selection is the union of three masks, one of them spatial
- * adjacency; this adds that adjacency to a Top-K list.  Cube ids follow the
- * cube-raster order of vsa_permute: c = (t * Hc + h) * Wc + w on the cube grid
- * (Tc, Hc, Wc) = (T / 4, H / 4, W / 4).
+ * adjacency; this adds that adjacency to a Top-K list.  Cube ids are
+ * positions in the cube sequence of g (g.cube_order; with NULL the raster id
+ * c = (t * Hc + h) * Wc + w on the cube grid (Tc, Hc, Wc) = (T/4, H/4, W/4));
+ * neighbourhoods are taken on the grid coordinates.
  *   kv_block_idx_in, valid_block_num_in (may be NULL = max_kv_blocks_in),
  *   max_kv_blocks_in   the input lists [BH, Nc, max_kv_blocks_in].
  *   g                  the video grid (as in vsa_forward; 4 x 4 x 4 cubes).

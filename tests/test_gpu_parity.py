@@ -149,7 +149,7 @@ def test_lut_errors_are_reported(vsa, oracle_mod):
 
 
 # ---------------------------------------------------------------- whole forward / backward
-def _e2e(vsa, oracle_mod, wl, gates, out_dtype, grad_dtype, heads=None):
+def _e2e(vsa, oracle_mod, wl, gates, out_dtype, grad_dtype, heads=None, cube_order=None):
     q, k, v = synth.make_qkv(wl, heads_subset=heads)
     gc = gf = None
     if gates:
@@ -157,7 +157,7 @@ def _e2e(vsa, oracle_mod, wl, gates, out_dtype, grad_dtype, heads=None):
     dout = synth.make_dout(wl, heads_subset=heads)
     D = lambda a: None if a is None else dev(a)
     out, st = vsa.forward(D(q), D(k), D(v), wl.T, wl.H, wl.W, wl.topk, g_coarse=D(gc), g_fine=D(gf),
-                          out_dtype=out_dtype)
+                          out_dtype=out_dtype, cube_order=cube_order)
     g = vsa.backward(st, D(dout), g_coarse=D(gc), g_fine=D(gf), grad_dtype=grad_dtype)
     status_ok(vsa)
     saved = st.saved()
@@ -397,3 +397,65 @@ def test_lut_add_neighbors_and_fine_fwd(vsa, oracle_mod, name, radius):
         rof, rlse = oracle_mod.fine_fwd(qp, kp, vp, ri, rc, wl.d ** -0.5)
         assert_close(host(of), rof, what="O_f on widened lists")
         assert_close(host(lse), rlse, what="lse on widened lists")
+
+
+# ---------------------------------------------------------------- Hilbert cube order
+@pytest.mark.parametrize("grid", [(4, 8, 8), (8, 16, 32), (16, 32, 64), (32, 48, 80), (12, 20, 28)])
+def test_cube_order_table(vsa, oracle_mod, grid):
+    """vsa_cube_order (point -> curve index on the GPU) against the oracle's
+    ranks (curve index -> point), both curves, bit for bit."""
+    T, H, W = grid
+    Tc, Hc, Wc = T // 4, H // 4, W // 4
+    Nc = Tc * Hc * Wc
+    for curve in ("raster", "hilbert"):
+        tab = vsa.cube_order(T, H, W, curve).cpu().numpy()
+        rank = oracle_mod.cube_rank(Tc, Hc, Wc, curve)
+        np.testing.assert_array_equal(tab[Nc:], rank)
+        np.testing.assert_array_equal(tab[:Nc], np.argsort(rank))
+    status_ok(vsa)
+
+
+@pytest.mark.parametrize("grid,d", [((8, 12, 20), 128), ((12, 20, 28), 64), ((16, 32, 64), 128)])
+def test_permute_hilbert(vsa, oracle_mod, grid, d):
+    T, H, W = grid
+    order = vsa.cube_order(T, H, W, "hilbert")
+    x = synth.make_random((2, T * H * W, d), seed=7 + d)
+    y, pooled = vsa.permute(dev(x), T, H, W, pool=True, cube_order=order)
+    ref = oracle_mod.permute(x, T, H, W, curve="hilbert")
+    assert np.array_equal(host(y), ref)
+    back = vsa.permute(y, T, H, W, inverse=True, cube_order=order)
+    assert np.array_equal(host(back), x.astype(np.float64))
+    np.testing.assert_allclose(host(pooled), oracle_mod.pool(ref), rtol=1e-5, atol=1e-6)
+    status_ok(vsa)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_forward_backward_hilbert(vsa, oracle_mod, name):
+    wl = synth.WORKLOADS[name]
+    order = vsa.cube_order(wl.T, wl.H, wl.W, "hilbert")
+    q, k, v, gc, gf, dout, out, g, saved = _e2e(vsa, oracle_mod, wl, True, torch.float32, torch.float32,
+                                                cube_order=order)
+    gidx = saved["idx"].cpu().numpy().reshape(wl.B, wl.heads, wl.Nc, wl.topk)
+    ref0 = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=gc, gf=gf, curve="hilbert")
+    check_topk_validity(gidx, ref0["scores"], wl.topk)
+    ref = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=gc, gf=gf, lut=gidx, curve="hilbert")
+    assert_close(host(out), ref["out"], what="out")
+    rg = oracle_mod.backward(q, k, v, dout, gidx, wl.T, wl.H, wl.W, gc=gc, gf=gf, curve="hilbert")
+    for n in ("dq", "dk", "dv", "dgc", "dgf"):
+        assert_close(host(g[n]), rg[n], what=n)
+
+
+def test_lut_add_neighbors_hilbert(vsa, oracle_mod):
+    T, H, W = 16, 32, 64
+    Nc = (T // 4) * (H // 4) * (W // 4)
+    order = vsa.cube_order(T, H, W, "hilbert")
+    rng = np.random.default_rng(11)
+    idx = np.stack([np.stack([rng.permutation(Nc)[:40] for _ in range(Nc)]) for _ in range(2)]).astype(np.int32)
+    cnt = np.full(idx.shape[:-1], 40, np.int32)
+    got, gcnt = vsa.lut_add_neighbors(dev(idx, torch.int32), dev(cnt, torch.int32), T, H, W, 2, 200,
+                                      cube_order=order)
+    status_ok(vsa)
+    ref, rcnt, ovf = oracle_mod.lut_add_neighbors(idx, cnt, T, H, W, 2, 200, curve="hilbert")
+    assert not ovf
+    np.testing.assert_array_equal(gcnt.cpu().numpy(), rcnt)
+    np.testing.assert_array_equal(got.cpu().numpy(), ref)
