@@ -54,18 +54,20 @@ def _load():
                 "orc_sfc_position": ([I, I, I, I, I, I, P], I64),
                 "orc_sfc_table": ([I, I, I, P, P], None),
                 "orc_permute": ([P, P, I64, I, I, I, I, P, I], None),
-                "orc_pool": ([P, P, I64, I64, I], None),
+                "orc_num_cubes": ([I, I, I], I64),
+                "orc_cube_slots": ([I, I, I, P, P, P], None),
+                "orc_pool": ([P, P, I64, I64, I, P], None),
                 "orc_coarse": ([P, P, P, I64, I, I, D, P, P, P], None),
                 "orc_topk": ([P, I64, I, I, P], None),
-                "orc_fine_fwd": ([P, P, P, P, P, I, I64, I64, I, D, P, P], None),
-                "orc_fine_fwd_rows": ([P, P, P, P, P, I, I64, I64, I, D, P, I64, P, P], None),
+                "orc_fine_fwd": ([P, P, P, P, P, I, I64, I64, I, D, P, P, P], None),
+                "orc_fine_fwd_rows": ([P, P, P, P, P, I, I64, I64, I, D, P, P, I64, P, P], None),
                 "orc_combine": ([P, P, P, P, I64, I64, I, P], None),
                 "orc_forward": ([P, P, P, P, P, I64, I, I, I, I, P, I, D, P, P, P, P, P, P, P], None),
-                "orc_fine_bwd": ([P, P, P, P, P, P, I, I64, I64, I, D, P, P, P], None),
+                "orc_fine_bwd": ([P, P, P, P, P, P, I, I64, I64, I, D, P, P, P, P], None),
                 "orc_coarse_bwd": ([P, P, P, P, I64, I, I, D, P, P, P], None),
                 "orc_backward": ([P, P, P, P, P, I64, I, I, I, I, P, I, D, P, P, P, P, P, P, P], None),
-                "orc_fine_bwd_query_rows": ([P, P, P, P, P, P, I, I64, I, D, P, I64, P], None),
-                "orc_fine_bwd_key_cube": ([P, P, P, P, P, P, I, I64, I, D, I64, I, P, P], None),
+                "orc_fine_bwd_query_rows": ([P, P, P, P, P, P, I, I64, I, D, P, P, I64, P], None),
+                "orc_fine_bwd_key_cube": ([P, P, P, P, P, P, I, I64, I, D, P, I64, I, P, P], None),
                 "orc_combine_bwd": ([P, P, P, P, P, I64, I64, I, P, P, P, P], None),
                 "orc_mask_to_lut": ([P, I64, I, I, P, P, P], None),
                 "orc_lut_add_neighbors": ([P, P, I, I64, I, I, I, P, I, I, P, P, P], None),
@@ -118,8 +120,26 @@ def cube_rank(Tc: int, Hc: int, Wc: int, curve: str = "raster") -> np.ndarray:
     return rank
 
 
+def cube_grid(T: int, H: int, W: int):
+    """Cubes along t, h, w: a side that is not a multiple of 4 ends in partial cubes."""
+    return (T + 3) // 4, (H + 3) // 4, (W + 3) // 4
+
+
+def num_cubes(T: int, H: int, W: int) -> int:
+    return int(_load().orc_num_cubes(T, H, W))
+
+
 def _rank_of(T: int, H: int, W: int, curve: str):
-    return None if curve == "raster" else cube_rank(T // 4, H // 4, W // 4, curve)
+    return None if curve == "raster" else cube_rank(*cube_grid(T, H, W), curve)
+
+
+def cube_slots(T: int, H: int, W: int, curve: str = "raster"):
+    """(slot_ok [Np] uint8: reordered slot holds a token, ntok [Nc] int32: tokens per cube)."""
+    Nc = num_cubes(T, H, W)
+    slot_ok = np.empty(64 * Nc, dtype=np.uint8)
+    ntok = np.empty(Nc, dtype=np.int32)
+    _load().orc_cube_slots(T, H, W, _p(_rank_of(T, H, W, curve)), _p(slot_ok), _p(ntok))
+    return slot_ok, ntok
 
 
 def sfc_table(T: int, H: int, W: int, curve: str = "raster") -> np.ndarray:
@@ -130,19 +150,22 @@ def sfc_table(T: int, H: int, W: int, curve: str = "raster") -> np.ndarray:
 
 
 def permute(x, T: int, H: int, W: int, inverse: bool = False, curve: str = "raster") -> np.ndarray:
+    """Native [.., N, d] -> reordered [.., Np, d] (padding slots zero), or back."""
     x = _f64(x)
     BH, N, d = _bh(x)
-    y = np.empty_like(x)
+    n_out = T * H * W if inverse else 64 * num_cubes(T, H, W)
+    y = np.empty(x.shape[:-2] + (n_out, d), dtype=np.float64)
     rank = _rank_of(T, H, W, curve)
     _load().orc_permute(_p(x), _p(y), BH, d, T, H, W, _p(rank), int(bool(inverse)))
     return y
 
 
-def pool(xp) -> np.ndarray:
+def pool(xp, ntok=None) -> np.ndarray:
+    """Cube means; ntok (tokens per cube, default 64) divides each sum."""
     xp = _f64(xp)
     BH, N, d = _bh(xp)
     out = np.empty(xp.shape[:-2] + (N // CUBE, d), dtype=np.float64)
-    _load().orc_pool(_p(xp), _p(out), BH, N, d)
+    _load().orc_pool(_p(xp), _p(out), BH, N, d, _p(_i32(ntok)))
     return out
 
 
@@ -170,7 +193,11 @@ def topk(scores, K: int) -> np.ndarray:
     return idx
 
 
-def fine_fwd(qp, kp, vp, idx, cnt, scale: float):
+def _u8(x):
+    return None if x is None else np.ascontiguousarray(x, dtype=np.uint8)
+
+
+def fine_fwd(qp, kp, vp, idx, cnt, scale: float, slot_ok=None):
     """-> (O_f [.., N, d], lse [.., N]) over the listed cubes only."""
     qp, kp, vp = _f64(qp), _f64(kp), _f64(vp)
     idx, cnt = _i32(idx), _i32(cnt)
@@ -178,11 +205,11 @@ def fine_fwd(qp, kp, vp, idx, cnt, scale: float):
     of = np.empty_like(qp)
     lse = np.empty(qp.shape[:-1], dtype=np.float64)
     _load().orc_fine_fwd(_p(qp), _p(kp), _p(vp), _p(idx), _p(cnt), idx.shape[-1], BH, N, d,
-                         float(scale), _p(of), _p(lse))
+                         float(scale), _p(_u8(slot_ok)), _p(of), _p(lse))
     return of, lse
 
 
-def fine_fwd_rows(qp, kp, vp, idx, cnt, scale: float, rows):
+def fine_fwd_rows(qp, kp, vp, idx, cnt, scale: float, rows, slot_ok=None):
     """Fine output for the listed flat rows r = bh*N + i only."""
     qp, kp, vp = _f64(qp), _f64(kp), _f64(vp)
     idx, cnt = _i32(idx), _i32(cnt)
@@ -191,7 +218,7 @@ def fine_fwd_rows(qp, kp, vp, idx, cnt, scale: float, rows):
     of = np.empty((rows.size, d), dtype=np.float64)
     lse = np.empty(rows.size, dtype=np.float64)
     _load().orc_fine_fwd_rows(_p(qp), _p(kp), _p(vp), _p(idx), _p(cnt), idx.shape[-1],
-                              BH, N, d, float(scale), _p(rows), rows.size, _p(of), _p(lse))
+                              BH, N, d, float(scale), _p(_u8(slot_ok)), _p(rows), rows.size, _p(of), _p(lse))
     return of, lse
 
 
@@ -215,14 +242,14 @@ def forward(q, k, v, T: int, H: int, W: int, K: int, scale=None,
     gc, gf = _f64(gc), _f64(gf)
     BH, N, d = _bh(q)
     assert N == T * H * W
-    Nc = N // CUBE
+    Nc = num_cubes(T, H, W)
     if scale is None:
         scale = default_scale(d)
     lead = q.shape[:-2]
     out = np.empty_like(q)
     idx = np.empty(lead + (Nc, K), dtype=np.int32)
-    of = np.empty_like(q)
-    lse = np.empty(lead + (N,), dtype=np.float64)
+    of = np.empty(lead + (64 * Nc, d), dtype=np.float64)
+    lse = np.empty(lead + (64 * Nc,), dtype=np.float64)
     oc = np.empty(lead + (Nc, d), dtype=np.float64)
     scores = np.empty(lead + (Nc, Nc), dtype=np.float64) if want_scores else None
     lut = _i32(lut)
@@ -233,17 +260,17 @@ def forward(q, k, v, T: int, H: int, W: int, K: int, scale=None,
     return dict(out=out, idx=idx, of=of, lse=lse, oc=oc, scores=scores)
 
 
-def fine_bwd(qp, kp, vp, dof, idx, cnt, scale: float):
+def fine_bwd(qp, kp, vp, dof, idx, cnt, scale: float, slot_ok=None):
     qp, kp, vp, dof = _f64(qp), _f64(kp), _f64(vp), _f64(dof)
     idx, cnt = _i32(idx), _i32(cnt)
     BH, N, d = _bh(qp)
     dq, dk, dv = np.empty_like(qp), np.empty_like(qp), np.empty_like(qp)
     _load().orc_fine_bwd(_p(qp), _p(kp), _p(vp), _p(dof), _p(idx), _p(cnt), idx.shape[-1],
-                         BH, N, d, float(scale), _p(dq), _p(dk), _p(dv))
+                         BH, N, d, float(scale), _p(_u8(slot_ok)), _p(dq), _p(dk), _p(dv))
     return dq, dk, dv
 
 
-def fine_bwd_query_rows(qp, kp, vp, dof, idx, cnt, scale: float, rows):
+def fine_bwd_query_rows(qp, kp, vp, dof, idx, cnt, scale: float, rows, slot_ok=None):
     """dQ of the fine stage for the listed flat rows r = bh*N + i."""
     qp, kp, vp, dof = _f64(qp), _f64(kp), _f64(vp), _f64(dof)
     idx, cnt = _i32(idx), _i32(cnt)
@@ -251,11 +278,11 @@ def fine_bwd_query_rows(qp, kp, vp, dof, idx, cnt, scale: float, rows):
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     out = np.empty((rows.size, d), dtype=np.float64)
     _load().orc_fine_bwd_query_rows(_p(qp), _p(kp), _p(vp), _p(dof), _p(idx), _p(cnt), idx.shape[-1],
-                                    N, d, float(scale), _p(rows), rows.size, _p(out))
+                                    N, d, float(scale), _p(_u8(slot_ok)), _p(rows), rows.size, _p(out))
     return out
 
 
-def fine_bwd_key_cube(qp, kp, vp, dof, idx, cnt, scale: float, bh: int, kcube: int):
+def fine_bwd_key_cube(qp, kp, vp, dof, idx, cnt, scale: float, bh: int, kcube: int, slot_ok=None):
     """(dK, dV) of the 64 tokens of key cube `kcube` in head `bh`, fine stage."""
     qp, kp, vp, dof = _f64(qp), _f64(kp), _f64(vp), _f64(dof)
     idx, cnt = _i32(idx), _i32(cnt)
@@ -263,7 +290,7 @@ def fine_bwd_key_cube(qp, kp, vp, dof, idx, cnt, scale: float, bh: int, kcube: i
     dk = np.empty((64, d), dtype=np.float64)
     dv = np.empty((64, d), dtype=np.float64)
     _load().orc_fine_bwd_key_cube(_p(qp), _p(kp), _p(vp), _p(dof), _p(idx), _p(cnt), idx.shape[-1],
-                                  N, d, float(scale), bh, kcube, _p(dk), _p(dv))
+                                  N, d, float(scale), _p(_u8(slot_ok)), bh, kcube, _p(dk), _p(dv))
     return dk, dv
 
 
@@ -326,7 +353,7 @@ def lut_add_neighbors(idx, cnt, T: int, H: int, W: int, radius: int, max_kv_bloc
     """Lists united with the radius-r cube neighbourhood -> (idx, cnt, overflow)."""
     idx = _i32(idx)
     cnt = None if cnt is None else _i32(cnt)
-    Tc, Hc, Wc = T // 4, H // 4, W // 4
+    Tc, Hc, Wc = cube_grid(T, H, W)
     Nc, kin = idx.shape[-2], idx.shape[-1]
     BH = idx.size // (Nc * kin)
     out = np.empty(idx.shape[:-1] + (max_kv_blocks,), dtype=np.int32)

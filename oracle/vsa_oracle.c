@@ -38,6 +38,12 @@
  *  - Top-K ties go to the lower cube id; the index list is stored in
  *    selection order (descending score), as torch.topk returns it.
  *  - A query cube with zero valid blocks has O_f = 0 and LSE = -inf.
+ *  - A grid side that is not a multiple of 4 is covered by ceil(side / 4)
+ *    cubes; a boundary cube keeps its 64 slots, and the slots whose token
+ *    would lie outside the grid are padding: zero in the reordered tensors,
+ *    left out of the cube's mean (which divides by the number of real
+ *    tokens), never attended to as keys, and never written back.  The
+ *    reordered length is Np = 64 * Nc >= N = T * H * W.
  *  - The Top-K set is a constant in the backward pass.
  */
 #include <math.h>
@@ -119,7 +125,7 @@ int64_t orc_sfc_position(int t, int h, int w, int T, int H, int W, const int32_t
 {
     (void)T;
     int64_t cube_t = t / 4, cube_h = h / 4, cube_w = w / 4;
-    int64_t cubes_h = H / 4, cubes_w = W / 4;
+    int64_t cubes_h = (H + 3) / 4, cubes_w = (W + 3) / 4;
     int64_t cube = (cube_t * cubes_h + cube_h) * cubes_w + cube_w;
     if (rank)
         cube = rank[cube];
@@ -138,19 +144,28 @@ void orc_sfc_table(int T, int H, int W, const int32_t *rank, int64_t *pos)
             }
 }
 
-/* inverse == 0: y[pos[n]] = x[n] (native -> cube order);
- * inverse != 0: y[n] = x[pos[n]] (cube order -> native). */
+/* Number of cubes covering the grid, and the reordered length 64 * Nc. */
+int64_t orc_num_cubes(int T, int H, int W)
+{
+    return (int64_t)((T + 3) / 4) * ((H + 3) / 4) * ((W + 3) / 4);
+}
+
+/* inverse == 0: y[pos[n]] = x[n] (native [BH, N, d] -> cube order
+ * [BH, Np, d], padding slots zero); inverse != 0: y[n] = x[pos[n]] (cube
+ * order -> native; padding slots are dropped). */
 void orc_permute(const double *x, double *y, int64_t BH, int d,
                  int T, int H, int W, const int32_t *rank, int inverse)
 {
-    int64_t N = (int64_t)T * H * W;
+    int64_t N = (int64_t)T * H * W, Np = CUBE * orc_num_cubes(T, H, W);
     int64_t *pos = (int64_t *)malloc(sizeof(int64_t) * N);
     orc_sfc_table(T, H, W, rank, pos);
+    if (!inverse)
+        memset(y, 0, sizeof(double) * BH * Np * d);
 #pragma omp parallel for
     for (int64_t bh = 0; bh < BH; bh++)
         for (int64_t n = 0; n < N; n++) {
-            const double *src = x + (bh * N + (inverse ? pos[n] : n)) * d;
-            double *dst = y + (bh * N + (inverse ? n : pos[n])) * d;
+            const double *src = inverse ? x + (bh * Np + pos[n]) * d : x + (bh * N + n) * d;
+            double *dst = inverse ? y + (bh * N + n) * d : y + (bh * Np + pos[n]) * d;
             for (int c = 0; c < d; c++)
                 dst[c] = src[c];
         }
@@ -161,7 +176,9 @@ void orc_permute(const double *x, double *y, int64_t BH, int d,
 /* Stage 1: cube mean-pool.  [AMD] "Stage 1: Coarse Selection": each cube of
  * 64 tokens is mean-pooled into one cube-level vector (Qc, Kc, Vc).
  * Input is in reordered (cube-contiguous) order. */
-void orc_pool(const double *xp, double *xc, int64_t BH, int64_t N, int d)
+/* ntok[c]: real tokens of cube c (NULL: 64 each); padding slots are zero,
+ * so the sum over the 64 slots is the sum over the real tokens. */
+void orc_pool(const double *xp, double *xc, int64_t BH, int64_t N, int d, const int32_t *ntok)
 {
     int64_t Nc = N / CUBE;
 #pragma omp parallel for
@@ -171,8 +188,25 @@ void orc_pool(const double *xp, double *xc, int64_t BH, int64_t N, int d)
                 double s = 0.0;
                 for (int o = 0; o < CUBE; o++)
                     s += xp[(bh * N + c * CUBE + o) * d + k];
-                xc[(bh * Nc + c) * d + k] = s / CUBE;
+                xc[(bh * Nc + c) * d + k] = s / (ntok ? ntok[c] : CUBE);
             }
+}
+
+/* slot_ok[p] = 1 when reordered position p holds a token of the grid (0 for
+ * padding), p in [0, Np); ntok[c] = number of tokens in cube position c. */
+void orc_cube_slots(int T, int H, int W, const int32_t *rank, unsigned char *slot_ok, int32_t *ntok)
+{
+    int64_t N = (int64_t)T * H * W, Nc = orc_num_cubes(T, H, W);
+    int64_t *pos = (int64_t *)malloc(sizeof(int64_t) * N);
+    orc_sfc_table(T, H, W, rank, pos);
+    memset(slot_ok, 0, (size_t)(Nc * CUBE));
+    for (int64_t c = 0; c < Nc; c++)
+        ntok[c] = 0;
+    for (int64_t n = 0; n < N; n++) {
+        slot_ok[pos[n]] = 1;
+        ntok[pos[n] / CUBE]++;
+    }
+    free(pos);
 }
 
 /* Stage 1: coarse cube-to-cube attention.
@@ -262,8 +296,8 @@ void orc_topk(const double *scores, int64_t rows, int Nc, int K, int32_t *idx)
  * tokens.  One row: query token i (reordered order) of head bh. */
 static void orc_fine_row(const double *qp, const double *kp, const double *vp,
                          const int32_t *idx, const int32_t *cnt, int Kmax,
-                         int64_t N, int d, double scale, int64_t bh, int64_t i,
-                         double *of_row, double *lse_row)
+                         int64_t N, int d, double scale, const unsigned char *slot_ok,
+                         int64_t bh, int64_t i, double *of_row, double *lse_row)
 {
     int64_t Nc = N / CUBE;
     int64_t qcube = i / CUBE;
@@ -285,7 +319,7 @@ static void orc_fine_row(const double *qp, const double *kp, const double *vp,
             double dot = 0.0;
             for (int c = 0; c < d; c++)
                 dot += q[c] * k[c];
-            s[e * CUBE + o] = scale * dot;
+            s[e * CUBE + o] = (slot_ok && !slot_ok[j]) ? -INFINITY : scale * dot;  /* padding: no key */
         }
     double m = -INFINITY;
     for (int64_t a = 0; a < nk; a++)
@@ -307,14 +341,15 @@ static void orc_fine_row(const double *qp, const double *kp, const double *vp,
     free(s);
 }
 
+/* slot_ok (NULL: every slot holds a token) masks padding keys out. */
 void orc_fine_fwd(const double *qp, const double *kp, const double *vp,
                   const int32_t *idx, const int32_t *cnt, int Kmax,
                   int64_t BH, int64_t N, int d, double scale,
-                  double *of, double *lse)
+                  const unsigned char *slot_ok, double *of, double *lse)
 {
 #pragma omp parallel for schedule(dynamic, 64)
     for (int64_t r = 0; r < BH * N; r++)
-        orc_fine_row(qp, kp, vp, idx, cnt, Kmax, N, d, scale, r / N, r % N,
+        orc_fine_row(qp, kp, vp, idx, cnt, Kmax, N, d, scale, slot_ok, r / N, r % N,
                      of + r * d, lse + r);
 }
 
@@ -323,13 +358,13 @@ void orc_fine_fwd(const double *qp, const double *kp, const double *vp,
 void orc_fine_fwd_rows(const double *qp, const double *kp, const double *vp,
                        const int32_t *idx, const int32_t *cnt, int Kmax,
                        int64_t BH, int64_t N, int d, double scale,
-                       const int64_t *rows, int64_t nrows,
+                       const unsigned char *slot_ok, const int64_t *rows, int64_t nrows,
                        double *of_rows, double *lse_rows)
 {
     (void)BH;
 #pragma omp parallel for schedule(dynamic, 4)
     for (int64_t a = 0; a < nrows; a++)
-        orc_fine_row(qp, kp, vp, idx, cnt, Kmax, N, d, scale, rows[a] / N,
+        orc_fine_row(qp, kp, vp, idx, cnt, Kmax, N, d, scale, slot_ok, rows[a] / N,
                      rows[a] % N, of_rows + a * d, lse_rows + a);
 }
 
@@ -356,16 +391,20 @@ void orc_combine(const double *gc, const double *gf, const double *oc,
  * lut_in: if not NULL, [BH, Nc, K] index list used instead of the Top-K
  * (the valid count is then K for every query cube).
  * Outputs (all caller-allocated):
- *   out [BH, N, d] native; idx [BH, Nc, K]; of [BH, N, d] and lse [BH, N]
- *   (reordered order); oc [BH, Nc, d]; scores [BH, Nc, Nc] (may be NULL). */
+ *   out [BH, N, d] native; idx [BH, Nc, K]; of [BH, Np, d] and lse [BH, Np]
+ *   (reordered order, Np = 64 Nc); oc [BH, Nc, d]; scores [BH, Nc, Nc] (may
+ *   be NULL). */
 void orc_forward(const double *q, const double *k, const double *v,
                  const double *gc, const double *gf, int64_t BH, int d,
                  int T, int H, int W, const int32_t *rank, int K, double scale,
                  const int32_t *lut_in, double *out, int32_t *idx,
                  double *of, double *lse, double *oc, double *scores)
 {
-    int64_t N = (int64_t)T * H * W, Nc = N / CUBE;
+    int64_t Nc = orc_num_cubes(T, H, W), N = Nc * CUBE;  /* N: reordered length */
     size_t big = sizeof(double) * BH * N * d, small = sizeof(double) * BH * Nc * d;
+    unsigned char *slot_ok = (unsigned char *)malloc((size_t)N);
+    int32_t *ntok = (int32_t *)malloc(sizeof(int32_t) * Nc);
+    orc_cube_slots(T, H, W, rank, slot_ok, ntok);
     double *qp = (double *)malloc(big), *kp = (double *)malloc(big), *vp = (double *)malloc(big);
     double *qc = (double *)malloc(small), *kc = (double *)malloc(small), *vc = (double *)malloc(small);
     double *sc = scores ? scores : (double *)malloc(sizeof(double) * BH * Nc * Nc);
@@ -373,9 +412,9 @@ void orc_forward(const double *q, const double *k, const double *v,
     orc_permute(q, qp, BH, d, T, H, W, rank, 0);
     orc_permute(k, kp, BH, d, T, H, W, rank, 0);
     orc_permute(v, vp, BH, d, T, H, W, rank, 0);
-    orc_pool(qp, qc, BH, N, d);
-    orc_pool(kp, kc, BH, N, d);
-    orc_pool(vp, vc, BH, N, d);
+    orc_pool(qp, qc, BH, N, d, ntok);
+    orc_pool(kp, kc, BH, N, d, ntok);
+    orc_pool(vp, vc, BH, N, d, ntok);
     orc_coarse(qc, kc, vc, BH, (int)Nc, d, scale, sc, oc, NULL);
     if (lut_in)
         memcpy(idx, lut_in, sizeof(int32_t) * BH * Nc * K);
@@ -383,7 +422,7 @@ void orc_forward(const double *q, const double *k, const double *v,
         orc_topk(sc, BH * Nc, (int)Nc, K, idx);
     for (int64_t r = 0; r < BH * Nc; r++)
         cnt[r] = K;
-    orc_fine_fwd(qp, kp, vp, idx, cnt, K, BH, N, d, scale, of, lse);
+    orc_fine_fwd(qp, kp, vp, idx, cnt, K, BH, N, d, scale, slot_ok, of, lse);
     double *gcp = NULL, *gfp = NULL, *outp = (double *)malloc(big);
     if (gc) {
         gcp = (double *)malloc(big);
@@ -397,7 +436,7 @@ void orc_forward(const double *q, const double *k, const double *v,
     orc_permute(outp, out, BH, d, T, H, W, rank, 1);
     free(qp); free(kp); free(vp); free(qc); free(kc); free(vc);
     if (!scores) free(sc);
-    free(cnt); free(gcp); free(gfp); free(outp);
+    free(cnt); free(gcp); free(gfp); free(outp); free(slot_ok); free(ntok);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -410,7 +449,7 @@ void orc_forward(const double *q, const double *k, const double *v,
 void orc_fine_bwd(const double *qp, const double *kp, const double *vp,
                   const double *dof, const int32_t *idx, const int32_t *cnt,
                   int Kmax, int64_t BH, int64_t N, int d, double scale,
-                  double *dq, double *dk, double *dv)
+                  const unsigned char *slot_ok, double *dq, double *dk, double *dv)
 {
     int64_t Nc = N / CUBE;
     memset(dq, 0, sizeof(double) * BH * N * d);
@@ -442,7 +481,7 @@ void orc_fine_bwd(const double *qp, const double *kp, const double *vp,
                 double dot = 0.0;
                 for (int c = 0; c < d; c++)
                     dot += q[c] * kk[c];
-                s[a] = scale * dot;
+                s[a] = (slot_ok && !slot_ok[key[a]]) ? -INFINITY : scale * dot;
                 if (s[a] > m)
                     m = s[a];
             }
@@ -483,7 +522,7 @@ void orc_fine_bwd(const double *qp, const double *kp, const double *vp,
  * softmax, dP and D are recomputed from scratch exactly as orc_fine_bwd does. */
 void orc_fine_bwd_query_rows(const double *qp, const double *kp, const double *vp,
                              const double *dof, const int32_t *idx, const int32_t *cnt,
-                             int Kmax, int64_t N, int d, double scale,
+                             int Kmax, int64_t N, int d, double scale, const unsigned char *slot_ok,
                              const int64_t *rows, int64_t nrows, double *dq_rows)
 {
     int64_t Nc = N / CUBE;
@@ -513,7 +552,7 @@ void orc_fine_bwd_query_rows(const double *qp, const double *kp, const double *v
                 dot += q[c] * kk[c];
                 dot2 += g[c] * vv[c];
             }
-            s[e] = scale * dot;
+            s[e] = (slot_ok && !slot_ok[j]) ? -INFINITY : scale * dot;
             dp[e] = dot2;
             if (s[e] > m)
                 m = s[e];
@@ -540,8 +579,8 @@ void orc_fine_bwd_query_rows(const double *qp, const double *kp, const double *v
  * every query row whose cube lists kcube.  dk_rows, dv_rows [64, d]. */
 void orc_fine_bwd_key_cube(const double *qp, const double *kp, const double *vp,
                            const double *dof, const int32_t *idx, const int32_t *cnt,
-                           int Kmax, int64_t N, int d, double scale, int64_t bh,
-                           int kcube, double *dk_rows, double *dv_rows)
+                           int Kmax, int64_t N, int d, double scale, const unsigned char *slot_ok,
+                           int64_t bh, int kcube, double *dk_rows, double *dv_rows)
 {
     int64_t Nc = N / CUBE;
     for (int64_t e = 0; e < (int64_t)CUBE * d; e++) {
@@ -582,7 +621,7 @@ void orc_fine_bwd_key_cube(const double *qp, const double *kp, const double *vp,
                     dot += q[c] * kk[c];
                     dot2 += g[c] * vv[c];
                 }
-                s[e] = scale * dot;
+                s[e] = (slot_ok && !slot_ok[j]) ? -INFINITY : scale * dot;
                 dp[e] = dot2;
                 if (s[e] > m)
                     m = s[e];
@@ -700,8 +739,11 @@ void orc_backward(const double *q, const double *k, const double *v,
                   const double *dout, double *dq, double *dk, double *dv,
                   double *dgc, double *dgf)
 {
-    int64_t N = (int64_t)T * H * W, Nc = N / CUBE;
+    int64_t Nc = orc_num_cubes(T, H, W), N = Nc * CUBE;  /* N: reordered length */
     size_t big = sizeof(double) * BH * N * d, small = sizeof(double) * BH * Nc * d;
+    unsigned char *slot_ok = (unsigned char *)malloc((size_t)N);
+    int32_t *ntok = (int32_t *)malloc(sizeof(int32_t) * Nc);
+    orc_cube_slots(T, H, W, rank, slot_ok, ntok);
     double *qp = (double *)malloc(big), *kp = (double *)malloc(big), *vp = (double *)malloc(big);
     double *qc = (double *)malloc(small), *kc = (double *)malloc(small), *vc = (double *)malloc(small);
     double *oc = (double *)malloc(small), *of = (double *)malloc(big);
@@ -719,11 +761,11 @@ void orc_backward(const double *q, const double *k, const double *v,
     orc_permute(q, qp, BH, d, T, H, W, rank, 0);
     orc_permute(k, kp, BH, d, T, H, W, rank, 0);
     orc_permute(v, vp, BH, d, T, H, W, rank, 0);
-    orc_pool(qp, qc, BH, N, d);
-    orc_pool(kp, kc, BH, N, d);
-    orc_pool(vp, vc, BH, N, d);
+    orc_pool(qp, qc, BH, N, d, ntok);
+    orc_pool(kp, kc, BH, N, d, ntok);
+    orc_pool(vp, vc, BH, N, d, ntok);
     orc_coarse(qc, kc, vc, BH, (int)Nc, d, scale, NULL, oc, NULL);
-    orc_fine_fwd(qp, kp, vp, idx, cnt, K, BH, N, d, scale, of, lse);
+    orc_fine_fwd(qp, kp, vp, idx, cnt, K, BH, N, d, scale, slot_ok, of, lse);
 
     /* Gated combination out_p = gc*Oc[cube] + gf*Of, differentiated. */
     orc_permute(dout, dop, BH, d, T, H, W, rank, 0);
@@ -737,17 +779,18 @@ void orc_backward(const double *q, const double *k, const double *v,
     if (gf && dgf)
         orc_permute(dgfp, dgf, BH, d, T, H, W, rank, 1);
 
-    orc_fine_bwd(qp, kp, vp, dof, idx, cnt, K, BH, N, d, scale, dqp, dkp, dvp);
+    orc_fine_bwd(qp, kp, vp, dof, idx, cnt, K, BH, N, d, scale, slot_ok, dqp, dkp, dvp);
     orc_coarse_bwd(qc, kc, vc, doc, BH, (int)Nc, d, scale, dqc, dkc, dvc);
 
-    /* Mean-pool backward: every token of a cube gets dXc / 64. */
+    /* Mean-pool backward: every token of a cube gets dXc / (tokens in the
+     * cube); padding slots are dropped by the inverse reordering. */
     for (int64_t bh = 0; bh < BH; bh++)
         for (int64_t i = 0; i < N; i++)
             for (int c = 0; c < d; c++) {
                 int64_t e = (bh * N + i) * d + c, ec = (bh * Nc + i / CUBE) * d + c;
-                dqp[e] += dqc[ec] / CUBE;
-                dkp[e] += dkc[ec] / CUBE;
-                dvp[e] += dvc[ec] / CUBE;
+                dqp[e] += dqc[ec] / ntok[i / CUBE];
+                dkp[e] += dkc[ec] / ntok[i / CUBE];
+                dvp[e] += dvc[ec] / ntok[i / CUBE];
             }
     orc_permute(dqp, dq, BH, d, T, H, W, rank, 1);
     orc_permute(dkp, dk, BH, d, T, H, W, rank, 1);
@@ -756,6 +799,7 @@ void orc_backward(const double *q, const double *k, const double *v,
     free(qp); free(kp); free(vp); free(qc); free(kc); free(vc); free(oc); free(of);
     free(lse); free(dop); free(gcp); free(gfp); free(dgcp); free(dgfp); free(dof); free(doc);
     free(dqp); free(dkp); free(dvp); free(dqc); free(dkc); free(dvc); free(cnt);
+    free(slot_ok); free(ntok);
 }
 
 /* ---- index-list conversions ("Sparse Encoding in CK Tile": Jenga's M x M

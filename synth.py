@@ -51,7 +51,9 @@ class Workload:
 
     @property
     def Nc(self) -> int:
-        return self.N // 64
+        """Cubes of (4, 4, 4) covering the grid (a side that is not a
+        multiple of 4 ends in partial cubes)."""
+        return ((self.T + 3) // 4) * ((self.H + 3) // 4) * ((self.W + 3) // 4)
 
     @property
     def BH(self) -> int:
@@ -74,6 +76,12 @@ WORKLOADS = {
     "wan1.3b_k64": Workload("wan1.3b_k64", 1, 12, 128, 16, 32, 64, 64),
     "wan14b": Workload("wan14b", 1, 40, 128, 16, 32, 64, 154),
     "long": Workload("long", 1, 24, 128, 32, 48, 80, 192),
+    # Grids whose sides are not multiples of 4 (partial boundary cubes).
+    "odd": Workload("odd", 1, 2, 64, 5, 6, 10, 3),
+    "odd_small": Workload("odd_small", 1, 4, 128, 9, 14, 22, 12),
+    # The Wan2.1 latent of an 832x480, 81-frame video after (1, 2, 2)
+    # patchify: 21 x 30 x 52 = 32760 tokens, 6 x 8 x 13 = 624 cubes.
+    "wan1.3b_latent": Workload("wan1.3b_latent", 1, 12, 128, 21, 30, 52, 187),
 }
 
 

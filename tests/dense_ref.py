@@ -14,24 +14,30 @@ import numpy as np
 import torch
 
 
-def cube_ids(T: int, H: int, W: int) -> np.ndarray:
-    """Cube id of every native token n = (t*H + h)*W + w, cubes in raster order."""
+def cube_ids(T: int, H: int, W: int, rank=None) -> np.ndarray:
+    """Cube id of every native token n = (t*H + h)*W + w: cubes of (4, 4, 4)
+    tokens in raster order over the ceil(T/4) x ceil(H/4) x ceil(W/4) cube
+    grid (boundary cubes may be partial), relabelled by rank[] if given."""
+    Hc, Wc = -(-H // 4), -(-W // 4)
     t, h, w = np.meshgrid(np.arange(T), np.arange(H), np.arange(W), indexing="ij")
-    return (((t // 4) * (H // 4) + h // 4) * (W // 4) + w // 4).reshape(-1)
+    cid = (((t // 4) * Hc + h // 4) * Wc + w // 4).reshape(-1)
+    return cid if rank is None else np.asarray(rank)[cid]
 
 
-def dense_vsa(q, k, v, T, H, W, lut, scale, gc=None, gf=None, cnt=None):
+def dense_vsa(q, k, v, T, H, W, lut, scale, gc=None, gf=None, cnt=None, rank=None):
     """q, k, v: torch float64 [BH, N, d] native order; lut: int [BH, Nc, Kmax].
 
+    Each cube's vector is the mean of the tokens that belong to it.
     Returns (out, O_f, O_c broadcast to tokens, coarse scores, lse), native order.
     """
     BH, N, d = q.shape
-    cid = torch.as_tensor(cube_ids(T, H, W), dtype=torch.long)
-    Nc = N // 64
+    cid = torch.as_tensor(cube_ids(T, H, W, rank), dtype=torch.long)
+    Nc = (-(-T // 4)) * (-(-H // 4)) * (-(-W // 4))
     onehot = (cid[:, None] == torch.arange(Nc)[None, :]).to(torch.float64)  # [N, Nc]
-    qc = onehot.T @ q / 64.0
-    kc = onehot.T @ k / 64.0
-    vc = onehot.T @ v / 64.0
+    members = onehot.sum(0)[:, None]
+    qc = onehot.T @ q / members
+    kc = onehot.T @ k / members
+    vc = onehot.T @ v / members
     sc = (qc @ kc.transpose(-1, -2)) * scale
     oc = torch.softmax(sc, dim=-1) @ vc                                  # [BH, Nc, d]
     lut = torch.as_tensor(np.asarray(lut), dtype=torch.long)

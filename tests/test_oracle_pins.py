@@ -477,3 +477,58 @@ def test_add_neighbors_is_order_independent(oracle_mod):
     for r in range(Nc):
         got = np.sort(order[out_h[0, rank[r], :cnt_h[0, rank[r]]]])
         np.testing.assert_array_equal(got, out_r[0, r, :cnt_r[0, r]])
+
+
+# ---------------------------------------------------------------- grids not divisible by 4
+# Reading: a side that is not a multiple of 4 ends in partial cubes; padding
+# slots are zero in the reordered tensors, left out of the cube means, never
+# attended to and never written back.  The dense formulation needs no padding
+# at all (cube ids straight from the coordinates, means over cube members), so
+# agreement pins the oracle's padded reordering, pooling and masking.
+@pytest.mark.parametrize("curve", ["raster", "hilbert"])
+@pytest.mark.parametrize("gates", [True, False])
+def test_padded_grid_matches_dense(oracle_mod, curve, gates):
+    wl = synth.WORKLOADS["odd"]
+    q, k, v, gc, gf, dout = _tiny_inputs(wl, gates)
+    scale = wl.d ** -0.5
+    r = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, scale, gc=gc, gf=gf, curve=curve)
+    rank = None if curve == "raster" else oracle_mod.cube_rank(*oracle_mod.cube_grid(wl.T, wl.H, wl.W), curve)
+    out, of, ocb, sc, lse = dense_vsa(_t(q), _t(k), _t(v), wl.T, wl.H, wl.W, r["idx"], scale,
+                                      gc=_t(gc), gf=_t(gf), rank=rank)
+    np.testing.assert_allclose(r["scores"], sc.numpy(), rtol=1e-12, atol=1e-10)
+    tk_idx = torch.topk(sc, wl.topk, dim=-1).indices.numpy()
+    assert np.array_equal(np.sort(tk_idx, -1), np.sort(r["idx"], -1))
+    np.testing.assert_allclose(r["out"], out.numpy(), rtol=1e-10, atol=1e-10)
+    pos = oracle_mod.sfc_table(wl.T, wl.H, wl.W, curve)
+    np.testing.assert_allclose(r["of"][:, pos], of.numpy(), rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(r["lse"][:, pos], lse.numpy(), rtol=1e-12)
+    # backward against autograd of the dense formulation
+    g = oracle_mod.backward(q, k, v, dout, r["idx"], wl.T, wl.H, wl.W, scale, gc=gc, gf=gf, curve=curve)
+    leaves = {n: torch.tensor(a, dtype=torch.float64, requires_grad=True)
+              for n, a in (("q", q), ("k", k), ("v", v), ("gc", gc), ("gf", gf)) if a is not None}
+    o2, *_ = dense_vsa(leaves["q"], leaves["k"], leaves["v"], wl.T, wl.H, wl.W, r["idx"], scale,
+                       gc=leaves.get("gc"), gf=leaves.get("gf"), rank=rank)
+    (o2 * torch.tensor(dout, dtype=torch.float64)).sum().backward()
+    for n, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("gc", "dgc"), ("gf", "dgf")):
+        if n in leaves:
+            np.testing.assert_allclose(g[key], leaves[n].grad.numpy(), rtol=1e-9, atol=1e-9, err_msg=key)
+
+
+def test_padded_reordering_slots(oracle_mod):
+    """Partial cubes: every token lands in its own cube's slot block, the
+    padding slots are zero, the token counts are the partial box volumes, and
+    the inverse drops the padding."""
+    T, H, W = 5, 6, 10
+    Tc, Hc, Wc = oracle_mod.cube_grid(T, H, W)
+    assert (Tc, Hc, Wc) == (2, 2, 3)
+    x = np.random.default_rng(5).standard_normal((2, T * H * W, 8))
+    y = oracle_mod.permute(x, T, H, W)
+    assert y.shape == (2, 64 * Tc * Hc * Wc, 8)
+    slot_ok, ntok = oracle_mod.cube_slots(T, H, W)
+    assert np.all(y[:, slot_ok == 0] == 0) and slot_ok.sum() == T * H * W
+    box = lambda c, n: min(4, n - 4 * c)
+    want = [box(ct, T) * box(ch, H) * box(cw, W) for ct in range(Tc) for ch in range(Hc) for cw in range(Wc)]
+    assert ntok.tolist() == want
+    pos = oracle_mod.sfc_table(T, H, W)
+    np.testing.assert_array_equal(pos // 64, cube_ids(T, H, W))
+    np.testing.assert_array_equal(oracle_mod.permute(y, T, H, W, inverse=True), x)
