@@ -17,7 +17,7 @@ import torch
 from . import _lib
 from ._lib import Grid, VSAError, VSA_DTYPE_BF16, VSA_DTYPE_F32
 
-__all__ = ["cube_order", "permute", "coarse_topk", "fine_fwd", "fine_bwd", "forward", "backward",
+__all__ = ["num_cubes", "cube_order", "permute", "coarse_topk", "fine_fwd", "fine_bwd", "forward", "backward",
            "workspace_bytes", "device_status", "timing_enable", "timing_read", "VSAError",
            "ForwardState", "Grid"]
 
@@ -46,10 +46,15 @@ def _bhnd(x: torch.Tensor):
     raise ValueError("expected [B, heads, N, d] or [BH, N, d]")
 
 
+def num_cubes(T: int, H: int, W: int) -> int:
+    """Cubes of (4, 4, 4) covering a (T, H, W) grid (partial ones included)."""
+    return ((T + 3) // 4) * ((H + 3) // 4) * ((W + 3) // 4)
+
+
 def cube_order(T: int, H: int, W: int, curve: str = "hilbert", device="cuda") -> torch.Tensor:
     """vsa_cube_order: int32 [2 * Nc] table (position -> raster cube id, then
     raster cube id -> position) for curve "raster" or "hilbert"."""
-    Nc = (T // 4) * (H // 4) * (W // 4)
+    Nc = num_cubes(T, H, W)
     order = torch.empty(2 * Nc, dtype=torch.int32, device=device)
     code = {"raster": _lib.VSA_CURVE_RASTER, "hilbert": _lib.VSA_CURVE_HILBERT}[curve]
     _lib.check("vsa_cube_order", _lib.load().vsa_cube_order(Grid.of(T, H, W), code, _ptr(order), _stream()))
@@ -58,12 +63,15 @@ def cube_order(T: int, H: int, W: int, curve: str = "hilbert", device="cuda") ->
 
 def permute(x: torch.Tensor, T: int, H: int, W: int, inverse: bool = False, pool: bool = False,
             cube_order=None):
-    """vsa_permute: native <-> cube order; with pool=True also the cube means."""
+    """vsa_permute: native [.., T*H*W, d] <-> cube order [.., 64*Nc, d] (a grid
+    side that is not a multiple of 4 ends in partial cubes whose padding slots
+    are zero); with pool=True also the cube means [.., Nc, d]."""
     BH, N, d = _bhnd(x)
-    y = torch.empty_like(x)
+    Nc = num_cubes(T, H, W)
+    y = torch.empty(x.shape[:-2] + ((T * H * W) if inverse else 64 * Nc, d), dtype=x.dtype, device=x.device)
     pooled = None
     if pool:
-        pooled = torch.empty(x.shape[:-2] + (N // 64, d), dtype=torch.float32, device=x.device)
+        pooled = torch.empty(x.shape[:-2] + (Nc, d), dtype=torch.float32, device=x.device)
     _lib.check("vsa_permute", _lib.load().vsa_permute(_ptr(x), _ptr(y), _ptr(pooled), BH, d,
                                                        Grid.of(T, H, W, _ptr(cube_order)), int(inverse),
                                                        _stream()))
@@ -168,8 +176,9 @@ class ForwardState:
         _lib.check("vsa_forward_saved", _lib.load().vsa_forward_saved(
             _ptr(self.ws), self.B, self.heads, self.d, Grid.of(self.T, self.H, self.W), self.topk,
             ctypes.byref(s)))
-        BH, N, d, K = self.B * self.heads, self.T * self.H * self.W, self.d, self.topk
-        Nc = N // 64
+        BH, d, K = self.B * self.heads, self.d, self.topk
+        Nc = num_cubes(self.T, self.H, self.W)
+        N = 64 * Nc  # reordered length (padding slots included)
         base = self.ws.data_ptr()
 
         def view(ptr, shape, dtype):

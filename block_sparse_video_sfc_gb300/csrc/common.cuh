@@ -18,15 +18,29 @@ __device__ __forceinline__ void flag_error(int* err, int bit) {
   if (err) atomicOr(err, bit);
 }
 
-// Native token index of offset o (0..63) of cube (ct, ch, cw):
-// t = 4ct + o/16, h = 4ch + (o/4)%4, w = 4cw + o%4.
-__host__ __device__ __forceinline__ int64_t native_token(int cube, int o, int H, int W) {
-  int cw_n = W >> 2, ch_n = H >> 2;
-  int cw = cube % cw_n;
-  int ch = (cube / cw_n) % ch_n;
-  int ct = cube / (cw_n * ch_n);
-  int t = 4 * ct + (o >> 4), h = 4 * ch + ((o >> 2) & 3), w = 4 * cw + (o & 3);
-  return (static_cast<int64_t>(t) * H + h) * W + w;
+// A (T, H, W) token grid covered by cubes of (4, 4, 4): Hc = ceil(H / 4)
+// and Wc = ceil(W / 4) cubes along h and w.  When a side is not a multiple
+// of 4 the boundary cubes stick out of the grid; their slots outside it are
+// padding.
+struct CubeGrid {
+  int T, H, W, Hc, Wc;
+};
+inline CubeGrid cube_grid(int T, int H, int W) { return CubeGrid{T, H, W, (H + 3) / 4, (W + 3) / 4}; }
+
+// Native token n = (t*H + h)*W + w at offset o (0..63) of raster cube rc =
+// (ct*Hc + ch)*Wc + cw, with t = 4ct + o/16, h = 4ch + (o/4)%4, w = 4cw + o%4;
+// -1 when that slot is padding.
+__host__ __device__ __forceinline__ int64_t native_token(int rc, int o, const CubeGrid& g) {
+  const int cw = rc % g.Wc, ch = (rc / g.Wc) % g.Hc, ct = rc / (g.Wc * g.Hc);
+  const int t = 4 * ct + (o >> 4), h = 4 * ch + ((o >> 2) & 3), w = 4 * cw + (o & 3);
+  if (t >= g.T || h >= g.H || w >= g.W) return -1;
+  return (static_cast<int64_t>(t) * g.H + h) * g.W + w;
+}
+
+// Number of grid tokens in raster cube rc (64 unless the cube is partial).
+__host__ __device__ __forceinline__ int cube_tokens(int rc, const CubeGrid& g) {
+  const int cw = rc % g.Wc, ch = (rc / g.Wc) % g.Hc, ct = rc / (g.Wc * g.Hc);
+  return min(4, g.T - 4 * ct) * min(4, g.H - 4 * ch) * min(4, g.W - 4 * cw);
 }
 
 // Raster id of the cube at position `pos` of the cube sequence: the first
@@ -97,7 +111,9 @@ int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH
                        cudaStream_t s);
 int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt,
                     int kmax, int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, int f16_in,
-                    const int32_t* pairs, cudaStream_t s);
+                    const int32_t* pairs, const uint64_t* kmask, cudaStream_t s);
+// kmask[c] (c = cube position): bit o set when slot o holds a grid token.
+int launch_slot_masks(int T, int H, int W, const int32_t* order, uint64_t* kmask, cudaStream_t s);
 size_t pair_plan_smem(int Nc);
 size_t pair_plan_ws_bytes(int BH, int Nc);  // pairs + overlap scratch of launch_pair_plan
 int launch_list_bits(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, uint32_t* bits,

@@ -76,7 +76,27 @@ __global__ void __launch_bounds__(kOrderThreads) cube_order_kernel(int Tc, int H
   }
 }
 
+// kmask[c]: bit o set when slot o of the cube at position c holds a grid
+// token (all 64 bits unless the cube sticks out of a grid whose side is not a
+// multiple of 4).
+__global__ void slot_mask_kernel(int Nc, CubeGrid g, const int32_t* __restrict__ order, uint64_t* __restrict__ kmask) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= Nc) return;
+  const int rc = raster_cube(order, c);
+  uint64_t m = 0;
+  for (int o = 0; o < kCube; ++o)
+    if (native_token(rc, o, g) >= 0) m |= 1ull << o;
+  kmask[c] = m;
+}
+
 }  // namespace
+
+int launch_slot_masks(int T, int H, int W, const int32_t* order, uint64_t* kmask, cudaStream_t s) {
+  const CubeGrid g = cube_grid(T, H, W);
+  const int Nc = ((T + 3) / 4) * g.Hc * g.Wc;
+  slot_mask_kernel<<<(Nc + 255) / 256, 256, 0, s>>>(Nc, g, order, kmask);
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
 
 int launch_cube_order(int Tc, int Hc, int Wc, int curve, int32_t* order, cudaStream_t s) {
   int b = 0;

@@ -55,6 +55,7 @@ struct FwdParams {
   const int32_t* idx;
   const int32_t* cnt;
   const int32_t* pairs;  // [BH][npairs][2] tile -> query cubes (second -1: none), or null
+  const uint64_t* kmask;  // [Nc]: bit o set when slot o of the cube holds a token; null: every slot does
   int kmax, N, Nc, npairs;
   int nk, nv;        // K and V ring depths (1..kMaxStages)
   float scale_log2;  // scale * log2(e)
@@ -440,6 +441,16 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       float mx = -INFINITY;
       if (valid) {
         tmem_ld64_wait(sb + 64 * half, sr);
+        if (p.kmask) {
+          // A partial cube (a grid side not a multiple of 4): its padding
+          // slots are no keys.  Column c of this half is slot c of the cube.
+          const uint64_t km = __ldg(p.kmask + (e & 0x3FFFFFFF));
+          if (km != ~0ull) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (!((km >> c) & 1ull)) sr[c] = 0xFF800000u;  // -inf
+          }
+        }
         mx = max64(sr) * p.scale_log2;
       }
       // S is in registers: the buffer may take S(j + 1).
@@ -594,7 +605,7 @@ int make_tile_map(void* map_out, const void* base, int64_t rows, int d, int f16)
 
 int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt, int kmax,
                     int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, int f16_in,
-                    const int32_t* pairs, cudaStream_t s) {
+                    const int32_t* pairs, const uint64_t* kmask, cudaStream_t s) {
   FwdParams p{};
   const int64_t rows = static_cast<int64_t>(BH) * N;
   int st;
@@ -602,6 +613,7 @@ int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_
   if ((st = make_tile_map(&p.tv, vp, rows, d, f16_in)) != VSA_OK) return st;
   p.q = static_cast<const uint16_t*>(qp);
   p.pairs = pairs;
+  p.kmask = kmask;
   p.idx = idx;
   p.cnt = cnt;
   p.kmax = kmax;

@@ -8,6 +8,9 @@
 // cube-order destination is one contiguous 64*d*2-byte block.  The pooled
 // mean is summed in fp32 while the data passes through registers.
 // HBM-bound: per tensor, N*d*2 bytes read + N*d*2 written (+ Nc*d*4 pooled).
+// A grid side that is not a multiple of 4 ends in partial cubes: their slots
+// outside the grid are written as zeros (cube order) or skipped (native
+// order), and the pooled mean divides by the cube's token count.
 #include "common.cuh"
 
 namespace vsa {
@@ -21,7 +24,7 @@ struct PermuteArgs {
 // F16OUT: the destination holds the same values as fp16 (exact for inputs of
 // magnitude <= 65504; larger ones saturate and latch kErrRange).
 template <int D, bool F16OUT>
-__global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc, int H, int W, int N,
+__global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc, CubeGrid g, int64_t Nn,
                                                            const int32_t* __restrict__ order, int inverse, int* err) {
   constexpr int kChunks = D / 8;           // 16-byte chunks per token
   constexpr int kTokPerPass = 256 / kChunks;
@@ -32,8 +35,9 @@ __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc
   const int64_t bh = cube_glob / Nc;
   const int cube = static_cast<int>(cube_glob % Nc);
   const int rcube = raster_cube(order, cube);
-  const __nv_bfloat16* src = a.src[tensor] + bh * static_cast<int64_t>(N) * D;
-  uint16_t* dst = static_cast<uint16_t*>(a.dst[tensor]) + bh * static_cast<int64_t>(N) * D;
+  const int64_t Np = static_cast<int64_t>(Nc) * kCube;  // reordered tokens per (batch, head)
+  const __nv_bfloat16* src = a.src[tensor] + bh * (inverse ? Np : Nn) * D;
+  uint16_t* dst = static_cast<uint16_t*>(a.dst[tensor]) + bh * (inverse ? Nn : Np) * D;
   float* pooled = a.pooled[tensor];
   const int j = threadIdx.x % kChunks;     // channel chunk, fixed per thread
   const int o0 = threadIdx.x / kChunks;
@@ -41,11 +45,12 @@ __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc
 #pragma unroll
   for (int p = 0; p < kPasses; ++p) {
     const int o = o0 + p * kTokPerPass;
-    const int64_t nat = native_token(rcube, o, H, W);
+    const int64_t nat = native_token(rcube, o, g);
     const int64_t cub = static_cast<int64_t>(cube) * kCube + o;
+    if (nat < 0 && inverse) continue;  // padding slot: nothing to write back
     const int64_t s_tok = inverse ? cub : nat;
     const int64_t d_tok = inverse ? nat : cub;
-    uint4 v = *reinterpret_cast<const uint4*>(src + s_tok * D + j * 8);
+    const uint4 v = nat < 0 ? make_uint4(0, 0, 0, 0) : *reinterpret_cast<const uint4*>(src + s_tok * D + j * 8);
     if (F16OUT) {
       const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
                           bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
@@ -73,7 +78,7 @@ __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc
       float s = 0.f;
 #pragma unroll 8
       for (int r = 0; r < kTokPerPass; ++r) s += red[r][c];
-      pooled[cube_glob * D + c] = s * (1.0f / kCube);
+      pooled[cube_glob * D + c] = s / static_cast<float>(cube_tokens(rcube, g));
     }
   }
 }
@@ -86,20 +91,22 @@ int launch_permute(const void* const* src, void* const* dst, float* const* poole
     a.dst[i] = dst[i];
     a.pooled[i] = pooled ? pooled[i] : nullptr;
   }
-  const int N = T * H * W, Nc = N / kCube;
+  const CubeGrid g = cube_grid(T, H, W);
+  const int Nc = ((T + 3) / 4) * g.Hc * g.Wc;
+  const int64_t Nn = static_cast<int64_t>(T) * H * W;
   dim3 grid(static_cast<unsigned>(static_cast<int64_t>(BH) * Nc), ntensors);
   int* err = device_error_word();
   timing_mark(VSA_K_PERMUTE, true, s);
   if (d == 128) {
     if (f16_out)
-      permute_pool_kernel<128, true><<<grid, 256, 0, s>>>(a, Nc, H, W, N, order, inverse, err);
+      permute_pool_kernel<128, true><<<grid, 256, 0, s>>>(a, Nc, g, Nn, order, inverse, err);
     else
-      permute_pool_kernel<128, false><<<grid, 256, 0, s>>>(a, Nc, H, W, N, order, inverse, err);
+      permute_pool_kernel<128, false><<<grid, 256, 0, s>>>(a, Nc, g, Nn, order, inverse, err);
   } else {
     if (f16_out)
-      permute_pool_kernel<64, true><<<grid, 256, 0, s>>>(a, Nc, H, W, N, order, inverse, err);
+      permute_pool_kernel<64, true><<<grid, 256, 0, s>>>(a, Nc, g, Nn, order, inverse, err);
     else
-      permute_pool_kernel<64, false><<<grid, 256, 0, s>>>(a, Nc, H, W, N, order, inverse, err);
+      permute_pool_kernel<64, false><<<grid, 256, 0, s>>>(a, Nc, g, Nn, order, inverse, err);
   }
   timing_mark(VSA_K_PERMUTE, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;

@@ -21,26 +21,29 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+// N is the reordered length 64 * Nc (>= T * H * W when a side of the grid is
+// not a multiple of 4 and the boundary cubes carry padding slots).
 struct Dims {
   int64_t BH, N, Nc;
   int d, T, H, W;
+  bool padded;
 };
 
 int check_grid(const vsa_grid_t& g, int d, Dims* out, int64_t BH) {
   if (g.ct != 4 || g.ch != 4 || g.cw != 4) return VSA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return VSA_ERR_UNSUPPORTED;
   if (g.T <= 0 || g.H <= 0 || g.W <= 0 || BH <= 0) return VSA_ERR_ARG;
-  if (g.T % 4 || g.H % 4 || g.W % 4) return VSA_ERR_SHAPE;
   if (reinterpret_cast<uintptr_t>(g.cube_order) & 3u) return VSA_ERR_ARG;
-  const int64_t N = static_cast<int64_t>(g.T) * g.H * g.W;
+  const int64_t Nc = static_cast<int64_t>((g.T + 3) / 4) * ((g.H + 3) / 4) * ((g.W + 3) / 4);
+  const int64_t N = Nc * kCube;
   if (N * BH >= (int64_t(1) << 31)) return VSA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
-  *out = Dims{BH, N, N / kCube, d, g.T, g.H, g.W};
+  *out = Dims{BH, N, Nc, d, g.T, g.H, g.W, (g.T % 4) || (g.H % 4) || (g.W % 4)};
   return VSA_OK;
 }
 
 // Forward workspace: the saved state of one vsa_forward call.
 struct FwdWs {
-  size_t qp, kp, vp, qc, kc, vc, oc, lsec, sc, idx, cnt, of, lse, lbits, pairs, total;
+  size_t qp, kp, vp, qc, kc, vc, oc, lsec, sc, idx, cnt, of, lse, lbits, pairs, kmask, total;
 };
 FwdWs fwd_layout(const Dims& D, int K) {
   FwdWs w{};
@@ -62,6 +65,7 @@ FwdWs fwd_layout(const Dims& D, int K) {
   w.lse = o; o += align256(sizeof(float) * D.BH * D.N);
   w.lbits = o; o += align256(sizeof(uint32_t) * D.BH * D.Nc * ((D.Nc + 31) / 32));
   w.pairs = o; o += align256(pair_plan_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.Nc)));
+  w.kmask = o; o += align256(sizeof(uint64_t) * D.Nc);
   w.total = o;
   return w;
 }
@@ -228,7 +232,8 @@ int vsa_lut_add_neighbors(const int32_t* kv_block_idx_in, const int32_t* valid_b
   if (!kv_block_idx_in || !kv_block_idx_out || !valid_block_num_out) return VSA_ERR_ARG;
   if (max_kv_blocks_in < 1 || max_kv_blocks_out < 1 || radius < 0 || radius > 7) return VSA_ERR_ARG;
   if (D.Nc > (1 << 16)) return VSA_ERR_UNSUPPORTED;
-  return launch_add_neighbors(kv_block_idx_in, valid_block_num_in, max_kv_blocks_in, BH, g.T / 4, g.H / 4, g.W / 4,
+  return launch_add_neighbors(kv_block_idx_in, valid_block_num_in, max_kv_blocks_in, BH, (g.T + 3) / 4,
+                              (g.H + 3) / 4, (g.W + 3) / 4,
                               g.cube_order, radius, max_kv_blocks_out, kv_block_idx_out, valid_block_num_out, as_stream(stream));
 }
 
@@ -239,7 +244,7 @@ int vsa_cube_order(vsa_grid_t g, int curve, int32_t* order, void* stream) {
   if (st != VSA_OK) return st;
   if (!order || (reinterpret_cast<uintptr_t>(order) & 3u)) return VSA_ERR_ARG;
   if (curve != VSA_CURVE_RASTER && curve != VSA_CURVE_HILBERT) return VSA_ERR_ARG;
-  return launch_cube_order(g.T / 4, g.H / 4, g.W / 4, curve, order, as_stream(stream));
+  return launch_cube_order((g.T + 3) / 4, (g.H + 3) / 4, (g.W + 3) / 4, curve, order, as_stream(stream));
 }
 
 int vsa_selftest_wait_timeout(uint32_t polls, void* stream) {
@@ -309,7 +314,7 @@ int vsa_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* 
   if (!o_fine || !aligned16(o_fine)) return VSA_ERR_ARG;
   if (o_dtype != VSA_DTYPE_BF16 && o_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
   return launch_fine_fwd(qp, kp, vp, kv_block_idx, valid_block_num, max_kv_blocks, BH, N, d, scale, o_fine, o_dtype,
-                         lse, 0, nullptr, as_stream(stream));
+                         lse, 0, nullptr, nullptr, as_stream(stream));
 }
 
 int vsa_fine_bwd(const void* qp, const void* kp, const void* vp, const void* o_fine, int o_dtype, const float* lse,
@@ -393,9 +398,12 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
                              s)) != VSA_OK)
     return st;
   if ((st = launch_pair_plan(at<uint32_t>(ws, w.lbits), BH, Nc, at<int32_t>(ws, w.pairs), s)) != VSA_OK) return st;
+  // Padding slots of partial cubes are masked out of the keys.
+  uint64_t* kmask = D.padded ? at<uint64_t>(ws, w.kmask) : nullptr;
+  if (kmask && (st = launch_slot_masks(g.T, g.H, g.W, g.cube_order, kmask, s)) != VSA_OK) return st;
   if ((st = launch_fine_fwd(dst[0], dst[1], dst[2], at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), topk, BH, N, d,
                             scale, at<float>(ws, w.of), VSA_DTYPE_F32, at<float>(ws, w.lse), 1,
-                            at<int32_t>(ws, w.pairs), s)) != VSA_OK)
+                            at<int32_t>(ws, w.pairs), kmask, s)) != VSA_OK)
     return st;
   return launch_combine(at<float>(ws, w.oc), at<float>(ws, w.of), g_coarse, g_fine, out, out_dtype, BH, d, g.T, g.H,
                         g.W, g.cube_order, s);

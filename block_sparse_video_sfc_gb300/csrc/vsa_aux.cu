@@ -21,7 +21,7 @@ template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ oc, const float* __restrict__ of,
                                                       const __nv_bfloat16* __restrict__ gc,
                                                       const __nv_bfloat16* __restrict__ gf, void* __restrict__ out,
-                                                      int out_dtype, int Nc, int H, int W, int N,
+                                                      int out_dtype, int Nc, CubeGrid g, int64_t Nn,
                                                       const int32_t* __restrict__ order) {
   constexpr int kChunks = D / 8, kTok = 256 / kChunks, kPasses = kCube / kTok;
   const int64_t cg = blockIdx.x;
@@ -34,8 +34,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 #pragma unroll
   for (int p = 0; p < kPasses; ++p) {
     const int o = o0 + p * kTok;
-    const int64_t nat = bh * N + native_token(rcube, o, H, W);
-    const int64_t cub = bh * N + static_cast<int64_t>(cube) * kCube + o;
+    const int64_t tok = native_token(rcube, o, g);
+    if (tok < 0) continue;  // padding slot
+    const int64_t nat = bh * Nn + tok;
+    const int64_t cub = (bh * Nc + cube) * kCube + o;
     float f[8], a[8], b[8], r[8];
     load8_f32(of, cub * D + j * 8, f);
     if (gc) load8_bf16(gc, nat * D + j * 8, a);
@@ -54,8 +56,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        const float* __restrict__ oc, const float* __restrict__ of,
                                                        __half* __restrict__ dof, float* __restrict__ delta,
                                                        float* __restrict__ doc, void* __restrict__ dgc,
-                                                       void* __restrict__ dgf, int grad_dtype, int Nc, int H, int W,
-                                                       int N, const int32_t* __restrict__ order, int* err) {
+                                                       void* __restrict__ dgf, int grad_dtype, int Nc, CubeGrid grid,
+                                                       int64_t Nn, const int32_t* __restrict__ order, int* err) {
   constexpr int kChunks = D / 8, kTok = 256 / kChunks, kPasses = kCube / kTok;
   __shared__ float red[kTok][D];
   const int64_t cg = blockIdx.x;
@@ -68,13 +70,17 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 #pragma unroll
   for (int p = 0; p < kPasses; ++p) {
     const int o = o0 + p * kTok;
-    const int64_t nat = bh * N + native_token(rcube, o, H, W);
-    const int64_t cub = bh * N + static_cast<int64_t>(cube) * kCube + o;
+    const int64_t tok = native_token(rcube, o, grid);
+    const bool real = tok >= 0;  // padding slots get dO = 0: zero dO_f and D
+    const int64_t nat = bh * Nn + (real ? tok : 0);
+    const int64_t cub = (bh * Nc + cube) * kCube + o;
     float g[8], a[8], b[8], f[8], t[8];
-    load8_bf16(dout, nat * D + j * 8, g);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[e] = a[e] = b[e] = 0.f;
+    if (real) load8_bf16(dout, nat * D + j * 8, g);
     load8_f32(of, cub * D + j * 8, f);
-    if (gc) load8_bf16(gc, nat * D + j * 8, a);
-    if (gf) load8_bf16(gf, nat * D + j * 8, b);
+    if (gc && real) load8_bf16(gc, nat * D + j * 8, a);
+    if (gf && real) load8_bf16(gf, nat * D + j * 8, b);
     uint4 packed;
     uint32_t* pk = reinterpret_cast<uint32_t*>(&packed);
     float dsum = 0.f;
@@ -95,12 +101,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
     if (j == 0) delta[cub] = dsum;
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = fmaf(gc ? a[e] : 1.f, g[e], acc[e]);
-    if (gc && dgc) {
+    if (gc && dgc && real) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) t[e] = g[e] * c[e];
       store8(dgc, nat * D + j * 8, t, grad_dtype);
     }
-    if (gf && dgf) {
+    if (gf && dgf && real) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) t[e] = g[e] * f[e];
       store8(dgf, nat * D + j * 8, t, grad_dtype);
@@ -124,7 +130,7 @@ struct FinalizeArgs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256) finalize_kernel(FinalizeArgs a, int grad_dtype, int Nc, int H, int W, int N,
+__global__ void __launch_bounds__(256) finalize_kernel(FinalizeArgs a, int grad_dtype, int Nc, CubeGrid g, int64_t Nn,
                                                        const int32_t* __restrict__ order) {
   constexpr int kChunks = D / 8, kTok = 256 / kChunks, kPasses = kCube / kTok;
   const int t = blockIdx.y;
@@ -135,13 +141,16 @@ __global__ void __launch_bounds__(256) finalize_kernel(FinalizeArgs a, int grad_
   const int j = threadIdx.x % kChunks, o0 = threadIdx.x / kChunks;
   float c[8];
   load8_f32(a.pooled[t], cg * D + j * 8, c);
+  const float inv_tokens = 1.0f / static_cast<float>(cube_tokens(rcube, g));
 #pragma unroll
-  for (int e = 0; e < 8; ++e) c[e] *= (1.0f / kCube);
+  for (int e = 0; e < 8; ++e) c[e] *= inv_tokens;
 #pragma unroll
   for (int p = 0; p < kPasses; ++p) {
     const int o = o0 + p * kTok;
-    const int64_t nat = bh * N + native_token(rcube, o, H, W);
-    const int64_t cub = bh * N + static_cast<int64_t>(cube) * kCube + o;
+    const int64_t tok = native_token(rcube, o, g);
+    if (tok < 0) continue;  // padding slot
+    const int64_t nat = bh * Nn + tok;
+    const int64_t cub = (bh * Nc + cube) * kCube + o;
     float f[8];
     load8_f32(a.fine[t], cub * D + j * 8, f);
 #pragma unroll
@@ -154,15 +163,17 @@ __global__ void __launch_bounds__(256) finalize_kernel(FinalizeArgs a, int grad_
 
 int launch_combine(const float* oc, const float* of, const void* gc, const void* gf, void* out, int out_dtype, int BH,
                    int d, int T, int H, int W, const int32_t* order, cudaStream_t s) {
-  const int N = T * H * W, Nc = N / kCube;
+  const CubeGrid cg = cube_grid(T, H, W);
+  const int Nc = ((T + 3) / 4) * cg.Hc * cg.Wc;
+  const int64_t Nn = static_cast<int64_t>(T) * H * W;
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(BH) * Nc);
   auto g = static_cast<const __nv_bfloat16*>(gc);
   auto f = static_cast<const __nv_bfloat16*>(gf);
   timing_mark(VSA_K_COMBINE, true, s);
   if (d == 128)
-    combine_kernel<128><<<grid, 256, 0, s>>>(oc, of, g, f, out, out_dtype, Nc, H, W, N, order);
+    combine_kernel<128><<<grid, 256, 0, s>>>(oc, of, g, f, out, out_dtype, Nc, cg, Nn, order);
   else
-    combine_kernel<64><<<grid, 256, 0, s>>>(oc, of, g, f, out, out_dtype, Nc, H, W, N, order);
+    combine_kernel<64><<<grid, 256, 0, s>>>(oc, of, g, f, out, out_dtype, Nc, cg, Nn, order);
   timing_mark(VSA_K_COMBINE, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
@@ -170,17 +181,19 @@ int launch_combine(const float* oc, const float* of, const void* gc, const void*
 int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const float* oc, const float* of,
                     __half* dof, float* delta, float* doc, void* dgc, void* dgf, int grad_dtype, int BH, int d,
                     int T, int H, int W, const int32_t* order, cudaStream_t s) {
-  const int N = T * H * W, Nc = N / kCube;
+  const CubeGrid cg = cube_grid(T, H, W);
+  const int Nc = ((T + 3) / 4) * cg.Hc * cg.Wc;
+  const int64_t Nn = static_cast<int64_t>(T) * H * W;
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(BH) * Nc);
   auto dO = static_cast<const __nv_bfloat16*>(dout);
   auto g = static_cast<const __nv_bfloat16*>(gc);
   auto f = static_cast<const __nv_bfloat16*>(gf);
   timing_mark(VSA_K_BWD_PREP, true, s);
   if (d == 128)
-    bwd_prep_kernel<128><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, H, W, N, order,
+    bwd_prep_kernel<128><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, cg, Nn, order,
                                               device_error_word());
   else
-    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, H, W, N, order,
+    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, cg, Nn, order,
                                              device_error_word());
   timing_mark(VSA_K_BWD_PREP, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
@@ -189,14 +202,16 @@ int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const floa
 int launch_finalize(const float* dqp, const float* dkp, const float* dvp, const float* dqc, const float* dkc,
                     const float* dvc, void* dq, void* dk, void* dv, int grad_dtype, int BH, int d, int T, int H,
                     int W, const int32_t* order, cudaStream_t s) {
-  const int N = T * H * W, Nc = N / kCube;
+  const CubeGrid cg = cube_grid(T, H, W);
+  const int Nc = ((T + 3) / 4) * cg.Hc * cg.Wc;
+  const int64_t Nn = static_cast<int64_t>(T) * H * W;
   FinalizeArgs a{{dqp, dkp, dvp}, {dqc, dkc, dvc}, {dq, dk, dv}};
   dim3 grid(static_cast<unsigned>(static_cast<int64_t>(BH) * Nc), 3);
   timing_mark(VSA_K_FINALIZE, true, s);
   if (d == 128)
-    finalize_kernel<128><<<grid, 256, 0, s>>>(a, grad_dtype, Nc, H, W, N, order);
+    finalize_kernel<128><<<grid, 256, 0, s>>>(a, grad_dtype, Nc, cg, Nn, order);
   else
-    finalize_kernel<64><<<grid, 256, 0, s>>>(a, grad_dtype, Nc, H, W, N, order);
+    finalize_kernel<64><<<grid, 256, 0, s>>>(a, grad_dtype, Nc, cg, Nn, order);
   timing_mark(VSA_K_FINALIZE, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }

@@ -17,11 +17,19 @@
  *    N = T*H*W tokens in native (t, h, w) raster order, token n = (t*H+h)*W+w,
  *    unless a function says it takes the "cube order" (after vsa_permute).
  *  - Cubes are (Ct, Ch, Cw) = (4, 4, 4) = 64 tokens ([AMD] "Stage 1: Coarse
- *    Selection"); T, H, W must be multiples of 4.  Nc = N / 64 cubes.
+ *    Selection"): Nc = ceil(T/4) * ceil(H/4) * ceil(W/4) cubes.  A side that
+ *    is not a multiple of 4 ends in partial cubes: the cube keeps its 64
+ *    slots in cube order, and the slots whose token would fall outside the
+ *    grid are padding -- zero in cube-order tensors, left out of the cube's
+ *    mean (which divides by the cube's token count), masked out of the keys
+ *    by vsa_forward, and never written back to native order.  Cube-order
+ *    tensors are [BH, Np, d] with Np = 64 * Nc (= N when 4 divides T, H, W).
  *  - d (head dim) must be 64 or 128.
  *  - Cube order: the 3D space-filling-curve reordering of [AMD] "Two-Stage
- *    Architecture" is taken as cube-raster order: cube c = ((t/4)*(H/4) +
- *    h/4)*(W/4) + w/4, offset o = ((t%4)*4 + h%4)*4 + w%4, position 64c + o.
+ *    Architecture".  By default cube-raster order: cube c = ((t/4)*Hc +
+ *    h/4)*Wc + w/4 with Hc = ceil(H/4), Wc = ceil(W/4), offset
+ *    o = ((t%4)*4 + h%4)*4 + w%4, position 64c + o; vsa_cube_order gives the
+ *    Hilbert order instead.
  *  - Block index list ("LUT", [AMD] "Block-Sparse Encoding" and "Using VSA
  *    with CK Tile"): kv_block_idx int32 [BH, Nc, max_kv_blocks] holds the key
  *    cubes each query cube attends to; valid_block_num int32 [BH, Nc] holds how
@@ -57,7 +65,7 @@ extern "C" {
 typedef enum {
     VSA_OK = 0,
     VSA_ERR_ARG = -1,         /* null pointer, bad enum, non-positive size */
-    VSA_ERR_SHAPE = -2,       /* grid not divisible by the cube, N mismatch */
+    VSA_ERR_SHAPE = -2,       /* N not a multiple of 64 where cube order is taken */
     VSA_ERR_UNSUPPORTED = -3, /* d not in {64,128}, cube shape not (4,4,4) */
     VSA_ERR_CUDA = -4,        /* a CUDA runtime call failed */
     VSA_ERR_TIMEOUT = -5,     /* a kernel's bounded wait expired */
@@ -87,7 +95,7 @@ enum { VSA_CURVE_RASTER = 0, VSA_CURVE_HILBERT = 1 };
  * space-filling curve so that each block of the sequence is a compact
  * spatio-temporal region; the page names the curve (Jenga's) but does not
  * print it.
- *   g       the grid (T, H, W multiples of 4; g.cube_order is ignored).
+ *   g       the grid (g.cube_order is ignored).
  *   curve   VSA_CURVE_RASTER: cube (ct, ch, cw) at position
  *           (ct * H/4 + ch) * W/4 + cw.
  *           VSA_CURVE_HILBERT: cubes in the order in which the 3-D Hilbert
@@ -109,10 +117,10 @@ int vsa_cube_order(vsa_grid_t g, int curve, int32_t* order, void* stream);
  * vsa_permute -- 3D space-filling-curve token reordering, with the cube
  * mean-pool fused.  [AMD] "Two-Stage Architecture" (pre-stage SFC reordering;
  * Stage 1 mean-pools each cube into one vector).
- *   x        bf16 [BH, N, d]: native order (inverse = 0) or cube order (1).
- *   y        bf16 [BH, N, d]: the same tokens in cube order (inverse = 0) or
- *            native order (inverse = 1).  Must not alias x.
- *   pooled   fp32 [BH, Nc, d] or NULL: with inverse = 0, the mean of the 64
+ *   x        bf16 native [BH, N, d] (inverse = 0) or cube order [BH, Np, d] (1).
+ *   y        bf16 cube order [BH, Np, d], padding slots zero (inverse = 0), or
+ *            native [BH, N, d] (inverse = 1).  Must not alias x.
+ *   pooled   fp32 [BH, Nc, d] or NULL: with inverse = 0, the mean of the
  *            tokens of every cube.  Must be NULL when inverse = 1.
  */
 int vsa_permute(const void* x, void* y, float* pooled, int BH, int d, vsa_grid_t g, int inverse, void* stream);

@@ -50,7 +50,10 @@ def test_workspace_bytes(lib):
     assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 0) == 0        # K < 1
     assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, Nc + 1) == 0   # K > Nc
     assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 96, g, 4) == 0         # d
-    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, lib.Grid.of(6, 8, 8), 1) == 0
+    # a side that is not a multiple of 4: partial cubes, sized like the covering grid
+    assert (L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, lib.Grid.of(6, 7, 5), 2)
+            == L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, lib.Grid.of(8, 8, 8), 2) > 0)
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, lib.Grid.of(0, 8, 8), 1) == 0
     assert L.vsa_workspace_bytes(7, 1, 12, 128, g, 4) == 0
 
 
@@ -60,7 +63,7 @@ def test_host_side_argument_errors(lib):
     fake2 = ctypes.c_void_p(0x2000)
     g = lib.Grid.of(4, 8, 8)
     # bad grid / cube / d
-    assert L.vsa_permute(fake, fake2, None, 1, 64, lib.Grid.of(4, 8, 6), 0, None) == lib.VSA_ERR_SHAPE
+    assert L.vsa_permute(fake, fake2, None, 1, 64, lib.Grid.of(4, 0, 8), 0, None) == lib.VSA_ERR_ARG
     assert L.vsa_permute(fake, fake2, None, 1, 64, lib.Grid(4, 8, 8, 2, 4, 4), 0, None) == lib.VSA_ERR_UNSUPPORTED
     assert L.vsa_permute(fake, fake2, None, 1, 80, g, 0, None) == lib.VSA_ERR_UNSUPPORTED
     # null, aliasing, misaligned, pooled with inverse
@@ -68,6 +71,8 @@ def test_host_side_argument_errors(lib):
     assert L.vsa_permute(fake, fake, None, 1, 64, g, 0, None) == lib.VSA_ERR_ARG
     assert L.vsa_permute(ctypes.c_void_p(0x1002), fake2, None, 1, 64, g, 0, None) == lib.VSA_ERR_ARG
     assert L.vsa_permute(fake, fake2, fake, 1, 64, g, 1, None) == lib.VSA_ERR_ARG
+    assert L.vsa_permute(fake, fake2, None, 1, 64, lib.Grid.of(4, 8, 8, 0x1002), 0, None) == lib.VSA_ERR_ARG
+    assert L.vsa_cube_order(g, 5, fake2, None) == lib.VSA_ERR_ARG                # unknown curve
     # Top-K range
     for K in (0, 5):
         assert L.vsa_coarse_topk(fake, fake, fake, 1, 4, 64, K, 0.125, None, None, fake2, None, None,

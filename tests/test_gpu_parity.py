@@ -261,32 +261,37 @@ def _sampled_checks(vsa, oracle_mod, wl, dtype, n_cubes=4, n_rows=48):
     gidx = saved["idx"].view(wl.B, wl.heads, wl.Nc, wl.topk).cpu().numpy()
     scale = wl.d ** -0.5
     pos = oracle_mod.sfc_table(wl.T, wl.H, wl.W)
-    native_of = np.argsort(pos)                          # reordered position -> native token
+    slot_ok, ntok = oracle_mod.cube_slots(wl.T, wl.H, wl.W)   # padding slots of partial cubes
+    native_of = np.full(64 * wl.Nc, -1, np.int64)
+    native_of[pos] = np.arange(wl.N)                     # reordered position -> native token
+    real = np.flatnonzero(slot_ok)
     rng = np.random.default_rng(zlib.crc32(wl.name.encode()))
     cnt1 = np.full((1, wl.Nc), wl.topk, np.int32)
     at = lambda t, h, nat: host(t[0, h, torch.from_numpy(nat).to(t.device)])
     for h in sorted({0, wl.heads - 1}):
         P = lambda a: oracle_mod.permute(a[0, h].reshape(1, wl.N, wl.d), wl.T, wl.H, wl.W)
         qp, kp, vp, gcp, gfp, dop = (P(a) for a in (q, k, v, gc, gf, dout))
-        pq, pk, pv = (oracle_mod.pool(a) for a in (qp, kp, vp))
+        pq, pk, pv = (oracle_mod.pool(a, ntok) for a in (qp, kp, vp))
         scores, oc, _ = oracle_mod.coarse(pq, pk, pv, scale)
         idx1 = gidx[0, h].reshape(1, wl.Nc, wl.topk)
         check_topk_validity(idx1, scores, wl.topk)
         # whole query cubes of the output (the first, the last, two random)
         cubes = np.unique(np.r_[0, wl.Nc - 1, rng.choice(wl.Nc, n_cubes - 2, replace=False)])
         rows = (64 * cubes[:, None] + np.arange(64)).reshape(-1)
-        of_rows, _ = oracle_mod.fine_fwd_rows(qp, kp, vp, idx1, cnt1, scale, rows)
+        rows = rows[slot_ok[rows] == 1]
+        of_rows, _ = oracle_mod.fine_fwd_rows(qp, kp, vp, idx1, cnt1, scale, rows, slot_ok=slot_ok)
         sub = lambda a: a[:, rows]
-        out_ref = oracle_mod.combine(sub(gcp), sub(gfp), oc[:, cubes], of_rows[None])
+        ocr = oc[0, rows // 64]                                          # O_c of each row's cube
+        out_ref = (sub(gcp)[0] * ocr + sub(gfp)[0] * of_rows)[None]
         assert_close(at(out, h, native_of[rows]), out_ref[0], bf16_out=bf, what=f"out head {h}")
-        _, _, dgc_ref, dgf_ref = oracle_mod.combine_bwd(sub(dop), sub(gcp), sub(gfp), oc[:, cubes], of_rows[None])
-        assert_close(at(g["dgc"], h, native_of[rows]), dgc_ref[0], bf16_out=bf, what=f"dgc head {h}")
-        assert_close(at(g["dgf"], h, native_of[rows]), dgf_ref[0], bf16_out=bf, what=f"dgf head {h}")
+        assert_close(at(g["dgc"], h, native_of[rows]), sub(dop)[0] * ocr, bf16_out=bf, what=f"dgc head {h}")
+        assert_close(at(g["dgf"], h, native_of[rows]), sub(dop)[0] * of_rows, bf16_out=bf, what=f"dgf head {h}")
         # dO_f and dO_c of every row (O_f enters only dg_f, not used from this call)
         dof, doc, _, _ = oracle_mod.combine_bwd(dop, gcp, gfp, oc, np.zeros_like(dop))
         dqc, dkc, dvc = oracle_mod.coarse_bwd(pq, pk, pv, doc, scale)
-        qrows = np.unique(np.r_[0, wl.N - 1, rng.choice(wl.N, n_rows - 2, replace=False)])
-        dq_ref = oracle_mod.fine_bwd_query_rows(qp, kp, vp, dof, idx1, cnt1, scale, qrows) + dqc[0, qrows // 64] / 64.0
+        qrows = np.unique(np.r_[real[0], real[-1], rng.choice(real, n_rows - 2, replace=False)])
+        dq_ref = (oracle_mod.fine_bwd_query_rows(qp, kp, vp, dof, idx1, cnt1, scale, qrows, slot_ok=slot_ok)
+                  + dqc[0, qrows // 64] / ntok[qrows // 64, None])
         assert_close(at(g["dq"], h, native_of[qrows]), dq_ref, bf16_out=bf, what=f"dq rows head {h}")
         if h == 0:
             inv_count = np.bincount(idx1.reshape(-1), minlength=wl.Nc)
@@ -294,10 +299,11 @@ def _sampled_checks(vsa, oracle_mod, wl, dtype, n_cubes=4, n_rows=48):
             if (inv_count == 0).any():
                 kcubes.append(int(np.argmax(inv_count == 0)))
             for c in kcubes:
-                dk_c, dv_c = oracle_mod.fine_bwd_key_cube(qp, kp, vp, dof, idx1, cnt1, scale, 0, c)
-                nat = native_of[64 * c:64 * c + 64]
-                assert_close(at(g["dk"], h, nat), dk_c + dkc[0, c] / 64.0, bf16_out=bf, what=f"dk cube {c}")
-                assert_close(at(g["dv"], h, nat), dv_c + dvc[0, c] / 64.0, bf16_out=bf, what=f"dv cube {c}")
+                dk_c, dv_c = oracle_mod.fine_bwd_key_cube(qp, kp, vp, dof, idx1, cnt1, scale, 0, c, slot_ok=slot_ok)
+                ok = slot_ok[64 * c:64 * c + 64] == 1
+                nat = native_of[64 * c:64 * c + 64][ok]
+                assert_close(at(g["dk"], h, nat), (dk_c + dkc[0, c] / ntok[c])[ok], bf16_out=bf, what=f"dk cube {c}")
+                assert_close(at(g["dv"], h, nat), (dv_c + dvc[0, c] / ntok[c])[ok], bf16_out=bf, what=f"dv cube {c}")
     dk_sum = g["dk"].float().sum(dim=2)
     dk_max = g["dk"].float().abs().amax()
     assert float(dk_sum.abs().amax()) < 5e-2 * max(1.0, float(dk_max))
@@ -400,12 +406,12 @@ def test_lut_add_neighbors_and_fine_fwd(vsa, oracle_mod, name, radius):
 
 
 # ---------------------------------------------------------------- Hilbert cube order
-@pytest.mark.parametrize("grid", [(4, 8, 8), (8, 16, 32), (16, 32, 64), (32, 48, 80), (12, 20, 28)])
+@pytest.mark.parametrize("grid", [(4, 8, 8), (8, 16, 32), (16, 32, 64), (32, 48, 80), (12, 20, 28), (21, 30, 52)])
 def test_cube_order_table(vsa, oracle_mod, grid):
     """vsa_cube_order (point -> curve index on the GPU) against the oracle's
     ranks (curve index -> point), both curves, bit for bit."""
     T, H, W = grid
-    Tc, Hc, Wc = T // 4, H // 4, W // 4
+    Tc, Hc, Wc = oracle_mod.cube_grid(T, H, W)
     Nc = Tc * Hc * Wc
     for curve in ("raster", "hilbert"):
         tab = vsa.cube_order(T, H, W, curve).cpu().numpy()
@@ -459,3 +465,46 @@ def test_lut_add_neighbors_hilbert(vsa, oracle_mod):
     assert not ovf
     np.testing.assert_array_equal(gcnt.cpu().numpy(), rcnt)
     np.testing.assert_array_equal(got.cpu().numpy(), ref)
+
+
+# ---------------------------------------------------------------- grids not divisible by 4
+@pytest.mark.parametrize("grid,d,curve", [((5, 6, 10), 64, "raster"), ((9, 14, 22), 128, "raster"),
+                                          ((9, 14, 22), 128, "hilbert"), ((21, 30, 52), 128, "raster")])
+def test_permute_pool_padded(vsa, oracle_mod, grid, d, curve):
+    """Partial boundary cubes: padding slots are zero in cube order, dropped on
+    the way back, and left out of the cube means (bit-exact data movement)."""
+    T, H, W = grid
+    order = None if curve == "raster" else vsa.cube_order(T, H, W, curve)
+    x = synth.make_random((2, T * H * W, d), seed=T + H + W)
+    y, pooled = vsa.permute(dev(x), T, H, W, pool=True, cube_order=order)
+    ref = oracle_mod.permute(x, T, H, W, curve=curve)
+    assert np.array_equal(host(y), ref)
+    back = vsa.permute(y, T, H, W, inverse=True, cube_order=order)
+    assert np.array_equal(host(back), x.astype(np.float64))
+    _, ntok = oracle_mod.cube_slots(T, H, W, curve)
+    np.testing.assert_allclose(host(pooled), oracle_mod.pool(ref, ntok), rtol=1e-5, atol=1e-6)
+    status_ok(vsa)
+
+
+@pytest.mark.parametrize("name,curve", [("odd", "raster"), ("odd", "hilbert"), ("odd_small", "raster"),
+                                        ("odd_small", "hilbert")])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_forward_backward_padded(vsa, oracle_mod, name, curve, dtype):
+    wl = synth.WORKLOADS[name]
+    order = None if curve == "raster" else vsa.cube_order(wl.T, wl.H, wl.W, curve)
+    q, k, v, gc, gf, dout, out, g, saved = _e2e(vsa, oracle_mod, wl, True, dtype, dtype, cube_order=order)
+    gidx = saved["idx"].cpu().numpy().reshape(wl.B, wl.heads, wl.Nc, wl.topk)
+    ref0 = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=gc, gf=gf, curve=curve)
+    check_topk_validity(gidx, ref0["scores"], wl.topk)
+    ref = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=gc, gf=gf, lut=gidx, curve=curve)
+    bf = dtype == torch.bfloat16
+    assert_close(host(out), ref["out"], bf16_out=bf, what="out")
+    rg = oracle_mod.backward(q, k, v, dout, gidx, wl.T, wl.H, wl.W, gc=gc, gf=gf, curve=curve)
+    for n in ("dq", "dk", "dv", "dgc", "dgf"):
+        assert_close(host(g[n]), rg[n], bf16_out=bf, what=n)
+
+
+def test_full_size_wan_latent(vsa, oracle_mod):
+    """The Wan2.1 latent grid itself, 21 x 30 x 52 = 32760 tokens (624 cubes,
+    partial along all three axes), 12 heads, K = 187, sampled as above."""
+    _sampled_checks(vsa, oracle_mod, synth.WORKLOADS["wan1.3b_latent"], torch.float32)
