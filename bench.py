@@ -46,7 +46,9 @@ WORKLOAD = "wan1.3b"
 
 
 def step_flops(wl: synth.Workload) -> dict:
-    keys = 64 * wl.topk
+    # keys per query: K cubes of N / Nc tokens on average (64 unless the grid
+    # has partial boundary cubes)
+    keys = wl.topk * wl.N / wl.Nc
     fine_fwd = 4.0 * wl.N * keys * wl.d * wl.BH
     fine_bwd = 10.0 * wl.N * keys * wl.d * wl.BH
     coarse = 14.0 * wl.Nc * wl.Nc * wl.d * wl.BH
@@ -274,12 +276,12 @@ def run_ours(args, rank: int, world: int):
     # Work each fine kernel does per launch (products of 2*N*64K*d FLOP each):
     # forward S and PV (2); backward dK/dV kernel S^T, dP^T, dV, dK (4); dQ
     # kernel S, dP, dQ (3).  The effective metric counts 2 + 5.
-    unit = 2.0 * wl.N * 64 * wl.topk * wl.d * wl.BH
+    unit = 2.0 * wl.N * (wl.topk * wl.N / wl.Nc) * wl.d * wl.BH
     kflops = {"fine_fwd": 2 * unit, "fine_bwd_kv": 4 * unit, "fine_bwd_dq": 3 * unit}
     dominant = max(kflops, key=lambda n: per_kernel[n])
     traffic = None  # DRAM bytes per launch from the committed ncu capture (profiles/traffic.txt)
     tpath = os.path.join(ROOT, "profiles", "traffic.txt")
-    if os.path.exists(tpath):
+    if os.path.exists(tpath) and args.config == WORKLOAD and args.curve == "raster":  # the captured case only
         with open(tpath) as f:
             for ln in f:
                 parts = ln.split()
