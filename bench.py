@@ -201,10 +201,10 @@ def run_ours(args, rank: int, world: int):
                       dtype=torch.uint8, device=dev)
     order = None if args.curve == "raster" else vsa.cube_order(wl.T, wl.H, wl.W, args.curve, device=dev)
 
-    def step(qd, kd, vd, gcd, gfd, dod):
-        _, st = vsa.forward(qd, kd, vd, wl.T, wl.H, wl.W, wl.topk, g_coarse=gcd, g_fine=gfd, out=out, ws=fws,
-                            cube_order=order)
-        vsa.backward(st, dod, g_coarse=gcd, g_fine=gfd, grads=grads, ws=bws)
+    def step(qd, kd, vd, gcd, gfd, dod, res_out=None, res_grads=None):
+        _, st = vsa.forward(qd, kd, vd, wl.T, wl.H, wl.W, wl.topk, g_coarse=gcd, g_fine=gfd,
+                            out=out if res_out is None else res_out, ws=fws, cube_order=order)
+        vsa.backward(st, dod, g_coarse=gcd, g_fine=gfd, grads=grads if res_grads is None else res_grads, ws=bws)
 
     def barrier():
         if world > 1:
@@ -239,23 +239,48 @@ def run_ours(args, rank: int, world: int):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  Every step
+    # copies its six inputs from pinned host memory and its six results back;
+    # the copies run on two copy streams, double-buffered, so that step i+1's
+    # uploads and step i-1's downloads overlap step i's kernels.
     e2e = None
     if not args.no_e2e:
         host_out = [torch.empty(out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(6)]
-        dev_in = [dq_, dk_, dv_, dgc_, dgf_, ddo]
-        results = [out, grads["dq"], grads["dk"], grads["dv"], grads["dgc"], grads["dgf"]]
+        dev_in = [[dq_, dk_, dv_, dgc_, dgf_, ddo], [torch.empty_like(dq_) for _ in range(6)]]
+        res = [dict(out=out, **grads),
+               dict(out=torch.empty_like(out), **{n: torch.empty_like(t) for n, t in grads.items()})]
+        order_res = ["out", "dq", "dk", "dv", "dgc", "dgf"]
         h2d = sum(h.numel() * h.element_size() for h in host)
-        d2h = sum(r.numel() * r.element_size() for r in results)
+        d2h = sum(res[0][n].numel() * res[0][n].element_size() for n in order_res)
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event()
+        in_ready, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
         barrier()
         torch.cuda.synchronize()
         e0.record(stream)
-        for _ in range(args.steps):
-            for d, h in zip(dev_in, host):
-                d.copy_(h, non_blocking=True)
-            step(*dev_in)
-            for h, r in zip(host_out, results):
-                h.copy_(r, non_blocking=True)
+        up.wait_event(e0)
+        down.wait_event(e0)
+        for i in range(args.steps):
+            b = i & 1
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(comp_done[b])          # step i-2 has finished reading these inputs
+                for d, h in zip(dev_in[b], host):
+                    d.copy_(h, non_blocking=True)
+                in_ready[b].record(up)
+            stream.wait_event(in_ready[b])
+            if i >= 2:
+                stream.wait_event(out_done[b])           # step i-2's results have been read out
+            g = res[b]
+            step(*dev_in[b], res_out=g["out"], res_grads={n: g[n] for n in order_res[1:]})
+            comp_done[b].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(comp_done[b])
+                for h, n in zip(host_out, order_res):
+                    h.copy_(g[n], non_blocking=True)
+                out_done[b].record(down)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
