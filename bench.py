@@ -45,6 +45,22 @@ KERNELS_PER_STEP = 19
 WORKLOAD = "wan1.3b"
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over all ranks (every rank receives it); x itself at world 1."""
+    if world == 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_step: float, steps: int, ms: float) -> float:
+    """Replicas: every rank runs the whole workload, so the job does world x the
+    work of one rank in the slowest rank's time."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 def step_flops(wl: synth.Workload) -> dict:
     # keys per query: K cubes of N / Nc tokens on average (64 unless the grid
     # has partial boundary cubes)
@@ -234,10 +250,7 @@ def run_ours(args, rank: int, world: int):
     kern = vsa.timing_read()
     status = vsa.device_status()
     assert status == 0, f"device error flag {status}"
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # ---- end to end through the public API with host buffers.  Every step
     # copies its six inputs from pinned host memory and its six results back;
@@ -285,17 +298,14 @@ def run_ours(args, rank: int, world: int):
         torch.cuda.synchronize()
         barrier()
         ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": round(world * fl["total"] * args.steps / (ems * 1e-3) / 1e12, 2), "unit": UNIT,
+        ems = max_over_ranks(ems, world, dev)
+        e2e = {"value": round(whole_job_tflops(world, fl["total"], args.steps, ems), 2), "unit": UNIT,
                "ms_per_step": round(ems / args.steps, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     if rank != 0:
         return
     peaks = load_peaks()
-    value = world * fl["total"] * args.steps / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, fl["total"], args.steps, ms)
     per_kernel = {n: round(t / max(c, 1), 4) for n, (t, c) in kern.items()}
     launches = {n: c for n, (t, c) in kern.items()}
     # Work each fine kernel does per launch (products of 2*N*64K*d FLOP each):
