@@ -42,15 +42,27 @@ __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc
   const int j = threadIdx.x % kChunks;     // channel chunk, fixed per thread
   const int o0 = threadIdx.x / kChunks;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  // All of this thread's loads are issued before any store, so that each
+  // thread keeps kPasses 16-byte reads in flight.
+  uint4 vin[kPasses];
+  int64_t nat_of[kPasses];
 #pragma unroll
   for (int p = 0; p < kPasses; ++p) {
     const int o = o0 + p * kTokPerPass;
     const int64_t nat = native_token(rcube, o, g);
     const int64_t cub = static_cast<int64_t>(cube) * kCube + o;
-    if (nat < 0 && inverse) continue;  // padding slot: nothing to write back
+    nat_of[p] = nat;
     const int64_t s_tok = inverse ? cub : nat;
+    vin[p] = nat < 0 ? make_uint4(0, 0, 0, 0) : __ldg(reinterpret_cast<const uint4*>(src + s_tok * D + j * 8));
+  }
+#pragma unroll
+  for (int p = 0; p < kPasses; ++p) {
+    const int o = o0 + p * kTokPerPass;
+    const int64_t nat = nat_of[p];
+    const int64_t cub = static_cast<int64_t>(cube) * kCube + o;
+    if (nat < 0 && inverse) continue;  // padding slot: nothing to write back
     const int64_t d_tok = inverse ? nat : cub;
-    const uint4 v = nat < 0 ? make_uint4(0, 0, 0, 0) : *reinterpret_cast<const uint4*>(src + s_tok * D + j * 8);
+    const uint4 v = vin[p];
     if (F16OUT) {
       const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
                           bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
