@@ -28,8 +28,10 @@
 // union of their index lists two key cubes per step, like the forward:
 //   S = Q K^T, dP = dO V^T            (A, B in shared memory)
 //   dQ += dS K                        (A = dS in TMEM)
-// S is double-buffered in TMEM so P(j+1) = exp(S - LSE) is computed while
-// dQ(j) and dP(j+1) run; K, V go through a 2-stage ring.
+// S and dP are released as soon as the compute warps have read them, so
+// S(j+1) and dP(j+1) run while dS(j) is computed; dS is double-buffered.  K
+// is read by S(j) and again by dQ(j), a step later, so it has a 3-stage ring;
+// V only by dP(j), so one stage suffices: V(j+1) lands while S(j+1) runs.
 //
 // Operands are fp16 (exact for the bf16 inputs within +-65504), accumulation
 // fp32.  The inverse lists come from a bit matrix inv[bh][key cube][query
@@ -424,9 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
 template <int D>
 struct DqLayout {
   static constexpr int kTile = 128 * D * 2;
-  static constexpr int kQ = 0, kDO = kTile, kK = 2 * kTile, kV = 4 * kTile;  // K, V: 2 stages each
+  // K: 3 stages (read by S(j) and, much later, by dQ(j)); V: 1 stage (read
+  // by dP(j) only, so V(j+1) can land while S(j+1) runs).
+  static constexpr int kQ = 0, kDO = kTile, kK = 2 * kTile, kV = 5 * kTile;
   static constexpr int kEnd = 6 * kTile;
 };
+constexpr int kDqKStages = 3;
 // TMEM: S 0 and dP 128 (128 fp32 columns each, released once the compute
 // warps have read them); dS buffer b at 256 + 64 b (64 columns of fp16
 // pairs); dQ 384.
@@ -442,12 +447,14 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
   uint32_t* bitA = ulist + 2 * p.kmax + 2;
   uint32_t* bitB = bitA + nwords;
 
-  // bar_k / bar_v [s]: K / V stage s filled; bar_kvfree[s]: dQ of the step
-  // using stage s done (K read); bar_vfree[s]: dP of that step done (V read).  s_done: S(j) and dP(j) done; s_free: the compute
-  // warps have read them (all compute threads); bar_ds[b]: dS(j) written into
-  // buffer b = j % 2; ds_free[b]: the dQ that read buffer b completed.  Every
-  // parity wait targets a barrier in the awaited phase or the one after it.
-  __shared__ uint64_t bar_qdo, bar_k[2], bar_v[2], bar_kvfree[2], bar_vfree[2], s_done, s_free, bar_ds[2], ds_free[2];
+  // bar_k[s]: K stage s filled; bar_kvfree[s]: dQ of the step using stage s
+  // done (K read).  bar_v: the V stage filled; bar_vfree: dP of its step done
+  // (V read).  s_done: S(j) and dP(j) done; s_free: the compute warps have
+  // read them (all compute threads); bar_ds[b]: dS(j) written into buffer
+  // b = j % 2; ds_free[b]: the dQ that read buffer b completed.  Every parity
+  // wait targets a barrier in the awaited phase or the one after it.
+  __shared__ uint64_t bar_qdo, bar_k[kDqKStages], bar_kvfree[kDqKStages], bar_v, bar_vfree, s_done, s_free, bar_ds[2],
+      ds_free[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int n_union, n_cnt[2];
 
@@ -461,11 +468,13 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
 
   if (tid == 0) {
     mbar_init(&bar_qdo, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kDqKStages; ++i) {
       mbar_init(&bar_k[i], 1);
-      mbar_init(&bar_v[i], 1);
       mbar_init(&bar_kvfree[i], 1);
-      mbar_init(&bar_vfree[i], 1);
+    }
+    mbar_init(&bar_v, 1);
+    mbar_init(&bar_vfree, 1);
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_ds[i], kCompute);
       mbar_init(&ds_free[i], 1);
     }
@@ -521,24 +530,24 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
       const int cq1 = has_b ? qb : qa;
       load_cube_pair<D>(sm + L::kQ, &p.tq, &bar_qdo, row_base, qa, cq1);
       load_cube_pair<D>(sm + L::kDO, &p.tdo, &bar_qdo, row_base, qa, cq1);
-      // V(j) goes in once dP(j - 2) is done, K(j) once dQ(j - 2) is: V is
-      // released a step earlier, so it is requested first.
-      for (int j = 0; j < steps; ++j) {
-        const int s = j & 1;
-        const int c0 = kcube(j, 0), c1 = kcube(j, 1);
-        if (j >= 2 && !mbar_wait(&bar_vfree[s], ((j >> 1) - 1) & 1)) {
-          flag_error(p.err, kErrTimeout);
-          break;
-        }
-        mbar_expect_tx(&bar_v[s], L::kTile);
-        load_cube_pair<D>(sm + L::kV + s * L::kTile, &p.tv, &bar_v[s], row_base, c0, c1);
-        if (j >= 2 && !mbar_wait(&bar_kvfree[s], ((j >> 1) - 1) & 1)) {
-          flag_error(p.err, kErrTimeout);
-          break;
-        }
+      // K(j) goes into stage j % 3 once dQ(j - 3) is done; V(j) into the V
+      // stage once dP(j - 1) is.  K runs one step ahead: K(j + 1), then V(j).
+      auto load_k = [&](int j) -> bool {
+        const int s = j % kDqKStages;
+        if (j >= kDqKStages && !mbar_wait(&bar_kvfree[s], ((j / kDqKStages) - 1) & 1)) return false;
         mbar_expect_tx(&bar_k[s], L::kTile);
-        load_cube_pair<D>(sm + L::kK + s * L::kTile, &p.tk, &bar_k[s], row_base, c0, c1);
+        load_cube_pair<D>(sm + L::kK + s * L::kTile, &p.tk, &bar_k[s], row_base, kcube(j, 0), kcube(j, 1));
+        return true;
+      };
+      bool ok = load_k(0);
+      for (int j = 0; ok && j < steps; ++j) {
+        if (j + 1 < steps) ok = load_k(j + 1);
+        if (ok && j >= 1 && !mbar_wait(&bar_vfree, (j - 1) & 1)) ok = false;
+        if (!ok) break;
+        mbar_expect_tx(&bar_v, L::kTile);
+        load_cube_pair<D>(sm + L::kV, &p.tv, &bar_v, row_base, kcube(j, 0), kcube(j, 1));
       }
+      if (!ok) flag_error(p.err, kErrTimeout);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: S(j+1) and dP(j+1) once the compute warps
@@ -559,36 +568,49 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
       const uint64_t kmn0 = sdesc_sw128(smem_u32(sm + L::kK), 16384, 1024);   // K stages, MN-major
       constexpr uint32_t kTileU = L::kTile >> 4;
       bool ok = mbar_spin(&bar_qdo, 0);
-      int ns = 0, ng = 0;  // next S / dP and next dQ to issue
+      int ns = 0, npd = 0, ng = 0;   // next S, next dP, next dQ to issue
+      uint32_t ks = 0, kph = 0;      // K stage of S(ns) and its fill parity
+      uint32_t kg = 0;               // K stage of dQ(ng)
       uint32_t idle = 0;
       while (ok && ng < steps) {
         bool progressed = false;
-        if (ns < steps && (ns == 0 || mbar_test(&s_free, (ns - 1) & 1)) &&
-            mbar_test(&bar_k[ns & 1], (ns >> 1) & 1) && mbar_test(&bar_v[ns & 1], (ns >> 1) & 1)) {
+        // S(ns) once the compute warps have read S / dP (ns - 1) and K(ns) landed.
+        if (ns < steps && ns == npd && (ns == 0 || mbar_test(&s_free, (ns - 1) & 1)) && mbar_test(&bar_k[ks], kph)) {
           tc_fence_after();
-          const uint64_t kd = kkm0 + (ns & 1) * kTileU, vd = vkm0 + (ns & 1) * kTileU;
+          const uint64_t kd = kkm0 + ks * kTileU;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + kDqS, qdesc[kk], kd + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + kDqDP, odesc[kk], vd + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
-          mma_commit(&s_done);
-          mma_commit(&bar_vfree[ns & 1]);
           ++ns;
+          if (++ks == static_cast<uint32_t>(kDqKStages)) {
+            ks = 0;
+            kph ^= 1u;
+          }
           progressed = true;
         }
-        if (ng < ns && mbar_test(&bar_ds[ng & 1], (ng >> 1) & 1)) {
+        // dP(npd) after its S, once V(npd) landed; then S and dP are done together.
+        if (npd < ns && mbar_test(&bar_v, npd & 1)) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + kDqDP, odesc[kk], vkm0 + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
+          mma_commit(&s_done);
+          mma_commit(&bar_vfree);
+          ++npd;
+          progressed = true;
+        }
+        if (ng < npd && mbar_test(&bar_ds[ng & 1], (ng >> 1) & 1)) {
           tc_fence_after();
           const uint32_t dsb = tmem + kDqDS + 64 * (ng & 1);
-          const uint64_t kd = kmn0 + (ng & 1) * kTileU;
+          const uint64_t kd = kmn0 + kg * kTileU;
           // A = dS (K = 128 keys in 8 steps of 16), B = the K stage (MN-major).
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ts(tmem + kDqDQ, dsb + kk * 8, kd + ((kk * 2048) >> 4), idesc_q, (ng > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bar_kvfree[ng & 1]);
+          mma_commit(&bar_kvfree[kg]);
           mma_commit(&ds_free[ng & 1]);
           ++ng;
+          if (++kg == static_cast<uint32_t>(kDqKStages)) kg = 0;
           progressed = true;
         }
         idle = progressed ? 0u : idle + 1u;
