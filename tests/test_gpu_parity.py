@@ -508,3 +508,45 @@ def test_full_size_wan_latent(vsa, oracle_mod):
     """The Wan2.1 latent grid itself, 21 x 30 x 52 = 32760 tokens (624 cubes,
     partial along all three axes), 12 heads, K = 187, sampled as above."""
     _sampled_checks(vsa, oracle_mod, synth.WORKLOADS["wan1.3b_latent"], torch.float32)
+
+
+# ---------------------------------------------------------------- CUDA graphs
+def test_forward_backward_capture_in_a_cuda_graph(vsa, oracle_mod):
+    """The forward and backward enqueue only stream work (no host sync, no
+    allocation), so a whole training step can be captured in a CUDA graph;
+    replays give the eager results bit for bit."""
+    wl = synth.WORKLOADS["small"]
+    q, k, v = synth.make_qkv(wl)
+    gc, gf = synth.make_gates(wl)
+    dout = synth.make_dout(wl)
+    ins = [dev(a) for a in (q, k, v, gc, gf, dout)]
+    out = torch.empty_like(ins[0])
+    grads = {n: torch.empty_like(ins[0]) for n in ("dq", "dk", "dv", "dgc", "dgf")}
+    fws = torch.empty(vsa.workspace_bytes(0, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk), dtype=torch.uint8,
+                      device="cuda")
+    bws = torch.empty(vsa.workspace_bytes(1, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk), dtype=torch.uint8,
+                      device="cuda")
+
+    def step():
+        _, st = vsa.forward(*ins[:3], wl.T, wl.H, wl.W, wl.topk, g_coarse=ins[3], g_fine=ins[4], out=out, ws=fws)
+        vsa.backward(st, ins[5], g_coarse=ins[3], g_fine=ins[4], grads=grads, ws=bws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()                                     # eager, on the capture stream's device state
+    torch.cuda.current_stream().wait_stream(side)
+    status_ok(vsa)
+    eager = [out.clone()] + [grads[n].clone() for n in ("dq", "dk", "dv", "dgc", "dgf")]
+    for t in [out] + list(grads.values()):
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    status_ok(vsa)
+    replay = [out] + [grads[n] for n in ("dq", "dk", "dv", "dgc", "dgf")]
+    for a, b in zip(eager, replay):
+        assert torch.equal(a, b)
