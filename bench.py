@@ -252,6 +252,37 @@ def run_ours(args, rank: int, world: int):
     assert status == 0, f"device error flag {status}"
     ms = max_over_ranks(ms, world, dev)
 
+    # ---- forward alone: vsa_forward (which also writes the state the
+    # backward needs) and vsa_forward_inference (the fine stage reads the
+    # native layout through 5-D TMA boxes; no reordered copies).  Reported
+    # beside the headline; not part of it.
+    fwd_only = None
+    if world == 1:
+        iws = torch.empty(vsa.workspace_bytes(3, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk), dtype=torch.uint8,
+                          device=dev)
+        runs = {
+            "forward": lambda: vsa.forward(dq_, dk_, dv_, wl.T, wl.H, wl.W, wl.topk, g_coarse=dgc_, g_fine=dgf_,
+                                           out=out, ws=fws, cube_order=order),
+            "forward_inference": lambda: vsa.forward_inference(dq_, dk_, dv_, wl.T, wl.H, wl.W, wl.topk,
+                                                               g_coarse=dgc_, g_fine=dgf_, out=out, ws=iws,
+                                                               cube_order=order),
+        }
+        fwd_only = {}
+        for name, fn in runs.items():
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            fms = e0.elapsed_time(e1) / args.steps
+            fwd_only[name] = {"ms": round(fms, 4),
+                              "tflops": round((fl["fine_fwd"] + fl["coarse"] * 4 / 14) / (fms * 1e-3) / 1e12, 2)}
+        assert vsa.device_status() == 0, "device error flag set in the forward-only runs"
+        del iws
+
     # ---- end to end through the public API with host buffers.  Every step
     # copies its six inputs from pinned host memory and its six results back;
     # the copies run on two copy streams, double-buffered, so that step i+1's
@@ -349,6 +380,7 @@ def run_ours(args, rank: int, world: int):
         "kernel_ms_per_step": per_kernel,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "kernel_launches_timed": launches,
+        "forward_only": fwd_only,
         "clocks": clocks.summary(),
         "e2e": e2e,
     }

@@ -17,7 +17,7 @@ import torch
 from . import _lib
 from ._lib import Grid, VSAError, VSA_DTYPE_BF16, VSA_DTYPE_F32
 
-__all__ = ["num_cubes", "cube_order", "permute", "coarse_topk", "fine_fwd", "fine_bwd", "forward", "backward",
+__all__ = ["num_cubes", "cube_order", "permute", "coarse_topk", "fine_fwd", "fine_bwd", "forward", "forward_inference", "backward",
            "workspace_bytes", "device_status", "timing_enable", "timing_read", "VSAError",
            "ForwardState", "Grid"]
 
@@ -217,6 +217,25 @@ def forward(q, k, v, T: int, H: int, W: int, topk: int, g_coarse=None, g_fine=No
         _ptr(q), _ptr(k), _ptr(v), _ptr(g_coarse), _ptr(g_fine), B, heads, d, Grid.of(T, H, W, _ptr(cube_order)), topk,
         float(scale), _ptr(out), _DT[out.dtype], _ptr(ws), nbytes, _stream()))
     return out, ForwardState(ws, B, heads, d, T, H, W, topk, scale, cube_order)
+
+
+def forward_inference(q, k, v, T: int, H: int, W: int, topk: int, g_coarse=None, g_fine=None,
+                      scale: Optional[float] = None, out_dtype=torch.bfloat16, out=None, ws=None, cube_order=None):
+    """vsa_forward_inference: the forward output without saved state; the fine
+    stage reads Q, K, V in their native layout (no reordered copies)."""
+    B, heads, N, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    nbytes = workspace_bytes(_lib.VSA_OP_FORWARD_INFERENCE, B, heads, d, T, H, W, topk)
+    if nbytes == 0:
+        raise VSAError("vsa_workspace_bytes", _lib.VSA_ERR_ARG)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    _lib.check("vsa_forward_inference", _lib.load().vsa_forward_inference(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g_coarse), _ptr(g_fine), B, heads, d, Grid.of(T, H, W, _ptr(cube_order)),
+        topk, float(scale), _ptr(out), _DT[out.dtype], _ptr(ws), nbytes, _stream()))
+    return out
 
 
 def backward(state: ForwardState, dout, g_coarse=None, g_fine=None, grad_dtype=torch.float32,

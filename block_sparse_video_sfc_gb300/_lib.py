@@ -27,6 +27,7 @@ VSA_DTYPE_F32 = 1
 VSA_OP_FORWARD = 0
 VSA_OP_BACKWARD = 1
 VSA_OP_FINE_BWD = 2
+VSA_OP_FORWARD_INFERENCE = 3
 VSA_CURVE_RASTER = 0
 VSA_CURVE_HILBERT = 1
 
@@ -63,6 +64,7 @@ SIGNATURES = {
     "vsa_fine_bwd": ([P, P, P, P, I, P, P, P, P, I, I, I, I, F, P, P, P, P, SZ, P], I),
     "vsa_fine_bwd_noalloc": ([P, P, P, P, I, P, P, P, P, I, I, I, I, F, P, P, P, P], I),
     "vsa_forward": ([P, P, P, P, P, I, I, I, Grid, I, F, P, I, P, SZ, P], I),
+    "vsa_forward_inference": ([P, P, P, P, P, I, I, I, Grid, I, F, P, I, P, SZ, P], I),
     "vsa_backward": ([P, P, P, P, I, I, I, Grid, I, F, P, P, P, P, P, I, P, SZ, P], I),
     "vsa_workspace_bytes": ([I, I, I, I, Grid, I], SZ),
     "vsa_forward_saved": ([P, I, I, I, Grid, I, ctypes.POINTER(Saved)], I),

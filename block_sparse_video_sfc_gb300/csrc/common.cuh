@@ -112,6 +112,11 @@ int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH
 int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt,
                     int kmax, int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, int f16_in,
                     const int32_t* pairs, const uint64_t* kmask, cudaStream_t s);
+// The fine forward reading Q, K, V straight from the native [BH, T, H, W, d]
+// bf16 layout (5-D TMA boxes, one per cube); O_f and lse come out in cube order.
+int launch_fine_fwd_native(const void* q, const void* k, const void* v, int T, int H, int W, const int32_t* order,
+                           const int32_t* idx, const int32_t* cnt, int kmax, int BH, int d, float scale, void* of,
+                           int of_dtype, float* lse, const int32_t* pairs, const uint64_t* kmask, cudaStream_t s);
 // kmask[c] (c = cube position): bit o set when slot o holds a grid token.
 int launch_slot_masks(int T, int H, int W, const int32_t* order, uint64_t* kmask, cudaStream_t s);
 size_t pair_plan_smem(int Nc);

@@ -56,6 +56,12 @@ struct FwdParams {
   const int32_t* cnt;
   const int32_t* pairs;  // [BH][npairs][2] tile -> query cubes (second -1: none), or null
   const uint64_t* kmask;  // [Nc]: bit o set when slot o of the cube holds a token; null: every slot does
+  // Native layout (the NATIVE kernels): Q, K, V are the [BH, T, H, W, d]
+  // tensors; tk / tv are 5-D maps whose {64, 4, 4, 4, 1} box is one (4, 4, 4)
+  // cube (zeros outside the grid), and Q rows are addressed through the grid.
+  CubeGrid cgrid;
+  const int32_t* order;  // cube position -> raster cube (null: raster order)
+  int64_t Nn;            // T * H * W
   int kmax, N, Nc, npairs;
   int nk, nv;        // K and V ring depths (1..kMaxStages)
   float scale_log2;  // scale * log2(e)
@@ -97,9 +103,11 @@ __device__ __forceinline__ float max64(const uint32_t* v) {
   return fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
 }
 
-// 64 weights P = exp2(S * sl2 - m) of one key cube: packed fp16 pairs into
-// pk[32], and their rounded values (what the PV product multiplies with)
-// added to the two row-sum partials.  S * sl2 - m runs as a packed fp32 pair.
+// 64 weights P = exp2(S * sl2 - m) of one key cube: packed fp16 (F16) or
+// bf16 pairs into pk[32], and their rounded values (what the PV product
+// multiplies with) added to the two row-sum partials.  S * sl2 - m runs as a
+// packed fp32 pair.
+template <bool F16>
 __device__ __forceinline__ void softmax64(const uint32_t* sv, uint64_t sl2x2, uint64_t negmx2, uint32_t* pk, float& acc0,
                                           float& acc1) {
 #pragma unroll
@@ -111,12 +119,18 @@ __device__ __forceinline__ void softmax64(const uint32_t* sv, uint64_t sl2x2, ui
     asm("mov.b64 {%0, %1}, %2;" : "=f"(t0), "=f"(t1) : "l"(t));
     const float a = fast_exp2(t0), b = fast_exp2(t1);
     uint32_t h;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(b), "f"(a));  // a -> low half
+    if (F16) {
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(b), "f"(a));  // a -> low half
+      asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+          "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+          : "+f"(acc0), "+f"(acc1)
+          : "r"(h));
+    } else {
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(b), "f"(a));
+      acc0 += __uint_as_float(h << 16);  // a bf16 is the top half of its fp32
+      acc1 += __uint_as_float(h & 0xFFFF0000u);
+    }
     pk[c >> 1] = h;
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
-        : "+f"(acc0), "+f"(acc1)
-        : "r"(h));
   }
 }
 
@@ -128,9 +142,14 @@ __device__ __forceinline__ uint64_t splat2(float v) {
 
 // F16IN: Q, K, V arrive as fp16; otherwise as bf16, and the softmax warps
 // convert each V tile to fp16 in shared memory (exact within +-65504) so that
-// P V always runs on fp16 operands (P rounded to 2^-12, not bf16's 2^-9).
-// Accumulation is fp32 either way.
-template <int D, bool F16IN>
+// P V always runs on fp16 operands (P rounded to 2^-12, not bf16's 2^-9: with
+// bf16 weights the output is too coarse for the D = dO . O_f of a following
+// backward).  Accumulation is fp32 either way.
+// NATIVE (bf16 only): Q, K, V in their native layout, K / V through 5-D boxes,
+// and P V in bf16 (P rounded to 2^-9): no V conversion on the softmax warps'
+// critical path.  The inference forward has no backward to feed, and its
+// output stays well within the forward tolerance.
+template <int D, bool F16IN, bool NATIVE>
 __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -307,9 +326,22 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
         const int c1 = (2 * j + 1 < U) ? (uent(2 * j + 1) & 0x3FFFFFFF) : c0;
         uint8_t* dst = ring + st * L::kTile;
         mbar_expect_tx(&full[st], L::kTile);
-        for (int b = 0; b < D / 64; ++b) {
-          tma_load_2d(dst + b * 16384, map, &full[st], 64 * b, static_cast<int>(row_base + 64 * c0));
-          tma_load_2d(dst + b * 16384 + 8192, map, &full[st], 64 * b, static_cast<int>(row_base + 64 * c1));
+        if (NATIVE) {
+          // One 5-D box per cube and 64 channels: rows come out in (t%4, h%4,
+          // w%4) order, which is the cube order inside a cube.
+          const int r0 = raster_cube(p.order, c0), r1 = raster_cube(p.order, c1);
+          const int Wc = p.cgrid.Wc, HWc = p.cgrid.Hc * p.cgrid.Wc;
+          for (int b = 0; b < D / 64; ++b) {
+            tma_load_5d(dst + b * 16384, map, &full[st], 64 * b, 4 * (r0 % Wc), 4 * ((r0 / Wc) % p.cgrid.Hc),
+                        4 * (r0 / HWc), static_cast<int>(bh));
+            tma_load_5d(dst + b * 16384 + 8192, map, &full[st], 64 * b, 4 * (r1 % Wc), 4 * ((r1 / Wc) % p.cgrid.Hc),
+                        4 * (r1 / HWc), static_cast<int>(bh));
+          }
+        } else {
+          for (int b = 0; b < D / 64; ++b) {
+            tma_load_2d(dst + b * 16384, map, &full[st], 64 * b, static_cast<int>(row_base + 64 * c0));
+            tma_load_2d(dst + b * 16384 + 8192, map, &full[st], 64 * b, static_cast<int>(row_base + 64 * c1));
+          }
         }
         return true;
       };
@@ -327,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
     // Q as well) from shared memory while the TMA writes the next tiles.
     if (lane == 0 && steps > 0) {
       constexpr uint32_t idesc_s = idesc_f32acc(128, 128, 0, 0, F16IN);
-      constexpr uint32_t idesc_pv = idesc_f32acc(128, D, 0, 1, 1);
+      constexpr uint32_t idesc_pv = idesc_f32acc(128, D, 0, 1, NATIVE ? 0 : 1);
       bool ok = mbar_wait(&bar_qt, 0);
       // The issuer shares its SM sub-partition with two busy softmax warps, so
       // it is kept lean: ring slots and parities are stepped, not divided,
@@ -411,8 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
     {
       // Q rows into TMEM (lane = row, column c = elements 2c and 2c + 1):
       // warp (q, h) writes elements [h D/2, (h + 1) D/2) of its 32 rows.
-      const bool qrow = row < 64 || has_b;
-      const int64_t qsrc = row_base + 64 * static_cast<int64_t>(row < 64 ? qa : (has_b ? qb : qa)) + (row & 63);
+      bool qrow = row < 64 || has_b;
+      int64_t qsrc = row_base + 64 * static_cast<int64_t>(row < 64 ? qa : (has_b ? qb : qa)) + (row & 63);
+      if (NATIVE) {
+        const int64_t tok = native_token(raster_cube(p.order, row < 64 ? qa : (has_b ? qb : qa)), row & 63, p.cgrid);
+        qrow = qrow && tok >= 0;  // a padding slot of a partial cube: zero row
+        qsrc = bh * p.Nn + (tok >= 0 ? tok : 0);
+      }
       const uint4* src = reinterpret_cast<const uint4*>(p.q + qsrc * D + half * (D / 2));
 #pragma unroll
       for (int c = 0; c < D / 4; c += 8) {
@@ -499,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       uint32_t pk[32];
       if (valid) {
         float acc0 = 0.f, acc1 = 0.f;
-        softmax64(sr, splat2(p.scale_log2), splat2(-m), pk, acc0, acc1);
+        softmax64<!NATIVE>(sr, splat2(p.scale_log2), splat2(-m), pk, acc0, acc1);
         l += acc0 + acc1;
       } else {
 #pragma unroll
@@ -514,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       }
 #pragma unroll
       for (int c = 0; c < 32; c += 8) tmem_st8(lane_addr + kColP + 64 * (j & 1) + 32 * half + c, pk + c);
-      if (!F16IN) {
+      if (!F16IN && !NATIVE) {
         // bf16 V tile -> fp16 in place, before the PV MMA may read it.
         const int st = j % nv;
         if (!mbar_wait(&vfull[st], (j / nv) & 1)) {
@@ -603,15 +640,31 @@ int make_tile_map(void* map_out, const void* base, int64_t rows, int d, int f16)
   return r == CUDA_SUCCESS ? VSA_OK : VSA_ERR_CUDA;
 }
 
-int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt, int kmax,
-                    int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, int f16_in,
-                    const int32_t* pairs, const uint64_t* kmask, cudaStream_t s) {
-  FwdParams p{};
-  const int64_t rows = static_cast<int64_t>(BH) * N;
-  int st;
-  if ((st = make_tile_map(&p.tk, kp, rows, d, f16_in)) != VSA_OK) return st;
-  if ((st = make_tile_map(&p.tv, vp, rows, d, f16_in)) != VSA_OK) return st;
-  p.q = static_cast<const uint16_t*>(qp);
+// 5-D bf16 tensor map over the native [BH, T, H, W, d] layout with a
+// {64, 4, 4, 4, 1} box: one (4, 4, 4) cube of 64 channels, 128-byte swizzle,
+// zeros where the box leaves the grid.
+int make_cube_map(void* map_out, const void* base, int BH, int T, int H, int W, int d) {
+  CUtensorMap* map = static_cast<CUtensorMap*>(map_out);
+  auto enc = get_encoder();
+  if (!enc) return VSA_ERR_CUDA;
+  const cuuint64_t row = static_cast<cuuint64_t>(d) * 2;
+  cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[4] = {row, row * W, row * W * H, row * W * H * T};
+  cuuint32_t box[5] = {64, 4, 4, 4, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? VSA_OK : VSA_ERR_CUDA;
+}
+
+namespace {
+
+// Fills the common fields, sizes the K / V rings and launches.
+int run_fine_fwd(FwdParams& p, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d, float scale,
+                 void* of, int of_dtype, float* lse, int f16_in, bool native, const int32_t* pairs,
+                 const uint64_t* kmask, cudaStream_t s) {
   p.pairs = pairs;
   p.kmask = kmask;
   p.idx = idx;
@@ -650,14 +703,46 @@ int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_
     timing_mark(VSA_K_FINE_FWD, false, s);
     return VSA_OK;
   };
+  int st;
   if (d == 128)
-    st = f16_in ? go(fine_fwd_kernel<128, true>, FwdLayout<128>::kTile)
-                : go(fine_fwd_kernel<128, false>, FwdLayout<128>::kTile);
+    st = native   ? go(fine_fwd_kernel<128, false, true>, FwdLayout<128>::kTile)
+         : f16_in ? go(fine_fwd_kernel<128, true, false>, FwdLayout<128>::kTile)
+                  : go(fine_fwd_kernel<128, false, false>, FwdLayout<128>::kTile);
   else
-    st = f16_in ? go(fine_fwd_kernel<64, true>, FwdLayout<64>::kTile)
-                : go(fine_fwd_kernel<64, false>, FwdLayout<64>::kTile);
+    st = native   ? go(fine_fwd_kernel<64, false, true>, FwdLayout<64>::kTile)
+         : f16_in ? go(fine_fwd_kernel<64, true, false>, FwdLayout<64>::kTile)
+                  : go(fine_fwd_kernel<64, false, false>, FwdLayout<64>::kTile);
   if (st != VSA_OK) return st;
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt, int kmax,
+                    int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, int f16_in,
+                    const int32_t* pairs, const uint64_t* kmask, cudaStream_t s) {
+  FwdParams p{};
+  const int64_t rows = static_cast<int64_t>(BH) * N;
+  int st;
+  if ((st = make_tile_map(&p.tk, kp, rows, d, f16_in)) != VSA_OK) return st;
+  if ((st = make_tile_map(&p.tv, vp, rows, d, f16_in)) != VSA_OK) return st;
+  p.q = static_cast<const uint16_t*>(qp);
+  return run_fine_fwd(p, idx, cnt, kmax, BH, N, d, scale, of, of_dtype, lse, f16_in, false, pairs, kmask, s);
+}
+
+int launch_fine_fwd_native(const void* q, const void* k, const void* v, int T, int H, int W, const int32_t* order,
+                           const int32_t* idx, const int32_t* cnt, int kmax, int BH, int d, float scale, void* of,
+                           int of_dtype, float* lse, const int32_t* pairs, const uint64_t* kmask, cudaStream_t s) {
+  FwdParams p{};
+  int st;
+  if ((st = make_cube_map(&p.tk, k, BH, T, H, W, d)) != VSA_OK) return st;
+  if ((st = make_cube_map(&p.tv, v, BH, T, H, W, d)) != VSA_OK) return st;
+  p.q = static_cast<const uint16_t*>(q);
+  p.cgrid = cube_grid(T, H, W);
+  p.order = order;
+  p.Nn = static_cast<int64_t>(T) * H * W;
+  const int Nc = ((T + 3) / 4) * p.cgrid.Hc * p.cgrid.Wc;
+  return run_fine_fwd(p, idx, cnt, kmax, BH, Nc * kCube, d, scale, of, of_dtype, lse, 0, true, pairs, kmask, s);
 }
 
 }  // namespace vsa

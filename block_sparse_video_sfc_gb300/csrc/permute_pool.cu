@@ -37,7 +37,9 @@ __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc
   const int rcube = raster_cube(order, cube);
   const int64_t Np = static_cast<int64_t>(Nc) * kCube;  // reordered tokens per (batch, head)
   const __nv_bfloat16* src = a.src[tensor] + bh * (inverse ? Np : Nn) * D;
-  uint16_t* dst = static_cast<uint16_t*>(a.dst[tensor]) + bh * (inverse ? Nn : Np) * D;
+  // A null destination pools only (the inference forward reads the native
+  // layout directly and needs no reordered copy).
+  uint16_t* dst = a.dst[tensor] ? static_cast<uint16_t*>(a.dst[tensor]) + bh * (inverse ? Nn : Np) * D : nullptr;
   float* pooled = a.pooled[tensor];
   const int j = threadIdx.x % kChunks;     // channel chunk, fixed per thread
   const int o0 = threadIdx.x / kChunks;
@@ -63,7 +65,9 @@ __global__ void __launch_bounds__(256) permute_pool_kernel(PermuteArgs a, int Nc
     if (nat < 0 && inverse) continue;  // padding slot: nothing to write back
     const int64_t d_tok = inverse ? nat : cub;
     const uint4 v = vin[p];
-    if (F16OUT) {
+    if (!dst) {
+      // pool only
+    } else if (F16OUT) {
       const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
                           bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
       bool big = false;

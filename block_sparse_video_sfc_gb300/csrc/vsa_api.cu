@@ -45,10 +45,11 @@ int check_grid(const vsa_grid_t& g, int d, Dims* out, int64_t BH) {
 struct FwdWs {
   size_t qp, kp, vp, qc, kc, vc, oc, lsec, sc, idx, cnt, of, lse, lbits, pairs, kmask, total;
 };
-FwdWs fwd_layout(const Dims& D, int K) {
+// copies = false: the inference forward, which reads Q, K, V in place.
+FwdWs fwd_layout(const Dims& D, int K, bool copies = true) {
   FwdWs w{};
   size_t o = 0;
-  const size_t big_bf16 = sizeof(__half) * D.BH * D.N * D.d;  // fp16 copies of Q, K, V
+  const size_t big_bf16 = copies ? sizeof(__half) * D.BH * D.N * D.d : 0;  // fp16 copies of Q, K, V
   const size_t pooled = sizeof(float) * D.BH * D.Nc * D.d;
   w.qp = o; o += align256(big_bf16);
   w.kp = o; o += align256(big_bf16);
@@ -341,6 +342,7 @@ size_t vsa_workspace_bytes(int op, int B, int heads, int d, vsa_grid_t g, int to
     case VSA_OP_FORWARD: return fwd_layout(D, topk).total;
     case VSA_OP_BACKWARD: return bwd_layout(D).total;
     case VSA_OP_FINE_BWD: return fine_bwd_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.N), topk);
+    case VSA_OP_FORWARD_INFERENCE: return fwd_layout(D, topk, false).total;
     default: return 0;
   }
 }
@@ -404,6 +406,46 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
   if ((st = launch_fine_fwd(dst[0], dst[1], dst[2], at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), topk, BH, N, d,
                             scale, at<float>(ws, w.of), VSA_DTYPE_F32, at<float>(ws, w.lse), 1,
                             at<int32_t>(ws, w.pairs), kmask, s)) != VSA_OK)
+    return st;
+  return launch_combine(at<float>(ws, w.oc), at<float>(ws, w.of), g_coarse, g_fine, out, out_dtype, BH, d, g.T, g.H,
+                        g.W, g.cube_order, s);
+}
+
+int vsa_forward_inference(const void* q, const void* k, const void* v, const void* g_coarse, const void* g_fine,
+                          int B, int heads, int d, vsa_grid_t g, int topk, float scale, void* out, int out_dtype,
+                          void* ws, size_t ws_bytes, void* stream) {
+  Dims D;
+  if (B <= 0 || heads <= 0) return VSA_ERR_ARG;
+  int st = check_grid(g, d, &D, static_cast<int64_t>(B) * heads);
+  if (st != VSA_OK) return st;
+  if (topk < 1 || topk > D.Nc) return VSA_ERR_ARG;
+  if (!q || !k || !v || !out) return VSA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (g_coarse && !aligned16(g_coarse)) ||
+      (g_fine && !aligned16(g_fine)))
+    return VSA_ERR_ARG;
+  if (out_dtype != VSA_DTYPE_BF16 && out_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
+  FwdWs w = fwd_layout(D, topk, false);
+  if (!ws || ws_bytes < w.total || !aligned16(ws)) return VSA_ERR_WORKSPACE;
+  cudaStream_t s = as_stream(stream);
+  const int BH = static_cast<int>(D.BH), Nc = static_cast<int>(D.Nc);
+  // Cube means only: the fine kernel reads Q, K, V in their native layout.
+  const void* src[3] = {q, k, v};
+  void* none[3] = {nullptr, nullptr, nullptr};
+  float* pooled[3] = {at<float>(ws, w.qc), at<float>(ws, w.kc), at<float>(ws, w.vc)};
+  if ((st = launch_permute(src, none, pooled, 3, BH, d, g.T, g.H, g.W, g.cube_order, 0, 0, s)) != VSA_OK) return st;
+  if ((st = launch_coarse_topk(pooled[0], pooled[1], pooled[2], BH, Nc, d, topk, scale, at<float>(ws, w.oc),
+                               at<float>(ws, w.lsec), at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt),
+                               at<float>(ws, w.sc), s)) != VSA_OK)
+    return st;
+  if ((st = launch_list_bits(at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), topk, BH, Nc, at<uint32_t>(ws, w.lbits),
+                             s)) != VSA_OK)
+    return st;
+  if ((st = launch_pair_plan(at<uint32_t>(ws, w.lbits), BH, Nc, at<int32_t>(ws, w.pairs), s)) != VSA_OK) return st;
+  uint64_t* kmask = D.padded ? at<uint64_t>(ws, w.kmask) : nullptr;
+  if (kmask && (st = launch_slot_masks(g.T, g.H, g.W, g.cube_order, kmask, s)) != VSA_OK) return st;
+  if ((st = launch_fine_fwd_native(q, k, v, g.T, g.H, g.W, g.cube_order, at<int32_t>(ws, w.idx),
+                                   at<int32_t>(ws, w.cnt), topk, BH, d, scale, at<float>(ws, w.of), VSA_DTYPE_F32,
+                                   at<float>(ws, w.lse), at<int32_t>(ws, w.pairs), kmask, s)) != VSA_OK)
     return st;
   return launch_combine(at<float>(ws, w.oc), at<float>(ws, w.of), g_coarse, g_fine, out, out_dtype, BH, d, g.T, g.H,
                         g.W, g.cube_order, s);

@@ -45,8 +45,9 @@
  *    and clears the flag.
  *  - Precision: the pooled vectors, coarse scores and Top-K are fp32; the
  *    fine-stage tensor-core products take 16-bit operands with fp32
- *    accumulation.  vsa_fine_fwd multiplies Q K^T in bf16 and P V in fp16
- *    (V converted on chip).  vsa_forward / vsa_backward / vsa_fine_bwd
+ *    accumulation.  vsa_fine_fwd multiplies Q K^T in bf16 and P V in fp16 (V
+ *    converted on chip); vsa_forward_inference both in bf16 (P rounded to
+ *    bf16: it feeds no backward).  vsa_forward / vsa_backward / vsa_fine_bwd
  *    convert Q, K, V and
  *    dO_f = g_fine * dO to fp16 (exact for bf16 values of magnitude up to
  *    65504; 8x finer rounding of the probabilities and of dS than bf16).  An
@@ -231,6 +232,22 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
                 size_t ws_bytes, void* stream);
 
 /*
+ * vsa_forward_inference -- the same output as vsa_forward, without the state
+ * a backward pass needs.  The fine stage reads Q, K and V in their native
+ * layout: each (4, 4, 4) cube is one 5-D TMA box of the [B*heads, T, H, W, d]
+ * tensor (zeros where the box leaves the grid), so no reordered copy of Q, K,
+ * V is written -- the permutation is folded into the TMA addressing; only the
+ * cube means are computed in a separate pass.  Arguments as vsa_forward; ws is
+ * vsa_workspace_bytes(VSA_OP_FORWARD_INFERENCE, ...) bytes of scratch.  The
+ * fine products run in bf16 with the softmax weights rounded to bf16
+ * (vsa_forward: fp16 copies and fp16 weights), so the two outputs agree to
+ * that rounding, well within the parity tolerance.
+ */
+int vsa_forward_inference(const void* q, const void* k, const void* v, const void* g_coarse, const void* g_fine,
+                          int B, int heads, int d, vsa_grid_t g, int topk, float scale, void* out, int out_dtype,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/*
  * vsa_backward -- gradients of vsa_forward.  [ABS].
  *   fwd_ws      the workspace the forward call filled (read only).
  *   g_coarse, g_fine, B, heads, d, g, topk, scale: the same as in the forward.
@@ -244,7 +261,7 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
                  int heads, int d, vsa_grid_t g, int topk, float scale, void* dq, void* dk, void* dv,
                  void* dg_coarse, void* dg_fine, int grad_dtype, void* ws, size_t ws_bytes, void* stream);
 
-enum { VSA_OP_FORWARD = 0, VSA_OP_BACKWARD = 1, VSA_OP_FINE_BWD = 2 };
+enum { VSA_OP_FORWARD = 0, VSA_OP_BACKWARD = 1, VSA_OP_FINE_BWD = 2, VSA_OP_FORWARD_INFERENCE = 3 };
 
 /* Workspace bytes for an operation (0 on a bad argument).  For
  * VSA_OP_FINE_BWD, B*heads is BH and g/topk give N and max_kv_blocks. */

@@ -550,3 +550,27 @@ def test_forward_backward_capture_in_a_cuda_graph(vsa, oracle_mod):
     replay = [out] + [grads[n] for n in ("dq", "dk", "dv", "dgc", "dgf")]
     for a, b in zip(eager, replay):
         assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------- inference forward (permute folded into TMA)
+@pytest.mark.parametrize("name,curve", [("tiny", "raster"), ("small", "raster"), ("small", "hilbert"),
+                                        ("odd", "raster"), ("odd_small", "hilbert"), ("wan1.3b", "raster")])
+def test_forward_inference(vsa, oracle_mod, name, curve):
+    """vsa_forward_inference reads Q, K, V through 5-D TMA boxes in native
+    layout and multiplies in bf16: the same index lists as vsa_forward, its
+    output within the parity tolerance of vsa_forward's and of the oracle's."""
+    wl = synth.WORKLOADS[name]
+    order = None if curve == "raster" else vsa.cube_order(wl.T, wl.H, wl.W, curve)
+    q, k, v = synth.make_qkv(wl)
+    gc, gf = synth.make_gates(wl)
+    ins = [dev(a) for a in (q, k, v, gc, gf)]
+    out_f, st = vsa.forward(*ins[:3], wl.T, wl.H, wl.W, wl.topk, g_coarse=ins[3], g_fine=ins[4],
+                            out_dtype=torch.float32, cube_order=order)
+    out_i = vsa.forward_inference(*ins[:3], wl.T, wl.H, wl.W, wl.topk, g_coarse=ins[3], g_fine=ins[4],
+                                  out_dtype=torch.float32, cube_order=order)
+    status_ok(vsa)
+    assert_close(host(out_i), host(out_f), what="out (inference vs forward)")
+    if wl.N <= 4096:
+        gidx = st.saved()["idx"].cpu().numpy().reshape(wl.B, wl.heads, wl.Nc, wl.topk)
+        ref = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=gc, gf=gf, lut=gidx, curve=curve)
+        assert_close(host(out_i), ref["out"], what="out (inference)")
