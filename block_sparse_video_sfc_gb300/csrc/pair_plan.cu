@@ -109,33 +109,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_pairs_kernel(const uint16_t
   for (int c = tid; c < Nc; c += blockDim.x) partner[c] = -1;
   __syncthreads();
 
-  // Each round one warp scores a cube's 2 * kWindow candidates at once (lane
-  // l: cube c - kWindow + l and cube c + 1 + l) and keeps the best by a warp
-  // maximum over the key (overlap, nearer, lower id).
-  const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  static_assert(kWindow == 32, "one candidate per lane on each side");
+  auto overlap = [&](int c, int b) -> int {
+    return c < b ? ov[c * kWindow + (b - c - 1)] : ov[b * kWindow + (c - b - 1)];
+  };
   for (int round = 0; round < kRounds; ++round) {
-    for (int c = warp; c < Nc; c += nwarps) {
-      uint64_t key = 0;  // 0: no candidate
+    for (int c = tid; c < Nc; c += blockDim.x) {
+      int best = -1, best_ov = -1, best_dist = 0;
       if (partner[c] < 0) {
-#pragma unroll
-        for (int side = 0; side < 2; ++side) {
-          const int b = side == 0 ? c - kWindow + lane : c + 1 + lane;
-          if (b >= 0 && b < Nc && partner[b] < 0) {
-            const int dist = side == 0 ? c - b : b - c;  // 1..kWindow
-            const int o = side == 0 ? ov[b * kWindow + (dist - 1)] : ov[c * kWindow + (dist - 1)];
-            const uint64_t k = (static_cast<uint64_t>(o + 1) << 32) | (static_cast<uint64_t>(kWindow - dist) << 16) |
-                               static_cast<uint64_t>(32767 - b);
-            key = k > key ? k : key;
+        const int lo = max(0, c - kWindow), hi = min(Nc - 1, c + kWindow);
+        for (int b = lo; b <= hi; ++b) {
+          if (b == c || partner[b] >= 0) continue;
+          const int o = overlap(c, b), dist = abs(b - c);
+          if (o > best_ov || (o == best_ov && dist < best_dist)) {  // scanning b upward keeps the lower id on a full tie
+            best = b;
+            best_ov = o;
+            best_dist = dist;
           }
         }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const uint64_t other = __shfl_xor_sync(0xffffffffu, key, off);
-        key = other > key ? other : key;
-      }
-      if (lane == 0) pick[c] = static_cast<int16_t>(key ? 32767 - static_cast<int>(key & 0xFFFF) : -1);
+      pick[c] = static_cast<int16_t>(best);
     }
     __syncthreads();
     for (int c = tid; c < Nc; c += blockDim.x) {
