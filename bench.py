@@ -257,7 +257,7 @@ def run_ours(args, rank: int, world: int):
     # native layout through 5-D TMA boxes; no reordered copies).  Reported
     # beside the headline; not part of it.
     fwd_only = None
-    if world == 1:
+    if world == 1 and not args.no_forward_only:
         iws = torch.empty(vsa.workspace_bytes(3, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk), dtype=torch.uint8,
                           device=dev)
         runs = {
@@ -430,6 +430,7 @@ def main():
     ap.add_argument("--config", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-forward-only", action="store_true", help="skip the forward-only timings")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--curve", choices=["raster", "hilbert"], default="raster",
                     help="cube order of the space-filling-curve reordering")
