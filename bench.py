@@ -344,7 +344,8 @@ def run_ours(args, rank: int, world: int):
     # kernel S, dP, dQ (3).  The effective metric counts 2 + 5.
     unit = 2.0 * wl.N * (wl.topk * wl.N / wl.Nc) * wl.d * wl.BH
     kflops = {"fine_fwd": 2 * unit, "fine_bwd_kv": 4 * unit, "fine_bwd_dq": 3 * unit}
-    dominant = max(kflops, key=lambda n: per_kernel[n])
+    # The roofline is reported for the kernel with the most work per step.
+    dominant = max(kflops, key=lambda n: kflops[n])
     traffic = None  # DRAM bytes per launch from the committed ncu capture (profiles/traffic.txt)
     tpath = os.path.join(ROOT, "profiles", "traffic.txt")
     if os.path.exists(tpath) and args.config == WORKLOAD and args.curve == "raster":  # the captured case only
@@ -359,7 +360,15 @@ def run_ours(args, rank: int, world: int):
         return {"ms": per_kernel[n], "tflops": round(a, 2), "frac": round(a / peaks["tflops"], 4),
                 "flops_per_launch": kflops[n]}
 
-    bwd_ms = per_kernel["fine_bwd_kv"] + per_kernel["fine_bwd_dq"]
+    # vsa_backward runs the dK/dV kernel on a higher-priority stream of its own
+    # while the coarse backward and then the dQ kernel run on the caller's
+    # stream, filling the SMs the dK/dV kernel leaves.  The coarse and dQ event
+    # pairs follow one another on the caller's stream from the fork on, so
+    # together they span the fine backward's wall time (the coarse backward
+    # included).  Run back to back (no overlap), the two kernel intervals add.
+    overlapped = per_kernel["fine_bwd_dq"] > per_kernel["fine_bwd_kv"]
+    bwd_ms = (per_kernel["coarse_bwd"] + per_kernel["fine_bwd_dq"] if overlapped
+              else per_kernel["fine_bwd_kv"] + per_kernel["fine_bwd_dq"])
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3), "higher_is_better": True,
@@ -374,7 +383,9 @@ def run_ours(args, rank: int, world: int):
                      "flops_per_launch": kflops[dominant]},
         "fine_fwd": roof("fine_fwd"),
         "fine_bwd_kv": roof("fine_bwd_kv"),
-        "fine_bwd_dq": roof("fine_bwd_dq"),
+        "fine_bwd_dq": ({"interval_ms": per_kernel["fine_bwd_dq"],
+                         "note": "runs beside fine_bwd_kv; with coarse_bwd before it the interval spans the fine backward"}
+                        if overlapped else roof("fine_bwd_dq")),
         "fine_bwd_effective": {"ms": round(bwd_ms, 4),
                                "tflops": round(fl["fine_bwd"] / (bwd_ms * 1e-3) / 1e12, 2)},
         "kernel_ms_per_step": per_kernel,

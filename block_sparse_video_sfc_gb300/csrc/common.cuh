@@ -136,7 +136,7 @@ int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* 
 int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const void* dof, const float* lse,
                          const float* delta, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
                          float scale, float* dq, float* dk, float* dv, uint32_t* inv_ws, const int32_t* qpairs,
-                         int32_t* kpairs_ws, cudaStream_t s);
+                         int32_t* kpairs_ws, cudaStream_t s, cudaStream_t s_kv);
 int launch_combine(const float* oc, const float* of, const void* gc, const void* gf, void* out, int out_dtype,
                    int BH, int d, int T, int H, int W, const int32_t* order, cudaStream_t s);
 int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const float* oc, const float* of,

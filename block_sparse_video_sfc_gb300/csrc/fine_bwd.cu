@@ -788,11 +788,13 @@ int launch_delta(const void* of, int of_dtype, const void* dof, int64_t rows, in
 // Fine backward with the row statistics D given.  qp, kp, vp, dof are fp16
 // (cube order); inv_ws: scratch for the inverse-list bit matrix; qpairs: the
 // query-cube tiles of the dQ kernel (null: cubes 2t, 2t + 1); kpairs_ws:
-// scratch for the key-cube pair plan (null: cubes 2t, 2t + 1).
+// scratch for the key-cube pair plan (null: cubes 2t, 2t + 1).  The inverse
+// lists, the key plan and the dK/dV kernel go on s_kv, the dQ kernel on s (the
+// two kernels are independent; s_kv may be s).
 int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const void* dof, const float* lse,
                          const float* delta, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
                          float scale, float* dq, float* dk, float* dv, uint32_t* inv_ws, const int32_t* qpairs,
-                         int32_t* kpairs_ws, cudaStream_t s) {
+                         int32_t* kpairs_ws, cudaStream_t s, cudaStream_t s_kv) {
   BwdParams p{};
   const int64_t rows = static_cast<int64_t>(BH) * N;
   int st;
@@ -820,32 +822,32 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   p.qpairs = qpairs;
   p.kpairs = kpairs_ws;
   const size_t inv_bytes = sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords;
-  if (cudaMemsetAsync(inv_ws, 0, inv_bytes, s) != cudaSuccess) return VSA_ERR_CUDA;
+  if (cudaMemsetAsync(inv_ws, 0, inv_bytes, s_kv) != cudaSuccess) return VSA_ERR_CUDA;
   const int64_t entries = static_cast<int64_t>(BH) * Nc * kmax;
   if (entries > 0)
-    build_inverse_bits<<<static_cast<unsigned>((entries + 255) / 256), 256, 0, s>>>(
+    build_inverse_bits<<<static_cast<unsigned>((entries + 255) / 256), 256, 0, s_kv>>>(
         idx, cnt, kmax, Nc, nwords, static_cast<int64_t>(BH) * Nc, inv_ws, p.err);
-  if (kpairs_ws && (st = launch_pair_plan(inv_ws, BH, Nc, kpairs_ws, s)) != VSA_OK) return st;
+  if (kpairs_ws && (st = launch_pair_plan(inv_ws, BH, Nc, kpairs_ws, s_kv)) != VSA_OK) return st;
   const size_t kv_extra = sizeof(uint32_t) * (2 * Nc + 2 + 2 * nwords);
   const size_t dq_extra = sizeof(uint32_t) * (2 * kmax + 2 + 2 * nwords);
   dim3 grid((Nc + 1) / 2, BH);
-  auto go = [&](auto kernel, size_t bytes) -> int {
+  auto go = [&](auto kernel, size_t bytes, cudaStream_t st_) -> int {
     const size_t smem = bytes + 1024;
     if (smem > 226 * 1024) return VSA_ERR_UNSUPPORTED;  // 1 KB of the 227 KB is left for static shared memory
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       return VSA_ERR_CUDA;
-    kernel<<<grid, kThreads, smem, s>>>(p);
+    kernel<<<grid, kThreads, smem, st_>>>(p);
     return VSA_OK;
   };
-  timing_mark(VSA_K_FINE_BWD, true, s);
-  st = d == 128 ? go(fine_bwd_kv_kernel<128>, KvLayout<128>::kEnd + kv_extra)
-                : go(fine_bwd_kv_kernel<64>, KvLayout<64>::kEnd + kv_extra);
-  timing_mark(VSA_K_FINE_BWD, false, s);
+  timing_mark(VSA_K_FINE_BWD, true, s_kv);
+  st = d == 128 ? go(fine_bwd_kv_kernel<128>, KvLayout<128>::kEnd + kv_extra, s_kv)
+                : go(fine_bwd_kv_kernel<64>, KvLayout<64>::kEnd + kv_extra, s_kv);
+  timing_mark(VSA_K_FINE_BWD, false, s_kv);
   if (st != VSA_OK) return st;
   timing_mark(VSA_K_FINE_BWD_DQ, true, s);
-  st = d == 128 ? go(fine_bwd_dq_kernel<128>, DqLayout<128>::kEnd + dq_extra)
-                : go(fine_bwd_dq_kernel<64>, DqLayout<64>::kEnd + dq_extra);
+  st = d == 128 ? go(fine_bwd_dq_kernel<128>, DqLayout<128>::kEnd + dq_extra, s)
+                : go(fine_bwd_dq_kernel<64>, DqLayout<64>::kEnd + dq_extra, s);
   timing_mark(VSA_K_FINE_BWD_DQ, false, s);
   if (st != VSA_OK) return st;
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
@@ -878,7 +880,7 @@ int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* 
   int st = launch_delta(of, of_dtype, h[3], rows, d, delta, s);
   if (st != VSA_OK) return st;
   return launch_fine_bwd_core(h[0], h[1], h[2], h[3], lse, delta, idx, cnt, kmax, BH, N, d, scale, dq, dk, dv, inv_ws,
-                              nullptr, kpairs, s);
+                              nullptr, kpairs, s, s);
 }
 
 }  // namespace vsa

@@ -158,6 +158,44 @@ int* device_error_word() {
   return g_err_ptr[dev];
 }
 
+// Per device, a stream of the highest priority for the dK/dV chain of
+// vsa_backward and the events of its fork from and join to the caller's
+// stream (created on first use).  At that priority the block scheduler runs
+// dK/dV first and the dQ kernel and the coarse backward, queued on the
+// caller's stream, fill the SMs that the dK/dV kernel's last wave leaves idle.
+struct AuxStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;  // one fork / join at a time per device (the events are shared)
+};
+AuxStream g_aux[kMaxDevices];
+
+AuxStream* aux_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  AuxStream& a = g_aux[dev];
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!a.s) {
+    int least = 0, greatest = 0;
+    cudaStream_t st = nullptr;
+    cudaEvent_t e1 = nullptr, e2 = nullptr;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+        cudaEventCreateWithFlags(&e1, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&e2, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();  // not fatal: the backward then runs on the caller's stream alone
+      if (st) cudaStreamDestroy(st);
+      if (e1) cudaEventDestroy(e1);
+      if (e2) cudaEventDestroy(e2);
+      return nullptr;
+    }
+    a.fork = e1;
+    a.join = e2;
+    a.s = st;
+  }
+  return &a;
+}
+
 int num_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
@@ -475,6 +513,18 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
                             g_coarse ? dg_coarse : nullptr, g_fine ? dg_fine : nullptr, grad_dtype, BH, d, g.T, g.H,
                             g.W, g.cube_order, s)) != VSA_OK)
     return st;
+  // Fork: the dK/dV chain on the auxiliary stream (highest priority), the
+  // coarse backward and the dQ kernel on the caller's stream; join before the
+  // finalize.  Without an auxiliary stream everything runs on s.
+  AuxStream* aux = aux_stream();
+  std::unique_lock<std::mutex> fork_lock;
+  cudaStream_t s_kv = s;
+  if (aux) {
+    fork_lock = std::unique_lock<std::mutex>(aux->mu);
+    if (cudaEventRecord(aux->fork, s) != cudaSuccess || cudaStreamWaitEvent(aux->s, aux->fork, 0) != cudaSuccess)
+      return VSA_ERR_CUDA;
+    s_kv = aux->s;
+  }
   if ((st = launch_coarse_bwd(at<float>(fwd_ws, f.qc), at<float>(fwd_ws, f.kc), at<float>(fwd_ws, f.vc),
                               at<float>(ws, w.doc), at<float>(fwd_ws, f.lsec), BH, Nc, d, scale, at<float>(ws, w.P),
                               at<float>(ws, w.dS), at<float>(ws, w.dqc), at<float>(ws, w.dkc), at<float>(ws, w.dvc),
@@ -485,8 +535,10 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
                                  at<int32_t>(fwd_ws, f.idx), at<int32_t>(fwd_ws, f.cnt), topk, BH, N, d, scale,
                                  at<float>(ws, w.dqp), at<float>(ws, w.dkp), at<float>(ws, w.dvp),
                                  at<uint32_t>(ws, w.inv), at<int32_t>(fwd_ws, f.pairs), at<int32_t>(ws, w.kpairs),
-                                 s)) != VSA_OK)
+                                 s, s_kv)) != VSA_OK)
     return st;
+  if (aux && (cudaEventRecord(aux->join, s_kv) != cudaSuccess || cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess))
+    return VSA_ERR_CUDA;
   return launch_finalize(at<float>(ws, w.dqp), at<float>(ws, w.dkp), at<float>(ws, w.dvp), at<float>(ws, w.dqc),
                          at<float>(ws, w.dkc), at<float>(ws, w.dvc), dq, dk, dv, grad_dtype, BH, d, g.T, g.H, g.W,
                          g.cube_order, s);
