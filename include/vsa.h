@@ -256,6 +256,12 @@ int vsa_forward_inference(const void* q, const void* k, const void* v, const voi
  *   dg_coarse, dg_fine  [B, heads, N, d] native, dtype grad_dtype; may be NULL,
  *               and are ignored when the matching gate is NULL.
  *   ws          workspace of vsa_workspace_bytes(VSA_OP_BACKWARD, ...) bytes.
+ * The dK/dV kernel runs on a library-owned stream of the highest priority
+ * (one per device, created on first use), forked from `stream` by an event
+ * and joined back into it before the call's last kernel; the dQ kernel runs
+ * on `stream` beside it.  To the caller this is ordinary stream-ordered work
+ * (it also records into a CUDA graph).  Calls on one device that overlap in
+ * time from several host threads take their turn at the fork.
  */
 int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, const void* dout, int B,
                  int heads, int d, vsa_grid_t g, int topk, float scale, void* dq, void* dk, void* dv,
