@@ -16,12 +16,13 @@
 // fine_bwd_kv_kernel (key-stationary): one CTA owns a PAIR of consecutive key
 // cubes (128 keys; K, V in shared memory; dK, dV accumulated in TMEM) and
 // walks the union of the two cubes' inverse lists (the query cubes whose index
-// list holds either key cube), two query cubes (128 rows) per step, masking
-// quadrants that are not listed.  Keys sit on the MMA M dimension:
+// list holds either key cube), one query cube (64 rows) per step, masking the
+// half of the tile whose key cube the query cube does not list.  Keys sit on
+// the MMA M dimension:
 //   S^T = K Q^T, dP^T = V dO^T        (A, B in shared memory)
 //   dV += P^T dO, dK += dS^T Q        (A = P^T / dS^T in TMEM)
-// dV(j) is issued as soon as P^T(j) is written, before dS^T(j) exists; Q and
-// dO are double-buffered.
+// S^T(j+1) and dP^T(j+1) run while the compute warps turn S^T(j), dP^T(j)
+// into P^T(j), dS^T(j) (two buffers); Q and dO go through a 4-stage ring.
 //
 // fine_bwd_dq_kernel (query-stationary): one CTA owns a pair of query cubes
 // (128 rows; Q, dO in shared memory; dQ accumulated in TMEM) and walks the
