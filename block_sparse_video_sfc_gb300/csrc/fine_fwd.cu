@@ -7,12 +7,15 @@
 //
 // GB300 mapping.  The tensor core's full rate needs M = 128 rows and N >= 128
 // columns per MMA, while the index list is per 64-token query cube.  One CTA
-// therefore owns a PAIR of consecutive query cubes (128 query rows) and walks
-// the UNION of their two lists, two key cubes (128 keys) per step; each half
-// of the tile masks the cubes its own list does not hold.  Per step j:
-//   S(j) = Q K(j)^T     tcgen05.mma, A = Q (smem), B = K (smem), D = TMEM
+// therefore owns a PAIR of query cubes (128 query rows; the pairs come from
+// the overlap plan of pair_plan.cu, or are cubes 2t, 2t + 1) and walks the
+// UNION of their two lists, two key cubes (128 keys) per step; each half of
+// the tile masks the cubes its own list does not hold.  Per step j:
+//   S(j) = Q K(j)^T     tcgen05.mma, A = Q (TMEM), B = K (smem), D = TMEM
 //   P(j) = exp2(S - m)  softmax warps, one thread per row, P -> TMEM (fp16)
 //   O   += P(j) V(j)    tcgen05.mma, A = P (TMEM), B = V (smem, fp16)
+// Padding slots of partial cubes (a grid side not a multiple of 4) are masked
+// out of the keys through a per-cube slot mask.
 // One CTA per SM.  K and V stream through rings of up to three 32 KB shared-
 // memory stages each.  Q sits in TMEM and is the A operand of S = Q K^T, so
 // the tensor core reads only K and V from shared memory: every byte of it
