@@ -318,6 +318,15 @@ size_t topk_rows_smem(int Nc, int K) {
   return kRowWarps * ((static_cast<size_t>(Nc) * 4 + static_cast<size_t>(K) * 8 + 15) & ~size_t(15));
 }
 
+// O_c = softmax(scores) Vc (the row softmax applied as the scores load).
+int launch_coarse_oc(const float* scores, const float* lse_c, const float* vc, int BH, int Nc, int d, float* oc,
+                     cudaStream_t s) {
+  const int64_t nd = static_cast<int64_t>(Nc) * d, nn = static_cast<int64_t>(Nc) * Nc;
+  GemmBatch b{};
+  b.job[0] = job(kNN, scores, vc, oc, 1.0f, Nc, d, Nc, nn, nd, nd, lse_c, Nc);
+  return launch_gemm(b, 1, BH, Nc, d, s);
+}
+
 int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk, float scale,
                        float* oc, float* lse_c, int32_t* idx, int32_t* cnt, float* scores, cudaStream_t s) {
   const size_t smem = topk_rows_smem(Nc, topk);
@@ -335,10 +344,7 @@ int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH
   topk_rows_kernel<<<static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps), kRowWarps * 32, smem, s>>>(
       scores, rows, Nc, topk, idx, cnt, lse_c);
   if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
-  if (oc) {
-    b.job[0] = job(kNN, scores, vc, oc, 1.0f, Nc, d, Nc, nn, nd, nd, lse_c, Nc);
-    if ((st = launch_gemm(b, 1, BH, Nc, d, s)) != VSA_OK) return st;
-  }
+  if (oc && (st = launch_coarse_oc(scores, lse_c, vc, BH, Nc, d, oc, s)) != VSA_OK) return st;
   timing_mark(VSA_K_COARSE, false, s);
   return VSA_OK;
 }

@@ -109,6 +109,8 @@ int make_tile_map(void* map, const void* base, int64_t rows, int d, int f16);
 int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk,
                        float scale, float* oc, float* lse_c, int32_t* idx, int32_t* cnt, float* scores,
                        cudaStream_t s);
+int launch_coarse_oc(const float* scores, const float* lse_c, const float* vc, int BH, int Nc, int d, float* oc,
+                     cudaStream_t s);
 int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt,
                     int kmax, int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, int f16_in,
                     const int32_t* pairs, const uint64_t* kmask, cudaStream_t s);

@@ -429,10 +429,25 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
   void* dst[3] = {at<void>(ws, w.qp), at<void>(ws, w.kp), at<void>(ws, w.vp)};
   float* pooled[3] = {at<float>(ws, w.qc), at<float>(ws, w.kc), at<float>(ws, w.vc)};
   if ((st = launch_permute(src, dst, pooled, 3, BH, d, g.T, g.H, g.W, g.cube_order, 0, 1, s)) != VSA_OK) return st;
-  if ((st = launch_coarse_topk(pooled[0], pooled[1], pooled[2], BH, Nc, d, topk, scale, at<float>(ws, w.oc),
-                               at<float>(ws, w.lsec), at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), at<float>(ws, w.sc), s)) !=
-      VSA_OK)
+  if ((st = launch_coarse_topk(pooled[0], pooled[1], pooled[2], BH, Nc, d, topk, scale, nullptr,
+                               at<float>(ws, w.lsec), at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt),
+                               at<float>(ws, w.sc), s)) != VSA_OK)
     return st;
+  // O_c is needed only by the combine: it runs on the auxiliary stream beside
+  // the pair planning and the fine kernel, and joins before the combine.
+  AuxStream* aux = aux_stream();
+  std::unique_lock<std::mutex> fork_lock;
+  cudaStream_t s_oc = s;
+  if (aux) {
+    fork_lock = std::unique_lock<std::mutex>(aux->mu);
+    if (cudaEventRecord(aux->fork, s) != cudaSuccess || cudaStreamWaitEvent(aux->s, aux->fork, 0) != cudaSuccess)
+      return VSA_ERR_CUDA;
+    s_oc = aux->s;
+  }
+  if ((st = launch_coarse_oc(at<float>(ws, w.sc), at<float>(ws, w.lsec), pooled[2], BH, Nc, d, at<float>(ws, w.oc),
+                             s_oc)) != VSA_OK)
+    return st;
+  if (aux && cudaEventRecord(aux->join, s_oc) != cudaSuccess) return VSA_ERR_CUDA;
   // Pair query cubes whose lists overlap most into the fine kernels' tiles.
   if ((st = launch_list_bits(at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), topk, BH, Nc, at<uint32_t>(ws, w.lbits),
                              s)) != VSA_OK)
@@ -445,6 +460,7 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
                             scale, at<float>(ws, w.of), VSA_DTYPE_F32, at<float>(ws, w.lse), 1,
                             at<int32_t>(ws, w.pairs), kmask, s)) != VSA_OK)
     return st;
+  if (aux && cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess) return VSA_ERR_CUDA;
   return launch_combine(at<float>(ws, w.oc), at<float>(ws, w.of), g_coarse, g_fine, out, out_dtype, BH, d, g.T, g.H,
                         g.W, g.cube_order, s);
 }
@@ -471,10 +487,25 @@ int vsa_forward_inference(const void* q, const void* k, const void* v, const voi
   void* none[3] = {nullptr, nullptr, nullptr};
   float* pooled[3] = {at<float>(ws, w.qc), at<float>(ws, w.kc), at<float>(ws, w.vc)};
   if ((st = launch_permute(src, none, pooled, 3, BH, d, g.T, g.H, g.W, g.cube_order, 0, 0, s)) != VSA_OK) return st;
-  if ((st = launch_coarse_topk(pooled[0], pooled[1], pooled[2], BH, Nc, d, topk, scale, at<float>(ws, w.oc),
+  if ((st = launch_coarse_topk(pooled[0], pooled[1], pooled[2], BH, Nc, d, topk, scale, nullptr,
                                at<float>(ws, w.lsec), at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt),
                                at<float>(ws, w.sc), s)) != VSA_OK)
     return st;
+  // O_c is needed only by the combine: it runs on the auxiliary stream beside
+  // the pair planning and the fine kernel, and joins before the combine.
+  AuxStream* aux = aux_stream();
+  std::unique_lock<std::mutex> fork_lock;
+  cudaStream_t s_oc = s;
+  if (aux) {
+    fork_lock = std::unique_lock<std::mutex>(aux->mu);
+    if (cudaEventRecord(aux->fork, s) != cudaSuccess || cudaStreamWaitEvent(aux->s, aux->fork, 0) != cudaSuccess)
+      return VSA_ERR_CUDA;
+    s_oc = aux->s;
+  }
+  if ((st = launch_coarse_oc(at<float>(ws, w.sc), at<float>(ws, w.lsec), pooled[2], BH, Nc, d, at<float>(ws, w.oc),
+                             s_oc)) != VSA_OK)
+    return st;
+  if (aux && cudaEventRecord(aux->join, s_oc) != cudaSuccess) return VSA_ERR_CUDA;
   if ((st = launch_list_bits(at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), topk, BH, Nc, at<uint32_t>(ws, w.lbits),
                              s)) != VSA_OK)
     return st;
@@ -485,6 +516,7 @@ int vsa_forward_inference(const void* q, const void* k, const void* v, const voi
                                    at<int32_t>(ws, w.cnt), topk, BH, d, scale, at<float>(ws, w.of), VSA_DTYPE_F32,
                                    at<float>(ws, w.lse), at<int32_t>(ws, w.pairs), kmask, s)) != VSA_OK)
     return st;
+  if (aux && cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess) return VSA_ERR_CUDA;
   return launch_combine(at<float>(ws, w.oc), at<float>(ws, w.of), g_coarse, g_fine, out, out_dtype, BH, d, g.T, g.H,
                         g.W, g.cube_order, s);
 }
