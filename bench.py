@@ -45,6 +45,42 @@ KERNELS_PER_STEP = 19
 WORKLOAD = "wan1.3b"
 
 
+class near_gpu_memory:
+    """Within the block, this thread runs on the CPUs of the GPU's own NUMA
+    node, so that pinned host buffers allocated there are first touched in
+    that node's memory (the host<->device copies then take the shortest path);
+    the previous CPU set is restored afterwards.  Does nothing where the
+    topology cannot be read."""
+
+    def __init__(self, device_index: int):
+        self.cpus = None
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(device_index)
+            bus = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+            with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+                node = int(f.read().strip())
+            if node >= 0:
+                with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+                    cpus = set()
+                    for part in f.read().strip().split(","):
+                        a, _, b = part.partition("-")
+                        cpus.update(range(int(a), int(b or a) + 1))
+                self.cpus = cpus & os.sched_getaffinity(0) or None
+        except (OSError, ValueError, AttributeError):
+            self.cpus = None
+
+    def __enter__(self):
+        self.saved = os.sched_getaffinity(0)
+        if self.cpus:
+            os.sched_setaffinity(0, self.cpus)
+        return self
+
+    def __exit__(self, *exc):
+        os.sched_setaffinity(0, self.saved)
+        return False
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     """The largest x over all ranks (every rank receives it); x itself at world 1."""
     if world == 1:
@@ -206,7 +242,8 @@ def run_ours(args, rank: int, world: int):
     q, k, v = synth.make_qkv(wl)
     gc, gf = synth.make_gates(wl)
     dout = synth.make_dout(wl)
-    host = [torch.from_numpy(a).to(torch.bfloat16).pin_memory() for a in (q, k, v, gc, gf, dout)]
+    with near_gpu_memory(local):
+        host = [torch.from_numpy(a).to(torch.bfloat16).pin_memory() for a in (q, k, v, gc, gf, dout)]
     dq_, dk_, dv_, dgc_, dgf_, ddo = (h.to(dev) for h in host)
     out = torch.empty_like(dq_)
     grads = dict(dq=torch.empty_like(dq_), dk=torch.empty_like(dq_), dv=torch.empty_like(dq_),
@@ -289,7 +326,8 @@ def run_ours(args, rank: int, world: int):
     # uploads and step i-1's downloads overlap step i's kernels.
     e2e = None
     if not args.no_e2e:
-        host_out = [torch.empty(out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(6)]
+        with near_gpu_memory(local):
+            host_out = [torch.empty(out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(6)]
         dev_in = [[dq_, dk_, dv_, dgc_, dgf_, ddo], [torch.empty_like(dq_) for _ in range(6)]]
         res = [dict(out=out, **grads),
                dict(out=torch.empty_like(out), **{n: torch.empty_like(t) for n, t in grads.items()})]
