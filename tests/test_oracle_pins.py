@@ -102,6 +102,39 @@ def test_coarse_equals_sdpa_on_pooled(oracle_mod):
     np.testing.assert_allclose(lse, torch.logsumexp(torch.tensor(scores), -1).numpy(), rtol=1e-13)
 
 
+@pytest.mark.parametrize("grid", [(8, 8, 8), (6, 7, 5)])
+def test_constant_cubes_tie_fine_to_coarse(oracle_mod, grid):
+    """Every cube constant, all cubes selected: the fine stage's 64 (or, in a
+    partial cube, fewer) copies of each key act as one key weighted by its
+    token count, so O_f = sum_j n_j e^{s q.k_j} v_j / sum_j n_j e^{s q.k_j},
+    LSE_f = log sum_j n_j e^{s q.k_j}, and O_c is the same sum without n_j.
+    With full cubes O_f equals O_c: the pool, the coarse scale and the fine
+    stage agree.  Closed form computed here from the cube values alone."""
+    T, H, W = grid
+    BH, d, scale = 2, 16, 0.3
+    Tc, Hc, Wc = (T + 3) // 4, (H + 3) // 4, (W + 3) // 4
+    Nc = Tc * Hc * Wc
+    t, h, w = np.meshgrid(np.arange(T), np.arange(H), np.arange(W), indexing="ij")
+    cube = ((t // 4 * Hc + h // 4) * Wc + w // 4).reshape(-1)       # raster cube of each native token
+    ntok = np.bincount(cube, minlength=Nc).astype(np.float64)
+    rng = np.random.default_rng(17)
+    qv, kv, vv = (rng.normal(size=(BH, Nc, d)) for _ in range(3))
+    q, k, v = (a[:, cube] for a in (qv, kv, vv))
+    r = oracle_mod.forward(q, k, v, T, H, W, Nc, scale)
+    e = np.exp(scale * np.einsum("bid,bjd->bij", qv, kv))
+    oc = np.einsum("bij,bjd->bid", e, vv) / e.sum(-1, keepdims=True)
+    en = e * ntok
+    of = np.einsum("bij,bjd->bid", en, vv) / en.sum(-1, keepdims=True)
+    lse = np.log(en.sum(-1))
+    pos = oracle_mod.sfc_table(T, H, W)
+    np.testing.assert_allclose(r["oc"], oc, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r["of"][:, pos], of[:, cube], rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(r["lse"][:, pos], lse[:, cube], rtol=1e-12)
+    np.testing.assert_allclose(r["out"], (oc + of)[:, cube], rtol=1e-11, atol=1e-11)
+    if T % 4 == 0 and H % 4 == 0 and W % 4 == 0:
+        np.testing.assert_allclose(of, oc, rtol=1e-12, atol=1e-12)
+
+
 def _bruteforce_topk(scores, K):
     Nc = scores.shape[-1]
     out = np.empty(scores.shape[:-1] + (K,), dtype=np.int64)
