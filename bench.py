@@ -38,10 +38,9 @@ METRIC = "VSA fwd+bwd effective TFLOPS at 32K tokens, 70% sparsity; % of bf16 te
 UNIT = "TFLOP/s"
 # libvsa kernels launched by one forward + backward step: permute_pool,
 # coarse_gemm, topk_rows, coarse_gemm, build_list_bits, pair_overlap,
-# plan_pairs, fine_fwd, combine | bwd_prep, coarse_gemm, bwd_rows, coarse_gemm,
-# build_inverse_bits, pair_overlap, plan_pairs, fine_bwd_kv, fine_bwd_dq,
-# finalize.
-KERNELS_PER_STEP = 19
+# plan_pairs, fine_fwd, combine | build_inverse_bits, pair_overlap, plan_pairs,
+# bwd_prep, coarse_gemm, bwd_rows, coarse_gemm, fine_bwd_kv, fine_bwd_dq.
+KERNELS_PER_STEP = 18
 WORKLOAD = "wan1.3b"
 
 

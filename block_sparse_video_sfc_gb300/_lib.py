@@ -77,8 +77,7 @@ SIGNATURES = {
     "vsa_timing_read": ([I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I)], I),
 }
 
-KERNELS = ["permute", "coarse_topk", "fine_fwd", "combine", "bwd_prep", "coarse_bwd", "fine_bwd_kv", "finalize",
-           "fine_bwd_dq"]
+KERNELS = ["permute", "coarse_topk", "fine_fwd", "combine", "bwd_prep", "coarse_bwd", "fine_bwd_kv", "fine_bwd_dq"]
 
 _lib = None
 

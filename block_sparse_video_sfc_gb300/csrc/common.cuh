@@ -131,14 +131,34 @@ int launch_add_neighbors(const int32_t* idx_in, const int32_t* cnt_in, int kmax_
                          const int32_t* order, int radius, int kmax_out, int32_t* idx_out, int32_t* cnt_out,
                          cudaStream_t s);
 size_t fine_bwd_ws_bytes(int BH, int N, int kmax);
+// Where the fine backward kernels put their gradient rows.  With no
+// FusedGrads, fp32 rows in cube order into dq / dk / dv [BH*N, d].  With one,
+// the backward of the mean pool and the inverse reorder run in the kernels'
+// epilogues: row (cube c, slot o) plus c's coarse gradient divided by c's
+// token count goes to its native token of the grad_dtype outputs
+// [BH, T*H*W, d]; padding slots are dropped.
+struct FusedGrads {
+  void* dq;
+  void* dk;
+  void* dv;
+  const float* dqc;  // coarse gradients [BH, Nc, d], cube order
+  const float* dkc;
+  const float* dvc;
+  int grad_dtype;
+  CubeGrid grid;
+  const int32_t* order;  // cube order table, or null (raster)
+};
 int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* of, int of_dtype,
                     const float* lse, const void* dof, const int32_t* idx, const int32_t* cnt, int kmax, int BH,
                     int N, int d, float scale, float* dq, float* dk, float* dv, void* ws, size_t ws_bytes,
                     cudaStream_t s);
+// kv_after: an event the dK/dV kernel waits for on s_kv (its inverse lists
+// and plan do not), or null.
 int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const void* dof, const float* lse,
                          const float* delta, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
-                         float scale, float* dq, float* dk, float* dv, uint32_t* inv_ws, const int32_t* qpairs,
-                         int32_t* kpairs_ws, cudaStream_t s, cudaStream_t s_kv);
+                         float scale, float* dq, float* dk, float* dv, const FusedGrads* fused, uint32_t* inv_ws,
+                         const int32_t* qpairs, int32_t* kpairs_ws, cudaStream_t s, cudaStream_t s_kv,
+                         cudaEvent_t kv_after);
 int launch_combine(const float* oc, const float* of, const void* gc, const void* gf, void* out, int out_dtype,
                    int BH, int d, int T, int H, int W, const int32_t* order, cudaStream_t s);
 int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const float* oc, const float* of,
@@ -147,8 +167,5 @@ int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const floa
 int launch_coarse_bwd(const float* qc, const float* kc, const float* vc, const float* doc, const float* lse_c,
                       int BH, int Nc, int d, float scale, float* P, float* dS, float* dqc, float* dkc, float* dvc,
                       cudaStream_t s);
-int launch_finalize(const float* dqp, const float* dkp, const float* dvp, const float* dqc, const float* dkc,
-                    const float* dvc, void* dq, void* dk, void* dv, int grad_dtype, int BH, int d, int T, int H,
-                    int W, const int32_t* order, cudaStream_t s);
 
 }  // namespace vsa

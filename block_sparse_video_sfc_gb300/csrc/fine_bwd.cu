@@ -37,6 +37,12 @@
 // Operands are fp16 (exact for the bf16 inputs within +-65504), accumulation
 // fp32.  The inverse lists come from a bit matrix inv[bh][key cube][query
 // cube] built from the index list (workspace).
+//
+// Epilogues: each kernel writes its rows once.  For the whole VSA backward
+// they also finish the gradient: a row of cube c gets c's coarse-stage
+// gradient divided by c's token count (the backward of the mean pool) and
+// goes to its native token in the caller's dtype (the inverse reorder), so no
+// fp32 copy in cube order is written and read back.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -58,15 +64,54 @@ struct BwdParams {
   const uint32_t* inv;          // [BH][Nc][nwords]
   const int32_t* idx;           // forward index list [BH][Nc][kmax]
   const int32_t* cnt;           // [BH][Nc] or null (= kmax)
-  float* dq;
+  float* dq;                    // fp32 rows in cube order (fused == 0)
   float* dk;
   float* dv;
+  FusedGrads fused;             // fused pool backward + inverse reorder (fused.dq != null)
+  int64_t Nn;                   // tokens of one head's grid (fused)
   const int32_t* qpairs;        // [BH][npairs][2] query-cube tiles of the dQ kernel, or null (2t, 2t + 1)
   const int32_t* kpairs;        // [BH][npairs][2] key-cube tiles of the dK/dV kernel, or null
   int N, Nc, nwords, kmax, npairs;
   float scale, scale_log2;
   int* err;
 };
+
+// Destination of one gradient row (cube `cube`, slot `slot` of head bh).
+// Unfused: the fp32 row in cube order.  Fused: its native token (row -1 for a
+// padding slot), and the cube's coarse gradient row with 1 / token count.
+struct GradRow {
+  void* out;
+  int64_t row;
+  const float* coarse;
+  float inv_tokens;
+};
+// coarse_row: the cube's coarse gradient row (global or shared memory).
+__device__ __forceinline__ GradRow grad_row(const BwdParams& p, void* fused_out, float* cube_out,
+                                            const float* coarse_row, int64_t bh, int cube, int slot) {
+  if (!fused_out) return GradRow{cube_out, bh * p.N + 64 * static_cast<int64_t>(cube) + slot, nullptr, 0.f};
+  const int rc = raster_cube(p.fused.order, cube);
+  const int64_t tok = native_token(rc, slot, p.fused.grid);
+  return GradRow{fused_out, tok < 0 ? -1 : bh * p.Nn + tok, coarse_row,
+                 1.0f / static_cast<float>(cube_tokens(rc, p.fused.grid))};
+}
+// Columns [c, c + 32) of a gradient row (v is consumed).
+template <int D>
+__device__ __forceinline__ void store_grad32(const BwdParams& p, const GradRow& g, float* v, int c) {
+  if (g.row < 0) return;
+  if (!g.coarse) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) store8(g.out, g.row * D + c + i, v + i, VSA_DTYPE_F32);
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 32; i += 8) {
+    float cv[8];
+    load8_f32(g.coarse, c + i, cv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[i + e] += cv[e] * g.inv_tokens;
+    store8(g.out, g.row * D + c + i, v + i, p.fused.grad_dtype);
+  }
+}
 
 // The two cubes of tile `t`: from a pair plan (second -1: none), else 2t and
 // 2t + 1.  A plan entry out of range latches kErrLut and leaves one cube.
@@ -164,13 +209,18 @@ struct KvLayout {
 // TMEM: S^T 0 and dP^T 64 (64 fp32 columns each); P^T / dS^T buffer b at
 // 128 + 64 b (32 columns of fp16 pairs each: P^T, then dS^T); dV 256, dK 384.
 constexpr uint32_t kKvS = 0, kKvDP = 64, kKvPB = 128, kKvDV = 256, kKvDK = 384;
+template <int D>
+constexpr int kKvCoarseBytes = 4 * D * static_cast<int>(sizeof(float));  // crow (fused epilogue)
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using L = KvLayout<D>;
-  uint32_t* ulist = reinterpret_cast<uint32_t*>(sm + L::kEnd);
+  // The coarse dV and dK rows of the two key cubes, [cube][dV, dK][D], read
+  // by the fused epilogue (staged here so that it waits on no global load).
+  float* crow = reinterpret_cast<float*>(sm + L::kEnd);
+  uint32_t* ulist = reinterpret_cast<uint32_t*>(sm + L::kEnd + kKvCoarseBytes<D>);
   uint32_t* bitA = ulist + 2 * p.Nc + 2;
   uint32_t* bitB = bitA + p.nwords;
 
@@ -209,6 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
   if (warp == 0) {
     tmem_alloc(&tmem_base_sh, 512);
     tmem_relinquish();
+  }
+  if (p.fused.dk) {
+    for (int e = tid; e < 4 * D; e += kThreads) {
+      const int kc = e < 2 * D || !has_k2 ? k1 : k2;
+      const float* src = (((e / D) & 1) ? p.fused.dkc : p.fused.dvc) + (bh * p.Nc + kc) * D + (e % D);
+      crow[e] = *src;
+    }
   }
   {
     const uint32_t* ra = p.inv + (bh * p.Nc + k1) * p.nwords;
@@ -392,10 +449,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
     if (!ok) flag_error(p.err, kErrTimeout);
     tc_fence_after();
     // ---------------- dK, dV rows of this key pair (warpgroup 0: dV, 1: dK)
-    const int kc = r < 64 ? k1 : k2;
     const bool key_valid = r < 64 || has_k2;
-    const int64_t krow = row_base + 64 * static_cast<int64_t>(kc) + (r & 63);
-    float* outp = g == 0 ? p.dv : p.dk;
+    const int kc = r < 64 || !has_k2 ? k1 : k2;
+    const GradRow dst = grad_row(p, g == 0 ? p.fused.dv : p.fused.dk, g == 0 ? p.dv : p.dk,
+                                 crow + (2 * (r < 64 ? 0 : 1) + g) * D, bh, kc, r & 63);
     const float mul = g == 0 ? 1.0f : p.scale;
 #pragma unroll
     for (int c = 0; c < D; c += 32) {
@@ -409,10 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       float o[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(a[i]) * mul;
-      if (key_valid) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 8) store8(outp, krow * D + c + i, o + i, VSA_DTYPE_F32);
-      }
+      if (key_valid) store_grad32<D>(p, dst, o, c);
     }
   }
   tc_fence_before();
@@ -678,6 +732,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
     if (!ok) flag_error(p.err, kErrTimeout);
     tc_fence_after();
     // ---------------- dQ rows (warpgroup g writes columns [g*D/2, (g+1)*D/2))
+    const int qc = row < 64 || !has_b ? qa : qb;
+    const GradRow dst = grad_row(p, p.fused.dq, p.dq, p.fused.dqc + (bh * p.Nc + qc) * D, bh, qc, row & 63);
 #pragma unroll
     for (int c0 = 0; c0 < D / 2; c0 += 32) {
       const int c = g * (D / 2) + c0;
@@ -691,10 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(a[i]) * p.scale;
-      if (row_valid) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 8) store8(p.dq, grow * D + c + i, v + i, VSA_DTYPE_F32);
-      }
+      if (row_valid) store_grad32<D>(p, dst, v, c);
     }
   }
   tc_fence_before();
@@ -787,15 +840,18 @@ int launch_delta(const void* of, int of_dtype, const void* dof, int64_t rows, in
 }
 
 // Fine backward with the row statistics D given.  qp, kp, vp, dof are fp16
-// (cube order); inv_ws: scratch for the inverse-list bit matrix; qpairs: the
+// (cube order); fused: where the gradient rows go (null: fp32 dq, dk, dv in
+// cube order); inv_ws: scratch for the inverse-list bit matrix; qpairs: the
 // query-cube tiles of the dQ kernel (null: cubes 2t, 2t + 1); kpairs_ws:
 // scratch for the key-cube pair plan (null: cubes 2t, 2t + 1).  The inverse
-// lists, the key plan and the dK/dV kernel go on s_kv, the dQ kernel on s (the
-// two kernels are independent; s_kv may be s).
+// lists, the key plan and the dK/dV kernel go on s_kv (the kernel after
+// kv_after, when given), the dQ kernel on s (the two kernels are independent;
+// s_kv may be s).
 int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const void* dof, const float* lse,
                          const float* delta, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
-                         float scale, float* dq, float* dk, float* dv, uint32_t* inv_ws, const int32_t* qpairs,
-                         int32_t* kpairs_ws, cudaStream_t s, cudaStream_t s_kv) {
+                         float scale, float* dq, float* dk, float* dv, const FusedGrads* fused, uint32_t* inv_ws,
+                         const int32_t* qpairs, int32_t* kpairs_ws, cudaStream_t s, cudaStream_t s_kv,
+                         cudaEvent_t kv_after) {
   BwdParams p{};
   const int64_t rows = static_cast<int64_t>(BH) * N;
   int st;
@@ -812,6 +868,10 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
+  if (fused) {
+    p.fused = *fused;
+    p.Nn = static_cast<int64_t>(fused->grid.T) * fused->grid.H * fused->grid.W;
+  }
   p.N = N;
   p.Nc = Nc;
   p.nwords = nwords;
@@ -829,7 +889,8 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
     build_inverse_bits<<<static_cast<unsigned>((entries + 255) / 256), 256, 0, s_kv>>>(
         idx, cnt, kmax, Nc, nwords, static_cast<int64_t>(BH) * Nc, inv_ws, p.err);
   if (kpairs_ws && (st = launch_pair_plan(inv_ws, BH, Nc, kpairs_ws, s_kv)) != VSA_OK) return st;
-  const size_t kv_extra = sizeof(uint32_t) * (2 * Nc + 2 + 2 * nwords);
+  if (kv_after && cudaStreamWaitEvent(s_kv, kv_after, 0) != cudaSuccess) return VSA_ERR_CUDA;
+  const size_t kv_extra = sizeof(uint32_t) * (2 * Nc + 2 + 2 * nwords) + 4 * sizeof(float) * d;
   const size_t dq_extra = sizeof(uint32_t) * (2 * kmax + 2 + 2 * nwords);
   dim3 grid((Nc + 1) / 2, BH);
   auto go = [&](auto kernel, size_t bytes, cudaStream_t st_) -> int {
@@ -880,8 +941,8 @@ int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* 
   int32_t* kpairs = reinterpret_cast<int32_t*>(w);
   int st = launch_delta(of, of_dtype, h[3], rows, d, delta, s);
   if (st != VSA_OK) return st;
-  return launch_fine_bwd_core(h[0], h[1], h[2], h[3], lse, delta, idx, cnt, kmax, BH, N, d, scale, dq, dk, dv, inv_ws,
-                              nullptr, kpairs, s, s);
+  return launch_fine_bwd_core(h[0], h[1], h[2], h[3], lse, delta, idx, cnt, kmax, BH, N, d, scale, dq, dk, dv, nullptr,
+                              inv_ws, nullptr, kpairs, s, s, nullptr);
 }
 
 }  // namespace vsa

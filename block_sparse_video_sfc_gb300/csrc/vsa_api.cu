@@ -73,13 +73,12 @@ FwdWs fwd_layout(const Dims& D, int K, bool copies = true) {
 
 // Backward workspace (scratch of one vsa_backward call).
 struct BwdWs {
-  size_t dof, delta, doc, P, dS, dqc, dkc, dvc, dqp, dkp, dvp, inv, kpairs, total;
+  size_t dof, delta, doc, P, dS, dqc, dkc, dvc, inv, kpairs, total;
 };
 BwdWs bwd_layout(const Dims& D) {
   BwdWs w{};
   size_t o = 0;
   const size_t pooled = sizeof(float) * D.BH * D.Nc * D.d;
-  const size_t big_f32 = sizeof(float) * D.BH * D.N * D.d;
   const int64_t nwords = (D.Nc + 31) / 32;
   w.dof = o; o += align256(sizeof(__half) * D.BH * D.N * D.d);
   w.delta = o; o += align256(sizeof(float) * D.BH * D.N);
@@ -89,9 +88,6 @@ BwdWs bwd_layout(const Dims& D) {
   w.dqc = o; o += align256(pooled);
   w.dkc = o; o += align256(pooled);
   w.dvc = o; o += align256(pooled);
-  w.dqp = o; o += align256(big_f32);
-  w.dkp = o; o += align256(big_f32);
-  w.dvp = o; o += align256(big_f32);
   w.inv = o; o += align256(sizeof(uint32_t) * D.BH * D.Nc * nwords);
   w.kpairs = o; o += align256(pair_plan_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.Nc)));
   w.total = o;
@@ -159,13 +155,13 @@ int* device_error_word() {
 }
 
 // Per device, a stream of the highest priority for the dK/dV chain of
-// vsa_backward and the events of its fork from and join to the caller's
-// stream (created on first use).  At that priority the block scheduler runs
-// dK/dV first and the dQ kernel and the coarse backward, queued on the
-// caller's stream, fill the SMs that the dK/dV kernel's last wave leaves idle.
+// vsa_backward and the events of its fork from, wait on and join to the
+// caller's stream (created on first use).  At that priority the block
+// scheduler runs dK/dV first and the dQ kernel, queued on the caller's
+// stream, fills the SMs that the dK/dV kernel's last wave leaves idle.
 struct AuxStream {
   cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, mid = nullptr;
   std::mutex mu;  // one fork / join at a time per device (the events are shared)
 };
 AuxStream g_aux[kMaxDevices];
@@ -178,19 +174,22 @@ AuxStream* aux_stream() {
   if (!a.s) {
     int least = 0, greatest = 0;
     cudaStream_t st = nullptr;
-    cudaEvent_t e1 = nullptr, e2 = nullptr;
+    cudaEvent_t e1 = nullptr, e2 = nullptr, e3 = nullptr;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
         cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest) != cudaSuccess ||
         cudaEventCreateWithFlags(&e1, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&e2, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventCreateWithFlags(&e2, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&e3, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();  // not fatal: the backward then runs on the caller's stream alone
       if (st) cudaStreamDestroy(st);
       if (e1) cudaEventDestroy(e1);
       if (e2) cudaEventDestroy(e2);
+      if (e3) cudaEventDestroy(e3);
       return nullptr;
     }
     a.fork = e1;
     a.join = e2;
+    a.mid = e3;
     a.s = st;
   }
   return &a;
@@ -540,14 +539,13 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
   FwdWs f = fwd_layout(D, topk);
   cudaStream_t s = as_stream(stream);
   const int BH = static_cast<int>(D.BH), Nc = static_cast<int>(D.Nc), N = static_cast<int>(D.N);
-  if ((st = launch_bwd_prep(dout, g_coarse, g_fine, at<float>(fwd_ws, f.oc), at<float>(fwd_ws, f.of),
-                            at<__half>(ws, w.dof), at<float>(ws, w.delta), at<float>(ws, w.doc),
-                            g_coarse ? dg_coarse : nullptr, g_fine ? dg_fine : nullptr, grad_dtype, BH, d, g.T, g.H,
-                            g.W, g.cube_order, s)) != VSA_OK)
-    return st;
-  // Fork: the dK/dV chain on the auxiliary stream (highest priority), the
-  // coarse backward and the dQ kernel on the caller's stream; join before the
-  // finalize.  Without an auxiliary stream everything runs on s.
+  // Fork at the start: the dK/dV chain on the auxiliary stream (highest
+  // priority), whose inverse lists and key plan need only the forward's index
+  // lists and so run beside the combine backward; the dK/dV kernel itself
+  // waits for the coarse backward (its epilogue adds dK_c, dV_c).  The combine
+  // backward, the coarse backward and the dQ kernel run on the caller's
+  // stream, which joins the chain at the end.  Without an auxiliary stream
+  // everything runs on s.
   AuxStream* aux = aux_stream();
   std::unique_lock<std::mutex> fork_lock;
   cudaStream_t s_kv = s;
@@ -557,23 +555,35 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
       return VSA_ERR_CUDA;
     s_kv = aux->s;
   }
+  if ((st = launch_bwd_prep(dout, g_coarse, g_fine, at<float>(fwd_ws, f.oc), at<float>(fwd_ws, f.of),
+                            at<__half>(ws, w.dof), at<float>(ws, w.delta), at<float>(ws, w.doc),
+                            g_coarse ? dg_coarse : nullptr, g_fine ? dg_fine : nullptr, grad_dtype, BH, d, g.T, g.H,
+                            g.W, g.cube_order, s)) != VSA_OK)
+    return st;
   if ((st = launch_coarse_bwd(at<float>(fwd_ws, f.qc), at<float>(fwd_ws, f.kc), at<float>(fwd_ws, f.vc),
                               at<float>(ws, w.doc), at<float>(fwd_ws, f.lsec), BH, Nc, d, scale, at<float>(ws, w.P),
                               at<float>(ws, w.dS), at<float>(ws, w.dqc), at<float>(ws, w.dkc), at<float>(ws, w.dvc),
                               s)) != VSA_OK)
     return st;
+  if (aux && cudaEventRecord(aux->mid, s) != cudaSuccess) return VSA_ERR_CUDA;
+  FusedGrads fg{dq,
+                dk,
+                dv,
+                at<float>(ws, w.dqc),
+                at<float>(ws, w.dkc),
+                at<float>(ws, w.dvc),
+                grad_dtype,
+                cube_grid(g.T, g.H, g.W),
+                g.cube_order};
   if ((st = launch_fine_bwd_core(at<void>(fwd_ws, f.qp), at<void>(fwd_ws, f.kp), at<void>(fwd_ws, f.vp),
                                  at<void>(ws, w.dof), at<float>(fwd_ws, f.lse), at<float>(ws, w.delta),
                                  at<int32_t>(fwd_ws, f.idx), at<int32_t>(fwd_ws, f.cnt), topk, BH, N, d, scale,
-                                 at<float>(ws, w.dqp), at<float>(ws, w.dkp), at<float>(ws, w.dvp),
-                                 at<uint32_t>(ws, w.inv), at<int32_t>(fwd_ws, f.pairs), at<int32_t>(ws, w.kpairs),
-                                 s, s_kv)) != VSA_OK)
+                                 nullptr, nullptr, nullptr, &fg, at<uint32_t>(ws, w.inv), at<int32_t>(fwd_ws, f.pairs),
+                                 at<int32_t>(ws, w.kpairs), s, s_kv, aux ? aux->mid : nullptr)) != VSA_OK)
     return st;
   if (aux && (cudaEventRecord(aux->join, s_kv) != cudaSuccess || cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess))
     return VSA_ERR_CUDA;
-  return launch_finalize(at<float>(ws, w.dqp), at<float>(ws, w.dkp), at<float>(ws, w.dvp), at<float>(ws, w.dqc),
-                         at<float>(ws, w.dkc), at<float>(ws, w.dvc), dq, dk, dv, grad_dtype, BH, d, g.T, g.H, g.W,
-                         g.cube_order, s);
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
 }  // extern "C"

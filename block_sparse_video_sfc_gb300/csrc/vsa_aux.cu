@@ -6,8 +6,8 @@
 //   bwd_prep  backward of the combine: dO to cube order, dO_f = g_f * dO
 //             (fp16 for the fine backward), D = dO_f . O_f, dO_c = sum over the
 //             cube of g_c * dO, and the gate gradients.
-//   finalize  mean-pool backward (+ dXc / 64 to every token of a cube) and
-//             the inverse reordering of dQ, dK, dV.
+// (The mean-pool backward and the inverse reordering of dQ, dK, dV run in
+// the epilogues of the fine backward kernels.)
 // The backward pass follows "VSA: Faster Video Diffusion with Trainable Sparse
 // Attention" (Abstract: trained end to end); derivatives are the textbook ones.
 // The per-cube kernels use one CTA per cube of one tensor, 16-byte accesses.
@@ -122,43 +122,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   }
 }
 
-// ---------------------------------------------------------------- finalize
-struct FinalizeArgs {
-  const float* fine[3];
-  const float* pooled[3];
-  void* out[3];
-};
-
-template <int D>
-__global__ void __launch_bounds__(256) finalize_kernel(FinalizeArgs a, int grad_dtype, int Nc, CubeGrid g, int64_t Nn,
-                                                       const int32_t* __restrict__ order) {
-  constexpr int kChunks = D / 8, kTok = 256 / kChunks, kPasses = kCube / kTok;
-  const int t = blockIdx.y;
-  const int64_t cg = blockIdx.x;
-  const int64_t bh = cg / Nc;
-  const int cube = static_cast<int>(cg % Nc);
-  const int rcube = raster_cube(order, cube);
-  const int j = threadIdx.x % kChunks, o0 = threadIdx.x / kChunks;
-  float c[8];
-  load8_f32(a.pooled[t], cg * D + j * 8, c);
-  const float inv_tokens = 1.0f / static_cast<float>(cube_tokens(rcube, g));
-#pragma unroll
-  for (int e = 0; e < 8; ++e) c[e] *= inv_tokens;
-#pragma unroll
-  for (int p = 0; p < kPasses; ++p) {
-    const int o = o0 + p * kTok;
-    const int64_t tok = native_token(rcube, o, g);
-    if (tok < 0) continue;  // padding slot
-    const int64_t nat = bh * Nn + tok;
-    const int64_t cub = (bh * Nc + cube) * kCube + o;
-    float f[8];
-    load8_f32(a.fine[t], cub * D + j * 8, f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] += c[e];
-    store8(a.out[t], nat * D + j * 8, f, grad_dtype);
-  }
-}
-
 }  // namespace
 
 int launch_combine(const float* oc, const float* of, const void* gc, const void* gf, void* out, int out_dtype, int BH,
@@ -196,23 +159,6 @@ int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const floa
     bwd_prep_kernel<64><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, cg, Nn, order,
                                              device_error_word());
   timing_mark(VSA_K_BWD_PREP, false, s);
-  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
-}
-
-int launch_finalize(const float* dqp, const float* dkp, const float* dvp, const float* dqc, const float* dkc,
-                    const float* dvc, void* dq, void* dk, void* dv, int grad_dtype, int BH, int d, int T, int H,
-                    int W, const int32_t* order, cudaStream_t s) {
-  const CubeGrid cg = cube_grid(T, H, W);
-  const int Nc = ((T + 3) / 4) * cg.Hc * cg.Wc;
-  const int64_t Nn = static_cast<int64_t>(T) * H * W;
-  FinalizeArgs a{{dqp, dkp, dvp}, {dqc, dkc, dvc}, {dq, dk, dv}};
-  dim3 grid(static_cast<unsigned>(static_cast<int64_t>(BH) * Nc), 3);
-  timing_mark(VSA_K_FINALIZE, true, s);
-  if (d == 128)
-    finalize_kernel<128><<<grid, 256, 0, s>>>(a, grad_dtype, Nc, cg, Nn, order);
-  else
-    finalize_kernel<64><<<grid, 256, 0, s>>>(a, grad_dtype, Nc, cg, Nn, order);
-  timing_mark(VSA_K_FINALIZE, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 

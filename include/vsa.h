@@ -256,10 +256,12 @@ int vsa_forward_inference(const void* q, const void* k, const void* v, const voi
  *   dg_coarse, dg_fine  [B, heads, N, d] native, dtype grad_dtype; may be NULL,
  *               and are ignored when the matching gate is NULL.
  *   ws          workspace of vsa_workspace_bytes(VSA_OP_BACKWARD, ...) bytes.
- * The dK/dV kernel runs on a library-owned stream of the highest priority
- * (one per device, created on first use), forked from `stream` by an event
- * and joined back into it before the call's last kernel; the dQ kernel runs
- * on `stream` beside it.  To the caller this is ordinary stream-ordered work
+ * The fine backward kernels finish the gradients in their epilogues (the
+ * backward of the mean pool and the inverse reorder), so dq, dk, dv are
+ * written once, by them.  The dK/dV kernel runs on a library-owned stream of
+ * the highest priority (one per device, created on first use), forked from
+ * `stream` by an event at the start of the call and joined back into it at
+ * the end; the dQ kernel runs on `stream` beside it.  To the caller this is ordinary stream-ordered work
  * (it also records into a CUDA graph).  Calls on one device that overlap in
  * time from several host threads take their turn at the fork.
  */
@@ -309,9 +311,8 @@ enum {
     VSA_K_BWD_PREP = 4,    /* backward of the combine */
     VSA_K_COARSE_BWD = 5,  /* coarse backward (three kernels) */
     VSA_K_FINE_BWD = 6,    /* tcgen05 fine backward, dK/dV kernel */
-    VSA_K_FINALIZE = 7,    /* pool backward + inverse reorder */
-    VSA_K_FINE_BWD_DQ = 8, /* tcgen05 fine backward, dQ kernel */
-    VSA_K_COUNT = 9
+    VSA_K_FINE_BWD_DQ = 7, /* tcgen05 fine backward, dQ kernel */
+    VSA_K_COUNT = 8
 };
 int vsa_timing_enable(int on);
 int vsa_timing_read(int kernel, double* total_ms, int* launches);

@@ -46,7 +46,9 @@ def test_workspace_bytes(lib):
     fwd = L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 154)
     N, Nc = 32768, 512
     assert fwd >= 12 * N * 128 * (3 * 2 + 4)   # permuted Q/K/V + fp32 O_f at least
-    assert L.vsa_workspace_bytes(lib.VSA_OP_BACKWARD, 1, 12, 128, g, 154) > 12 * N * 128 * 12
+    bwd = L.vsa_workspace_bytes(lib.VSA_OP_BACKWARD, 1, 12, 128, g, 154)
+    # fp16 dO_f plus per-row and per-cube scratch; the fine gradients go straight to the outputs
+    assert 12 * N * 128 * 2 < bwd < 12 * N * 128 * 3
     assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 0) == 0        # K < 1
     assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, Nc + 1) == 0   # K > Nc
     assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 96, g, 4) == 0         # d
