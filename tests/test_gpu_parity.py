@@ -510,6 +510,31 @@ def test_full_size_wan_latent(vsa, oracle_mod):
     _sampled_checks(vsa, oracle_mod, synth.WORKLOADS["wan1.3b_latent"], torch.float32)
 
 
+@pytest.mark.parametrize("name,curve,dtype", [("odd", "hilbert", torch.bfloat16), ("odd_small", "raster", torch.float32),
+                                              ("small", "hilbert", torch.float32), ("wan1.3b", "raster", torch.bfloat16)])
+def test_every_output_element_is_written(vsa, name, curve, dtype):
+    """out, dq, dk, dv, dg_c, dg_f are written in full by the library (the
+    gradients by the fine backward epilogues, each native token once, padding
+    slots never): buffers pre-filled with NaN come back finite and equal, bit
+    for bit, to a run into zero-filled buffers."""
+    wl = synth.WORKLOADS[name]
+    order = None if curve == "raster" else vsa.cube_order(wl.T, wl.H, wl.W, curve)
+    q, k, v = (dev(a) for a in synth.make_qkv(wl))
+    gc, gf = (dev(a) for a in synth.make_gates(wl))
+    dout = dev(synth.make_dout(wl))
+    runs = []
+    for fill in (float("nan"), 0.0):
+        out = torch.full_like(q, fill, dtype=dtype)
+        _, st = vsa.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, g_coarse=gc, g_fine=gf, out=out, cube_order=order)
+        grads = {n: torch.full_like(q, fill, dtype=dtype) for n in ("dq", "dk", "dv", "dgc", "dgf")}
+        vsa.backward(st, dout, g_coarse=gc, g_fine=gf, grads=grads)
+        status_ok(vsa)
+        runs.append([out] + [grads[n] for n in ("dq", "dk", "dv", "dgc", "dgf")])
+    for a, b in zip(*runs):
+        assert bool(torch.isfinite(a).all())
+        assert torch.equal(a, b)
+
+
 # ---------------------------------------------------------------- CUDA graphs
 def test_forward_backward_capture_in_a_cuda_graph(vsa, oracle_mod):
     """The forward and backward enqueue only stream work (no host sync, no
