@@ -1,0 +1,206 @@
+"""CPU model of the barrier protocol of the fine forward kernel (fine_fwd_kernel).
+
+Roles, as in the kernel: a TMA producer (K(j) into ring stage j % nk, V(j)
+into stage j % nv, K(j + 1) requested before V(j)), one MMA-issuing thread,
+and eight softmax warps, two per TMEM lane quarter.  Barriers:
+  bar_qt        Q rows written into TMEM          (256 softmax threads)
+  kfull/vfull   ring stage landed                 (TMA)
+  kfree/vfree   S(j) / PV(j) that read the stage done   (commits)
+  bar_s         S(j) done                         (commit)
+  s_free        S(j) read into registers          (256 softmax threads)
+  pair_bar[q]   row-max exchange of quarter q     (its two warps, 64 threads)
+  bar_p[b]      P(j) written into P buffer b = j % 2   (256 threads)
+  pv_done[b]    PV(j) done                        (commit)
+A softmax warp that raises its row max first waits for PV(j - 1) and then
+rescales O; before writing P(j) it waits for PV(j - 2), the last reader of
+that P buffer.  The model asserts the parity rule (a wait for phase k sees k
+or k + 1 completed phases), that no ring stage, S buffer or P buffer is
+overwritten before its reader is done, that PV(j) reads a complete P(j), that
+O is rescaled only with PV(0..j-1) done and PV(j) not yet issued, and that
+every schedule of random delays terminates.
+"""
+import random
+
+import pytest
+
+WARPS = 8          # softmax warps; warp w is in lane quarter w % 4
+THREADS = 32 * WARPS
+
+
+def delay(rnd, hi):
+    """Mostly short, sometimes long: a late TMA tile or a slow MMA group."""
+    return rnd.randint(1, hi) if rnd.random() < 0.85 else rnd.randint(4 * hi, 12 * hi)
+
+
+class Barrier:
+    def __init__(self, name, count):
+        self.name, self.count, self.arrived, self.phases = name, count, 0, 0
+
+    def arrive(self, n=1):
+        self.arrived += n
+        assert self.arrived <= self.count, self.name
+        if self.arrived == self.count:
+            self.arrived = 0
+            self.phases += 1
+
+    def test(self, k):
+        assert k <= self.phases <= k + 1, (self.name, k, self.phases)
+        return self.phases > k
+
+
+def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
+    """drop: waits left out on purpose (to show the model catches them)."""
+    rnd = random.Random(seed)
+    bar_qt = Barrier("bar_qt", THREADS)
+    kfull = [Barrier(f"kfull{i}", 1) for i in range(nk)]
+    kfree = [Barrier(f"kfree{i}", 1) for i in range(nk)]
+    vfull = [Barrier(f"vfull{i}", 1) for i in range(nv)]
+    vfree = [Barrier(f"vfree{i}", 1) for i in range(nv)]
+    bar_s, s_free = Barrier("bar_s", 1), Barrier("s_free", THREADS)
+    pair = [Barrier(f"pair{q}", 64) for q in range(4)]
+    bar_p = [Barrier(f"bar_p{i}", THREADS) for i in range(2)]
+    pv_done = [Barrier(f"pv_done{i}", 1) for i in range(2)]
+
+    kring = [None] * nk            # stage -> [step, consumed]
+    vring = [None] * nv
+    s_buf = None                   # [step, set of warps that read it]
+    p_buf = [None, None]           # buffer -> [step, warps that wrote it, consumed]
+    pv_completed = -1              # last PV completed (in order)
+    pv_issued = -1
+    rescale = {}                   # (step, quarter) -> bool, the same for both warps of a quarter
+    pipe, loads = [], []
+
+    # producer program: K0, then per j: K(j+1), V(j)
+    prog = [("K", 0)] if steps else []
+    for j in range(steps):
+        if j + 1 < steps:
+            prog.append(("K", j + 1))
+        prog.append(("V", j))
+    pc = 0
+    ns = npv = 0
+    qt_ok = False
+    warp_j = [0] * WARPS
+    warp_pc = [0] * WARPS          # 0 wait S, 1 arrive pair, 2 wait pair, 3 rescale, 4 write P
+    warp_qt = [False] * WARPS
+
+    for tick in range(max_ticks):
+        # tensor pipe, in order
+        if pipe:
+            pipe[0][2] -= 1
+            if pipe[0][2] <= 0:
+                kind, j, _, bars = pipe.pop(0)
+                if kind == "S":
+                    st = j % nk
+                    assert kring[st] is not None and kring[st][0] == j, ("K stage", kring[st], j)
+                    assert s_buf is None or len(s_buf[1]) == WARPS, ("S overwritten unread", s_buf, j)
+                    kring[st][1] = True
+                    s_buf = [j, set()]
+                else:
+                    st, b = j % nv, j & 1
+                    assert vring[st] is not None and vring[st][0] == j, ("V stage", vring[st], j)
+                    assert p_buf[b] is not None and p_buf[b][0] == j and len(p_buf[b][1]) == WARPS, \
+                        ("PV reads incomplete P", p_buf[b], j)
+                    vring[st][1] = True
+                    p_buf[b][2] = True
+                    assert pv_completed == j - 1
+                    pv_completed = j
+                for bar in bars:
+                    bar.arrive()
+        for ld in list(loads):
+            ld[2] -= 1
+            if ld[2] <= 0:
+                loads.remove(ld)
+                kind, j = ld[0], ld[1]
+                ring, depth = (kring, nk) if kind == "K" else (vring, nv)
+                st = j % depth
+                assert ring[st] is None or ring[st][1], (kind, "stage overwritten before read", ring[st], j)
+                ring[st] = [j, False]
+                (kfull if kind == "K" else vfull)[st].arrive()
+        # producer
+        if pc < len(prog) and rnd.random() < 0.5:
+            kind, j = prog[pc]
+            depth, free = (nk, kfree) if kind == "K" else (nv, vfree)
+            st, use = j % depth, j // depth
+            if use == 0 or (kind == "K" and "kfree" in drop) or free[st].test(use - 1):
+                loads.append([kind, j, delay(rnd, 10)])
+                pc += 1
+        # issuer
+        if steps and rnd.random() < 0.7:
+            if not qt_ok:
+                qt_ok = bar_qt.test(0)
+            elif ns < steps and (ns == 0 or "s_free" in drop or s_free.test(ns - 1)) and \
+                    kfull[ns % nk].test(ns // nk):
+                pipe.append(["S", ns, delay(rnd, 6), [bar_s, kfree[ns % nk]]])
+                ns += 1
+            elif npv < ns and bar_p[npv & 1].test(npv >> 1) and vfull[npv % nv].test(npv // nv):
+                pipe.append(["PV", npv, delay(rnd, 6), [vfree[npv % nv], pv_done[npv & 1]]])
+                pv_issued = npv
+                npv += 1
+        # softmax warps
+        for w in range(WARPS):
+            if rnd.random() > 0.35:
+                continue
+            q = w % 4
+            if not warp_qt[w]:
+                warp_qt[w] = True
+                bar_qt.arrive(32)
+                continue
+            j = warp_j[w]
+            if j >= steps:
+                continue
+            if warp_pc[w] == 0:
+                if bar_s.test(j):
+                    assert s_buf is not None and s_buf[0] == j, ("S buffer", s_buf, j)
+                    s_buf[1].add(w)
+                    s_free.arrive(32)
+                    warp_pc[w] = 1
+            elif warp_pc[w] == 1:
+                pair[q].arrive(32)
+                warp_pc[w] = 2
+            elif warp_pc[w] == 2:
+                if pair[q].test(j):
+                    rescale.setdefault((j, q), j > 0 and rnd.random() < 0.3)
+                    warp_pc[w] = 3
+            elif warp_pc[w] == 3:
+                if not rescale[(j, q)]:
+                    warp_pc[w] = 4
+                elif "rescale" in drop or pv_done[(j - 1) & 1].test((j - 1) >> 1):
+                    assert pv_completed >= j - 1 and pv_issued < j, ("rescale of O", pv_completed, pv_issued, j)
+                    warp_pc[w] = 4
+            elif warp_pc[w] == 4:
+                b = j & 1
+                if j < 2 or "p_free" in drop or pv_done[b].test((j >> 1) - 1):
+                    if p_buf[b] is not None and p_buf[b][0] != j:
+                        assert p_buf[b][2], ("P overwritten before PV read it", p_buf[b], j)
+                        p_buf[b] = None
+                    if p_buf[b] is None:
+                        p_buf[b] = [j, set(), False]
+                    p_buf[b][1].add(w)
+                    bar_p[b].arrive(32)
+                    warp_j[w] += 1
+                    warp_pc[w] = 0
+        if steps == 0:
+            return tick
+        if npv == steps and not pipe and all(x == steps for x in warp_j):
+            assert pv_done[(steps - 1) & 1].test((steps - 1) >> 1)   # epilogue wait
+            return tick
+    raise AssertionError(f"no progress: steps={steps} nk={nk} nv={nv} seed={seed} ns={ns} npv={npv} warps={warp_j}")
+
+
+@pytest.mark.parametrize("nk,nv", [(1, 1), (2, 1), (2, 2), (3, 3), (3, 2)])
+@pytest.mark.parametrize("steps", [0, 1, 2, 3, 4, 7, 12, 31])
+def test_fwd_protocol_random_schedules(nk, nv, steps):
+    for seed in range(12):
+        simulate(steps, nk, nv, seed)
+
+
+@pytest.mark.parametrize("drop", ["kfree", "s_free", "rescale", "p_free"])
+def test_model_catches_each_missing_wait(drop):
+    """Leaving out any one of the waits makes some schedule fail."""
+    caught = 0
+    for seed in range(60):
+        try:
+            simulate(12, 2, 2, seed, max_ticks=50000, drop=(drop,))
+        except AssertionError:
+            caught += 1
+    assert caught > 0, drop

@@ -22,6 +22,11 @@ import pytest
 STAGES = 4
 
 
+def delay(rnd, hi):
+    """Mostly short, sometimes long: a late TMA tile or a slow MMA group."""
+    return rnd.randint(1, hi) if rnd.random() < 0.85 else rnd.randint(4 * hi, 12 * hi)
+
+
 class Barrier:
     def __init__(self, name, count):
         self.name, self.count, self.arrived, self.phases = name, count, 0, 0
@@ -73,15 +78,15 @@ def simulate(steps, seed, max_ticks=200000):
         if produced < steps and rnd.random() < 0.5:   # producer
             st = produced % STAGES
             if produced < STAGES or stage_free[st].test(produced // STAGES - 1):
-                loads.append([st, rnd.randint(1, 8)])
+                loads.append([st, delay(rnd, 8)])
                 produced += 1
         if rnd.random() < 0.7:                        # MMA issuer
             if ns < steps and (ns < 2 or buf_free[ns & 1].test((ns >> 1) - 1)) and \
                     full[ns % STAGES].test(ns // STAGES):
-                pipe.append(["S", ns, rnd.randint(1, 5), [s_done[ns & 1]]])
+                pipe.append(["S", ns, delay(rnd, 5), [s_done[ns & 1]]])
                 ns += 1
             elif ng < ns and pds[ng & 1].test(ng >> 1):
-                pipe.append(["G", ng, rnd.randint(1, 5), [stage_free[ng % STAGES], buf_free[ng & 1]]])
+                pipe.append(["G", ng, delay(rnd, 5), [stage_free[ng % STAGES], buf_free[ng & 1]]])
                 ng += 1
         for g in range(2):                            # compute warpgroups
             j = computed[g]
