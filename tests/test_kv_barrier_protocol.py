@@ -44,7 +44,8 @@ class Barrier:
         return self.phases > k
 
 
-def simulate(steps, seed, max_ticks=200000):
+def simulate(steps, seed, max_ticks=200000, drop=()):
+    """drop: waits left out on purpose (to show the model catches them)."""
     rnd = random.Random(seed)
     full = [Barrier(f"full{i}", 1) for i in range(STAGES)]
     stage_free = [Barrier(f"stage_free{i}", 1) for i in range(STAGES)]
@@ -52,6 +53,7 @@ def simulate(steps, seed, max_ticks=200000):
     pds = [Barrier(f"pds{i}", 2) for i in range(2)]
     buf_free = [Barrier(f"buf_free{i}", 1) for i in range(2)]
     tmem = [None, None]          # buffer -> (content, step)
+    ring = [None] * STAGES       # stage -> [step, read by dV/dK]
     wrote = set()                # (step, warpgroup) that wrote P^T / dS^T
     pipe, loads = [], []         # in-order MMA groups; TMA loads in flight
     produced = ns = ng = 0
@@ -62,26 +64,31 @@ def simulate(steps, seed, max_ticks=200000):
             if pipe[0][2] <= 0:
                 kind, j, _, bars = pipe.pop(0)
                 b = j & 1
+                assert ring[j % STAGES] is not None and ring[j % STAGES][0] == j, ("ring", ring[j % STAGES], j)
                 if kind == "S":
                     assert tmem[b] is None or tmem[b] == ("read", j - 2), (tmem[b], j)
                     tmem[b] = ("S", j)
                 else:
                     assert tmem[b] == ("P", j), (tmem[b], j)
                     tmem[b] = ("read", j)
+                    ring[j % STAGES][1] = True
                 for bar in bars:
                     bar.arrive()
         for load in list(loads):  # TMA completions
             load[1] -= 1
             if load[1] <= 0:
                 loads.remove(load)
-                full[load[0]].arrive()
+                st, j = load[0], load[2]
+                assert ring[st] is None or ring[st][1], ("ring stage overwritten before dV/dK read it", ring[st], j)
+                ring[st] = [j, False]
+                full[st].arrive()
         if produced < steps and rnd.random() < 0.5:   # producer
             st = produced % STAGES
-            if produced < STAGES or stage_free[st].test(produced // STAGES - 1):
-                loads.append([st, delay(rnd, 8)])
+            if produced < STAGES or "stage_free" in drop or stage_free[st].test(produced // STAGES - 1):
+                loads.append([st, delay(rnd, 8), produced])
                 produced += 1
         if rnd.random() < 0.7:                        # MMA issuer
-            if ns < steps and (ns < 2 or buf_free[ns & 1].test((ns >> 1) - 1)) and \
+            if ns < steps and (ns < 2 or "buf_free" in drop or buf_free[ns & 1].test((ns >> 1) - 1)) and \
                     full[ns % STAGES].test(ns // STAGES):
                 pipe.append(["S", ns, delay(rnd, 5), [s_done[ns & 1]]])
                 ns += 1
@@ -112,44 +119,14 @@ def test_kv_protocol_random_schedules(steps):
         simulate(steps, seed)
 
 
-def test_model_catches_a_missing_buffer_wait():
-    """The model is not vacuous: issuing S^T(j) without waiting for
-    buf_free (dV/dK(j - 2)) is caught as an overwrite of unread P^T."""
+@pytest.mark.parametrize("drop", ["buf_free", "stage_free"])
+def test_model_catches_each_missing_wait(drop):
+    """The model is not vacuous: leaving out the wait for the buffer's last
+    reader, or for the ring stage's, makes some schedule fail."""
     caught = 0
-    for seed in range(40):
+    for seed in range(60):
         try:
-            _simulate_without_buf_free(12, seed)
+            simulate(12, seed, max_ticks=50000, drop=(drop,))
         except AssertionError:
             caught += 1
-    assert caught > 0
-
-
-def _simulate_without_buf_free(steps, seed):
-    rnd = random.Random(seed)
-    s_done = [Barrier(f"s_done{i}", 1) for i in range(2)]
-    tmem = [None, None]
-    pipe, ns, ng, computed = [], 0, 0, 0
-    ready = set()
-    for _ in range(20000):
-        if pipe:
-            pipe[0][2] -= 1
-            if pipe[0][2] <= 0:
-                kind, j, _ = pipe.pop(0)
-                b = j & 1
-                if kind == "S":
-                    assert tmem[b] is None or tmem[b] == ("read", j - 2), (tmem[b], j)
-                    tmem[b] = ("S", j)
-                    s_done[b].phases += 1
-                else:
-                    tmem[b] = ("read", j)
-        if ns < steps and rnd.random() < 0.9:        # no buf_free wait
-            pipe.append(["S", ns, rnd.randint(1, 3)])
-            ns += 1
-        if computed < steps and rnd.random() < 0.2 and s_done[computed & 1].phases > computed >> 1:
-            ready.add(computed)
-            computed += 1
-        if ng in ready and rnd.random() < 0.5:
-            pipe.append(["G", ng, rnd.randint(1, 3)])
-            ng += 1
-        if ng == steps and not pipe:
-            return
+    assert caught > 0, drop
