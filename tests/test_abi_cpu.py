@@ -91,3 +91,14 @@ def test_host_side_argument_errors(lib):
                          None) == lib.VSA_ERR_ARG
     assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, 0.125, fake2, fake2, fake2, None, None, 3,
                           fake2, 1 << 30, None) == lib.VSA_ERR_ARG
+    # backward: workspace too small, null or misaligned outputs, Top-K out of range
+    bf16 = lib.VSA_DTYPE_BF16
+    assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, 0.125, fake2, fake2, fake2, None, None, bf16,
+                          fake2, 16, None) == lib.VSA_ERR_WORKSPACE
+    assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, 0.125, None, fake2, fake2, None, None, bf16,
+                          fake2, 1 << 30, None) == lib.VSA_ERR_ARG
+    assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, 0.125, fake2, ctypes.c_void_p(0x2008), fake2,
+                          None, None, bf16, fake2, 1 << 30, None) == lib.VSA_ERR_ARG
+    for K in (0, 5):
+        assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, K, 0.125, fake2, fake2, fake2, None, None, bf16,
+                              fake2, 1 << 30, None) == lib.VSA_ERR_ARG
