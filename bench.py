@@ -106,6 +106,33 @@ def step_flops(wl: synth.Workload) -> dict:
     return dict(fine_fwd=fine_fwd, fine_bwd=fine_bwd, coarse=coarse, total=fine_fwd + fine_bwd + coarse)
 
 
+def kernel_flops(wl: synth.Workload) -> dict:
+    """Work each fine kernel does per launch, in products of 2*N*64K*d FLOP per
+    (batch, head): forward S and PV (2); backward dK/dV kernel S^T, dP^T, dV,
+    dK (4); dQ kernel S, dP, dQ (3).  The effective metric counts 2 + 5: of the
+    dQ kernel only its dQ product (dq_product) is new work."""
+    unit = 2.0 * wl.N * (wl.topk * wl.N / wl.Nc) * wl.d * wl.BH
+    return {"fine_fwd": 2 * unit, "fine_bwd_kv": 4 * unit, "fine_bwd_dq": 3 * unit, "dq_product": unit}
+
+
+def roof(flops: float, ms: float, peak: float) -> dict:
+    a = flops / (ms * 1e-3) / 1e12
+    return {"ms": round(ms, 4), "tflops": round(a, 2), "frac": round(a / peak, 4), "flops_per_launch": flops}
+
+
+def fine_bwd_wall(per_kernel: dict) -> tuple:
+    """(ms, overlapped): the fine backward's wall time per step.  vsa_backward
+    runs the dK/dV kernel on a higher-priority stream of its own while the
+    coarse backward and then the dQ kernel run on the caller's stream, filling
+    the SMs the dK/dV kernel leaves; the coarse and dQ event pairs then follow
+    one another on the caller's stream and together span the fine backward
+    (the coarse backward included).  Back to back, the two kernel intervals add."""
+    overlapped = per_kernel["fine_bwd_dq"] > per_kernel["fine_bwd_kv"]
+    ms = (per_kernel["coarse_bwd"] + per_kernel["fine_bwd_dq"] if overlapped
+          else per_kernel["fine_bwd_kv"] + per_kernel["fine_bwd_dq"])
+    return ms, overlapped
+
+
 def config_of(wl: synth.Workload, parallelism: str, curve: str = "raster") -> dict:
     return {
         "workload": (f"{wl.name}: B={wl.B}, heads={wl.heads}, d={wl.d}, grid (T,H,W)=({wl.T},{wl.H},{wl.W}) = "
@@ -125,13 +152,30 @@ def config_of(wl: synth.Workload, parallelism: str, curve: str = "raster") -> di
 
 
 def load_peaks() -> dict:
+    """The dense bf16 tensor peaks and the copy bandwidth: measured on this
+    pool's GB300s when MEASURED_PEAKS.json is present, else the fallback.
+    burst: cuBLAS timed alone at full clock; sustained: a seconds-long GEMM
+    loop under the power cap (fp16 has the same nominal rate as bf16)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        return dict(tflops=p.get("bf16_tflops_sustained") or p["bf16_tflops"], tflops_burst=p["bf16_tflops"],
+        return dict(burst=p["bf16_tflops"], sustained=p.get("bf16_tflops_sustained") or p["bf16_tflops"],
                     hbm=p["hbm_gbs"], source="measured (MEASURED_PEAKS.json)")
-    return dict(tflops=1700.0, tflops_burst=1900.0, hbm=6800.0, source="fallback")
+    return dict(burst=1900.0, sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+def pick_peak(peaks: dict, clocks: dict) -> tuple:
+    """(peak, kind) for the timed region: the burst peak when its SM clock
+    stayed at the maximum (median within 3%) with no power cap or slowdown
+    active, as for the burst measurement; the sustained peak otherwise."""
+    sm, smax, reasons = clocks.get("sm_mhz"), clocks.get("sm_max_mhz"), clocks.get("reasons") or []
+    at_max = bool(sm and smax and sm >= 0.97 * smax)
+    capped = any(r in reasons for r in ("sw_power_cap", "hw_slowdown", "hw_thermal_slowdown",
+                                        "sw_thermal_slowdown", "no samples"))
+    if at_max and not capped:
+        return peaks["burst"], "burst"
+    return peaks["sustained"], "sustained"
 
 
 class ClockSampler:
@@ -225,6 +269,87 @@ def oracle_sample(wl: synth.Workload, budget_s: float, rows_hint: int = 0):
     flops, dt = run(rows_hint)
     threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     return flops, dt, rows_hint, threads
+
+
+# ----------------------------------------------------------------------------- other configurations
+OTHER_CONFIGS = ["wan1.3b_k512", "wan1.3b_k256", "wan1.3b_k64", "wan14b", "long"]
+
+
+def measure_other_configs(vsa, dev, args, headline_inputs, order) -> dict:
+    """The sparsity sweep (Top-K 512 / 256 / 64 of 512 cubes), the 40-head
+    Wan-14B-shaped layer and the 122880-token long video: each a full
+    forward + backward step, timed like the headline (warm-up, then CUDA
+    events around `config_steps` steps, per-kernel event pairs).  The sweep
+    reuses the headline layer's inputs (same tensors, another K); the other
+    two get their own seeded inputs.  Each also gets an oracle sample on the
+    host cores (head 0, coarse stage in full plus sampled fine rows)."""
+    import torch
+    runs = {}
+    with ClockSampler(dev.index or 0) as clocks:
+        for name in OTHER_CONFIGS:
+            wl = synth.WORKLOADS[name]
+            if wl.T == synth.WORKLOADS[WORKLOAD].T and wl.heads == synth.WORKLOADS[WORKLOAD].heads and \
+                    wl.H == synth.WORKLOADS[WORKLOAD].H and wl.W == synth.WORKLOADS[WORKLOAD].W:
+                inputs, src = headline_inputs, f"the {WORKLOAD} layer's inputs"
+            else:
+                q, k, v = synth.make_qkv(wl)
+                gc, gf = synth.make_gates(wl)
+                dout = synth.make_dout(wl)
+                inputs = tuple(torch.from_numpy(a).to(dev).to(torch.bfloat16) for a in (q, k, v, gc, gf, dout))
+                del q, k, v, gc, gf, dout
+                src = "own seeded inputs"
+            qd, kd, vd, gcd, gfd, dod = inputs
+            out = torch.empty_like(qd)
+            grads = {n: torch.empty_like(qd) for n in ("dq", "dk", "dv", "dgc", "dgf")}
+            fws = torch.empty(vsa.workspace_bytes(0, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk),
+                              dtype=torch.uint8, device=dev)
+            bws = torch.empty(vsa.workspace_bytes(1, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk),
+                              dtype=torch.uint8, device=dev)
+            ordr = None if order is None else vsa.cube_order(wl.T, wl.H, wl.W, args.curve, device=dev)
+
+            def step():
+                _, st = vsa.forward(qd, kd, vd, wl.T, wl.H, wl.W, wl.topk, g_coarse=gcd, g_fine=gfd, out=out,
+                                    ws=fws, cube_order=ordr)
+                vsa.backward(st, dod, g_coarse=gcd, g_fine=gfd, grads=grads, ws=bws)
+
+            for _ in range(max(3, args.warmup)):
+                step()
+            torch.cuda.synchronize()
+            assert vsa.device_status() == 0, f"device error flag set in {name}"
+            vsa.timing_read()
+            stream = torch.cuda.current_stream()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            vsa.timing_enable(True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(args.config_steps):
+                step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            vsa.timing_enable(False)
+            ms = e0.elapsed_time(e1) / args.config_steps
+            kern = vsa.timing_read()
+            assert vsa.device_status() == 0, f"device error flag set in {name}"
+            per_kernel = {n: t / max(c, 1) for n, (t, c) in kern.items()}
+            fl = step_flops(wl)
+            bwd_ms, _ = fine_bwd_wall(per_kernel)
+            runs[name] = {
+                "workload": config_of(wl, "single GPU", args.curve)["workload"],
+                "inputs": src, "steps": args.config_steps, "ms_per_step": round(ms, 3),
+                "tflops": round(fl["total"] / (ms * 1e-3) / 1e12, 2),
+                "fine_fwd_ms": round(per_kernel["fine_fwd"], 4),
+                "fine_bwd_ms": round(bwd_ms, 4),
+                "per_kernel": per_kernel, "kflops": kernel_flops(wl),
+            }
+            del out, grads, fws, bws, inputs, qd, kd, vd, gcd, gfd, dod
+            torch.cuda.empty_cache()
+    if not args.no_cpu_baseline:
+        for name in OTHER_CONFIGS:
+            flops, dt, rows, threads = oracle_sample(synth.WORKLOADS[name], args.config_cpu_seconds)
+            runs[name]["cpu_oracle"] = {"tflops": round(flops / dt / 1e12, 6), "cores": threads,
+                                        "sample": f"head 0: coarse stage in full + fine fwd/bwd (dQ) of {rows} rows"}
+    return {"clocks": clocks.summary(), "runs": runs,
+            "note": "fractions against the same peak as the headline; each config's own timed steps"}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -370,19 +495,21 @@ def run_ours(args, rank: int, world: int):
         e2e = {"value": round(whole_job_tflops(world, fl["total"], args.steps, ems), 2), "unit": UNIT,
                "ms_per_step": round(ems / args.steps, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = measure_other_configs(vsa, dev, args, (dq_, dk_, dv_, dgc_, dgf_, ddo), order)
+
     if rank != 0:
         return
     peaks = load_peaks()
+    csum = clocks.summary()
+    peak, peak_kind = pick_peak(peaks, csum)
     value = whole_job_tflops(world, fl["total"], args.steps, ms)
     per_kernel = {n: round(t / max(c, 1), 4) for n, (t, c) in kern.items()}
     launches = {n: c for n, (t, c) in kern.items()}
-    # Work each fine kernel does per launch (products of 2*N*64K*d FLOP each):
-    # forward S and PV (2); backward dK/dV kernel S^T, dP^T, dV, dK (4); dQ
-    # kernel S, dP, dQ (3).  The effective metric counts 2 + 5.
-    unit = 2.0 * wl.N * (wl.topk * wl.N / wl.Nc) * wl.d * wl.BH
-    kflops = {"fine_fwd": 2 * unit, "fine_bwd_kv": 4 * unit, "fine_bwd_dq": 3 * unit}
+    kflops = kernel_flops(wl)
     # The roofline is reported for the kernel with the most work per step.
-    dominant = max(kflops, key=lambda n: kflops[n])
+    dominant = max(("fine_fwd", "fine_bwd_kv", "fine_bwd_dq"), key=lambda n: kflops[n])
     traffic = None  # DRAM bytes per launch from the committed ncu capture (profiles/traffic.txt)
     tpath = os.path.join(ROOT, "profiles", "traffic.txt")
     if os.path.exists(tpath) and args.config == WORKLOAD and args.curve == "raster":  # the captured case only
@@ -391,47 +518,50 @@ def run_ours(args, rank: int, world: int):
                 parts = ln.split()
                 if len(parts) == 2 and not ln.startswith("#") and parts[0] == dominant:
                     traffic = int(parts[1])
-
-    def roof(n):
-        a = kflops[n] / (per_kernel[n] * 1e-3) / 1e12
-        return {"ms": per_kernel[n], "tflops": round(a, 2), "frac": round(a / peaks["tflops"], 4),
-                "flops_per_launch": kflops[n]}
-
-    # vsa_backward runs the dK/dV kernel on a higher-priority stream of its own
-    # while the coarse backward and then the dQ kernel run on the caller's
-    # stream, filling the SMs the dK/dV kernel leaves.  The coarse and dQ event
-    # pairs follow one another on the caller's stream from the fork on, so
-    # together they span the fine backward's wall time (the coarse backward
-    # included).  Run back to back (no overlap), the two kernel intervals add.
-    overlapped = per_kernel["fine_bwd_dq"] > per_kernel["fine_bwd_kv"]
-    bwd_ms = (per_kernel["coarse_bwd"] + per_kernel["fine_bwd_dq"] if overlapped
-              else per_kernel["fine_bwd_kv"] + per_kernel["fine_bwd_dq"])
+    bwd_ms, overlapped = fine_bwd_wall(per_kernel)
+    dom = roof(kflops[dominant], per_kernel[dominant], peak)
+    dq_roof = roof(kflops["fine_bwd_dq"], per_kernel["fine_bwd_dq"], peak)
+    dq_eff = roof(kflops["dq_product"], per_kernel["fine_bwd_dq"], peak)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded smooth field + noise; Wan2.1 activations are not available)",
         "config": config_of(wl, "replicas" if world > 1 else "single GPU", args.curve),
-        "pct_of_peak": round(100 * value / world / peaks["tflops"], 2),
-        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": roof(dominant)["tflops"],
-                     "peak": peaks["tflops"], "unit": "TFLOP/s", "frac": roof(dominant)["frac"],
-                     "traffic": traffic,
-                     "peak_source": peaks["source"] + ", bf16 sustained (fp16 nominal rate = bf16)",
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": dom["tflops"], "peak": peak,
+                     "unit": "TFLOP/s", "frac": dom["frac"], "traffic": traffic,
+                     "peak_kind": peak_kind, "peak_burst": peaks["burst"], "peak_sustained": peaks["sustained"],
+                     "frac_burst": round(dom["tflops"] / peaks["burst"], 4),
+                     "frac_sustained": round(dom["tflops"] / peaks["sustained"], 4),
+                     "peak_source": (peaks["source"] + f", dense bf16 {peak_kind} (fp16 has the same nominal rate); "
+                                     "burst when the timed region held the maximum SM clock with no power cap"),
                      "flops_per_launch": kflops[dominant]},
-        "fine_fwd": roof("fine_fwd"),
-        "fine_bwd_kv": roof("fine_bwd_kv"),
-        "fine_bwd_dq": ({"interval_ms": per_kernel["fine_bwd_dq"],
-                         "note": "runs beside fine_bwd_kv; with coarse_bwd before it the interval spans the fine backward"}
-                        if overlapped else roof("fine_bwd_dq")),
+        "fine_fwd": roof(kflops["fine_fwd"], per_kernel["fine_fwd"], peak),
+        "fine_bwd_kv": roof(kflops["fine_bwd_kv"], per_kernel["fine_bwd_kv"], peak),
+        "fine_bwd_dq": dict(dq_roof, effective_tflops=dq_eff["tflops"], effective_frac=dq_eff["frac"],
+                            note=("interval on the caller's stream, beside fine_bwd_kv (shares the SMs of its last "
+                                  "wave); effective = the dQ product alone, 2*N*64K*d per head"
+                                  if overlapped else "effective = the dQ product alone, 2*N*64K*d per head")),
         "fine_bwd_effective": {"ms": round(bwd_ms, 4),
-                               "tflops": round(fl["fine_bwd"] / (bwd_ms * 1e-3) / 1e12, 2)},
+                               "tflops": round(fl["fine_bwd"] / (bwd_ms * 1e-3) / 1e12, 2),
+                               "frac": round(fl["fine_bwd"] / (bwd_ms * 1e-3) / 1e12 / peak, 4)},
         "kernel_ms_per_step": per_kernel,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "kernel_launches_timed": launches,
         "forward_only": fwd_only,
-        "clocks": clocks.summary(),
+        "clocks": csum,
         "e2e": e2e,
     }
+    if configs is not None:
+        for c in configs.get("runs", {}).values():
+            if "per_kernel" in c:
+                pk = c.pop("per_kernel")
+                cf = c.pop("kflops")
+                c["fine_fwd_frac"] = roof(cf["fine_fwd"], pk["fine_fwd"], peak)["frac"]
+                c["fine_bwd_kv_frac"] = roof(cf["fine_bwd_kv"], pk["fine_bwd_kv"], peak)["frac"]
+                c["pct_of_peak"] = round(100 * c["tflops"] / peak, 2)
+        line["configs"] = configs
     if not args.no_cpu_baseline and world == 1:
         flops, dt, rows, threads = oracle_sample(wl, args.cpu_seconds)
         line["cpu_baseline"] = {
@@ -480,6 +610,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-forward-only", action="store_true", help="skip the forward-only timings")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other workloads (sparsity sweep, Wan-14B layer, long video)")
+    ap.add_argument("--config-steps", type=int, default=5, help="timed steps per other workload")
+    ap.add_argument("--config-cpu-seconds", type=float, default=3.0, help="oracle sample per other workload")
     ap.add_argument("--curve", choices=["raster", "hilbert"], default="raster",
                     help="cube order of the space-filling-curve reordering")
     args = ap.parse_args()

@@ -18,6 +18,7 @@ from . import _lib
 from ._lib import Grid, VSAError, VSA_DTYPE_BF16, VSA_DTYPE_F32
 
 __all__ = ["num_cubes", "cube_order", "permute", "coarse_topk", "fine_fwd", "fine_bwd", "forward", "forward_inference", "backward",
+           "backward_tile_pairs",
            "workspace_bytes", "device_status", "timing_enable", "timing_read", "VSAError",
            "ForwardState", "Grid"]
 
@@ -256,6 +257,18 @@ def backward(state: ForwardState, dout, g_coarse=None, g_fine=None, grad_dtype=t
         _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads.get("dgc")), _ptr(grads.get("dgf")), _DT[dt],
         _ptr(ws), nbytes, _stream()))
     return grads
+
+
+def backward_tile_pairs(state: ForwardState, ws: torch.Tensor) -> torch.Tensor:
+    """vsa_backward_tile_pairs: view of the key-cube pairs [BH, (Nc + 1) // 2, 2]
+    that the dK/dV kernel's tiles used in the backward call made with `ws`."""
+    ptr = ctypes.c_void_p()
+    _lib.check("vsa_backward_tile_pairs", _lib.load().vsa_backward_tile_pairs(
+        _ptr(ws), state.B, state.heads, state.d, Grid.of(state.T, state.H, state.W), state.topk, ctypes.byref(ptr)))
+    Nc = num_cubes(state.T, state.H, state.W)
+    n = state.B * state.heads * ((Nc + 1) // 2) * 2
+    off = ptr.value - ws.data_ptr()
+    return ws[off:off + 4 * n].view(torch.int32).view(state.B * state.heads, (Nc + 1) // 2, 2)
 
 
 def timing_enable(on: bool = True) -> None:

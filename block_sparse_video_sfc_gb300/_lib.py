@@ -30,6 +30,7 @@ VSA_OP_FINE_BWD = 2
 VSA_OP_FORWARD_INFERENCE = 3
 VSA_CURVE_RASTER = 0
 VSA_CURVE_HILBERT = 1
+VSA_NOALLOC_SCRATCH_BYTES = 64 << 20   # the fixed scratch array of vsa_fine_bwd_noalloc
 
 # Every function the header declares, with its ctypes signature.
 P = ctypes.c_void_p
@@ -68,6 +69,7 @@ SIGNATURES = {
     "vsa_backward": ([P, P, P, P, I, I, I, Grid, I, F, P, P, P, P, P, I, P, SZ, P], I),
     "vsa_workspace_bytes": ([I, I, I, I, Grid, I], SZ),
     "vsa_forward_saved": ([P, I, I, I, Grid, I, ctypes.POINTER(Saved)], I),
+    "vsa_backward_tile_pairs": ([P, I, I, I, Grid, I, ctypes.POINTER(P)], I),
     "vsa_device_status": ([P], I),
     "vsa_selftest_wait_timeout": ([ctypes.c_uint32, P], I),
     "vsa_mask_to_lut": ([P, I, I, I, P, P, P], I),

@@ -193,10 +193,12 @@ __device__ __forceinline__ uint32_t orderable(float f) {
 // ascending id, as many keys equal to it as K still needs are kept.  Order:
 // each pick's rank is the number of picks that beat it (higher score, or the
 // same score and a lower id), so the row comes out highest first.
+// A NaN score has no place in the order: it latches kErrNan (the row is still
+// completed, NaN ranking above every number).
 __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const float* __restrict__ S, int64_t rows, int Nc,
                                                                    int K, int32_t* __restrict__ idx,
                                                                    int32_t* __restrict__ cnt,
-                                                                   float* __restrict__ lse) {
+                                                                   float* __restrict__ lse, int* err) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + warp;
@@ -207,11 +209,14 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const float* 
   const float* s = S + row * Nc;
 
   float m = -INFINITY;
+  bool nan = false;
   for (int j = lane; j < Nc; j += 32) {
     const float v = s[j];
     keys[j] = orderable(v);
     m = fmaxf(m, v);
+    nan |= v != v;
   }
+  if (__any_sync(0xffffffffu, nan) && lane == 0) flag_error(err, kErrNan);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   float l = 0.f;
@@ -342,7 +347,7 @@ int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH
       cudaSuccess)
     return VSA_ERR_CUDA;
   topk_rows_kernel<<<static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps), kRowWarps * 32, smem, s>>>(
-      scores, rows, Nc, topk, idx, cnt, lse_c);
+      scores, rows, Nc, topk, idx, cnt, lse_c, device_error_word());
   if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
   if (oc && (st = launch_coarse_oc(scores, lse_c, vc, BH, Nc, d, oc, s)) != VSA_OK) return st;
   timing_mark(VSA_K_COARSE, false, s);

@@ -12,7 +12,7 @@ namespace vsa {
 constexpr int kCube = 64;  // (4, 4, 4) tokens per cube
 
 // Bits of the device-side error word (see vsa_device_status).
-enum : int { kErrLut = 1, kErrTimeout = 2, kErrRange = 4 };
+enum : int { kErrLut = 1, kErrTimeout = 2, kErrRange = 4, kErrNan = 8 };
 
 __device__ __forceinline__ void flag_error(int* err, int bit) {
   if (err) atomicOr(err, bit);
@@ -108,7 +108,7 @@ int launch_cube_order(int Tc, int Hc, int Wc, int curve, int32_t* order, cudaStr
 int make_tile_map(void* map, const void* base, int64_t rows, int d, int f16);
 int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk,
                        float scale, float* oc, float* lse_c, int32_t* idx, int32_t* cnt, float* scores,
-                       cudaStream_t s);
+                       cudaStream_t s);  // a NaN score latches kErrNan
 int launch_coarse_oc(const float* scores, const float* lse_c, const float* vc, int BH, int Nc, int d, float* oc,
                      cudaStream_t s);
 int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt,

@@ -303,6 +303,7 @@ int vsa_device_status(void* stream) {
   if (v & kErrTimeout) return VSA_ERR_TIMEOUT;
   if (v & kErrLut) return VSA_ERR_LUT;
   if (v & kErrRange) return VSA_ERR_RANGE;
+  if (v & kErrNan) return VSA_ERR_ARG;
   return VSA_OK;
 }
 
@@ -404,6 +405,17 @@ int vsa_forward_saved(const void* fwd_ws, int B, int heads, int d, vsa_grid_t g,
   out->o_fine = at<float>(fwd_ws, w.of);
   out->lse = at<float>(fwd_ws, w.lse);
   out->tile_pairs = at<int32_t>(fwd_ws, w.pairs);
+  return VSA_OK;
+}
+
+int vsa_backward_tile_pairs(const void* bwd_ws, int B, int heads, int d, vsa_grid_t g, int topk,
+                            int32_t** key_pairs) {
+  Dims D;
+  if (!bwd_ws || !key_pairs || B <= 0 || heads <= 0) return VSA_ERR_ARG;
+  int st = check_grid(g, d, &D, static_cast<int64_t>(B) * heads);
+  if (st != VSA_OK) return st;
+  if (topk < 1 || topk > D.Nc) return VSA_ERR_ARG;
+  *key_pairs = at<int32_t>(bwd_ws, bwd_layout(D).kpairs);
   return VSA_OK;
 }
 

@@ -7,13 +7,16 @@
 // have the input and output buffers but nothing to pass as a workspace.  For
 // them this entry point keeps its scratch (the inverse-list bit matrix, the
 // per-row D and the fp16 copies of Q, K, V, dO) in one file-scope device
-// array of fixed size.  The array is part of the library's device image, so
-// every GPU that loads the library holds it until the process exits.
+// array of fixed size.  The array belongs to this file's device module: a
+// device holds it from the first call on that device (CUDA loads modules
+// lazily by default; with CUDA_MODULE_LOADING=EAGER from library load) until
+// the process exits.
 //
 // Host code cannot use the array's name as a device address (in host code it
 // names a host-side stand-in), so the device address is looked up once per
 // device with cudaGetSymbolAddress, on the first call made with that device
-// current, and cached.
+// current, and cached.  A cudaDeviceReset destroys the array with the
+// context, which leaves the cached address stale.
 #include <mutex>
 
 #include "common.cuh"

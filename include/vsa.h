@@ -193,14 +193,19 @@ int vsa_fine_bwd(const void* qp, const void* kp, const void* vp, const void* o_f
  * outputs but no allocator for a workspace.
  *   Arguments and results are those of vsa_fine_bwd, minus ws / ws_bytes.
  *   Scratch: a fixed device array of VSA_NOALLOC_SCRATCH_BYTES inside the
- *   library (held by every GPU that loads the library, until exit).  Problems
- *   whose vsa_fine_bwd workspace exceeds it are rejected with
- *   VSA_ERR_WORKSPACE before anything is enqueued: the limit is about
- *   BH * N <= 65000 query rows (for example 12 heads of 4096 tokens); use
- *   vsa_fine_bwd beyond it.
+ *   library.  A device holds it from the first vsa_fine_bwd_noalloc call on
+ *   that device until the process exits (from library load instead when
+ *   CUDA_MODULE_LOADING=EAGER).  Problems whose vsa_fine_bwd workspace
+ *   exceeds it are rejected with VSA_ERR_WORKSPACE before anything is
+ *   enqueued: the limit is about BH * N <= 65000 query rows (for example 15
+ *   heads of 4096 tokens at d = 128 and 16 listed cubes); use vsa_fine_bwd
+ *   beyond it.
  *   The call allocates nothing.  Its first call on a device looks up the
- *   array's device address (cudaGetSymbolAddress) with that device current;
- *   make that first call before any stream capture.  All calls share the one
+ *   array's device address (cudaGetSymbolAddress) with that device current
+ *   and keeps it for the life of the process; make that first call before
+ *   any stream capture.  cudaDeviceReset destroys the array with the
+ *   context, and the kept address then points at nothing: do not use this
+ *   entry point on a device after resetting it.  All calls share the one
  *   array and leave their contents in it (the parts that must start at zero
  *   are cleared on the stream by each call): calls whose GPU work overlaps
  *   -- on different streams, or from different threads -- race with each
@@ -296,6 +301,13 @@ typedef struct {
 
 int vsa_forward_saved(const void* fwd_ws, int B, int heads, int d, vsa_grid_t g, int topk, vsa_saved_t* out);
 
+/* Device pointer into a backward workspace after vsa_backward: the key-cube
+ * pairs of the dK/dV kernel's tiles, int32 [BH, (Nc + 1) / 2, 2] (second -1:
+ * a lone cube).  A scheduling choice, not a result: each tile computes dK and
+ * dV of its two key cubes over the union of their inverse lists. */
+int vsa_backward_tile_pairs(const void* bwd_ws, int B, int heads, int d, vsa_grid_t g, int topk,
+                            int32_t** key_pairs);
+
 /*
  * Kernel timing (instrumentation, off by default).  While enabled, every
  * launch of the kernels below is bracketed by a pair of CUDA events recorded
@@ -318,7 +330,9 @@ int vsa_timing_enable(int on);
 int vsa_timing_read(int kernel, double* total_ms, int* launches);
 
 /* Waits for `stream`, then returns and clears the device-side error flag:
- * VSA_OK, VSA_ERR_LUT or VSA_ERR_TIMEOUT (or VSA_ERR_CUDA). */
+ * VSA_OK, VSA_ERR_LUT, VSA_ERR_TIMEOUT, VSA_ERR_RANGE, or VSA_ERR_ARG when a
+ * coarse score was NaN (a non-finite input; the Top-K then ranks NaN above
+ * every number) -- or VSA_ERR_CUDA. */
 int vsa_device_status(void* stream);
 
 /* Static description of a status code. */

@@ -5,6 +5,23 @@ import numpy as np
 
 MAX_ABS = 2e-2    # max-abs tolerance for outputs and gradients (fp32 accumulate, bf16 inputs)
 MEAN_ABS = 2e-3   # mean-abs tolerance
+# The fine forward's log-sum-exp.  The row sum l adds the n = 64 K softmax
+# weights exp2(s - m) rounded to fp16 (the operand the P.V product uses);
+# every weight is <= 256 and the largest is >= 1, so l >= 1, and a rounding
+# errs by at most 2^-11 of the weight (fp16 normal range) or by 2^-25
+# (below it).  Hence |log l - log l_exact| <= 2^-11 + n 2^-25 even if every
+# rounding went the same way.  S is an fp32 sum of exact products of the
+# 16-bit operands, and exp2 is the hardware approximation (relative error
+# ~2^-22): 1e-4 covers both.  Mean-abs 1e-4.
+LSE_MEAN_ABS = 1e-4
+
+
+def lse_max_abs(keys: int) -> float:
+    """Max-abs bound on the fine LSE of a row that attends to `keys` keys."""
+    return 2.0 ** -11 + keys * 2.0 ** -25 + 1e-4
+
+
+LSE_MAX_ABS = lse_max_abs(64 * 16)   # the unit tests' lists: at most 16 cubes (6.2e-4)
 
 
 def half_ulp_bf16(x: np.ndarray) -> np.ndarray:

@@ -74,14 +74,40 @@ def test_clock_summary_without_samples():
     assert _sampler([]).summary()["reasons"] == ["no samples"]
 
 
-def test_peaks_prefer_the_sustained_measurement():
+def test_peaks_read_both_measurements():
     p = bench.load_peaks()
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if not os.path.exists(path):
-        assert p["source"] == "fallback"
+        assert p["source"] == "fallback" and p["burst"] > p["sustained"]
         return
     import json
     with open(path) as f:
         m = json.load(f)
-    assert p["tflops"] == (m.get("bf16_tflops_sustained") or m["bf16_tflops"])
+    assert p["burst"] == m["bf16_tflops"]
+    assert p["sustained"] == (m.get("bf16_tflops_sustained") or m["bf16_tflops"])
     assert p["hbm"] == m["hbm_gbs"] and p["source"].startswith("measured")
+
+
+PEAKS = {"burst": 1919.9, "sustained": 1716.3}
+
+
+@pytest.mark.parametrize("clocks,kind", [
+    ({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}, "burst"),           # full clock, no cap
+    ({"sm_mhz": 2040.0, "sm_max_mhz": 2070.0, "reasons": []}, "burst"),           # within 3%
+    ({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}, "sustained"),
+    ({"sm_mhz": 1455.0, "sm_max_mhz": 2070.0, "reasons": []}, "sustained"),       # below the maximum
+    ({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}, "sustained"),
+])
+def test_peak_follows_the_clocks_of_the_timed_region(clocks, kind):
+    peak, got = bench.pick_peak(PEAKS, clocks)
+    assert got == kind and peak == PEAKS[kind]
+
+
+def test_roofline_fraction_reproduces_from_its_fields():
+    wl = synth.WORKLOADS["wan1.3b"]
+    kf = bench.kernel_flops(wl)
+    r = bench.roof(kf["fine_bwd_kv"], 5.7576, PEAKS["burst"])
+    assert r["tflops"] == pytest.approx(kf["fine_bwd_kv"] / 5.7576e-3 / 1e12, abs=0.01)
+    assert r["frac"] == pytest.approx(r["tflops"] / PEAKS["burst"], abs=1e-4)
+    assert kf["fine_bwd_kv"] == 4 * kf["dq_product"] and kf["fine_fwd"] == 2 * kf["dq_product"]
+    assert kf["fine_fwd"] == bench.step_flops(wl)["fine_fwd"]

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import synth
-from parity import assert_close, check_topk_validity, exact_topk
+from parity import LSE_MAX_ABS, LSE_MEAN_ABS, assert_close, check_topk_validity, exact_topk, lse_max_abs
 
 pytestmark = pytest.mark.gpu
 
@@ -80,6 +80,20 @@ def test_coarse_topk(vsa, oracle_mod, name):
     np.testing.assert_allclose(host(r["lse_c"]), lse_c, rtol=1e-5, atol=1e-4)
 
 
+def test_nan_scores_are_reported(vsa):
+    """A NaN coarse score cannot be ranked: the Top-K latches an error that
+    vsa_device_status reports as VSA_ERR_ARG (and clears); clean inputs then
+    run clean."""
+    g = torch.Generator().manual_seed(3)
+    qc, kc, vc = (torch.randn(2, 64, 128, generator=g).cuda() for _ in range(3))
+    vsa.coarse_topk(qc, kc, vc, 8)
+    assert vsa.device_status() == 0
+    qc[1, 17, 5] = float("nan")
+    vsa.coarse_topk(qc, kc, vc, 8)
+    assert vsa.device_status() == -1   # VSA_ERR_ARG
+    assert vsa.device_status() == 0
+
+
 # ---------------------------------------------------------------- fine forward
 def _fine_case(oracle_mod, wl, heads=None):
     q, k, v = synth.make_qkv(wl, heads_subset=heads)
@@ -103,7 +117,7 @@ def test_fine_fwd(vsa, oracle_mod, name, out_dtype):
     status_ok(vsa)
     rof, rlse = oracle_mod.fine_fwd(qp, kp, vp, idx, cnt, wl.d ** -0.5)
     assert_close(host(of), rof, bf16_out=out_dtype == torch.bfloat16, what="O_f")
-    assert_close(host(lse), rlse, what="lse")
+    assert_close(host(lse), rlse, max_abs=LSE_MAX_ABS, mean_abs=LSE_MEAN_ABS, what="lse")
 
 
 def test_fine_fwd_ragged_and_edge_lists(vsa, oracle_mod):
@@ -118,7 +132,7 @@ def test_fine_fwd_ragged_and_edge_lists(vsa, oracle_mod):
     assert_close(host(of), rof, what="O_f ragged")
     empty = np.isneginf(rlse)
     assert np.all(np.isneginf(host(lse)[empty])) and np.all(host(of)[empty] == 0)
-    assert_close(host(lse)[~empty], rlse[~empty], what="lse")
+    assert_close(host(lse)[~empty], rlse[~empty], max_abs=LSE_MAX_ABS, mean_abs=LSE_MEAN_ABS, what="lse")
 
 
 def test_fine_fwd_dense_is_sdpa(vsa, oracle_mod):
@@ -158,10 +172,40 @@ def _e2e(vsa, oracle_mod, wl, gates, out_dtype, grad_dtype, heads=None, cube_ord
     D = lambda a: None if a is None else dev(a)
     out, st = vsa.forward(D(q), D(k), D(v), wl.T, wl.H, wl.W, wl.topk, g_coarse=D(gc), g_fine=D(gf),
                           out_dtype=out_dtype, cube_order=cube_order)
-    g = vsa.backward(st, D(dout), g_coarse=D(gc), g_fine=D(gf), grad_dtype=grad_dtype)
+    bws = torch.empty(vsa.workspace_bytes(1, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk), dtype=torch.uint8,
+                      device="cuda")
+    g = vsa.backward(st, D(dout), g_coarse=D(gc), g_fine=D(gf), grad_dtype=grad_dtype, ws=bws)
     status_ok(vsa)
     saved = st.saved()
+    saved["key_pairs"] = vsa.backward_tile_pairs(st, bws)
     return q, k, v, gc, gf, dout, out, g, saved
+
+
+def _key_cubes(idx1, kpairs0, keys_per_row, budget_flop=2.5e11):
+    """Key cubes of one head whose dK / dV are compared element by element:
+    the most-listed (longest inverse-list walk), a median one, the
+    least-listed listed one, an unlisted one if any, and both cubes of the
+    planned dK/dV tile holding the most-listed cube.  A cube is skipped when
+    the oracle's cost for it (every listing query row recomputes its softmax
+    over keys_per_row keys) exceeds budget_flop, except the first cube."""
+    Nc = idx1.shape[-2]
+    inv = np.bincount(idx1.reshape(-1), minlength=Nc)
+    listed = np.flatnonzero(inv > 0)
+    order = listed[np.argsort(inv[listed], kind="stable")]
+    top = int(order[-1])
+    tile = [t for t in kpairs0 if top in (int(t[0]), int(t[1]))]
+    assert len(tile) == 1, "the most-listed key cube sits in exactly one planned tile"
+    picks = [top, int(order[len(order) // 2]), int(order[0])] + [int(c) for c in tile[0] if c >= 0]
+    if (inv == 0).any():
+        picks.append(int(np.flatnonzero(inv == 0)[0]))
+    out, spent = [], 0.0
+    for c in dict.fromkeys(picks):
+        cost = 4.0 * inv[c] * 64 * keys_per_row * 128
+        if out and spent + cost > budget_flop:
+            continue
+        out.append(c)
+        spent += cost
+    return out, tile[0]
 
 
 @pytest.mark.parametrize("name,gates", [("tiny", True), ("tiny", False), ("tiny_dense", True), ("small", True)])
@@ -234,9 +278,13 @@ def test_full_size_head_sample(vsa, oracle_mod):
     dq_rows += dqc[0, rows // 64] / 64.0
     native = np.argsort(pos)[rows]                                          # native token of each row
     assert_close(host(g["dq"])[0, 0, native], dq_rows, what="dq rows")
-    inv_count = np.bincount(idx1.reshape(-1), minlength=wl.Nc)
-    for c in (int(np.argmin(np.where(inv_count > 0, inv_count, 1 << 30))), int(np.argmax(inv_count == 0)) if
-              (inv_count == 0).any() else 0):
+    lse_rows = np.asarray(rows)
+    _, rl = oracle_mod.fine_fwd_rows(qp, kp, vp, idx1, cnt1, scale, lse_rows)
+    assert_close(host(saved["lse"])[0, lse_rows], rl, max_abs=lse_max_abs(64 * wl.topk), mean_abs=LSE_MEAN_ABS,
+                 what="lse rows")
+    kcubes, tile = _key_cubes(idx1, saved["key_pairs"][0].cpu().numpy(), 64 * wl.topk)
+    assert tile[0] in kcubes and (tile[1] < 0 or tile[1] in kcubes)
+    for c in kcubes:
         dk_c, dv_c = oracle_mod.fine_bwd_key_cube(qp, kp, vp, dof, idx1, cnt1, scale, 0, c)
         dk_c += dkc[0, c] / 64.0
         dv_c += dvc[0, c] / 64.0
@@ -252,10 +300,11 @@ def test_full_size_head_sample(vsa, oracle_mod):
 def _sampled_checks(vsa, oracle_mod, wl, dtype, n_cubes=4, n_rows=48):
     """Full-size run of `wl` (all heads, bench launch configuration); the
     oracle recomputes, for the first and last head: the coarse scores (Top-K
-    validity of the GPU lists), whole query cubes of the output, dQ on sampled
-    rows and dg_c / dg_f on the sampled cubes; and, for head 0, dK / dV of the
-    least-listed key cube (and of an unlisted one, if any).  All heads:
-    sum_j dK_j = 0 per channel."""
+    validity of the GPU lists), whole query cubes of the output, the fine LSE
+    and dQ on sampled rows and dg_c / dg_f on the sampled cubes; and, for head
+    0, dK / dV of the key cubes _key_cubes picks (most-listed, median,
+    least-listed, unlisted, both cubes of a planned dK/dV tile) within the
+    oracle's time budget.  All heads: sum_j dK_j = 0 per channel."""
     q, k, v, gc, gf, dout, out, g, saved = _e2e(vsa, oracle_mod, wl, True, dtype, dtype)
     bf = dtype == torch.bfloat16
     gidx = saved["idx"].view(wl.B, wl.heads, wl.Nc, wl.topk).cpu().numpy()
@@ -293,11 +342,11 @@ def _sampled_checks(vsa, oracle_mod, wl, dtype, n_cubes=4, n_rows=48):
         dq_ref = (oracle_mod.fine_bwd_query_rows(qp, kp, vp, dof, idx1, cnt1, scale, qrows, slot_ok=slot_ok)
                   + dqc[0, qrows // 64] / ntok[qrows // 64, None])
         assert_close(at(g["dq"], h, native_of[qrows]), dq_ref, bf16_out=bf, what=f"dq rows head {h}")
+        _, rl = oracle_mod.fine_fwd_rows(qp, kp, vp, idx1, cnt1, scale, qrows, slot_ok=slot_ok)
+        assert_close(host(saved["lse"][h])[qrows], rl, max_abs=lse_max_abs(64 * wl.topk), mean_abs=LSE_MEAN_ABS,
+                     what=f"lse rows head {h}")
         if h == 0:
-            inv_count = np.bincount(idx1.reshape(-1), minlength=wl.Nc)
-            kcubes = [int(np.argmin(np.where(inv_count > 0, inv_count, 1 << 30)))]
-            if (inv_count == 0).any():
-                kcubes.append(int(np.argmax(inv_count == 0)))
+            kcubes, _ = _key_cubes(idx1, saved["key_pairs"][0].cpu().numpy(), 64 * wl.topk)
             for c in kcubes:
                 dk_c, dv_c = oracle_mod.fine_bwd_key_cube(qp, kp, vp, dof, idx1, cnt1, scale, 0, c, slot_ok=slot_ok)
                 ok = slot_ok[64 * c:64 * c + 64] == 1

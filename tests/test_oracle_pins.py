@@ -383,6 +383,46 @@ def test_sampled_backward_functions_match_full(oracle_mod):
     assert pos.size == wl.N
 
 
+@pytest.mark.parametrize("curve", ["raster", "hilbert"])
+def test_sampled_forward_rows_match_full_and_dense(oracle_mod, curve):
+    """The sampled fine-forward function (the checker of every full-size
+    forward comparison) against the full fine forward and against the dense
+    masked torch formulation, on a grid with partial cubes (padding slots
+    masked through slot_ok) and ragged counts, empty rows included."""
+    wl = synth.WORKLOADS["odd_small"]                      # 9 x 14 x 22: every side ends in a partial cube
+    q, k, v = (a.reshape(1, wl.N, wl.d)[:, :, :32] for a in synth.make_qkv(wl, heads_subset=[1]))
+    T, H, W = wl.T, wl.H, wl.W
+    rank = None if curve == "raster" else oracle_mod.cube_rank(*oracle_mod.cube_grid(T, H, W), curve)
+    qp, kp, vp = (oracle_mod.permute(a, T, H, W, curve=curve) for a in (q, k, v))
+    slot_ok, _ = oracle_mod.cube_slots(T, H, W, curve)
+    Nc = oracle_mod.num_cubes(T, H, W)
+    rng = np.random.default_rng(17)
+    kmax = 9
+    idx = np.stack([rng.permutation(Nc)[:kmax] for _ in range(Nc)])[None].astype(np.int32)
+    cnt = rng.integers(0, kmax + 1, size=(1, Nc)).astype(np.int32)
+    cnt[0, 3] = 0                                          # an empty list
+    scale = 32 ** -0.5
+    of, lse = oracle_mod.fine_fwd(qp, kp, vp, idx, cnt, scale, slot_ok=slot_ok)
+    rows = np.unique(np.r_[0, 63, 64 * 3 + 5, rng.choice(64 * Nc, 40, replace=False), 64 * Nc - 1])
+    ro, rl = oracle_mod.fine_fwd_rows(qp, kp, vp, idx, cnt, scale, rows, slot_ok=slot_ok)
+    np.testing.assert_allclose(ro, of[0, rows], rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(rl), np.isneginf(lse[0, rows]))
+    fin = ~np.isneginf(rl)
+    np.testing.assert_allclose(rl[fin], lse[0, rows][fin], rtol=1e-12, atol=1e-12)
+    assert np.all(ro[~fin] == 0)
+    # dense masked formulation (native order, cube ids from the coordinates)
+    _, dof_, _, _, dlse = dense_vsa(_t(q), _t(k), _t(v), T, H, W, idx, scale, cnt=cnt, rank=rank)
+    pos = oracle_mod.sfc_table(T, H, W, curve)
+    native_of = np.full(64 * Nc, -1, np.int64)
+    native_of[pos] = np.arange(wl.N)
+    real = rows[slot_ok[rows] == 1]
+    sel = np.searchsorted(rows, real)
+    nat = native_of[real]
+    np.testing.assert_allclose(ro[sel][fin[sel]], dof_.numpy()[0, nat][fin[sel]], rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(rl[sel][fin[sel]], dlse.numpy()[0, nat][fin[sel]], rtol=1e-12)
+    assert fin.sum() > 10 and (~fin).sum() >= 1
+
+
 # ---------------------------------------------------------------- index-list conversions
 def test_mask_to_lut_matches_nonzero(oracle_mod):
     """Block matrix -> list: the ascending nonzero columns of each row (brute
