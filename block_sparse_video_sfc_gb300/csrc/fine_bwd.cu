@@ -137,6 +137,52 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+
+// Packed fp32 pairs (one instruction for two lanes of arithmetic).  The
+// compute warps' budget per step is set by the special-function pipe (ex2 and
+// the f32 -> f16x2 conversion both take 4 clk per warp instruction per SM
+// sub-partition on GB300), so the surrounding arithmetic runs as f32x2 and the
+// fp16 packs saturate in the conversion itself instead of through min / max.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2u(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// exp2 of both lanes.
+__device__ __forceinline__ uint64_t exp2x2(uint64_t x) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+  return f2(fast_exp2(a), fast_exp2(b));
+}
+// Both lanes to an fp16 pair (low lane in the low half), round to nearest,
+// saturating at +-65504 (beyond-range values are clamped, never infinite).
+__device__ __forceinline__ uint32_t f16x2_sat(uint64_t x) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+  uint32_t h;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(b), "f"(a));
+  return h;
+}
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -415,21 +461,21 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
         tmem_ld32_wait(sb + kKvDP, dv);
       }
       if (valid) {
+        // P^T = exp2(log2e (S^T scale - LSE)) = exp2((LSE - scale S^T) (-log2e)),
+        // dS^T = P^T (dP^T - D), two query columns per packed operation.
+        const uint64_t nsc = f2(-p.scale, -p.scale), nl2e = f2(-1.4426950408889634f, -1.4426950408889634f);
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(lse + c);
           const float4 d4 = *reinterpret_cast<const float4*>(dlt + c);
-          const float l[4] = {l4.x, l4.y, l4.z, l4.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pr[4], ds[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            pr[i] = fast_exp2(fmaf(__uint_as_float(sv[c + i]), p.scale_log2, -l[i] * 1.4426950408889634f));
-            ds[i] = pr[i] * (__uint_as_float(dv[c + i]) - dd[i]);
-          }
-          pk[c >> 1] = pack_f16(pr[0], pr[1]);
-          pk[(c >> 1) + 1] = pack_f16(pr[2], pr[3]);
-          dk[c >> 1] = pack_f16(ds[0], ds[1]);
-          dk[(c >> 1) + 1] = pack_f16(ds[2], ds[3]);
+          const uint64_t p0 = exp2x2(mul2(fma2(f2u(sv[c], sv[c + 1]), nsc, f2(l4.x, l4.y)), nl2e));
+          const uint64_t p1 = exp2x2(mul2(fma2(f2u(sv[c + 2], sv[c + 3]), nsc, f2(l4.z, l4.w)), nl2e));
+          const uint64_t g0 = mul2(p0, sub2(f2u(dv[c], dv[c + 1]), f2(d4.x, d4.y)));
+          const uint64_t g1 = mul2(p1, sub2(f2u(dv[c + 2], dv[c + 3]), f2(d4.z, d4.w)));
+          pk[c >> 1] = f16x2_sat(p0);
+          pk[(c >> 1) + 1] = f16x2_sat(p1);
+          dk[c >> 1] = f16x2_sat(g0);
+          dk[(c >> 1) + 1] = f16x2_sat(g1);
         }
       } else {
 #pragma unroll
@@ -685,6 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
     const int64_t grow = row_base + 64 * static_cast<int64_t>(row < 64 ? qa : (has_b ? qb : qa)) + (row & 63);
     const float lse2 = row_valid ? p.lse[grow] * 1.4426950408889634f : 0.f;
     const float dlt = row_valid ? p.delta[grow] : 0.f;
+    const uint64_t sl2 = f2(p.scale_log2, p.scale_log2), nlse2 = f2(-lse2, -lse2), dlt2 = f2(dlt, dlt);
     bool ok = true;
     for (int j = 0; j < steps; ++j) {
       const int b = j & 1;
@@ -704,11 +751,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
       // P = exp2(S * scale - LSE), dS = P (dP - D), packed fp16.
       uint32_t ds[32];
       if (valid) {
+        // P = exp2(S scale log2e - LSE log2e), dS = P (dP - D), packed pairs.
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[i]), p.scale_log2, -lse2));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[i + 1]), p.scale_log2, -lse2));
-          ds[i >> 1] = pack_f16(p0 * (__uint_as_float(dv[i]) - dlt), p1 * (__uint_as_float(dv[i + 1]) - dlt));
+          const uint64_t pr = exp2x2(fma2(f2u(sv[i], sv[i + 1]), sl2, nlse2));
+          ds[i >> 1] = f16x2_sat(mul2(pr, sub2(f2u(dv[i], dv[i + 1]), dlt2)));
         }
       } else {
 #pragma unroll

@@ -504,6 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
         break;
       }
       mx = fmaxf(mx, xmax[j & 1][half ^ 1][row]);
+      // P(j) goes into P buffer j % 2 once PV(j - 2) has read it: test now,
+      // so that the answer is in by the time P is ready.
+      const bool pv_free = j < 2 || mbar_test(&pv_done[j & 1], ((j >> 1) - 1) & 1);
 
       // Raise the running max only when it grows by more than the threshold.
       const bool raise = mx > m + kRescaleThreshold;
@@ -545,13 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
 #pragma unroll
         for (int c = 0; c < 32; ++c) pk[c] = 0u;
       }
-      if (j >= 2) {
-        if (!mbar_spin(&pv_done[j & 1], ((j >> 1) - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      if (!pv_free && !mbar_spin(&pv_done[j & 1], ((j >> 1) - 1) & 1)) {
+        ok = false;
+        break;
       }
+      if (j >= 2) tc_fence_after();
 #pragma unroll
       for (int c = 0; c < 32; c += 8) tmem_st8(lane_addr + kColP + 64 * (j & 1) + 32 * half + c, pk + c);
       if (!F16IN && !NATIVE) {
