@@ -13,18 +13,20 @@
 // global memory (an fp32 reduce-add into L2 runs at only ~3-4 TB/s on GB300,
 // which would bound a fused key-stationary kernel's dQ traffic).
 //
-// fine_bwd_kv_kernel (key-stationary): one CTA owns a PAIR of consecutive key
-// cubes (128 keys; K, V in shared memory; dK, dV accumulated in TMEM) and
-// walks the union of the two cubes' inverse lists (the query cubes whose index
-// list holds either key cube), one query cube (64 rows) per step, masking the
-// half of the tile whose key cube the query cube does not list.  Keys sit on
-// the MMA M dimension:
+// fine_bwd_kv_kernel (key-stationary): one CTA owns a PAIR of key cubes (128
+// keys; K, V in shared memory; dK, dV accumulated in TMEM) and walks the union
+// of the two cubes' inverse lists (the query cubes whose index list holds
+// either key cube), one query cube (64 rows) per step, masking the half of
+// the tile whose key cube the query cube does not list.  Keys sit on the MMA
+// M dimension:
 //   S^T = K Q^T, dP^T = V dO^T        (A, B in shared memory)
 //   dV += P^T dO, dK += dS^T Q        (A = P^T / dS^T in TMEM)
-// S^T and dP^T are double-buffered in TMEM, and the compute warps write
-// P^T(j), dS^T(j) (fp16) over the S^T(j), dP^T(j) they read, so the issuer
-// waits only for dV/dK(j - 2) before S^T(j): S^T(j+1) and dP^T(j+1) run while
-// the compute warps work on step j.  Q and dO go through a 4-stage ring.
+// One S^T / dP^T buffer, released as soon as the compute warps have read it
+// into registers, and two P^T / dS^T buffers: S^T(j + 1) waits only for that
+// read, never for an MMA to complete (the MMA issuer is the busy resource: an
+// issue returns about when the tensor core takes the instruction, so each
+// wait for a completion leaves it idle), and dV / dK(j) run after S^T(j + 1).
+// Q and dO go through a 4-stage ring.
 //
 // fine_bwd_dq_kernel (query-stationary): one CTA owns a pair of query cubes
 // (128 rows; Q, dO in shared memory; dQ accumulated in TMEM) and walks the
@@ -254,11 +256,11 @@ struct KvLayout {
   static constexpr int kStats = kRing + kKvStages * kStage;  // [stage][LSE 64 | D 64] fp32
   static constexpr int kEnd = kStats + kKvStages * 512;
 };
-// TMEM: two buffers b of S^T (column 128 b) and dP^T (128 b + 64), 64 fp32
-// columns each; P^T and dS^T (fp16 pairs) are written over the S^T and dP^T
-// they come from: compute warpgroup g reads columns [32 g, 32 g + 32) of each
-// and writes its 16 packed columns at 32 g.  dV at 256, dK at 384.
-constexpr uint32_t kKvBuf = 128, kKvDP = 64, kKvDV = 256, kKvDK = 384;
+// TMEM: S^T at column 0 and dP^T at 64 (64 fp32 columns each); P buffer b at
+// 128 + 64 b: P^T in its first 32 columns of fp16 pairs, dS^T in the next 32
+// (compute warpgroup g reads query columns [32 g, 32 g + 32) of S^T / dP^T and
+// writes its 16 packed columns at 16 g of each); dV at 256, dK at 384.
+constexpr uint32_t kKvS = 0, kKvDP = 64, kKvPB = 128, kKvDV = 256, kKvDK = 384;
 template <int D>
 constexpr int kKvCoarseBytes = 4 * D * static_cast<int>(sizeof(float));  // crow (fused epilogue)
 
@@ -275,12 +277,14 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
   uint32_t* bitB = bitA + p.nwords;
 
   // full[s]: Q, dO, LSE and D of the step in stage s landed; stage_free[s]:
-  // dV and dK of that step completed.  For buffer b = j % 2: s_done[b]:
-  // S^T(j) and dP^T(j) done; pds[b]: P^T / dS^T(j) written over them (all
-  // compute threads); buf_free[b]: dV(j) and dK(j), which read them,
-  // completed, so S^T(j + 2) may overwrite the buffer.  Every parity wait
-  // targets a barrier in the awaited phase or the one after it.
-  __shared__ uint64_t bar_kv, full[kKvStages], stage_free[kKvStages], s_done[2], pds[2], buf_free[2];
+  // dV and dK of that step completed.  s_done: S^T(j) and dP^T(j) done;
+  // s_free: the compute warps have read them (all compute threads), so
+  // S^T(j + 1) may overwrite the buffer.  For P buffer b = j % 2: pds[b]:
+  // P^T / dS^T(j) written (all compute threads); pbuf_free[b]: dV(j) and
+  // dK(j), which read them, completed.  Every parity wait targets a barrier in
+  // the awaited phase or the one after it: S^T(j + 1) needs the read of
+  // S^T(j), and P(j + 2) is written only after dV / dK(j) completed.
+  __shared__ uint64_t bar_kv, full[kKvStages], stage_free[kKvStages], s_done, s_free, pds[2], pbuf_free[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int n_union;
 
@@ -298,10 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       mbar_init(&full[i], 1);
       mbar_init(&stage_free[i], 1);
     }
+    mbar_init(&s_done, 1);
+    mbar_init(&s_free, kCompute);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_done[i], 1);
       mbar_init(&pds[i], kCompute);
-      mbar_init(&buf_free[i], 1);
+      mbar_init(&pbuf_free[i], 1);
     }
     fence_mbar_init();
   }
@@ -364,10 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer: S^T / dP^T (j) into buffer j % 2 once dV /
-    // dK (j - 2) have read it; dV / dK (j) once P^T / dS^T (j) are written.
-    // Polls with test_wait and issues whichever is ready, so S^T(j + 1) runs
-    // while the compute warps work on step j.
+    // ---------------- MMA issuer: S^T / dP^T (j) once the compute warps have
+    // read S^T / dP^T (j - 1); dV / dK (j) once P^T / dS^T (j) are written.
+    // Polls with test_wait and issues whichever is ready, S first, so that
+    // S^T(j + 1) runs while the compute warps work on step j.
     if (lane == 0 && steps > 0) {
       constexpr uint32_t idesc_s = idesc_f32acc(128, 64, 0, 0, 1);
       constexpr uint32_t idesc_g = idesc_f32acc(128, D, 0, 1, 1);
@@ -390,19 +395,18 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       uint32_t idle = 0;
       while (ok && ng < steps) {
         bool progressed = false;
-        if (ns < steps && (ns < 2 || mbar_test(&buf_free[ns & 1], ((ns >> 1) - 1) & 1)) &&
+        if (ns < steps && (ns == 0 || mbar_test(&s_free, (ns - 1) & 1)) &&
             mbar_test(&full[ns & (kKvStages - 1)], (ns / kKvStages) & 1)) {
           tc_fence_after();
           const uint64_t qd = qkm0 + (ns & (kKvStages - 1)) * kStageU;
-          const uint32_t sb = tmem + kKvBuf * (ns & 1);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(sb, kdesc[kk], qd + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
+            mma_ss(tmem + kKvS, kdesc[kk], qd + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(sb + kKvDP, vdesc[kk], qd + kTileQU + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s,
+            mma_ss(tmem + kKvDP, vdesc[kk], qd + kTileQU + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s,
                    kk > 0);
-          mma_commit(&s_done[ns & 1]);
+          mma_commit(&s_done);
           ++ns;
           progressed = true;
         }
@@ -410,20 +414,18 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
           tc_fence_after();
           const int st = ng & (kKvStages - 1);
           const uint64_t qd = qmn0 + st * kStageU;
-          const uint32_t sb = tmem + kKvBuf * (ng & 1);
+          const uint32_t pb = tmem + kKvPB + 64 * (ng & 1);
           // A = P^T / dS^T (K = 64 queries in 4 steps of 16: queries 16 kk..
-          // at column 32 (kk / 2) + 8 (kk % 2) of S^T / dP^T), B = dO / Q
-          // (MN-major).
+          // at column 8 kk of the P buffer's half), B = dO / Q (MN-major).
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kKvDV, sb + 32 * (kk >> 1) + 8 * (kk & 1), qd + kTileQU + ((kk * 2048) >> 4), idesc_g,
+            mma_ts(tmem + kKvDV, pb + 8 * kk, qd + kTileQU + ((kk * 2048) >> 4), idesc_g,
                    (ng > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kKvDK, sb + kKvDP + 32 * (kk >> 1) + 8 * (kk & 1), qd + ((kk * 2048) >> 4), idesc_g,
-                   (ng > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + kKvDK, pb + 32 + 8 * kk, qd + ((kk * 2048) >> 4), idesc_g, (ng > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&stage_free[st]);
-          mma_commit(&buf_free[ng & 1]);
+          mma_commit(&pbuf_free[ng & 1]);
           ++ng;
           progressed = true;
         }
@@ -445,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       const int st = j & (kKvStages - 1), b = j & 1;
       // The stage's LSE / D are read from shared memory: wait for its fill
       // too (it has landed once S^T(j) is done, but this makes it visible).
-      if (!mbar_spin(&s_done[b], (j >> 1) & 1) || !mbar_spin(&full[st], (j / kKvStages) & 1)) {
+      if (!mbar_spin(&s_done, j & 1) || !mbar_spin(&full[st], (j / kKvStages) & 1)) {
         ok = false;
         break;
       }
@@ -455,11 +457,14 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       const float* dlt = lse + 64;
       uint32_t pk[16], dk[16];
       uint32_t sv[32], dv[32];
-      const uint32_t sb = lane_addr + kKvBuf * b + 32 * g;  // this warpgroup's S^T columns
-      if (valid) {
-        tmem_ld32_wait(sb, sv);
-        tmem_ld32_wait(sb + kKvDP, dv);
-      }
+      const uint32_t sb = lane_addr + kKvS + 32 * g;  // this warpgroup's S^T columns
+      if (valid) tmem_ld64x2_half(sb, sv, sb + kKvDP, dv);
+      // S^T / dP^T are in registers: the buffer may take S^T(j + 1).
+      tc_fence_before();
+      mbar_arrive(&s_free);
+      // P buffer b is free once dV / dK(j - 2) completed: test now, so that
+      // the answer is in by the time P^T / dS^T are ready.
+      const bool pfree = j < 2 || mbar_test(&pbuf_free[b], ((j >> 1) - 1) & 1);
       if (valid) {
         // P^T = exp2(log2e (S^T scale - LSE)) = exp2((LSE - scale S^T) (-log2e)),
         // dS^T = P^T (dP^T - D), two query columns per packed operation.
@@ -481,17 +486,22 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = dk[i] = 0u;
       }
-      // P^T / dS^T over the S^T / dP^T columns just read (this thread's own
-      // lane; the other warpgroup's columns are untouched).
-      tmem_st8(sb, pk);
-      tmem_st8(sb + 8, pk + 8);
-      tmem_st8(sb + kKvDP, dk);
-      tmem_st8(sb + kKvDP + 8, dk + 8);
+      if (!pfree && !mbar_spin(&pbuf_free[b], ((j >> 1) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      if (j >= 2) tc_fence_after();
+      // P^T / dS^T into P buffer b (this warpgroup's 16 packed columns of each).
+      const uint32_t pb = lane_addr + kKvPB + 64 * b + 16 * g;
+      tmem_st8(pb, pk);
+      tmem_st8(pb + 8, pk + 8);
+      tmem_st8(pb + 32, dk);
+      tmem_st8(pb + 32 + 8, dk + 8);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&pds[b]);
     }
-    if (ok && steps > 0 && !mbar_spin(&buf_free[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
+    if (ok && steps > 0 && !mbar_spin(&pbuf_free[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
     if (!ok) flag_error(p.err, kErrTimeout);
     tc_fence_after();
     // ---------------- dK, dV rows of this key pair (warpgroup 0: dV, 1: dK)
