@@ -96,22 +96,23 @@ def whole_job_tflops(world: int, flops_per_step: float, steps: int, ms: float) -
     return world * flops_per_step * steps / (ms * 1e-3) / 1e12
 
 
-def step_flops(wl: synth.Workload) -> dict:
-    # keys per query: K cubes of N / Nc tokens on average (64 unless the grid
-    # has partial boundary cubes)
-    keys = wl.topk * wl.N / wl.Nc
+def step_flops(wl: synth.Workload, cubes: float = None) -> dict:
+    # keys per query: the listed cubes (K, or the mean list length when the
+    # lists are Top-K united with a neighbourhood) of N / Nc tokens on average
+    # (64 unless the grid has partial boundary cubes)
+    keys = (wl.topk if cubes is None else cubes) * wl.N / wl.Nc
     fine_fwd = 4.0 * wl.N * keys * wl.d * wl.BH
     fine_bwd = 10.0 * wl.N * keys * wl.d * wl.BH
     coarse = 14.0 * wl.Nc * wl.Nc * wl.d * wl.BH
     return dict(fine_fwd=fine_fwd, fine_bwd=fine_bwd, coarse=coarse, total=fine_fwd + fine_bwd + coarse)
 
 
-def kernel_flops(wl: synth.Workload) -> dict:
+def kernel_flops(wl: synth.Workload, cubes: float = None) -> dict:
     """Work each fine kernel does per launch, in products of 2*N*64K*d FLOP per
     (batch, head): forward S and PV (2); backward dK/dV kernel S^T, dP^T, dV,
     dK (4); dQ kernel S, dP, dQ (3).  The effective metric counts 2 + 5: of the
     dQ kernel only its dQ product (dq_product) is new work."""
-    unit = 2.0 * wl.N * (wl.topk * wl.N / wl.Nc) * wl.d * wl.BH
+    unit = 2.0 * wl.N * ((wl.topk if cubes is None else cubes) * wl.N / wl.Nc) * wl.d * wl.BH
     return {"fine_fwd": 2 * unit, "fine_bwd_kv": 4 * unit, "fine_bwd_dq": 3 * unit, "dq_product": unit}
 
 
@@ -133,7 +134,7 @@ def fine_bwd_wall(per_kernel: dict) -> tuple:
     return ms, overlapped
 
 
-def config_of(wl: synth.Workload, parallelism: str, curve: str = "raster") -> dict:
+def config_of(wl: synth.Workload, parallelism: str, curve: str = "raster", radius: int = -1) -> dict:
     return {
         "workload": (f"{wl.name}: B={wl.B}, heads={wl.heads}, d={wl.d}, grid (T,H,W)=({wl.T},{wl.H},{wl.W}) = "
                      f"{wl.N} tokens, {wl.Nc} cubes of (4,4,4), Top-K={wl.topk} "
@@ -148,6 +149,7 @@ def config_of(wl: synth.Workload, parallelism: str, curve: str = "raster") -> di
         "inputs": "synthetic smooth field + noise (synth.py), seed base 20250519",
         "out_dtype": "bf16", "grad_dtype": "bf16",
         "cube_order": curve,
+        "selection": ("Top-K" if radius < 0 else f"Top-K united with the radius-{radius} cube neighbourhood"),
     }
 
 
@@ -361,7 +363,6 @@ def run_ours(args, rank: int, world: int):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = synth.WORKLOADS[args.config]
-    fl = step_flops(wl)
 
     q, k, v = synth.make_qkv(wl)
     gc, gf = synth.make_gates(wl)
@@ -372,15 +373,15 @@ def run_ours(args, rank: int, world: int):
     out = torch.empty_like(dq_)
     grads = dict(dq=torch.empty_like(dq_), dk=torch.empty_like(dq_), dv=torch.empty_like(dq_),
                  dgc=torch.empty_like(dq_), dgf=torch.empty_like(dq_))
-    fws = torch.empty(vsa.workspace_bytes(0, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk),
+    fws = torch.empty(vsa.workspace_bytes(0, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk, args.radius),
                       dtype=torch.uint8, device=dev)
-    bws = torch.empty(vsa.workspace_bytes(1, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk),
+    bws = torch.empty(vsa.workspace_bytes(1, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk, args.radius),
                       dtype=torch.uint8, device=dev)
     order = None if args.curve == "raster" else vsa.cube_order(wl.T, wl.H, wl.W, args.curve, device=dev)
 
     def step(qd, kd, vd, gcd, gfd, dod, res_out=None, res_grads=None):
         _, st = vsa.forward(qd, kd, vd, wl.T, wl.H, wl.W, wl.topk, g_coarse=gcd, g_fine=gfd,
-                            out=out if res_out is None else res_out, ws=fws, cube_order=order)
+                            out=out if res_out is None else res_out, ws=fws, cube_order=order, radius=args.radius)
         vsa.backward(st, dod, g_coarse=gcd, g_fine=gfd, grads=grads if res_grads is None else res_grads, ws=bws)
 
     def barrier():
@@ -391,6 +392,14 @@ def run_ours(args, rank: int, world: int):
         step(dq_, dk_, dv_, dgc_, dgf_, ddo)
     torch.cuda.synchronize()
     assert vsa.device_status() == 0, "device error flag set during warm-up"
+    # Listed cubes per query cube: K, or with a neighbourhood radius the mean
+    # length of the lists the forward selected (the work the method does).
+    cubes = None
+    if args.radius >= 0:
+        _, st0 = vsa.forward(dq_, dk_, dv_, wl.T, wl.H, wl.W, wl.topk, g_coarse=dgc_, g_fine=dgf_, out=out, ws=fws,
+                             cube_order=order, radius=args.radius)
+        cubes = float(st0.saved()["cnt"].float().mean())
+    fl = step_flops(wl, cubes)
     vsa.timing_read()
 
     # ---- timed region: inputs resident in HBM
@@ -419,14 +428,14 @@ def run_ours(args, rank: int, world: int):
     # beside the headline; not part of it.
     fwd_only = None
     if world == 1 and not args.no_forward_only:
-        iws = torch.empty(vsa.workspace_bytes(3, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk), dtype=torch.uint8,
-                          device=dev)
+        iws = torch.empty(vsa.workspace_bytes(3, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk, args.radius),
+                          dtype=torch.uint8, device=dev)
         runs = {
             "forward": lambda: vsa.forward(dq_, dk_, dv_, wl.T, wl.H, wl.W, wl.topk, g_coarse=dgc_, g_fine=dgf_,
-                                           out=out, ws=fws, cube_order=order),
+                                           out=out, ws=fws, cube_order=order, radius=args.radius),
             "forward_inference": lambda: vsa.forward_inference(dq_, dk_, dv_, wl.T, wl.H, wl.W, wl.topk,
                                                                g_coarse=dgc_, g_fine=dgf_, out=out, ws=iws,
-                                                               cube_order=order),
+                                                               cube_order=order, radius=args.radius),
         }
         fwd_only = {}
         for name, fn in runs.items():
@@ -507,7 +516,7 @@ def run_ours(args, rank: int, world: int):
     value = whole_job_tflops(world, fl["total"], args.steps, ms)
     per_kernel = {n: round(t / max(c, 1), 4) for n, (t, c) in kern.items()}
     launches = {n: c for n, (t, c) in kern.items()}
-    kflops = kernel_flops(wl)
+    kflops = kernel_flops(wl, cubes)
     # The roofline is reported for the kernel with the most work per step.
     dominant = max(("fine_fwd", "fine_bwd_kv", "fine_bwd_dq"), key=lambda n: kflops[n])
     traffic = None  # DRAM bytes per launch from the committed ncu capture (profiles/traffic.txt)
@@ -527,7 +536,7 @@ def run_ours(args, rank: int, world: int):
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded smooth field + noise; Wan2.1 activations are not available)",
-        "config": config_of(wl, "replicas" if world > 1 else "single GPU", args.curve),
+        "config": config_of(wl, "replicas" if world > 1 else "single GPU", args.curve, args.radius),
         "pct_of_peak": round(100 * value / world / peak, 2),
         "roofline": {"bound": "tensor", "kernel": dominant, "achieved": dom["tflops"], "peak": peak,
                      "unit": "TFLOP/s", "frac": dom["frac"], "traffic": traffic,
@@ -616,6 +625,8 @@ def main():
     ap.add_argument("--config-cpu-seconds", type=float, default=3.0, help="oracle sample per other workload")
     ap.add_argument("--curve", choices=["raster", "hilbert"], default="raster",
                     help="cube order of the space-filling-curve reordering")
+    ap.add_argument("--radius", type=int, default=-1,
+                    help="unite each Top-K list with the radius-r cube neighbourhood (-1: Top-K alone)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

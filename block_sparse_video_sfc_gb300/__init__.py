@@ -136,8 +136,8 @@ def fine_fwd(qp, kp, vp, idx, cnt, scale: Optional[float] = None, out_dtype=torc
     return of, lse
 
 
-def workspace_bytes(op: int, B: int, heads: int, d: int, T: int, H: int, W: int, topk: int) -> int:
-    return int(_lib.load().vsa_workspace_bytes(op, B, heads, d, Grid.of(T, H, W), topk))
+def workspace_bytes(op: int, B: int, heads: int, d: int, T: int, H: int, W: int, topk: int, radius: int = -1) -> int:
+    return int(_lib.load().vsa_workspace_bytes(op, B, heads, d, Grid.of(T, H, W), topk, radius))
 
 
 def fine_bwd(qp, kp, vp, of, lse, dof, idx, cnt, scale: Optional[float] = None):
@@ -170,14 +170,15 @@ class ForwardState:
     topk: int
     scale: float
     cube_order: Optional[torch.Tensor] = None
+    radius: int = -1
 
     def saved(self) -> dict:
         """Views of the saved intermediates as torch tensors."""
         s = _lib.Saved()
         _lib.check("vsa_forward_saved", _lib.load().vsa_forward_saved(
-            _ptr(self.ws), self.B, self.heads, self.d, Grid.of(self.T, self.H, self.W), self.topk,
+            _ptr(self.ws), self.B, self.heads, self.d, Grid.of(self.T, self.H, self.W), self.topk, self.radius,
             ctypes.byref(s)))
-        BH, d, K = self.B * self.heads, self.d, self.topk
+        BH, d, K = self.B * self.heads, self.d, s.max_kv_blocks
         Nc = num_cubes(self.T, self.H, self.W)
         N = 64 * Nc  # reordered length (padding slots included)
         base = self.ws.data_ptr()
@@ -203,11 +204,13 @@ class ForwardState:
 
 
 def forward(q, k, v, T: int, H: int, W: int, topk: int, g_coarse=None, g_fine=None,
-            scale: Optional[float] = None, out_dtype=torch.bfloat16, out=None, ws=None, cube_order=None):
-    """vsa_forward on native-order [B, heads, N, d] bf16 -> (out, ForwardState)."""
+            scale: Optional[float] = None, out_dtype=torch.bfloat16, out=None, ws=None, cube_order=None,
+            radius: int = -1):
+    """vsa_forward on native-order [B, heads, N, d] bf16 -> (out, ForwardState).
+    radius >= 0 unites each Top-K list with the radius-r cube neighbourhood."""
     B, heads, N, d = q.shape
     scale = d ** -0.5 if scale is None else scale
-    nbytes = workspace_bytes(_lib.VSA_OP_FORWARD, B, heads, d, T, H, W, topk)
+    nbytes = workspace_bytes(_lib.VSA_OP_FORWARD, B, heads, d, T, H, W, topk, radius)
     if nbytes == 0:
         raise VSAError("vsa_workspace_bytes", _lib.VSA_ERR_ARG)
     if ws is None or ws.numel() < nbytes:
@@ -216,17 +219,18 @@ def forward(q, k, v, T: int, H: int, W: int, topk: int, g_coarse=None, g_fine=No
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     _lib.check("vsa_forward", _lib.load().vsa_forward(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g_coarse), _ptr(g_fine), B, heads, d, Grid.of(T, H, W, _ptr(cube_order)), topk,
-        float(scale), _ptr(out), _DT[out.dtype], _ptr(ws), nbytes, _stream()))
-    return out, ForwardState(ws, B, heads, d, T, H, W, topk, scale, cube_order)
+        radius, float(scale), _ptr(out), _DT[out.dtype], _ptr(ws), nbytes, _stream()))
+    return out, ForwardState(ws, B, heads, d, T, H, W, topk, scale, cube_order, radius)
 
 
 def forward_inference(q, k, v, T: int, H: int, W: int, topk: int, g_coarse=None, g_fine=None,
-                      scale: Optional[float] = None, out_dtype=torch.bfloat16, out=None, ws=None, cube_order=None):
+                      scale: Optional[float] = None, out_dtype=torch.bfloat16, out=None, ws=None, cube_order=None,
+                      radius: int = -1):
     """vsa_forward_inference: the forward output without saved state; the fine
     stage reads Q, K, V in their native layout (no reordered copies)."""
     B, heads, N, d = q.shape
     scale = d ** -0.5 if scale is None else scale
-    nbytes = workspace_bytes(_lib.VSA_OP_FORWARD_INFERENCE, B, heads, d, T, H, W, topk)
+    nbytes = workspace_bytes(_lib.VSA_OP_FORWARD_INFERENCE, B, heads, d, T, H, W, topk, radius)
     if nbytes == 0:
         raise VSAError("vsa_workspace_bytes", _lib.VSA_ERR_ARG)
     if ws is None or ws.numel() < nbytes:
@@ -235,7 +239,7 @@ def forward_inference(q, k, v, T: int, H: int, W: int, topk: int, g_coarse=None,
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     _lib.check("vsa_forward_inference", _lib.load().vsa_forward_inference(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g_coarse), _ptr(g_fine), B, heads, d, Grid.of(T, H, W, _ptr(cube_order)),
-        topk, float(scale), _ptr(out), _DT[out.dtype], _ptr(ws), nbytes, _stream()))
+        topk, radius, float(scale), _ptr(out), _DT[out.dtype], _ptr(ws), nbytes, _stream()))
     return out
 
 
@@ -243,7 +247,7 @@ def backward(state: ForwardState, dout, g_coarse=None, g_fine=None, grad_dtype=t
              grads=None, ws=None):
     """vsa_backward -> dict(dq, dk, dv, dgc, dgf) in native order."""
     B, heads, d = state.B, state.heads, state.d
-    nbytes = workspace_bytes(_lib.VSA_OP_BACKWARD, B, heads, d, state.T, state.H, state.W, state.topk)
+    nbytes = workspace_bytes(_lib.VSA_OP_BACKWARD, B, heads, d, state.T, state.H, state.W, state.topk, state.radius)
     if ws is None or ws.numel() < nbytes:
         ws = torch.empty(nbytes, dtype=torch.uint8, device=dout.device)
     if grads is None:
@@ -253,7 +257,8 @@ def backward(state: ForwardState, dout, g_coarse=None, g_fine=None, grad_dtype=t
     dt = grads["dq"].dtype
     _lib.check("vsa_backward", _lib.load().vsa_backward(
         _ptr(state.ws), _ptr(g_coarse), _ptr(g_fine), _ptr(dout), B, heads, d,
-        Grid.of(state.T, state.H, state.W, _ptr(state.cube_order)), state.topk, float(state.scale), _ptr(grads["dq"]),
+        Grid.of(state.T, state.H, state.W, _ptr(state.cube_order)), state.topk, state.radius, float(state.scale),
+        _ptr(grads["dq"]),
         _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads.get("dgc")), _ptr(grads.get("dgf")), _DT[dt],
         _ptr(ws), nbytes, _stream()))
     return grads
@@ -264,7 +269,8 @@ def backward_tile_pairs(state: ForwardState, ws: torch.Tensor) -> torch.Tensor:
     that the dK/dV kernel's tiles used in the backward call made with `ws`."""
     ptr = ctypes.c_void_p()
     _lib.check("vsa_backward_tile_pairs", _lib.load().vsa_backward_tile_pairs(
-        _ptr(ws), state.B, state.heads, state.d, Grid.of(state.T, state.H, state.W), state.topk, ctypes.byref(ptr)))
+        _ptr(ws), state.B, state.heads, state.d, Grid.of(state.T, state.H, state.W), state.topk, state.radius,
+        ctypes.byref(ptr)))
     Nc = num_cubes(state.T, state.H, state.W)
     n = state.B * state.heads * ((Nc + 1) // 2) * 2
     off = ptr.value - ws.data_ptr()

@@ -51,10 +51,11 @@ class Grid(ctypes.Structure):
 
 
 class Saved(ctypes.Structure):
-    """vsa_saved_t: device pointers into a forward workspace."""
+    """vsa_saved_t: device pointers into a forward workspace, and the list width."""
 
     _fields_ = [(n, P) for n in ("qp", "kp", "vp", "qc", "kc", "vc", "o_coarse", "lse_coarse",
-                                 "kv_block_idx", "valid_block_num", "o_fine", "lse", "tile_pairs")]
+                                 "kv_block_idx", "valid_block_num", "o_fine", "lse", "tile_pairs")] + \
+        [("max_kv_blocks", I)]
 
 
 SIGNATURES = {
@@ -64,12 +65,12 @@ SIGNATURES = {
     "vsa_fine_fwd": ([P, P, P, P, P, I, I, I, I, F, P, I, P, P], I),
     "vsa_fine_bwd": ([P, P, P, P, I, P, P, P, P, I, I, I, I, F, P, P, P, P, SZ, P], I),
     "vsa_fine_bwd_noalloc": ([P, P, P, P, I, P, P, P, P, I, I, I, I, F, P, P, P, P], I),
-    "vsa_forward": ([P, P, P, P, P, I, I, I, Grid, I, F, P, I, P, SZ, P], I),
-    "vsa_forward_inference": ([P, P, P, P, P, I, I, I, Grid, I, F, P, I, P, SZ, P], I),
-    "vsa_backward": ([P, P, P, P, I, I, I, Grid, I, F, P, P, P, P, P, I, P, SZ, P], I),
-    "vsa_workspace_bytes": ([I, I, I, I, Grid, I], SZ),
-    "vsa_forward_saved": ([P, I, I, I, Grid, I, ctypes.POINTER(Saved)], I),
-    "vsa_backward_tile_pairs": ([P, I, I, I, Grid, I, ctypes.POINTER(P)], I),
+    "vsa_forward": ([P, P, P, P, P, I, I, I, Grid, I, I, F, P, I, P, SZ, P], I),
+    "vsa_forward_inference": ([P, P, P, P, P, I, I, I, Grid, I, I, F, P, I, P, SZ, P], I),
+    "vsa_backward": ([P, P, P, P, I, I, I, Grid, I, I, F, P, P, P, P, P, I, P, SZ, P], I),
+    "vsa_workspace_bytes": ([I, I, I, I, Grid, I, I], SZ),
+    "vsa_forward_saved": ([P, I, I, I, Grid, I, I, ctypes.POINTER(Saved)], I),
+    "vsa_backward_tile_pairs": ([P, I, I, I, Grid, I, I, ctypes.POINTER(P)], I),
     "vsa_device_status": ([P], I),
     "vsa_selftest_wait_timeout": ([ctypes.c_uint32, P], I),
     "vsa_mask_to_lut": ([P, I, I, I, P, P, P], I),

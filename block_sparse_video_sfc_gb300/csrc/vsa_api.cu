@@ -41,13 +41,34 @@ int check_grid(const vsa_grid_t& g, int d, Dims* out, int64_t BH) {
   return VSA_OK;
 }
 
+template <typename T>
+T* at(const void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(const_cast<void*>(base)) + off);
+}
+
+// Width of the selection lists: the Top-K alone (radius < 0), or with room
+// for the radius-r cube neighbourhood added ((2r + 1)^3 cubes at most).
+int list_width(int topk, int radius, int64_t Nc) {
+  if (radius < 0) return topk;
+  const int64_t n = static_cast<int64_t>(topk) + (2 * radius + 1) * (2 * radius + 1) * (2 * radius + 1);
+  return static_cast<int>(n < Nc ? n : Nc);
+}
+int check_selection(const Dims& D, int topk, int radius) {
+  if (topk < 1 || topk > D.Nc) return VSA_ERR_ARG;
+  if (radius < -1 || radius > 7) return VSA_ERR_ARG;
+  return VSA_OK;
+}
+
 // Forward workspace: the saved state of one vsa_forward call.
 struct FwdWs {
-  size_t qp, kp, vp, qc, kc, vc, oc, lsec, sc, idx, cnt, of, lse, lbits, pairs, kmask, total;
+  size_t qp, kp, vp, qc, kc, vc, oc, lsec, sc, idx, cnt, of, lse, lbits, pairs, kmask, idx_tk, total;
+  int kmax;  // width of the saved lists
 };
 // copies = false: the inference forward, which reads Q, K, V in place.
-FwdWs fwd_layout(const Dims& D, int K, bool copies = true) {
+FwdWs fwd_layout(const Dims& D, int topk, int radius, bool copies = true) {
   FwdWs w{};
+  const int K = list_width(topk, radius, D.Nc);
+  w.kmax = K;
   size_t o = 0;
   const size_t big_bf16 = copies ? sizeof(__half) * D.BH * D.N * D.d : 0;  // fp16 copies of Q, K, V
   const size_t pooled = sizeof(float) * D.BH * D.Nc * D.d;
@@ -67,8 +88,25 @@ FwdWs fwd_layout(const Dims& D, int K, bool copies = true) {
   w.lbits = o; o += align256(sizeof(uint32_t) * D.BH * D.Nc * ((D.Nc + 31) / 32));
   w.pairs = o; o += align256(pair_plan_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.Nc)));
   w.kmask = o; o += align256(sizeof(uint64_t) * D.Nc);
+  w.idx_tk = o; o += radius >= 0 ? align256(sizeof(int32_t) * D.BH * D.Nc * topk) : 0;  // the Top-K before the union
   w.total = o;
   return w;
+}
+
+// The selection of vsa_forward / vsa_forward_inference: Top-K lists into the
+// saved lists, or, with a radius, into scratch and then united with each
+// query cube's neighbourhood (ascending lists with counts).
+int select_lists(const float* qc, const float* kc, const float* vc, const Dims& D, const vsa_grid_t& g, int topk,
+                 int radius, float scale, const FwdWs& w, void* ws, cudaStream_t s) {
+  const int BH = static_cast<int>(D.BH), Nc = static_cast<int>(D.Nc);
+  int32_t* idx = at<int32_t>(ws, w.idx);
+  int32_t* cnt = at<int32_t>(ws, w.cnt);
+  int st = launch_coarse_topk(qc, kc, vc, BH, Nc, D.d, topk, scale, nullptr, at<float>(ws, w.lsec),
+                              radius >= 0 ? at<int32_t>(ws, w.idx_tk) : idx, radius >= 0 ? nullptr : cnt,
+                              at<float>(ws, w.sc), s);
+  if (st != VSA_OK || radius < 0) return st;
+  return launch_add_neighbors(at<int32_t>(ws, w.idx_tk), nullptr, topk, BH, (g.T + 3) / 4, (g.H + 3) / 4,
+                              (g.W + 3) / 4, g.cube_order, radius, w.kmax, idx, cnt, s);
 }
 
 // Backward workspace (scratch of one vsa_backward call).
@@ -92,11 +130,6 @@ BwdWs bwd_layout(const Dims& D) {
   w.kpairs = o; o += align256(pair_plan_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.Nc)));
   w.total = o;
   return w;
-}
-
-template <typename T>
-T* at(const void* base, size_t off) {
-  return reinterpret_cast<T*>(static_cast<uint8_t*>(const_cast<void*>(base)) + off);
 }
 
 struct TimedLaunch {
@@ -371,27 +404,28 @@ int vsa_fine_bwd(const void* qp, const void* kp, const void* vp, const void* o_f
                          BH, N, d, scale, dq, dk, dv, ws, ws_bytes, as_stream(stream));
 }
 
-size_t vsa_workspace_bytes(int op, int B, int heads, int d, vsa_grid_t g, int topk) {
+size_t vsa_workspace_bytes(int op, int B, int heads, int d, vsa_grid_t g, int topk, int radius) {
   Dims D;
   if (B <= 0 || heads <= 0) return 0;
   if (check_grid(g, d, &D, static_cast<int64_t>(B) * heads) != VSA_OK) return 0;
-  if (topk < 1 || topk > D.Nc) return 0;
+  if (check_selection(D, topk, op == VSA_OP_FINE_BWD ? -1 : radius) != VSA_OK) return 0;
   switch (op) {
-    case VSA_OP_FORWARD: return fwd_layout(D, topk).total;
+    case VSA_OP_FORWARD: return fwd_layout(D, topk, radius).total;
     case VSA_OP_BACKWARD: return bwd_layout(D).total;
     case VSA_OP_FINE_BWD: return fine_bwd_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.N), topk);
-    case VSA_OP_FORWARD_INFERENCE: return fwd_layout(D, topk, false).total;
+    case VSA_OP_FORWARD_INFERENCE: return fwd_layout(D, topk, radius, false).total;
     default: return 0;
   }
 }
 
-int vsa_forward_saved(const void* fwd_ws, int B, int heads, int d, vsa_grid_t g, int topk, vsa_saved_t* out) {
+int vsa_forward_saved(const void* fwd_ws, int B, int heads, int d, vsa_grid_t g, int topk, int radius,
+                      vsa_saved_t* out) {
   Dims D;
   if (!fwd_ws || !out || B <= 0 || heads <= 0) return VSA_ERR_ARG;
   int st = check_grid(g, d, &D, static_cast<int64_t>(B) * heads);
   if (st != VSA_OK) return st;
-  if (topk < 1 || topk > D.Nc) return VSA_ERR_ARG;
-  FwdWs w = fwd_layout(D, topk);
+  if ((st = check_selection(D, topk, radius)) != VSA_OK) return st;
+  FwdWs w = fwd_layout(D, topk, radius);
   out->qp = at<void>(fwd_ws, w.qp);
   out->kp = at<void>(fwd_ws, w.kp);
   out->vp = at<void>(fwd_ws, w.vp);
@@ -405,45 +439,44 @@ int vsa_forward_saved(const void* fwd_ws, int B, int heads, int d, vsa_grid_t g,
   out->o_fine = at<float>(fwd_ws, w.of);
   out->lse = at<float>(fwd_ws, w.lse);
   out->tile_pairs = at<int32_t>(fwd_ws, w.pairs);
+  out->max_kv_blocks = w.kmax;
   return VSA_OK;
 }
 
-int vsa_backward_tile_pairs(const void* bwd_ws, int B, int heads, int d, vsa_grid_t g, int topk,
+int vsa_backward_tile_pairs(const void* bwd_ws, int B, int heads, int d, vsa_grid_t g, int topk, int radius,
                             int32_t** key_pairs) {
   Dims D;
   if (!bwd_ws || !key_pairs || B <= 0 || heads <= 0) return VSA_ERR_ARG;
   int st = check_grid(g, d, &D, static_cast<int64_t>(B) * heads);
   if (st != VSA_OK) return st;
-  if (topk < 1 || topk > D.Nc) return VSA_ERR_ARG;
+  if ((st = check_selection(D, topk, radius)) != VSA_OK) return st;
   *key_pairs = at<int32_t>(bwd_ws, bwd_layout(D).kpairs);
   return VSA_OK;
 }
 
 int vsa_forward(const void* q, const void* k, const void* v, const void* g_coarse, const void* g_fine, int B,
-                int heads, int d, vsa_grid_t g, int topk, float scale, void* out, int out_dtype, void* ws,
+                int heads, int d, vsa_grid_t g, int topk, int radius, float scale, void* out, int out_dtype, void* ws,
                 size_t ws_bytes, void* stream) {
   Dims D;
   if (B <= 0 || heads <= 0) return VSA_ERR_ARG;
   int st = check_grid(g, d, &D, static_cast<int64_t>(B) * heads);
   if (st != VSA_OK) return st;
-  if (topk < 1 || topk > D.Nc) return VSA_ERR_ARG;
+  if ((st = check_selection(D, topk, radius)) != VSA_OK) return st;
   if (!q || !k || !v || !out) return VSA_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (g_coarse && !aligned16(g_coarse)) ||
       (g_fine && !aligned16(g_fine)))
     return VSA_ERR_ARG;
   if (out_dtype != VSA_DTYPE_BF16 && out_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
-  FwdWs w = fwd_layout(D, topk);
+  FwdWs w = fwd_layout(D, topk, radius);
   if (!ws || ws_bytes < w.total || !aligned16(ws)) return VSA_ERR_WORKSPACE;
   cudaStream_t s = as_stream(stream);
   const int BH = static_cast<int>(D.BH), Nc = static_cast<int>(D.Nc), N = static_cast<int>(D.N);
+  const int kmax = w.kmax;
   const void* src[3] = {q, k, v};
   void* dst[3] = {at<void>(ws, w.qp), at<void>(ws, w.kp), at<void>(ws, w.vp)};
   float* pooled[3] = {at<float>(ws, w.qc), at<float>(ws, w.kc), at<float>(ws, w.vc)};
   if ((st = launch_permute(src, dst, pooled, 3, BH, d, g.T, g.H, g.W, g.cube_order, 0, 1, s)) != VSA_OK) return st;
-  if ((st = launch_coarse_topk(pooled[0], pooled[1], pooled[2], BH, Nc, d, topk, scale, nullptr,
-                               at<float>(ws, w.lsec), at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt),
-                               at<float>(ws, w.sc), s)) != VSA_OK)
-    return st;
+  if ((st = select_lists(pooled[0], pooled[1], pooled[2], D, g, topk, radius, scale, w, ws, s)) != VSA_OK) return st;
   // O_c is needed only by the combine: it runs on the auxiliary stream beside
   // the pair planning and the fine kernel, and joins before the combine.
   AuxStream* aux = aux_stream();
@@ -460,14 +493,14 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
     return st;
   if (aux && cudaEventRecord(aux->join, s_oc) != cudaSuccess) return VSA_ERR_CUDA;
   // Pair query cubes whose lists overlap most into the fine kernels' tiles.
-  if ((st = launch_list_bits(at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), topk, BH, Nc, at<uint32_t>(ws, w.lbits),
+  if ((st = launch_list_bits(at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), kmax, BH, Nc, at<uint32_t>(ws, w.lbits),
                              s)) != VSA_OK)
     return st;
   if ((st = launch_pair_plan(at<uint32_t>(ws, w.lbits), BH, Nc, at<int32_t>(ws, w.pairs), s)) != VSA_OK) return st;
   // Padding slots of partial cubes are masked out of the keys.
   uint64_t* kmask = D.padded ? at<uint64_t>(ws, w.kmask) : nullptr;
   if (kmask && (st = launch_slot_masks(g.T, g.H, g.W, g.cube_order, kmask, s)) != VSA_OK) return st;
-  if ((st = launch_fine_fwd(dst[0], dst[1], dst[2], at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), topk, BH, N, d,
+  if ((st = launch_fine_fwd(dst[0], dst[1], dst[2], at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), kmax, BH, N, d,
                             scale, at<float>(ws, w.of), VSA_DTYPE_F32, at<float>(ws, w.lse), 1,
                             at<int32_t>(ws, w.pairs), kmask, s)) != VSA_OK)
     return st;
@@ -477,31 +510,29 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
 }
 
 int vsa_forward_inference(const void* q, const void* k, const void* v, const void* g_coarse, const void* g_fine,
-                          int B, int heads, int d, vsa_grid_t g, int topk, float scale, void* out, int out_dtype,
-                          void* ws, size_t ws_bytes, void* stream) {
+                          int B, int heads, int d, vsa_grid_t g, int topk, int radius, float scale, void* out,
+                          int out_dtype, void* ws, size_t ws_bytes, void* stream) {
   Dims D;
   if (B <= 0 || heads <= 0) return VSA_ERR_ARG;
   int st = check_grid(g, d, &D, static_cast<int64_t>(B) * heads);
   if (st != VSA_OK) return st;
-  if (topk < 1 || topk > D.Nc) return VSA_ERR_ARG;
+  if ((st = check_selection(D, topk, radius)) != VSA_OK) return st;
   if (!q || !k || !v || !out) return VSA_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (g_coarse && !aligned16(g_coarse)) ||
       (g_fine && !aligned16(g_fine)))
     return VSA_ERR_ARG;
   if (out_dtype != VSA_DTYPE_BF16 && out_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
-  FwdWs w = fwd_layout(D, topk, false);
+  FwdWs w = fwd_layout(D, topk, radius, false);
   if (!ws || ws_bytes < w.total || !aligned16(ws)) return VSA_ERR_WORKSPACE;
   cudaStream_t s = as_stream(stream);
   const int BH = static_cast<int>(D.BH), Nc = static_cast<int>(D.Nc);
+  const int kmax = w.kmax;
   // Cube means only: the fine kernel reads Q, K, V in their native layout.
   const void* src[3] = {q, k, v};
   void* none[3] = {nullptr, nullptr, nullptr};
   float* pooled[3] = {at<float>(ws, w.qc), at<float>(ws, w.kc), at<float>(ws, w.vc)};
   if ((st = launch_permute(src, none, pooled, 3, BH, d, g.T, g.H, g.W, g.cube_order, 0, 0, s)) != VSA_OK) return st;
-  if ((st = launch_coarse_topk(pooled[0], pooled[1], pooled[2], BH, Nc, d, topk, scale, nullptr,
-                               at<float>(ws, w.lsec), at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt),
-                               at<float>(ws, w.sc), s)) != VSA_OK)
-    return st;
+  if ((st = select_lists(pooled[0], pooled[1], pooled[2], D, g, topk, radius, scale, w, ws, s)) != VSA_OK) return st;
   // O_c is needed only by the combine: it runs on the auxiliary stream beside
   // the pair planning and the fine kernel, and joins before the combine.
   AuxStream* aux = aux_stream();
@@ -517,14 +548,14 @@ int vsa_forward_inference(const void* q, const void* k, const void* v, const voi
                              s_oc)) != VSA_OK)
     return st;
   if (aux && cudaEventRecord(aux->join, s_oc) != cudaSuccess) return VSA_ERR_CUDA;
-  if ((st = launch_list_bits(at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), topk, BH, Nc, at<uint32_t>(ws, w.lbits),
+  if ((st = launch_list_bits(at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), kmax, BH, Nc, at<uint32_t>(ws, w.lbits),
                              s)) != VSA_OK)
     return st;
   if ((st = launch_pair_plan(at<uint32_t>(ws, w.lbits), BH, Nc, at<int32_t>(ws, w.pairs), s)) != VSA_OK) return st;
   uint64_t* kmask = D.padded ? at<uint64_t>(ws, w.kmask) : nullptr;
   if (kmask && (st = launch_slot_masks(g.T, g.H, g.W, g.cube_order, kmask, s)) != VSA_OK) return st;
   if ((st = launch_fine_fwd_native(q, k, v, g.T, g.H, g.W, g.cube_order, at<int32_t>(ws, w.idx),
-                                   at<int32_t>(ws, w.cnt), topk, BH, d, scale, at<float>(ws, w.of), VSA_DTYPE_F32,
+                                   at<int32_t>(ws, w.cnt), kmax, BH, d, scale, at<float>(ws, w.of), VSA_DTYPE_F32,
                                    at<float>(ws, w.lse), at<int32_t>(ws, w.pairs), kmask, s)) != VSA_OK)
     return st;
   if (aux && cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess) return VSA_ERR_CUDA;
@@ -533,13 +564,13 @@ int vsa_forward_inference(const void* q, const void* k, const void* v, const voi
 }
 
 int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, const void* dout, int B, int heads,
-                 int d, vsa_grid_t g, int topk, float scale, void* dq, void* dk, void* dv, void* dg_coarse,
+                 int d, vsa_grid_t g, int topk, int radius, float scale, void* dq, void* dk, void* dv, void* dg_coarse,
                  void* dg_fine, int grad_dtype, void* ws, size_t ws_bytes, void* stream) {
   Dims D;
   if (B <= 0 || heads <= 0) return VSA_ERR_ARG;
   int st = check_grid(g, d, &D, static_cast<int64_t>(B) * heads);
   if (st != VSA_OK) return st;
-  if (topk < 1 || topk > D.Nc) return VSA_ERR_ARG;
+  if ((st = check_selection(D, topk, radius)) != VSA_OK) return st;
   if (!fwd_ws || !dout || !dq || !dk || !dv) return VSA_ERR_ARG;
   if (!aligned16(fwd_ws) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       (g_coarse && !aligned16(g_coarse)) || (g_fine && !aligned16(g_fine)) || (dg_coarse && !aligned16(dg_coarse)) ||
@@ -548,7 +579,7 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
   if (grad_dtype != VSA_DTYPE_BF16 && grad_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
   BwdWs w = bwd_layout(D);
   if (!ws || ws_bytes < w.total || !aligned16(ws)) return VSA_ERR_WORKSPACE;
-  FwdWs f = fwd_layout(D, topk);
+  FwdWs f = fwd_layout(D, topk, radius);
   cudaStream_t s = as_stream(stream);
   const int BH = static_cast<int>(D.BH), Nc = static_cast<int>(D.Nc), N = static_cast<int>(D.N);
   // Fork at the start: the dK/dV chain on the auxiliary stream (highest
@@ -589,7 +620,7 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
                 g.cube_order};
   if ((st = launch_fine_bwd_core(at<void>(fwd_ws, f.qp), at<void>(fwd_ws, f.kp), at<void>(fwd_ws, f.vp),
                                  at<void>(ws, w.dof), at<float>(fwd_ws, f.lse), at<float>(ws, w.delta),
-                                 at<int32_t>(fwd_ws, f.idx), at<int32_t>(fwd_ws, f.cnt), topk, BH, N, d, scale,
+                                 at<int32_t>(fwd_ws, f.idx), at<int32_t>(fwd_ws, f.cnt), f.kmax, BH, N, d, scale,
                                  nullptr, nullptr, nullptr, &fg, at<uint32_t>(ws, w.inv), at<int32_t>(fwd_ws, f.pairs),
                                  at<int32_t>(ws, w.kpairs), s, s_kv, aux ? aux->mid : nullptr)) != VSA_OK)
     return st;

@@ -226,6 +226,15 @@ int vsa_fine_bwd_noalloc(const void* qp, const void* kp, const void* vp, const v
  * the 64 tokens of its cube.
  *   q, k, v     bf16 [B, heads, N, d] native order.
  *   g_coarse, g_fine  bf16 [B, heads, N, d] native order, or NULL (= ones).
+ *   topk        1 <= topk <= Nc: the Top-K of each coarse score row.
+ *   radius      -1: the selection is the Top-K alone (rows in descending
+ *               score).  0..7: the Top-K united with every cube whose (t, h,
+ *               w) cube coordinates each differ from the query cube's by at
+ *               most radius (the query cube included) -- [AMD] "Comparison
+ *               with Jenga", "Algorithmic Design": block selection as the union
+ *               of an importance mask and an adjacency mask; the rows are then
+ *               ascending with per-row counts, max_kv_blocks = min(Nc, topk +
+ *               (2 radius + 1)^3) wide.  vsa_backward uses the same lists.
  *   scale       score scale for both stages (1/sqrt(d) for SDPA).
  *   out         [B, heads, N, d] native order, dtype out_dtype.
  *   ws          workspace of vsa_workspace_bytes(VSA_OP_FORWARD, ...) bytes.
@@ -233,7 +242,7 @@ int vsa_fine_bwd_noalloc(const void* qp, const void* kp, const void* vp, const v
  *               keep it unchanged until the matching vsa_backward is done.
  */
 int vsa_forward(const void* q, const void* k, const void* v, const void* g_coarse, const void* g_fine, int B,
-                int heads, int d, vsa_grid_t g, int topk, float scale, void* out, int out_dtype, void* ws,
+                int heads, int d, vsa_grid_t g, int topk, int radius, float scale, void* out, int out_dtype, void* ws,
                 size_t ws_bytes, void* stream);
 
 /*
@@ -249,13 +258,14 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
  * that rounding, well within the parity tolerance.
  */
 int vsa_forward_inference(const void* q, const void* k, const void* v, const void* g_coarse, const void* g_fine,
-                          int B, int heads, int d, vsa_grid_t g, int topk, float scale, void* out, int out_dtype,
-                          void* ws, size_t ws_bytes, void* stream);
+                          int B, int heads, int d, vsa_grid_t g, int topk, int radius, float scale, void* out,
+                          int out_dtype, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * vsa_backward -- gradients of vsa_forward.  [ABS].
  *   fwd_ws      the workspace the forward call filled (read only).
- *   g_coarse, g_fine, B, heads, d, g, topk, scale: the same as in the forward.
+ *   g_coarse, g_fine, B, heads, d, g, topk, radius, scale: the same as in the
+ *               forward (the selection lists it saved are held constant).
  *   dout        bf16 [B, heads, N, d] native order: dL/dout.
  *   dq, dk, dv  [B, heads, N, d] native order, dtype grad_dtype.
  *   dg_coarse, dg_fine  [B, heads, N, d] native, dtype grad_dtype; may be NULL,
@@ -271,14 +281,15 @@ int vsa_forward_inference(const void* q, const void* k, const void* v, const voi
  * time from several host threads take their turn at the fork.
  */
 int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, const void* dout, int B,
-                 int heads, int d, vsa_grid_t g, int topk, float scale, void* dq, void* dk, void* dv,
+                 int heads, int d, vsa_grid_t g, int topk, int radius, float scale, void* dq, void* dk, void* dv,
                  void* dg_coarse, void* dg_fine, int grad_dtype, void* ws, size_t ws_bytes, void* stream);
 
 enum { VSA_OP_FORWARD = 0, VSA_OP_BACKWARD = 1, VSA_OP_FINE_BWD = 2, VSA_OP_FORWARD_INFERENCE = 3 };
 
-/* Workspace bytes for an operation (0 on a bad argument).  For
- * VSA_OP_FINE_BWD, B*heads is BH and g/topk give N and max_kv_blocks. */
-size_t vsa_workspace_bytes(int op, int B, int heads, int d, vsa_grid_t g, int topk);
+/* Workspace bytes for an operation (0 on a bad argument); topk and radius as
+ * in vsa_forward.  For VSA_OP_FINE_BWD, B*heads is BH, g/topk give N and
+ * max_kv_blocks, and radius is ignored. */
+size_t vsa_workspace_bytes(int op, int B, int heads, int d, vsa_grid_t g, int topk, int radius);
 
 /* Device pointers into a forward workspace (the saved state), for callers
  * that want the intermediate results. */
@@ -291,21 +302,23 @@ typedef struct {
     float* vc;
     float* o_coarse;   /* fp32 [BH, Nc, d] */
     float* lse_coarse; /* fp32 [BH, Nc] */
-    int32_t* kv_block_idx;    /* [BH, Nc, topk] */
+    int32_t* kv_block_idx;    /* [BH, Nc, max_kv_blocks] the selection lists */
     int32_t* valid_block_num; /* [BH, Nc] */
     float* o_fine;     /* fp32 [BH, N, d] cube order */
     float* lse;        /* fp32 [BH, N] */
     int32_t* tile_pairs; /* [BH, (Nc + 1) / 2, 2] query cubes of each fine-kernel tile
                             (second -1: a lone cube); a scheduling choice, not a result */
+    int max_kv_blocks;   /* width of the lists: topk, or min(Nc, topk + (2 radius + 1)^3) */
 } vsa_saved_t;
 
-int vsa_forward_saved(const void* fwd_ws, int B, int heads, int d, vsa_grid_t g, int topk, vsa_saved_t* out);
+int vsa_forward_saved(const void* fwd_ws, int B, int heads, int d, vsa_grid_t g, int topk, int radius,
+                      vsa_saved_t* out);
 
 /* Device pointer into a backward workspace after vsa_backward: the key-cube
  * pairs of the dK/dV kernel's tiles, int32 [BH, (Nc + 1) / 2, 2] (second -1:
  * a lone cube).  A scheduling choice, not a result: each tile computes dK and
  * dV of its two key cubes over the union of their inverse lists. */
-int vsa_backward_tile_pairs(const void* bwd_ws, int B, int heads, int d, vsa_grid_t g, int topk,
+int vsa_backward_tile_pairs(const void* bwd_ws, int B, int heads, int d, vsa_grid_t g, int topk, int radius,
                             int32_t** key_pairs);
 
 /*

@@ -62,10 +62,10 @@ def _load():
                 "orc_fine_fwd": ([P, P, P, P, P, I, I64, I64, I, D, P, P, P], None),
                 "orc_fine_fwd_rows": ([P, P, P, P, P, I, I64, I64, I, D, P, P, I64, P, P], None),
                 "orc_combine": ([P, P, P, P, I64, I64, I, P], None),
-                "orc_forward": ([P, P, P, P, P, I64, I, I, I, I, P, I, D, P, P, P, P, P, P, P], None),
+                "orc_forward": ([P, P, P, P, P, I64, I, I, I, I, P, I, I, I, D, P, P, P, P, P, P, P, P, P], None),
                 "orc_fine_bwd": ([P, P, P, P, P, P, I, I64, I64, I, D, P, P, P, P], None),
                 "orc_coarse_bwd": ([P, P, P, P, I64, I, I, D, P, P, P], None),
-                "orc_backward": ([P, P, P, P, P, I64, I, I, I, I, P, I, D, P, P, P, P, P, P, P], None),
+                "orc_backward": ([P, P, P, P, P, I64, I, I, I, I, P, I, D, P, P, P, P, P, P, P, P], None),
                 "orc_fine_bwd_query_rows": ([P, P, P, P, P, P, I, I64, I, D, P, P, I64, P], None),
                 "orc_fine_bwd_key_cube": ([P, P, P, P, P, P, I, I64, I, D, P, I64, I, P, P], None),
                 "orc_combine_bwd": ([P, P, P, P, P, I64, I64, I, P, P, P, P], None),
@@ -232,11 +232,21 @@ def combine(gc, gf, oc, of) -> np.ndarray:
     return out
 
 
+def list_width(K: int, radius: int, Nc: int) -> int:
+    """Width of the selection lists: K for a pure Top-K (radius < 0); with the
+    radius-r neighbourhood added, room for K + (2r + 1)^3 cubes (at most Nc)."""
+    return K if radius < 0 else min(Nc, K + (2 * radius + 1) ** 3)
+
+
 def forward(q, k, v, T: int, H: int, W: int, K: int, scale=None,
-            gc=None, gf=None, lut=None, want_scores: bool = True, curve: str = "raster"):
+            gc=None, gf=None, lut=None, want_scores: bool = True, curve: str = "raster",
+            radius: int = -1, cnt=None):
     """Whole forward pass (native order in/out).
 
-    Returns a dict with out, idx, of, lse, oc and scores.
+    The selection: lut [.., Nc, kmax] with counts cnt (None: every row full)
+    if given; otherwise the Top-K of the coarse scores, united with the
+    radius-r cube neighbourhood when radius >= 0 (ascending lists).
+    Returns a dict with out, idx, cnt, of, lse, oc and scores.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     gc, gf = _f64(gc), _f64(gf)
@@ -247,17 +257,20 @@ def forward(q, k, v, T: int, H: int, W: int, K: int, scale=None,
         scale = default_scale(d)
     lead = q.shape[:-2]
     out = np.empty_like(q)
-    idx = np.empty(lead + (Nc, K), dtype=np.int32)
+    kmax = np.asarray(lut).shape[-1] if lut is not None else list_width(K, radius, Nc)
+    idx = np.empty(lead + (Nc, kmax), dtype=np.int32)
+    cnt_out = np.empty(lead + (Nc,), dtype=np.int32)
     of = np.empty(lead + (64 * Nc, d), dtype=np.float64)
     lse = np.empty(lead + (64 * Nc,), dtype=np.float64)
     oc = np.empty(lead + (Nc, d), dtype=np.float64)
     scores = np.empty(lead + (Nc, Nc), dtype=np.float64) if want_scores else None
     lut = _i32(lut)
+    cnt = None if cnt is None or lut is None else _i32(cnt)
     rank = _rank_of(T, H, W, curve)
-    _load().orc_forward(_p(q), _p(k), _p(v), _p(gc), _p(gf), BH, d, T, H, W, _p(rank), K,
-                        float(scale), _p(lut), _p(out), _p(idx), _p(of), _p(lse),
+    _load().orc_forward(_p(q), _p(k), _p(v), _p(gc), _p(gf), BH, d, T, H, W, _p(rank), K, radius, kmax,
+                        float(scale), _p(lut), _p(cnt), _p(out), _p(idx), _p(cnt_out), _p(of), _p(lse),
                         _p(oc), _p(scores))
-    return dict(out=out, idx=idx, of=of, lse=lse, oc=oc, scores=scores)
+    return dict(out=out, idx=idx, cnt=cnt_out, of=of, lse=lse, oc=oc, scores=scores)
 
 
 def fine_bwd(qp, kp, vp, dof, idx, cnt, scale: float, slot_ok=None):
@@ -316,11 +329,13 @@ def coarse_bwd(qc, kc, vc, doc, scale: float):
 
 
 def backward(q, k, v, dout, idx, T: int, H: int, W: int, scale=None,
-             gc=None, gf=None, curve: str = "raster"):
-    """Whole backward pass; returns dict dq, dk, dv, dgc, dgf (native order)."""
+             gc=None, gf=None, curve: str = "raster", cnt=None):
+    """Whole backward pass for the lists idx [.., Nc, kmax] (counts cnt; None:
+    every row full); returns dict dq, dk, dv, dgc, dgf (native order)."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     gc, gf = _f64(gc), _f64(gf)
     idx = _i32(idx)
+    cnt = None if cnt is None else _i32(cnt)
     BH, N, d = _bh(q)
     K = idx.shape[-1]
     if scale is None:
@@ -330,7 +345,7 @@ def backward(q, k, v, dout, idx, T: int, H: int, W: int, scale=None,
     dgf = np.empty_like(q) if gf is not None else None
     rank = _rank_of(T, H, W, curve)
     _load().orc_backward(_p(q), _p(k), _p(v), _p(gc), _p(gf), BH, d, T, H, W, _p(rank), K,
-                         float(scale), _p(idx), _p(dout), _p(dq), _p(dk), _p(dv),
+                         float(scale), _p(idx), _p(cnt), _p(dout), _p(dq), _p(dk), _p(dv),
                          _p(dgc), _p(dgf))
     return dict(dq=dq, dk=dk, dv=dv, dgc=dgc, dgf=dgf)
 

@@ -386,18 +386,28 @@ void orc_combine(const double *gc, const double *gf, const double *oc,
             }
 }
 
+void orc_lut_add_neighbors(const int32_t *idx_in, const int32_t *cnt_in, int kin, int64_t BH, int Tc, int Hc,
+                           int Wc, const int32_t *rank, int radius, int kout, int32_t *idx_out, int32_t *cnt_out,
+                           int *overflow);
+
 /* The whole forward pass, native order in and out.
  * q, k, v, gc, gf: [BH, N, d] native (t, h, w) order; gc, gf may be NULL.
- * lut_in: if not NULL, [BH, Nc, K] index list used instead of the Top-K
- * (the valid count is then K for every query cube).
+ * The selected key cubes of each query cube: lut_in, if not NULL ([BH, Nc,
+ * kmax] lists with counts cnt_in, NULL meaning kmax for every query cube);
+ * otherwise the Top-K of each coarse score row ([AMD] "Stage 1: Coarse
+ * Selection"), united, when radius >= 0, with the cubes whose (t, h, w) cube
+ * coordinates each differ from the query cube's by at most radius ([AMD]
+ * "Comparison with Jenga": the block selection as the union of an importance
+ * and an adjacency mask); the lists are then ascending, kmax wide (kmax = K
+ * when radius < 0).
  * Outputs (all caller-allocated):
- *   out [BH, N, d] native; idx [BH, Nc, K]; of [BH, Np, d] and lse [BH, Np]
- *   (reordered order, Np = 64 Nc); oc [BH, Nc, d]; scores [BH, Nc, Nc] (may
- *   be NULL). */
+ *   out [BH, N, d] native; idx [BH, Nc, kmax]; cnt [BH, Nc]; of [BH, Np, d]
+ *   and lse [BH, Np] (reordered order, Np = 64 Nc); oc [BH, Nc, d]; scores
+ *   [BH, Nc, Nc] (may be NULL). */
 void orc_forward(const double *q, const double *k, const double *v,
                  const double *gc, const double *gf, int64_t BH, int d,
-                 int T, int H, int W, const int32_t *rank, int K, double scale,
-                 const int32_t *lut_in, double *out, int32_t *idx,
+                 int T, int H, int W, const int32_t *rank, int K, int radius, int kmax, double scale,
+                 const int32_t *lut_in, const int32_t *cnt_in, double *out, int32_t *idx, int32_t *cnt,
                  double *of, double *lse, double *oc, double *scores)
 {
     int64_t Nc = orc_num_cubes(T, H, W), N = Nc * CUBE;  /* N: reordered length */
@@ -408,7 +418,6 @@ void orc_forward(const double *q, const double *k, const double *v,
     double *qp = (double *)malloc(big), *kp = (double *)malloc(big), *vp = (double *)malloc(big);
     double *qc = (double *)malloc(small), *kc = (double *)malloc(small), *vc = (double *)malloc(small);
     double *sc = scores ? scores : (double *)malloc(sizeof(double) * BH * Nc * Nc);
-    int32_t *cnt = (int32_t *)malloc(sizeof(int32_t) * BH * Nc);
     orc_permute(q, qp, BH, d, T, H, W, rank, 0);
     orc_permute(k, kp, BH, d, T, H, W, rank, 0);
     orc_permute(v, vp, BH, d, T, H, W, rank, 0);
@@ -416,13 +425,23 @@ void orc_forward(const double *q, const double *k, const double *v,
     orc_pool(kp, kc, BH, N, d, ntok);
     orc_pool(vp, vc, BH, N, d, ntok);
     orc_coarse(qc, kc, vc, BH, (int)Nc, d, scale, sc, oc, NULL);
-    if (lut_in)
-        memcpy(idx, lut_in, sizeof(int32_t) * BH * Nc * K);
-    else
+    if (lut_in) {
+        memcpy(idx, lut_in, sizeof(int32_t) * BH * Nc * kmax);
+        for (int64_t r = 0; r < BH * Nc; r++)
+            cnt[r] = cnt_in ? cnt_in[r] : kmax;
+    } else if (radius < 0) {
         orc_topk(sc, BH * Nc, (int)Nc, K, idx);
-    for (int64_t r = 0; r < BH * Nc; r++)
-        cnt[r] = K;
-    orc_fine_fwd(qp, kp, vp, idx, cnt, K, BH, N, d, scale, slot_ok, of, lse);
+        for (int64_t r = 0; r < BH * Nc; r++)
+            cnt[r] = K;
+    } else {
+        int32_t *tk = (int32_t *)malloc(sizeof(int32_t) * BH * Nc * K);
+        int overflow = 0;
+        orc_topk(sc, BH * Nc, (int)Nc, K, tk);
+        orc_lut_add_neighbors(tk, NULL, K, BH, (T + 3) / 4, (H + 3) / 4, (W + 3) / 4, rank, radius, kmax, idx, cnt,
+                              &overflow);
+        free(tk);
+    }
+    orc_fine_fwd(qp, kp, vp, idx, cnt, kmax, BH, N, d, scale, slot_ok, of, lse);
     double *gcp = NULL, *gfp = NULL, *outp = (double *)malloc(big);
     if (gc) {
         gcp = (double *)malloc(big);
@@ -436,7 +455,7 @@ void orc_forward(const double *q, const double *k, const double *v,
     orc_permute(outp, out, BH, d, T, H, W, rank, 1);
     free(qp); free(kp); free(vp); free(qc); free(kc); free(vc);
     if (!scores) free(sc);
-    free(cnt); free(gcp); free(gfp); free(outp); free(slot_ok); free(ntok);
+    free(gcp); free(gfp); free(outp); free(slot_ok); free(ntok);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -730,13 +749,14 @@ void orc_coarse_bwd(const double *qc, const double *kc, const double *vc,
 }
 
 /* The whole backward pass, native order in and out.
- * Inputs as orc_forward, plus idx (the index list the forward used, [BH,Nc,K])
- * and dout [BH, N, d] native.  Outputs (caller-allocated, native order):
- * dq, dk, dv [BH, N, d]; dgc, dgf [BH, N, d] (ignored when the gate is NULL). */
+ * Inputs as orc_forward, plus the lists the forward used (idx [BH, Nc, kmax]
+ * with counts cnt_in, NULL meaning kmax for every query cube) and dout
+ * [BH, N, d] native.  Outputs (caller-allocated, native order): dq, dk, dv
+ * [BH, N, d]; dgc, dgf [BH, N, d] (ignored when the gate is NULL). */
 void orc_backward(const double *q, const double *k, const double *v,
                   const double *gc, const double *gf, int64_t BH, int d,
-                  int T, int H, int W, const int32_t *rank, int K, double scale, const int32_t *idx,
-                  const double *dout, double *dq, double *dk, double *dv,
+                  int T, int H, int W, const int32_t *rank, int kmax, double scale, const int32_t *idx,
+                  const int32_t *cnt_in, const double *dout, double *dq, double *dk, double *dv,
                   double *dgc, double *dgf)
 {
     int64_t Nc = orc_num_cubes(T, H, W), N = Nc * CUBE;  /* N: reordered length */
@@ -755,7 +775,7 @@ void orc_backward(const double *q, const double *k, const double *v,
     double *dqc = (double *)malloc(small), *dkc = (double *)malloc(small), *dvc = (double *)malloc(small);
     int32_t *cnt = (int32_t *)malloc(sizeof(int32_t) * BH * Nc);
     for (int64_t r = 0; r < BH * Nc; r++)
-        cnt[r] = K;
+        cnt[r] = cnt_in ? cnt_in[r] : kmax;
 
     /* Recompute the forward intermediates. */
     orc_permute(q, qp, BH, d, T, H, W, rank, 0);
@@ -765,7 +785,7 @@ void orc_backward(const double *q, const double *k, const double *v,
     orc_pool(kp, kc, BH, N, d, ntok);
     orc_pool(vp, vc, BH, N, d, ntok);
     orc_coarse(qc, kc, vc, BH, (int)Nc, d, scale, NULL, oc, NULL);
-    orc_fine_fwd(qp, kp, vp, idx, cnt, K, BH, N, d, scale, slot_ok, of, lse);
+    orc_fine_fwd(qp, kp, vp, idx, cnt, kmax, BH, N, d, scale, slot_ok, of, lse);
 
     /* Gated combination out_p = gc*Oc[cube] + gf*Of, differentiated. */
     orc_permute(dout, dop, BH, d, T, H, W, rank, 0);
@@ -779,7 +799,7 @@ void orc_backward(const double *q, const double *k, const double *v,
     if (gf && dgf)
         orc_permute(dgfp, dgf, BH, d, T, H, W, rank, 1);
 
-    orc_fine_bwd(qp, kp, vp, dof, idx, cnt, K, BH, N, d, scale, slot_ok, dqp, dkp, dvp);
+    orc_fine_bwd(qp, kp, vp, dof, idx, cnt, kmax, BH, N, d, scale, slot_ok, dqp, dkp, dvp);
     orc_coarse_bwd(qc, kc, vc, doc, BH, (int)Nc, d, scale, dqc, dkc, dvc);
 
     /* Mean-pool backward: every token of a cube gets dXc / (tokens in the

@@ -43,20 +43,26 @@ def test_status_strings(lib):
 def test_workspace_bytes(lib):
     L = lib.load()
     g = lib.Grid.of(16, 32, 64)
-    fwd = L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 154)
+    fwd = L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 154, -1)
     N, Nc = 32768, 512
     assert fwd >= 12 * N * 128 * (3 * 2 + 4)   # permuted Q/K/V + fp32 O_f at least
-    bwd = L.vsa_workspace_bytes(lib.VSA_OP_BACKWARD, 1, 12, 128, g, 154)
+    bwd = L.vsa_workspace_bytes(lib.VSA_OP_BACKWARD, 1, 12, 128, g, 154, -1)
     # fp16 dO_f plus per-row and per-cube scratch; the fine gradients go straight to the outputs
     assert 12 * N * 128 * 2 < bwd < 12 * N * 128 * 3
-    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 0) == 0        # K < 1
-    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, Nc + 1) == 0   # K > Nc
-    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 96, g, 4) == 0         # d
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 0, -1) == 0        # K < 1
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, Nc + 1, -1) == 0   # K > Nc
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 96, g, 4, -1) == 0         # d
     # a side that is not a multiple of 4: partial cubes, sized like the covering grid
-    assert (L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, lib.Grid.of(6, 7, 5), 2)
-            == L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, lib.Grid.of(8, 8, 8), 2) > 0)
-    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, lib.Grid.of(0, 8, 8), 1) == 0
-    assert L.vsa_workspace_bytes(7, 1, 12, 128, g, 4) == 0
+    assert (L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, lib.Grid.of(6, 7, 5), 2, -1)
+            == L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, lib.Grid.of(8, 8, 8), 2, -1) > 0)
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, lib.Grid.of(0, 8, 8), 1, -1) == 0
+    assert L.vsa_workspace_bytes(7, 1, 12, 128, g, 4, -1) == 0
+    # adjacency-forced selection: lists of topk + (2r + 1)^3 entries (at most Nc), radius in -1..7
+    with_r1 = L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 154, 1)
+    assert with_r1 > fwd and (with_r1 - fwd) >= 12 * Nc * (154 + 27) * 4 - 12 * Nc * 154 * 4
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 154, 8) == 0
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 154, -2) == 0
+    assert L.vsa_workspace_bytes(lib.VSA_OP_BACKWARD, 1, 12, 128, g, 154, 1) == bwd
 
 
 def test_host_side_argument_errors(lib):
@@ -85,20 +91,25 @@ def test_host_side_argument_errors(lib):
     assert L.vsa_fine_fwd(fake, fake, fake, fake2, None, 2, 1, 128, 64, 0.125, fake2, 7, None,
                           None) == lib.VSA_ERR_ARG
     # forward: workspace too small
-    assert L.vsa_forward(fake, fake, fake, None, None, 1, 2, 64, g, 2, 0.125, fake2, 0, fake2, 16,
+    assert L.vsa_forward(fake, fake, fake, None, None, 1, 2, 64, g, 2, -1, 0.125, fake2, 0, fake2, 16,
                          None) == lib.VSA_ERR_WORKSPACE
-    assert L.vsa_forward(fake, fake, fake, None, None, 1, 2, 64, g, 9, 0.125, fake2, 0, fake2, 1 << 30,
+    assert L.vsa_forward(fake, fake, fake, None, None, 1, 2, 64, g, 9, -1, 0.125, fake2, 0, fake2, 1 << 30,
                          None) == lib.VSA_ERR_ARG
-    assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, 0.125, fake2, fake2, fake2, None, None, 3,
+    assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, -1, 0.125, fake2, fake2, fake2, None, None, 3,
                           fake2, 1 << 30, None) == lib.VSA_ERR_ARG
     # backward: workspace too small, null or misaligned outputs, Top-K out of range
     bf16 = lib.VSA_DTYPE_BF16
-    assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, 0.125, fake2, fake2, fake2, None, None, bf16,
+    assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, -1, 0.125, fake2, fake2, fake2, None, None, bf16,
                           fake2, 16, None) == lib.VSA_ERR_WORKSPACE
-    assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, 0.125, None, fake2, fake2, None, None, bf16,
+    assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, -1, 0.125, None, fake2, fake2, None, None, bf16,
                           fake2, 1 << 30, None) == lib.VSA_ERR_ARG
-    assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, 0.125, fake2, ctypes.c_void_p(0x2008), fake2,
+    assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, -1, 0.125, fake2, ctypes.c_void_p(0x2008), fake2,
                           None, None, bf16, fake2, 1 << 30, None) == lib.VSA_ERR_ARG
     for K in (0, 5):
-        assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, K, 0.125, fake2, fake2, fake2, None, None, bf16,
+        assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, K, -1, 0.125, fake2, fake2, fake2, None, None, bf16,
+                              fake2, 1 << 30, None) == lib.VSA_ERR_ARG
+    for r in (-2, 8):   # radius out of range
+        assert L.vsa_forward(fake, fake, fake, None, None, 1, 2, 64, g, 2, r, 0.125, fake2, 0, fake2, 1 << 30,
+                             None) == lib.VSA_ERR_ARG
+        assert L.vsa_backward(fake, None, None, fake, 1, 2, 64, g, 2, r, 0.125, fake2, fake2, fake2, None, None, bf16,
                               fake2, 1 << 30, None) == lib.VSA_ERR_ARG

@@ -163,7 +163,7 @@ def test_lut_errors_are_reported(vsa, oracle_mod):
 
 
 # ---------------------------------------------------------------- whole forward / backward
-def _e2e(vsa, oracle_mod, wl, gates, out_dtype, grad_dtype, heads=None, cube_order=None):
+def _e2e(vsa, oracle_mod, wl, gates, out_dtype, grad_dtype, heads=None, cube_order=None, radius=-1):
     q, k, v = synth.make_qkv(wl, heads_subset=heads)
     gc = gf = None
     if gates:
@@ -171,14 +171,40 @@ def _e2e(vsa, oracle_mod, wl, gates, out_dtype, grad_dtype, heads=None, cube_ord
     dout = synth.make_dout(wl, heads_subset=heads)
     D = lambda a: None if a is None else dev(a)
     out, st = vsa.forward(D(q), D(k), D(v), wl.T, wl.H, wl.W, wl.topk, g_coarse=D(gc), g_fine=D(gf),
-                          out_dtype=out_dtype, cube_order=cube_order)
-    bws = torch.empty(vsa.workspace_bytes(1, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk), dtype=torch.uint8,
-                      device="cuda")
+                          out_dtype=out_dtype, cube_order=cube_order, radius=radius)
+    bws = torch.empty(vsa.workspace_bytes(1, wl.B, wl.heads, wl.d, wl.T, wl.H, wl.W, wl.topk, radius),
+                      dtype=torch.uint8, device="cuda")
     g = vsa.backward(st, D(dout), g_coarse=D(gc), g_fine=D(gf), grad_dtype=grad_dtype, ws=bws)
     status_ok(vsa)
     saved = st.saved()
     saved["key_pairs"] = vsa.backward_tile_pairs(st, bws)
     return q, k, v, gc, gf, dout, out, g, saved
+
+
+def _gpu_lists(vsa, oracle_mod, wl, saved, scores_by_head, radius, curve="raster"):
+    """The selection lists the GPU forward saved, checked: with radius < 0 they
+    are a valid Top-K of the oracle's scores; with a radius, the GPU's own
+    Top-K (the coarse kernel rerun on the saved pooled vectors) is a valid
+    Top-K and the saved lists are exactly its union with the radius
+    neighbourhood (the oracle's list transform, bit for bit).
+    scores_by_head: {head: oracle scores [Nc, Nc]}.  Returns (idx, cnt) as
+    [heads, Nc, kmax] and [heads, Nc]."""
+    kmax = oracle_mod.list_width(wl.topk, radius, wl.Nc)
+    idx = saved["idx"].view(wl.heads, wl.Nc, kmax).cpu().numpy()
+    cnt = saved["cnt"].view(wl.heads, wl.Nc).cpu().numpy()
+    if radius < 0:
+        tk = idx
+        assert np.all(cnt == wl.topk)
+    else:
+        r = vsa.coarse_topk(saved["qc"], saved["kc"], saved["vc"], wl.topk, want_oc=False)
+        tk = r["idx"].view(wl.heads, wl.Nc, wl.topk).cpu().numpy()
+        ridx, rcnt, ovf = oracle_mod.lut_add_neighbors(tk, None, wl.T, wl.H, wl.W, radius, kmax, curve=curve)
+        assert not ovf
+        np.testing.assert_array_equal(idx, ridx)
+        np.testing.assert_array_equal(cnt, rcnt)
+    for h, sc in scores_by_head.items():
+        check_topk_validity(tk[h:h + 1], sc, wl.topk)
+    return idx, cnt
 
 
 def _key_cubes(idx1, kpairs0, keys_per_row, budget_flop=2.5e11):
@@ -189,7 +215,7 @@ def _key_cubes(idx1, kpairs0, keys_per_row, budget_flop=2.5e11):
     the oracle's cost for it (every listing query row recomputes its softmax
     over keys_per_row keys) exceeds budget_flop, except the first cube."""
     Nc = idx1.shape[-2]
-    inv = np.bincount(idx1.reshape(-1), minlength=Nc)
+    inv = np.bincount(idx1.reshape(-1)[idx1.reshape(-1) >= 0], minlength=Nc)
     listed = np.flatnonzero(inv > 0)
     order = listed[np.argsort(inv[listed], kind="stable")]
     top = int(order[-1])
@@ -224,6 +250,29 @@ def test_forward_backward(vsa, oracle_mod, name, gates, dtype):
     for n in ("dq", "dk", "dv", "dgc", "dgf"):
         if rg[n] is not None:
             assert_close(host(g[n]), rg[n], bf16_out=bf, what=n)
+
+
+@pytest.mark.parametrize("name,radius,curve", [("tiny", 0, "raster"), ("small", 1, "raster"),
+                                               ("odd_small", 1, "hilbert"), ("small", 2, "hilbert")])
+def test_adjacency_forward_backward(vsa, oracle_mod, name, radius, curve):
+    """Top-K united with the radius-r cube neighbourhood ([AMD] "Comparison
+    with Jenga": importance and adjacency masks), through vsa_forward and
+    vsa_backward: lists checked by _gpu_lists, then the output and every
+    gradient against the oracle run on the GPU's lists."""
+    wl = synth.WORKLOADS[name]
+    order = None if curve == "raster" else vsa.cube_order(wl.T, wl.H, wl.W, curve)
+    q, k, v, gc, gf, dout, out, g, saved = _e2e(vsa, oracle_mod, wl, True, torch.float32, torch.float32,
+                                                cube_order=order, radius=radius)
+    ref0 = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=gc, gf=gf, curve=curve)
+    scores = ref0["scores"].reshape(wl.heads, wl.Nc, wl.Nc)
+    idx, cnt = _gpu_lists(vsa, oracle_mod, wl, saved, {h: scores[h] for h in range(wl.heads)}, radius, curve)
+    assert cnt.max() > wl.topk
+    lut, lcnt = idx.reshape((wl.B, wl.heads) + idx.shape[1:]), cnt.reshape(wl.B, wl.heads, wl.Nc)
+    ref = oracle_mod.forward(q, k, v, wl.T, wl.H, wl.W, wl.topk, gc=gc, gf=gf, lut=lut, cnt=lcnt, curve=curve)
+    assert_close(host(out), ref["out"], what="out")
+    rg = oracle_mod.backward(q, k, v, dout, lut, wl.T, wl.H, wl.W, gc=gc, gf=gf, curve=curve, cnt=lcnt)
+    for n in ("dq", "dk", "dv", "dgc", "dgf"):
+        assert_close(host(g[n]), rg[n], what=n)
 
 
 def test_fine_bwd_entry_point(vsa, oracle_mod):
@@ -297,7 +346,7 @@ def test_full_size_head_sample(vsa, oracle_mod):
 
 
 # ---------------------------------------------------------------- full sizes, sampled
-def _sampled_checks(vsa, oracle_mod, wl, dtype, n_cubes=4, n_rows=48):
+def _sampled_checks(vsa, oracle_mod, wl, dtype, n_cubes=4, n_rows=48, radius=-1):
     """Full-size run of `wl` (all heads, bench launch configuration); the
     oracle recomputes, for the first and last head: the coarse scores (Top-K
     validity of the GPU lists), whole query cubes of the output, the fine LSE
@@ -305,9 +354,9 @@ def _sampled_checks(vsa, oracle_mod, wl, dtype, n_cubes=4, n_rows=48):
     0, dK / dV of the key cubes _key_cubes picks (most-listed, median,
     least-listed, unlisted, both cubes of a planned dK/dV tile) within the
     oracle's time budget.  All heads: sum_j dK_j = 0 per channel."""
-    q, k, v, gc, gf, dout, out, g, saved = _e2e(vsa, oracle_mod, wl, True, dtype, dtype)
+    q, k, v, gc, gf, dout, out, g, saved = _e2e(vsa, oracle_mod, wl, True, dtype, dtype, radius=radius)
     bf = dtype == torch.bfloat16
-    gidx = saved["idx"].view(wl.B, wl.heads, wl.Nc, wl.topk).cpu().numpy()
+    kmax = oracle_mod.list_width(wl.topk, radius, wl.Nc)
     scale = wl.d ** -0.5
     pos = oracle_mod.sfc_table(wl.T, wl.H, wl.W)
     slot_ok, ntok = oracle_mod.cube_slots(wl.T, wl.H, wl.W)   # padding slots of partial cubes
@@ -315,15 +364,21 @@ def _sampled_checks(vsa, oracle_mod, wl, dtype, n_cubes=4, n_rows=48):
     native_of[pos] = np.arange(wl.N)                     # reordered position -> native token
     real = np.flatnonzero(slot_ok)
     rng = np.random.default_rng(zlib.crc32(wl.name.encode()))
-    cnt1 = np.full((1, wl.Nc), wl.topk, np.int32)
     at = lambda t, h, nat: host(t[0, h, torch.from_numpy(nat).to(t.device)])
-    for h in sorted({0, wl.heads - 1}):
+    heads = sorted({0, wl.heads - 1})
+    pooled, scores_h = {}, {}
+    for h in heads:
+        P = lambda a: oracle_mod.permute(a[0, h].reshape(1, wl.N, wl.d), wl.T, wl.H, wl.W)
+        pooled[h] = [oracle_mod.pool(P(a), ntok) for a in (q, k, v)]
+        scores_h[h] = oracle_mod.coarse(*pooled[h], scale)[0]
+    gidx, gcnt = _gpu_lists(vsa, oracle_mod, wl, saved, scores_h, radius)
+    for h in heads:
         P = lambda a: oracle_mod.permute(a[0, h].reshape(1, wl.N, wl.d), wl.T, wl.H, wl.W)
         qp, kp, vp, gcp, gfp, dop = (P(a) for a in (q, k, v, gc, gf, dout))
-        pq, pk, pv = (oracle_mod.pool(a, ntok) for a in (qp, kp, vp))
+        pq, pk, pv = pooled[h]
         scores, oc, _ = oracle_mod.coarse(pq, pk, pv, scale)
-        idx1 = gidx[0, h].reshape(1, wl.Nc, wl.topk)
-        check_topk_validity(idx1, scores, wl.topk)
+        idx1 = gidx[h].reshape(1, wl.Nc, kmax)
+        cnt1 = gcnt[h].reshape(1, wl.Nc)
         # whole query cubes of the output (the first, the last, two random)
         cubes = np.unique(np.r_[0, wl.Nc - 1, rng.choice(wl.Nc, n_cubes - 2, replace=False)])
         rows = (64 * cubes[:, None] + np.arange(64)).reshape(-1)
@@ -343,10 +398,10 @@ def _sampled_checks(vsa, oracle_mod, wl, dtype, n_cubes=4, n_rows=48):
                   + dqc[0, qrows // 64] / ntok[qrows // 64, None])
         assert_close(at(g["dq"], h, native_of[qrows]), dq_ref, bf16_out=bf, what=f"dq rows head {h}")
         _, rl = oracle_mod.fine_fwd_rows(qp, kp, vp, idx1, cnt1, scale, qrows, slot_ok=slot_ok)
-        assert_close(host(saved["lse"][h])[qrows], rl, max_abs=lse_max_abs(64 * wl.topk), mean_abs=LSE_MEAN_ABS,
+        assert_close(host(saved["lse"][h])[qrows], rl, max_abs=lse_max_abs(64 * kmax), mean_abs=LSE_MEAN_ABS,
                      what=f"lse rows head {h}")
         if h == 0:
-            kcubes, _ = _key_cubes(idx1, saved["key_pairs"][0].cpu().numpy(), 64 * wl.topk)
+            kcubes, _ = _key_cubes(idx1, saved["key_pairs"][0].cpu().numpy(), 64 * kmax)
             for c in kcubes:
                 dk_c, dv_c = oracle_mod.fine_bwd_key_cube(qp, kp, vp, dof, idx1, cnt1, scale, 0, c, slot_ok=slot_ok)
                 ok = slot_ok[64 * c:64 * c + 64] == 1
@@ -365,6 +420,12 @@ def test_full_size_sampled(vsa, oracle_mod, name, dtype):
     """The 32K-token sparsity sweep (K = 512, 256, 64 of 512 cubes), the
     40-head Wan-14B-shaped layer and the 122880-token long video, at full size."""
     _sampled_checks(vsa, oracle_mod, synth.WORKLOADS[name], dtype)
+
+
+def test_full_size_adjacency(vsa, oracle_mod):
+    """The Wan-1.3B-shaped layer with each Top-K list united with its radius-1
+    cube neighbourhood (up to 154 + 27 cubes per row), fwd + bwd at full size."""
+    _sampled_checks(vsa, oracle_mod, synth.WORKLOADS["wan1.3b"], torch.float32, radius=1)
 
 
 @pytest.mark.parametrize("name", ["small", "wan1.3b"])

@@ -587,6 +587,56 @@ def test_padded_grid_matches_dense(oracle_mod, curve, gates):
             np.testing.assert_allclose(g[key], leaves[n].grad.numpy(), rtol=1e-9, atol=1e-9, err_msg=key)
 
 
+# ---------------------------------------------------------------- adjacency-forced selection
+# [AMD] "Comparison with Jenga": the block selection as the union of an
+# importance mask (the Top-K) and an adjacency mask.  The expected lists are
+# rebuilt here from torch.topk on the dense coarse scores and from the cube
+# coordinates alone, and the whole forward and backward are checked against
+# the dense masked formulation with those lists.
+@pytest.mark.parametrize("curve,radius", [("raster", 1), ("hilbert", 1), ("raster", 0), ("hilbert", 2)])
+def test_adjacency_selection_matches_dense(oracle_mod, curve, radius):
+    wl = synth.WORKLOADS["odd"]                          # 5 x 6 x 10: partial cubes on every side
+    q, k, v, gc, gf, dout = _tiny_inputs(wl, True)
+    T, H, W = wl.T, wl.H, wl.W
+    Tc, Hc, Wc = oracle_mod.cube_grid(T, H, W)
+    Nc = Tc * Hc * Wc
+    scale = wl.d ** -0.5
+    rank = None if curve == "raster" else oracle_mod.cube_rank(Tc, Hc, Wc, curve)
+    r = oracle_mod.forward(q, k, v, T, H, W, wl.topk, scale, gc=gc, gf=gf, curve=curve, radius=radius)
+    kmax = oracle_mod.list_width(wl.topk, radius, Nc)
+    assert r["idx"].shape == (wl.BH, Nc, kmax)
+    # the expected selection, from the dense scores and the coordinates
+    *_, sc, _ = dense_vsa(_t(q), _t(k), _t(v), T, H, W, np.zeros((wl.BH, Nc, 1), np.int64), scale, rank=rank)
+    top = torch.topk(sc, wl.topk, dim=-1).indices.numpy()
+    pos = np.arange(Nc) if rank is None else np.asarray(rank)          # raster id -> position
+    coord = np.stack(np.unravel_index(np.arange(Nc), (Tc, Hc, Wc)), 1)  # raster id -> (t, h, w)
+    exp_idx = np.full((wl.BH, Nc, kmax), -1, np.int32)
+    exp_cnt = np.zeros((wl.BH, Nc), np.int32)
+    for bh in range(wl.BH):
+        for qpos in range(Nc):
+            qr = int(np.flatnonzero(pos == qpos)[0])
+            near = pos[np.flatnonzero(np.abs(coord - coord[qr]).max(1) <= radius)]
+            sel = sorted(set(top[bh, qpos].tolist()) | set(near.tolist()))
+            exp_cnt[bh, qpos] = len(sel)
+            exp_idx[bh, qpos, :len(sel)] = sel
+    np.testing.assert_array_equal(r["cnt"], exp_cnt)
+    np.testing.assert_array_equal(r["idx"], exp_idx)
+    assert exp_cnt.max() > wl.topk                       # the neighbourhood adds cubes
+    out, of, _, _, lse = dense_vsa(_t(q), _t(k), _t(v), T, H, W, exp_idx, scale, gc=_t(gc), gf=_t(gf),
+                                   cnt=exp_cnt, rank=rank)
+    np.testing.assert_allclose(r["out"], out.numpy(), rtol=1e-10, atol=1e-10)
+    p_ = oracle_mod.sfc_table(T, H, W, curve)
+    np.testing.assert_allclose(r["lse"][:, p_], lse.numpy(), rtol=1e-12)
+    g = oracle_mod.backward(q, k, v, dout, r["idx"], T, H, W, scale, gc=gc, gf=gf, curve=curve, cnt=r["cnt"])
+    leaves = {n: torch.tensor(a, dtype=torch.float64, requires_grad=True)
+              for n, a in (("q", q), ("k", k), ("v", v), ("gc", gc), ("gf", gf))}
+    o2, *_ = dense_vsa(leaves["q"], leaves["k"], leaves["v"], T, H, W, exp_idx, scale, gc=leaves["gc"],
+                       gf=leaves["gf"], cnt=exp_cnt, rank=rank)
+    (o2 * torch.tensor(dout, dtype=torch.float64)).sum().backward()
+    for n, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("gc", "dgc"), ("gf", "dgf")):
+        np.testing.assert_allclose(g[key], leaves[n].grad.numpy(), rtol=1e-9, atol=1e-9, err_msg=key)
+
+
 def test_padded_reordering_slots(oracle_mod):
     """Partial cubes: every token lands in its own cube's slot block, the
     padding slots are zero, the token counts are the partial box volumes, and

@@ -92,7 +92,7 @@ def test_noalloc_head_dim_64(lib, oracle_mod):
 def _limit_heads(lib, N, d, K):
     """The largest BH whose scratch fits the fixed array at (N, d, K)."""
     L = lib.load()
-    need = lambda bh: L.vsa_workspace_bytes(lib.VSA_OP_FINE_BWD, 1, bh, d, lib.Grid.of(4, 4, N // 16), K)
+    need = lambda bh: L.vsa_workspace_bytes(lib.VSA_OP_FINE_BWD, 1, bh, d, lib.Grid.of(4, 4, N // 16), K, -1)
     bh = 1
     while need(bh + 1) <= lib.VSA_NOALLOC_SCRATCH_BYTES:
         bh += 1
