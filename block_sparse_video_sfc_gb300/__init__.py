@@ -90,11 +90,11 @@ def coarse_topk(qc, kc, vc, topk: int, scale: Optional[float] = None, want_oc: b
     cnt = torch.empty(lead + (Nc,), dtype=torch.int32, device=dev)
     oc = torch.empty_like(qc) if want_oc else None
     lse_c = torch.empty(lead + (Nc,), dtype=torch.float32, device=dev)
-    scores = torch.empty(lead + (Nc, Nc), dtype=torch.float32, device=dev)
+    scores = torch.empty(lead + (Nc, Nc), dtype=torch.float32, device=dev) if want_scores else None
     _lib.check("vsa_coarse_topk", _lib.load().vsa_coarse_topk(
         _ptr(qc), _ptr(kc), _ptr(vc if want_oc else None), BH, Nc, d, topk, float(scale), _ptr(oc),
         _ptr(lse_c), _ptr(idx), _ptr(cnt), _ptr(scores), _stream()))
-    return dict(idx=idx, cnt=cnt, oc=oc, lse_c=lse_c, scores=scores if want_scores else None)
+    return dict(idx=idx, cnt=cnt, oc=oc, lse_c=lse_c, scores=scores)
 
 
 def mask_to_lut(mask, max_kv_blocks: int):

@@ -6,236 +6,222 @@
 // (scores of pooled Q against pooled K; torch.topk over the last dimension,
 // highest first), and the coarse output of "Stage 2: Fine Computation".
 //
-// Every product here is a small fp32 matrix product per (batch, head): the
-// score matrix S = scale Qc Kc^T (Nc x Nc), O_c = softmax(S) Vc, and in the
-// backward dP = dOc Vc^T, dQc = scale dS Kc, dKc = scale dS^T Qc, dVc = P^T dOc.
-// They all run through one register-tiled SIMT kernel (coarse_gemm); the
-// row-wise steps (Top-K and log-sum-exp of each score row; P and dS of each
-// row in the backward) are one warp per row.  The score rows live in a
-// caller-provided [BH, Nc, Nc] buffer (12.6 MB for 12 heads of 512 cubes,
-// L2-resident between the launches).  All arithmetic is fp32.
+// Every product here is a small fp32 product per (batch, head): the score
+// rows S = scale Qc Kc^T, O_c = softmax(S) Vc, and in the backward
+// dP = dOc Vc^T, dS = P (dP - D) with D = rowsum(P dP) = dOc . O_c (the
+// latter computed by the combine backward), dQc = scale dS Kc,
+// dKc = scale dS^T Qc, dVc = P^T dOc.  No Nc x Nc matrix is ever stored:
+//   coarse_fwd_kernel  a CTA keeps the score rows of 16 query cubes in shared
+//                      memory (Kc streamed through in tiles of 128 cubes),
+//                      takes each row's log-sum-exp and Top-K there (one warp
+//                      per row, radix selection), turns the rows into P and
+//                      streams Vc through for O_c;
+//   coarse_bwd_kernel  one launch, two kinds of CTA over 16 cubes each: a
+//                      key CTA streams every query cube through in tiles of
+//                      64 (S^T, dP^T, then dKc and dVc accumulated in
+//                      registers), a query CTA every key cube (S, dP, then
+//                      dQc).  Both recompute the scores instead of reading
+//                      them.
+// The products are register-tiled SIMT fp32: a lane owns a 4 x 4 or 4 x 2
+// block of the output; the operand layouts in shared memory (row strides of
+// 4 or 8 mod 32 floats) make every operand load one wavefront per warp.
+// Tiles arrive by cp.async (16 bytes, zero fill past the last cube).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace vsa {
 namespace {
 
-// ---------------------------------------------------------------- GEMM
-// C[bh] (M x N) = alpha * op(A[bh]) * op(B[bh]), row-major operands:
-//   kNT: A [M x K], B [N x K]     (C = A B^T)
-//   kNN: A [M x K], B [K x N]     (C = A B)
-//   kTN: A [K x M], B [K x N]     (C = A^T B)
-// With row_lse set (kNN only), every A element is replaced by
-// exp(A - row_lse[row]) on load: the softmax of a score row, applied on the fly.
-enum { kNT = 0, kNN = 1, kTN = 2 };
+constexpr int kThreads = 256, kWarps = kThreads / 32;
+constexpr int kRows = 16;      // cubes per CTA
+constexpr int kFwdTile = 128;  // key cubes per streamed tile, forward
+constexpr int kBwdTile = 64;   // cubes per streamed tile, backward
+constexpr int kHist = 256;     // radix histogram bins per warp
 
-struct GemmJob {
-  const float* A;
-  const float* B;
-  float* C;
-  const float* row_lse;
-  float alpha;
-  int op, M, N, K;
-  int64_t bsA, bsB, bsC, bsL;  // per-(batch, head) strides in elements
-};
-constexpr int kMaxJobs = 3;
-struct GemmBatch {
-  GemmJob job[kMaxJobs];
-};
+// Row stride of the score / probability rows: 8 (mod 32) floats, so that the
+// stores of a 4 x 8 lane grid and the float4 loads of 4 rows hit distinct
+// banks; the key dimension is padded to whole tiles (zeros past Nc).
+__host__ __device__ __forceinline__ int score_ld(int Nc) { return (Nc + kFwdTile - 1) / kFwdTile * kFwdTile + 8; }
+constexpr int kProbLd = kBwdTile + 8;
 
-// CTA tile 64 x 64, k-step 16, 256 threads.  Warp w covers rows 16*(w/2)..+15
-// and columns 32*(w%2)..+31; lane l computes the 4 x 4 block at rows
-// 4*(l/8), columns 4*(l%8) of that.  Per k both operands come from shared
-// memory as one float4 each (one wavefront per warp for A and one for B), so
-// the 16 FMAs per k keep the FMA pipe, not shared memory, the limit.
-constexpr int kBM = 64, kBN = 64, kBK = 16, kGThreads = 256, kSPad = 4;
-
-struct TileRegs {
-  float a[4], b[4];
-};
-
-// Four consecutive floats from p (all in range: ok), else those of the first
-// n (n <= 4, possibly 0) and zeros.
-__device__ __forceinline__ void load4(const float* p, int n, float* v) {
-  if (n >= 4 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
-    const float4 x = __ldg(reinterpret_cast<const float4*>(p));
-    v[0] = x.x;
-    v[1] = x.y;
-    v[2] = x.z;
-    v[3] = x.w;
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = i < n ? __ldg(p + i) : 0.f;
-  }
-}
-
-// Loads this thread's 4 elements of the A tile (rows m0.., k0..) and of the B
-// tile into registers; out-of-range elements read 0.
-__device__ __forceinline__ void gemm_load(const GemmJob& j, const float* A, const float* B, const float* lse,
-                                          int m0, int n0, int k0, TileRegs& r) {
-  const int t = threadIdx.x;
-  if (j.op == kTN) {  // A is [K x M]: thread -> (k, 4 consecutive m)
-    const int k = k0 + (t >> 4), m = m0 + (t & 15) * 4;
-    load4(A + static_cast<int64_t>(k) * j.M + m, k < j.K ? min(4, j.M - m) : 0, r.a);
-  } else {  // A is [M x K]: thread -> (m, 4 consecutive k)
-    const int m = m0 + (t >> 2), k = k0 + (t & 3) * 4;
-    const int n = m < j.M ? min(4, j.K - k) : 0;
-    load4(A + static_cast<int64_t>(m) * j.K + k, n, r.a);
-    if (lse) {
-      const float l = m < j.M ? lse[m] : 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) r.a[i] = i < n ? __expf(r.a[i] - l) : 0.f;
-    }
-  }
-  if (j.op == kNT) {  // B is [N x K]: thread -> (n, 4 consecutive k)
-    const int n = n0 + (t >> 2), k = k0 + (t & 3) * 4;
-    load4(B + static_cast<int64_t>(n) * j.K + k, n < j.N ? min(4, j.K - k) : 0, r.b);
-  } else {  // B is [K x N]: thread -> (k, 4 consecutive n)
-    const int k = k0 + (t >> 4), n = n0 + (t & 15) * 4;
-    load4(B + static_cast<int64_t>(k) * j.N + n, k < j.K ? min(4, j.N - n) : 0, r.b);
-  }
-}
-
-__device__ __forceinline__ void gemm_store(int op, const TileRegs& r, float (*sA)[kBM + kSPad],
-                                           float (*sB)[kBN + kSPad]) {
-  const int t = threadIdx.x;
-  if (op == kTN) {
-    *reinterpret_cast<float4*>(&sA[t >> 4][(t & 15) * 4]) = make_float4(r.a[0], r.a[1], r.a[2], r.a[3]);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sA[(t & 3) * 4 + i][t >> 2] = r.a[i];
-  }
-  if (op == kNT) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sB[(t & 3) * 4 + i][t >> 2] = r.b[i];
-  } else {
-    *reinterpret_cast<float4*>(&sB[t >> 4][(t & 15) * 4]) = make_float4(r.b[0], r.b[1], r.b[2], r.b[3]);
-  }
-}
-
-// grid: (ceil(N/64), ceil(M/64), BH * njobs); blockIdx.z = job * BH + bh.
-__global__ void __launch_bounds__(kGThreads) coarse_gemm(GemmBatch batch, int BH) {
-  __shared__ __align__(16) float sA[2][kBK][kBM + kSPad];
-  __shared__ __align__(16) float sB[2][kBK][kBN + kSPad];
-  const GemmJob& j = batch.job[blockIdx.z / BH];
-  const int64_t bh = blockIdx.z % BH;
-  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
-  if (m0 >= j.M || n0 >= j.N) return;
-  const float* A = j.A + bh * j.bsA;
-  const float* B = j.B + bh * j.bsB;
-  const float* lse = j.row_lse ? j.row_lse + bh * j.bsL : nullptr;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rm = (warp >> 1) * 16 + (lane >> 3) * 4, cn = (warp & 1) * 32 + (lane & 7) * 4;
-  float acc[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
-
-  const int nk = (j.K + kBK - 1) / kBK;
-  TileRegs r;
-  gemm_load(j, A, B, lse, m0, n0, 0, r);
-  gemm_store(j.op, r, sA[0], sB[0]);
-  __syncthreads();
-  for (int kt = 0; kt < nk; ++kt) {
-    const int cur = kt & 1;
-    if (kt + 1 < nk) gemm_load(j, A, B, lse, m0, n0, (kt + 1) * kBK, r);
-#pragma unroll
-    for (int k = 0; k < kBK; ++k) {
-      const float4 a = *reinterpret_cast<const float4*>(&sA[cur][k][rm]);
-      const float4 b = *reinterpret_cast<const float4*>(&sB[cur][k][cn]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[i][c] = fmaf(av[i], bv[c], acc[i][c]);
-    }
-    // The other buffer was last read in iteration kt-1, before its barrier.
-    if (kt + 1 < nk) gemm_store(j.op, r, sA[cur ^ 1], sB[cur ^ 1]);
-    __syncthreads();
-  }
-  float* C = j.C + bh * j.bsC;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + rm + i;
-    if (m >= j.M) continue;
-    const int n = n0 + cn;
-    float* crow = C + static_cast<int64_t>(m) * j.N;
-    if (n + 3 < j.N && (reinterpret_cast<uintptr_t>(crow + n) & 15) == 0) {
-      *reinterpret_cast<float4*>(crow + n) =
-          make_float4(j.alpha * acc[i][0], j.alpha * acc[i][1], j.alpha * acc[i][2], j.alpha * acc[i][3]);
-    } else {
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (n + c < j.N) crow[n + c] = j.alpha * acc[i][c];
-    }
-  }
-}
-
-int launch_gemm(const GemmBatch& b, int njobs, int BH, int M, int N, cudaStream_t s) {
-  if (njobs < 1 || njobs > kMaxJobs || static_cast<int64_t>(BH) * njobs > 65535) return VSA_ERR_UNSUPPORTED;
-  dim3 grid((N + kBN - 1) / kBN, (M + kBM - 1) / kBM, BH * njobs);
-  coarse_gemm<<<grid, kGThreads, 0, s>>>(b, BH);
-  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
-}
-
-// ---------------------------------------------------------------- Top-K rows
-constexpr int kRowWarps = 8;
-
-// Float -> unsigned key with the same order (+0 and -0 equal).
+// Float -> unsigned key with the same order (+0 and -0 equal), and back.
 __device__ __forceinline__ uint32_t orderable(float f) {
   uint32_t b = __float_as_uint(f);
   if (f == 0.0f) b = 0;
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
+__device__ __forceinline__ float from_orderable(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
 
-// One warp per score row.  Selection: the K-th largest key is found bit by bit
-// (the largest t with #{key >= t} >= K), then every key above it and, in
-// ascending id, as many keys equal to it as K still needs are kept.  Order:
-// each pick's rank is the number of picks that beat it (higher score, or the
-// same score and a lower id), so the row comes out highest first.
-// A NaN score has no place in the order: it latches kErrNan (the row is still
-// completed, NaN ranking above every number).
-__global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const float* __restrict__ S, int64_t rows, int Nc,
-                                                                   int K, int32_t* __restrict__ idx,
-                                                                   int32_t* __restrict__ cnt,
-                                                                   float* __restrict__ lse, int* err) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + warp;
-  if (row >= rows) return;
-  const size_t per_warp = (static_cast<size_t>(Nc) * 4 + static_cast<size_t>(K) * 8 + 15) & ~size_t(15);
-  uint64_t* picks = reinterpret_cast<uint64_t*>(smem + per_warp * warp);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(picks + K);
-  const float* s = S + row * Nc;
-
-  float m = -INFINITY;
-  bool nan = false;
-  for (int j = lane; j < Nc; j += 32) {
-    const float v = s[j];
-    keys[j] = orderable(v);
-    m = fmaxf(m, v);
-    nan |= v != v;
-  }
-  if (__any_sync(0xffffffffu, nan) && lane == 0) flag_error(err, kErrNan);
+__device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  float l = 0.f;
-  for (int j = lane; j < Nc; j += 32) l += __expf(s[j] - m);
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-  if (lse && lane == 0) lse[row] = m + __logf(l);
-  __syncwarp();
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
 
-  uint32_t thr = 0;
-  for (int b = 31; b >= 0; --b) {
-    const uint32_t cand = thr | (1u << b);
-    unsigned c = 0;
-    for (int j = lane; j < Nc; j += 32) c += keys[j] >= cand;
-    if (__reduce_add_sync(0xffffffffu, c) >= static_cast<unsigned>(K)) thr = cand;
+// ---------------------------------------------------------------- tiles
+__device__ __forceinline__ void cp_async16(float* dst, const float* src, int src_bytes) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// Rows row0 .. row0 + n - 1 of a [rows, D] fp32 matrix into dst [n][D + 4],
+// asynchronously; rows at or past `rows` read zero.
+template <int D>
+__device__ __forceinline__ void load_rows_async(float* dst, const float* src, int row0, int n, int rows) {
+  constexpr int kVec = D / 4;
+  for (int i = threadIdx.x; i < n * kVec; i += kThreads) {
+    const int r = i / kVec, c = (i % kVec) * 4;
+    const bool in = row0 + r < rows;
+    cp_async16(dst + r * (D + 4) + c, src + static_cast<int64_t>(in ? row0 + r : 0) * D + c, in ? 16 : 0);
   }
-  unsigned above = 0;
-  for (int j = lane; j < Nc; j += 32) above += keys[j] > thr;
-  const int need_eq = K - static_cast<int>(__reduce_add_sync(0xffffffffu, above));
+}
+
+__device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+template <int kk>
+__device__ __forceinline__ float comp(const float4& v) {
+  return kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w;
+}
+
+// acc[i][j] += sum_{k < kdim} A[4 i lda + k] B[8 j ldb + k]  (kdim % 4 == 0).
+// A points at the lane's first row (row group lane / 8 of four consecutive
+// rows), B at its first column row (lane % 8 of eight consecutive rows).
+template <int NT>
+__device__ __forceinline__ void mma_nt(float (&acc)[4][NT], const float* A, int lda, const float* B, int ldb,
+                                       int kdim) {
+#pragma unroll 2
+  for (int k = 0; k < kdim; k += 4) {
+    float4 a[4], b[NT];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = lds4(A + 4 * i * lda + k);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) b[j] = lds4(B + 8 * j * ldb + k);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        acc[i][j] = fmaf(a[i].x, b[j].x, acc[i][j]);
+        acc[i][j] = fmaf(a[i].y, b[j].y, acc[i][j]);
+        acc[i][j] = fmaf(a[i].z, b[j].z, acc[i][j]);
+        acc[i][j] = fmaf(a[i].w, b[j].w, acc[i][j]);
+      }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void load_row(float (&b)[NT], const float* p) {
+  if constexpr (NT == 4) {
+    const float4 v = lds4(p);
+    b[0] = v.x, b[1] = v.y, b[2] = v.z, b[3] = v.w;
+  } else if constexpr (NT == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    b[0] = v.x, b[1] = v.y;
+  } else {
+    b[0] = *p;
+  }
+}
+
+template <int kk, int NT>
+__device__ __forceinline__ void nn_step(float (&acc)[4][NT], const float4 (&a)[4], const float* B) {
+  float b[NT];
+  load_row<NT>(b, B);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < NT; ++j) acc[i][j] = fmaf(comp<kk>(a[i]), b[j], acc[i][j]);
+}
+
+// acc[i][j] += sum_{k < kdim} A[4 i lda + k] B[k ldb + j]  (kdim % 4 == 0):
+// A as in mma_nt, B at the lane's NT consecutive columns of row 0.
+template <int NT>
+__device__ __forceinline__ void mma_nn(float (&acc)[4][NT], const float* A, int lda, const float* B, int ldb,
+                                       int kdim) {
+#pragma unroll 2
+  for (int k = 0; k < kdim; k += 4) {
+    float4 a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = lds4(A + 4 * i * lda + k);
+    nn_step<0, NT>(acc, a, B + (k + 0) * ldb);
+    nn_step<1, NT>(acc, a, B + (k + 1) * ldb);
+    nn_step<2, NT>(acc, a, B + (k + 2) * ldb);
+    nn_step<3, NT>(acc, a, B + (k + 3) * ldb);
+  }
+}
+
+// ---------------------------------------------------------------- Top-K
+// One warp: the K-th largest of keys[0 .. Nc) (orderable keys), by radix
+// selection on 8-bit digits from the top: each pass counts the keys that
+// share the digits found so far by their next digit (a 256-bin histogram in
+// shared memory) and keeps the digit in which the K-th largest falls.  thr
+// is that key; need (>= 1) is how many keys equal to thr the Top-K holds.
+__device__ void radix_select(const uint32_t* keys, int Nc, int K, uint32_t* hist, uint32_t& thr, int& need) {
+  const int lane = threadIdx.x & 31;
+  uint32_t prefix = 0, mask = 0;
+  int want = K;
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    reinterpret_cast<uint4*>(hist)[lane] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(hist)[lane + 32] = make_uint4(0, 0, 0, 0);
+    __syncwarp();
+    for (int j = lane; j < Nc; j += 32) {
+      const uint32_t u = keys[j];
+      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+    }
+    __syncwarp();
+    // Lane l owns bins 255 - 8 l - e (e = 0 .. 7), counted from the top.
+    const uint4 lo = reinterpret_cast<const uint4*>(hist)[62 - 2 * lane];
+    const uint4 hi = reinterpret_cast<const uint4*>(hist)[63 - 2 * lane];
+    const int c[8] = {static_cast<int>(hi.w), static_cast<int>(hi.z), static_cast<int>(hi.y), static_cast<int>(hi.x),
+                      static_cast<int>(lo.w), static_cast<int>(lo.z), static_cast<int>(lo.y), static_cast<int>(lo.x)};
+    int tot = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) tot += c[e];
+    int incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    const int excl = incl - tot;
+    const uint32_t hit = __ballot_sync(0xffffffffu, excl < want && want <= incl);
+    const int src = __ffs(hit) - 1;
+    int digit = 0, above = 0;
+    if (lane == src) {
+      int cum = excl;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (cum + c[e] >= want) {
+          digit = 255 - 8 * lane - e;
+          above = cum;
+          break;
+        }
+        cum += c[e];
+      }
+    }
+    digit = __shfl_sync(0xffffffffu, digit, src);
+    above = __shfl_sync(0xffffffffu, above, src);
+    want -= above;
+    prefix |= static_cast<uint32_t>(digit) << shift;
+    mask |= 255u << shift;
+    __syncwarp();
+  }
+  thr = prefix;
+  need = want;
+}
+
+// Calls f(position, j) for the Top-K entries in ascending j: every key above
+// thr and the first `need` keys equal to it.
+template <typename F>
+__device__ __forceinline__ void for_each_pick(const uint32_t* keys, int Nc, uint32_t thr, int need, F f) {
+  const int lane = threadIdx.x & 31;
   const uint32_t lt = (1u << lane) - 1u;
   int nsel = 0, eq_seen = 0;
   for (int base = 0; base < Nc; base += 32) {
@@ -243,15 +229,23 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const float* 
     const uint32_t u = j < Nc ? keys[j] : 0u;
     const bool eq = j < Nc && u == thr;
     const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
-    const bool take = (j < Nc && u > thr) || (eq && eq_seen + __popc(eqm & lt) < need_eq);
+    const bool take = (j < Nc && u > thr) || (eq && eq_seen + __popc(eqm & lt) < need);
     const uint32_t tm = __ballot_sync(0xffffffffu, take);
-    if (take) picks[nsel + __popc(tm & lt)] = (static_cast<uint64_t>(u) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j));
+    if (take) f(nsel + __popc(tm & lt), j);
     nsel += __popc(tm);
     eq_seen += __popc(eqm);
   }
+}
+
+// Highest first, ties to the lower id: each pick's rank is the number of
+// picks that beat it.  picks: K entries of scratch (key << 32 | ~id).
+__device__ void sorted_picks(const uint32_t* keys, int Nc, int K, uint32_t thr, int need, uint64_t* picks,
+                             int32_t* out) {
+  const int lane = threadIdx.x & 31;
+  for_each_pick(keys, Nc, thr, need, [&](int pos, int j) {
+    picks[pos] = (static_cast<uint64_t>(keys[j]) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j));
+  });
   __syncwarp();
-  // nsel == K: the keys above thr number < K and those >= thr number >= K.
-  int32_t* out = idx + row * K;
   constexpr int kPer = 8;
   for (int i0 = 0; i0 < K; i0 += 32 * kPer) {
     uint64_t mine[kPer];
@@ -272,107 +266,359 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const float* 
       if (i0 + q * 32 + lane < K)
         out[rank[q]] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(mine[q] & 0xFFFFFFFFu));
   }
-  if (cnt && lane == 0) cnt[row] = K;
+  __syncwarp();
 }
 
-// ---------------------------------------------------------------- backward rows
-// Row a of the backward: P = exp(S - lse_c), dS = P (dP - sum_b P dP).  S and
-// dP come in the two buffers; P and dS are written over them.
-__global__ void __launch_bounds__(kRowWarps * 32) bwd_rows_kernel(float* __restrict__ SP, float* __restrict__ dPdS,
-                                                                  const float* __restrict__ lse, int64_t rows,
-                                                                  int Nc) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + warp;
-  if (row >= rows) return;
-  float* s = SP + row * Nc;
-  float* dp = dPdS + row * Nc;
-  const float l = lse[row];
-  float dsum = 0.f;
-  for (int b = lane; b < Nc; b += 32) dsum = fmaf(__expf(s[b] - l), dp[b], dsum);
+// ---------------------------------------------------------------- forward
+// Shared memory (bytes): score rows [16][score_ld], the Q block [16][D + 4],
+// and a region used in turn by the streamed Kc / Vc tile [128][D + 4], the
+// selecting warps' histograms and (sorted lists) their Top-K scratch, and
+// the split partials of O_c.
+template <int D>
+size_t fwd_smem(int Nc, int K, int sort_warps) {
+  const size_t tile = sizeof(float) * kFwdTile * (D + 4);
+  const size_t sel = sizeof(uint32_t) * kWarps * kHist + sizeof(uint64_t) * static_cast<size_t>(sort_warps) * K;
+  return sizeof(float) * (static_cast<size_t>(kRows) * score_ld(Nc) + kRows * (D + 4)) + std::max(tile, sel);
+}
+
+// grid (ceil(Nc / 16), BH).  sort_warps == 0: each list in ascending cube
+// id; else highest first, with that many warps selecting (the Top-K scratch
+// of each must fit).  scores: null, or [BH, Nc, Nc] to receive the score
+// rows as well; oc null skips O_c (then vc may be null).
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2)
+    coarse_fwd_kernel(const float* __restrict__ qc, const float* __restrict__ kc, const float* __restrict__ vc, int Nc,
+                      int K, float scale, int sort_warps, float* __restrict__ oc, float* __restrict__ lse_c,
+                      int32_t* __restrict__ idx, int32_t* __restrict__ cnt, float* __restrict__ scores, int* err) {
+  extern __shared__ __align__(16) float smem[];
+  constexpr int ldt = D + 4;
+  const int lds = score_ld(Nc);
+  float* srow = smem;
+  float* qa = srow + kRows * lds;
+  float* region = qa + kRows * ldt;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, rg = lane >> 3, cg = lane & 7;
+  const int64_t bh = blockIdx.y;
+  const int q0 = blockIdx.x * kRows, nr = min(kRows, Nc - q0);
+  const float* Kc = kc + bh * Nc * D;
+  load_rows_async<D>(qa, qc + bh * Nc * D, q0, kRows, Nc);
+  // Score rows: warp w computes keys 16 w .. 16 w + 15 of each tile.
+  for (int t0 = 0; t0 < Nc; t0 += kFwdTile) {
+    __syncthreads();  // the previous tile is used up
+    load_rows_async<D>(region, Kc, t0, kFwdTile, Nc);
+    cp_async_wait_all();
+    __syncthreads();
+    float acc[4][2] = {};
+    mma_nt<2>(acc, qa + rg * ldt, ldt, region + (16 * warp + cg) * ldt, ldt, D);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
-  for (int b = lane; b < Nc; b += 32) {
-    const float p = __expf(s[b] - l);
-    s[b] = p;
-    dp[b] = p * (dp[b] - dsum);
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int key = t0 + 16 * warp + cg + 8 * j;
+        srow[(rg + 4 * i) * lds + key] = key < Nc ? scale * acc[i][j] : 0.f;
+      }
+  }
+  __syncthreads();
+  // Per row (one warp each): log-sum-exp, Top-K, then P in place.
+  const int sel_warps = sort_warps ? sort_warps : kWarps;
+  if (warp < sel_warps) {
+    uint32_t* hist = reinterpret_cast<uint32_t*>(region) + warp * kHist;
+    uint64_t* picks = reinterpret_cast<uint64_t*>(region + kWarps * kHist) + static_cast<size_t>(warp) * K;
+    for (int r = warp; r < nr; r += sel_warps) {
+      float* s = srow + r * lds;
+      const int64_t row = bh * Nc + q0 + r;
+      if (scores)
+        for (int j = lane; j < Nc; j += 32) scores[row * Nc + j] = s[j];
+      float m = -INFINITY;
+      bool nan = false;
+      for (int j = lane; j < Nc; j += 32) {
+        m = fmaxf(m, s[j]);
+        nan |= s[j] != s[j];
+      }
+      // A NaN score has no place in the order: it latches kErrNan (the row is
+      // still completed, NaN ranking above every number).
+      if (__any_sync(0xffffffffu, nan) && lane == 0) flag_error(err, kErrNan);
+      m = warp_max(m);
+      float l = 0.f;
+      for (int j = lane; j < Nc; j += 32) l += __expf(s[j] - m);
+      const float lse = m + __logf(warp_sum(l));
+      if (lane == 0 && lse_c) lse_c[row] = lse;
+      uint32_t* keys = reinterpret_cast<uint32_t*>(s);
+      for (int j = lane; j < Nc; j += 32) keys[j] = orderable(s[j]);
+      __syncwarp();
+      uint32_t thr;
+      int need;
+      radix_select(keys, Nc, K, hist, thr, need);
+      int32_t* out = idx + row * K;
+      if (sort_warps)
+        sorted_picks(keys, Nc, K, thr, need, picks, out);
+      else
+        for_each_pick(keys, Nc, thr, need, [&](int pos, int j) { out[pos] = j; });
+      if (cnt && lane == 0) cnt[row] = K;
+      if (oc)
+        for (int j = lane; j < Nc; j += 32) s[j] = __expf(from_orderable(keys[j]) - lse);
+      __syncwarp();
+    }
+  }
+  if (!oc) return;
+  // O_c = P Vc: warp w owns columns 32 (w % (D / 32)) .. + 31 and a share of
+  // the keys of each tile; the shares are summed at the end.
+  constexpr int kColWarps = D / 32, kSplits = kWarps / kColWarps, kPer = kFwdTile / kSplits;
+  const int col0 = 32 * (warp % kColWarps), h = warp / kColWarps;
+  const float* V = vc + bh * Nc * D;
+  float acc[4][4] = {};
+  for (int t0 = 0; t0 < Nc; t0 += kFwdTile) {
+    __syncthreads();  // histograms / the previous tile are used up
+    load_rows_async<D>(region, V, t0, kFwdTile, Nc);
+    cp_async_wait_all();
+    __syncthreads();
+    mma_nn<4>(acc, srow + rg * lds + t0 + h * kPer, lds, region + h * kPer * ldt + col0 + 4 * cg, ldt, kPer);
+  }
+  __syncthreads();
+  float* part = region;  // [kSplits - 1][16][D + 4]
+  if (h > 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(part + ((h - 1) * kRows + rg + 4 * i) * ldt + col0 + 4 * cg) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+  }
+  __syncthreads();
+  if (h == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float4 o = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      for (int p = 0; p < kSplits - 1; ++p) {
+        const float4 v = lds4(part + (p * kRows + rg + 4 * i) * ldt + col0 + 4 * cg);
+        o.x += v.x, o.y += v.y, o.z += v.z, o.w += v.w;
+      }
+      const int r = rg + 4 * i;
+      if (r < nr) *reinterpret_cast<float4*>(oc + (bh * Nc + q0 + r) * D + col0 + 4 * cg) = o;
+    }
   }
 }
 
-GemmJob job(int op, const float* A, const float* B, float* C, float alpha, int M, int N, int K, int64_t bsA,
-            int64_t bsB, int64_t bsC, const float* row_lse = nullptr, int64_t bsL = 0) {
-  GemmJob j{};
-  j.A = A;
-  j.B = B;
-  j.C = C;
-  j.row_lse = row_lse;
-  j.alpha = alpha;
-  j.op = op;
-  j.M = M;
-  j.N = N;
-  j.K = K;
-  j.bsA = bsA;
-  j.bsB = bsB;
-  j.bsC = bsC;
-  j.bsL = bsL;
-  return j;
+// ---------------------------------------------------------------- backward
+// Shared memory (bytes): the CTA's two blocks [16][D + 4], two streamed
+// tiles [64][D + 4], the P and dS tiles [16][72], and the streamed query
+// cubes' log-sum-exp and D.
+template <int D>
+constexpr size_t bwd_smem() {
+  return sizeof(float) * (2 * kRows * (D + 4) + 2 * kBwdTile * (D + 4) + 2 * kRows * kProbLd + 2 * kBwdTile);
+}
+
+// Key CTA: dKc and dVc of key cubes r0 .. r0 + 15.  Warps 0-3 compute S^T
+// (then P^T) and accumulate dKc; warps 4-7 compute dP^T (then dS^T) and
+// accumulate dVc.
+template <int D>
+__device__ __forceinline__ void bwd_keys(const float* Q, const float* Kc, const float* V, const float* G,
+                                         const float* lse, const float* delta, int Nc, float scale, int r0,
+                                         float* dk, float* dv, float* smem) {
+  constexpr int ldt = D + 4, kNk = D / 32;
+  float* a1 = smem;
+  float* a2 = a1 + kRows * ldt;
+  float* t1 = a2 + kRows * ldt;
+  float* t2 = t1 + kBwdTile * ldt;
+  float* pt = t2 + kBwdTile * ldt;
+  float* dt = pt + kRows * kProbLd;
+  float* sl = dt + kRows * kProbLd;
+  float* sd = sl + kBwdTile;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, rg = lane >> 3, cg = lane & 7;
+  const int half = warp >> 2, w4 = warp & 3;
+  load_rows_async<D>(a1, Kc, r0, kRows, Nc);
+  load_rows_async<D>(a2, V, r0, kRows, Nc);
+  const int col0 = w4 * (D / 4) + kNk * cg;
+  float acc[4][kNk] = {};
+  for (int t0 = 0; t0 < Nc; t0 += kBwdTile) {
+    __syncthreads();  // the previous tiles are used up
+    load_rows_async<D>(t1, Q, t0, kBwdTile, Nc);
+    load_rows_async<D>(t2, G, t0, kBwdTile, Nc);
+    if (tid < kBwdTile) {
+      const bool in = t0 + tid < Nc;
+      sl[tid] = in ? lse[t0 + tid] : INFINITY;  // past the last query cube: P = 0
+      sd[tid] = in ? delta[t0 + tid] : 0.f;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    float x[4][2] = {};
+    mma_nt<2>(x, (half ? a2 : a1) + rg * ldt, ldt, (half ? t2 : t1) + (16 * w4 + cg) * ldt, ldt, D);
+    if (half == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int q = 16 * w4 + cg + 8 * j;
+          pt[(rg + 4 * i) * kProbLd + q] = __expf(scale * x[i][j] - sl[q]);
+        }
+    }
+    __syncthreads();
+    if (half == 1) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int q = 16 * w4 + cg + 8 * j, e = (rg + 4 * i) * kProbLd + q;
+          dt[e] = pt[e] * (x[i][j] - sd[q]);
+        }
+    }
+    __syncthreads();
+    // dKc += dS^T Q (warps 0-3), dVc += P^T dOc (warps 4-7).
+    mma_nn<kNk>(acc, (half ? pt : dt) + rg * kProbLd, kProbLd, (half ? t2 : t1) + col0, ldt, kBwdTile);
+  }
+  float* dst = half ? dv : dk;
+  const float f = half ? 1.f : scale;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = r0 + rg + 4 * i;
+    if (r < Nc)
+#pragma unroll
+      for (int j = 0; j < kNk; ++j) dst[static_cast<int64_t>(r) * D + col0 + j] = f * acc[i][j];
+  }
+}
+
+// Query CTA: dQc of query cubes r0 .. r0 + 15.  Warps 0-3 compute S (then
+// P), warps 4-7 dP (then dS); all eight accumulate dQc.
+template <int D>
+__device__ __forceinline__ void bwd_queries(const float* Q, const float* Kc, const float* V, const float* G,
+                                            const float* lse, const float* delta, int Nc, float scale, int r0,
+                                            float* dq, float* smem) {
+  constexpr int ldt = D + 4, kNq = D / 64;
+  float* a1 = smem;
+  float* a2 = a1 + kRows * ldt;
+  float* t1 = a2 + kRows * ldt;
+  float* t2 = t1 + kBwdTile * ldt;
+  float* pt = t2 + kBwdTile * ldt;
+  float* dt = pt + kRows * kProbLd;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, rg = lane >> 3, cg = lane & 7;
+  const int half = warp >> 2, w4 = warp & 3;
+  load_rows_async<D>(a1, Q, r0, kRows, Nc);
+  load_rows_async<D>(a2, G, r0, kRows, Nc);
+  float own_l[4], own_d[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = r0 + rg + 4 * i;
+    own_l[i] = r < Nc ? lse[r] : 0.f;
+    own_d[i] = r < Nc ? delta[r] : 0.f;
+  }
+  const int col0 = warp * (D / 8) + kNq * cg;
+  float acc[4][kNq] = {};
+  for (int t0 = 0; t0 < Nc; t0 += kBwdTile) {
+    __syncthreads();
+    load_rows_async<D>(t1, Kc, t0, kBwdTile, Nc);
+    load_rows_async<D>(t2, V, t0, kBwdTile, Nc);
+    cp_async_wait_all();
+    __syncthreads();
+    float x[4][2] = {};
+    mma_nt<2>(x, (half ? a2 : a1) + rg * ldt, ldt, (half ? t2 : t1) + (16 * w4 + cg) * ldt, ldt, D);
+    if (half == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int kk = 16 * w4 + cg + 8 * j;
+          pt[(rg + 4 * i) * kProbLd + kk] = t0 + kk < Nc ? __expf(scale * x[i][j] - own_l[i]) : 0.f;
+        }
+    }
+    __syncthreads();
+    if (half == 1) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int e = (rg + 4 * i) * kProbLd + 16 * w4 + cg + 8 * j;
+          dt[e] = pt[e] * (x[i][j] - own_d[i]);
+        }
+    }
+    __syncthreads();
+    mma_nn<kNq>(acc, dt + rg * kProbLd, kProbLd, t1 + col0, ldt, kBwdTile);  // dQc += dS Kc
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = r0 + rg + 4 * i;
+    if (r < Nc)
+#pragma unroll
+      for (int j = 0; j < kNq; ++j) dq[static_cast<int64_t>(r) * D + col0 + j] = scale * acc[i][j];
+  }
+}
+
+// grid (2 ceil(Nc / 16), BH): the key CTAs first, then the query CTAs.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2)
+    coarse_bwd_kernel(const float* __restrict__ qc, const float* __restrict__ kc, const float* __restrict__ vc,
+                      const float* __restrict__ doc, const float* __restrict__ lse_c,
+                      const float* __restrict__ delta_c, int Nc, float scale, float* __restrict__ dqc,
+                      float* __restrict__ dkc, float* __restrict__ dvc) {
+  extern __shared__ __align__(16) float smem[];
+  const int64_t bh = blockIdx.y, off = bh * Nc * D;
+  const int nb = (Nc + kRows - 1) / kRows;
+  if (static_cast<int>(blockIdx.x) < nb)
+    bwd_keys<D>(qc + off, kc + off, vc + off, doc + off, lse_c + bh * Nc, delta_c + bh * Nc, Nc, scale,
+                blockIdx.x * kRows, dkc + off, dvc + off, smem);
+  else
+    bwd_queries<D>(qc + off, kc + off, vc + off, doc + off, lse_c + bh * Nc, delta_c + bh * Nc, Nc, scale,
+                   (blockIdx.x - nb) * kRows, dqc + off, smem);
+}
+
+constexpr size_t kSmemLimit = 226 * 1024;  // of the 227 KB per block; the static shared memory is a few words
+
+template <int D>
+int fwd_launch(const float* qc, const float* kc, const float* vc, int BH, int Nc, int topk, float scale, bool sorted,
+               float* oc, float* lse_c, int32_t* idx, int32_t* cnt, float* scores, cudaStream_t s) {
+  int sort_warps = 0;
+  if (sorted) {  // as many selecting warps as have room for their scratch
+    sort_warps = kWarps;
+    while (sort_warps > 1 && fwd_smem<D>(Nc, topk, sort_warps) > kSmemLimit) sort_warps >>= 1;
+  }
+  const size_t smem = fwd_smem<D>(Nc, topk, sort_warps);
+  if (smem > kSmemLimit) return VSA_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(coarse_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  dim3 grid((Nc + kRows - 1) / kRows, BH);
+  coarse_fwd_kernel<D><<<grid, kThreads, smem, s>>>(qc, kc, vc, Nc, topk, scale, sort_warps, oc, lse_c, idx, cnt,
+                                                    scores, device_error_word());
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
+template <int D>
+int bwd_launch(const float* qc, const float* kc, const float* vc, const float* doc, const float* lse_c,
+               const float* delta_c, int BH, int Nc, float scale, float* dqc, float* dkc, float* dvc,
+               cudaStream_t s) {
+  constexpr size_t smem = bwd_smem<D>();
+  if (cudaFuncSetAttribute(coarse_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  dim3 grid(2 * ((Nc + kRows - 1) / kRows), BH);
+  coarse_bwd_kernel<D><<<grid, kThreads, smem, s>>>(qc, kc, vc, doc, lse_c, delta_c, Nc, scale, dqc, dkc, dvc);
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
 }  // namespace
 
-size_t topk_rows_smem(int Nc, int K) {
-  return kRowWarps * ((static_cast<size_t>(Nc) * 4 + static_cast<size_t>(K) * 8 + 15) & ~size_t(15));
-}
-
-// O_c = softmax(scores) Vc (the row softmax applied as the scores load).
-int launch_coarse_oc(const float* scores, const float* lse_c, const float* vc, int BH, int Nc, int d, float* oc,
-                     cudaStream_t s) {
-  const int64_t nd = static_cast<int64_t>(Nc) * d, nn = static_cast<int64_t>(Nc) * Nc;
-  GemmBatch b{};
-  b.job[0] = job(kNN, scores, vc, oc, 1.0f, Nc, d, Nc, nn, nd, nd, lse_c, Nc);
-  return launch_gemm(b, 1, BH, Nc, d, s);
+bool coarse_fits(int Nc, int d, int topk, int sorted) {
+  const int w = sorted ? 1 : 0;
+  return (d == 128 ? fwd_smem<128>(Nc, topk, w) : fwd_smem<64>(Nc, topk, w)) <= kSmemLimit;
 }
 
 int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk, float scale,
-                       float* oc, float* lse_c, int32_t* idx, int32_t* cnt, float* scores, cudaStream_t s) {
-  const size_t smem = topk_rows_smem(Nc, topk);
-  if (smem > 200 * 1024) return VSA_ERR_UNSUPPORTED;
-  if (!scores || (oc && (!lse_c || !vc))) return VSA_ERR_ARG;
-  const int64_t nd = static_cast<int64_t>(Nc) * d, nn = static_cast<int64_t>(Nc) * Nc, rows = int64_t(BH) * Nc;
+                       int sorted, float* oc, float* lse_c, int32_t* idx, int32_t* cnt, float* scores,
+                       cudaStream_t s) {
+  if (oc && (!lse_c || !vc)) return VSA_ERR_ARG;
+  if (BH > 65535) return VSA_ERR_UNSUPPORTED;
   timing_mark(VSA_K_COARSE, true, s);
-  GemmBatch b{};
-  b.job[0] = job(kNT, qc, kc, scores, scale, Nc, Nc, d, nd, nd, nn);
-  int st = launch_gemm(b, 1, BH, Nc, Nc, s);
-  if (st != VSA_OK) return st;
-  if (cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-      cudaSuccess)
-    return VSA_ERR_CUDA;
-  topk_rows_kernel<<<static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps), kRowWarps * 32, smem, s>>>(
-      scores, rows, Nc, topk, idx, cnt, lse_c, device_error_word());
-  if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
-  if (oc && (st = launch_coarse_oc(scores, lse_c, vc, BH, Nc, d, oc, s)) != VSA_OK) return st;
+  const int st = d == 128 ? fwd_launch<128>(qc, kc, vc, BH, Nc, topk, scale, sorted != 0, oc, lse_c, idx, cnt, scores, s)
+                          : fwd_launch<64>(qc, kc, vc, BH, Nc, topk, scale, sorted != 0, oc, lse_c, idx, cnt, scores, s);
   timing_mark(VSA_K_COARSE, false, s);
-  return VSA_OK;
+  return st;
 }
 
-int launch_coarse_bwd(const float* qc, const float* kc, const float* vc, const float* doc, const float* lse_c, int BH,
-                      int Nc, int d, float scale, float* P, float* dS, float* dqc, float* dkc, float* dvc,
+int launch_coarse_bwd(const float* qc, const float* kc, const float* vc, const float* doc, const float* lse_c,
+                      const float* delta_c, int BH, int Nc, int d, float scale, float* dqc, float* dkc, float* dvc,
                       cudaStream_t s) {
-  const int64_t nd = static_cast<int64_t>(Nc) * d, nn = static_cast<int64_t>(Nc) * Nc, rows = int64_t(BH) * Nc;
+  if (BH > 65535) return VSA_ERR_UNSUPPORTED;
   timing_mark(VSA_K_COARSE_BWD, true, s);
-  GemmBatch b{};
-  b.job[0] = job(kNT, qc, kc, P, scale, Nc, Nc, d, nd, nd, nn);   // S
-  b.job[1] = job(kNT, doc, vc, dS, 1.0f, Nc, Nc, d, nd, nd, nn);  // dP
-  int st = launch_gemm(b, 2, BH, Nc, Nc, s);
-  if (st != VSA_OK) return st;
-  bwd_rows_kernel<<<static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps), kRowWarps * 32, 0, s>>>(P, dS, lse_c,
-                                                                                                    rows, Nc);
-  if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
-  b.job[0] = job(kNN, dS, kc, dqc, scale, Nc, d, Nc, nn, nd, nd);  // dQc = scale dS Kc
-  b.job[1] = job(kTN, dS, qc, dkc, scale, Nc, d, Nc, nn, nd, nd);  // dKc = scale dS^T Qc
-  b.job[2] = job(kTN, P, doc, dvc, 1.0f, Nc, d, Nc, nn, nd, nd);   // dVc = P^T dOc
-  if ((st = launch_gemm(b, 3, BH, Nc, d, s)) != VSA_OK) return st;
+  const int st = d == 128 ? bwd_launch<128>(qc, kc, vc, doc, lse_c, delta_c, BH, Nc, scale, dqc, dkc, dvc, s)
+                          : bwd_launch<64>(qc, kc, vc, doc, lse_c, delta_c, BH, Nc, scale, dqc, dkc, dvc, s);
   timing_mark(VSA_K_COARSE_BWD, false, s);
-  return VSA_OK;
+  return st;
 }
 
 }  // namespace vsa

@@ -106,11 +106,15 @@ int launch_permute(const void* const* src, void* const* dst, float* const* poole
                    int d, int T, int H, int W, const int32_t* order, int inverse, int f16_out, cudaStream_t s);
 int launch_cube_order(int Tc, int Hc, int Wc, int curve, int32_t* order, cudaStream_t s);
 int make_tile_map(void* map, const void* base, int64_t rows, int d, int f16);
+// Coarse scores, each row's log-sum-exp and Top-K, and O_c (oc non-null),
+// score rows kept on chip; scores non-null receives them as well.  sorted:
+// lists highest first (ties to the lower id), else in ascending cube id.  A
+// NaN score latches kErrNan.
 int launch_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk,
-                       float scale, float* oc, float* lse_c, int32_t* idx, int32_t* cnt, float* scores,
-                       cudaStream_t s);  // a NaN score latches kErrNan
-int launch_coarse_oc(const float* scores, const float* lse_c, const float* vc, int BH, int Nc, int d, float* oc,
-                     cudaStream_t s);
+                       float scale, int sorted, float* oc, float* lse_c, int32_t* idx, int32_t* cnt, float* scores,
+                       cudaStream_t s);
+// Whether the coarse forward's score rows and scratch fit shared memory.
+bool coarse_fits(int Nc, int d, int topk, int sorted);
 int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* idx, const int32_t* cnt,
                     int kmax, int BH, int N, int d, float scale, void* of, int of_dtype, float* lse, int f16_in,
                     const int32_t* pairs, const uint64_t* kmask, cudaStream_t s);
@@ -123,9 +127,24 @@ int launch_fine_fwd_native(const void* q, const void* k, const void* v, int T, i
 int launch_slot_masks(int T, int H, int W, const int32_t* order, uint64_t* kmask, cudaStream_t s);
 size_t pair_plan_smem(int Nc);
 size_t pair_plan_ws_bytes(int BH, int Nc);  // pairs + overlap scratch of launch_pair_plan
-int launch_list_bits(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, uint32_t* bits,
+// Inverse lists in CSR form: for head bh, the query cubes whose index list
+// holds key cube c are ids[bh * stride + off[bh][c] .. off[bh][c + 1]) (in no
+// particular order); off is [BH][Nc + 1].
+struct InverseLists {
+  const int32_t* off;
+  const int32_t* ids;
+  int64_t stride;
+};
+size_t inverse_lists_bytes(int BH, int Nc, int kmax);  // off, cursors and ids of build_inverse_lists
+// Builds the CSR inverse lists of [BH, Nc, kmax] index lists (counts cnt, or
+// null for full rows) in ws (inverse_lists_bytes); entries outside [0, Nc)
+// and counts outside [0, kmax] latch kErrLut.
+int launch_inverse_lists(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, void* ws,
+                         InverseLists* out, cudaStream_t s);
+// Pairs query cubes by their index lists / key cubes by their inverse lists.
+int launch_pair_plan(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, int32_t* pairs,
                      cudaStream_t s);
-int launch_pair_plan(const uint32_t* bits, int BH, int Nc, int32_t* pairs, cudaStream_t s);
+int launch_pair_plan_inverse(const InverseLists& inv, int BH, int Nc, int32_t* pairs, cudaStream_t s);
 int launch_mask_to_lut(const uint8_t* mask, int BH, int Nc, int kmax, int32_t* idx, int32_t* cnt, cudaStream_t s);
 int launch_add_neighbors(const int32_t* idx_in, const int32_t* cnt_in, int kmax_in, int BH, int Tc, int Hc, int Wc,
                          const int32_t* order, int radius, int kmax_out, int32_t* idx_out, int32_t* cnt_out,
@@ -156,16 +175,19 @@ int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* 
 // and plan do not), or null.
 int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const void* dof, const float* lse,
                          const float* delta, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
-                         float scale, float* dq, float* dk, float* dv, const FusedGrads* fused, uint32_t* inv_ws,
+                         float scale, float* dq, float* dk, float* dv, const FusedGrads* fused, void* inv_ws,
                          const int32_t* qpairs, int32_t* kpairs_ws, cudaStream_t s, cudaStream_t s_kv,
                          cudaEvent_t kv_after);
 int launch_combine(const float* oc, const float* of, const void* gc, const void* gf, void* out, int out_dtype,
                    int BH, int d, int T, int H, int W, const int32_t* order, cudaStream_t s);
+// delta_c (may be null) receives D_c = dO_c . O_c of each cube.
 int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const float* oc, const float* of,
-                    __half* dof, float* delta, float* doc, void* dgc, void* dgf, int grad_dtype, int BH, int d,
-                    int T, int H, int W, const int32_t* order, cudaStream_t s);
+                    __half* dof, float* delta, float* doc, float* delta_c, void* dgc, void* dgf, int grad_dtype,
+                    int BH, int d, int T, int H, int W, const int32_t* order, cudaStream_t s);
+// Coarse backward from the row statistic delta_c [BH, Nc] (D = dO_c . O_c,
+// written by launch_bwd_prep).
 int launch_coarse_bwd(const float* qc, const float* kc, const float* vc, const float* doc, const float* lse_c,
-                      int BH, int Nc, int d, float scale, float* P, float* dS, float* dqc, float* dkc, float* dvc,
+                      const float* delta_c, int BH, int Nc, int d, float scale, float* dqc, float* dkc, float* dvc,
                       cudaStream_t s);
 
 }  // namespace vsa

@@ -39,8 +39,8 @@
 // V only by dP(j), so one stage suffices: V(j+1) lands while S(j+1) runs.
 //
 // Operands are fp16 (exact for the bf16 inputs within +-65504), accumulation
-// fp32.  The inverse lists come from a bit matrix inv[bh][key cube][query
-// cube] built from the index list (workspace).
+// fp32.  The inverse lists (the query cubes whose list holds a key cube) are
+// built from the index lists in CSR form, by counting sort (workspace).
 //
 // Epilogues: each kernel writes its rows once.  For the whole VSA backward
 // they also finish the gradient: a row of cube c gets c's coarse-stage
@@ -65,7 +65,7 @@ struct BwdParams {
   CUtensorMap tq, tk, tv, tdo;  // fp16 [BH*N, d], box {64, 64}, 128B swizzle
   const float* lse;             // natural-log LSE per row [BH*N]
   const float* delta;           // D per row [BH*N]
-  const uint32_t* inv;          // [BH][Nc][nwords]
+  InverseLists inv;             // CSR inverse lists
   const int32_t* idx;           // forward index list [BH][Nc][kmax]
   const int32_t* cnt;           // [BH][Nc] or null (= kmax)
   float* dq;                    // fp32 rows in cube order (fused == 0)
@@ -321,12 +321,19 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       crow[e] = *src;
     }
   }
+  for (int w = tid; w < 2 * p.nwords; w += kThreads) bitA[w] = 0u;  // bitA and bitB are contiguous
+  __syncthreads();
   {
-    const uint32_t* ra = p.inv + (bh * p.Nc + k1) * p.nwords;
-    const uint32_t* rb = p.inv + (bh * p.Nc + (has_k2 ? k2 : k1)) * p.nwords;
-    for (int w = tid; w < p.nwords; w += kThreads) {
-      bitA[w] = ra[w];
-      bitB[w] = has_k2 ? rb[w] : 0u;
+    // The two key cubes' inverse lists as bitmaps of query cubes.
+    const int32_t* off = p.inv.off + bh * (p.Nc + 1);
+    const int32_t* ids = p.inv.ids + bh * p.inv.stride;
+    const int a0 = off[k1], na = off[k1 + 1] - a0;
+    const int b0 = has_k2 ? off[k2] : 0, nb = has_k2 ? off[k2 + 1] - b0 : 0;
+    for (int e = tid; e < na + nb; e += kThreads) {
+      const bool isA = e < na;
+      const int q = ids[isA ? a0 + e : b0 + e - na];
+      const uint32_t old = atomicOr(&(isA ? bitA : bitB)[q >> 5], 1u << (q & 31));
+      if (old & (1u << (q & 31))) flag_error(p.err, kErrLut);  // a list holding this key cube twice
     }
   }
   __syncthreads();
@@ -815,9 +822,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
   }
 }
 
-// inv[bh][key cube][query cube / 32] |= bit for every listed (query, key).
-__global__ void build_inverse_bits(const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int kmax,
-                                   int Nc, int nwords, int64_t rows, uint32_t* __restrict__ inv, int* err) {
+// Inverse lists by counting sort: counts[bh][c] = number of query cubes
+// listing key cube c (entries outside [0, Nc) and counts outside [0, kmax]
+// latch kErrLut and are skipped).
+__global__ void inv_count_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int kmax, int Nc,
+                                 int64_t rows, int* __restrict__ counts, int* err) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= rows * kmax) return;
   const int64_t row = e / kmax;  // bh * Nc + query cube
@@ -833,10 +842,66 @@ __global__ void build_inverse_bits(const int32_t* __restrict__ idx, const int32_
     flag_error(err, kErrLut);
     return;
   }
+  atomicAdd(counts + (row / Nc) * Nc + c, 1);
+}
+
+// One CTA per head: off[0 .. Nc] = exclusive prefix sums of the counts, and
+// the counts replaced by the same offsets (the fill kernel's cursors).
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads) inv_scan_kernel(int* __restrict__ counts, int Nc,
+                                                                int32_t* __restrict__ off) {
+  __shared__ int warp_sum[32];
+  const int64_t bh = blockIdx.x;
+  int* cnt = counts + bh * Nc;
+  int32_t* o = off + bh * (Nc + 1);
+  const int per = (Nc + kScanThreads - 1) / kScanThreads;
+  const int c0 = threadIdx.x * per, c1 = min(Nc, c0 + per);
+  int mine = 0;
+  for (int c = c0; c < c1; ++c) mine += cnt[c];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = mine;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += t;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = warp_sum[lane];
+    int wi = w;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, wi, d);
+      if (lane >= d) wi += t;
+    }
+    warp_sum[lane] = wi - w;  // exclusive sum of the warps before
+  }
+  __syncthreads();
+  int run = warp_sum[warp] + incl - mine;
+  for (int c = c0; c < c1; ++c) {
+    const int v = cnt[c];
+    o[c] = run;
+    cnt[c] = run;
+    run += v;
+  }
+  if (threadIdx.x == kScanThreads - 1) o[Nc] = run;
+}
+
+// ids[bh * stride + slot] = query cube, one slot per (query, key) entry.
+__global__ void inv_fill_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int kmax, int Nc,
+                                int64_t rows, int* __restrict__ cursor, int32_t* __restrict__ ids, int64_t stride) {
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (e >= rows * kmax) return;
+  const int64_t row = e / kmax;
+  const int slot = static_cast<int>(e % kmax);
+  const int n = min(max(cnt ? cnt[row] : kmax, 0), kmax);
+  if (slot >= n) return;
+  const int c = idx[e];
+  if (c < 0 || c >= Nc) return;
   const int64_t bh = row / Nc;
-  const int q = static_cast<int>(row % Nc);
-  const uint32_t old = atomicOr(inv + (bh * Nc + c) * nwords + (q >> 5), 1u << (q & 31));
-  if (old & (1u << (q & 31))) flag_error(err, kErrLut);  // repeated cube in a row
+  const int pos = atomicAdd(cursor + bh * Nc + c, 1);
+  ids[bh * stride + pos] = static_cast<int32_t>(row % Nc);
 }
 
 // D_i = dO_i . O_i (fp32, dO as the fp16 operand the MMAs use), one warp per row.
@@ -878,10 +943,35 @@ __global__ void to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__
 
 }  // namespace
 
+size_t inverse_lists_bytes(int BH, int Nc, int kmax) {
+  auto a = [](size_t x) { return (x + 255) & ~size_t(255); };
+  return a(sizeof(int32_t) * static_cast<size_t>(BH) * (Nc + 1)) + a(sizeof(int) * static_cast<size_t>(BH) * Nc) +
+         a(sizeof(int32_t) * static_cast<size_t>(BH) * Nc * kmax);
+}
+
+int launch_inverse_lists(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, void* ws,
+                         InverseLists* out, cudaStream_t s) {
+  auto a = [](size_t x) { return (x + 255) & ~size_t(255); };
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* off = reinterpret_cast<int32_t*>(w);
+  w += a(sizeof(int32_t) * static_cast<size_t>(BH) * (Nc + 1));
+  int* counts = reinterpret_cast<int*>(w);
+  w += a(sizeof(int) * static_cast<size_t>(BH) * Nc);
+  int32_t* ids = reinterpret_cast<int32_t*>(w);
+  *out = InverseLists{off, ids, static_cast<int64_t>(Nc) * kmax};
+  if (cudaMemsetAsync(counts, 0, sizeof(int) * static_cast<size_t>(BH) * Nc, s) != cudaSuccess) return VSA_ERR_CUDA;
+  const int64_t rows = static_cast<int64_t>(BH) * Nc, entries = rows * kmax;
+  int* err = device_error_word();
+  const unsigned blocks = static_cast<unsigned>((entries + 255) / 256);
+  if (entries > 0) inv_count_kernel<<<blocks, 256, 0, s>>>(idx, cnt, kmax, Nc, rows, counts, err);
+  inv_scan_kernel<<<BH, kScanThreads, 0, s>>>(counts, Nc, off);
+  if (entries > 0) inv_fill_kernel<<<blocks, 256, 0, s>>>(idx, cnt, kmax, Nc, rows, counts, ids, out->stride);
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
 size_t fine_bwd_ws_bytes(int BH, int N, int kmax) {
-  (void)kmax;
-  const int64_t Nc = N / kCube, nwords = (Nc + 31) / 32;
-  size_t inv = sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords;
+  const int64_t Nc = N / kCube;
+  size_t inv = inverse_lists_bytes(BH, static_cast<int>(Nc), kmax);
   size_t delta = sizeof(float) * static_cast<size_t>(BH) * N;
   size_t copy = sizeof(__half) * static_cast<size_t>(BH) * N * 128;  // room for d <= 128
   size_t kpairs = pair_plan_ws_bytes(BH, static_cast<int>(Nc));
@@ -898,7 +988,7 @@ int launch_delta(const void* of, int of_dtype, const void* dof, int64_t rows, in
 
 // Fine backward with the row statistics D given.  qp, kp, vp, dof are fp16
 // (cube order); fused: where the gradient rows go (null: fp32 dq, dk, dv in
-// cube order); inv_ws: scratch for the inverse-list bit matrix; qpairs: the
+// cube order); inv_ws: scratch for the inverse lists (inverse_lists_bytes); qpairs: the
 // query-cube tiles of the dQ kernel (null: cubes 2t, 2t + 1); kpairs_ws:
 // scratch for the key-cube pair plan (null: cubes 2t, 2t + 1).  The inverse
 // lists, the key plan and the dK/dV kernel go on s_kv (the kernel after
@@ -906,7 +996,7 @@ int launch_delta(const void* of, int of_dtype, const void* dof, int64_t rows, in
 // s_kv may be s).
 int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const void* dof, const float* lse,
                          const float* delta, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
-                         float scale, float* dq, float* dk, float* dv, const FusedGrads* fused, uint32_t* inv_ws,
+                         float scale, float* dq, float* dk, float* dv, const FusedGrads* fused, void* inv_ws,
                          const int32_t* qpairs, int32_t* kpairs_ws, cudaStream_t s, cudaStream_t s_kv,
                          cudaEvent_t kv_after) {
   BwdParams p{};
@@ -919,7 +1009,6 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   const int Nc = N / kCube, nwords = (Nc + 31) / 32;
   p.lse = lse;
   p.delta = delta;
-  p.inv = inv_ws;
   p.idx = idx;
   p.cnt = cnt;
   p.dq = dq;
@@ -939,13 +1028,8 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   p.npairs = (Nc + 1) / 2;
   p.qpairs = qpairs;
   p.kpairs = kpairs_ws;
-  const size_t inv_bytes = sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords;
-  if (cudaMemsetAsync(inv_ws, 0, inv_bytes, s_kv) != cudaSuccess) return VSA_ERR_CUDA;
-  const int64_t entries = static_cast<int64_t>(BH) * Nc * kmax;
-  if (entries > 0)
-    build_inverse_bits<<<static_cast<unsigned>((entries + 255) / 256), 256, 0, s_kv>>>(
-        idx, cnt, kmax, Nc, nwords, static_cast<int64_t>(BH) * Nc, inv_ws, p.err);
-  if (kpairs_ws && (st = launch_pair_plan(inv_ws, BH, Nc, kpairs_ws, s_kv)) != VSA_OK) return st;
+  if ((st = launch_inverse_lists(idx, cnt, kmax, BH, Nc, inv_ws, &p.inv, s_kv)) != VSA_OK) return st;
+  if (kpairs_ws && (st = launch_pair_plan_inverse(p.inv, BH, Nc, kpairs_ws, s_kv)) != VSA_OK) return st;
   if (kv_after && cudaStreamWaitEvent(s_kv, kv_after, 0) != cudaSuccess) return VSA_ERR_CUDA;
   const size_t kv_extra = sizeof(uint32_t) * (2 * Nc + 2 + 2 * nwords) + 4 * sizeof(float) * d;
   const size_t dq_extra = sizeof(uint32_t) * (2 * kmax + 2 + 2 * nwords);
@@ -977,11 +1061,11 @@ int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* 
                     const void* dof, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
                     float scale, float* dq, float* dk, float* dv, void* ws, size_t ws_bytes, cudaStream_t s) {
   if (!ws || ws_bytes < fine_bwd_ws_bytes(BH, N, kmax)) return VSA_ERR_WORKSPACE;
-  const int64_t Nc = N / kCube, nwords = (Nc + 31) / 32, rows = static_cast<int64_t>(BH) * N;
+  const int64_t Nc = N / kCube, rows = static_cast<int64_t>(BH) * N;
   auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
   uint8_t* w = static_cast<uint8_t*>(ws);
-  uint32_t* inv_ws = reinterpret_cast<uint32_t*>(w);
-  w += a256(sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords);
+  void* inv_ws = w;
+  w += inverse_lists_bytes(BH, static_cast<int>(Nc), kmax);
   float* delta = reinterpret_cast<float*>(w);
   w += a256(sizeof(float) * rows);
   const size_t copy = a256(sizeof(__half) * static_cast<size_t>(rows) * 128);

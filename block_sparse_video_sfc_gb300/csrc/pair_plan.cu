@@ -17,6 +17,13 @@
 // the synthetic 32K-token layer (K = 154 cubes per list) this cuts the mean
 // union per pair from 1.63 K to about 1.51 K cubes, i.e. from 251 to 233
 // (a global greedy matching reaches 1.48 K).
+//
+// The overlaps come straight from the lists: a CTA takes kBlock consecutive
+// cubes, turns their lists and those of the kWindow cubes after them into
+// bitmaps in shared memory and counts the common bits, so no Nc x Nc matrix
+// is ever stored.  The lists are either the forward index lists (row c:
+// kv_block_idx[c][0 .. valid_block_num[c])) or the inverse lists of the
+// backward in CSR form (row c: the query cubes listing key cube c).
 #include "common.cuh"
 
 namespace vsa {
@@ -25,22 +32,31 @@ namespace {
 constexpr int kWindow = 32;
 constexpr int kRounds = 8;
 constexpr int kPlanThreads = 512;
+constexpr int kBlock = 64;               // cubes whose overlaps one CTA counts
+constexpr int kOverlapThreads = 256;
 
-// bits[bh][c][nwords] |= bit of every cube listed in row c (the lists as a
-// bit matrix; entries outside [0, Nc) are skipped, the fine kernels report them).
-__global__ void build_list_bits(const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int kmax, int Nc,
-                                int nwords, int64_t rows, uint32_t* __restrict__ bits) {
-  const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (e >= rows * kmax) return;
-  const int64_t row = e / kmax;
-  const int slot = static_cast<int>(e % kmax);
-  int n = cnt ? cnt[row] : kmax;
-  n = min(max(n, 0), kmax);
-  if (slot >= n) return;
-  const int c = idx[e];
-  if (c < 0 || c >= Nc) return;
-  atomicOr(bits + row * nwords + (c >> 5), 1u << (c & 31));
-}
+// Row c of the forward index lists of head bh.
+struct ListRows {
+  const int32_t* idx;
+  const int32_t* cnt;  // null: every row holds kmax entries
+  int kmax, Nc;
+  __device__ __forceinline__ int get(int64_t bh, int c, const int32_t** p) const {
+    const int64_t row = bh * Nc + c;
+    *p = idx + row * kmax;
+    const int n = cnt ? __ldg(cnt + row) : kmax;
+    return min(max(n, 0), kmax);
+  }
+};
+// Row c of the inverse lists (CSR) of head bh.
+struct CsrRows {
+  InverseLists inv;
+  int Nc;
+  __device__ __forceinline__ int get(int64_t bh, int c, const int32_t** p) const {
+    const int32_t* off = inv.off + bh * (Nc + 1);
+    *p = inv.ids + bh * inv.stride + __ldg(off + c);
+    return __ldg(off + c + 1) - __ldg(off + c);
+  }
+};
 
 // Exclusive prefix sum of one int per thread over the block; returns the
 // thread's offset, and the total in *total.
@@ -73,20 +89,41 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
 }
 
 // ov[bh][c][d - 1] = |list c & list c + d| for d = 1..kWindow (0 past the
-// last cube): one thread per (cube, offset), spread over the whole GPU.
-__global__ void __launch_bounds__(256) pair_overlap_kernel(const uint32_t* __restrict__ bits, int Nc, int nwords,
-                                                           uint16_t* __restrict__ ov) {
+// last cube).  CTA (block, bh): cubes c0 .. c0 + kBlock - 1 and the kWindow
+// after them become bitmaps in shared memory (row stride nwords + 1 words,
+// odd, so that the threads of a warp, which read different rows at the same
+// word, hit different banks); then one thread per (cube, offset) counts.
+template <class Rows>
+__global__ void __launch_bounds__(kOverlapThreads) pair_overlap_kernel(Rows rows, int Nc, uint16_t* __restrict__ ov) {
+  extern __shared__ uint32_t wbits[];
   const int64_t bh = blockIdx.y;
-  const int it = blockIdx.x * blockDim.x + threadIdx.x;
-  if (it >= Nc * kWindow) return;
-  const int c = it / kWindow, d = it % kWindow + 1;
-  int n = 0;
-  if (c + d < Nc) {
-    const uint32_t* a = bits + (bh * Nc + c) * nwords;
-    const uint32_t* b = a + static_cast<int64_t>(d) * nwords;
-    for (int w = 0; w < nwords; ++w) n += __popc(__ldg(a + w) & __ldg(b + w));
+  const int c0 = blockIdx.x * kBlock;
+  const int nwords = (Nc + 31) >> 5, stride = nwords + 1;
+  const int ncubes = min(kBlock + kWindow, Nc - c0);
+  for (int i = threadIdx.x; i < ncubes * stride; i += blockDim.x) wbits[i] = 0u;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < ncubes; i += kOverlapThreads / 32) {
+    const int32_t* list;
+    const int n = rows.get(bh, c0 + i, &list);
+    for (int e = lane; e < n; e += 32) {
+      const int c = __ldg(list + e);
+      if (c >= 0 && c < Nc) atomicOr(&wbits[i * stride + (c >> 5)], 1u << (c & 31));  // others: reported elsewhere
+    }
   }
-  ov[bh * Nc * kWindow + it] = static_cast<uint16_t>(n);
+  __syncthreads();
+  for (int it = threadIdx.x; it < kBlock * kWindow; it += blockDim.x) {
+    const int i = it / kWindow, d = it % kWindow + 1;
+    const int c = c0 + i;
+    if (c >= Nc) continue;
+    int n = 0;
+    if (c + d < Nc) {
+      const uint32_t* a = wbits + i * stride;
+      const uint32_t* b = wbits + (i + d) * stride;
+      for (int w = 0; w < nwords; ++w) n += __popc(a[w] & b[w]);
+    }
+    ov[(bh * Nc + c) * kWindow + d - 1] = static_cast<uint16_t>(n);
+  }
 }
 
 // One CTA per (batch, head).  Shared memory: the head's overlaps
@@ -179,33 +216,39 @@ size_t pair_plan_ws_bytes(int BH, int Nc) {
          a256(sizeof(uint16_t) * static_cast<size_t>(BH) * Nc * kWindow);
 }
 
-int launch_list_bits(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, uint32_t* bits,
-                     cudaStream_t s) {
-  const int nwords = (Nc + 31) / 32;
-  if (cudaMemsetAsync(bits, 0, sizeof(uint32_t) * static_cast<size_t>(BH) * Nc * nwords, s) != cudaSuccess)
-    return VSA_ERR_CUDA;
-  const int64_t rows = static_cast<int64_t>(BH) * Nc, entries = rows * kmax;
-  if (entries > 0)
-    build_list_bits<<<static_cast<unsigned>((entries + 255) / 256), 256, 0, s>>>(idx, cnt, kmax, Nc, nwords, rows,
-                                                                                    bits);
-  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
-}
+namespace {
 
-// pairs_ws: pair_plan_ws_bytes(BH, Nc) bytes; the pairs come first, the
-// overlap scratch after them.
-int launch_pair_plan(const uint32_t* bits, int BH, int Nc, int32_t* pairs_ws, cudaStream_t s) {
+template <class Rows>
+int plan(const Rows& rows, int BH, int Nc, int32_t* pairs_ws, cudaStream_t s) {
   if (Nc > 32767) return VSA_ERR_UNSUPPORTED;
   const size_t smem = pair_plan_smem(Nc);
   if (smem > 200 * 1024) return VSA_ERR_UNSUPPORTED;
+  const size_t osmem = sizeof(uint32_t) * static_cast<size_t>(kBlock + kWindow) * ((Nc + 31) / 32 + 1);
+  if (osmem > 200 * 1024) return VSA_ERR_UNSUPPORTED;
   uint16_t* ov = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(pairs_ws) +
                                              a256(sizeof(int32_t) * static_cast<size_t>(BH) * ((Nc + 1) / 2) * 2));
-  dim3 g1((Nc * kWindow + 255) / 256, BH);
-  pair_overlap_kernel<<<g1, 256, 0, s>>>(bits, Nc, (Nc + 31) / 32, ov);
+  if (cudaFuncSetAttribute(pair_overlap_kernel<Rows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(osmem)) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  dim3 g1((Nc + kBlock - 1) / kBlock, BH);
+  pair_overlap_kernel<Rows><<<g1, kOverlapThreads, osmem, s>>>(rows, Nc, ov);
   if (cudaFuncSetAttribute(plan_pairs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return VSA_ERR_CUDA;
   plan_pairs_kernel<<<BH, kPlanThreads, smem, s>>>(ov, Nc, pairs_ws);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
+}  // namespace
+
+// pairs_ws: pair_plan_ws_bytes(BH, Nc) bytes; the pairs come first, the
+// overlap scratch after them.
+int launch_pair_plan(const int32_t* idx, const int32_t* cnt, int kmax, int BH, int Nc, int32_t* pairs_ws,
+                     cudaStream_t s) {
+  return plan(ListRows{idx, cnt, kmax, Nc}, BH, Nc, pairs_ws, s);
+}
+int launch_pair_plan_inverse(const InverseLists& inv, int BH, int Nc, int32_t* pairs_ws, cudaStream_t s) {
+  return plan(CsrRows{inv, Nc}, BH, Nc, pairs_ws, s);
 }
 
 }  // namespace vsa

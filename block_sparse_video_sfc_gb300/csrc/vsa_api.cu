@@ -53,15 +53,17 @@ int list_width(int topk, int radius, int64_t Nc) {
   const int64_t n = static_cast<int64_t>(topk) + (2 * radius + 1) * (2 * radius + 1) * (2 * radius + 1);
   return static_cast<int>(n < Nc ? n : Nc);
 }
-int check_selection(const Dims& D, int topk, int radius) {
+// coarse: the coarse stage runs too (its score rows must fit on chip).
+int check_selection(const Dims& D, int topk, int radius, bool coarse = true) {
   if (topk < 1 || topk > D.Nc) return VSA_ERR_ARG;
   if (radius < -1 || radius > 7) return VSA_ERR_ARG;
+  if (coarse && !coarse_fits(static_cast<int>(D.Nc), D.d, topk, 0)) return VSA_ERR_UNSUPPORTED;
   return VSA_OK;
 }
 
 // Forward workspace: the saved state of one vsa_forward call.
 struct FwdWs {
-  size_t qp, kp, vp, qc, kc, vc, oc, lsec, sc, idx, cnt, of, lse, lbits, pairs, kmask, idx_tk, total;
+  size_t qp, kp, vp, qc, kc, vc, oc, lsec, idx, cnt, of, lse, pairs, kmask, idx_tk, total;
   int kmax;  // width of the saved lists
 };
 // copies = false: the inference forward, which reads Q, K, V in place.
@@ -80,12 +82,10 @@ FwdWs fwd_layout(const Dims& D, int topk, int radius, bool copies = true) {
   w.vc = o; o += align256(pooled);
   w.oc = o; o += align256(pooled);
   w.lsec = o; o += align256(sizeof(float) * D.BH * D.Nc);
-  w.sc = o; o += align256(sizeof(float) * D.BH * D.Nc * D.Nc);
   w.idx = o; o += align256(sizeof(int32_t) * D.BH * D.Nc * K);
   w.cnt = o; o += align256(sizeof(int32_t) * D.BH * D.Nc);
   w.of = o; o += align256(sizeof(float) * D.BH * D.N * D.d);
   w.lse = o; o += align256(sizeof(float) * D.BH * D.N);
-  w.lbits = o; o += align256(sizeof(uint32_t) * D.BH * D.Nc * ((D.Nc + 31) / 32));
   w.pairs = o; o += align256(pair_plan_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.Nc)));
   w.kmask = o; o += align256(sizeof(uint64_t) * D.Nc);
   w.idx_tk = o; o += radius >= 0 ? align256(sizeof(int32_t) * D.BH * D.Nc * topk) : 0;  // the Top-K before the union
@@ -93,17 +93,17 @@ FwdWs fwd_layout(const Dims& D, int topk, int radius, bool copies = true) {
   return w;
 }
 
-// The selection of vsa_forward / vsa_forward_inference: Top-K lists into the
-// saved lists, or, with a radius, into scratch and then united with each
-// query cube's neighbourhood (ascending lists with counts).
+// The coarse stage of vsa_forward / vsa_forward_inference: O_c, the coarse
+// log-sum-exp and the selection -- Top-K lists into the saved lists, or, with
+// a radius, into scratch and then united with each query cube's neighbourhood
+// (ascending lists with counts).
 int select_lists(const float* qc, const float* kc, const float* vc, const Dims& D, const vsa_grid_t& g, int topk,
                  int radius, float scale, const FwdWs& w, void* ws, cudaStream_t s) {
   const int BH = static_cast<int>(D.BH), Nc = static_cast<int>(D.Nc);
   int32_t* idx = at<int32_t>(ws, w.idx);
   int32_t* cnt = at<int32_t>(ws, w.cnt);
-  int st = launch_coarse_topk(qc, kc, vc, BH, Nc, D.d, topk, scale, nullptr, at<float>(ws, w.lsec),
-                              radius >= 0 ? at<int32_t>(ws, w.idx_tk) : idx, radius >= 0 ? nullptr : cnt,
-                              at<float>(ws, w.sc), s);
+  int st = launch_coarse_topk(qc, kc, vc, BH, Nc, D.d, topk, scale, 0, at<float>(ws, w.oc), at<float>(ws, w.lsec),
+                              radius >= 0 ? at<int32_t>(ws, w.idx_tk) : idx, radius >= 0 ? nullptr : cnt, nullptr, s);
   if (st != VSA_OK || radius < 0) return st;
   return launch_add_neighbors(at<int32_t>(ws, w.idx_tk), nullptr, topk, BH, (g.T + 3) / 4, (g.H + 3) / 4,
                               (g.W + 3) / 4, g.cube_order, radius, w.kmax, idx, cnt, s);
@@ -111,22 +111,21 @@ int select_lists(const float* qc, const float* kc, const float* vc, const Dims& 
 
 // Backward workspace (scratch of one vsa_backward call).
 struct BwdWs {
-  size_t dof, delta, doc, P, dS, dqc, dkc, dvc, inv, kpairs, total;
+  size_t dof, delta, doc, deltac, dqc, dkc, dvc, inv, kpairs, total;
 };
-BwdWs bwd_layout(const Dims& D) {
+// kmax: the width of the forward's saved lists.
+BwdWs bwd_layout(const Dims& D, int kmax) {
   BwdWs w{};
   size_t o = 0;
   const size_t pooled = sizeof(float) * D.BH * D.Nc * D.d;
-  const int64_t nwords = (D.Nc + 31) / 32;
   w.dof = o; o += align256(sizeof(__half) * D.BH * D.N * D.d);
   w.delta = o; o += align256(sizeof(float) * D.BH * D.N);
   w.doc = o; o += align256(pooled);
-  w.P = o; o += align256(sizeof(float) * D.BH * D.Nc * D.Nc);
-  w.dS = o; o += align256(sizeof(float) * D.BH * D.Nc * D.Nc);
+  w.deltac = o; o += align256(sizeof(float) * D.BH * D.Nc);
   w.dqc = o; o += align256(pooled);
   w.dkc = o; o += align256(pooled);
   w.dvc = o; o += align256(pooled);
-  w.inv = o; o += align256(sizeof(uint32_t) * D.BH * D.Nc * nwords);
+  w.inv = o; o += align256(inverse_lists_bytes(static_cast<int>(D.BH), static_cast<int>(D.Nc), kmax));
   w.kpairs = o; o += align256(pair_plan_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.Nc)));
   w.total = o;
   return w;
@@ -359,11 +358,11 @@ int vsa_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, i
   if (d != 64 && d != 128) return VSA_ERR_UNSUPPORTED;
   if (BH <= 0 || Nc <= 0) return VSA_ERR_ARG;
   if (topk < 1 || topk > Nc) return VSA_ERR_ARG;
-  if (!qc || !kc || !kv_block_idx || !scores || (o_coarse && (!vc || !lse_coarse))) return VSA_ERR_ARG;
-  if (!aligned16(qc) || !aligned16(kc) || (vc && !aligned16(vc)) || (o_coarse && !aligned16(o_coarse)) ||
-      !aligned16(scores))
+  if (!qc || !kc || !kv_block_idx || (o_coarse && (!vc || !lse_coarse))) return VSA_ERR_ARG;
+  if (!aligned16(qc) || !aligned16(kc) || (vc && !aligned16(vc)) || (o_coarse && !aligned16(o_coarse)))
     return VSA_ERR_ARG;
-  return launch_coarse_topk(qc, kc, vc, BH, Nc, d, topk, scale, o_coarse, lse_coarse, kv_block_idx,
+  if (!coarse_fits(Nc, d, topk, 1)) return VSA_ERR_UNSUPPORTED;
+  return launch_coarse_topk(qc, kc, vc, BH, Nc, d, topk, scale, 1, o_coarse, lse_coarse, kv_block_idx,
                             valid_block_num, scores, as_stream(stream));
 }
 
@@ -408,10 +407,10 @@ size_t vsa_workspace_bytes(int op, int B, int heads, int d, vsa_grid_t g, int to
   Dims D;
   if (B <= 0 || heads <= 0) return 0;
   if (check_grid(g, d, &D, static_cast<int64_t>(B) * heads) != VSA_OK) return 0;
-  if (check_selection(D, topk, op == VSA_OP_FINE_BWD ? -1 : radius) != VSA_OK) return 0;
+  if (check_selection(D, topk, op == VSA_OP_FINE_BWD ? -1 : radius, op != VSA_OP_FINE_BWD) != VSA_OK) return 0;
   switch (op) {
     case VSA_OP_FORWARD: return fwd_layout(D, topk, radius).total;
-    case VSA_OP_BACKWARD: return bwd_layout(D).total;
+    case VSA_OP_BACKWARD: return bwd_layout(D, list_width(topk, radius, D.Nc)).total;
     case VSA_OP_FINE_BWD: return fine_bwd_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.N), topk);
     case VSA_OP_FORWARD_INFERENCE: return fwd_layout(D, topk, radius, false).total;
     default: return 0;
@@ -450,7 +449,7 @@ int vsa_backward_tile_pairs(const void* bwd_ws, int B, int heads, int d, vsa_gri
   int st = check_grid(g, d, &D, static_cast<int64_t>(B) * heads);
   if (st != VSA_OK) return st;
   if ((st = check_selection(D, topk, radius)) != VSA_OK) return st;
-  *key_pairs = at<int32_t>(bwd_ws, bwd_layout(D).kpairs);
+  *key_pairs = at<int32_t>(bwd_ws, bwd_layout(D, list_width(topk, radius, D.Nc)).kpairs);
   return VSA_OK;
 }
 
@@ -477,26 +476,10 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
   float* pooled[3] = {at<float>(ws, w.qc), at<float>(ws, w.kc), at<float>(ws, w.vc)};
   if ((st = launch_permute(src, dst, pooled, 3, BH, d, g.T, g.H, g.W, g.cube_order, 0, 1, s)) != VSA_OK) return st;
   if ((st = select_lists(pooled[0], pooled[1], pooled[2], D, g, topk, radius, scale, w, ws, s)) != VSA_OK) return st;
-  // O_c is needed only by the combine: it runs on the auxiliary stream beside
-  // the pair planning and the fine kernel, and joins before the combine.
-  AuxStream* aux = aux_stream();
-  std::unique_lock<std::mutex> fork_lock;
-  cudaStream_t s_oc = s;
-  if (aux) {
-    fork_lock = std::unique_lock<std::mutex>(aux->mu);
-    if (cudaEventRecord(aux->fork, s) != cudaSuccess || cudaStreamWaitEvent(aux->s, aux->fork, 0) != cudaSuccess)
-      return VSA_ERR_CUDA;
-    s_oc = aux->s;
-  }
-  if ((st = launch_coarse_oc(at<float>(ws, w.sc), at<float>(ws, w.lsec), pooled[2], BH, Nc, d, at<float>(ws, w.oc),
-                             s_oc)) != VSA_OK)
-    return st;
-  if (aux && cudaEventRecord(aux->join, s_oc) != cudaSuccess) return VSA_ERR_CUDA;
   // Pair query cubes whose lists overlap most into the fine kernels' tiles.
-  if ((st = launch_list_bits(at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), kmax, BH, Nc, at<uint32_t>(ws, w.lbits),
-                             s)) != VSA_OK)
+  if ((st = launch_pair_plan(at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), kmax, BH, Nc, at<int32_t>(ws, w.pairs),
+                              s)) != VSA_OK)
     return st;
-  if ((st = launch_pair_plan(at<uint32_t>(ws, w.lbits), BH, Nc, at<int32_t>(ws, w.pairs), s)) != VSA_OK) return st;
   // Padding slots of partial cubes are masked out of the keys.
   uint64_t* kmask = D.padded ? at<uint64_t>(ws, w.kmask) : nullptr;
   if (kmask && (st = launch_slot_masks(g.T, g.H, g.W, g.cube_order, kmask, s)) != VSA_OK) return st;
@@ -504,7 +487,6 @@ int vsa_forward(const void* q, const void* k, const void* v, const void* g_coars
                             scale, at<float>(ws, w.of), VSA_DTYPE_F32, at<float>(ws, w.lse), 1,
                             at<int32_t>(ws, w.pairs), kmask, s)) != VSA_OK)
     return st;
-  if (aux && cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess) return VSA_ERR_CUDA;
   return launch_combine(at<float>(ws, w.oc), at<float>(ws, w.of), g_coarse, g_fine, out, out_dtype, BH, d, g.T, g.H,
                         g.W, g.cube_order, s);
 }
@@ -533,32 +515,15 @@ int vsa_forward_inference(const void* q, const void* k, const void* v, const voi
   float* pooled[3] = {at<float>(ws, w.qc), at<float>(ws, w.kc), at<float>(ws, w.vc)};
   if ((st = launch_permute(src, none, pooled, 3, BH, d, g.T, g.H, g.W, g.cube_order, 0, 0, s)) != VSA_OK) return st;
   if ((st = select_lists(pooled[0], pooled[1], pooled[2], D, g, topk, radius, scale, w, ws, s)) != VSA_OK) return st;
-  // O_c is needed only by the combine: it runs on the auxiliary stream beside
-  // the pair planning and the fine kernel, and joins before the combine.
-  AuxStream* aux = aux_stream();
-  std::unique_lock<std::mutex> fork_lock;
-  cudaStream_t s_oc = s;
-  if (aux) {
-    fork_lock = std::unique_lock<std::mutex>(aux->mu);
-    if (cudaEventRecord(aux->fork, s) != cudaSuccess || cudaStreamWaitEvent(aux->s, aux->fork, 0) != cudaSuccess)
-      return VSA_ERR_CUDA;
-    s_oc = aux->s;
-  }
-  if ((st = launch_coarse_oc(at<float>(ws, w.sc), at<float>(ws, w.lsec), pooled[2], BH, Nc, d, at<float>(ws, w.oc),
-                             s_oc)) != VSA_OK)
+  if ((st = launch_pair_plan(at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), kmax, BH, Nc, at<int32_t>(ws, w.pairs),
+                              s)) != VSA_OK)
     return st;
-  if (aux && cudaEventRecord(aux->join, s_oc) != cudaSuccess) return VSA_ERR_CUDA;
-  if ((st = launch_list_bits(at<int32_t>(ws, w.idx), at<int32_t>(ws, w.cnt), kmax, BH, Nc, at<uint32_t>(ws, w.lbits),
-                             s)) != VSA_OK)
-    return st;
-  if ((st = launch_pair_plan(at<uint32_t>(ws, w.lbits), BH, Nc, at<int32_t>(ws, w.pairs), s)) != VSA_OK) return st;
   uint64_t* kmask = D.padded ? at<uint64_t>(ws, w.kmask) : nullptr;
   if (kmask && (st = launch_slot_masks(g.T, g.H, g.W, g.cube_order, kmask, s)) != VSA_OK) return st;
   if ((st = launch_fine_fwd_native(q, k, v, g.T, g.H, g.W, g.cube_order, at<int32_t>(ws, w.idx),
                                    at<int32_t>(ws, w.cnt), kmax, BH, d, scale, at<float>(ws, w.of), VSA_DTYPE_F32,
                                    at<float>(ws, w.lse), at<int32_t>(ws, w.pairs), kmask, s)) != VSA_OK)
     return st;
-  if (aux && cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess) return VSA_ERR_CUDA;
   return launch_combine(at<float>(ws, w.oc), at<float>(ws, w.of), g_coarse, g_fine, out, out_dtype, BH, d, g.T, g.H,
                         g.W, g.cube_order, s);
 }
@@ -577,7 +542,7 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
       (dg_fine && !aligned16(dg_fine)))
     return VSA_ERR_ARG;
   if (grad_dtype != VSA_DTYPE_BF16 && grad_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
-  BwdWs w = bwd_layout(D);
+  BwdWs w = bwd_layout(D, list_width(topk, radius, D.Nc));
   if (!ws || ws_bytes < w.total || !aligned16(ws)) return VSA_ERR_WORKSPACE;
   FwdWs f = fwd_layout(D, topk, radius);
   cudaStream_t s = as_stream(stream);
@@ -600,13 +565,12 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
   }
   if ((st = launch_bwd_prep(dout, g_coarse, g_fine, at<float>(fwd_ws, f.oc), at<float>(fwd_ws, f.of),
                             at<__half>(ws, w.dof), at<float>(ws, w.delta), at<float>(ws, w.doc),
-                            g_coarse ? dg_coarse : nullptr, g_fine ? dg_fine : nullptr, grad_dtype, BH, d, g.T, g.H,
-                            g.W, g.cube_order, s)) != VSA_OK)
+                            at<float>(ws, w.deltac), g_coarse ? dg_coarse : nullptr, g_fine ? dg_fine : nullptr,
+                            grad_dtype, BH, d, g.T, g.H, g.W, g.cube_order, s)) != VSA_OK)
     return st;
   if ((st = launch_coarse_bwd(at<float>(fwd_ws, f.qc), at<float>(fwd_ws, f.kc), at<float>(fwd_ws, f.vc),
-                              at<float>(ws, w.doc), at<float>(fwd_ws, f.lsec), BH, Nc, d, scale, at<float>(ws, w.P),
-                              at<float>(ws, w.dS), at<float>(ws, w.dqc), at<float>(ws, w.dkc), at<float>(ws, w.dvc),
-                              s)) != VSA_OK)
+                              at<float>(ws, w.doc), at<float>(fwd_ws, f.lsec), at<float>(ws, w.deltac), BH, Nc, d,
+                              scale, at<float>(ws, w.dqc), at<float>(ws, w.dkc), at<float>(ws, w.dvc), s)) != VSA_OK)
     return st;
   if (aux && cudaEventRecord(aux->mid, s) != cudaSuccess) return VSA_ERR_CUDA;
   FusedGrads fg{dq,
@@ -621,7 +585,7 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
   if ((st = launch_fine_bwd_core(at<void>(fwd_ws, f.qp), at<void>(fwd_ws, f.kp), at<void>(fwd_ws, f.vp),
                                  at<void>(ws, w.dof), at<float>(fwd_ws, f.lse), at<float>(ws, w.delta),
                                  at<int32_t>(fwd_ws, f.idx), at<int32_t>(fwd_ws, f.cnt), f.kmax, BH, N, d, scale,
-                                 nullptr, nullptr, nullptr, &fg, at<uint32_t>(ws, w.inv), at<int32_t>(fwd_ws, f.pairs),
+                                 nullptr, nullptr, nullptr, &fg, at<void>(ws, w.inv), at<int32_t>(fwd_ws, f.pairs),
                                  at<int32_t>(ws, w.kpairs), s, s_kv, aux ? aux->mid : nullptr)) != VSA_OK)
     return st;
   if (aux && (cudaEventRecord(aux->join, s_kv) != cudaSuccess || cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess))

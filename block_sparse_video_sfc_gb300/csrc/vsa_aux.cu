@@ -5,7 +5,9 @@
 //             combines the coarse and fine outputs through learnable gates).
 //   bwd_prep  backward of the combine: dO to cube order, dO_f = g_f * dO
 //             (fp16 for the fine backward), D = dO_f . O_f, dO_c = sum over the
-//             cube of g_c * dO, and the gate gradients.
+//             cube of g_c * dO, D_c = dO_c . O_c (the coarse backward's row
+//             statistic: sum_j P_j dP_j = dO_c . sum_j P_j V_j), and the gate
+//             gradients.
 // (The mean-pool backward and the inverse reordering of dQ, dK, dV run in
 // the epilogues of the fine backward kernels.)
 // The backward pass follows "VSA: Faster Video Diffusion with Trainable Sparse
@@ -55,11 +57,13 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        const __nv_bfloat16* __restrict__ gf,
                                                        const float* __restrict__ oc, const float* __restrict__ of,
                                                        __half* __restrict__ dof, float* __restrict__ delta,
-                                                       float* __restrict__ doc, void* __restrict__ dgc,
+                                                       float* __restrict__ doc, float* __restrict__ delta_c,
+                                                       void* __restrict__ dgc,
                                                        void* __restrict__ dgf, int grad_dtype, int Nc, CubeGrid grid,
                                                        int64_t Nn, const int32_t* __restrict__ order, int* err) {
   constexpr int kChunks = D / 8, kTok = 256 / kChunks, kPasses = kCube / kTok;
   __shared__ float red[kTok][D];
+  __shared__ float dcw[D / 32];
   const int64_t cg = blockIdx.x;
   const int64_t bh = cg / Nc;
   const int cube = static_cast<int>(cg % Nc);
@@ -115,10 +119,24 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[o0][j * 8 + e] = acc[e];
   __syncthreads();
+  float dprod = 0.f;
   for (int ch = threadIdx.x; ch < D; ch += 256) {
     float s = 0.f;
     for (int r = 0; r < kTok; ++r) s += red[r][ch];
     doc[cg * D + ch] = s;
+    dprod = s * oc[cg * D + ch];
+  }
+  if (delta_c) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dprod += __shfl_xor_sync(0xffffffffu, dprod, off);
+    if (threadIdx.x < D && (threadIdx.x & 31) == 0) dcw[threadIdx.x >> 5] = dprod;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < D / 32; ++w) t += dcw[w];
+      delta_c[cg] = t;
+    }
   }
 }
 
@@ -142,8 +160,8 @@ int launch_combine(const float* oc, const float* of, const void* gc, const void*
 }
 
 int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const float* oc, const float* of,
-                    __half* dof, float* delta, float* doc, void* dgc, void* dgf, int grad_dtype, int BH, int d,
-                    int T, int H, int W, const int32_t* order, cudaStream_t s) {
+                    __half* dof, float* delta, float* doc, float* delta_c, void* dgc, void* dgf, int grad_dtype,
+                    int BH, int d, int T, int H, int W, const int32_t* order, cudaStream_t s) {
   const CubeGrid cg = cube_grid(T, H, W);
   const int Nc = ((T + 3) / 4) * cg.Hc * cg.Wc;
   const int64_t Nn = static_cast<int64_t>(T) * H * W;
@@ -153,11 +171,11 @@ int launch_bwd_prep(const void* dout, const void* gc, const void* gf, const floa
   auto f = static_cast<const __nv_bfloat16*>(gf);
   timing_mark(VSA_K_BWD_PREP, true, s);
   if (d == 128)
-    bwd_prep_kernel<128><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, cg, Nn, order,
-                                              device_error_word());
+    bwd_prep_kernel<128><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, delta_c, dgc, dgf, grad_dtype, Nc,
+                                              cg, Nn, order, device_error_word());
   else
-    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, dgc, dgf, grad_dtype, Nc, cg, Nn, order,
-                                             device_error_word());
+    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(dO, g, f, oc, of, dof, delta, doc, delta_c, dgc, dgf, grad_dtype, Nc,
+                                             cg, Nn, order, device_error_word());
   timing_mark(VSA_K_BWD_PREP, false, s);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }

@@ -35,7 +35,9 @@
  *    cubes each query cube attends to; valid_block_num int32 [BH, Nc] holds how
  *    many entries of each row are used (0 <= count <= max_kv_blocks).
  *    vsa_coarse_topk writes rows in descending coarse score, ties to the lower
- *    cube id.  Entries are used as given (a repeated cube counts twice).
+ *    cube id; vsa_forward saves the same sets in ascending cube id (the fine
+ *    kernels walk a row as a set, so its order changes no result).  Entries
+ *    are used as given (a repeated cube counts twice).
  *  - Output dtype selectors take VSA_DTYPE_BF16 or VSA_DTYPE_F32.
  *  - Return value: VSA_OK, or a negative vsa_status_t.  Argument and shape
  *    errors are found on the host before anything is enqueued.  Errors found
@@ -141,12 +143,14 @@ int vsa_permute(const void* x, void* y, float* pooled, int BH, int d, vsa_grid_t
  *               only when o_coarse is NULL.
  *   kv_block_idx    int32 [BH, Nc, topk]: selected key cubes, highest first.
  *   valid_block_num int32 [BH, Nc] or NULL: set to topk.
- *   scores      fp32 [BH, Nc, Nc], 16-byte aligned, required: receives the
- *               scaled coarse scores, which the selection and O_c read back
- *               (the caller's scratch; the library allocates nothing).
- * The score matrix comes from one tiled fp32 product, the selection and the
- * log-sum-exp from one warp per row, and O_c from a second product that
- * applies the row softmax as it loads the scores.
+ *   scores      fp32 [BH, Nc, Nc] or NULL: receives the scaled coarse scores
+ *               too (for inspection; the computation does not need it).
+ * No Nc x Nc matrix is needed: a CTA keeps the score rows of 16 query cubes
+ * in shared memory while Kc streams through, takes each row's log-sum-exp
+ * and Top-K there (one warp per row: radix selection, then the picks ranked),
+ * and streams Vc through for O_c.  Limit (the rows must fit the 227 KB of
+ * shared memory): Nc <= 2304 for d = 128, Nc <= 2944 for d = 64, else
+ * VSA_ERR_UNSUPPORTED; vsa_forward has the same limit.
  */
 int vsa_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, int Nc, int d, int topk,
                     float scale, float* o_coarse, float* lse_coarse, int32_t* kv_block_idx,
@@ -227,8 +231,8 @@ int vsa_fine_bwd_noalloc(const void* qp, const void* kp, const void* vp, const v
  *   q, k, v     bf16 [B, heads, N, d] native order.
  *   g_coarse, g_fine  bf16 [B, heads, N, d] native order, or NULL (= ones).
  *   topk        1 <= topk <= Nc: the Top-K of each coarse score row.
- *   radius      -1: the selection is the Top-K alone (rows in descending
- *               score).  0..7: the Top-K united with every cube whose (t, h,
+ *   radius      -1: the selection is the Top-K alone (rows in ascending
+ *               cube id).  0..7: the Top-K united with every cube whose (t, h,
  *               w) cube coordinates each differ from the query cube's by at
  *               most radius (the query cube included) -- [AMD] "Comparison
  *               with Jenga", "Algorithmic Design": block selection as the union

@@ -62,7 +62,26 @@ def test_workspace_bytes(lib):
     assert with_r1 > fwd and (with_r1 - fwd) >= 12 * Nc * (154 + 27) * 4 - 12 * Nc * 154 * 4
     assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 154, 8) == 0
     assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 154, -2) == 0
-    assert L.vsa_workspace_bytes(lib.VSA_OP_BACKWARD, 1, 12, 128, g, 154, 1) == bwd
+    # the backward's inverse lists (CSR) hold one id per listed (query, key) cube pair
+    assert L.vsa_workspace_bytes(lib.VSA_OP_BACKWARD, 1, 12, 128, g, 154, 1) - bwd == 12 * Nc * 27 * 4
+
+
+def test_workspaces_hold_no_cube_by_cube_matrix(lib):
+    """The long video (24 heads, 1920 cubes, Top-K 192): the workspaces grow
+    with the tokens and the listed cubes, not with Nc x Nc (one fp32 [BH, Nc,
+    Nc] matrix alone would be 354 MB)."""
+    L = lib.load()
+    g = lib.Grid.of(32, 48, 80)
+    BH, N, Nc, K, d = 24, 122880, 1920, 192, 128
+    fwd = L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, BH, d, g, K, -1)
+    bwd = L.vsa_workspace_bytes(lib.VSA_OP_BACKWARD, 1, BH, d, g, K, -1)
+    per_token_fwd = BH * N * (3 * d * 2 + d * 4 + 4)        # fp16 Q/K/V copies, fp32 O_f, the LSE
+    plan = 4 + 32 * 2 + 8                                   # pair plan, its window overlaps, slot mask
+    per_cube = BH * Nc * (4 * d * 4 + 4 + K * 4 + 4 + plan)  # pooled Q/K/V, O_c, LSE_c, lists, counts
+    assert fwd < per_token_fwd + per_cube + (1 << 20)
+    per_token_bwd = BH * N * (d * 2 + 4)                    # fp16 dO_f, D
+    per_cube_bwd = BH * Nc * (4 * d * 4 + 4 + (K + 2) * 4 + 4 + plan)  # dO_c, dX_c, D_c, CSR
+    assert bwd < per_token_bwd + per_cube_bwd + (1 << 20)   # 1 MB of slack against 354 MB per matrix
 
 
 def test_host_side_argument_errors(lib):

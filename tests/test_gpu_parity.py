@@ -195,6 +195,11 @@ def _gpu_lists(vsa, oracle_mod, wl, saved, scores_by_head, radius, curve="raster
     if radius < 0:
         tk = idx
         assert np.all(cnt == wl.topk)
+        # saved in ascending cube id: the sets the public (highest-first)
+        # selection gives on the saved pooled vectors
+        assert np.all(np.diff(idx, axis=-1) > 0)
+        r = vsa.coarse_topk(saved["qc"], saved["kc"], saved["vc"], wl.topk, want_oc=False)
+        np.testing.assert_array_equal(idx, np.sort(r["idx"].view(wl.heads, wl.Nc, wl.topk).cpu().numpy(), -1))
     else:
         r = vsa.coarse_topk(saved["qc"], saved["kc"], saved["vc"], wl.topk, want_oc=False)
         tk = r["idx"].view(wl.heads, wl.Nc, wl.topk).cpu().numpy()
