@@ -134,6 +134,17 @@ def fine_bwd_wall(per_kernel: dict) -> tuple:
     return ms, overlapped
 
 
+def public_calls(public, per_kernel: dict, bwd_ms: float, overlapped: bool):
+    """The public calls' times beside the fine stage inside the whole pass:
+    vsa_fine_fwd against the fine forward kernel, vsa_fine_bwd against the
+    fine backward's wall time (without the coarse backward)."""
+    if not public:
+        return None
+    inner = {"fine_fwd": per_kernel["fine_fwd"],
+             "fine_bwd": bwd_ms - per_kernel["coarse_bwd"] if overlapped else bwd_ms}
+    return {n: dict(v, internal_ms=round(inner[n], 4), ratio=round(v["ms"] / inner[n], 3)) for n, v in public.items()}
+
+
 def config_of(wl: synth.Workload, parallelism: str, curve: str = "raster", radius: int = -1) -> dict:
     return {
         "workload": (f"{wl.name}: B={wl.B}, heads={wl.heads}, d={wl.d}, grid (T,H,W)=({wl.T},{wl.H},{wl.W}) = "
@@ -453,6 +464,40 @@ def run_ours(args, rank: int, world: int):
         assert vsa.device_status() == 0, "device error flag set in the forward-only runs"
         del iws
 
+    # ---- the public single-stage calls, vsa_fine_fwd and vsa_fine_bwd with
+    # their workspaces, on the layer's inputs in cube order and the lists the
+    # forward selected; compared with the same kernels inside vsa_forward /
+    # vsa_backward.  Reported beside the headline; not part of it.
+    public = None
+    if world == 1 and not args.no_forward_only:
+        _, st = vsa.forward(dq_, dk_, dv_, wl.T, wl.H, wl.W, wl.topk, g_coarse=dgc_, g_fine=dgf_, out=out, ws=fws,
+                            cube_order=order, radius=args.radius)
+        sv = st.saved()
+        lists = (sv["idx"], sv["cnt"])
+        qp, kp, vp, dop = (vsa.permute(t, wl.T, wl.H, wl.W, cube_order=order).view(wl.BH, -1, wl.d)
+                           for t in (dq_, dk_, dv_, ddo))
+        fres = {}
+
+        def pub_fwd():
+            fres["of"], fres["lse"] = vsa.fine_fwd(qp, kp, vp, *lists)
+
+        def pub_bwd():
+            vsa.fine_bwd(qp, kp, vp, fres["of"], fres["lse"], dop, *lists)
+
+        public = {}
+        for name, fn in (("fine_fwd", pub_fwd), ("fine_bwd", pub_bwd)):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            public[name] = {"ms": round(e0.elapsed_time(e1) / args.steps, 4)}
+        assert vsa.device_status() == 0, "device error flag set in the public-call runs"
+        del qp, kp, vp, dop, fres
+
     # ---- end to end through the public API with host buffers.  Every step
     # copies its six inputs from pinned host memory and its six results back;
     # the copies run on two copy streams, double-buffered, so that step i+1's
@@ -559,6 +604,7 @@ def run_ours(args, rank: int, world: int):
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "kernel_launches_timed": launches,
         "forward_only": fwd_only,
+        "public_calls": public_calls(public, per_kernel, bwd_ms, overlapped),
         "clocks": csum,
         "e2e": e2e,
     }

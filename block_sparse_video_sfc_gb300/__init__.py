@@ -124,15 +124,22 @@ def lut_add_neighbors(idx, cnt, T: int, H: int, W: int, radius: int, max_kv_bloc
     return out, ocnt
 
 
-def fine_fwd(qp, kp, vp, idx, cnt, scale: Optional[float] = None, out_dtype=torch.float32):
-    """vsa_fine_fwd on cube-ordered bf16 tensors -> (O_f, lse)."""
+def fine_fwd(qp, kp, vp, idx, cnt, scale: Optional[float] = None, out_dtype=torch.float32, workspace: bool = True):
+    """vsa_fine_fwd on cube-ordered bf16 tensors -> (O_f, lse).  workspace:
+    give the call its workspace (fp16 copies and the overlap pair plan);
+    False runs the allocation-free form."""
     BH, N, d = _bhnd(qp)
     scale = d ** -0.5 if scale is None else scale
     of = torch.empty(qp.shape, dtype=out_dtype, device=qp.device)
     lse = torch.empty(qp.shape[:-1], dtype=torch.float32, device=qp.device)
+    kmax = idx.shape[-1] if idx is not None else 0
+    nbytes = 0
+    if workspace and N % 64 == 0:
+        nbytes = workspace_bytes(_lib.VSA_OP_FINE_FWD, 1, BH, d, 4, 4, N // 16, max(kmax, 1))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=qp.device) if nbytes else None
     _lib.check("vsa_fine_fwd", _lib.load().vsa_fine_fwd(
-        _ptr(qp), _ptr(kp), _ptr(vp), _ptr(idx), _ptr(cnt), idx.shape[-1], BH, N, d, float(scale),
-        _ptr(of), _DT[out_dtype], _ptr(lse), _stream()))
+        _ptr(qp), _ptr(kp), _ptr(vp), _ptr(idx), _ptr(cnt), kmax, BH, N, d, float(scale),
+        _ptr(of), _DT[out_dtype], _ptr(lse), _ptr(ws), nbytes, _stream()))
     return of, lse
 
 

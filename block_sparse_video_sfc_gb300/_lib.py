@@ -28,6 +28,7 @@ VSA_OP_FORWARD = 0
 VSA_OP_BACKWARD = 1
 VSA_OP_FINE_BWD = 2
 VSA_OP_FORWARD_INFERENCE = 3
+VSA_OP_FINE_FWD = 4
 VSA_CURVE_RASTER = 0
 VSA_CURVE_HILBERT = 1
 VSA_NOALLOC_SCRATCH_BYTES = 64 << 20   # the fixed scratch array of vsa_fine_bwd_noalloc
@@ -62,7 +63,7 @@ SIGNATURES = {
     "vsa_permute": ([P, P, P, I, I, Grid, I, P], I),
     "vsa_cube_order": ([Grid, I, P, P], I),
     "vsa_coarse_topk": ([P, P, P, I, I, I, I, F, P, P, P, P, P, P], I),
-    "vsa_fine_fwd": ([P, P, P, P, P, I, I, I, I, F, P, I, P, P], I),
+    "vsa_fine_fwd": ([P, P, P, P, P, I, I, I, I, F, P, I, P, P, SZ, P], I),
     "vsa_fine_bwd": ([P, P, P, P, I, P, P, P, P, I, I, I, I, F, P, P, P, P, SZ, P], I),
     "vsa_fine_bwd_noalloc": ([P, P, P, P, I, P, P, P, P, I, I, I, I, F, P, P, P, P], I),
     "vsa_forward": ([P, P, P, P, P, I, I, I, Grid, I, I, F, P, I, P, SZ, P], I),

@@ -167,10 +167,19 @@ struct FusedGrads {
   CubeGrid grid;
   const int32_t* order;  // cube order table, or null (raster)
 };
+// bf16 -> fp16 copies of n (1..4) tensors of elems elements each (elems % 8
+// == 0, 16-byte aligned), one launch; out-of-range values latch kErrRange.
+int launch_to_f16(const void* const* src, void* const* dst, int n, int64_t elems, cudaStream_t s);
+// Workspace of the public fine forward: fp16 copies of Q, K, V and the
+// query-cube pair plan.
+size_t fine_fwd_ws_bytes(int BH, int N, int d);
+// The public fine backward.  s_kv: the stream of the dK/dV chain (may be s);
+// ready: an event recorded on s once the fp16 copies exist, which the dK/dV
+// kernel waits for (null when s_kv is s).
 int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* of, int of_dtype,
                     const float* lse, const void* dof, const int32_t* idx, const int32_t* cnt, int kmax, int BH,
                     int N, int d, float scale, float* dq, float* dk, float* dv, void* ws, size_t ws_bytes,
-                    cudaStream_t s);
+                    cudaStream_t s, cudaStream_t s_kv, cudaEvent_t ready);
 // kv_after: an event the dK/dV kernel waits for on s_kv (its inverse lists
 // and plan do not), or null.
 int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const void* dof, const float* lse,

@@ -925,9 +925,15 @@ __global__ void delta_kernel(const void* __restrict__ of, int of_dtype, const __
   if (lane == 0) delta[row] = s;
 }
 
-// bf16 -> fp16 copy (exact within the fp16 range; larger values saturate and
-// latch kErrRange).  n8 = number of 8-element groups.
-__global__ void to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n8, int* err) {
+// bf16 -> fp16 copies (exact within the fp16 range; larger values saturate
+// and latch kErrRange): tensor blockIdx.y, n8 = its 8-element groups.
+struct F16Copies {
+  const uint4* src[4];
+  uint4* dst[4];
+};
+__global__ void to_f16_kernel(F16Copies c, int64_t n8, int* err) {
+  const uint4* __restrict__ src = c.src[blockIdx.y];
+  uint4* __restrict__ dst = c.dst[blockIdx.y];
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     uint4 v = src[i];
@@ -969,14 +975,28 @@ int launch_inverse_lists(const int32_t* idx, const int32_t* cnt, int kmax, int B
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
+int launch_to_f16(const void* const* src, void* const* dst, int n, int64_t elems, cudaStream_t s) {
+  if (n < 1 || n > 4 || elems % 8) return VSA_ERR_ARG;
+  F16Copies c{};
+  for (int i = 0; i < n; ++i) {
+    c.src[i] = static_cast<const uint4*>(src[i]);
+    c.dst[i] = static_cast<uint4*>(dst[i]);
+  }
+  const int64_t n8 = elems / 8, nblk = (n8 + 255) / 256;
+  // Enough CTAs to cover the SMs several times over; each strides the rest.
+  const unsigned gx = static_cast<unsigned>(nblk < 4096 ? (nblk > 0 ? nblk : 1) : 4096);
+  to_f16_kernel<<<dim3(gx, n), 256, 0, s>>>(c, n8, device_error_word());
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
 size_t fine_bwd_ws_bytes(int BH, int N, int kmax) {
   const int64_t Nc = N / kCube;
   size_t inv = inverse_lists_bytes(BH, static_cast<int>(Nc), kmax);
   size_t delta = sizeof(float) * static_cast<size_t>(BH) * N;
   size_t copy = sizeof(__half) * static_cast<size_t>(BH) * N * 128;  // room for d <= 128
-  size_t kpairs = pair_plan_ws_bytes(BH, static_cast<int>(Nc));
+  size_t plan = pair_plan_ws_bytes(BH, static_cast<int>(Nc));
   return ((inv + 255) & ~size_t(255)) + ((delta + 255) & ~size_t(255)) + 4 * ((copy + 255) & ~size_t(255)) +
-         ((kpairs + 255) & ~size_t(255));
+         2 * ((plan + 255) & ~size_t(255));
 }
 
 int launch_delta(const void* of, int of_dtype, const void* dof, int64_t rows, int d, float* delta, cudaStream_t s) {
@@ -1029,7 +1049,13 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   p.qpairs = qpairs;
   p.kpairs = kpairs_ws;
   if ((st = launch_inverse_lists(idx, cnt, kmax, BH, Nc, inv_ws, &p.inv, s_kv)) != VSA_OK) return st;
-  if (kpairs_ws && (st = launch_pair_plan_inverse(p.inv, BH, Nc, kpairs_ws, s_kv)) != VSA_OK) return st;
+  if (kpairs_ws) {
+    st = launch_pair_plan_inverse(p.inv, BH, Nc, kpairs_ws, s_kv);
+    if (st == VSA_ERR_UNSUPPORTED)
+      p.kpairs = nullptr;  // too many cubes for the planner's shared memory: cubes 2t, 2t + 1
+    else if (st != VSA_OK)
+      return st;
+  }
   if (kv_after && cudaStreamWaitEvent(s_kv, kv_after, 0) != cudaSuccess) return VSA_ERR_CUDA;
   const size_t kv_extra = sizeof(uint32_t) * (2 * Nc + 2 + 2 * nwords) + 4 * sizeof(float) * d;
   const size_t dq_extra = sizeof(uint32_t) * (2 * kmax + 2 + 2 * nwords);
@@ -1056,10 +1082,13 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
-// Public fine backward: bf16 inputs are copied to fp16 in the workspace first.
+// Public fine backward: bf16 inputs are copied to fp16 in the workspace
+// first; the query cubes of the dQ kernel and the key cubes of the dK/dV
+// kernel are paired by list overlap, as in vsa_backward.
 int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* of, int of_dtype, const float* lse,
                     const void* dof, const int32_t* idx, const int32_t* cnt, int kmax, int BH, int N, int d,
-                    float scale, float* dq, float* dk, float* dv, void* ws, size_t ws_bytes, cudaStream_t s) {
+                    float scale, float* dq, float* dk, float* dv, void* ws, size_t ws_bytes, cudaStream_t s,
+                    cudaStream_t s_kv, cudaEvent_t ready) {
   if (!ws || ws_bytes < fine_bwd_ws_bytes(BH, N, kmax)) return VSA_ERR_WORKSPACE;
   const int64_t Nc = N / kCube, rows = static_cast<int64_t>(BH) * N;
   auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -1071,19 +1100,21 @@ int launch_fine_bwd(const void* qp, const void* kp, const void* vp, const void* 
   const size_t copy = a256(sizeof(__half) * static_cast<size_t>(rows) * 128);
   const void* srcs[4] = {qp, kp, vp, dof};
   void* h[4];
-  int* err = device_error_word();
-  for (int i = 0; i < 4; ++i, w += copy) {
-    h[i] = w;
-    const int64_t n8 = rows * d / 8;
-    const int64_t nblk = (n8 + 255) / 256;
-    to_f16_kernel<<<static_cast<unsigned>(nblk < 65535 ? nblk : 65535), 256, 0, s>>>(
-        static_cast<const uint4*>(srcs[i]), static_cast<uint4*>(h[i]), n8, err);
-  }
+  for (int i = 0; i < 4; ++i, w += copy) h[i] = w;
+  const size_t plan = a256(pair_plan_ws_bytes(BH, static_cast<int>(Nc)));
   int32_t* kpairs = reinterpret_cast<int32_t*>(w);
-  int st = launch_delta(of, of_dtype, h[3], rows, d, delta, s);
+  int32_t* qpairs = reinterpret_cast<int32_t*>(w + plan);
+  int st = launch_to_f16(srcs, h, 4, rows * d, s);
   if (st != VSA_OK) return st;
+  if ((st = launch_delta(of, of_dtype, h[3], rows, d, delta, s)) != VSA_OK) return st;
+  st = launch_pair_plan(idx, cnt, kmax, BH, static_cast<int>(Nc), qpairs, s);
+  if (st == VSA_ERR_UNSUPPORTED)
+    qpairs = nullptr;  // too many cubes for the planner's shared memory: cubes 2t, 2t + 1
+  else if (st != VSA_OK)
+    return st;
+  if (ready && cudaEventRecord(ready, s) != cudaSuccess) return VSA_ERR_CUDA;
   return launch_fine_bwd_core(h[0], h[1], h[2], h[3], lse, delta, idx, cnt, kmax, BH, N, d, scale, dq, dk, dv, nullptr,
-                              inv_ws, nullptr, kpairs, s, s, nullptr);
+                              inv_ws, qpairs, kpairs, s, s_kv, ready);
 }
 
 }  // namespace vsa

@@ -734,6 +734,11 @@ int launch_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_
   return run_fine_fwd(p, idx, cnt, kmax, BH, N, d, scale, of, of_dtype, lse, f16_in, false, pairs, kmask, s);
 }
 
+size_t fine_fwd_ws_bytes(int BH, int N, int d) {
+  auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+  return 3 * a256(sizeof(uint16_t) * static_cast<size_t>(BH) * N * d) + a256(pair_plan_ws_bytes(BH, N / kCube));
+}
+
 int launch_fine_fwd_native(const void* q, const void* k, const void* v, int T, int H, int W, const int32_t* order,
                            const int32_t* idx, const int32_t* cnt, int kmax, int BH, int d, float scale, void* of,
                            int of_dtype, float* lse, const int32_t* pairs, const uint64_t* kmask, cudaStream_t s) {

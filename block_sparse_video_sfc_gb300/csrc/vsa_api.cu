@@ -379,13 +379,30 @@ static int check_fine(const void* qp, const void* kp, const void* vp, const int3
 
 int vsa_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* kv_block_idx,
                  const int32_t* valid_block_num, int max_kv_blocks, int BH, int N, int d, float scale, void* o_fine,
-                 int o_dtype, float* lse, void* stream) {
+                 int o_dtype, float* lse, void* ws, size_t ws_bytes, void* stream) {
   int st = check_fine(qp, kp, vp, kv_block_idx, max_kv_blocks, BH, N, d);
   if (st != VSA_OK) return st;
   if (!o_fine || !aligned16(o_fine)) return VSA_ERR_ARG;
   if (o_dtype != VSA_DTYPE_BF16 && o_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
-  return launch_fine_fwd(qp, kp, vp, kv_block_idx, valid_block_num, max_kv_blocks, BH, N, d, scale, o_fine, o_dtype,
-                         lse, 0, nullptr, nullptr, as_stream(stream));
+  cudaStream_t s = as_stream(stream);
+  if (!ws)  // bf16 operands as given, V converted on chip, cubes 2t and 2t + 1 paired
+    return launch_fine_fwd(qp, kp, vp, kv_block_idx, valid_block_num, max_kv_blocks, BH, N, d, scale, o_fine,
+                           o_dtype, lse, 0, nullptr, nullptr, s);
+  if (ws_bytes < fine_fwd_ws_bytes(BH, N, d) || !aligned16(ws)) return VSA_ERR_WORKSPACE;
+  // fp16 copies of Q, K, V (one pass), the query cubes paired by list
+  // overlap, then the kernel vsa_forward runs.
+  const size_t copy = align256(sizeof(uint16_t) * static_cast<size_t>(BH) * N * d);
+  void* h[3] = {at<void>(ws, 0), at<void>(ws, copy), at<void>(ws, 2 * copy)};
+  const void* src[3] = {qp, kp, vp};
+  int32_t* pairs = at<int32_t>(ws, 3 * copy);
+  if ((st = launch_to_f16(src, h, 3, static_cast<int64_t>(BH) * N * d, s)) != VSA_OK) return st;
+  st = launch_pair_plan(kv_block_idx, valid_block_num, max_kv_blocks, BH, N / kCube, pairs, s);
+  if (st == VSA_ERR_UNSUPPORTED)
+    pairs = nullptr;  // too many cubes for the planner's shared memory: cubes 2t, 2t + 1
+  else if (st != VSA_OK)
+    return st;
+  return launch_fine_fwd(h[0], h[1], h[2], kv_block_idx, valid_block_num, max_kv_blocks, BH, N, d, scale, o_fine,
+                         o_dtype, lse, 1, pairs, nullptr, s);
 }
 
 int vsa_fine_bwd(const void* qp, const void* kp, const void* vp, const void* o_fine, int o_dtype, const float* lse,
@@ -399,19 +416,36 @@ int vsa_fine_bwd(const void* qp, const void* kp, const void* vp, const void* o_f
       !aligned16(dv))
     return VSA_ERR_ARG;
   if (o_dtype != VSA_DTYPE_BF16 && o_dtype != VSA_DTYPE_F32) return VSA_ERR_ARG;
-  return launch_fine_bwd(qp, kp, vp, o_fine, o_dtype, lse, do_fine, kv_block_idx, valid_block_num, max_kv_blocks,
-                         BH, N, d, scale, dq, dk, dv, ws, ws_bytes, as_stream(stream));
+  if (!ws || ws_bytes < fine_bwd_ws_bytes(BH, N, max_kv_blocks)) return VSA_ERR_WORKSPACE;
+  // As in vsa_backward: the dK/dV chain on the auxiliary stream, the dQ
+  // kernel on the caller's.
+  cudaStream_t s = as_stream(stream), s_kv = s;
+  AuxStream* aux = aux_stream();
+  std::unique_lock<std::mutex> fork_lock;
+  if (aux) {
+    fork_lock = std::unique_lock<std::mutex>(aux->mu);
+    if (cudaEventRecord(aux->fork, s) != cudaSuccess || cudaStreamWaitEvent(aux->s, aux->fork, 0) != cudaSuccess)
+      return VSA_ERR_CUDA;
+    s_kv = aux->s;
+  }
+  st = launch_fine_bwd(qp, kp, vp, o_fine, o_dtype, lse, do_fine, kv_block_idx, valid_block_num, max_kv_blocks, BH,
+                       N, d, scale, dq, dk, dv, ws, ws_bytes, s, s_kv, aux ? aux->mid : nullptr);
+  if (aux && (cudaEventRecord(aux->join, s_kv) != cudaSuccess || cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess))
+    return VSA_ERR_CUDA;
+  return st;
 }
 
 size_t vsa_workspace_bytes(int op, int B, int heads, int d, vsa_grid_t g, int topk, int radius) {
   Dims D;
   if (B <= 0 || heads <= 0) return 0;
   if (check_grid(g, d, &D, static_cast<int64_t>(B) * heads) != VSA_OK) return 0;
-  if (check_selection(D, topk, op == VSA_OP_FINE_BWD ? -1 : radius, op != VSA_OP_FINE_BWD) != VSA_OK) return 0;
+  const bool fine = op == VSA_OP_FINE_BWD || op == VSA_OP_FINE_FWD;
+  if (check_selection(D, topk, fine ? -1 : radius, !fine) != VSA_OK) return 0;
   switch (op) {
     case VSA_OP_FORWARD: return fwd_layout(D, topk, radius).total;
     case VSA_OP_BACKWARD: return bwd_layout(D, list_width(topk, radius, D.Nc)).total;
     case VSA_OP_FINE_BWD: return fine_bwd_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.N), topk);
+    case VSA_OP_FINE_FWD: return fine_fwd_ws_bytes(static_cast<int>(D.BH), static_cast<int>(D.N), d);
     case VSA_OP_FORWARD_INFERENCE: return fwd_layout(D, topk, radius, false).total;
     default: return 0;
   }

@@ -47,13 +47,14 @@
  *    and clears the flag.
  *  - Precision: the pooled vectors, coarse scores and Top-K are fp32; the
  *    fine-stage tensor-core products take 16-bit operands with fp32
- *    accumulation.  vsa_fine_fwd multiplies Q K^T in bf16 and P V in fp16 (V
- *    converted on chip); vsa_forward_inference both in bf16 (P rounded to
- *    bf16: it feeds no backward).  vsa_forward / vsa_backward / vsa_fine_bwd
- *    convert Q, K, V and
- *    dO_f = g_fine * dO to fp16 (exact for bf16 values of magnitude up to
- *    65504; 8x finer rounding of the probabilities and of dS than bf16).  An
- *    operand beyond 65504 is saturated and latches VSA_ERR_RANGE.
+ *    accumulation.  vsa_forward / vsa_backward / vsa_fine_bwd, and
+ *    vsa_fine_fwd given a workspace, convert Q, K, V and dO_f = g_fine * dO
+ *    to fp16 (exact for bf16 values of magnitude up to 65504; 8x finer
+ *    rounding of the probabilities and of dS than bf16).  An operand beyond
+ *    65504 is saturated and latches VSA_ERR_RANGE.  vsa_fine_fwd without a
+ *    workspace multiplies Q K^T in bf16 and P V in fp16 (V converted on
+ *    chip); vsa_forward_inference both in bf16 (P rounded to bf16: it feeds
+ *    no backward).
  */
 #ifndef VSA_H_
 #define VSA_H_
@@ -167,10 +168,18 @@ int vsa_coarse_topk(const float* qc, const float* kc, const float* vc, int BH, i
  *               are 0.
  *   lse         fp32 [BH, N] or NULL: natural-log sum-exp of each row
  *               (-inf for count 0).
+ *   ws          NULL, or a workspace of vsa_workspace_bytes(VSA_OP_FINE_FWD,
+ *               ...) bytes (16-byte aligned).  With it the call copies Q, K, V
+ *               to fp16 in one pass (as vsa_forward does: exact within
+ *               +-65504, VSA_ERR_RANGE beyond) and pairs the query cubes of
+ *               each 128-row tile by list overlap, then runs vsa_forward's
+ *               fine kernel.  Without it the call allocates nothing: Q K^T
+ *               takes the bf16 operands, V is converted on chip, and cubes
+ *               2t, 2t + 1 share a tile (slower).
  */
 int vsa_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* kv_block_idx,
                  const int32_t* valid_block_num, int max_kv_blocks, int BH, int N, int d, float scale,
-                 void* o_fine, int o_dtype, float* lse, void* stream);
+                 void* o_fine, int o_dtype, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * vsa_fine_bwd -- gradient of the fine stage.  [ABS] (VSA is trained end to
@@ -181,7 +190,14 @@ int vsa_fine_fwd(const void* qp, const void* kp, const void* vp, const int32_t* 
  *   do_fine     bf16 [BH, N, d]: dL/dO_f in cube order.
  *   Every pointer 16-byte aligned (VSA_ERR_ARG otherwise).
  *   dq, dk, dv  fp32 [BH, N, d] in cube order (overwritten).
- *   ws          workspace of vsa_workspace_bytes(VSA_OP_FINE_BWD, ...) bytes.
+ *   ws          workspace of vsa_workspace_bytes(VSA_OP_FINE_BWD, ...) bytes:
+ *               fp16 copies of Q, K, V, dO_f (one pass), the inverse lists,
+ *               and the query-cube and key-cube pair plans (the tiles of the
+ *               dQ and dK/dV kernels, paired by list overlap as in
+ *               vsa_backward).
+ * As in vsa_backward, the dK/dV kernel runs on the library's auxiliary
+ * stream, forked from `stream` and joined back to it before the call's work
+ * ends, beside the dQ kernel on `stream`.
  */
 int vsa_fine_bwd(const void* qp, const void* kp, const void* vp, const void* o_fine, int o_dtype,
                  const float* lse, const void* do_fine, const int32_t* kv_block_idx,
@@ -288,11 +304,18 @@ int vsa_backward(const void* fwd_ws, const void* g_coarse, const void* g_fine, c
                  int heads, int d, vsa_grid_t g, int topk, int radius, float scale, void* dq, void* dk, void* dv,
                  void* dg_coarse, void* dg_fine, int grad_dtype, void* ws, size_t ws_bytes, void* stream);
 
-enum { VSA_OP_FORWARD = 0, VSA_OP_BACKWARD = 1, VSA_OP_FINE_BWD = 2, VSA_OP_FORWARD_INFERENCE = 3 };
+enum {
+    VSA_OP_FORWARD = 0,
+    VSA_OP_BACKWARD = 1,
+    VSA_OP_FINE_BWD = 2,
+    VSA_OP_FORWARD_INFERENCE = 3,
+    VSA_OP_FINE_FWD = 4
+};
 
 /* Workspace bytes for an operation (0 on a bad argument); topk and radius as
- * in vsa_forward.  For VSA_OP_FINE_BWD, B*heads is BH, g/topk give N and
- * max_kv_blocks, and radius is ignored. */
+ * in vsa_forward.  For VSA_OP_FINE_FWD and VSA_OP_FINE_BWD, B*heads is BH,
+ * g gives N (its cube count times 64), topk is max_kv_blocks, and radius is
+ * ignored. */
 size_t vsa_workspace_bytes(int op, int B, int heads, int d, vsa_grid_t g, int topk, int radius);
 
 /* Device pointers into a forward workspace (the saved state), for callers

@@ -64,6 +64,19 @@ def test_workspace_bytes(lib):
     assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 12, 128, g, 154, -2) == 0
     # the backward's inverse lists (CSR) hold one id per listed (query, key) cube pair
     assert L.vsa_workspace_bytes(lib.VSA_OP_BACKWARD, 1, 12, 128, g, 154, 1) - bwd == 12 * Nc * 27 * 4
+    # the public fine forward: fp16 Q, K, V plus the pair plan (pairs, window overlaps); the fine
+    # backward: fp16 Q, K, V, dO_f, D, the inverse lists and two pair plans
+    plan = 12 * Nc // 2 * 8 + 12 * Nc * 32 * 2
+    ffwd = L.vsa_workspace_bytes(lib.VSA_OP_FINE_FWD, 1, 12, 128, g, 154, -1)
+    assert 12 * N * 128 * 2 * 3 + plan <= ffwd < 12 * N * 128 * 2 * 3 + plan + 4096
+    fbwd = L.vsa_workspace_bytes(lib.VSA_OP_FINE_BWD, 1, 12, 128, g, 154, -1)
+    assert 12 * N * (128 * 2 * 4 + 4) + 12 * Nc * 154 * 4 + 2 * plan <= fbwd
+    # the coarse rows must fit on chip: Nc = 2400 cubes is too many at d = 128, not at d = 64;
+    # the fine calls have no such limit
+    big = lib.Grid.of(4, 4 * 48, 4 * 50)
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 1, 128, big, 16, -1) == 0
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FORWARD, 1, 1, 64, big, 16, -1) > 0
+    assert L.vsa_workspace_bytes(lib.VSA_OP_FINE_FWD, 1, 1, 128, big, 16, -1) > 0
 
 
 def test_workspaces_hold_no_cube_by_cube_matrix(lib):
@@ -106,9 +119,14 @@ def test_host_side_argument_errors(lib):
                                  None) == lib.VSA_ERR_ARG
     # fine: N not a multiple of 64
     assert L.vsa_fine_fwd(fake, fake, fake, fake2, None, 2, 1, 100, 64, 0.125, fake2, 1, None,
-                          None) == lib.VSA_ERR_SHAPE
+                          None, 0, None) == lib.VSA_ERR_SHAPE
     assert L.vsa_fine_fwd(fake, fake, fake, fake2, None, 2, 1, 128, 64, 0.125, fake2, 7, None,
-                          None) == lib.VSA_ERR_ARG
+                          None, 0, None) == lib.VSA_ERR_ARG
+    # fine forward given a workspace: too small, or misaligned
+    assert L.vsa_fine_fwd(fake, fake, fake, fake2, None, 2, 1, 128, 64, 0.125, fake2, 1, None,
+                          fake2, 16, None) == lib.VSA_ERR_WORKSPACE
+    assert L.vsa_fine_fwd(fake, fake, fake, fake2, None, 2, 1, 128, 64, 0.125, fake2, 1, None,
+                          ctypes.c_void_p(0x2008), 1 << 30, None) == lib.VSA_ERR_WORKSPACE
     # forward: workspace too small
     assert L.vsa_forward(fake, fake, fake, None, None, 1, 2, 64, g, 2, -1, 0.125, fake2, 0, fake2, 16,
                          None) == lib.VSA_ERR_WORKSPACE

@@ -105,7 +105,10 @@ def _fine_case(oracle_mod, wl, heads=None):
 
 @pytest.mark.parametrize("name", ["tiny", "tiny_dense", "small"])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-def test_fine_fwd(vsa, oracle_mod, name, out_dtype):
+@pytest.mark.parametrize("workspace", [True, False])
+def test_fine_fwd(vsa, oracle_mod, name, out_dtype, workspace):
+    """vsa_fine_fwd with a workspace (fp16 copies, overlap pair plan) and
+    without one (bf16 operands, V converted on chip)."""
     wl = synth.WORKLOADS[name]
     qp, kp, vp = _fine_case(oracle_mod, wl)
     rng = np.random.default_rng(1)
@@ -113,20 +116,22 @@ def test_fine_fwd(vsa, oracle_mod, name, out_dtype):
                     for _ in range(wl.BH)]).astype(np.int32)
     cnt = np.full(idx.shape[:-1], wl.topk, np.int32)
     of, lse = vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), dev(cnt, torch.int32),
-                           out_dtype=out_dtype)
+                           out_dtype=out_dtype, workspace=workspace)
     status_ok(vsa)
     rof, rlse = oracle_mod.fine_fwd(qp, kp, vp, idx, cnt, wl.d ** -0.5)
     assert_close(host(of), rof, bf16_out=out_dtype == torch.bfloat16, what="O_f")
     assert_close(host(lse), rlse, max_abs=LSE_MAX_ABS, mean_abs=LSE_MEAN_ABS, what="lse")
 
 
-def test_fine_fwd_ragged_and_edge_lists(vsa, oracle_mod):
+@pytest.mark.parametrize("workspace", [True, False])
+def test_fine_fwd_ragged_and_edge_lists(vsa, oracle_mod, workspace):
     """Counts 0 / 1 / odd / K, K = 1 and an odd number of cubes (lone last pair)."""
     wl = synth.Workload("odd", 1, 3, 128, 4, 4, 20, 3)   # Nc = 5 cubes (odd)
     qp, kp, vp = _fine_case(oracle_mod, wl)
     idx = np.array([[[4, 0, 2], [1, 3, 0], [0, 1, 2], [2, 4, 3], [3, 2, 1]]] * 3, dtype=np.int32)
     cnt = np.array([[3, 0, 1, 2, 3], [0, 0, 0, 0, 1], [1, 1, 1, 1, 1]], dtype=np.int32)
-    of, lse = vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), dev(cnt, torch.int32))
+    of, lse = vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), dev(cnt, torch.int32),
+                           workspace=workspace)
     status_ok(vsa)
     rof, rlse = oracle_mod.fine_fwd(qp, kp, vp, idx, cnt, wl.d ** -0.5)
     assert_close(host(of), rof, what="O_f ragged")
@@ -146,19 +151,20 @@ def test_fine_fwd_dense_is_sdpa(vsa, oracle_mod):
     assert_close(host(of), ref, what="dense")
 
 
-def test_lut_errors_are_reported(vsa, oracle_mod):
+@pytest.mark.parametrize("workspace", [True, False])
+def test_lut_errors_are_reported(vsa, oracle_mod, workspace):
     wl = synth.WORKLOADS["tiny"]
     qp, kp, vp = _fine_case(oracle_mod, wl)
     idx = np.zeros((wl.BH, wl.Nc, 2), np.int32)
     idx[..., 1] = 1
     idx[0, 1, 1] = 7            # out of range
-    of, _ = vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), None)
+    of, _ = vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), None, workspace=workspace)
     assert vsa.device_status() == -6
     idx[0, 1, 1] = 0            # repeated cube in a row
-    vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), None)
+    vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), None, workspace=workspace)
     assert vsa.device_status() == -6
     idx[0, 1, 1] = 1
-    vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), None)
+    vsa.fine_fwd(dev(qp), dev(kp), dev(vp), dev(idx, torch.int32), None, workspace=workspace)
     assert vsa.device_status() == 0
 
 
