@@ -649,21 +649,23 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
       load_cube_pair<D>(sm + L::kQ, &p.tq, &bar_qdo, row_base, qa, cq1);
       load_cube_pair<D>(sm + L::kDO, &p.tdo, &bar_qdo, row_base, qa, cq1);
       // K(j) goes into stage j % 3 once dQ(j - 3) is done; V(j) into the V
-      // stage once dP(j - 1) is.  K runs one step ahead: K(j + 1), then V(j).
+      // stage once dP(j - 1) is.  V(j) is needed first (dP(j) follows S(j)),
+      // so it goes out before K(j + 1), and the waits spin: a suspended wait
+      // wakes hundreds of cycles late, all of it on dP(j)'s path.
       auto load_k = [&](int j) -> bool {
         const int s = j % kDqKStages;
-        if (j >= kDqKStages && !mbar_wait(&bar_kvfree[s], ((j / kDqKStages) - 1) & 1)) return false;
+        if (j >= kDqKStages && !mbar_spin(&bar_kvfree[s], ((j / kDqKStages) - 1) & 1)) return false;
         mbar_expect_tx(&bar_k[s], L::kTile);
         load_cube_pair<D>(sm + L::kK + s * L::kTile, &p.tk, &bar_k[s], row_base, kcube(j, 0), kcube(j, 1));
         return true;
       };
       bool ok = load_k(0);
       for (int j = 0; ok && j < steps; ++j) {
-        if (j + 1 < steps) ok = load_k(j + 1);
-        if (ok && j >= 1 && !mbar_wait(&bar_vfree, (j - 1) & 1)) ok = false;
+        if (j >= 1 && !mbar_spin(&bar_vfree, (j - 1) & 1)) ok = false;
         if (!ok) break;
         mbar_expect_tx(&bar_v, L::kTile);
         load_cube_pair<D>(sm + L::kV, &p.tv, &bar_v, row_base, kcube(j, 0), kcube(j, 1));
+        if (j + 1 < steps) ok = load_k(j + 1);
       }
       if (!ok) flag_error(p.err, kErrTimeout);
     }
