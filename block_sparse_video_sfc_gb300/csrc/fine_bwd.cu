@@ -60,9 +60,11 @@ namespace {
 
 constexpr int kThreads = 320;  // producer, MMA issuer, 2 compute warpgroups
 constexpr int kCompute = 256;
+constexpr int kDqThreads = 352;  // the dQ kernel adds a second MMA issuer (warp 10)
 
 struct BwdParams {
   CUtensorMap tq, tk, tv, tdo;  // fp16 [BH*N, d], box {64, 64}, 128B swizzle
+  const uint16_t* dof;          // the same dO_f rows (fp16), read directly into TMEM by the dQ kernel
   const float* lse;             // natural-log LSE per row [BH*N]
   const float* delta;           // D per row [BH*N]
   InverseLists inv;             // CSR inverse lists
@@ -544,19 +546,20 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
 template <int D>
 struct DqLayout {
   static constexpr int kTile = 128 * D * 2;
-  // K: 3 stages (read by S(j) and, much later, by dQ(j)); V: 1 stage (read
-  // by dP(j) only, so V(j+1) can land while S(j+1) runs).
-  static constexpr int kQ = 0, kDO = kTile, kK = 2 * kTile, kV = 5 * kTile;
+  // K: 3 stages (read by S(j) and, much later, by dQ(j)); V: 2 stages (read
+  // by dP(j) only, so V(j + 1) lands while step j runs).  dO is not here: it
+  // is the A operand of dP from TMEM.
+  static constexpr int kQ = 0, kK = kTile, kV = 4 * kTile;
   static constexpr int kEnd = 6 * kTile;
 };
-constexpr int kDqKStages = 3;
+constexpr int kDqKStages = 3, kDqVStages = 2;
 // TMEM: S 0 and dP 128 (128 fp32 columns each, released once the compute
-// warps have read them); dS buffer b at 256 + 64 b (64 columns of fp16
-// pairs); dQ 384.
-constexpr uint32_t kDqS = 0, kDqDP = 128, kDqDS = 256, kDqDQ = 384;
+// warps have read them); dS 256 (64 columns of fp16 pairs); dO 320 (D / 2
+// columns of fp16 pairs, written once); dQ 384.
+constexpr uint32_t kDqS = 0, kDqDP = 128, kDqDS = 256, kDqDO = 320, kDqDQ = 384;
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kDqThreads, 1) fine_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using L = DqLayout<D>;
@@ -565,14 +568,16 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
   uint32_t* bitA = ulist + 2 * p.kmax + 2;
   uint32_t* bitB = bitA + nwords;
 
-  // bar_k[s]: K stage s filled; bar_kvfree[s]: dQ of the step using stage s
-  // done (K read).  bar_v: the V stage filled; bar_vfree: dP of its step done
-  // (V read).  s_done: S(j) and dP(j) done; s_free: the compute warps have
-  // read them (all compute threads); bar_ds[b]: dS(j) written into buffer
-  // b = j % 2; ds_free[b]: the dQ that read buffer b completed.  Every parity
-  // wait targets a barrier in the awaited phase or the one after it.
-  __shared__ uint64_t bar_qdo, bar_k[kDqKStages], bar_kvfree[kDqKStages], bar_v, bar_vfree, s_done, s_free, bar_ds[2],
-      ds_free[2];
+  // bar_q: the Q tile landed.  bar_dot: the compute warps have written dO
+  // into TMEM (all compute threads).  bar_k[s]: K stage s filled;
+  // bar_kvfree[s]: dQ of the step using stage s done (K read).  bar_v[s]: V
+  // stage s filled; bar_vfree[s]: dP of the step using it done (V read).
+  // s_done: S(j) and dP(j) done; s_free: the compute warps have read them
+  // (all compute threads); bar_ds: dS(j) written; ds_free: dQ(j), which read
+  // it, done.  Every parity wait targets a barrier in the awaited phase or
+  // the one after it.
+  __shared__ uint64_t bar_q, bar_dot, bar_k[kDqKStages], bar_kvfree[kDqKStages], bar_v[kDqVStages],
+      bar_vfree[kDqVStages], s_done, s_free, bar_ds, ds_free;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int n_union, n_cnt[2];
 
@@ -585,17 +590,18 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
   const int64_t row_base = bh * p.N;
 
   if (tid == 0) {
-    mbar_init(&bar_qdo, 1);
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_dot, kCompute);
     for (int i = 0; i < kDqKStages; ++i) {
       mbar_init(&bar_k[i], 1);
       mbar_init(&bar_kvfree[i], 1);
     }
-    mbar_init(&bar_v, 1);
-    mbar_init(&bar_vfree, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_ds[i], kCompute);
-      mbar_init(&ds_free[i], 1);
+    for (int i = 0; i < kDqVStages; ++i) {
+      mbar_init(&bar_v[i], 1);
+      mbar_init(&bar_vfree[i], 1);
     }
+    mbar_init(&bar_ds, kCompute);
+    mbar_init(&ds_free, 1);
     mbar_init(&s_done, 1);
     mbar_init(&s_free, kCompute);
     fence_mbar_init();
@@ -604,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
     tmem_alloc(&tmem_base_sh, 512);
     tmem_relinquish();
   }
-  for (int w = tid; w < 2 * nwords; w += kThreads) bitA[w] = 0;  // bitA and bitB are contiguous
+  for (int w = tid; w < 2 * nwords; w += kDqThreads) bitA[w] = 0;  // bitA and bitB are contiguous
   __syncthreads();
   {
     const int64_t rowa = bh * p.Nc + qa, rowb = bh * p.Nc + (has_b ? qb : qa);
@@ -618,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
     }
     const int32_t* la = p.idx + rowa * p.kmax;
     const int32_t* lb = p.idx + rowb * p.kmax;
-    for (int e = tid; e < ca + cb; e += kThreads) {
+    for (int e = tid; e < ca + cb; e += kDqThreads) {
       const bool isA = e < ca;
       const int c = isA ? la[e] : lb[e - ca];
       if (c < 0 || c >= p.Nc) continue;  // reported by the inverse-list build
@@ -644,14 +650,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
   if (warp == 0) {
     // ---------------- TMA producer
     if (lane == 0 && steps > 0) {
-      mbar_expect_tx(&bar_qdo, 2 * L::kTile);
-      const int cq1 = has_b ? qb : qa;
-      load_cube_pair<D>(sm + L::kQ, &p.tq, &bar_qdo, row_base, qa, cq1);
-      load_cube_pair<D>(sm + L::kDO, &p.tdo, &bar_qdo, row_base, qa, cq1);
-      // K(j) goes into stage j % 3 once dQ(j - 3) is done; V(j) into the V
-      // stage once dP(j - 1) is.  V(j) is needed first (dP(j) follows S(j)),
+      mbar_expect_tx(&bar_q, L::kTile);
+      load_cube_pair<D>(sm + L::kQ, &p.tq, &bar_q, row_base, qa, has_b ? qb : qa);
+      // K(j) goes into stage j % 3 once dQ(j - 3) is done; V(j) into stage
+      // j % 2 once dP(j - 2) is.  V(j) is needed first (dP(j) follows S(j)),
       // so it goes out before K(j + 1), and the waits spin: a suspended wait
-      // wakes hundreds of cycles late, all of it on dP(j)'s path.
+      // wakes hundreds of cycles late.
       auto load_k = [&](int j) -> bool {
         const int s = j % kDqKStages;
         if (j >= kDqKStages && !mbar_spin(&bar_kvfree[s], ((j / kDqKStages) - 1) & 1)) return false;
@@ -661,80 +665,88 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
       };
       bool ok = load_k(0);
       for (int j = 0; ok && j < steps; ++j) {
-        if (j >= 1 && !mbar_spin(&bar_vfree, (j - 1) & 1)) ok = false;
+        const int vs = j % kDqVStages;
+        if (j >= kDqVStages && !mbar_spin(&bar_vfree[vs], ((j / kDqVStages) - 1) & 1)) ok = false;
         if (!ok) break;
-        mbar_expect_tx(&bar_v, L::kTile);
-        load_cube_pair<D>(sm + L::kV, &p.tv, &bar_v, row_base, kcube(j, 0), kcube(j, 1));
+        mbar_expect_tx(&bar_v[vs], L::kTile);
+        load_cube_pair<D>(sm + L::kV + vs * L::kTile, &p.tv, &bar_v[vs], row_base, kcube(j, 0), kcube(j, 1));
         if (j + 1 < steps) ok = load_k(j + 1);
       }
       if (!ok) flag_error(p.err, kErrTimeout);
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer: S(j+1) and dP(j+1) once the compute warps
-    // have read S(j) and dP(j); dQ(j) once dS(j) is written.  Polls with
-    // test_wait and issues whichever is ready; descriptors are precomputed.
+  } else if (warp == 1 || warp == 10) {
+    // ---------------- MMA issuers.  An MMA issue holds the issuing thread
+    // about as long as the tensor core takes to run it, and each barrier poll
+    // costs ~100+ cycles while the tensor core streams shared memory, so one
+    // thread issuing everything leaves the pipe idle between groups.  Two
+    // threads issue instead, each in its own fixed order: warp 1 S(j) then
+    // dP(j) (S(j) once the compute warps have read S / dP(j - 1)), warp 10
+    // dQ(j) once dS(j) is written.  Their groups touch disjoint TMEM columns;
+    // each thread's commits track its own MMAs.
     if (lane == 0 && steps > 0) {
       constexpr uint32_t idesc_s = idesc_f32acc(128, 128, 0, 0, 1);
       constexpr uint32_t idesc_q = idesc_f32acc(128, D, 0, 1, 1);
-      uint64_t qdesc[D / 16], odesc[D / 16];
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        qdesc[kk] = sdesc_sw128(smem_u32(sm + L::kQ + off), 16, 1024);
-        odesc[kk] = sdesc_sw128(smem_u32(sm + L::kDO + off), 16, 1024);
-      }
-      const uint64_t kkm0 = sdesc_sw128(smem_u32(sm + L::kK), 16, 1024);      // K stages, K-major
-      const uint64_t vkm0 = sdesc_sw128(smem_u32(sm + L::kV), 16, 1024);      // V stages, K-major
-      const uint64_t kmn0 = sdesc_sw128(smem_u32(sm + L::kK), 16384, 1024);   // K stages, MN-major
       constexpr uint32_t kTileU = L::kTile >> 4;
-      bool ok = mbar_spin(&bar_qdo, 0);
-      int ns = 0, npd = 0, ng = 0;   // next S, next dP, next dQ to issue
-      uint32_t ks = 0, kph = 0;      // K stage of S(ns) and its fill parity
-      uint32_t kg = 0;               // K stage of dQ(ng)
-      uint32_t idle = 0;
-      while (ok && ng < steps) {
-        bool progressed = false;
-        // S(ns) once the compute warps have read S / dP (ns - 1) and K(ns) landed.
-        if (ns < steps && ns == npd && (ns == 0 || mbar_test(&s_free, (ns - 1) & 1)) && mbar_test(&bar_k[ks], kph)) {
+      bool ok = true;
+      if (warp == 1) {
+        uint64_t qdesc[D / 16];
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          qdesc[kk] = sdesc_sw128(smem_u32(sm + L::kQ + (kk >> 2) * 16384 + (kk & 3) * 32), 16, 1024);
+        const uint64_t kkm0 = sdesc_sw128(smem_u32(sm + L::kK), 16, 1024);  // K stages, K-major
+        const uint64_t vkm0 = sdesc_sw128(smem_u32(sm + L::kV), 16, 1024);  // V stages, K-major
+        ok = mbar_spin(&bar_q, 0) && mbar_spin(&bar_dot, 0);
+        uint32_t ks = 0, kph = 0, vs = 0, vph = 0;  // ring stages of step j and their fill parities
+        for (int j = 0; ok && j < steps; ++j) {
+          if ((j > 0 && !mbar_spin(&s_free, (j - 1) & 1)) || !mbar_spin(&bar_k[ks], kph)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint64_t kd = kkm0 + ks * kTileU;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + kDqS, qdesc[kk], kd + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
-          ++ns;
+          // dP(j) = dO V^T (A = dO from TMEM); then S and dP are done together.
+          if (!mbar_spin(&bar_v[vs], vph)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t vd = vkm0 + vs * kTileU;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ts(tmem + kDqDP, tmem + kDqDO + kk * 8, vd + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), idesc_s,
+                   kk > 0);
+          mma_commit(&s_done);
+          mma_commit(&bar_vfree[vs]);
           if (++ks == static_cast<uint32_t>(kDqKStages)) {
             ks = 0;
             kph ^= 1u;
           }
-          progressed = true;
+          if (++vs == static_cast<uint32_t>(kDqVStages)) {
+            vs = 0;
+            vph ^= 1u;
+          }
         }
-        // dP(npd) after its S, once V(npd) landed; then S and dP are done together.
-        if (npd < ns && mbar_test(&bar_v, npd & 1)) {
+      } else {
+        const uint64_t kmn0 = sdesc_sw128(smem_u32(sm + L::kK), 16384, 1024);  // K stages, MN-major
+        uint32_t kg = 0;  // K stage of dQ(j)
+        for (int j = 0; ok && j < steps; ++j) {
+          if (!mbar_spin(&bar_ds, j & 1)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + kDqDP, odesc[kk], vkm0 + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
-          mma_commit(&s_done);
-          mma_commit(&bar_vfree);
-          ++npd;
-          progressed = true;
-        }
-        if (ng < npd && mbar_test(&bar_ds[ng & 1], (ng >> 1) & 1)) {
-          tc_fence_after();
-          const uint32_t dsb = tmem + kDqDS + 64 * (ng & 1);
           const uint64_t kd = kmn0 + kg * kTileU;
           // A = dS (K = 128 keys in 8 steps of 16), B = the K stage (MN-major).
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + kDqDQ, dsb + kk * 8, kd + ((kk * 2048) >> 4), idesc_q, (ng > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + kDqDQ, tmem + kDqDS + kk * 8, kd + ((kk * 2048) >> 4), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bar_kvfree[kg]);
-          mma_commit(&ds_free[ng & 1]);
-          ++ng;
+          mma_commit(&ds_free);
           if (++kg == static_cast<uint32_t>(kDqKStages)) kg = 0;
-          progressed = true;
         }
-        idle = progressed ? 0u : idle + 1u;
-        if (idle > (1u << 26)) ok = false;
       }
       if (!ok) flag_error(p.err, kErrTimeout);
     }
@@ -752,8 +764,25 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
     const float dlt = row_valid ? p.delta[grow] : 0.f;
     const uint64_t sl2 = f2(p.scale_log2, p.scale_log2), nlse2 = f2(-lse2, -lse2), dlt2 = f2(dlt, dlt);
     bool ok = true;
+    {
+      // dO rows into TMEM (lane = row, column c = elements 2c and 2c + 1):
+      // warpgroup g writes elements [g D/2, (g + 1) D/2) of its rows.
+      const uint4* src = reinterpret_cast<const uint4*>(p.dof + grow * D + g * (D / 2));
+#pragma unroll
+      for (int c = 0; c < D / 4; c += 8) {
+        uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+        if (row_valid && steps > 0) {
+          a = src[c / 4];
+          b = src[c / 4 + 1];
+        }
+        const uint32_t r[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        tmem_st8(lane_addr + kDqDO + g * (D / 4) + c, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar_dot);
+    }
     for (int j = 0; j < steps; ++j) {
-      const int b = j & 1;
       const bool has1 = 2 * j + 1 < U;
       const uint32_t e = (g == 0) ? ulist[2 * j] : (has1 ? ulist[2 * j + 1] : 0u);
       const bool valid = (g == 0 || has1) && ((e >> my_bit) & 1u) != 0;  // warp-uniform
@@ -780,21 +809,22 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_c
 #pragma unroll
         for (int i = 0; i < 32; ++i) ds[i] = 0u;
       }
-      // Into dS buffer b once dQ(j - 2) has read it.
-      if (j >= 2) {
-        if (!mbar_spin(&ds_free[b], ((j >> 1) - 1) & 1)) {
+      // Into the dS buffer once dQ(j - 1) has read it (dQ(j - 1) runs right
+      // after dP(j), so this rarely waits).
+      if (j >= 1) {
+        if (!mbar_spin(&ds_free, (j - 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
       }
 #pragma unroll
-      for (int c = 0; c < 32; c += 8) tmem_st8(lane_addr + kDqDS + 64 * b + 32 * g + c, ds + c);
+      for (int c = 0; c < 32; c += 8) tmem_st8(lane_addr + kDqDS + 32 * g + c, ds + c);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bar_ds[b]);
+      mbar_arrive(&bar_ds);
     }
-    if (ok && steps > 0 && !mbar_spin(&ds_free[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
+    if (ok && steps > 0 && !mbar_spin(&ds_free, (steps - 1) & 1)) ok = false;
     if (!ok) flag_error(p.err, kErrTimeout);
     tc_fence_after();
     // ---------------- dQ rows (warpgroup g writes columns [g*D/2, (g+1)*D/2))
@@ -1028,6 +1058,7 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   if ((st = make_tile_map(&p.tk, kp, rows, d, 1)) != VSA_OK) return st;
   if ((st = make_tile_map(&p.tv, vp, rows, d, 1)) != VSA_OK) return st;
   if ((st = make_tile_map(&p.tdo, dof, rows, d, 1)) != VSA_OK) return st;
+  p.dof = static_cast<const uint16_t*>(dof);
   const int Nc = N / kCube, nwords = (Nc + 31) / 32;
   p.lse = lse;
   p.delta = delta;
@@ -1062,23 +1093,23 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   const size_t kv_extra = sizeof(uint32_t) * (2 * Nc + 2 + 2 * nwords) + 4 * sizeof(float) * d;
   const size_t dq_extra = sizeof(uint32_t) * (2 * kmax + 2 + 2 * nwords);
   dim3 grid((Nc + 1) / 2, BH);
-  auto go = [&](auto kernel, size_t bytes, cudaStream_t st_) -> int {
+  auto go = [&](auto kernel, size_t bytes, int threads, cudaStream_t st_) -> int {
     const size_t smem = bytes + 1024;
     if (smem > 226 * 1024) return VSA_ERR_UNSUPPORTED;  // 1 KB of the 227 KB is left for static shared memory
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       return VSA_ERR_CUDA;
-    kernel<<<grid, kThreads, smem, st_>>>(p);
+    kernel<<<grid, threads, smem, st_>>>(p);
     return VSA_OK;
   };
   timing_mark(VSA_K_FINE_BWD, true, s_kv);
-  st = d == 128 ? go(fine_bwd_kv_kernel<128>, KvLayout<128>::kEnd + kv_extra, s_kv)
-                : go(fine_bwd_kv_kernel<64>, KvLayout<64>::kEnd + kv_extra, s_kv);
+  st = d == 128 ? go(fine_bwd_kv_kernel<128>, KvLayout<128>::kEnd + kv_extra, kThreads, s_kv)
+                : go(fine_bwd_kv_kernel<64>, KvLayout<64>::kEnd + kv_extra, kThreads, s_kv);
   timing_mark(VSA_K_FINE_BWD, false, s_kv);
   if (st != VSA_OK) return st;
   timing_mark(VSA_K_FINE_BWD_DQ, true, s);
-  st = d == 128 ? go(fine_bwd_dq_kernel<128>, DqLayout<128>::kEnd + dq_extra, s)
-                : go(fine_bwd_dq_kernel<64>, DqLayout<64>::kEnd + dq_extra, s);
+  st = d == 128 ? go(fine_bwd_dq_kernel<128>, DqLayout<128>::kEnd + dq_extra, kDqThreads, s)
+                : go(fine_bwd_dq_kernel<64>, DqLayout<64>::kEnd + dq_extra, kDqThreads, s);
   timing_mark(VSA_K_FINE_BWD_DQ, false, s);
   if (st != VSA_OK) return st;
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
