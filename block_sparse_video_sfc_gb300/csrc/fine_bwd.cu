@@ -58,9 +58,10 @@ int make_tile_map(void* map, const void* base, int64_t rows, int d, int f16);
 
 namespace {
 
-constexpr int kThreads = 320;  // producer, MMA issuer, 2 compute warpgroups
+// Warp 0: TMA producer; warps 1 and 10: MMA issuers; warps 2-9: two compute
+// warpgroups.
+constexpr int kThreads = 352;
 constexpr int kCompute = 256;
-constexpr int kDqThreads = 352;  // the dQ kernel adds a second MMA issuer (warp 10)
 
 struct BwdParams {
   CUtensorMap tq, tk, tv, tdo;  // fp16 [BH*N, d], box {64, 64}, 128B swizzle
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       load_cube_pair<D>(sm + L::kV, &p.tv, &bar_kv, row_base, k1, c1);
       for (int j = 0; j < steps; ++j) {
         const int st = j & (kKvStages - 1);
-        if (j >= kKvStages && !mbar_wait(&stage_free[st], ((j / kKvStages) - 1) & 1)) {
+        if (j >= kKvStages && !mbar_spin(&stage_free[st], ((j / kKvStages) - 1) & 1)) {
           flag_error(p.err, kErrTimeout);
           break;
         }
@@ -377,37 +378,40 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
         bulk_load(stats + 64, p.delta + qrow, 256, &full[st]);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer: S^T / dP^T (j) once the compute warps have
-    // read S^T / dP^T (j - 1); dV / dK (j) once P^T / dS^T (j) are written.
-    // Polls with test_wait and issues whichever is ready, S first, so that
-    // S^T(j + 1) runs while the compute warps work on step j.
+  } else if (warp == 1 || warp == 10) {
+    // ---------------- MMA issuers, each in its own fixed order: warp 1
+    // S^T(j) and dP^T(j) once the compute warps have read S^T / dP^T (j - 1);
+    // warp 10 dV(j) and dK(j) once P^T / dS^T (j) are written.  (An MMA issue
+    // holds its thread about as long as the group runs, and a barrier poll
+    // costs ~100+ cycles under the tensor core's shared-memory traffic: one
+    // thread issuing both kinds leaves the pipe idle between groups.)  The
+    // two threads' groups touch disjoint TMEM columns; each thread's commits
+    // track its own MMAs.
     if (lane == 0 && steps > 0) {
       constexpr uint32_t idesc_s = idesc_f32acc(128, 64, 0, 0, 1);
       constexpr uint32_t idesc_g = idesc_f32acc(128, D, 0, 1, 1);
-      bool ok = mbar_spin(&bar_kv, 0);
-      // The issuer shares its sub-partition with two busy compute warps, so
-      // every descriptor is precomputed: K / V per K-step, Q / dO stage bases
-      // (the start-address field is linear in the byte address, so a K-step
-      // or a stage is a constant added to a base).
-      uint64_t kdesc[D / 16], vdesc[D / 16];
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        kdesc[kk] = sdesc_sw128(smem_u32(sm + L::kK + off), 16, 1024);
-        vdesc[kk] = sdesc_sw128(smem_u32(sm + L::kV + off), 16, 1024);
-      }
-      const uint64_t qkm0 = sdesc_sw128(smem_u32(sm + L::kRing), 16, 1024);          // Q / dO, K-major
-      const uint64_t qmn0 = sdesc_sw128(smem_u32(sm + L::kRing), 8192, 1024);        // Q / dO, MN-major
       constexpr uint32_t kStageU = L::kStage >> 4, kTileQU = L::kTileQ >> 4;
-      int ns = 0, ng = 0;  // next S^T / dP^T and next dV / dK to issue
-      uint32_t idle = 0;
-      while (ok && ng < steps) {
-        bool progressed = false;
-        if (ns < steps && (ns == 0 || mbar_test(&s_free, (ns - 1) & 1)) &&
-            mbar_test(&full[ns & (kKvStages - 1)], (ns / kKvStages) & 1)) {
+      bool ok = true;
+      if (warp == 1) {
+        // Descriptors precomputed: K / V per K-step, the Q / dO stage base
+        // (the start-address field is linear in the byte address).
+        uint64_t kdesc[D / 16], vdesc[D / 16];
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          kdesc[kk] = sdesc_sw128(smem_u32(sm + L::kK + off), 16, 1024);
+          vdesc[kk] = sdesc_sw128(smem_u32(sm + L::kV + off), 16, 1024);
+        }
+        const uint64_t qkm0 = sdesc_sw128(smem_u32(sm + L::kRing), 16, 1024);  // Q / dO, K-major
+        ok = mbar_spin(&bar_kv, 0);
+        for (int j = 0; ok && j < steps; ++j) {
+          const int st = j & (kKvStages - 1);
+          if ((j > 0 && !mbar_spin(&s_free, (j - 1) & 1)) || !mbar_spin(&full[st], (j / kKvStages) & 1)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint64_t qd = qkm0 + (ns & (kKvStages - 1)) * kStageU;
+          const uint64_t qd = qkm0 + st * kStageU;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + kKvS, kdesc[kk], qd + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
@@ -416,30 +420,30 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
             mma_ss(tmem + kKvDP, vdesc[kk], qd + kTileQU + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s,
                    kk > 0);
           mma_commit(&s_done);
-          ++ns;
-          progressed = true;
         }
-        if (ng < ns && mbar_test(&pds[ng & 1], (ng >> 1) & 1)) {
+      } else {
+        const uint64_t qmn0 = sdesc_sw128(smem_u32(sm + L::kRing), 8192, 1024);  // Q / dO, MN-major
+        for (int j = 0; ok && j < steps; ++j) {
+          if (!mbar_spin(&pds[j & 1], (j >> 1) & 1)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const int st = ng & (kKvStages - 1);
+          const int st = j & (kKvStages - 1);
           const uint64_t qd = qmn0 + st * kStageU;
-          const uint32_t pb = tmem + kKvPB + 64 * (ng & 1);
+          const uint32_t pb = tmem + kKvPB + 64 * (j & 1);
           // A = P^T / dS^T (K = 64 queries in 4 steps of 16: queries 16 kk..
           // at column 8 kk of the P buffer's half), B = dO / Q (MN-major).
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ts(tmem + kKvDV, pb + 8 * kk, qd + kTileQU + ((kk * 2048) >> 4), idesc_g,
-                   (ng > 0 || kk > 0) ? 1u : 0u);
+                   (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kKvDK, pb + 32 + 8 * kk, qd + ((kk * 2048) >> 4), idesc_g, (ng > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + kKvDK, pb + 32 + 8 * kk, qd + ((kk * 2048) >> 4), idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&stage_free[st]);
-          mma_commit(&pbuf_free[ng & 1]);
-          ++ng;
-          progressed = true;
+          mma_commit(&pbuf_free[j & 1]);
         }
-        idle = progressed ? 0u : idle + 1u;
-        if (idle > (1u << 26)) ok = false;
       }
       if (!ok) flag_error(p.err, kErrTimeout);
     }
@@ -559,7 +563,7 @@ constexpr int kDqKStages = 3, kDqVStages = 2;
 constexpr uint32_t kDqS = 0, kDqDP = 128, kDqDS = 256, kDqDO = 320, kDqDQ = 384;
 
 template <int D>
-__global__ void __launch_bounds__(kDqThreads, 1) fine_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) fine_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using L = DqLayout<D>;
@@ -610,7 +614,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) fine_bwd_dq_kernel(const __grid
     tmem_alloc(&tmem_base_sh, 512);
     tmem_relinquish();
   }
-  for (int w = tid; w < 2 * nwords; w += kDqThreads) bitA[w] = 0;  // bitA and bitB are contiguous
+  for (int w = tid; w < 2 * nwords; w += kThreads) bitA[w] = 0;  // bitA and bitB are contiguous
   __syncthreads();
   {
     const int64_t rowa = bh * p.Nc + qa, rowb = bh * p.Nc + (has_b ? qb : qa);
@@ -624,7 +628,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) fine_bwd_dq_kernel(const __grid
     }
     const int32_t* la = p.idx + rowa * p.kmax;
     const int32_t* lb = p.idx + rowb * p.kmax;
-    for (int e = tid; e < ca + cb; e += kDqThreads) {
+    for (int e = tid; e < ca + cb; e += kThreads) {
       const bool isA = e < ca;
       const int c = isA ? la[e] : lb[e - ca];
       if (c < 0 || c >= p.Nc) continue;  // reported by the inverse-list build
@@ -1093,23 +1097,23 @@ int launch_fine_bwd_core(const void* qp, const void* kp, const void* vp, const v
   const size_t kv_extra = sizeof(uint32_t) * (2 * Nc + 2 + 2 * nwords) + 4 * sizeof(float) * d;
   const size_t dq_extra = sizeof(uint32_t) * (2 * kmax + 2 + 2 * nwords);
   dim3 grid((Nc + 1) / 2, BH);
-  auto go = [&](auto kernel, size_t bytes, int threads, cudaStream_t st_) -> int {
+  auto go = [&](auto kernel, size_t bytes, cudaStream_t st_) -> int {
     const size_t smem = bytes + 1024;
     if (smem > 226 * 1024) return VSA_ERR_UNSUPPORTED;  // 1 KB of the 227 KB is left for static shared memory
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       return VSA_ERR_CUDA;
-    kernel<<<grid, threads, smem, st_>>>(p);
+    kernel<<<grid, kThreads, smem, st_>>>(p);
     return VSA_OK;
   };
   timing_mark(VSA_K_FINE_BWD, true, s_kv);
-  st = d == 128 ? go(fine_bwd_kv_kernel<128>, KvLayout<128>::kEnd + kv_extra, kThreads, s_kv)
-                : go(fine_bwd_kv_kernel<64>, KvLayout<64>::kEnd + kv_extra, kThreads, s_kv);
+  st = d == 128 ? go(fine_bwd_kv_kernel<128>, KvLayout<128>::kEnd + kv_extra, s_kv)
+                : go(fine_bwd_kv_kernel<64>, KvLayout<64>::kEnd + kv_extra, s_kv);
   timing_mark(VSA_K_FINE_BWD, false, s_kv);
   if (st != VSA_OK) return st;
   timing_mark(VSA_K_FINE_BWD_DQ, true, s);
-  st = d == 128 ? go(fine_bwd_dq_kernel<128>, DqLayout<128>::kEnd + dq_extra, kDqThreads, s)
-                : go(fine_bwd_dq_kernel<64>, DqLayout<64>::kEnd + dq_extra, kDqThreads, s);
+  st = d == 128 ? go(fine_bwd_dq_kernel<128>, DqLayout<128>::kEnd + dq_extra, s)
+                : go(fine_bwd_dq_kernel<64>, DqLayout<64>::kEnd + dq_extra, s);
   timing_mark(VSA_K_FINE_BWD_DQ, false, s);
   if (st != VSA_OK) return st;
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;

@@ -1,7 +1,8 @@
 """CPU model of the barrier protocol of the dK/dV kernel (fine_bwd_kv_kernel).
 
 The kernel runs four roles on shared-memory mbarriers: a TMA producer filling
-a 4-stage Q/dO ring, one MMA-issuing thread, and two compute warpgroups.  One
+a 4-stage Q/dO ring, two MMA-issuing threads (one issues S^T(j) and dP^T(j),
+the other dV(j) and dK(j)), and two compute warpgroups.  One
 S^T / dP^T buffer in TMEM is released as soon as both warpgroups have read it
 into registers; P^T / dS^T go to one of two P buffers (b = j % 2), which the
 dV / dK products read.  The barriers, per the kernel:
@@ -15,8 +16,9 @@ A parity wait for phase k is only correct while the barrier has completed k
 or k + 1 phases; the model asserts that at every test, that S^T(j + 1) never
 overwrites the buffer before both warpgroups read S^T(j), that P(j + 2) is
 never written before dV/dK(j) read P buffer b, that dV/dK(j) read P(j), and
-that every schedule of random delays terminates.  The tensor pipe executes the
-issued MMA groups in order, as the hardware does.
+that every schedule of random delays terminates.  The MMA groups of one
+issuing thread complete in the order issued; nothing orders the two threads'
+groups, so the model runs them as two independent queues.
 """
 import random
 
@@ -60,12 +62,14 @@ def simulate(steps, seed, max_ticks=200000, drop=()):
     pbuf = [None, None]          # P buffer -> (content, step)
     ring = [None] * STAGES       # stage -> [step, read by dV/dK]
     read_by, wrote = {}, {}      # step -> warpgroups that read S^T / wrote P^T
-    pipe, loads = [], []         # in-order MMA groups; TMA loads in flight
+    pipes, loads = {"A": [], "B": []}, []   # each issuer's in-order MMA groups; TMA loads in flight
     produced = ns = ng = 0
     computed = [0, 0]
     phase = [0, 0]               # per warpgroup: 0 = read S^T(j), 1 = write P(j)
     for tick in range(max_ticks):
-        if pipe:                 # tensor pipe: in order
+        for pipe in pipes.values():  # each issuer's groups: in order
+            if not pipe or rnd.random() < 0.3:
+                continue
             pipe[0][2] -= 1
             if pipe[0][2] <= 0:
                 kind, j, _, bars = pipe.pop(0)
@@ -92,14 +96,13 @@ def simulate(steps, seed, max_ticks=200000, drop=()):
             if produced < STAGES or "stage_free" in drop or stage_free[st].test(produced // STAGES - 1):
                 loads.append([st, delay(rnd, 8), produced])
                 produced += 1
-        if rnd.random() < 0.7:                        # MMA issuer: S first, then dV / dK
-            if ns < steps and (ns == 0 or "s_free" in drop or s_free.test(ns - 1)) and \
-                    full[ns % STAGES].test(ns // STAGES):
-                pipe.append(["S", ns, delay(rnd, 5), [s_done]])
-                ns += 1
-            elif ng < ns and pds[ng & 1].test(ng >> 1):
-                pipe.append(["G", ng, delay(rnd, 5), [stage_free[ng % STAGES], pbuf_free[ng & 1]]])
-                ng += 1
+        if rnd.random() < 0.7 and ns < steps and (ns == 0 or "s_free" in drop or s_free.test(ns - 1)) and \
+                full[ns % STAGES].test(ns // STAGES):   # issuer A: S^T(j), dP^T(j)
+            pipes["A"].append(["S", ns, delay(rnd, 5), [s_done]])
+            ns += 1
+        if rnd.random() < 0.7 and ng < ns and pds[ng & 1].test(ng >> 1):   # issuer B: dV(j), dK(j)
+            pipes["B"].append(["G", ng, delay(rnd, 5), [stage_free[ng % STAGES], pbuf_free[ng & 1]]])
+            ng += 1
         for g in range(2):                            # compute warpgroups
             j = computed[g]
             if j >= steps or rnd.random() >= 0.4:
@@ -122,7 +125,7 @@ def simulate(steps, seed, max_ticks=200000, drop=()):
                 pds[b].arrive()
                 computed[g] += 1
                 phase[g] = 0
-        if ng == steps and not pipe and computed == [steps, steps]:
+        if ng == steps and not pipes["A"] and not pipes["B"] and computed == [steps, steps]:
             if steps:            # the epilogue's wait for the last dV/dK
                 assert pbuf_free[(steps - 1) & 1].test((steps - 1) >> 1)
             return tick
