@@ -259,11 +259,15 @@ struct KvLayout {
   static constexpr int kStats = kRing + kKvStages * kStage;  // [stage][LSE 64 | D 64] fp32
   static constexpr int kEnd = kStats + kKvStages * 512;
 };
-// TMEM: S^T at column 0 and dP^T at 64 (64 fp32 columns each); P buffer b at
-// 128 + 64 b: P^T in its first 32 columns of fp16 pairs, dS^T in the next 32
-// (compute warpgroup g reads query columns [32 g, 32 g + 32) of S^T / dP^T and
-// writes its 16 packed columns at 16 g of each); dV at 256, dK at 384.
-constexpr uint32_t kKvS = 0, kKvDP = 64, kKvPB = 128, kKvDV = 256, kKvDK = 384;
+// TMEM: two step buffers, b = j % 2 at 128 b: S^T(j) in its columns [0, 64)
+// and dP^T(j) in [64, 128) (fp32).  Compute warpgroup g reads query columns
+// [32 g, 32 g + 32) of S^T and of dP^T and overwrites the first 16 of each
+// range with its P^T and dS^T (fp16 pairs): every thread rewrites only
+// columns of its own lane that it has itself read, so the two warpgroups
+// never touch each other's values.  The dV / dK MMA takes queries
+// 16 kk .. 16 kk + 15 from column 32 (kk / 2) + 8 (kk % 2).  dV at 256, dK
+// at 384.
+constexpr uint32_t kKvBuf = 128, kKvDPOff = 64, kKvDV = 256, kKvDK = 384;
 template <int D>
 constexpr int kKvCoarseBytes = 4 * D * static_cast<int>(sizeof(float));  // crow (fused epilogue)
 
@@ -280,14 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
   uint32_t* bitB = bitA + p.nwords;
 
   // full[s]: Q, dO, LSE and D of the step in stage s landed; stage_free[s]:
-  // dV and dK of that step completed.  s_done: S^T(j) and dP^T(j) done;
-  // s_free: the compute warps have read them (all compute threads), so
-  // S^T(j + 1) may overwrite the buffer.  For P buffer b = j % 2: pds[b]:
-  // P^T / dS^T(j) written (all compute threads); pbuf_free[b]: dV(j) and
-  // dK(j), which read them, completed.  Every parity wait targets a barrier in
-  // the awaited phase or the one after it: S^T(j + 1) needs the read of
-  // S^T(j), and P(j + 2) is written only after dV / dK(j) completed.
-  __shared__ uint64_t bar_kv, full[kKvStages], stage_free[kKvStages], s_done, s_free, pds[2], pbuf_free[2];
+  // dK of that step (the last reader of the stage) completed.  For step
+  // buffer b = j % 2, whose S^T half and dP^T half are pipelined apart:
+  // st_done[b] / dpt_done[b]: S^T(j) / dP^T(j) done; p_ready[b] / ds_ready[b]:
+  // P^T(j) / dS^T(j) written over them (all compute threads); st_free[b] /
+  // dpt_free[b]: dV(j) / dK(j), which read them, completed, so S^T(j + 2) /
+  // dP^T(j + 2) may overwrite that half.  Every parity wait targets a
+  // barrier in the awaited phase or the one after it.
+  __shared__ uint64_t bar_kv, full[kKvStages], stage_free[kKvStages], st_done[2], dpt_done[2], p_ready[2],
+      ds_ready[2], st_free[2], dpt_free[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int n_union;
 
@@ -305,11 +310,13 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       mbar_init(&full[i], 1);
       mbar_init(&stage_free[i], 1);
     }
-    mbar_init(&s_done, 1);
-    mbar_init(&s_free, kCompute);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&pds[i], kCompute);
-      mbar_init(&pbuf_free[i], 1);
+      mbar_init(&st_done[i], 1);
+      mbar_init(&dpt_done[i], 1);
+      mbar_init(&p_ready[i], kCompute);
+      mbar_init(&ds_ready[i], kCompute);
+      mbar_init(&st_free[i], 1);
+      mbar_init(&dpt_free[i], 1);
     }
     fence_mbar_init();
   }
@@ -360,7 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       load_cube_pair<D>(sm + L::kV, &p.tv, &bar_kv, row_base, k1, c1);
       for (int j = 0; j < steps; ++j) {
         const int st = j & (kKvStages - 1);
-        if (j >= kKvStages && !mbar_spin(&stage_free[st], ((j / kKvStages) - 1) & 1)) {
+        // A suspended wait: the ring has slack, and a polling producer would
+        // take issue slots from the two compute warps on its sub-partition.
+        if (j >= kKvStages && !mbar_wait(&stage_free[st], ((j / kKvStages) - 1) & 1)) {
           flag_error(p.err, kErrTimeout);
           break;
         }
@@ -380,8 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
     }
   } else if (warp == 1 || warp == 10) {
     // ---------------- MMA issuers, each in its own fixed order: warp 1
-    // S^T(j) and dP^T(j) once the compute warps have read S^T / dP^T (j - 1);
-    // warp 10 dV(j) and dK(j) once P^T / dS^T (j) are written.  (An MMA issue
+    // S^T(j) into step buffer j % 2 once dV(j - 2) has read that half, then
+    // dP^T(j) once dK(j - 2) has; warp 10 dV(j) once P^T(j) is written, then
+    // dK(j) once dS^T(j) is.  The compute warps start on S^T(j) while dP^T(j)
+    // runs, and dV(j) runs while they finish dS^T(j).  (An MMA issue
     // holds its thread about as long as the group runs, and a barrier poll
     // costs ~100+ cycles under the tensor core's shared-memory traffic: one
     // thread issuing both kinds leaves the pipe idle between groups.)  The
@@ -405,44 +416,60 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
         const uint64_t qkm0 = sdesc_sw128(smem_u32(sm + L::kRing), 16, 1024);  // Q / dO, K-major
         ok = mbar_spin(&bar_kv, 0);
         for (int j = 0; ok && j < steps; ++j) {
-          const int st = j & (kKvStages - 1);
-          if ((j > 0 && !mbar_spin(&s_free, (j - 1) & 1)) || !mbar_spin(&full[st], (j / kKvStages) & 1)) {
+          const int st = j & (kKvStages - 1), b = j & 1;
+          const uint32_t ph = ((j >> 1) - 1) & 1;
+          if ((j >= 2 && !mbar_spin(&st_free[b], ph)) || !mbar_spin(&full[st], (j / kKvStages) & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t qd = qkm0 + st * kStageU;
+          const uint32_t sb = tmem + kKvBuf * b;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + kKvS, kdesc[kk], qd + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + kKvDP, vdesc[kk], qd + kTileQU + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s,
-                   kk > 0);
-          mma_commit(&s_done);
-        }
-      } else {
-        const uint64_t qmn0 = sdesc_sw128(smem_u32(sm + L::kRing), 8192, 1024);  // Q / dO, MN-major
-        for (int j = 0; ok && j < steps; ++j) {
-          if (!mbar_spin(&pds[j & 1], (j >> 1) & 1)) {
+            mma_ss(sb, kdesc[kk], qd + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
+          mma_commit(&st_done[b]);
+          if (j >= 2 && !mbar_spin(&dpt_free[b], ph)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const int st = j & (kKvStages - 1);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(sb + kKvDPOff, vdesc[kk], qd + kTileQU + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s,
+                   kk > 0);
+          mma_commit(&dpt_done[b]);
+        }
+      } else {
+        const uint64_t qmn0 = sdesc_sw128(smem_u32(sm + L::kRing), 8192, 1024);  // Q / dO, MN-major
+        for (int j = 0; ok && j < steps; ++j) {
+          const int st = j & (kKvStages - 1), b = j & 1;
+          const uint32_t ph = (j >> 1) & 1;
           const uint64_t qd = qmn0 + st * kStageU;
-          const uint32_t pb = tmem + kKvPB + 64 * (j & 1);
-          // A = P^T / dS^T (K = 64 queries in 4 steps of 16: queries 16 kk..
-          // at column 8 kk of the P buffer's half), B = dO / Q (MN-major).
+          const uint32_t pb = tmem + kKvBuf * b;
+          // A = P^T / dS^T (K = 64 queries in 4 steps of 16), B = dO / Q
+          // (MN-major).
+          if (!mbar_spin(&p_ready[b], ph)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kKvDV, pb + 8 * kk, qd + kTileQU + ((kk * 2048) >> 4), idesc_g,
+            mma_ts(tmem + kKvDV, pb + 32 * (kk >> 1) + 8 * (kk & 1), qd + kTileQU + ((kk * 2048) >> 4), idesc_g,
                    (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&st_free[b]);
+          if (!mbar_spin(&ds_ready[b], ph)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kKvDK, pb + 32 + 8 * kk, qd + ((kk * 2048) >> 4), idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + kKvDK, pb + kKvDPOff + 32 * (kk >> 1) + 8 * (kk & 1), qd + ((kk * 2048) >> 4), idesc_g,
+                   (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&stage_free[st]);
-          mma_commit(&pbuf_free[j & 1]);
+          mma_commit(&dpt_free[b]);
         }
       }
       if (!ok) flag_error(p.err, kErrTimeout);
@@ -458,9 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
     bool ok = true;
     for (int j = 0; j < steps; ++j) {
       const int st = j & (kKvStages - 1), b = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
       // The stage's LSE / D are read from shared memory: wait for its fill
       // too (it has landed once S^T(j) is done, but this makes it visible).
-      if (!mbar_spin(&s_done, j & 1) || !mbar_spin(&full[st], (j / kKvStages) & 1)) {
+      if (!mbar_spin(&st_done[b], ph) || !mbar_spin(&full[st], (j / kKvStages) & 1)) {
         ok = false;
         break;
       }
@@ -468,53 +496,63 @@ __global__ void __launch_bounds__(kThreads, 1) fine_bwd_kv_kernel(const __grid_c
       const bool valid = ((ulist[j] >> key_bit) & 1u) != 0;
       const float* lse = reinterpret_cast<const float*>(sm + L::kStats + st * 512) + 32 * g;
       const float* dlt = lse + 64;
-      uint32_t pk[16], dk[16];
-      uint32_t sv[32], dv[32];
-      const uint32_t sb = lane_addr + kKvS + 32 * g;  // this warpgroup's S^T columns
-      if (valid) tmem_ld64x2_half(sb, sv, sb + kKvDP, dv);
-      // S^T / dP^T are in registers: the buffer may take S^T(j + 1).
-      tc_fence_before();
-      mbar_arrive(&s_free);
-      // P buffer b is free once dV / dK(j - 2) completed: test now, so that
-      // the answer is in by the time P^T / dS^T are ready.
-      const bool pfree = j < 2 || mbar_test(&pbuf_free[b], ((j >> 1) - 1) & 1);
+      const uint32_t sb = lane_addr + kKvBuf * b + 32 * g;  // this warpgroup's S^T columns
+      // P^T = exp2(log2e (S^T scale - LSE)) = exp2((LSE - scale S^T) (-log2e)),
+      // two query columns per packed operation; written over the first 16 of
+      // the S^T columns this thread read (its own lane; its loads completed).
+      uint64_t pr[16];
+      uint32_t pk[16];
       if (valid) {
-        // P^T = exp2(log2e (S^T scale - LSE)) = exp2((LSE - scale S^T) (-log2e)),
-        // dS^T = P^T (dP^T - D), two query columns per packed operation.
+        uint32_t sv[32];
+        tmem_ld32_wait(sb, sv);
         const uint64_t nsc = f2(-p.scale, -p.scale), nl2e = f2(-1.4426950408889634f, -1.4426950408889634f);
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(lse + c);
-          const float4 d4 = *reinterpret_cast<const float4*>(dlt + c);
-          const uint64_t p0 = exp2x2(mul2(fma2(f2u(sv[c], sv[c + 1]), nsc, f2(l4.x, l4.y)), nl2e));
-          const uint64_t p1 = exp2x2(mul2(fma2(f2u(sv[c + 2], sv[c + 3]), nsc, f2(l4.z, l4.w)), nl2e));
-          const uint64_t g0 = mul2(p0, sub2(f2u(dv[c], dv[c + 1]), f2(d4.x, d4.y)));
-          const uint64_t g1 = mul2(p1, sub2(f2u(dv[c + 2], dv[c + 3]), f2(d4.z, d4.w)));
-          pk[c >> 1] = f16x2_sat(p0);
-          pk[(c >> 1) + 1] = f16x2_sat(p1);
-          dk[c >> 1] = f16x2_sat(g0);
-          dk[(c >> 1) + 1] = f16x2_sat(g1);
+          pr[c >> 1] = exp2x2(mul2(fma2(f2u(sv[c], sv[c + 1]), nsc, f2(l4.x, l4.y)), nl2e));
+          pr[(c >> 1) + 1] = exp2x2(mul2(fma2(f2u(sv[c + 2], sv[c + 3]), nsc, f2(l4.z, l4.w)), nl2e));
+          pk[c >> 1] = f16x2_sat(pr[c >> 1]);
+          pk[(c >> 1) + 1] = f16x2_sat(pr[(c >> 1) + 1]);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = dk[i] = 0u;
+        for (int i = 0; i < 16; ++i) {
+          pk[i] = 0u;
+          pr[i] = 0ull;
+        }
       }
-      if (!pfree && !mbar_spin(&pbuf_free[b], ((j >> 1) - 1) & 1)) {
+      tmem_st8(sb, pk);
+      tmem_st8(sb + 8, pk + 8);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_ready[b]);
+      // dS^T = P^T (dP^T - D), over the first 16 of this thread's dP^T columns.
+      if (!mbar_spin(&dpt_done[b], ph)) {
         ok = false;
         break;
       }
-      if (j >= 2) tc_fence_after();
-      // P^T / dS^T into P buffer b (this warpgroup's 16 packed columns of each).
-      const uint32_t pb = lane_addr + kKvPB + 64 * b + 16 * g;
-      tmem_st8(pb, pk);
-      tmem_st8(pb + 8, pk + 8);
-      tmem_st8(pb + 32, dk);
-      tmem_st8(pb + 32 + 8, dk + 8);
+      tc_fence_after();
+      uint32_t dk[16];
+      if (valid) {
+        uint32_t dv[32];
+        tmem_ld32_wait(sb + kKvDPOff, dv);
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dlt + c);
+          dk[c >> 1] = f16x2_sat(mul2(pr[c >> 1], sub2(f2u(dv[c], dv[c + 1]), f2(d4.x, d4.y))));
+          dk[(c >> 1) + 1] = f16x2_sat(mul2(pr[(c >> 1) + 1], sub2(f2u(dv[c + 2], dv[c + 3]), f2(d4.z, d4.w))));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dk[i] = 0u;
+      }
+      tmem_st8(sb + kKvDPOff, dk);
+      tmem_st8(sb + kKvDPOff + 8, dk + 8);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&pds[b]);
+      mbar_arrive(&ds_ready[b]);
     }
-    if (ok && steps > 0 && !mbar_spin(&pbuf_free[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
+    if (ok && steps > 0 && !mbar_spin(&dpt_free[(steps - 1) & 1], ((steps - 1) >> 1) & 1)) ok = false;
     if (!ok) flag_error(p.err, kErrTimeout);
     tc_fence_after();
     // ---------------- dK, dV rows of this key pair (warpgroup 0: dV, 1: dK)
