@@ -42,8 +42,8 @@
 namespace vsa {
 namespace {
 
-constexpr int kSoftmaxThreads = 256;  // 8 softmax warps
-constexpr int kThreads = 64 + kSoftmaxThreads;
+constexpr int kSoftmaxThreads = 256;  // 8 softmax warps (2-9)
+constexpr int kThreads = 96 + kSoftmaxThreads;  // + warp 0 (K loads), warp 1 (MMA issue), warp 10 (V loads)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kTmemCols = 512;        // the whole SM: one CTA per SM
 constexpr uint32_t kColS = 0;              // S: 128 fp32 columns
@@ -314,10 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
   const int steps = (U + 1) >> 1;
   const int64_t row_base = bh * p.N;  // first row of this head in the 2D tensor maps
 
-  if (warp == 0) {
-    // ---------------- TMA producer.  K(j) goes to stage j % nk once S(j - nk)
-    // has completed; V(j) to stage j % nv once PV(j - nv) has.  K(j + 1) is
-    // requested before V(j): the MMA issuer needs them in that order.
+  if (warp == 0 || warp == 10) {
+    // ---------------- TMA producers: warp 0 loads K(j) into stage j % nk once
+    // S(j - nk) has completed, warp 10 V(j) into stage j % nv once PV(j - nv)
+    // has.  One thread loading both spent ~650 cycles per tile on its waits,
+    // bookkeeping and four TMA instructions, ~1300 per step, and so ran
+    // barely a step ahead of the MMAs; split, each runs its ring ahead.
+    // The waits suspend: the producers are ahead, and a polling thread
+    // would take issue slots from the softmax warps on its sub-partition.
     if (lane == 0 && steps > 0) {
       tma_prefetch_desc(&p.tk);
       tma_prefetch_desc(&p.tv);
@@ -348,11 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
         }
         return true;
       };
-      bool ok = load(0, &p.tk, kring, nk, kfull, kfree);
-      for (int j = 0; ok && j < steps; ++j) {
-        if (j + 1 < steps) ok = load(j + 1, &p.tk, kring, nk, kfull, kfree);
-        ok = ok && load(j, &p.tv, vring, nv, vfull, vfree);
-      }
+      bool ok = true;
+      for (int j = 0; ok && j < steps; ++j)
+        ok = warp == 0 ? load(j, &p.tk, kring, nk, kfull, kfree) : load(j, &p.tv, vring, nv, vfull, vfree);
       if (!ok) flag_error(p.err, kErrTimeout);
     }
   } else if (warp == 1) {

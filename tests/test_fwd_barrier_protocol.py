@@ -1,8 +1,9 @@
 """CPU model of the barrier protocol of the fine forward kernel (fine_fwd_kernel).
 
-Roles, as in the kernel: a TMA producer (K(j) into ring stage j % nk, V(j)
-into stage j % nv, K(j + 1) requested before V(j)), one MMA-issuing thread,
-and eight softmax warps, two per TMEM lane quarter.  Barriers:
+Roles, as in the kernel: two TMA producers (one loads K(j) into ring stage
+j % nk, the other V(j) into stage j % nv, each in step order and
+independently of the other), one MMA-issuing thread, and eight softmax
+warps, two per TMEM lane quarter.  Barriers:
   bar_qt        Q rows written into TMEM          (256 softmax threads)
   kfull/vfull   ring stage landed                 (TMA)
   kfree/vfree   S(j) / PV(j) that read the stage done   (commits)
@@ -70,13 +71,9 @@ def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
     rescale = {}                   # (step, quarter) -> bool, the same for both warps of a quarter
     pipe, loads = [], []
 
-    # producer program: K0, then per j: K(j+1), V(j)
-    prog = [("K", 0)] if steps else []
-    for j in range(steps):
-        if j + 1 < steps:
-            prog.append(("K", j + 1))
-        prog.append(("V", j))
-    pc = 0
+    # producer programs: K(0), K(1), ... and V(0), V(1), ..., each in its own thread
+    progs = [[("K", j) for j in range(steps)], [("V", j) for j in range(steps)]]
+    pcs = [0, 0]
     ns = npv = 0
     qt_ok = False
     warp_j = [0] * WARPS
@@ -116,14 +113,15 @@ def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
                 assert ring[st] is None or ring[st][1], (kind, "stage overwritten before read", ring[st], j)
                 ring[st] = [j, False]
                 (kfull if kind == "K" else vfull)[st].arrive()
-        # producer
-        if pc < len(prog) and rnd.random() < 0.5:
-            kind, j = prog[pc]
-            depth, free = (nk, kfree) if kind == "K" else (nv, vfree)
-            st, use = j % depth, j // depth
-            if use == 0 or (kind == "K" and "kfree" in drop) or free[st].test(use - 1):
-                loads.append([kind, j, delay(rnd, 10)])
-                pc += 1
+        # producers
+        for pi in range(2):
+            if pcs[pi] < len(progs[pi]) and rnd.random() < 0.5:
+                kind, j = progs[pi][pcs[pi]]
+                depth, free = (nk, kfree) if kind == "K" else (nv, vfree)
+                st, use = j % depth, j // depth
+                if use == 0 or (kind == "K" and "kfree" in drop) or free[st].test(use - 1):
+                    loads.append([kind, j, delay(rnd, 10)])
+                    pcs[pi] += 1
         # issuer
         if steps and rnd.random() < 0.7:
             if not qt_ok:
