@@ -471,7 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       mbar_arrive(&bar_qt);
     }
     for (int j = 0; j < steps; ++j) {
-      if (!mbar_spin(&bar_s, j & 1)) {
+      // A suspended wait: the pair usually finds S(j) done, and a spinning
+      // warp would take issue slots from the MMA issuer on its sub-partition.
+      if (!mbar_wait(&bar_s, j & 1)) {
         ok = false;
         break;
       }
