@@ -36,11 +36,11 @@ import synth  # noqa: E402
 
 METRIC = "VSA fwd+bwd effective TFLOPS at 32K tokens, 70% sparsity; % of bf16 tensor peak"
 UNIT = "TFLOP/s"
-# libvsa kernels launched by one forward + backward step: permute_pool,
-# coarse_gemm, topk_rows, coarse_gemm, build_list_bits, pair_overlap,
-# plan_pairs, fine_fwd, combine | build_inverse_bits, pair_overlap, plan_pairs,
-# bwd_prep, coarse_gemm, bwd_rows, coarse_gemm, fine_bwd_kv, fine_bwd_dq.
-KERNELS_PER_STEP = 18
+# libvsa kernels launched by one forward + backward step (the ncu launch list
+# of the bench's step shows exactly these): permute_pool, coarse_fwd,
+# pair_overlap, plan_pairs, fine_fwd, combine | inv_count, inv_scan, inv_fill,
+# pair_overlap, plan_pairs, bwd_prep, coarse_bwd, fine_bwd_kv, fine_bwd_dq.
+KERNELS_PER_STEP = 15
 WORKLOAD = "wan1.3b"
 
 
