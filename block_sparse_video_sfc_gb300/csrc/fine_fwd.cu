@@ -20,11 +20,14 @@
 // memory stages each.  Q sits in TMEM and is the A operand of S = Q K^T, so
 // the tensor core reads only K and V from shared memory: every byte of it
 // also has to be written there by the TMA, and the two share the shared-
-// memory bandwidth (an SM ingests only ~45 B/clk from L2).  TMEM columns:
-// S (128), two P buffers (2 x 64), O (D) and Q (D / 2).  The S buffer is
-// released as soon as the softmax warps have read it into registers, so
-// S(j+1) runs while they compute P(j); P is double-buffered so that storing
-// P(j) never waits for the PV product just before it.
+// memory bandwidth (a step moves 128 KB through it, ~1000 cycles at
+// 128 B/clk, about the step's 1024 cycles of tensor work).  TMEM columns:
+// two S buffers (2 x 128), O (D) and Q (D / 2).  S(j) goes into buffer j % 2
+// and P(j) (fp16 pairs, 64 columns) is written over the first half of S(j)
+// once both softmax warps of a lane quarter hold their half of S(j) in
+// registers; S(j + 2) may take the buffer once PV(j) has read P(j).  So
+// S(j + 1) runs while the softmax warps work on step j, and waits for
+// neither their loads nor a separate P buffer.
 // The running max is only raised (and O rescaled) when a row's max grows by
 // more than 2^8, so P <= 256.
 // A warp's 32 rows all belong to one query cube, so a key cube outside that
@@ -46,8 +49,7 @@ constexpr int kSoftmaxThreads = 256;  // 8 softmax warps (2-9)
 constexpr int kThreads = 96 + kSoftmaxThreads;  // + warp 0 (K loads), warp 1 (MMA issue), warp 10 (V loads)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kTmemCols = 512;        // the whole SM: one CTA per SM
-constexpr uint32_t kColS = 0;              // S: 128 fp32 columns
-constexpr uint32_t kColP = 128;            // P(j) in 128 + 64 (j % 2): 64 columns of fp16 pairs
+constexpr uint32_t kColS = 0;              // S(j) in 128 (j % 2): 128 fp32 columns; P(j) over its first 64
 constexpr uint32_t kColO = 256;            // O: D columns
 constexpr uint32_t kColQ = 384;            // Q as the A operand: D / 2 columns of fp16 pairs
 constexpr int kMaxStages = 3;              // K and V ring depth
@@ -166,14 +168,14 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
   uint32_t* bitB = bitA + nwords;
 
   // kfull/vfull: a stage's TMA landed.  kfree/vfree: the MMA that read the
-  // stage completed.  bar_s: S(j) done.  s_free: the softmax warps have read
-  // S(j) (the buffer may take S(j+1)).  bar_p[b]: P(j) written into P buffer
-  // b = j % 2 (all softmax threads).  pv_done[b]: PV(j) completed (O
-  // includes it and P buffer b is free).  A parity wait is only correct while
-  // the barrier is in the awaited phase or the one after it; each wait below
-  // keeps to that (P(j) is stored only after PV(j - 2) has completed).
+  // stage completed.  With b = j % 2: bar_s[b]: S(j) done.  bar_p[b]: P(j)
+  // written over S(j) (all softmax threads).  pv_done[b]: PV(j) completed (O
+  // includes it, and buffer b may take S(j + 2)).  A parity wait is only
+  // correct while the barrier is in the awaited phase or the one after it;
+  // each wait below keeps to that (S(j) is issued only after PV(j - 2) has
+  // completed, so a warp that sees S(j) knows PV(0..j-2) are done).
   __shared__ uint64_t bar_qt, kfull[kMaxStages], kfree[kMaxStages], vfull[kMaxStages], vfree[kMaxStages];
-  __shared__ uint64_t bar_s, s_free, bar_p[2], pv_done[2];
+  __shared__ uint64_t bar_s[2], bar_p[2], pv_done[2];
   __shared__ uint64_t pair_bar[4];  // per lane quarter: its two softmax warps (64 threads)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int n_union, n_first, n_cnt[2];
@@ -205,9 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       mbar_init(&vfull[i], 1);
       mbar_init(&vfree[i], 1);
     }
-    mbar_init(&bar_s, 1);
-    mbar_init(&s_free, kSoftmaxThreads);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_s[i], 1);
       mbar_init(&bar_p[i], kSoftmaxThreads);
       mbar_init(&pv_done[i], 1);
     }
@@ -382,8 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       // whichever of S(ns) and PV(npv) is ready first.
       while (ok && npv < steps) {
         bool progressed = false;
-        // S(ns) once the softmax warps have read S(ns - 1) out of the buffer.
-        if (ns < steps && (ns == 0 || mbar_test(&s_free, (ns - 1) & 1)) && mbar_test(&kfull[ks], kph)) {
+        // S(ns) once PV(ns - 2) has read P(ns - 2) out of its buffer.
+        if (ns < steps && (ns < 2 || mbar_test(&pv_done[ns & 1], ((ns >> 1) - 1) & 1)) &&
+            mbar_test(&kfull[ks], kph)) {
           tc_fence_after();
           const uint64_t kd = kdesc0 + ks * kTileUnits;
 #pragma unroll
@@ -391,10 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
             const uint64_t bd = kd + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
             asm volatile(
                 "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem + kColS),
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem + kColS + 128 * (ns & 1)),
                 "r"(tmem + kColQ + kk * 8), "l"(bd), "r"(idesc_s), "r"(static_cast<uint32_t>(kk > 0)));
           }
-          mma_commit(&bar_s);
+          mma_commit(&bar_s[ns & 1]);
           mma_commit(&kfree[ks]);
           ++ns;
           if (++ks == static_cast<uint32_t>(nk)) {
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
         }
         if (npv < ns && mbar_test(&bar_p[npv & 1], (npv >> 1) & 1) && mbar_test(&vfull[vs], vph)) {
           tc_fence_after();
-          const uint32_t pcol = tmem + kColP + 64 * (npv & 1);
+          const uint32_t pcol = tmem + kColS + 128 * (npv & 1);
           const uint64_t vd = vdesc0 + vs * kTileUnits;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -473,12 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
     for (int j = 0; j < steps; ++j) {
       // A suspended wait: the pair usually finds S(j) done, and a spinning
       // warp would take issue slots from the MMA issuer on its sub-partition.
-      if (!mbar_wait(&bar_s, j & 1)) {
+      if (!mbar_wait(&bar_s[j & 1], (j >> 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sb = lane_addr + kColS;
+      const uint32_t sb = lane_addr + kColS + 128 * (j & 1);
       const uint32_t e = (2 * j + half < U) ? uent(2 * j + half) : 0u;
       const bool valid = ((e >> my_bit) & 1u) != 0;  // warp-uniform
       uint32_t sr[64];
@@ -497,10 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
         }
         mx = max64(sr) * p.scale_log2;
       }
-      // S is in registers: the buffer may take S(j + 1).
+      // Exchange the half maxima (double-buffered by step parity).  The
+      // exchange also tells each warp that its partner holds its half of
+      // S(j), so P(j) may then be written over the first half.
       tc_fence_before();
-      mbar_arrive(&s_free);
-      // Exchange the half maxima (double-buffered by step parity).
       xmax[j & 1][half][row] = mx;
       mbar_arrive(pair_mb);
       if (!mbar_spin(pair_mb, pair_uses++ & 1)) {
@@ -508,9 +510,6 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
         break;
       }
       mx = fmaxf(mx, xmax[j & 1][half ^ 1][row]);
-      // P(j) goes into P buffer j % 2 once PV(j - 2) has read it: test now,
-      // so that the answer is in by the time P is ready.
-      const bool pv_free = j < 2 || mbar_test(&pv_done[j & 1], ((j >> 1) - 1) & 1);
 
       // Raise the running max only when it grows by more than the threshold.
       const bool raise = mx > m + kRescaleThreshold;
@@ -539,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
       }
       m = m_new;
       // P = exp2(S * scale - m), fp16 pairs into columns [32h, 32h + 32) of
-      // P buffer j % 2 once PV(j - 2) has read P(j - 2) out of it.
+      // S(j)'s buffer.
       // The row sum adds the same rounded weights the PV MMA sees, so O / l
       // stays an exact convex combination of V rows (summing the unrounded
       // weights instead made the output ~4x and dK ~6x less accurate).
@@ -552,13 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_fwd_kernel(const __grid_cons
 #pragma unroll
         for (int c = 0; c < 32; ++c) pk[c] = 0u;
       }
-      if (!pv_free && !mbar_spin(&pv_done[j & 1], ((j >> 1) - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      if (j >= 2) tc_fence_after();
+      tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 32; c += 8) tmem_st8(lane_addr + kColP + 64 * (j & 1) + 32 * half + c, pk + c);
+      for (int c = 0; c < 32; c += 8) tmem_st8(sb + 32 * half + c, pk + c);
       if (!F16IN && !NATIVE) {
         // bf16 V tile -> fp16 in place, before the PV MMA may read it.
         const int st = j % nv;

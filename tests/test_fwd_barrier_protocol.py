@@ -3,22 +3,27 @@
 Roles, as in the kernel: two TMA producers (one loads K(j) into ring stage
 j % nk, the other V(j) into stage j % nv, each in step order and
 independently of the other), one MMA-issuing thread, and eight softmax
-warps, two per TMEM lane quarter.  Barriers:
+warps, two per TMEM lane quarter (one per key cube of the step).  S(j) goes
+into TMEM buffer j % 2, and P(j) is written over the first half of S(j):
+each warp writes 32 of those 64 columns, one of which is its partner's half
+of S(j), so it may only write once its partner holds that half in
+registers.  Barriers:
   bar_qt        Q rows written into TMEM          (256 softmax threads)
   kfull/vfull   ring stage landed                 (TMA)
   kfree/vfree   S(j) / PV(j) that read the stage done   (commits)
-  bar_s         S(j) done                         (commit)
-  s_free        S(j) read into registers          (256 softmax threads)
-  pair_bar[q]   row-max exchange of quarter q     (its two warps, 64 threads)
-  bar_p[b]      P(j) written into P buffer b = j % 2   (256 threads)
-  pv_done[b]    PV(j) done                        (commit)
-A softmax warp that raises its row max first waits for PV(j - 1) and then
-rescales O; before writing P(j) it waits for PV(j - 2), the last reader of
-that P buffer.  The model asserts the parity rule (a wait for phase k sees k
-or k + 1 completed phases), that no ring stage, S buffer or P buffer is
-overwritten before its reader is done, that PV(j) reads a complete P(j), that
-O is rescaled only with PV(0..j-1) done and PV(j) not yet issued, and that
-every schedule of random delays terminates.
+  bar_s[b]      S(j) done, b = j % 2              (commit)
+  pair[q]       row-max exchange of quarter q     (its two warps, 64 threads;
+                                                   both have loaded S(j))
+  bar_p[b]      P(j) written over S(j)            (256 threads)
+  pv_done[b]    PV(j) done                        (commit; buffer b may take S(j + 2))
+The issuer issues S(j) once PV(j - 2) is done and PV(j) once P(j) is
+written.  A softmax warp that raises its row max first waits for PV(j - 1)
+and then rescales O.  The model asserts the parity rule (a wait for phase k
+sees k or k + 1 completed phases), that no ring stage or TMEM buffer is
+overwritten before its reader is done, that P(j) is written over S(j) only
+after both warps of the quarter read their halves, that PV(j) reads a
+complete P(j), that O is rescaled only with PV(0..j-1) done and PV(j) not yet
+issued, and that every schedule of random delays terminates.
 """
 import random
 
@@ -57,21 +62,21 @@ def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
     kfree = [Barrier(f"kfree{i}", 1) for i in range(nk)]
     vfull = [Barrier(f"vfull{i}", 1) for i in range(nv)]
     vfree = [Barrier(f"vfree{i}", 1) for i in range(nv)]
-    bar_s, s_free = Barrier("bar_s", 1), Barrier("s_free", THREADS)
+    bar_s = [Barrier(f"bar_s{i}", 1) for i in range(2)]
     pair = [Barrier(f"pair{q}", 64) for q in range(4)]
     bar_p = [Barrier(f"bar_p{i}", THREADS) for i in range(2)]
     pv_done = [Barrier(f"pv_done{i}", 1) for i in range(2)]
 
     kring = [None] * nk            # stage -> [step, consumed]
     vring = [None] * nv
-    s_buf = None                   # [step, set of warps that read it]
-    p_buf = [None, None]           # buffer -> [step, warps that wrote it, consumed]
+    # TMEM buffer b -> [step, kind "S" / "P", warps that read S, warps that wrote P, read by PV];
+    # warp w works on lane quarter w % 4, w and w ^ 4 are the two warps of a quarter
+    buf = [None, None]
     pv_completed = -1              # last PV completed (in order)
     pv_issued = -1
     rescale = {}                   # (step, quarter) -> bool, the same for both warps of a quarter
     pipe, loads = [], []
 
-    # producer programs: K(0), K(1), ... and V(0), V(1), ..., each in its own thread
     progs = [[("K", j) for j in range(steps)], [("V", j) for j in range(steps)]]
     pcs = [0, 0]
     ns = npv = 0
@@ -86,19 +91,20 @@ def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
             pipe[0][2] -= 1
             if pipe[0][2] <= 0:
                 kind, j, _, bars = pipe.pop(0)
+                b = j & 1
                 if kind == "S":
                     st = j % nk
                     assert kring[st] is not None and kring[st][0] == j, ("K stage", kring[st], j)
-                    assert s_buf is None or len(s_buf[1]) == WARPS, ("S overwritten unread", s_buf, j)
+                    assert buf[b] is None or (buf[b][0] == j - 2 and buf[b][4]), ("S over an unread P", buf[b], j)
                     kring[st][1] = True
-                    s_buf = [j, set()]
+                    buf[b] = [j, "S", set(), set(), False]
                 else:
-                    st, b = j % nv, j & 1
+                    st = j % nv
                     assert vring[st] is not None and vring[st][0] == j, ("V stage", vring[st], j)
-                    assert p_buf[b] is not None and p_buf[b][0] == j and len(p_buf[b][1]) == WARPS, \
-                        ("PV reads incomplete P", p_buf[b], j)
+                    assert buf[b] is not None and buf[b][0] == j and len(buf[b][3]) == WARPS, \
+                        ("PV reads incomplete P", buf[b], j)
                     vring[st][1] = True
-                    p_buf[b][2] = True
+                    buf[b][4] = True
                     assert pv_completed == j - 1
                     pv_completed = j
                 for bar in bars:
@@ -126,9 +132,9 @@ def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
         if steps and rnd.random() < 0.7:
             if not qt_ok:
                 qt_ok = bar_qt.test(0)
-            elif ns < steps and (ns == 0 or "s_free" in drop or s_free.test(ns - 1)) and \
+            elif ns < steps and (ns < 2 or "pv_s" in drop or pv_done[ns & 1].test((ns >> 1) - 1)) and \
                     kfull[ns % nk].test(ns // nk):
-                pipe.append(["S", ns, delay(rnd, 6), [bar_s, kfree[ns % nk]]])
+                pipe.append(["S", ns, delay(rnd, 6), [bar_s[ns & 1], kfree[ns % nk]]])
                 ns += 1
             elif npv < ns and bar_p[npv & 1].test(npv >> 1) and vfull[npv % nv].test(npv // nv):
                 pipe.append(["PV", npv, delay(rnd, 6), [vfree[npv % nv], pv_done[npv & 1]]])
@@ -146,17 +152,20 @@ def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
             j = warp_j[w]
             if j >= steps:
                 continue
+            b = j & 1
             if warp_pc[w] == 0:
-                if bar_s.test(j):
-                    assert s_buf is not None and s_buf[0] == j, ("S buffer", s_buf, j)
-                    s_buf[1].add(w)
-                    s_free.arrive(32)
+                if bar_s[b].test(j >> 1):
+                    # the lanes of a quarter are its own: only P written by
+                    # the two warps of this quarter would overwrite this half
+                    assert buf[b] is not None and buf[b][0] == j, ("S buffer", buf[b], j)
+                    assert not (buf[b][3] & {q, q + 4}), ("S read after P was written over it", buf[b], j, w)
+                    buf[b][2].add(w)
                     warp_pc[w] = 1
             elif warp_pc[w] == 1:
                 pair[q].arrive(32)
                 warp_pc[w] = 2
             elif warp_pc[w] == 2:
-                if pair[q].test(j):
+                if "pair" in drop or pair[q].test(j):
                     rescale.setdefault((j, q), j > 0 and rnd.random() < 0.3)
                     warp_pc[w] = 3
             elif warp_pc[w] == 3:
@@ -166,17 +175,14 @@ def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
                     assert pv_completed >= j - 1 and pv_issued < j, ("rescale of O", pv_completed, pv_issued, j)
                     warp_pc[w] = 4
             elif warp_pc[w] == 4:
-                b = j & 1
-                if j < 2 or "p_free" in drop or pv_done[b].test((j >> 1) - 1):
-                    if p_buf[b] is not None and p_buf[b][0] != j:
-                        assert p_buf[b][2], ("P overwritten before PV read it", p_buf[b], j)
-                        p_buf[b] = None
-                    if p_buf[b] is None:
-                        p_buf[b] = [j, set(), False]
-                    p_buf[b][1].add(w)
-                    bar_p[b].arrive(32)
-                    warp_j[w] += 1
-                    warp_pc[w] = 0
+                partner = w ^ 4
+                assert buf[b][0] == j and partner in buf[b][2] and w in buf[b][2], \
+                    ("P written over S its partner has not read", buf[b], j, w)
+                buf[b][1] = "P"
+                buf[b][3].add(w)
+                bar_p[b].arrive(32)
+                warp_j[w] += 1
+                warp_pc[w] = 0
         if steps == 0:
             return tick
         if npv == steps and not pipe and all(x == steps for x in warp_j):
@@ -192,7 +198,7 @@ def test_fwd_protocol_random_schedules(nk, nv, steps):
         simulate(steps, nk, nv, seed)
 
 
-@pytest.mark.parametrize("drop", ["kfree", "s_free", "rescale", "p_free"])
+@pytest.mark.parametrize("drop", ["kfree", "pv_s", "pair", "rescale"])
 def test_model_catches_each_missing_wait(drop):
     """Leaving out any one of the waits makes some schedule fail."""
     caught = 0
