@@ -32,8 +32,9 @@
 // more than 2^8, so P <= 256.
 // A warp's 32 rows all belong to one query cube, so a key cube outside that
 // cube's list is skipped by the whole warp (no loads, no exponentials).
-// Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2-9 softmax/epilogue
-// (two warps per TMEM lane quarter, one per key cube of the step).
+// Roles: warp 0 loads K and warp 10 loads V (TMA), warp 1 issues the MMAs,
+// warps 2-9 compute the softmax and the epilogue (two warps per TMEM lane
+// quarter, one per key cube of the step).
 #include <algorithm>
 
 #include <cuda.h>
