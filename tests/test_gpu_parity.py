@@ -140,6 +140,43 @@ def test_fine_fwd_ragged_and_edge_lists(vsa, oracle_mod, workspace):
     assert_close(host(lse)[~empty], rlse[~empty], max_abs=LSE_MAX_ABS, mean_abs=LSE_MEAN_ABS, what="lse")
 
 
+@pytest.mark.parametrize("workspace", [True, False])
+@pytest.mark.parametrize("d", [64, 128])
+def test_fine_fwd_rising_scores_rescale_often(vsa, oracle_mod, workspace, d):
+    """Scores that rise by ~3 log2 units per key cube, and lists whose first
+    entry (the one a tile visits first) is their lowest-scored cube.  The
+    kernel raises a row's running max only when it grows by more than 2^8, so
+    here it does so every few steps, and each time rescales O after waiting
+    for the PV product before it: a path that inputs whose largest scores sit
+    in the first-visited cubes never take."""
+    BH, Nc, K = 2, 48, 24
+    N = 64 * Nc
+    rng = np.random.default_rng(7 + d)
+    u = rng.standard_normal(d)
+    u /= np.linalg.norm(u)
+    scale = d ** -0.5
+    beta = 3.0 / (scale * np.log2(np.e))          # q . k grows by 3 log2 units per cube
+    cube = np.repeat(np.arange(Nc), 64)
+    bf = lambda a: torch.tensor(a, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+    q = bf(0.3 * rng.standard_normal((BH, N, d)) + u)
+    k = bf(0.3 * rng.standard_normal((BH, N, d)) + (beta * cube)[None, :, None] * u)
+    v = bf(rng.standard_normal((BH, N, d)))
+    idx = np.empty((BH, Nc, K), np.int32)
+    for b in range(BH):
+        for c in range(Nc):
+            pick = rng.permutation(Nc)[:K]
+            lo = int(np.argmin(pick))
+            idx[b, c] = np.concatenate([pick[lo:lo + 1], np.delete(pick, lo)])   # lowest cube first
+    cnt = np.full((BH, Nc), K, np.int32)
+    of, lse = vsa.fine_fwd(dev(q), dev(k), dev(v), dev(idx, torch.int32), dev(cnt, torch.int32),
+                           workspace=workspace)
+    status_ok(vsa)
+    rof, rlse = oracle_mod.fine_fwd(q, k, v, idx, cnt, scale)
+    assert rlse.max() > 50                                                      # the scores do rise
+    assert_close(host(of), rof, what="O_f (rescaled rows)")
+    assert_close(host(lse), rlse, max_abs=LSE_MAX_ABS, mean_abs=LSE_MEAN_ABS, what="lse (rescaled rows)")
+
+
 def test_fine_fwd_dense_is_sdpa(vsa, oracle_mod):
     """K = all cubes: the fine kernel equals dense attention (torch SDPA, fp32)."""
     wl = synth.WORKLOADS["small"]
