@@ -2,8 +2,10 @@
 
 Roles, as in the kernel: two TMA producers (one loads K(j) into ring stage
 j % nk, the other V(j) into stage j % nv, each in step order and
-independently of the other), one MMA-issuing thread, and eight softmax
-warps, two per TMEM lane quarter (one per key cube of the step).  S(j) goes
+independently of the other), the MMA issue (one polling thread for both
+kinds of group in the native-layout kernel; one thread for S and one for PV
+in the others, whose groups nothing orders against each other), and eight
+softmax warps, two per TMEM lane quarter (one per key cube of the step).  S(j) goes
 into TMEM buffer j % 2, and P(j) is written over the first half of S(j):
 each warp writes 32 of those 64 columns, one of which is its partner's half
 of S(j), so it may only write once its partner holds that half in
@@ -54,8 +56,10 @@ class Barrier:
         return self.phases > k
 
 
-def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
-    """drop: waits left out on purpose (to show the model catches them)."""
+def simulate(steps, nk, nv, seed, max_ticks=400000, drop=(), two_issuers=False):
+    """drop: waits left out on purpose (to show the model catches them).
+    two_issuers: S and PV issued by two threads (the kernels that read
+    reordered tiles), else by one polling thread (the native-layout kernel)."""
     rnd = random.Random(seed)
     bar_qt = Barrier("bar_qt", THREADS)
     kfull = [Barrier(f"kfull{i}", 1) for i in range(nk)]
@@ -75,7 +79,9 @@ def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
     pv_completed = -1              # last PV completed (in order)
     pv_issued = -1
     rescale = {}                   # (step, quarter) -> bool, the same for both warps of a quarter
-    pipe, loads = [], []
+    pipes, loads = {"S": [], "PV": []}, []
+    if not two_issuers:
+        pipes["PV"] = pipes["S"]          # one thread: one queue, in issue order
 
     progs = [[("K", j) for j in range(steps)], [("V", j) for j in range(steps)]]
     pcs = [0, 0]
@@ -86,8 +92,11 @@ def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
     warp_qt = [False] * WARPS
 
     for tick in range(max_ticks):
-        # tensor pipe, in order
-        if pipe:
+        # tensor pipe: each issuing thread's groups complete in issue order;
+        # nothing orders two threads' groups (one thread: a single queue)
+        for pipe in {id(q): q for q in pipes.values()}.values():
+            if not pipe or rnd.random() < 0.3:
+                continue
             pipe[0][2] -= 1
             if pipe[0][2] <= 0:
                 kind, j, _, bars = pipe.pop(0)
@@ -128,18 +137,24 @@ def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
                 if use == 0 or (kind == "K" and "kfree" in drop) or free[st].test(use - 1):
                     loads.append([kind, j, delay(rnd, 10)])
                     pcs[pi] += 1
-        # issuer
-        if steps and rnd.random() < 0.7:
-            if not qt_ok:
-                qt_ok = bar_qt.test(0)
-            elif ns < steps and (ns < 2 or "pv_s" in drop or pv_done[ns & 1].test((ns >> 1) - 1)) and \
-                    kfull[ns % nk].test(ns // nk):
-                pipe.append(["S", ns, delay(rnd, 6), [bar_s[ns & 1], kfree[ns % nk]]])
-                ns += 1
-            elif npv < ns and bar_p[npv & 1].test(npv >> 1) and vfull[npv % nv].test(npv // nv):
-                pipe.append(["PV", npv, delay(rnd, 6), [vfree[npv % nv], pv_done[npv & 1]]])
-                pv_issued = npv
-                npv += 1
+        # issuers: S(ns) once PV(ns - 2) is done and K(ns) has landed; PV(npv)
+        # once P(npv) is written and V(npv) has landed.  One polling thread
+        # tries S first; with two threads each goes on its own.
+        s_go = steps and rnd.random() < 0.7
+        pv_go = (rnd.random() < 0.7) if two_issuers else not s_go
+        if s_go and not qt_ok:
+            qt_ok = bar_qt.test(0)
+        elif s_go and ns < steps and (ns < 2 or "pv_s" in drop or pv_done[ns & 1].test((ns >> 1) - 1)) and \
+                kfull[ns % nk].test(ns // nk):
+            pipes["S"].append(["S", ns, delay(rnd, 6), [bar_s[ns & 1], kfree[ns % nk]]])
+            ns += 1
+            pv_go = pv_go and two_issuers
+        elif not two_issuers and s_go:
+            pv_go = True
+        if steps and pv_go and npv < ns and bar_p[npv & 1].test(npv >> 1) and vfull[npv % nv].test(npv // nv):
+            pipes["PV"].append(["PV", npv, delay(rnd, 6), [vfree[npv % nv], pv_done[npv & 1]]])
+            pv_issued = npv
+            npv += 1
         # softmax warps
         for w in range(WARPS):
             if rnd.random() > 0.35:
@@ -185,26 +200,28 @@ def simulate(steps, nk, nv, seed, max_ticks=400000, drop=()):
                 warp_pc[w] = 0
         if steps == 0:
             return tick
-        if npv == steps and not pipe and all(x == steps for x in warp_j):
+        if npv == steps and not pipes["S"] and not pipes["PV"] and all(x == steps for x in warp_j):
             assert pv_done[(steps - 1) & 1].test((steps - 1) >> 1)   # epilogue wait
             return tick
     raise AssertionError(f"no progress: steps={steps} nk={nk} nv={nv} seed={seed} ns={ns} npv={npv} warps={warp_j}")
 
 
+@pytest.mark.parametrize("two_issuers", [False, True])
 @pytest.mark.parametrize("nk,nv", [(1, 1), (2, 1), (2, 2), (3, 3), (3, 2)])
 @pytest.mark.parametrize("steps", [0, 1, 2, 3, 4, 7, 12, 31])
-def test_fwd_protocol_random_schedules(nk, nv, steps):
+def test_fwd_protocol_random_schedules(nk, nv, steps, two_issuers):
     for seed in range(12):
-        simulate(steps, nk, nv, seed)
+        simulate(steps, nk, nv, seed, two_issuers=two_issuers)
 
 
+@pytest.mark.parametrize("two_issuers", [False, True])
 @pytest.mark.parametrize("drop", ["kfree", "pv_s", "pair", "rescale"])
-def test_model_catches_each_missing_wait(drop):
+def test_model_catches_each_missing_wait(drop, two_issuers):
     """Leaving out any one of the waits makes some schedule fail."""
     caught = 0
     for seed in range(60):
         try:
-            simulate(12, 2, 2, seed, max_ticks=50000, drop=(drop,))
+            simulate(12, 2, 2, seed, max_ticks=50000, drop=(drop,), two_issuers=two_issuers)
         except AssertionError:
             caught += 1
     assert caught > 0, drop
